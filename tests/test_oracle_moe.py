@@ -1,0 +1,205 @@
+"""Pins for the oracle's routing, grouping and FFN (CPU only)."""
+import os
+
+import numpy as np
+import pytest
+
+import synth
+import oracle
+from oracle import brute, nvfp4
+
+
+# ---------------------------------------------------------------------------
+# routing
+# ---------------------------------------------------------------------------
+
+def test_route_matches_python_sort_with_ties():
+    rng = np.random.default_rng(3)
+    logits = rng.standard_normal((50, 40)).astype(np.float32)
+    logits[:, 7] = logits[:, 3]                     # exact ties between ids 3 and 7
+    logits[::5, :] = np.round(logits[::5, :])       # many ties
+    k = 6
+    ids, w = oracle.route_topk(logits, k)
+    for t in range(logits.shape[0]):
+        bids, bw = brute.route(logits[t], k)
+        assert list(ids[t]) == bids
+        assert np.allclose(w[t], bw, rtol=1e-15, atol=0)
+
+
+def test_route_weights_equal_renormalised_full_softmax():
+    rng = np.random.default_rng(4)
+    logits = (rng.standard_normal((20, 64)) * 3).astype(np.float32)
+    ids, w = oracle.route_topk(logits, 10)
+    l = logits.astype(np.float64)
+    full = np.exp(l - l.max(axis=1, keepdims=True))
+    full /= full.sum(axis=1, keepdims=True)
+    sel = np.take_along_axis(full, ids.astype(np.int64), axis=1)
+    assert np.allclose(w, sel / sel.sum(axis=1, keepdims=True), rtol=1e-13)
+    assert np.all(np.diff(np.take_along_axis(l, ids.astype(np.int64), 1), axis=1) <= 0)
+
+
+# ---------------------------------------------------------------------------
+# CSR
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("T,k,E", [(4, 2, 16), (8, 10, 512), (300, 8, 288), (1, 1, 1)])
+def test_csr_matches_stable_argsort(T, k, E):
+    rng = np.random.default_rng(T * 31 + k)
+    ids = synth.skewed_ids(rng, T, k, E)
+    csr = oracle.build_expert_csr(ids, E)
+    flat = ids.reshape(-1)
+    order = np.argsort(flat, kind="stable")
+    assert np.array_equal(csr.pair_ids, order)
+    counts = np.bincount(flat, minlength=E)
+    assert np.array_equal(csr.offsets, np.concatenate([[0], np.cumsum(counts)]))
+    assert np.array_equal(csr.active, np.nonzero(counts)[0])
+    assert csr.n_active == np.count_nonzero(counts)
+    assert np.array_equal(csr.pair_pos[csr.pair_ids], np.arange(flat.size))
+    # brute force buckets
+    buckets = [[] for _ in range(E)]
+    for p, e in enumerate(flat):
+        buckets[e].append(p)
+    assert list(csr.pair_ids) == [p for b in buckets for p in b]
+
+
+def test_csr_skips_invalid_ids():
+    ids = np.array([[0, 5], [-1, 2], [2, 9]], np.int32)
+    csr = oracle.build_expert_csr(ids, 6)
+    assert list(csr.pair_ids) == [0, 3, 4, 1]
+    assert list(csr.pair_pos) == [0, 3, -1, 1, 2, -1]
+    assert list(csr.offsets) == [0, 1, 1, 3, 3, 3, 4]
+
+
+def test_union_ids_distinct_per_token():
+    for U in (60, 30, 20, 10):
+        ids = synth.union_ids(6, 10, 512, U)
+        assert len(np.unique(ids)) == U
+        for t in range(6):
+            assert len(set(ids[t])) == 10
+
+
+# ---------------------------------------------------------------------------
+# FFN
+# ---------------------------------------------------------------------------
+
+def test_ffn_matches_brute_force_tiny():
+    w = synth.tiny()
+    ids, ww = oracle.route_topk(w.logits, w.k)
+    res = oracle.ffn(w.x_bits, ids, ww, w.gate_up, w.down)
+    bids, bw, by = brute.moe_ffn(w.x_bits, w.logits, w.gate_up, w.down, w.k)
+    assert np.array_equal(np.array(bids), ids)
+    by = np.array(by)
+    assert np.max(np.abs(by - res.y)) <= 1e-11 * np.max(np.abs(res.tsum))
+
+
+def _brute_dense(bank, e):
+    rows, half = bank.codes.shape[1], bank.codes.shape[2]
+    return np.array([[float(brute.weight(bank.codes[e][r], bank.scales[e][r], c))
+                      for c in range(2 * half)] for r in range(rows)])
+
+
+def test_ffn_single_expert_equals_dense_matmul():
+    """k=1, every token on expert 3 with weight 1: y = Wd (silu(Wg x) * (Wu x))."""
+    w = synth.tiny(seed=5)
+    T, F = w.T, w.F
+    ids = np.full((T, 1), 3, np.int32)
+    ones = np.ones((T, 1))
+    res = oracle.ffn(w.x_bits, ids, ones, w.gate_up, w.down)
+    wgu = _brute_dense(w.gate_up, 3)
+    wd = _brute_dense(w.down, 3)
+    x = nvfp4.bf16_to_f64(w.x_bits)
+    g = x @ wgu[:F].T
+    u = x @ wgu[F:].T
+    h = g / (1 + np.exp(-g)) * u
+    y = h @ wd.T
+    assert np.allclose(res.y, y, rtol=1e-12, atol=1e-12 * np.abs(y).max())
+
+
+def test_ffn_invariant_under_pair_order_and_expert_relabel():
+    w = synth.tiny(seed=6)
+    ids, ww = oracle.route_topk(w.logits, w.k)
+    ref = oracle.ffn(w.x_bits, ids, ww, w.gate_up, w.down)
+    # permute the j order of each token's pairs (weights move with their ids)
+    perm = np.array([1, 0])
+    r2 = oracle.ffn(w.x_bits, ids[:, perm], ww[:, perm], w.gate_up, w.down)
+    assert np.allclose(r2.y, ref.y, rtol=1e-13, atol=1e-12)
+    # relabel experts: bank[e'] = bank[pi^-1(e')], ids -> pi(ids)
+    rng = np.random.default_rng(0)
+    pi = rng.permutation(w.E)
+    inv = np.argsort(pi)
+    gu = synth.Bank(w.gate_up.codes[inv], w.gate_up.scales[inv])
+    dn = synth.Bank(w.down.codes[inv], w.down.scales[inv])
+    r3 = oracle.ffn(w.x_bits, pi[ids].astype(np.int32), ww, gu, dn)
+    assert np.array_equal(r3.y, ref.y)
+
+
+def test_ffn_split_tokens_invariance():
+    """Computing two halves of the batch separately gives the same rows (page 4's
+    "shared N160 + N160 versus full N320" check, read as a split of the batch)."""
+    w = synth.decode(T=4)
+    sub = synth.Bank(w.gate_up.codes, w.gate_up.scales)
+    ids, ww = oracle.route_topk(w.logits, w.k)
+    full = oracle.ffn(w.x_bits, ids, ww, sub, w.down)
+    a = oracle.ffn(w.x_bits, ids, ww, sub, w.down, tokens=[0, 1])
+    b = oracle.ffn(w.x_bits, ids, ww, sub, w.down, tokens=[2, 3])
+    assert np.array_equal(full.y[:2], a.y[:2]) and np.array_equal(full.y[2:], b.y[2:])
+    assert np.all(a.y[2:] == 0)
+
+
+def test_ffn_prefill_mode_uses_quantised_operands():
+    w = synth.tiny(seed=7)
+    ids, ww = oracle.route_topk(w.logits, w.k)
+    res = oracle.ffn(w.x_bits, ids, ww, w.gate_up, w.down, mode="prefill")
+    cx, sx, ex = res.qx
+    x = nvfp4.bf16_to_f64(w.x_bits)
+    assert np.array_equal(cx, nvfp4.quantize(x)[0])
+    dec = oracle.ffn(w.x_bits, ids, ww, w.gate_up, w.down)
+    rel = np.abs(res.y - dec.y).max() / np.abs(dec.y).max()
+    assert 1e-3 < rel < 0.5        # quantising activations moves y, but not wildly
+    # the h fed to the down projection is exactly the dequantised Q(f32(h))
+    qc, qs, qe = res.qh
+    h32 = res.h.astype(np.float32).astype(np.float64)
+    c2, s2, e2 = nvfp4.quantize(h32)
+    assert np.array_equal(qc, c2) and np.array_equal(qs, s2)
+    assert np.array_equal(res.h_used, nvfp4.dequant_q(qc, qs, qe))
+
+
+def test_prefill_ambiguity_covers_perturbations():
+    """Any h within the band quantises to codes that differ only where flagged, by at
+    most the flagged allowance."""
+    w = synth.tiny(seed=8)
+    ids, ww = oracle.route_topk(w.logits, w.k)
+    res = oracle.ffn(w.x_bits, ids, ww, w.gate_up, w.down, mode="prefill")
+    P = w.P
+    band_scale = 300       # widen the band so that flags actually occur on a tiny case
+    amb = oracle.qh_ambiguity(res, np.arange(P), beta=oracle.moe.H_BAND * band_scale)
+    base = nvfp4.dequant_q(*res.qh)
+    rng = np.random.default_rng(0)
+    hit = 0
+    for trial in range(20):
+        pert = res.h + amb.band * rng.uniform(-1, 1, res.h.shape)
+        h32 = pert.astype(np.float32).astype(np.float64)
+        c, s, e = nvfp4.quantize(h32)
+        d = nvfp4.dequant_q(c, s, e)
+        diff = np.abs(d - base)
+        changed = diff > 0
+        hit += changed.sum()
+        assert np.all(amb.flagged[changed])
+        assert np.all(diff <= amb.delta + 1e-300)
+    assert hit > 0
+
+
+def test_expert_bytes_match_page_traffic(golden_dir):
+    per = oracle.unique_expert_bytes(2560, 640)
+    assert per == 2 * 640 * (1280 + 160) + 2560 * (320 + 40) == 2764800
+    rows = [l.split() for l in open(os.path.join(golden_dir, "rows_traffic.txt"))
+            if l.strip() and not l.startswith("#")]
+    for path, nrows, traffic, uniq in rows:
+        if uniq == "-":
+            continue
+        rest = int(traffic) - int(uniq) * per
+        assert 0 < rest < 4_000_000, path        # activations, routing and outputs only
+
+
+def test_useful_flops_prefill():
+    assert oracle.useful_flops(32768, 4096, 640) == 515_396_075_520
