@@ -1,0 +1,454 @@
+"""Benchmark of the routed-MoE NVFP4 FFN layer on GB300 (one JSON line on stdout).
+
+Default workload: the decode sweep's largest point, T=8 tokens, hidden=2560, ff=640,
+E=512 experts, top-10 ("moe_sel_census.rs" column curve at t=8 with the
+"moe_union_probe.rs" geometry).  One step = one full layer (route, CSR, gate/up+SiLU,
+down, combine) over a fresh batch; the metric is GB/s of unique NVFP4 expert bytes
+(decode) or TFLOP/s of useful work (prefill), with the fraction of roofline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own replica of the workload (weak scaling);
+the slowest rank's time is reported and `value` counts the work of all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FP4_OVER_BF16 = 6.0          # nominal dense ratio 13.5 / 2.25 PFLOP/s
+L2_FLUSH_BYTES = 512 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="decode_T8")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--batches", type=int, default=8, help="distinct input batches rotated")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-tokens", type=int, default=1)
+    return ap.parse_args()
+
+
+def workload_desc(wl) -> str:
+    return f"{wl.name}: T={wl.T} H={wl.H} F={wl.F} E={wl.E} k={wl.k}"
+
+
+def is_prefill(name: str) -> bool:
+    return name.startswith("prefill")
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            return d, "measured"
+        except Exception:
+            pass
+    return None, "fallback"
+
+
+def peak_hbm(peaks):
+    if peaks:
+        for k in ("hbm_gbs", "hbm_GBps", "hbm"):
+            if k in peaks:
+                return float(peaks[k]), "of measured"
+    return FALLBACK_HBM_GBS, "of fallback"
+
+
+def peak_fp4(peaks, sustained: bool):
+    if peaks:
+        key = "bf16_tflops_sustained" if sustained and "bf16_tflops_sustained" in peaks else "bf16_tflops"
+        if key in peaks:
+            return float(peaks[key]) * FP4_OVER_BF16, f"of measured ({key} x {FP4_OVER_BF16:g} nominal fp4/bf16)"
+    return FALLBACK_BF16_TFLOPS * FP4_OVER_BF16, f"of fallback (1.9 PF bf16 x {FP4_OVER_BF16:g})"
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle as it stands, on a bounded sample, in a fresh process
+# ---------------------------------------------------------------------------
+
+def cpu_baseline(workload: str, tokens: int, seed: int = 0, threads: int = 1):
+    env = dict(os.environ)
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[v] = str(threads)
+    code = (
+        "import json,sys,time; sys.path.insert(0, %r)\n"
+        "import numpy as np, synth, oracle\n"
+        "wl = synth.by_name(%r, %d)\n"
+        "toks = np.arange(min(%d, wl.T))\n"
+        "t0 = time.perf_counter()\n"
+        "if wl.logits is not None:\n"
+        "    ids, w = oracle.route_topk(wl.logits[toks], wl.k)\n"
+        "else:\n"
+        "    ids, w = wl.ids[toks], wl.weights[toks].astype(np.float64)\n"
+        "sub = synth.Workload(wl.name, len(toks), wl.H, wl.F, wl.E, wl.k, wl.x_bits[toks], wl.gate_up, wl.down)\n"
+        "mode = 'prefill' if wl.name.startswith('prefill') else 'decode'\n"
+        "res = oracle.ffn(sub.x_bits, ids, w, sub.gate_up, sub.down, mode=mode)\n"
+        "dt = time.perf_counter() - t0\n"
+        "U = len(np.unique(ids))\n"
+        "print(json.dumps({'seconds': dt, 'unique': int(U), 'pairs': int(ids.size), 'tokens': int(len(toks))}))\n"
+    ) % (ROOT, workload, seed, tokens)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                       timeout=600)
+    if r.returncode != 0:
+        return {"error": r.stderr[-400:]}
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_value(workload, info, H, F):
+    import oracle
+    if is_prefill(workload):
+        flops = oracle.useful_flops(info["pairs"], H, F)
+        return flops / info["seconds"] / 1e12, "TFLOP/s"
+    return info["unique"] * oracle.unique_expert_bytes(H, F) / info["seconds"] / 1e9, "GB/s"
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the CPU oracle timed on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import synth
+    wl = synth.by_name(args.workload)
+    times = []
+    info = None
+    for i in range(args.warmup + args.steps):
+        info = cpu_baseline(args.workload, args.cpu_sample_tokens)
+        if "error" in info:
+            print(json.dumps({"impl": "reference", "unavailable": info["error"][-200:]}))
+            return
+        if i >= args.warmup:
+            times.append(info)
+    tot_s = sum(t["seconds"] for t in times)
+    vals = [cpu_value(args.workload, t, wl.H, wl.F)[0] for t in times]
+    unit = cpu_value(args.workload, times[0], wl.H, wl.F)[1]
+    value = statistics.median(vals)
+    sample = f"{args.cpu_sample_tokens} token(s) of {workload_desc(wl)} per step, float64 numpy oracle"
+    line = {
+        "impl": "reference", "metric": metric_name(args.workload), "value": value, "unit": unit,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": tot_s / len(times) * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_desc(wl), "sample": sample},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def metric_name(workload):
+    if is_prefill(workload):
+        return "routed-MoE layer TFLOP/s (prefill, NVFP4 block-scaled tcgen05), % of FP4 roof"
+    return "routed-MoE layer GB/s of unique NVFP4 expert bytes (decode), % of HBM roof"
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import synth
+    import oracle
+    import nvfp4_grouped_gemm_gb300 as moe
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    wl = synth.by_name(args.workload, seed=rank)
+    prefill = is_prefill(args.workload)
+    path = moe.PATH_PREFILL if prefill else moe.PATH_DECODE
+    gu = moe.NvFp4Bank.from_numpy(wl.gate_up, dev)
+    dn = moe.NvFp4Bank.from_numpy(wl.down, dev)
+    layer = moe.MoeLayer(gu, dn, wl.k)
+
+    # distinct batches of the same shape, rotated step by step
+    rng = np.random.default_rng(1000 + rank)
+    nb = max(1, args.batches)
+    xs, lgs, idss, wss = [], [], [], []
+    for b in range(nb):
+        x = synth.f32_to_bf16_bits(rng.standard_normal((wl.T, wl.H), dtype=np.float32))
+        xs.append(torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16))
+        if wl.logits is not None:
+            lgs.append(torch.from_numpy(rng.standard_normal((wl.T, wl.E), dtype=np.float32)).to(dev))
+        else:
+            ids = wl.ids if b == 0 else (synth.skewed_ids(rng, wl.T, wl.k, wl.E) if prefill
+                                          else wl.ids)
+            idss.append(torch.from_numpy(np.ascontiguousarray(ids)).to(dev))
+            wss.append(torch.from_numpy(wl.weights).to(dev))
+
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step(b, ev=None):
+        kw = {"logits": lgs[b]} if lgs else {"ids": idss[b], "w": wss[b]}
+        return layer.forward(xs[b], path=path, stream=stream, **kw)
+
+    # unique experts per batch (from the device CSR of an untimed run)
+    uniq = []
+    with torch.cuda.stream(stream):
+        for b in range(nb):
+            step(b)
+            uniq.append(int(layer.buffers(wl.T, path)["csr"].n_active.item()))
+    stream.synchronize()
+    per_expert = oracle.unique_expert_bytes(wl.H, wl.F)
+    gu_bytes_per_expert = 2 * wl.F * (wl.H // 2 + wl.H // 16)
+    flops_per_step = oracle.useful_flops(wl.P, wl.H, wl.F)
+
+    # device-timed region: per-step events around the layer, L2 flushed between steps
+    def timed(n_steps, warm):
+        evs = []
+        for i in range(warm + n_steps):
+            b = i % nb
+            with torch.cuda.stream(stream):
+                flush.zero_()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e2 = torch.cuda.Event(enable_timing=True)
+                e3 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                kw = {"logits": lgs[b]} if lgs else {"ids": idss[b], "w": wss[b]}
+                bufs = layer.buffers(wl.T, path)
+                if lgs:
+                    moe.moe_route_topk(lgs[b], wl.k, bufs["ids"], bufs["w"], stream)
+                    ids_t, w_t = bufs["ids"], bufs["w"]
+                else:
+                    ids_t, w_t = idss[b], wss[b]
+                moe.moe_build_expert_csr(ids_t, wl.E, bufs["csr"], bufs["ws"], stream)
+                e1.record(stream)
+                moe.moe_grouped_gate_up_silu_nvfp4(xs[b], wl.k, wl.F, gu, bufs["csr"], bufs["ws"],
+                                                   path, stream)
+                e2.record(stream)
+                moe.moe_grouped_down_combine_nvfp4(dn, bufs["csr"], w_t, wl.T, wl.H, wl.F, wl.k,
+                                                   bufs["y"], bufs["ws"], path, stream)
+                e3.record(stream)
+            if i >= warm:
+                evs.append((b, e0, e1, e2, e3))
+        return evs
+
+    timed(0, args.warmup)
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(local)
+    sampler.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.perf_counter()
+    evs = timed(args.steps, 0)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    t_wall = time.perf_counter() - t_wall0
+    clocks = sampler.stop()
+
+    step_ms = [e0.elapsed_time(e3) for (_, e0, _, _, e3) in evs]
+    gu_ms = [e1.elapsed_time(e2) for (_, _, e1, e2, _) in evs]
+    dn_ms = [e2.elapsed_time(e3) for (_, _, _, e2, e3) in evs]
+    tot_ms = sum(step_ms)
+    uniq_steps = [uniq[b] for (b, *_r) in evs]
+    if world > 1:
+        t = torch.tensor([tot_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        tot_ms = float(t.item())
+
+    if prefill:
+        work = flops_per_step * args.steps * world
+        value = work / (tot_ms * 1e-3) / 1e12
+        unit = "TFLOP/s"
+    else:
+        work = sum(u * per_expert for u in uniq_steps) * world
+        value = work / (tot_ms * 1e-3) / 1e9
+        unit = "GB/s"
+
+    peaks, _src = load_peaks()
+    gu_avg_ms = sum(gu_ms) / len(gu_ms)
+    if prefill:
+        pk, pk_src = peak_fp4(peaks, sustained=False)
+        gu_flops = wl.P * 2 * (2 * wl.F * wl.H)
+        ach = gu_flops / (gu_avg_ms * 1e-3) / 1e12
+        roof = {"bound": "hbm", "kernel": "prefill gate_up (tcgen05)", "achieved": ach,
+                "peak": pk, "unit": "TFLOP/s", "frac": ach / pk, "traffic": None,
+                "peak_source": pk_src}
+    else:
+        pk, pk_src = peak_hbm(peaks)
+        gu_bytes = [uniq[b] * gu_bytes_per_expert for (b, *_r) in evs]
+        ach = sum(gu_bytes) / (sum(gu_ms) * 1e-3) / 1e9
+        roof = {"bound": "hbm", "kernel": "decode gate_up+SiLU (moe_grouped_gate_up_silu_nvfp4)",
+                "achieved": ach, "peak": pk, "unit": "GB/s", "frac": ach / pk,
+                "traffic": None, "peak_source": pk_src,
+                "algorithmic_bytes_per_launch": sum(gu_bytes) / len(gu_bytes)}
+
+    # end to end through the public API with pinned host buffers
+    e2e = None
+    if rank == 0 or world > 1:
+        x_h = [xx.cpu().pin_memory() for xx in xs]
+        l_h = [ll.cpu().pin_memory() for ll in lgs] if lgs else None
+        i_h = [ii.cpu().pin_memory() for ii in idss] if idss else None
+        w_h = [ww.cpu().pin_memory() for ww in wss] if wss else None
+        y_h = torch.empty(wl.T, wl.H, dtype=torch.float32).pin_memory()
+        x_d = torch.empty_like(xs[0])
+        l_d = torch.empty_like(lgs[0]) if lgs else None
+        i_d = torch.empty_like(idss[0]) if idss else None
+        w_d = torch.empty_like(wss[0]) if wss else None
+        e2e_ms = []
+        for i in range(args.warmup + args.steps):
+            b = i % nb
+            with torch.cuda.stream(stream):
+                flush.zero_()
+                a0 = torch.cuda.Event(enable_timing=True)
+                a1 = torch.cuda.Event(enable_timing=True)
+                a0.record(stream)
+                x_d.copy_(x_h[b], non_blocking=True)
+                if lgs:
+                    l_d.copy_(l_h[b], non_blocking=True)
+                    y = layer.forward(x_d, logits=l_d, path=path, stream=stream)
+                else:
+                    i_d.copy_(i_h[b], non_blocking=True)
+                    w_d.copy_(w_h[b], non_blocking=True)
+                    y = layer.forward(x_d, ids=i_d, w=w_d, path=path, stream=stream)
+                y_h.copy_(y, non_blocking=True)
+                a1.record(stream)
+            if i >= args.warmup:
+                e2e_ms.append((b, a0, a1))
+        torch.cuda.synchronize(dev)
+        e_tot = sum(a0.elapsed_time(a1) for (_, a0, a1) in e2e_ms)
+        if prefill:
+            e_val = flops_per_step * len(e2e_ms) / (e_tot * 1e-3) / 1e12
+        else:
+            e_val = sum(uniq[b] * per_expert for (b, _, _) in e2e_ms) / (e_tot * 1e-3) / 1e9
+        h2d = xs[0].numel() * 2 + (lgs[0].numel() * 4 if lgs else idss[0].numel() * 4 + wss[0].numel() * 4)
+        e2e = {"value": e_val, "unit": unit, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(wl.T * wl.H * 4), "ms_per_step": e_tot / len(e2e_ms)}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        info = cpu_baseline(args.workload, args.cpu_sample_tokens)
+        if "error" not in info:
+            v, u = cpu_value(args.workload, info, wl.H, wl.F)
+            cpu = {"value": v, "unit": u, "cores": 1, "kind": "oracle",
+                   "sample": f"{info['tokens']} token(s), {info['pairs']} pairs, "
+                             f"{info['unique']} experts of {workload_desc(wl)}; float64 numpy oracle, "
+                             f"{info['seconds']:.2f} s"}
+        else:
+            cpu = {"error": info["error"][-200:]}
+
+    launches_per_step = 5 if not prefill else 7
+    line = {
+        "metric": metric_name(args.workload), "value": value, "unit": unit, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "nvfp4 weights (e2m1 x ue4m3) * f16 activations, f32 accumulate" if not prefill
+                 else "nvfp4 x nvfp4 block-scaled (e2m1, ue4m3), f32 accumulate",
+        "data": "synthetic",
+        "config": {"workload": workload_desc(wl), "l2": "flushed (512 MiB write) before every step",
+                   "batches_rotated": nb, "unique_experts_mean": float(np.mean(uniq_steps)),
+                   "path": "prefill" if prefill else "decode"},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "breakdown_ms": {"route+csr": float(np.mean([e0.elapsed_time(e1) for (_, e0, e1, _, _) in evs])),
+                         "gate_up": float(np.mean(gu_ms)), "down+combine": float(np.mean(dn_ms))},
+        "wall_s": t_wall,
+    }
+    print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,178 @@
+/*
+ * moe.h -- C ABI of the routed Mixture-of-Experts FFN with NVFP4 weights
+ * (libmoe_gb300.so, hand-written CUDA for sm_103a).
+ *
+ * One layer runs four calls on one stream:
+ *
+ *   moe_route_topk                  top-k routing of router logits
+ *   moe_build_expert_csr            expert-first grouping of the (token, expert) pairs
+ *   moe_grouped_gate_up_silu_nvfp4  per expert: h = silu(W_gate a) * (W_up a)
+ *   moe_grouped_down_combine_nvfp4  per expert: z = W_down h, then y[t] = sum_j w[t,j] z[t*k+j]
+ *
+ * Sources of the definitions (the pages the method is taken from):
+ *   - "moe_sk_repro.rs" (fn main): pairs p = t*k + j grouped by expert in ascending p
+ *     (buckets / ex_ids / ex_off / ex_pairs), token of a pair = p / k, three grouped
+ *     projections per layer (gate, up, down);
+ *   - "moe_union_probe.rs" (header comment and fn main): fused gate_up bank
+ *     [E, 2*ff, hidden] (ff gate rows then ff up rows), down bank [E, hidden, ff], a row
+ *     is in_f/2 E2M1 code bytes + in_f/16 UE4M3 scale bytes, each distinct expert's
+ *     bytes read once per call (the union-of-experts gather);
+ *   - "moe_sel_census.rs" (header constants): NVFP4 = E2M1 codes with one UE4M3 scale
+ *     per 16 weights;
+ *   - "Rank-local E256 MoE misses the Qwen K1 and K4 step budgets" (numeric check
+ *     table and the paragraph after it): the atomic BF16 FC2 accumulation made replays
+ *     differ; this library's combine uses no floating-point atomics and is bit-identical
+ *     across replays.
+ *
+ * Conventions for every call:
+ *   - Array pointers are DEVICE pointers owned by the caller; nothing is allocated or
+ *     freed by the library, and no state survives a call.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream). Calls are asynchronous,
+ *     do no host synchronisation and no allocation, so they can be captured in a CUDA
+ *     graph (moe_get_device_error excepted).
+ *   - Shapes are validated on the host before anything is launched; a bad argument
+ *     returns an error status and launches nothing. No call prints, aborts or throws.
+ *   - The workspace `ws` of moe_workspace_bytes(T, H, F, E, k, path) bytes (256-byte
+ *     aligned) carries state from moe_build_expert_csr to the two projection calls:
+ *     pass the SAME ws (and the same T, k, path) to the three calls of one layer.
+ *     Zero-fill it once after allocating it (its first word is the device error word).
+ *   - Problems only the device can see (an expert id outside [0, E)) set a sticky bit
+ *     in the workspace's error word; the offending pair is skipped (it contributes
+ *     nothing to y). moe_get_device_error reads and clears the word.
+ *
+ * NVFP4 bank layout (planar, row-major):
+ *   codes  u8 [E][rows][in_f/2]  two E2M1 codes per byte, low nibble = even element
+ *   scales u8 [E][rows][in_f/16] one UE4M3 byte per 16 consecutive elements of a row
+ *   value(e, r, c) = E2M1(code) * UE4M3(scale[e][r][c/16]); scale bytes must be <= 0x7E.
+ *   Both planes must be 16-byte aligned.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, k > E, misalignment */
+  MOE_ERR_UNSUPPORTED = 2,   /* valid but outside what the kernels handle (see limits) */
+  MOE_ERR_WORKSPACE = 3,     /* ws smaller than moe_workspace_bytes() or misaligned */
+  MOE_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+  MOE_ERR_TIMEOUT = 5        /* a bounded device wait gave up (device error word) */
+} moe_status;
+
+/* Path selection: DECODE multiplies the exact bf16 activations by the dequantised
+ * weights and keeps h in float32; PREFILL quantises x and h to NVFP4 (per-row power-of-two
+ * scale, UE4M3 per 16, E2M1 codes; nearest-even) and runs block-scaled FP4 tensor-core
+ * GEMMs. AUTO picks PREFILL when T*k >= moe_prefill_min_pairs(). The two paths differ
+ * in numerics by design. */
+enum { MOE_PATH_AUTO = 0, MOE_PATH_DECODE = 1, MOE_PATH_PREFILL = 2 };
+
+/* Bits of the device error word. */
+enum { MOE_DEVERR_EXPERT_ID = 1, MOE_DEVERR_TIMEOUT = 2 };
+
+/* One NVFP4 weight bank. gate_up: rows = 2F (gate rows 0..F-1, up rows F..2F-1),
+ * in_f = H. down: rows = H, in_f = F. */
+typedef struct moe_nvfp4_bank {
+  const uint8_t* codes;
+  const uint8_t* scales;
+  int32_t E, rows, in_f;
+} moe_nvfp4_bank;
+
+/* Expert-first CSR written by moe_build_expert_csr (all device arrays, caller-owned):
+ *   expert_offsets i32 [E+1]  exclusive prefix sum of per-expert pair counts
+ *   pair_ids       i32 [T*k]  pair indices p = t*k + j sorted by (expert, p); entries past
+ *                             expert_offsets[E] are unspecified (pairs with invalid ids)
+ *   active_experts i32 [E]    experts with at least one pair, ascending; first n_active valid
+ *   n_active       i32 [1]    number of active experts (stays on the device) */
+typedef struct moe_csr {
+  int32_t* expert_offsets;
+  int32_t* pair_ids;
+  int32_t* active_experts;
+  int32_t* n_active;
+} moe_csr;
+
+/* Byte offsets of the workspace regions (for tests and tools; the layout depends only
+ * on the arguments of moe_workspace_bytes). A region of size 0 is absent. */
+typedef struct moe_ws_layout {
+  size_t total;
+  size_t error_word;   /* u32 device error word */
+  size_t pair_pos;     /* i32 [P]   CSR position of pair p, -1 if its expert id is invalid */
+  size_t h;            /* f32 [P][F] h = silu(g) * u, rows in CSR order */
+  size_t qx_codes;     /* prefill: u8 [P][H/2]  Q(x) in CSR order */
+  size_t qx_scales;    /* prefill: u8 [P][H/16] */
+  size_t qx_exp;       /* prefill: i32 [P] row exponents */
+  size_t qh_codes;     /* prefill: u8 [P][F/2]  Q(h) in CSR order */
+  size_t qh_scales;    /* prefill: u8 [P][F/16] */
+  size_t qh_exp;       /* prefill: i32 [P] */
+  size_t partial;      /* f32 [P][H] per-pair down projections z, rows in CSR order */
+  size_t tiles;        /* prefill: i32 [2 * max_tiles + 1] (expert, row start) M-tile list */
+} moe_ws_layout;
+
+/* Limits (MOE_ERR_UNSUPPORTED beyond them): 1 <= k <= min(E, 32); E <= 1024;
+ * H % 128 == 0; F % 64 == 0; T*k < 2^31 / max(H, F). */
+
+/* Workspace size in bytes for one layer with these sizes (0 if the sizes are invalid). */
+size_t moe_workspace_bytes(int32_t T, int32_t H, int32_t F, int32_t E, int32_t k, int32_t path);
+
+/* Fill *out with the workspace region offsets for these sizes. */
+moe_status moe_workspace_layout(int32_t T, int32_t H, int32_t F, int32_t E, int32_t k,
+                                int32_t path, moe_ws_layout* out);
+
+/* Path AUTO resolves to: PREFILL if T*k >= this value, else DECODE. */
+int32_t moe_prefill_min_pairs(void);
+/* The path a call with these arguments runs (DECODE or PREFILL). */
+int32_t moe_resolve_path(int32_t T, int32_t k, int32_t path);
+
+/* Top-k routing of router logits (the pages' probes start from already-routed pairs;
+ * this is the router that produces them). For each token t: the k experts with the largest
+ * logits[t, :] in descending order, ties broken towards the lower expert id, comparing
+ * the float32 values exactly; topk_w[t, j] = exp(l_j - l_0) / sum_j' exp(l_j' - l_0),
+ * i.e. the softmax over the selected logits (equal to the full softmax renormalised
+ * over the selection). logits f32 [T][E] (finite), topk_ids i32 [T][k], topk_w f32 [T][k]. */
+moe_status moe_route_topk(const float* logits, int32_t T, int32_t E, int32_t k,
+                          int32_t* topk_ids, float* topk_w, void* stream);
+
+/* Expert-first CSR of the P = T*k pairs ("moe_sk_repro.rs", fn main): a counting sort by
+ * expert that keeps ascending p within an expert (placement by prefix sums, not by
+ * atomic arrival order, so the result is bit-exact and deterministic). topk_ids i32
+ * [T][k]. Writes `csr` and the workspace's pair_pos; ids outside [0, E) set
+ * MOE_DEVERR_EXPERT_ID and are left out. */
+moe_status moe_build_expert_csr(const int32_t* topk_ids, int32_t T, int32_t k, int32_t E,
+                                moe_csr csr, void* ws, size_t ws_bytes, void* stream);
+
+/* Grouped gate/up projection with SiLU(gate) * up over the active experts. Each active
+ * expert's 2F x H NVFP4 rows are read from HBM once per call whatever its number of
+ * pairs (the union-of-experts gather of "moe_union_probe.rs"). x_bf16 bf16 [T][H]
+ * (16-byte aligned); w_gate_up: rows = 2F, in_f = H. Result h f32 [P][F] in the
+ * workspace, rows in CSR order. */
+moe_status moe_grouped_gate_up_silu_nvfp4(const void* x_bf16, int32_t T, int32_t H, int32_t F,
+                                          int32_t k, const moe_nvfp4_bank* w_gate_up,
+                                          moe_csr csr, int32_t path, void* ws, size_t ws_bytes,
+                                          void* stream);
+
+/* Grouped down projection z_p = W_down[e] h_p over the active experts, then the
+ * deterministic combine y[t, :] = sum_{j=0..k-1} topk_w[t, j] * z_{t*k+j} summed in
+ * ascending j with no floating-point atomics. w_down: rows = H, in_f = F; topk_w f32
+ * [T][k]; y f32 [T][H] (overwritten; rows of tokens whose pairs are all invalid are 0). */
+moe_status moe_grouped_down_combine_nvfp4(const moe_nvfp4_bank* w_down, moe_csr csr,
+                                          const float* topk_w, int32_t T, int32_t H, int32_t F,
+                                          int32_t k, int32_t path, float* y, void* ws,
+                                          size_t ws_bytes, void* stream);
+
+/* Human-readable name of a status (static string, never NULL). */
+const char* moe_status_string(moe_status status);
+
+/* Synchronise `stream`, read the workspace's device error word into *code and clear
+ * it. For tests and diagnostics only: it blocks and cannot be graph-captured. */
+moe_status moe_get_device_error(const void* ws, void* stream, int32_t* code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

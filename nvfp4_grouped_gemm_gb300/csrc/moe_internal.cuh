@@ -1,0 +1,102 @@
+// Internal declarations shared by the translation units of libmoe_gb300.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "moe.h"
+
+namespace moe {
+
+constexpr int kMaxE = 1024;
+constexpr int kMaxK = 32;
+constexpr int kPrefillMinPairs = 2048;
+constexpr size_t kAlign = 256;
+
+inline size_t align_up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a; }
+
+// Workspace layout for one layer; pure function of the sizes (see moe_ws_layout).
+bool compute_layout(int T, int H, int F, int E, int k, int path, moe_ws_layout* L);
+int resolve_path(int T, int k, int path);
+
+// Launchers (return cudaGetLastError() of the launch sequence).
+cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w,
+                              cudaStream_t s);
+cudaError_t launch_build_csr(const int32_t* ids, int P, int k, int E, moe_csr csr,
+                             int32_t* pair_pos, uint32_t* err, cudaStream_t s);
+cudaError_t launch_decode_gate_up(const uint16_t* x_bf16, int T, int H, int F, int k,
+                                  const moe_nvfp4_bank& b, moe_csr csr, const moe_ws_layout& L,
+                                  char* ws, cudaStream_t s);
+cudaError_t launch_decode_down(const moe_nvfp4_bank& b, moe_csr csr, int T, int H, int F, int k,
+                               const moe_ws_layout& L, char* ws, cudaStream_t s);
+cudaError_t launch_combine(const float* w, int T, int H, int k, const moe_ws_layout& L, char* ws,
+                           float* y, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// Device helpers
+// ---------------------------------------------------------------------------
+
+// Two E2M1 codes (one byte, low nibble = even element) to an f16x2 (low half = even).
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+      : "=r"(r) : "r"(byte));
+  return r;
+}
+
+// Two UE4M3 bytes (low 16 bits of v) to f16x2.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
+      : "=r"(r) : "r"(v));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// Broadcast the low (hi=false) or high half of an f16x2 to both halves.
+__device__ __forceinline__ uint32_t bcast_lo(uint32_t v) { return __byte_perm(v, v, 0x1010); }
+__device__ __forceinline__ uint32_t bcast_hi(uint32_t v) { return __byte_perm(v, v, 0x3232); }
+
+// D += A(16x16 f16, row) * B(16x8 f16, col), f32 accumulate.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Streaming 128-bit load that does not allocate in L1 (weights are read once).
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint2 ldg_stream64(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
+               : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+
+// Exponent e with |v| * 2^-e in [2^14, 2^15) for v != 0 (0 for v == 0): the power-of-two
+// prescale that maps a row's largest magnitude into the top binade below f16's 2^15.
+__device__ __forceinline__ int f16_prescale_exp(float amax) {
+  if (!(amax > 0.0f)) return 0;
+  int e;
+  frexpf(amax, &e);          // amax = m * 2^e, m in [0.5, 1)
+  return (e - 1) - 14;
+}
+
+}  // namespace moe

@@ -1,0 +1,188 @@
+// Top-k routing and the expert-first CSR.
+//
+// route_topk_kernel: one warp per token.  Round r selects the largest (logit, -id) pair
+// among those ordered strictly after the pair selected in round r-1, so no element is
+// ever removed or overwritten and ties resolve to the lower id exactly as the float32
+// comparison dictates.
+//
+// build_csr_kernel: one CTA.  The P pairs are cut into 32 contiguous slices, one per warp.
+// Pass A counts each slice's pairs per expert in shared memory, pass B turns the
+// [slice][expert] counts into starting positions (expert offset + pairs of the same
+// expert in earlier slices), pass C walks each slice in ascending p and places pairs with
+// a warp-level match so that equal experts keep ascending p.  Placement never depends on
+// the order atomics happen to arrive in, so the output is bit-exact.
+#include "moe_internal.cuh"
+
+namespace moe {
+
+namespace {
+
+__device__ __forceinline__ bool before(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+__global__ void route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
+                                  int32_t* __restrict__ ids, float* __restrict__ w) {
+  const int warps = blockDim.x / 32;
+  const int t = blockIdx.x * warps + threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const float* row = logits + (size_t)t * E;
+  float prev_v = 0.0f;
+  int prev_i = -1;
+  float sel_v = 0.0f, first_v = 0.0f, denom = 0.0f;
+  float my_val = 0.0f;   // lane j < k keeps the j-th selected logit
+  int my_id = 0;
+  for (int r = 0; r < k; ++r) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int e = lane; e < E; e += 32) {
+      float v = row[e];
+      bool eligible = (prev_i < 0) || before(prev_v, prev_i, v, e);
+      if (eligible && (bi == 0x7fffffff || before(v, e, bv, bi))) { bv = v; bi = e; }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (oi != 0x7fffffff && (bi == 0x7fffffff || before(ov, oi, bv, bi))) { bv = ov; bi = oi; }
+    }
+    prev_v = bv;
+    prev_i = bi;
+    if (r == 0) first_v = bv;
+    if (lane == r) { my_val = bv; my_id = bi; }
+    sel_v = bv;
+  }
+  (void)sel_v;
+  float ex = (lane < k) ? expf(my_val - first_v) : 0.0f;
+  // sum in ascending j so every lane sees the same value
+  for (int j = 0; j < k; ++j) denom += __shfl_sync(0xffffffffu, ex, j);
+  if (lane < k) {
+    ids[(size_t)t * k + lane] = my_id;
+    w[(size_t)t * k + lane] = ex / denom;
+  }
+}
+
+constexpr int kCsrThreads = 1024;
+constexpr int kCsrWarps = kCsrThreads / 32;
+
+__device__ __forceinline__ int block_exclusive_scan(int v, int* scratch, int* total) {
+  // scratch: kCsrWarps ints
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int s = scratch[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    scratch[lane] = s;   // inclusive
+  }
+  __syncthreads();
+  int base = warp ? scratch[warp - 1] : 0;
+  *total = scratch[kCsrWarps - 1];
+  __syncthreads();
+  return base + x - v;
+}
+
+__global__ void __launch_bounds__(kCsrThreads, 1)
+build_csr_kernel(const int32_t* __restrict__ ids, int P, int E, int32_t* __restrict__ offsets,
+                 int32_t* __restrict__ pair_ids, int32_t* __restrict__ active,
+                 int32_t* __restrict__ n_active, int32_t* __restrict__ pair_pos,
+                 uint32_t* __restrict__ err) {
+  extern __shared__ int smem[];
+  int* hist = smem;                           // [kCsrWarps][E]
+  int* scratch = smem + kCsrWarps * E;        // [kCsrWarps]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < kCsrWarps * E; i += kCsrThreads) hist[i] = 0;
+  __syncthreads();
+
+  const int slice = (P + kCsrWarps - 1) / kCsrWarps;
+  const int p_beg = min(P, warp * slice), p_end = min(P, p_beg + slice);
+  int* my = hist + warp * E;
+  bool bad = false;
+  // pass A: per-slice counts
+  for (int p = p_beg + lane; p < p_end; p += 32) {
+    int e = ids[p];
+    if (e >= 0 && e < E) atomicAdd(&my[e], 1);
+    else { bad = true; pair_pos[p] = -1; }
+  }
+  if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(err, (uint32_t)MOE_DEVERR_EXPERT_ID);
+  __syncthreads();
+
+  // pass B: per expert, slice prefix and the expert's total; then the offsets scan
+  int cnt = 0;
+  if (tid < E) {
+    for (int w = 0; w < kCsrWarps; ++w) {
+      int c = hist[w * E + tid];
+      hist[w * E + tid] = cnt;
+      cnt += c;
+    }
+  }
+  int total;
+  int off = block_exclusive_scan(tid < E ? cnt : 0, scratch, &total);
+  int act_total;
+  int act_pos = block_exclusive_scan((tid < E && cnt > 0) ? 1 : 0, scratch, &act_total);
+  if (tid < E) {
+    offsets[tid] = off;
+    if (cnt > 0) active[act_pos] = tid;
+    for (int w = 0; w < kCsrWarps; ++w) hist[w * E + tid] += off;
+  }
+  if (tid == 0) {
+    offsets[E] = total;
+    *n_active = act_total;
+  }
+  __syncthreads();
+
+  // pass C: stable placement within each slice
+  for (int base = p_beg; base < p_end; base += 32) {
+    const int p = base + lane;
+    const bool in = p < p_end;
+    int e = in ? ids[p] : -1;
+    const bool valid = in && e >= 0 && e < E;
+    if (!valid) e = -1 - lane;                           // unique key: matches nobody
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const unsigned lower = peers & ((1u << lane) - 1u);
+    int start = valid ? my[e] : 0;
+    __syncwarp();
+    if (valid) {
+      const int pos = start + __popc(lower);
+      pair_ids[pos] = p;
+      pair_pos[p] = pos;
+      if (lower == 0) my[e] = start + __popc(peers);     // lowest lane of the group advances
+    }
+    __syncwarp();
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w,
+                              cudaStream_t s) {
+  const int warps = 8;
+  dim3 grid((T + warps - 1) / warps);
+  route_topk_kernel<<<grid, warps * 32, 0, s>>>(logits, T, E, k, ids, w);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_build_csr(const int32_t* ids, int P, int k, int E, moe_csr csr,
+                             int32_t* pair_pos, uint32_t* err, cudaStream_t s) {
+  (void)k;
+  const size_t smem = (size_t)(kCsrWarps * E + kCsrWarps) * sizeof(int);
+  cudaError_t st = cudaFuncSetAttribute(build_csr_kernel,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (st != cudaSuccess) return st;
+  build_csr_kernel<<<1, kCsrThreads, smem, s>>>(ids, P, E, csr.expert_offsets, csr.pair_ids,
+                                                csr.active_experts, csr.n_active, pair_pos, err);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

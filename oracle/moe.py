@@ -7,8 +7,8 @@ Steps, in the order the pages run them:
 
 1. ``route_topk``  -- per token, the k largest router logits (ties to the lower
    expert id), weights = softmax over the selected logits (equal to the full
-   softmax renormalised over the selection).  Router described in the
-   spec task text; the pages feed pre-routed pairs.
+   softmax renormalised over the selection).  The pages' probes start from
+   already-routed pairs; this is the router that produces them.
 2. ``build_expert_csr`` -- pairs p = t*k + j bucketed by expert in ascending p
    ("moe_sk_repro.rs", fn main: buckets, ex_ids, ex_off, ex_pairs); the token of
    a pair is p / k (csr_tok there).

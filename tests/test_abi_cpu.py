@@ -1,0 +1,97 @@
+"""The C-ABI library loads and exports every declared symbol; host-side logic (no GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import nvfp4_grouped_gemm_gb300 as moe
+from nvfp4_grouped_gemm_gb300 import _native
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?[\w\s\*]*?\b(moe_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(_native.lib_path()):
+        import nvfp4_grouped_gemm_gb300.build as b
+        b.build()
+    return _native.load()
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+    bound = {s[0] for s in _native.SIGNATURES}
+    assert set(names) <= bound | set(), set(names) - bound
+
+
+def test_status_strings(lib):
+    for code, name in _native.STATUS.items():
+        assert lib.moe_status_string(code).decode() == name
+    assert lib.moe_status_string(99).decode() == "MOE_ERR_UNKNOWN"
+
+
+def test_workspace_layout_host_logic(lib):
+    H, F, E, k = 2560, 640, 512, 10
+    for T in (1, 8, 128):
+        L = moe.workspace_layout(T, H, F, E, k, moe.PATH_DECODE)
+        P = T * k
+        assert L["error_word"] == 0 and L["pair_pos"] == 256
+        assert L["h"] >= L["pair_pos"] + 4 * P
+        assert L["partial"] >= L["h"] + 4 * P * F
+        assert L["total"] == moe.workspace_bytes(T, H, F, E, k, moe.PATH_DECODE)
+        for v in L.values():
+            assert v % 256 == 0
+    Lp = moe.workspace_layout(4096, 4096, 640, 288, 8, moe.PATH_PREFILL)
+    assert Lp["qx_codes"] > 0 and Lp["qh_codes"] > 0
+    assert moe.workspace_bytes(0, H, F, E, k) == 0
+    assert moe.workspace_bytes(4, 100, F, E, k) == 0        # H % 128 != 0 unsupported
+    assert moe.workspace_bytes(4, H, F, 8, 10) == 0         # k > E
+
+
+def test_path_resolution(lib):
+    th = moe.prefill_min_pairs()
+    assert moe.resolve_path(1, 10) == moe.PATH_DECODE
+    assert moe.resolve_path(th, 1) == moe.PATH_PREFILL
+    assert moe.resolve_path(th - 1, 1) == moe.PATH_DECODE
+    assert moe.resolve_path(4096, 8, moe.PATH_DECODE) == moe.PATH_DECODE
+
+
+def test_host_validation_rejects_before_launch(lib):
+    """Null pointers and bad sizes are rejected on the host (no CUDA call is made)."""
+    assert lib.moe_route_topk(None, 4, 16, 2, None, None, None) == 1
+    assert lib.moe_route_topk(8, 4, 16, 20, 8, 8, None) == 1            # k > E
+    assert lib.moe_route_topk(8, 4, 16, 64, 8, 8, None) == 1
+    assert lib.moe_route_topk(16, 4, 64, 40, 16, 16, None) == 2         # k > 32
+    csr = _native.CSR(None, None, None, None)
+    assert lib.moe_build_expert_csr(16, 4, 2, 16, csr, 256, 1 << 20, None) == 1
+    good = _native.CSR(16, 16, 16, 16)
+    assert lib.moe_build_expert_csr(16, 4, 2, 2048, good, 256, 1 << 20, None) == 2   # E > 1024
+    assert lib.moe_build_expert_csr(16, 4, 2, 16, good, None, 0, None) == 3
+    assert lib.moe_build_expert_csr(16, 4, 2, 16, good, 258, 1 << 20, None) == 3     # misaligned
+    bank = _native.Bank(16, 16, 16, 128, 256)
+    # x misaligned
+    assert lib.moe_grouped_gate_up_silu_nvfp4(8, 4, 256, 64, 2, ctypes.byref(bank), good, 0,
+                                              256, 1 << 20, None) == 1
+    # rows mismatch (2F = 128 expected, bank says 128 ok; give F=96 -> unsupported F%64)
+    assert lib.moe_grouped_gate_up_silu_nvfp4(16, 4, 256, 96, 2, ctypes.byref(bank), good, 0,
+                                              256, 1 << 20, None) == 2
+    # workspace too small
+    assert lib.moe_grouped_gate_up_silu_nvfp4(16, 4, 256, 64, 2, ctypes.byref(bank), good, 0,
+                                              256, 16, None) == 3
+    dbank = _native.Bank(16, 16, 16, 256, 64)
+    assert lib.moe_grouped_down_combine_nvfp4(ctypes.byref(dbank), good, 16, 4, 256, 64, 2, 0,
+                                              None, 256, 1 << 20, None) == 1

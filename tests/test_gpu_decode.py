@@ -1,0 +1,193 @@
+"""GPU parity of the decode path against the CPU oracle, through the C ABI.
+
+Integer outputs (expert ids, CSR offsets, pair order, active list, n_active) must be
+bit-exact; floating point must satisfy |y_gpu - y| <= 2e-3 * sum_j |w_j * terms| + 1e-5
+per element, and replays must be bit-identical.
+"""
+import hashlib
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+import oracle
+import nvfp4_grouped_gemm_gb300 as moe
+from gpu_util import run_layer, h_tolerance, assert_within, device_banks
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_csr(run, ids, E):
+    ref = oracle.build_expert_csr(ids, E)
+    n_valid = int(ref.offsets[-1])
+    assert np.array_equal(run.offsets, ref.offsets)
+    assert np.array_equal(run.pair_ids[:n_valid], ref.pair_ids)
+    assert run.n_active == ref.n_active
+    assert np.array_equal(run.active[:ref.n_active], ref.active)
+    assert np.array_equal(run.pair_pos, ref.pair_pos)
+    return ref
+
+
+def _check_layer(wl, run, tokens=None, check_h=True):
+    if wl.logits is not None:
+        ids, w = oracle.route_topk(wl.logits, wl.k)
+        assert np.array_equal(run.ids, ids), "routing ids differ"
+        assert np.allclose(run.w, w, rtol=2e-6, atol=1e-7), "routing weights differ"
+    else:
+        ids, w = wl.ids, wl.weights.astype(np.float64)
+    _check_csr(run, ids, wl.E)
+    res = oracle.ffn(wl.x_bits, ids, w, wl.gate_up, wl.down, tokens=tokens)
+    toks = np.arange(wl.T) if tokens is None else np.asarray(tokens)
+    pairs = (toks[:, None] * wl.k + np.arange(wl.k)).reshape(-1)
+    if check_h:
+        h_gpu = run.h_csr[run.pair_pos[pairs]]
+        assert_within(h_gpu, res.h[pairs], h_tolerance(res)[pairs], "h")
+    worst = assert_within(run.y[toks], res.y[toks], oracle.tolerance(res.tsum)[toks], "y")
+    return worst
+
+
+def test_tiny_decode():
+    wl = synth.tiny()
+    run = run_layer(wl)
+    assert run.err == 0
+    _check_layer(wl, run)
+
+
+@pytest.mark.parametrize("T", [1, 2, 4, 8])
+def test_decode_sweep(T):
+    wl = synth.decode(T)
+    run = run_layer(wl)
+    assert run.err == 0
+    _check_layer(wl, run)
+
+
+@pytest.mark.parametrize("U", [60, 30, 20, 10])
+def test_union_sweep(U):
+    wl = synth.union(U)
+    run = run_layer(wl)
+    assert run.err == 0
+    assert run.n_active == U
+    _check_layer(wl, run)
+
+
+@pytest.mark.parametrize("T", [16, 32, 64, 80, 128])
+def test_verify_batch(T):
+    wl = synth.verify(T)
+    run = run_layer(wl)
+    assert run.err == 0
+    tokens = None if T <= 32 else np.linspace(0, T - 1, 12).astype(int)
+    _check_layer(wl, run, tokens=tokens)
+
+
+def test_verify_replays_bit_identical():
+    """Ten CUDA-graph replays of the whole layer give one hash (deterministic combine)."""
+    wl = synth.verify(128)
+    gu, dn = device_banks(wl)
+    layer = moe.MoeLayer(gu, dn, wl.k)
+    x = torch.from_numpy(wl.x_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    logits = torch.from_numpy(wl.logits).cuda()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        layer.forward(x, logits=logits, stream=s)      # allocate buffers, warm up
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        y = layer.forward(x, logits=logits, stream=s)
+    hashes = set()
+    for _ in range(10):
+        g.replay()
+        torch.cuda.synchronize()
+        hashes.add(hashlib.sha256(y.cpu().numpy().tobytes()).hexdigest())
+    assert len(hashes) == 1
+    # eager calls agree with the graph bit for bit
+    y2 = layer.forward(x, logits=logits).cpu().numpy()
+    assert hashlib.sha256(y2.tobytes()).hexdigest() in hashes
+
+
+def test_split_batch_bit_identical():
+    """Page 4's split check: a batch computed as two halves equals the whole, bit for bit."""
+    wl = synth.decode(8)
+    gu, dn = device_banks(wl)
+    full = run_layer(wl, banks=(gu, dn), fetch=False).y
+    for lo, hi in ((0, 4), (4, 8)):
+        part = synth.Workload(wl.name, hi - lo, wl.H, wl.F, wl.E, wl.k, wl.x_bits[lo:hi],
+                              wl.gate_up, wl.down, logits=wl.logits[lo:hi])
+        y = run_layer(part, banks=(gu, dn), fetch=False).y
+        assert np.array_equal(y, full[lo:hi])
+
+
+def test_single_token_single_expert():
+    """k = 1, T = 1: the smallest layer."""
+    wl = synth.tiny(seed=3)
+    one = synth.Workload("one", 1, wl.H, wl.F, wl.E, 1, wl.x_bits[:1], wl.gate_up, wl.down,
+                         ids=np.array([[5]], np.int32), weights=np.array([[1.0]], np.float32))
+    run = run_layer(one)
+    _check_layer(one, run)
+
+
+def test_invalid_expert_ids_are_flagged_and_skipped():
+    wl = synth.tiny(seed=4)
+    ids = np.array([[1, 3], [99, 3], [-2, 0], [7, 7]], np.int32)
+    w = np.full((4, 2), 0.5, np.float32)
+    bad = synth.Workload("bad", 4, wl.H, wl.F, wl.E, 2, wl.x_bits, wl.gate_up, wl.down,
+                         ids=ids, weights=w)
+    run = run_layer(bad)
+    assert run.err & moe.DEVERR_EXPERT_ID
+    res = oracle.ffn(bad.x_bits, ids, w.astype(np.float64), bad.gate_up, bad.down)
+    ref = _check_csr(run, ids, bad.E)
+    assert int(ref.offsets[-1]) == 6
+    assert_within(run.y, res.y, oracle.tolerance(res.tsum), "y")
+    # the error word is cleared by reading it
+    assert moe.get_device_error(torch.zeros(256, dtype=torch.uint8, device="cuda")) == 0
+
+
+def test_duplicate_expert_in_one_token():
+    wl = synth.tiny(seed=9)
+    ids = np.array([[2, 2], [2, 5], [5, 2], [2, 2]], np.int32)
+    w = np.array([[0.3, 0.7], [0.5, 0.5], [0.9, 0.1], [0.25, 0.75]], np.float32)
+    dup = synth.Workload("dup", 4, wl.H, wl.F, wl.E, 2, wl.x_bits, wl.gate_up, wl.down,
+                         ids=ids, weights=w)
+    run = run_layer(dup)
+    _check_layer(dup, run)
+
+
+def test_many_pairs_on_one_expert():
+    """One expert with more pairs than one 8- or 16-token pass holds."""
+    wl = synth.decode(T=40)
+    ids = np.zeros((40, 10), np.int32)
+    ids[:, 0] = 17                         # 40 pairs on expert 17
+    ids[:, 1:] = synth.union_ids(40, 9, 400, 9) + 100
+    w = np.full((40, 10), 0.1, np.float32)
+    many = synth.Workload("many", 40, wl.H, wl.F, wl.E, 10, wl.x_bits, wl.gate_up, wl.down,
+                          ids=ids, weights=w)
+    run = run_layer(many)
+    _check_layer(many, run, tokens=[0, 13, 39])
+
+
+def test_route_ties_to_lower_id():
+    T, E, k = 64, 512, 10
+    rng = np.random.default_rng(11)
+    logits = np.round(rng.standard_normal((T, E)) * 2).astype(np.float32)   # many exact ties
+    ids = torch.zeros(T, k, dtype=torch.int32, device="cuda")
+    w = torch.zeros(T, k, dtype=torch.float32, device="cuda")
+    moe.moe_route_topk(torch.from_numpy(logits).cuda(), k, ids, w)
+    ref_ids, ref_w = oracle.route_topk(logits, k)
+    assert np.array_equal(ids.cpu().numpy(), ref_ids)
+    assert np.allclose(w.cpu().numpy(), ref_w, rtol=2e-6)
+
+
+@pytest.mark.parametrize("T,k,E", [(4096, 8, 288), (1, 1, 1), (3, 7, 1024), (2048, 1, 64)])
+def test_csr_bit_exact_large(T, k, E):
+    rng = np.random.default_rng(T + E)
+    ids = synth.skewed_ids(rng, T, k, E)
+    csr = moe.ExpertCSR(E, T * k)
+    ws = torch.zeros(moe.workspace_bytes(T, 128, 64, E, k, moe.PATH_DECODE), dtype=torch.uint8,
+                     device="cuda")
+    moe.moe_build_expert_csr(torch.from_numpy(ids).cuda(), E, csr, ws)
+    torch.cuda.synchronize()
+    ref = oracle.build_expert_csr(ids, E)
+    assert np.array_equal(csr.expert_offsets.cpu().numpy(), ref.offsets)
+    assert np.array_equal(csr.pair_ids.cpu().numpy()[:T * k], ref.pair_ids)
+    assert int(csr.n_active.item()) == ref.n_active
+    assert np.array_equal(csr.active_experts.cpu().numpy()[:ref.n_active], ref.active)
