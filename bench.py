@@ -21,6 +21,11 @@ import subprocess
 import sys
 import time
 
+if "reference" in sys.argv:
+    # the reference arm times the single-threaded CPU oracle: pin BLAS to one thread
+    for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[_v] = "1"
+
 import numpy as np
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -176,6 +181,25 @@ def cpu_value(workload, info, H, F):
 # reference arm: the CPU oracle timed on the host cores
 # ---------------------------------------------------------------------------
 
+def oracle_sample(wl, tokens):
+    """Run the oracle on the first `tokens` tokens of wl; returns the cpu_baseline info."""
+    import oracle
+    import synth
+    toks = np.arange(min(tokens, wl.T))
+    t0 = time.perf_counter()
+    if wl.logits is not None:
+        ids, w = oracle.route_topk(wl.logits[toks], wl.k)
+    else:
+        ids, w = wl.ids[toks], wl.weights[toks].astype(np.float64)
+    sub = synth.Workload(wl.name, len(toks), wl.H, wl.F, wl.E, wl.k, wl.x_bits[toks],
+                         wl.gate_up, wl.down)
+    mode = "prefill" if is_prefill(wl.name) else "decode"
+    oracle.ffn(sub.x_bits, ids, w, sub.gate_up, sub.down, mode=mode)
+    dt = time.perf_counter() - t0
+    return {"seconds": dt, "unique": int(len(np.unique(ids))), "pairs": int(ids.size),
+            "tokens": int(len(toks))}
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -183,19 +207,16 @@ def run_reference(args):
     import synth
     wl = synth.by_name(args.workload)
     times = []
-    info = None
     for i in range(args.warmup + args.steps):
-        info = cpu_baseline(args.workload, args.cpu_sample_tokens)
-        if "error" in info:
-            print(json.dumps({"impl": "reference", "unavailable": info["error"][-200:]}))
-            return
+        info = oracle_sample(wl, args.cpu_sample_tokens)
         if i >= args.warmup:
             times.append(info)
     tot_s = sum(t["seconds"] for t in times)
     vals = [cpu_value(args.workload, t, wl.H, wl.F)[0] for t in times]
     unit = cpu_value(args.workload, times[0], wl.H, wl.F)[1]
     value = statistics.median(vals)
-    sample = f"{args.cpu_sample_tokens} token(s) of {workload_desc(wl)} per step, float64 numpy oracle"
+    sample = (f"{times[0]['tokens']} token(s) ({times[0]['pairs']} pairs, {times[0]['unique']} "
+              f"experts) of {workload_desc(wl)} per step, float64 numpy oracle, 1 thread")
     line = {
         "impl": "reference", "metric": metric_name(args.workload), "value": value, "unit": unit,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -258,24 +279,59 @@ def run_ours(args):
             wss.append(torch.from_numpy(wl.weights).to(dev))
 
     stream = torch.cuda.Stream(device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_out = torch.empty((), dtype=torch.float32, device=dev)
 
-    def step(b, ev=None):
-        kw = {"logits": lgs[b]} if lgs else {"ids": idss[b], "w": wss[b]}
-        return layer.forward(xs[b], path=path, stream=stream, **kw)
+    class _Flush:
+        """Write a buffer 4x the L2, then read another one: the write evicts everything,
+        the read leaves only clean lines so no dirty write-back spills into the next step."""
+        @staticmethod
+        def zero_():
+            flush_w.zero_()
+            torch.sum(flush_r, out=flush_out)
+    flush = _Flush
+    bufs = layer.buffers(wl.T, path)
 
-    # unique experts per batch (from the device CSR of an untimed run)
+    def pre(b):           # route + CSR
+        if lgs:
+            moe.moe_route_topk(lgs[b], wl.k, bufs["ids"], bufs["w"], stream)
+            ids_t = bufs["ids"]
+        else:
+            ids_t = idss[b]
+        moe.moe_build_expert_csr(ids_t, wl.E, bufs["csr"], bufs["ws"], stream)
+
+    def gate_up(b):
+        moe.moe_grouped_gate_up_silu_nvfp4(xs[b], wl.k, wl.F, gu, bufs["csr"], bufs["ws"], path,
+                                           stream)
+
+    def post(b):          # down + combine
+        w_t = bufs["w"] if lgs else wss[b]
+        moe.moe_grouped_down_combine_nvfp4(dn, bufs["csr"], w_t, wl.T, wl.H, wl.F, wl.k,
+                                           bufs["y"], bufs["ws"], path, stream)
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        return g
+
+    # eager warm-up (allocations, attribute setup), unique experts per batch
     uniq = []
     with torch.cuda.stream(stream):
         for b in range(nb):
-            step(b)
-            uniq.append(int(layer.buffers(wl.T, path)["csr"].n_active.item()))
-    stream.synchronize()
+            pre(b); gate_up(b); post(b)
+            stream.synchronize()
+            uniq.append(int(bufs["csr"].n_active.item()))
     per_expert = oracle.unique_expert_bytes(wl.H, wl.F)
     gu_bytes_per_expert = 2 * wl.F * (wl.H // 2 + wl.H // 16)
     flops_per_step = oracle.useful_flops(wl.P, wl.H, wl.F)
 
-    # device-timed region: per-step events around the layer, L2 flushed between steps
+    # one CUDA graph per batch for the whole layer, and split graphs for the breakdown
+    full_g = [capture(lambda b=b: (pre(b), gate_up(b), post(b))) for b in range(nb)]
+    split_g = [(capture(lambda b=b: pre(b)), capture(lambda b=b: gate_up(b)),
+                capture(lambda b=b: post(b))) for b in range(nb)]
+
     def timed(n_steps, warm):
         evs = []
         for i in range(warm + n_steps):
@@ -284,26 +340,11 @@ def run_ours(args):
                 flush.zero_()
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
-                e2 = torch.cuda.Event(enable_timing=True)
-                e3 = torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
-                kw = {"logits": lgs[b]} if lgs else {"ids": idss[b], "w": wss[b]}
-                bufs = layer.buffers(wl.T, path)
-                if lgs:
-                    moe.moe_route_topk(lgs[b], wl.k, bufs["ids"], bufs["w"], stream)
-                    ids_t, w_t = bufs["ids"], bufs["w"]
-                else:
-                    ids_t, w_t = idss[b], wss[b]
-                moe.moe_build_expert_csr(ids_t, wl.E, bufs["csr"], bufs["ws"], stream)
+                full_g[b].replay()
                 e1.record(stream)
-                moe.moe_grouped_gate_up_silu_nvfp4(xs[b], wl.k, wl.F, gu, bufs["csr"], bufs["ws"],
-                                                   path, stream)
-                e2.record(stream)
-                moe.moe_grouped_down_combine_nvfp4(dn, bufs["csr"], w_t, wl.T, wl.H, wl.F, wl.k,
-                                                   bufs["y"], bufs["ws"], path, stream)
-                e3.record(stream)
             if i >= warm:
-                evs.append((b, e0, e1, e2, e3))
+                evs.append((b, e0, e1))
         return evs
 
     timed(0, args.warmup)
@@ -321,11 +362,9 @@ def run_ours(args):
     t_wall = time.perf_counter() - t_wall0
     clocks = sampler.stop()
 
-    step_ms = [e0.elapsed_time(e3) for (_, e0, _, _, e3) in evs]
-    gu_ms = [e1.elapsed_time(e2) for (_, _, e1, e2, _) in evs]
-    dn_ms = [e2.elapsed_time(e3) for (_, _, _, e2, e3) in evs]
+    step_ms = [e0.elapsed_time(e1) for (_, e0, e1) in evs]
     tot_ms = sum(step_ms)
-    uniq_steps = [uniq[b] for (b, *_r) in evs]
+    uniq_steps = [uniq[b] for (b, _, _) in evs]
     if world > 1:
         t = torch.tensor([tot_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -340,65 +379,89 @@ def run_ours(args):
         value = work / (tot_ms * 1e-3) / 1e9
         unit = "GB/s"
 
+    # per-kernel breakdown: the same layer as three graphs, L2 flushed before each step
+    brk = []
+    for i in range(args.warmup + args.steps):
+        b = i % nb
+        with torch.cuda.stream(stream):
+            flush.zero_()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            ev[0].record(stream)
+            split_g[b][0].replay()
+            ev[1].record(stream)
+            split_g[b][1].replay()
+            ev[2].record(stream)
+            split_g[b][2].replay()
+            ev[3].record(stream)
+        if i >= args.warmup:
+            brk.append((b, ev))
+    torch.cuda.synchronize(dev)
+    pre_ms = [ev[0].elapsed_time(ev[1]) for (_, ev) in brk]
+    gu_ms = [ev[1].elapsed_time(ev[2]) for (_, ev) in brk]
+    dn_ms = [ev[2].elapsed_time(ev[3]) for (_, ev) in brk]
+
     peaks, _src = load_peaks()
-    gu_avg_ms = sum(gu_ms) / len(gu_ms)
     if prefill:
         pk, pk_src = peak_fp4(peaks, sustained=False)
         gu_flops = wl.P * 2 * (2 * wl.F * wl.H)
-        ach = gu_flops / (gu_avg_ms * 1e-3) / 1e12
-        roof = {"bound": "hbm", "kernel": "prefill gate_up (tcgen05)", "achieved": ach,
-                "peak": pk, "unit": "TFLOP/s", "frac": ach / pk, "traffic": None,
-                "peak_source": pk_src}
+        ach = gu_flops / (float(np.mean(gu_ms)) * 1e-3) / 1e12
+        roof = {"bound": "hbm", "kernel": "prefill gate_up (tcgen05 block-scaled, graph of "
+                "tiles + Q(x) + GEMM)", "achieved": ach, "peak": pk, "unit": "TFLOP/s",
+                "frac": ach / pk, "traffic": None, "peak_source": pk_src}
     else:
         pk, pk_src = peak_hbm(peaks)
-        gu_bytes = [uniq[b] * gu_bytes_per_expert for (b, *_r) in evs]
+        gu_bytes = [uniq[b] * gu_bytes_per_expert for (b, _) in brk]
         ach = sum(gu_bytes) / (sum(gu_ms) * 1e-3) / 1e9
         roof = {"bound": "hbm", "kernel": "decode gate_up+SiLU (moe_grouped_gate_up_silu_nvfp4)",
                 "achieved": ach, "peak": pk, "unit": "GB/s", "frac": ach / pk,
                 "traffic": None, "peak_source": pk_src,
                 "algorithmic_bytes_per_launch": sum(gu_bytes) / len(gu_bytes)}
 
-    # end to end through the public API with pinned host buffers
+    # end to end through the public API: pinned host inputs in, host result out, per step
     e2e = None
-    if rank == 0 or world > 1:
-        x_h = [xx.cpu().pin_memory() for xx in xs]
-        l_h = [ll.cpu().pin_memory() for ll in lgs] if lgs else None
-        i_h = [ii.cpu().pin_memory() for ii in idss] if idss else None
-        w_h = [ww.cpu().pin_memory() for ww in wss] if wss else None
-        y_h = torch.empty(wl.T, wl.H, dtype=torch.float32).pin_memory()
-        x_d = torch.empty_like(xs[0])
-        l_d = torch.empty_like(lgs[0]) if lgs else None
-        i_d = torch.empty_like(idss[0]) if idss else None
-        w_d = torch.empty_like(wss[0]) if wss else None
-        e2e_ms = []
-        for i in range(args.warmup + args.steps):
-            b = i % nb
-            with torch.cuda.stream(stream):
-                flush.zero_()
-                a0 = torch.cuda.Event(enable_timing=True)
-                a1 = torch.cuda.Event(enable_timing=True)
-                a0.record(stream)
-                x_d.copy_(x_h[b], non_blocking=True)
-                if lgs:
-                    l_d.copy_(l_h[b], non_blocking=True)
-                    y = layer.forward(x_d, logits=l_d, path=path, stream=stream)
-                else:
-                    i_d.copy_(i_h[b], non_blocking=True)
-                    w_d.copy_(w_h[b], non_blocking=True)
-                    y = layer.forward(x_d, ids=i_d, w=w_d, path=path, stream=stream)
-                y_h.copy_(y, non_blocking=True)
-                a1.record(stream)
-            if i >= args.warmup:
-                e2e_ms.append((b, a0, a1))
-        torch.cuda.synchronize(dev)
-        e_tot = sum(a0.elapsed_time(a1) for (_, a0, a1) in e2e_ms)
-        if prefill:
-            e_val = flops_per_step * len(e2e_ms) / (e_tot * 1e-3) / 1e12
-        else:
-            e_val = sum(uniq[b] * per_expert for (b, _, _) in e2e_ms) / (e_tot * 1e-3) / 1e9
-        h2d = xs[0].numel() * 2 + (lgs[0].numel() * 4 if lgs else idss[0].numel() * 4 + wss[0].numel() * 4)
-        e2e = {"value": e_val, "unit": unit, "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(wl.T * wl.H * 4), "ms_per_step": e_tot / len(e2e_ms)}
+    x_h = [xx.cpu().pin_memory() for xx in xs]
+    l_h = [ll.cpu().pin_memory() for ll in lgs] if lgs else None
+    i_h = [ii.cpu().pin_memory() for ii in idss] if idss else None
+    w_h = [ww.cpu().pin_memory() for ww in wss] if wss else None
+    y_h = torch.empty(wl.T, wl.H, dtype=torch.float32).pin_memory()
+    x_d = torch.empty_like(xs[0])
+    l_d = torch.empty_like(lgs[0]) if lgs else None
+    i_d = torch.empty_like(idss[0]) if idss else None
+    w_d = torch.empty_like(wss[0]) if wss else None
+
+    def e2e_layer():
+        if lgs:
+            return layer.forward(x_d, logits=l_d, path=path, stream=stream)
+        return layer.forward(x_d, ids=i_d, w=w_d, path=path, stream=stream)
+    g_e2e = capture(e2e_layer)
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        b = i % nb
+        with torch.cuda.stream(stream):
+            flush.zero_()
+            a0 = torch.cuda.Event(enable_timing=True)
+            a1 = torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            x_d.copy_(x_h[b], non_blocking=True)
+            if lgs:
+                l_d.copy_(l_h[b], non_blocking=True)
+            else:
+                i_d.copy_(i_h[b], non_blocking=True)
+                w_d.copy_(w_h[b], non_blocking=True)
+            g_e2e.replay()
+            y_h.copy_(bufs["y"], non_blocking=True)
+            a1.record(stream)
+        if i >= args.warmup:
+            e2e_ms.append((b, a0, a1))
+    torch.cuda.synchronize(dev)
+    e_tot = sum(a0.elapsed_time(a1) for (_, a0, a1) in e2e_ms)
+    if prefill:
+        e_val = flops_per_step * len(e2e_ms) / (e_tot * 1e-3) / 1e12
+    else:
+        e_val = sum(uniq[b] * per_expert for (b, _, _) in e2e_ms) / (e_tot * 1e-3) / 1e9
+    h2d = xs[0].numel() * 2 + (lgs[0].numel() * 4 if lgs else idss[0].numel() * 4 + wss[0].numel() * 4)
+    e2e = {"value": e_val, "unit": unit, "h2d_bytes_per_step": int(h2d),
+           "d2h_bytes_per_step": int(wl.T * wl.H * 4), "ms_per_step": e_tot / len(e2e_ms)}
 
     if rank != 0:
         if world > 1:
@@ -417,7 +480,7 @@ def run_ours(args):
         else:
             cpu = {"error": info["error"][-200:]}
 
-    launches_per_step = 5 if not prefill else 7
+    launches_per_step = (5 if lgs else 4) if not prefill else (7 if lgs else 6)
     line = {
         "metric": metric_name(args.workload), "value": value, "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_ms / args.steps,
@@ -425,7 +488,8 @@ def run_ours(args):
         "dtype": "nvfp4 weights (e2m1 x ue4m3) * f16 activations, f32 accumulate" if not prefill
                  else "nvfp4 x nvfp4 block-scaled (e2m1, ue4m3), f32 accumulate",
         "data": "synthetic",
-        "config": {"workload": workload_desc(wl), "l2": "flushed (512 MiB write) before every step",
+        "config": {"workload": workload_desc(wl),
+                   "l2": "flushed before every step (512 MiB write, then 512 MiB read)",
                    "batches_rotated": nb, "unique_experts_mean": float(np.mean(uniq_steps)),
                    "path": "prefill" if prefill else "decode"},
         "roofline": roof,
@@ -433,8 +497,10 @@ def run_ours(args):
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
-        "breakdown_ms": {"route+csr": float(np.mean([e0.elapsed_time(e1) for (_, e0, e1, _, _) in evs])),
-                         "gate_up": float(np.mean(gu_ms)), "down+combine": float(np.mean(dn_ms))},
+        "breakdown_ms": {"route+csr": float(np.mean(pre_ms)), "gate_up": float(np.mean(gu_ms)),
+                         "down+combine": float(np.mean(dn_ms)),
+                         "note": "three graphs per step, L2 flushed before each step"},
+        "timing": "one CUDA graph per step (the whole layer), CUDA events around each replay",
         "wall_s": t_wall,
     }
     print(json.dumps(line))

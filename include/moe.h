@@ -110,7 +110,7 @@ typedef struct moe_ws_layout {
   size_t qh_scales;    /* prefill: u8 [P][F/16] */
   size_t qh_exp;       /* prefill: i32 [P] */
   size_t partial;      /* f32 [P][H] per-pair down projections z, rows in CSR order */
-  size_t tiles;        /* prefill: i32 [2 * max_tiles + 1] (expert, row start) M-tile list */
+  size_t tiles;        /* prefill: i32 count, pad to 16 B, then int4 {row0, rows, expert, 0} per M-tile */
 } moe_ws_layout;
 
 /* Limits (MOE_ERR_UNSUPPORTED beyond them): 1 <= k <= min(E, 32); E <= 1024;

@@ -79,7 +79,7 @@ bool compute_layout(int T, int H, int F, int E, int k, int path, moe_ws_layout* 
     L->qh_scales = take(P * (F / 16));
     L->qh_exp = take(P * sizeof(int32_t));
     const size_t max_tiles = P / 128 + (size_t)(E < (int)P ? E : (int)P) + 1;
-    L->tiles = take((2 * max_tiles + 1) * sizeof(int32_t));
+    L->tiles = take(16 + 16 * max_tiles);
   }
   L->total = o;
   return true;
@@ -126,7 +126,7 @@ moe_status moe_route_topk(const float* logits, int32_t T, int32_t E, int32_t k,
                           int32_t* topk_ids, float* topk_w, void* stream) {
   if (!logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
   if (T <= 0 || E <= 0 || k <= 0 || k > E) return MOE_ERR_INVALID_ARG;
-  if (k > kMaxK) return MOE_ERR_UNSUPPORTED;
+  if (k > kMaxK || E > kMaxE) return MOE_ERR_UNSUPPORTED;
   if ((long long)T * E >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
   return from_cuda(launch_route_topk(logits, T, E, k, topk_ids, topk_w,
                                      static_cast<cudaStream_t>(stream)));
@@ -169,7 +169,13 @@ moe_status moe_grouped_gate_up_silu_nvfp4(const void* x_bf16, int32_t T, int32_t
   if ((st = check_ws(ws, ws_bytes, L)) != MOE_OK) return st;
   const int p = resolve_path(T, k, path);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (p == MOE_PATH_PREFILL) return MOE_ERR_UNSUPPORTED;
+  if (p == MOE_PATH_PREFILL) {
+    bool unsup = false;
+    cudaError_t ce = launch_prefill_gate_up(static_cast<const uint16_t*>(x_bf16), T, H, F, k,
+                                            *w_gate_up, csr, L, static_cast<char*>(ws), s, &unsup);
+    if (unsup) return MOE_ERR_UNSUPPORTED;
+    return from_cuda(ce);
+  }
   return from_cuda(launch_decode_gate_up(static_cast<const uint16_t*>(x_bf16), T, H, F, k,
                                          *w_gate_up, csr, L, static_cast<char*>(ws), s));
 }
@@ -191,8 +197,14 @@ moe_status moe_grouped_down_combine_nvfp4(const moe_nvfp4_bank* w_down, moe_csr 
   const int p = resolve_path(T, k, path);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* w = static_cast<char*>(ws);
-  if (p == MOE_PATH_PREFILL) return MOE_ERR_UNSUPPORTED;
-  cudaError_t ce = launch_decode_down(*w_down, csr, T, H, F, k, L, w, s);
+  cudaError_t ce;
+  if (p == MOE_PATH_PREFILL) {
+    bool unsup = false;
+    ce = launch_prefill_down(*w_down, csr, T, H, F, k, L, w, s, &unsup);
+    if (unsup) return MOE_ERR_UNSUPPORTED;
+  } else {
+    ce = launch_decode_down(*w_down, csr, T, H, F, k, L, w, s);
+  }
   if (ce != cudaSuccess) return MOE_ERR_CUDA;
   return from_cuda(launch_combine(topk_w, T, H, k, L, w, y, s));
 }

@@ -106,7 +106,8 @@ decode_gate_up_kernel(const GateUpArgs args) {
   unsigned char* xs = smem;                                        // [8NT][xrow_bytes]
   int* slot_exp = reinterpret_cast<int*>(smem + 8 * NT * xrow_bytes);   // [8NT]
   uint32_t* slot_amax = reinterpret_cast<uint32_t*>(slot_exp + 8 * NT);  // [8NT]
-  float* red = reinterpret_cast<float*>(smem + 8 * NT * xrow_bytes + 16 * NT * sizeof(int));
+  int* slot_tok = reinterpret_cast<int*>(slot_amax + 8 * NT);             // [8NT]
+  float* red = reinterpret_cast<float*>(smem + 8 * NT * xrow_bytes + 24 * NT * sizeof(int));
 
   for (int tok0 = 0; tok0 < m; tok0 += 8 * NT) {
     // prefetch the first k-block of weights before staging the activations
@@ -121,25 +122,28 @@ decode_gate_up_kernel(const GateUpArgs args) {
       s3 = *reinterpret_cast<const uint16_t*>(su1 + kb_beg * 8);
     }
     __syncthreads();   // previous pass done with xs
-    // stage the pass's activation rows: raw bf16 first, with each row's amax
-    if (threadIdx.x < 8 * NT) slot_amax[threadIdx.x] = 0u;
+    // stage the pass's activation rows (only the live ones): raw bf16 first, with each
+    // row's amax; dead slots keep stale data, which only reaches discarded output columns
+    const int live = min(8 * NT, m - tok0);
+    if (threadIdx.x < 8 * NT) {
+      slot_amax[threadIdx.x] = 0u;
+      slot_tok[threadIdx.x] =
+          threadIdx.x < live ? args.pair_ids[off + tok0 + threadIdx.x] / args.k : 0;
+    }
     __syncthreads();
     const int nchunk = H / 8;
-    for (int idx = threadIdx.x; idx < 8 * NT * nchunk; idx += blockDim.x) {
+    for (int idx = threadIdx.x; idx < live * nchunk; idx += blockDim.x) {
       const int slot = idx / nchunk, ch = idx - slot * nchunk;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (tok0 + slot < m) {
-        const int t = args.pair_ids[off + tok0 + slot] / args.k;
-        v = *reinterpret_cast<const uint4*>(args.x + (size_t)t * H + ch * 8);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint32_t am = 0;
+      const uint4 v =
+          *reinterpret_cast<const uint4*>(args.x + (size_t)slot_tok[slot] * H + ch * 8);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t am = 0;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          am = max(am, (w[i] << 16) & 0x7fffffffu);
-          am = max(am, w[i] & 0x7fff0000u);
-        }
-        if (am) atomicMax(&slot_amax[slot], am);       // |x| as ordered integer bits
+      for (int i = 0; i < 4; ++i) {
+        am = max(am, (w[i] << 16) & 0x7fffffffu);
+        am = max(am, w[i] & 0x7fff0000u);
       }
+      if (am) atomicMax(&slot_amax[slot], am);         // |x| as ordered integer bits
       *reinterpret_cast<uint4*>(xs + slot * xrow_bytes + swz_chunk(ch)) = v;
     }
     __syncthreads();
@@ -147,9 +151,8 @@ decode_gate_up_kernel(const GateUpArgs args) {
       slot_exp[threadIdx.x] = f16_prescale_exp(__uint_as_float(slot_amax[threadIdx.x]));
     __syncthreads();
     // convert in place to f16 times 2^-exp (same thread, same chunk as above)
-    for (int idx = threadIdx.x; idx < 8 * NT * nchunk; idx += blockDim.x) {
+    for (int idx = threadIdx.x; idx < live * nchunk; idx += blockDim.x) {
       const int slot = idx / nchunk, ch = idx - slot * nchunk;
-      if (tok0 + slot >= m) continue;
       uint4* q = reinterpret_cast<uint4*>(xs + slot * xrow_bytes + swz_chunk(ch));
       const uint4 v = *q;
       const int ex = slot_exp[slot];
@@ -310,8 +313,9 @@ decode_down_kernel(const DownArgs args) {
   for (int tok0 = 0; tok0 < m; tok0 += 8 * NT) {
     __syncthreads();
     // stage h rows as f16 with a per-row power-of-two prescale (one warp per row)
-    for (int slot = warp; slot < 8 * NT; slot += WARPS) {
-      const bool live = tok0 + slot < m;
+    const int nlive = min(8 * NT, m - tok0);
+    for (int slot = warp; slot < nlive; slot += WARPS) {
+      const bool live = true;
       const float* hr = args.h + (size_t)(off + tok0 + slot) * F;
       float amax = 0.0f;
       if (live)
@@ -451,7 +455,7 @@ combine_kernel(const float* __restrict__ w, const int32_t* __restrict__ pair_pos
 template <int KS, int RB, int NT>
 cudaError_t run_gate_up(const GateUpArgs& a, int F, int max_active, cudaStream_t s) {
   const int H = a.H;
-  const size_t smem = (size_t)8 * NT * (H * 2 + 16) + 16 * NT * sizeof(int) +
+  const size_t smem = (size_t)8 * NT * (H * 2 + 16) + 24 * NT * sizeof(int) +
                       (KS > 1 ? (size_t)KS * RB * NT * 32 * 8 * sizeof(float) : 0);
   auto kern = decode_gate_up_kernel<KS, RB, NT>;
   cudaError_t st = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -1,0 +1,736 @@
+// Prefill path: hundreds of pairs per expert, a dense grouped contraction on the
+// block-scaled FP4 tensor cores (tcgen05.mma kind::mxf4nvf4, UE4M3 scale per 16).
+//
+//   tiles_kernel    128-row M-tiles (expert, first CSR row, rows) from the CSR offsets
+//   quant_x_kernel  Q(x): each token's bf16 row to NVFP4 with a power-of-two row scale,
+//                   written to every CSR row of the token's pairs
+//   gemm_kernel     persistent, warp-specialised grouped GEMM over (M-tile, N-tile) work:
+//                   TMA (SWIZZLE_128B) feeds FP4 code tiles, cp.async feeds the UE4M3
+//                   scale factors in the layout tcgen05.cp expects, one thread issues
+//                   tcgen05.cp + tcgen05.mma into TMEM, four warps drain TMEM with
+//                   tcgen05.ld and apply the epilogue (SiLU(g)*u -> h, or z -> partials)
+//   quant_h_kernel  Q(h) per CSR row
+//
+// The quantiser Q (the pages never quantise activations; block-scaled FP4 x FP4 needs it):
+// s = smallest integer with amax_row <= 6*448*2^s; block scale = the UE4M3 value nearest
+// to amax_16 / (6*2^s) (ties to the even encoding); code = the E2M1 value nearest to
+// v / (scale*2^s), saturating at 6, ties to even, sign bit iff v < 0.  Every decision is
+// an exact float32 comparison of |v|*2^-s against midpoint*scale products.
+//
+// Every wait on an mbarrier is bounded by a 2 s %globaltimer budget; on expiry the CTA
+// sets MOE_DEVERR_TIMEOUT in the workspace error word, drains and frees its TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+
+namespace {
+
+// ---------------------------------------------------------------------------
+// number formats (device side, written from the format definitions)
+// ---------------------------------------------------------------------------
+
+// Value of UE4M3 encoding b (0 <= b <= 0x7E).
+__device__ __forceinline__ float ue4m3_val(int b) {
+  const int e = b >> 3, m = b & 7;
+  if (e == 0) return (float)m * (1.0f / 512.0f);                    // m/8 * 2^-6
+  return __uint_as_float((uint32_t)(e + 120) << 23 | (uint32_t)m << 20);   // (1+m/8)*2^(e-7)
+}
+
+// Nearest UE4M3 encoding to key/6 (key = block amax * 2^-s <= 2688), ties to even.
+__device__ __forceinline__ int ue4m3_code_of(float key) {
+  // thresholds t(j) = 6 * (v(j) + v(j+1)) / 2 between encodings j and j+1, j = 0..125
+  int lo = 0, hi = 126;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    const float t = 3.0f * (ue4m3_val(mid) + ue4m3_val(mid + 1));
+    if (t < key) lo = mid + 1; else hi = mid;
+  }
+  if (lo < 126 && 3.0f * (ue4m3_val(lo) + ue4m3_val(lo + 1)) == key && ((lo + 1) & 1) == 0)
+    ++lo;
+  return lo;
+}
+
+// E2M1 magnitude code of key / sbv (key = |v| * 2^-s), nearest with ties to the even code.
+__device__ __forceinline__ uint32_t e2m1_mag(float key, float sbv) {
+  const float mids[7] = {0.25f, 0.75f, 1.25f, 1.75f, 2.5f, 3.5f, 5.0f};
+  uint32_t c = 0;
+#pragma unroll
+  for (int j = 0; j < 7; ++j) {
+    const float t = mids[j] * sbv;
+    c += (key > t) || ((j & 1) && key == t);
+  }
+  return c;
+}
+
+// Row exponent: smallest s with amax <= 2688 * 2^s (2688 = 0.65625 * 2^12).
+__device__ __forceinline__ int row_exp_of(float amax) {
+  if (!(amax > 0.0f)) return 0;
+  int ea;
+  const float m = frexpf(amax, &ea);
+  return ea - 12 + (m > 0.65625f ? 1 : 0);
+}
+
+// Quantise 16 values (already |v| * 2^-s in `key`, signs in `neg`) with block code sbc.
+__device__ __forceinline__ uint64_t quant_block(const float (&key)[16], uint32_t negmask, int sbc) {
+  if (sbc == 0) return 0ull;
+  const float sbv = ue4m3_val(sbc);
+  uint64_t out = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    uint64_t c = e2m1_mag(key[i], sbv) | (((negmask >> i) & 1u) << 3);
+    out |= c << (4 * i);
+  }
+  return out;
+}
+
+// ---------------------------------------------------------------------------
+// M-tile list
+// ---------------------------------------------------------------------------
+constexpr int kTileRows = 128;
+
+// tiles region: int n_mtiles, pad to 16 B, then int4 {row0, rows, expert, 0} per M-tile.
+__global__ void __launch_bounds__(1024) tiles_kernel(const int32_t* __restrict__ offsets, int E,
+                                                     int32_t* __restrict__ tiles) {
+  __shared__ int scratch[32];
+  const int e = threadIdx.x;
+  const int lane = e & 31, warp = e >> 5;
+  int cnt = 0, off = 0;
+  if (e < E) {
+    off = offsets[e];
+    cnt = (offsets[e + 1] - off + kTileRows - 1) / kTileRows;
+  }
+  int x = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int s = scratch[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    scratch[lane] = s;
+  }
+  __syncthreads();
+  const int base = (warp ? scratch[warp - 1] : 0) + x - cnt;
+  int4* list = reinterpret_cast<int4*>(tiles + 4);
+  if (e < E) {
+    const int m = offsets[e + 1] - off;
+    for (int i = 0; i < cnt; ++i) {
+      const int r = m - i * kTileRows;
+      list[base + i] = make_int4(off + i * kTileRows, r < kTileRows ? r : kTileRows, e, 0);
+    }
+  }
+  if (threadIdx.x == 0) tiles[0] = scratch[31];
+}
+
+// ---------------------------------------------------------------------------
+// Q(x): one warp per token, the result copied to each of the token's CSR rows
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) quant_x_kernel(const uint16_t* __restrict__ x, int T, int H,
+                                                      int k, const int32_t* __restrict__ pair_pos,
+                                                      uint8_t* __restrict__ qc,
+                                                      uint8_t* __restrict__ qs,
+                                                      int32_t* __restrict__ qe) {
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const uint16_t* row = x + (size_t)t * H;
+  const int nblk = H / 16;
+  float amax = 0.0f;
+  for (int b = lane; b < nblk; b += 32) {
+    const uint4* p = reinterpret_cast<const uint4*>(row + b * 16);
+    const uint4 v0 = p[0], v1 = p[1];
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      amax = fmaxf(amax, fabsf(__uint_as_float(w[i] << 16)));
+      amax = fmaxf(amax, fabsf(__uint_as_float(w[i] & 0xffff0000u)));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const int s = row_exp_of(amax);
+  int pos[kMaxK];
+  for (int j = 0; j < k; ++j) pos[j] = pair_pos[(size_t)t * k + j];
+  if (lane == 0)
+    for (int j = 0; j < k; ++j)
+      if (pos[j] >= 0) qe[pos[j]] = s;
+  for (int b = lane; b < nblk; b += 32) {
+    const uint4* p = reinterpret_cast<const uint4*>(row + b * 16);
+    const uint4 v0 = p[0], v1 = p[1];
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    float key[16];
+    uint32_t neg = 0;
+    float bmax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
+      key[2 * i] = ldexpf(fabsf(lo), -s);
+      key[2 * i + 1] = ldexpf(fabsf(hi), -s);
+      neg |= (lo < 0.0f ? 1u : 0u) << (2 * i);
+      neg |= (hi < 0.0f ? 1u : 0u) << (2 * i + 1);
+      bmax = fmaxf(bmax, fmaxf(key[2 * i], key[2 * i + 1]));
+    }
+    const int sbc = ue4m3_code_of(bmax);
+    const uint64_t codes = quant_block(key, neg, sbc);
+    for (int j = 0; j < k; ++j) {
+      if (pos[j] < 0) continue;
+      *reinterpret_cast<uint64_t*>(qc + (size_t)pos[j] * (H / 2) + b * 8) = codes;
+      qs[(size_t)pos[j] * nblk + b] = (uint8_t)sbc;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Q(h): one warp per CSR row
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) quant_h_kernel(const float* __restrict__ h, int P, int F,
+                                                      const int32_t* __restrict__ offsets, int E,
+                                                      uint8_t* __restrict__ qc,
+                                                      uint8_t* __restrict__ qs,
+                                                      int32_t* __restrict__ qe) {
+  const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= P || r >= offsets[E]) return;
+  const float* row = h + (size_t)r * F;
+  const int nblk = F / 16;
+  float amax = 0.0f;
+  for (int b = lane; b < nblk; b += 32) {
+    const float4* p = reinterpret_cast<const float4*>(row + b * 16);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 v = p[q];
+      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const int s = row_exp_of(amax);
+  if (lane == 0) qe[r] = s;
+  for (int b = lane; b < nblk; b += 32) {
+    const float4* p = reinterpret_cast<const float4*>(row + b * 16);
+    float key[16];
+    uint32_t neg = 0;
+    float bmax = 0.0f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 v = p[q];
+      const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        key[4 * q + i] = ldexpf(fabsf(vv[i]), -s);
+        neg |= (vv[i] < 0.0f ? 1u : 0u) << (4 * q + i);
+        bmax = fmaxf(bmax, key[4 * q + i]);
+      }
+    }
+    const int sbc = ue4m3_code_of(bmax);
+    *reinterpret_cast<uint64_t*>(qc + (size_t)r * (F / 2) + b * 8) = quant_block(key, neg, sbc);
+    qs[(size_t)r * nblk + b] = (uint8_t)sbc;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// PTX wrappers: mbarrier, TMA, cp.async, tcgen05
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+constexpr uint64_t kWaitBudgetNs = 2000000000ull;   // 2 s
+
+// Bounded wait; returns false (after flagging) on timeout or when another role aborted.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          uint32_t* err) {
+  if (mbar_try(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try(bar, parity)) return true;
+    if ((it & 255) == 0) {
+      if (*abort_flag) return false;
+      if (global_ns() - t0 > kWaitBudgetNs) {
+        *abort_flag = 1;
+        atomicOr(err, (uint32_t)MOE_DEVERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(smem_u32(dst)), "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void cp_async4(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;"
+               ::"r"(smem_u32(dst)), "l"(src), "r"(valid ? 4 : 0) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05): start >> 4, LBO >> 4, SBO >> 4, version 1,
+// swizzle mode in bits 61..63 (0 none, 2 = 128-byte).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo,
+                                              uint32_t swz) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr & 0x3FFFF) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)(swz & 7) << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::mxf4nvf4: A/B E2M1 (1), K-major, N>>3 at 17, UE4M3 scales
+// (bit 23 = 0), M>>4 at 24, scale-factor ids 0, dense K = 64.
+__host__ __device__ constexpr uint32_t mxf4_idesc(int M, int N) {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+      ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+      ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ---------------------------------------------------------------------------
+// grouped block-scaled GEMM
+// ---------------------------------------------------------------------------
+// GATE_UP: A = Q(x) rows [P][H], B = gate rows and up rows of the expert, out h f32 [P][F].
+// DOWN:    A = Q(h) rows [P][F], B = down rows [H][F] of the expert, out partial f32 [P][H].
+struct GemmArgs {
+  const uint8_t* a_scales;      // [P][K/16]
+  const int32_t* a_exp;         // [P]
+  const uint8_t* b_scales;      // [E][rows][K/16]
+  const int32_t* tiles;         // n_mtiles, then int4 list
+  float* out;                   // [P][out_cols]
+  uint32_t* err;
+  int P, K, rows_per_expert, n_tiles_n, out_cols, F;
+};
+
+template <int BN, bool GATE_UP>
+struct Cfg {
+  static constexpr int BM = 128;
+  static constexpr int KB = 128;                    // bytes of K per stage (256 elements)
+  static constexpr int NB = GATE_UP ? 2 : 1;        // B tiles per stage
+  static constexpr int G = (BN + 127) / 128;        // 128-row scale-factor atoms per B tile
+  static constexpr int STAGES = 3;
+  static constexpr int A_BYTES = BM * KB;
+  static constexpr int B_BYTES = BN * KB;
+  static constexpr int SFA_BYTES = 4 * 512;         // 4 k-steps x one atom
+  static constexpr int SFB_BYTES = 4 * G * 512;
+  static constexpr int STAGE_BYTES = A_BYTES + NB * B_BYTES + SFA_BYTES + NB * SFB_BYTES;
+  static constexpr int ACC_COLS = NB * BN;
+  static constexpr int SF_COLS = 16 + NB * 16 * G;  // one stage's scale factors in TMEM
+  // one scale-factor buffer per smem stage: a buffer is rewritten only after the stage's
+  // empty barrier (committed behind the MMAs that read it) has completed
+  static constexpr int TMEM_COLS_USED = ACC_COLS + STAGES * SF_COLS;
+  static constexpr int TMEM_COLS = TMEM_COLS_USED <= 256 ? 256 : 512;
+  static constexpr int THREADS = 320;               // 10 warps
+  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+  static constexpr uint32_t TX_BYTES = A_BYTES + NB * B_BYTES;
+  static_assert(TMEM_COLS_USED <= 512, "TMEM budget");
+};
+
+template <int BN, bool GATE_UP>
+__global__ void __launch_bounds__(320, 1)
+gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+            const GemmArgs args) {
+  using C = Cfg<BN, GATE_UP>;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* acc_full = empty + C::STAGES;
+  uint64_t* acc_empty = acc_full + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_mtiles = args.tiles[0];
+  const int4* tlist = reinterpret_cast<const int4*>(args.tiles + 4);
+  const int n_work = n_mtiles * args.n_tiles_n;
+  const int k_stages = (args.K / 2 + C::KB - 1) / C::KB;
+  const int sfrow = args.K / 16;                    // scale bytes per row
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1 + 128);                  // TMA expect_tx + 128 scale threads
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 4);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(smem_u32(tmem_holder)), "n"(C::TMEM_COLS) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const uint32_t acc_col = tmem;                              // accumulators at column 0
+  const uint32_t sf_col0 = tmem + C::ACC_COLS;                 // per-stage scale-factor buffers
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      int it = 0;
+      for (int w = blockIdx.x; w < n_work && !*abort_flag; w += gridDim.x) {
+        const int4 tile = tlist[w / args.n_tiles_n];
+        const int n0 = (w % args.n_tiles_n) * BN;
+        const int brow = tile.z * args.rows_per_expert + n0;
+        for (int ks = 0; ks < k_stages; ++ks, ++it) {
+          const int st = it % C::STAGES;
+          if (!mbar_wait(&empty[st], ((it / C::STAGES) & 1) ^ 1, abort_flag, args.err)) break;
+          unsigned char* sb = smem + st * C::STAGE_BYTES;
+          mbar_expect_tx(&full[st], C::TX_BYTES);
+          tma_load_2d(sb, &tmap_a, ks * C::KB, tile.x, &full[st]);
+          tma_load_2d(sb + C::A_BYTES, &tmap_b, ks * C::KB, brow, &full[st]);
+          if (GATE_UP)
+            tma_load_2d(sb + C::A_BYTES + C::B_BYTES, &tmap_b, ks * C::KB, brow + args.F,
+                        &full[st]);
+        }
+      }
+      // drain: wait (bounded) until every issued stage has landed
+      if (*abort_flag) {
+        for (int s = 0; s < C::STAGES; ++s) {
+          if (it <= s) continue;
+          const int last = s + ((it - 1 - s) / C::STAGES) * C::STAGES;   // last issue on s
+          const uint64_t t0 = global_ns();
+          while (!mbar_try(&full[s], (last / C::STAGES) & 1) &&
+                 global_ns() - t0 < 100000000ull) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = mxf4_idesc(128, BN);
+      int it = 0, tcount = 0;
+      for (int w = blockIdx.x; w < n_work && !*abort_flag; w += gridDim.x, ++tcount) {
+        if (!mbar_wait(acc_empty, (tcount & 1) ^ 1, abort_flag, args.err)) break;
+        tc_fence_after();
+        bool ok = true;
+        for (int ks = 0; ks < k_stages; ++ks, ++it) {
+          const int st = it % C::STAGES;
+          if (!mbar_wait(&full[st], (it / C::STAGES) & 1, abort_flag, args.err)) { ok = false; break; }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          tc_fence_after();
+          unsigned char* sb = smem + st * C::STAGE_BYTES;
+          const uint32_t a_addr = smem_u32(sb);
+          const uint32_t sfa_smem = smem_u32(sb + C::A_BYTES + C::NB * C::B_BYTES);
+          const uint32_t sfb_smem = sfa_smem + C::SFA_BYTES;
+          const uint32_t sfc = sf_col0 + st * C::SF_COLS;
+          // scale factors: smem atoms -> TMEM (4 columns per 128-row atom)
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            tc_cp_sf(sfc + 4 * j, smem_desc(sfa_smem + j * 512, 0, 128, 0));
+#pragma unroll
+          for (int b = 0; b < C::NB; ++b)
+#pragma unroll
+            for (int q = 0; q < 4 * C::G; ++q)
+              tc_cp_sf(sfc + 16 + b * 16 * C::G + 4 * q,
+                       smem_desc(sfb_smem + b * C::SFB_BYTES + q * 512, 0, 128, 0));
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint64_t adesc = smem_desc(a_addr + 32 * j, 16, 1024, 2);
+#pragma unroll
+            for (int b = 0; b < C::NB; ++b) {
+              const uint32_t b_addr = smem_u32(sb + C::A_BYTES + b * C::B_BYTES);
+              const uint64_t bdesc = smem_desc(b_addr + 32 * j, 16, 1024, 2);
+              tc_mma(acc_col + b * BN, adesc, bdesc, idesc, sfc + 4 * j,
+                     sfc + 16 + b * 16 * C::G + 4 * C::G * j, (ks | j) != 0);
+            }
+          }
+          tc_commit(&empty[st]);
+        }
+        if (!ok) break;
+        tc_commit(acc_full);
+      }
+    }
+  } else if (warp < 6) {
+    // ---------------- scale-factor loaders (128 threads) ----------------
+    const int t = threadIdx.x - 64;
+    int it = 0;
+    for (int w = blockIdx.x; w < n_work && !*abort_flag; w += gridDim.x) {
+      const int4 tile = tlist[w / args.n_tiles_n];
+      const int n0 = (w % args.n_tiles_n) * BN;
+      const int brow0 = tile.z * args.rows_per_expert + n0;
+      bool ok = true;
+      for (int ks = 0; ks < k_stages; ++ks, ++it) {
+        const int st = it % C::STAGES;
+        if (!mbar_wait(&empty[st], ((it / C::STAGES) & 1) ^ 1, abort_flag, args.err)) {
+          ok = false;
+          break;
+        }
+        unsigned char* sfa = smem + st * C::STAGE_BYTES + C::A_BYTES + C::NB * C::B_BYTES;
+        unsigned char* sfb = sfa + C::SFA_BYTES;
+        {
+          const int m = t;                       // A row of the tile
+          const bool rv = m < tile.y;
+          const uint8_t* src = args.a_scales + (size_t)(rv ? tile.x + m : 0) * sfrow;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int byte = 16 * ks + 4 * j;
+            const bool v = rv && byte < sfrow;
+            cp_async4(sfa + j * 512 + 16 * (m & 31) + 4 * (m >> 5), src + (v ? byte : 0), v);
+          }
+        }
+#pragma unroll
+        for (int b = 0; b < C::NB; ++b) {
+          for (int n = t; n < BN; n += 128) {
+            const uint8_t* src = args.b_scales +
+                                 (size_t)(brow0 + (b ? args.F : 0) + n) * sfrow;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int byte = 16 * ks + 4 * j;
+              const bool v = byte < sfrow;
+              cp_async4(sfb + b * C::SFB_BYTES + (j * C::G + (n >> 7)) * 512 + 16 * (n & 31) +
+                            4 * ((n & 127) >> 5),
+                        src + (v ? byte : 0), v);
+            }
+          }
+        }
+        cp_async_arrive(&full[st]);
+      }
+      if (!ok) break;
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+  } else {
+    // ---------------- epilogue (warps 6..9 -> TMEM lane quarters 2,3,0,1) ----------------
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    int tcount = 0;
+    for (int w = blockIdx.x; w < n_work && !*abort_flag; w += gridDim.x, ++tcount) {
+      const int4 tile = tlist[w / args.n_tiles_n];
+      const int n0 = (w % args.n_tiles_n) * BN;
+      if (!mbar_wait(acc_full, tcount & 1, abort_flag, args.err)) break;
+      tc_fence_after();
+      const bool valid = row < tile.y;
+      const int pos = tile.x + row;
+      const int sx = valid ? args.a_exp[pos] : 0;
+      const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+      float* orow = args.out + (size_t)(valid ? pos : 0) * args.out_cols + n0;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        float v[32];
+        tc_ld32(acc_col + lane_base + c * 32, v);
+        if (GATE_UP) {
+          float u[32];
+          tc_ld32(acc_col + lane_base + BN + c * 32, u);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = silu_f(ldexpf(v[i], sx)) * ldexpf(u[i], sx);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = ldexpf(v[i], sx);
+        }
+        if (valid) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(orow + c * 32 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "n"(C::TMEM_COLS) : "memory");
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host helpers
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2D u8 tensor map over [rows][row_bytes], box {128 bytes, box_rows}, 128-byte swizzle.
+bool make_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows,
+              uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {row_bytes, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
+template <int BN, bool GATE_UP>
+cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& a,
+                     int max_tiles, cudaStream_t s) {
+  using C = Cfg<BN, GATE_UP>;
+  auto kern = gemm_kernel<BN, GATE_UP>;
+  cudaError_t st = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (st != cudaSuccess) return st;
+  int grid = max_tiles * a.n_tiles_n;
+  if (grid > num_sms()) grid = num_sms();
+  if (grid < 1) grid = 1;
+  kern<<<grid, C::THREADS, C::SMEM, s>>>(ma, mb, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_gate_up(const uint16_t* x_bf16, int T, int H, int F, int k,
+                                   const moe_nvfp4_bank& b, moe_csr csr, const moe_ws_layout& L,
+                                   char* ws, cudaStream_t s, bool* unsupported) {
+  *unsupported = false;
+  if (H % 256 != 0 || (F % 128 != 0 && F != 64)) { *unsupported = true; return cudaSuccess; }
+  const int P = T * k;
+  int32_t* tiles = reinterpret_cast<int32_t*>(ws + L.tiles);
+  tiles_kernel<<<1, 1024, 0, s>>>(csr.expert_offsets, b.E, tiles);
+  cudaError_t st = cudaGetLastError();
+  if (st != cudaSuccess) return st;
+  uint8_t* qc = reinterpret_cast<uint8_t*>(ws + L.qx_codes);
+  uint8_t* qs = reinterpret_cast<uint8_t*>(ws + L.qx_scales);
+  int32_t* qe = reinterpret_cast<int32_t*>(ws + L.qx_exp);
+  quant_x_kernel<<<(T + 7) / 8, 256, 0, s>>>(x_bf16, T, H, k,
+                                              reinterpret_cast<const int32_t*>(ws + L.pair_pos),
+                                              qc, qs, qe);
+  if ((st = cudaGetLastError()) != cudaSuccess) return st;
+  CUtensorMap ma, mb;
+  const int BN = (F % 128 == 0) ? 128 : 64;
+  if (!make_map(&ma, qc, H / 2, P, 128)) return cudaErrorInvalidValue;
+  if (!make_map(&mb, b.codes, H / 2, (uint64_t)b.E * 2 * F, BN)) return cudaErrorInvalidValue;
+  GemmArgs a{qs, qe, b.scales, tiles, reinterpret_cast<float*>(ws + L.h),
+             reinterpret_cast<uint32_t*>(ws + L.error_word), P, H, 2 * F, F / BN, F, F};
+  const int max_tiles = P / 128 + (P < b.E ? P : b.E) + 1;
+  if (BN == 128) return run_gemm<128, true>(ma, mb, a, max_tiles, s);
+  return run_gemm<64, true>(ma, mb, a, max_tiles, s);
+}
+
+cudaError_t launch_prefill_down(const moe_nvfp4_bank& b, moe_csr csr, int T, int H, int F, int k,
+                                const moe_ws_layout& L, char* ws, cudaStream_t s,
+                                bool* unsupported) {
+  *unsupported = false;
+  if (H % 256 != 0 || F % 64 != 0) { *unsupported = true; return cudaSuccess; }
+  const int P = T * k;
+  uint8_t* qc = reinterpret_cast<uint8_t*>(ws + L.qh_codes);
+  uint8_t* qs = reinterpret_cast<uint8_t*>(ws + L.qh_scales);
+  int32_t* qe = reinterpret_cast<int32_t*>(ws + L.qh_exp);
+  quant_h_kernel<<<(P + 7) / 8, 256, 0, s>>>(reinterpret_cast<const float*>(ws + L.h), P, F,
+                                              csr.expert_offsets, b.E, qc, qs, qe);
+  cudaError_t st = cudaGetLastError();
+  if (st != cudaSuccess) return st;
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, qc, F / 2, P, 128)) return cudaErrorInvalidValue;
+  if (!make_map(&mb, b.codes, F / 2, (uint64_t)b.E * H, 256)) return cudaErrorInvalidValue;
+  GemmArgs a{qs, qe, b.scales, reinterpret_cast<const int32_t*>(ws + L.tiles),
+             reinterpret_cast<float*>(ws + L.partial),
+             reinterpret_cast<uint32_t*>(ws + L.error_word), P, F, H, H / 256, H, F};
+  const int max_tiles = P / 128 + (P < b.E ? P : b.E) + 1;
+  return run_gemm<256, false>(ma, mb, a, max_tiles, s);
+}
+
+}  // namespace moe

@@ -21,6 +21,8 @@ __device__ __forceinline__ bool before(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
 }
 
+constexpr int kRouteMaxPerLane = kMaxE / 32;
+
 __global__ void route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
                                   int32_t* __restrict__ ids, float* __restrict__ w) {
   const int warps = blockDim.x / 32;
@@ -28,34 +30,43 @@ __global__ void route_topk_kernel(const float* __restrict__ logits, int T, int E
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
   const float* row = logits + (size_t)t * E;
+  // the token's logits, once, in registers: lane holds experts lane, lane+32, ...
+  float v[kRouteMaxPerLane];
+#pragma unroll
+  for (int i = 0; i < kRouteMaxPerLane; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = e < E ? __ldg(row + e) : -INFINITY;
+  }
   float prev_v = 0.0f;
   int prev_i = -1;
-  float sel_v = 0.0f, first_v = 0.0f, denom = 0.0f;
+  float first_v = 0.0f;
   float my_val = 0.0f;   // lane j < k keeps the j-th selected logit
   int my_id = 0;
   for (int r = 0; r < k; ++r) {
     float bv = -INFINITY;
     int bi = 0x7fffffff;
-    for (int e = lane; e < E; e += 32) {
-      float v = row[e];
-      bool eligible = (prev_i < 0) || before(prev_v, prev_i, v, e);
-      if (eligible && (bi == 0x7fffffff || before(v, e, bv, bi))) { bv = v; bi = e; }
+#pragma unroll
+    for (int i = 0; i < kRouteMaxPerLane; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) {
+        const bool eligible = (prev_i < 0) || before(prev_v, prev_i, v[i], e);
+        if (eligible && (bi == 0x7fffffff || before(v[i], e, bv, bi))) { bv = v[i]; bi = e; }
+      }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-      float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
       if (oi != 0x7fffffff && (bi == 0x7fffffff || before(ov, oi, bv, bi))) { bv = ov; bi = oi; }
     }
     prev_v = bv;
     prev_i = bi;
     if (r == 0) first_v = bv;
     if (lane == r) { my_val = bv; my_id = bi; }
-    sel_v = bv;
   }
-  (void)sel_v;
-  float ex = (lane < k) ? expf(my_val - first_v) : 0.0f;
+  const float ex = (lane < k) ? expf(my_val - first_v) : 0.0f;
   // sum in ascending j so every lane sees the same value
+  float denom = 0.0f;
   for (int j = 0; j < k; ++j) denom += __shfl_sync(0xffffffffu, ex, j);
   if (lane < k) {
     ids[(size_t)t * k + lane] = my_id;

@@ -25,6 +25,12 @@ class DeviceRun:
     y: np.ndarray
     err: int
     ws: dict
+    ws_raw: Optional[np.ndarray] = None     # host copy of the whole workspace
+    layer: Optional[object] = None
+
+    def region(self, name, nbytes, dtype, shape):
+        off = self.ws[name]
+        return self.ws_raw[off:off + nbytes].view(dtype).reshape(shape)
 
 
 def device_banks(wl, device="cuda"):
@@ -73,6 +79,8 @@ def run_layer(wl, path=moe.PATH_DECODE, banks=None, ids=None, w=None, fetch=True
         y=y.cpu().numpy().copy(),
         err=err,
         ws=L,
+        ws_raw=ws.cpu().numpy(),
+        layer=layer,
     )
     return out
 

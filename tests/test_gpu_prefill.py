@@ -1,0 +1,168 @@
+"""GPU parity of the prefill path (Q(x) -> tcgen05 block-scaled gate/up -> Q(h) ->
+tcgen05 down -> combine) against the CPU oracle, stage by stage, through the C ABI.
+
+Stages: (i) Q(x) is bit-exact; (ii) h is within the accumulation tolerance of the
+oracle's h from the same Q(x) and within the quantisation band the oracle assumes;
+(iii) Q(h) is bit-exact wherever the oracle's decision is not within that band;
+(iv) the down projection and combine, fed the oracle's own h, match the oracle within
+2e-3 * sum|w * terms| + 1e-5 and reproduce Q(h) bit-exactly; (v) end to end, y is within
+that tolerance plus the allowance of the flagged Q(h) decisions.
+"""
+import hashlib
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+import oracle
+from oracle import nvfp4
+import nvfp4_grouped_gemm_gb300 as moe
+from gpu_util import run_layer, h_tolerance, assert_within, device_banks
+
+pytestmark = pytest.mark.gpu
+PF = moe.PATH_PREFILL
+
+
+def _unpack(packed):
+    out = np.empty(packed.shape[:-1] + (packed.shape[-1] * 2,), np.uint8)
+    out[..., 0::2] = packed & 0xF
+    out[..., 1::2] = packed >> 4
+    return out
+
+
+def _routing(wl):
+    if wl.logits is not None:
+        return oracle.route_topk(wl.logits, wl.k)
+    return wl.ids, wl.weights.astype(np.float64)
+
+
+def _stages(wl, run, tokens):
+    ids, w = _routing(wl)
+    P, H, F, k = wl.P, wl.H, wl.F, wl.k
+    toks = np.asarray(tokens)
+    pairs = (toks[:, None] * k + np.arange(k)).reshape(-1)
+    pairs = pairs[run.pair_pos[pairs] >= 0]
+    pos = run.pair_pos[pairs]
+    # (i) Q(x), bit-exact, for every token (cheap) at its CSR rows
+    x = nvfp4.bf16_to_f64(wl.x_bits)
+    cx, sx, ex = nvfp4.quantize(x)
+    g_c = run.region("qx_codes", P * H // 2, np.uint8, (P, H // 2))
+    g_s = run.region("qx_scales", P * H // 16, np.uint8, (P, H // 16))
+    g_e = run.region("qx_exp", P * 4, np.int32, (P,))
+    allp = np.nonzero(run.pair_pos >= 0)[0]
+    allpos = run.pair_pos[allp]
+    assert np.array_equal(g_c[allpos], cx[allp // k]), "Q(x) codes"
+    assert np.array_equal(g_s[allpos], sx[allp // k]), "Q(x) scales"
+    assert np.array_equal(g_e[allpos], ex[allp // k]), "Q(x) row exponents"
+    # oracle in prefill mode on the sampled tokens
+    res = oracle.ffn(wl.x_bits, ids, w, wl.gate_up, wl.down, mode="prefill", tokens=toks)
+    # (ii) h
+    h_gpu = run.region("h", P * F * 4, np.float32, (P, F))[pos].astype(np.float64)
+    assert_within(h_gpu, res.h[pairs], h_tolerance(res)[pairs], "h")
+    amb = oracle.qh_ambiguity(res, pairs)
+    ratio = np.abs(h_gpu - res.h[pairs]) / amb.band[pairs]
+    band_ratio = float(np.max(ratio))
+    gscale = res.g_abs[pairs]
+    print(f"h error / band: max {band_ratio:.3g} p99 {np.percentile(ratio, 99):.3g} "
+          f"median {np.median(ratio):.3g}; |h_gpu-h|/|h| max "
+          f"{np.max(np.abs(h_gpu - res.h[pairs]) / (np.abs(res.h[pairs]) + 1e-30)):.3g}")
+    assert band_ratio <= 1.0, f"h error exceeds the quantisation band by {band_ratio:.3g}x"
+    # (iii) Q(h) where the decision is not ambiguous
+    q_c = _unpack(run.region("qh_codes", P * F // 2, np.uint8, (P, F // 2))[pos])
+    q_s = run.region("qh_scales", P * F // 16, np.uint8, (P, F // 16))[pos]
+    q_e = run.region("qh_exp", P * 4, np.int32, (P,))[pos]
+    r_c = _unpack(res.qh[0][pairs])
+    flagged = amb.flagged[pairs]
+    assert np.array_equal(q_c[~flagged], r_c[~flagged]), "Q(h) codes outside the band"
+    blk_flag = flagged.reshape(len(pairs), F // 16, 16).any(axis=2)
+    assert np.array_equal(q_s[~blk_flag], res.qh[1][pairs][~blk_flag]), "Q(h) block scales"
+    row_flag = flagged.all(axis=1)
+    assert np.array_equal(q_e[~row_flag], res.qh[2][pairs][~row_flag]), "Q(h) row exponents"
+    # (v) end to end
+    extra = oracle.prefill_allowance(res, amb, wl.down, ids, w, toks)
+    worst = assert_within(run.y[toks], res.y[toks], oracle.tolerance(res.tsum, extra)[toks], "y")
+    return res, {"flagged_frac": float(flagged.mean()), "band_ratio": float(band_ratio),
+                 "y_worst": worst}
+
+
+def _down_from_oracle_h(wl, run, res, tokens):
+    """(iv): overwrite the workspace's h with the oracle's h, rerun down+combine."""
+    layer = run.layer
+    b = layer.buffers(wl.T, PF)
+    ws = b["ws"]
+    P, F, H, k = wl.P, wl.F, wl.H, wl.k
+    toks = np.asarray(tokens)
+    pairs = (toks[:, None] * k + np.arange(k)).reshape(-1)
+    pairs = pairs[run.pair_pos[pairs] >= 0]
+    pos = run.pair_pos[pairs]
+    h_all = run.region("h", P * F * 4, np.float32, (P, F)).copy()
+    h_all[pos] = res.h[pairs].astype(np.float32)
+    off = run.ws["h"]
+    ws[off:off + P * F * 4].copy_(torch.from_numpy(h_all.view(np.uint8).reshape(-1)).cuda())
+    ids, w = _routing(wl)
+    w_t = torch.from_numpy(np.ascontiguousarray(w, dtype=np.float32)).cuda()
+    y = torch.zeros(wl.T, H, dtype=torch.float32, device="cuda")
+    moe.moe_grouped_down_combine_nvfp4(layer.down, b["csr"], w_t, wl.T, H, F, k, y, ws, PF)
+    torch.cuda.synchronize()
+    wsn = ws.cpu().numpy()
+    L = run.ws
+    q_c = wsn[L["qh_codes"]:L["qh_codes"] + P * F // 2].reshape(P, F // 2)[pos]
+    q_s = wsn[L["qh_scales"]:L["qh_scales"] + P * F // 16].reshape(P, F // 16)[pos]
+    assert np.array_equal(q_c, res.qh[0][pairs]), "Q(oracle h) codes"
+    assert np.array_equal(q_s, res.qh[1][pairs]), "Q(oracle h) scales"
+    yy = y.cpu().numpy()
+    return assert_within(yy[toks], res.y[toks], oracle.tolerance(res.tsum)[toks], "y from oracle h")
+
+
+def test_tiny_prefill():
+    wl = synth.tiny()
+    run = run_layer(wl, path=PF)
+    assert run.err == 0
+    res, info = _stages(wl, run, np.arange(wl.T))
+    _down_from_oracle_h(wl, run, res, np.arange(wl.T))
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_prefill_small(seed):
+    wl = synth.prefill(seed=seed, T=256)
+    run = run_layer(wl, path=PF)
+    assert run.err == 0
+    from test_gpu_decode import _check_csr
+    _check_csr(run, wl.ids, wl.E)
+    toks = np.arange(0, 256, 37)
+    res, info = _stages(wl, run, toks)
+    _down_from_oracle_h(wl, run, res, toks)
+
+
+def test_prefill_full_size_sampled():
+    """The prefill workload at full size (4096 tokens, 32768 pairs, 288 experts)."""
+    wl = synth.prefill()
+    run = run_layer(wl, path=PF)
+    assert run.err == 0
+    from test_gpu_decode import _check_csr
+    _check_csr(run, wl.ids, wl.E)
+    toks = np.array([0, 1, 777, 2048, 4095])
+    res, info = _stages(wl, run, toks)
+    _down_from_oracle_h(wl, run, res, toks)
+
+
+def test_prefill_replays_bit_identical():
+    wl = synth.prefill(T=512)
+    gu, dn = device_banks(wl)
+    layer = moe.MoeLayer(gu, dn, wl.k)
+    x = torch.from_numpy(wl.x_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    ids = torch.from_numpy(wl.ids).cuda()
+    w = torch.from_numpy(wl.weights).cuda()
+    hashes = set()
+    for _ in range(5):
+        y = layer.forward(x, ids=ids, w=w, path=PF)
+        torch.cuda.synchronize()
+        hashes.add(hashlib.sha256(y.cpu().numpy().tobytes()).hexdigest())
+    assert len(hashes) == 1
+
+
+def test_auto_path_switch():
+    th = moe.prefill_min_pairs()
+    assert moe.resolve_path(th // 8, 8) == moe.PATH_PREFILL
+    assert moe.resolve_path(th // 8 - 1, 8) == moe.PATH_DECODE
