@@ -289,7 +289,7 @@ def run_ours(args):
         @staticmethod
         def zero_():
             flush_w.zero_()
-            torch.sum(flush_r, out=flush_out)
+            torch.sum(flush_r, dim=0, out=flush_out)
     flush = _Flush
     bufs = layer.buffers(wl.T, path)
 

@@ -261,8 +261,11 @@ def qh_ambiguity(res: FFNResult, pairs: np.ndarray, beta: float = H_BAND) -> QAm
     """Flag the elements of Q(h) whose code could differ for an h within the band.
 
     The band for h_i is eps_i = beta * (|silu'(g)| |u| G_abs + |silu(g)| U_abs)
-    + 2^-22 |h_i|, G_abs/U_abs being the sums of absolute products of the gate and
-    up dot products.  An element is flagged if its row exponent, its block scale
+    + 2^-22 |h_i| + 2^-26 amax_row, G_abs/U_abs being the sums of absolute products of
+    the gate and up dot products.  The last term covers values far below every
+    decision of their row: a float32 SiLU underflows to 0 for g below about -88, where
+    the float64 value is ~1e-38; no threshold of Q lies below 2^-22 amax_row except the
+    zero-scale one near 2^-19 amax_row, so the floor cannot hide a decision.  An element is flagged if its row exponent, its block scale
     or its own code changes between the two ends of the band.  A flagged
     element's dequantised value then moves by at most
     |deq' - h'| + |h' - h| + |h - deq| <= 1.375 unit' + eps + 1.375 unit, a
@@ -275,6 +278,7 @@ def qh_ambiguity(res: FFNResult, pairs: np.ndarray, beta: float = H_BAND) -> QAm
     g, u = res.g, res.u
     eps = beta * (np.abs(_silu_prime(g)) * np.abs(u) * res.g_abs + np.abs(silu(g)) * res.u_abs)
     eps = eps + 2.0 ** -22 * np.abs(res.h)
+    eps = eps + 2.0 ** -26 * np.abs(res.h).max(axis=1, keepdims=True)
     flagged = np.zeros((P, F), dtype=bool)
     delta = np.zeros((P, F))
     mids6 = nvfp4._UE4M3_MID6
