@@ -164,6 +164,26 @@ moe_status moe_grouped_down_combine_nvfp4(const moe_nvfp4_bank* w_down, moe_csr 
                                           int32_t k, int32_t path, float* y, void* ws,
                                           size_t ws_bytes, void* stream);
 
+/* moe_build_expert_csr without a workspace, for callers that cannot allocate device
+ * memory: a plugin or engine that owns every device allocation and hands kernels only its
+ * own tensors, code issuing work inside a CUDA stream capture that must not call
+ * cudaMalloc (which may also synchronise the device), or latency-critical loops where an
+ * allocation's implicit synchronisation is unacceptable. The paper the method comes from
+ * has no counterpart to this entry point; it is an addition of this library.
+ *
+ * Same inputs and CSR outputs as moe_build_expert_csr (bit-identical results). Its scratch
+ * (the per-pair CSR positions) lives in a fixed device array inside the library, 256 KiB
+ * per GPU that loads the library, held until the process exits; nothing is allocated or
+ * freed. Limits: T * k <= 65536 (else MOE_ERR_UNSUPPORTED), plus the limits above.
+ * The first call on each device looks up the array's device address (once per device, on
+ * the current device); make that first call before any stream capture. All calls share
+ * the one array: calls that can overlap on the GPU (different streams, or different host
+ * threads, on the same device) race, so serialise them. Invalid expert ids are left out
+ * as in moe_build_expert_csr, but no error word is reported: expert_offsets[E] < T*k
+ * tells the caller that some were dropped. */
+moe_status moe_build_expert_csr_static(const int32_t* topk_ids, int32_t T, int32_t k, int32_t E,
+                                       moe_csr csr, void* stream);
+
 /* Human-readable name of a status (static string, never NULL). */
 const char* moe_status_string(moe_status status);
 

@@ -16,6 +16,7 @@ from ._native import PATH_AUTO, PATH_DECODE, PATH_PREFILL, DEVERR_EXPERT_ID, DEV
 
 __all__ = ["MoeError", "NvFp4Bank", "ExpertCSR", "workspace_bytes", "workspace_layout",
            "resolve_path", "prefill_min_pairs", "moe_route_topk", "moe_build_expert_csr",
+           "moe_build_expert_csr_static",
            "moe_grouped_gate_up_silu_nvfp4", "moe_grouped_down_combine_nvfp4",
            "get_device_error", "MoeLayer", "PATH_AUTO", "PATH_DECODE", "PATH_PREFILL"]
 
@@ -108,6 +109,16 @@ def moe_build_expert_csr(topk_ids: torch.Tensor, E: int, csr: ExpertCSR, ws: tor
     _check(_native.load().moe_build_expert_csr(_ptr(topk_ids), T, k, E, csr._c, _ptr(ws),
                                                ws.numel() * ws.element_size(), _stream(stream)),
            "moe_build_expert_csr")
+
+
+def moe_build_expert_csr_static(topk_ids: torch.Tensor, E: int, csr: ExpertCSR,
+                                stream=None) -> None:
+    """The CSR without a workspace (scratch in a fixed device array inside the library);
+    for callers that cannot allocate device memory. T*k <= 65536."""
+    T, k = topk_ids.shape
+    _check(_native.load().moe_build_expert_csr_static(_ptr(topk_ids), T, k, E, csr._c,
+                                                      _stream(stream)),
+           "moe_build_expert_csr_static")
 
 
 def moe_grouped_gate_up_silu_nvfp4(x_bf16: torch.Tensor, k: int, F: int, w_gate_up: NvFp4Bank,

@@ -45,6 +45,7 @@ SIGNATURES = [
     ("moe_grouped_down_combine_nvfp4", c_i32,
      [ctypes.POINTER(Bank), CSR, c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_size,
       c_vp]),
+    ("moe_build_expert_csr_static", c_i32, [c_vp, c_i32, c_i32, c_i32, CSR, c_vp]),
     ("moe_status_string", ctypes.c_char_p, [c_i32]),
     ("moe_get_device_error", c_i32, [c_vp, c_vp, ctypes.POINTER(c_i32)]),
 ]

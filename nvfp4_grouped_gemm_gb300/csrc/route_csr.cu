@@ -11,6 +11,8 @@
 // expert in earlier slices), pass C walks each slice in ascending p and places pairs with
 // a warp-level match so that equal experts keep ascending p.  Placement never depends on
 // the order atomics happen to arrive in, so the output is bit-exact.
+#include <mutex>
+
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -196,4 +198,56 @@ cudaError_t launch_build_csr(const int32_t* ids, int P, int k, int E, moe_csr cs
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Allocation-free variant of moe_build_expert_csr
+// ---------------------------------------------------------------------------
+// Its scratch (the per-pair CSR positions and the device error word, which the regular
+// entry point keeps in the caller's workspace) lives in this file-scope device array.
+// Every GPU that loads the library holds it until the process exits.
+constexpr int kStaticMaxPairs = 65536;
+static __device__ __align__(256) int32_t g_csr_scratch[kStaticMaxPairs + 64];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+int32_t* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_csr_scratch on the current device, looked up once per device.
+// In host code the array's name is only a host-side handle, never a device address.
+cudaError_t scratch_for_current_device(int32_t** out) {
+  int dev = 0;
+  cudaError_t st = cudaGetDevice(&dev);
+  if (st != cudaSuccess) return st;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    st = cudaGetSymbolAddress(&p, g_csr_scratch);
+    if (st != cudaSuccess) return st;
+    g_scratch_ptr[dev] = static_cast<int32_t*>(p);
+  }
+  *out = g_scratch_ptr[dev];
+  return cudaSuccess;
+}
+}  // namespace
+
 }  // namespace moe
+
+extern "C" moe_status moe_build_expert_csr_static(const int32_t* topk_ids, int32_t T, int32_t k,
+                                                  int32_t E, moe_csr csr, void* stream) {
+  using namespace moe;
+  if (!topk_ids) return MOE_ERR_INVALID_ARG;
+  if (T <= 0 || k <= 0 || E <= 0 || k > E) return MOE_ERR_INVALID_ARG;
+  if (!csr.expert_offsets || !csr.pair_ids || !csr.active_experts || !csr.n_active)
+    return MOE_ERR_INVALID_ARG;
+  if (k > kMaxK || E > kMaxE) return MOE_ERR_UNSUPPORTED;
+  if ((long long)T * k > kStaticMaxPairs) return MOE_ERR_UNSUPPORTED;
+  int32_t* scratch = nullptr;
+  if (scratch_for_current_device(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
+  // every pair's position is rewritten by the kernel; the error word is only OR-ed into
+  // and never read back by this entry point, so nothing needs clearing between calls
+  cudaError_t st = launch_build_csr(topk_ids, T * k, k, E, csr, scratch,
+                                    reinterpret_cast<uint32_t*>(scratch + kStaticMaxPairs),
+                                    static_cast<cudaStream_t>(stream));
+  return st == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
