@@ -230,6 +230,23 @@ def run_reference(args):
     print(json.dumps(line))
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """MAX of a per-rank float over the process group (identity without one)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(work_per_rank: float, world: int, slowest_s: float) -> float:
+    """Whole-job throughput: the work of every rank over the slowest rank's time."""
+    return work_per_rank * world / slowest_s
+
+
 def metric_name(workload):
     if is_prefill(workload):
         return "routed-MoE layer TFLOP/s (prefill, NVFP4 block-scaled tcgen05), % of FP4 roof"
@@ -365,18 +382,13 @@ def run_ours(args):
     step_ms = [e0.elapsed_time(e1) for (_, e0, e1) in evs]
     tot_ms = sum(step_ms)
     uniq_steps = [uniq[b] for (b, _, _) in evs]
-    if world > 1:
-        t = torch.tensor([tot_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        tot_ms = float(t.item())
-
+    tot_ms = max_over_ranks(tot_ms, dev)
     if prefill:
-        work = flops_per_step * args.steps * world
-        value = work / (tot_ms * 1e-3) / 1e12
+        value = weak_scaling_value(flops_per_step * args.steps, world, tot_ms * 1e-3) / 1e12
         unit = "TFLOP/s"
     else:
-        work = sum(u * per_expert for u in uniq_steps) * world
-        value = work / (tot_ms * 1e-3) / 1e9
+        value = weak_scaling_value(sum(u * per_expert for u in uniq_steps), world,
+                                   tot_ms * 1e-3) / 1e9
         unit = "GB/s"
 
     # per-kernel breakdown: the same layer as three graphs, L2 flushed before each step

@@ -103,18 +103,25 @@ typedef struct moe_ws_layout {
   size_t error_word;   /* u32 device error word */
   size_t pair_pos;     /* i32 [P]   CSR position of pair p, -1 if its expert id is invalid */
   size_t h;            /* f32 [P][F] h = silu(g) * u, rows in CSR order */
+  size_t xg;           /* decode: f16 [P][H] activation rows gathered in CSR order, times 2^-xe */
+  size_t xe;           /* decode: i32 [P] power-of-two prescale of each gathered row */
+  size_t hg;           /* decode: f16 [P][F] h times 2^-he */
+  size_t he;           /* decode: i32 [P] */
   size_t qx_codes;     /* prefill: u8 [P][H/2]  Q(x) in CSR order */
   size_t qx_scales;    /* prefill: u8 [P][H/16] */
   size_t qx_exp;       /* prefill: i32 [P] row exponents */
   size_t qh_codes;     /* prefill: u8 [P][F/2]  Q(h) in CSR order */
   size_t qh_scales;    /* prefill: u8 [P][F/16] */
   size_t qh_exp;       /* prefill: i32 [P] */
-  size_t partial;      /* f32 [P][H] per-pair down projections z, rows in CSR order */
+  size_t partial;      /* per-pair down projections z, rows in CSR order: f32 [P][H] on the
+                          decode path; on the prefill path f16 [P][H] holding
+                          z * 2^-(qh_exp[row] + c_F), c_F the smallest shift with
+                          F * 2688^2 * 2^-c_F < 2^15 */
   size_t tiles;        /* prefill: i32 count, pad to 16 B, then int4 {row0, rows, expert, 0} per M-tile */
 } moe_ws_layout;
 
 /* Limits (MOE_ERR_UNSUPPORTED beyond them): 1 <= k <= min(E, 32); E <= 1024;
- * H % 128 == 0; F % 64 == 0; T*k < 2^31 / max(H, F). */
+ * H % 256 == 0 and H <= 4096; F % 64 == 0; T*k < 2^31 / max(H, F). */
 
 /* Workspace size in bytes for one layer with these sizes (0 if the sizes are invalid). */
 size_t moe_workspace_bytes(int32_t T, int32_t H, int32_t F, int32_t E, int32_t k, int32_t path);

@@ -18,7 +18,7 @@ moe_status sizes_supported(int T, int H, int F, int E, int k) {
   if (!sizes_ok(T, H, F, E, k)) return MOE_ERR_INVALID_ARG;
   if (k > E) return MOE_ERR_INVALID_ARG;
   if (k > kMaxK || E > kMaxE) return MOE_ERR_UNSUPPORTED;
-  if (H % 128 != 0 || F % 64 != 0) return MOE_ERR_UNSUPPORTED;
+  if (H % 256 != 0 || H > 4096 || F % 64 != 0) return MOE_ERR_UNSUPPORTED;
   const long long P = (long long)T * k;
   const long long big = H > F ? H : F;
   if (P * big >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
@@ -71,7 +71,12 @@ bool compute_layout(int T, int H, int F, int E, int k, int path, moe_ws_layout* 
   L->pair_pos = take(P * sizeof(int32_t));
   L->h = take(P * F * sizeof(float));
   L->partial = take(P * H * sizeof(float));
-  if (path == MOE_PATH_PREFILL) {
+  if (path == MOE_PATH_DECODE) {
+    L->xg = take(P * H * 2);
+    L->xe = take(P * sizeof(int32_t));
+    L->hg = take(P * F * 2);
+    L->he = take(P * sizeof(int32_t));
+  } else {
     L->qx_codes = take(P * (H / 2));
     L->qx_scales = take(P * (H / 16));
     L->qx_exp = take(P * sizeof(int32_t));
@@ -143,7 +148,7 @@ moe_status moe_build_expert_csr(const int32_t* topk_ids, int32_t T, int32_t k, i
   // the CSR needs only the error word and pair_pos, which sit at the same offsets for
   // every (H, F, path); validate against the smallest legal layout
   moe_ws_layout L;
-  if (!compute_layout(T, 128, 64, E, k, MOE_PATH_DECODE, &L)) return MOE_ERR_UNSUPPORTED;
+  if (!compute_layout(T, 256, 64, E, k, MOE_PATH_DECODE, &L)) return MOE_ERR_UNSUPPORTED;
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MOE_ERR_WORKSPACE;
   if (ws_bytes < L.pair_pos + (size_t)T * k * sizeof(int32_t)) return MOE_ERR_WORKSPACE;
   char* w = static_cast<char*>(ws);
@@ -202,9 +207,10 @@ moe_status moe_grouped_down_combine_nvfp4(const moe_nvfp4_bank* w_down, moe_csr 
     bool unsup = false;
     ce = launch_prefill_down(*w_down, csr, T, H, F, k, L, w, s, &unsup);
     if (unsup) return MOE_ERR_UNSUPPORTED;
-  } else {
-    ce = launch_decode_down(*w_down, csr, T, H, F, k, L, w, s);
+    if (ce != cudaSuccess) return MOE_ERR_CUDA;
+    return from_cuda(launch_prefill_combine(topk_w, T, H, F, k, L, w, y, s));
   }
+  ce = launch_decode_down(*w_down, csr, T, H, F, k, L, w, s);
   if (ce != cudaSuccess) return MOE_ERR_CUDA;
   return from_cuda(launch_combine(topk_w, T, H, k, L, w, y, s));
 }

@@ -1,30 +1,51 @@
 // Decode path: few pairs per expert, memory-bound on the NVFP4 weight bytes.
 //
-// Every active expert's rows are streamed from HBM exactly once per call with 128-bit
-// non-allocating loads (the union-of-experts gather: the grid is indexed by active
-// expert, not by pair), dequantised in registers (E2M1 -> f16 via cvt, times the UE4M3
-// scale, exact in f16), and multiplied on the tensor cores (mma.sync m16n8k16, f32
-// accumulate) against the expert's activation rows, which are staged once per CTA in
-// shared memory as f16 with a per-row power-of-two prescale (exact for bf16 inputs in
-// f16's normal range: the row's largest magnitude lands in [2^14, 2^15)) and reused by
-// every weight row of the CTA.
+// The grid is indexed by active expert, not by pair, so every active expert's rows are
+// streamed from HBM exactly once per call (the union-of-experts gather).  Kernels:
 //
-// Lane layout of one m16n8k16 step: lane = 4g + c holds 16 contiguous code bytes (32
-// elements) of weight rows g and g+8 per 128-element k-block; MMA step s consumes bytes
-// 2s, 2s+1, i.e. elements 32c + 4s .. 32c + 4s + 3, and the activation fragment is read
-// from the same four elements.  The tensor core sums over k in any order, so this
-// permutation of k (identical for both operands) leaves the product unchanged.
+//   x_gather_kernel   CSR row r <- token x row as f16 times 2^-e (e from the row's amax,
+//                     so the largest magnitude lands in [2^14, 2^15): exact for bf16
+//                     values in f16's normal range)
+//   gate_up_kernel    CTA = (active expert, 16 gate rows + the matching 16 up rows); the
+//                     CTA's weight bytes land in shared memory with 16-byte cp.async
+//                     issued by every thread up front, the activation fragments come
+//                     straight from the gathered f16 rows, 8 warps split the H
+//                     reduction (summed in a fixed order), one warp writes h = silu(g)*u
+//   h_prep_kernel     CSR row r of h (f32) -> f16 times 2^-e, as for x
+//   down_kernel       CTA = (active expert, 128 output rows), weights and the expert's h
+//                     rows in shared memory, warp w owns 16 rows over the whole F
+//   combine_kernel    y[t] = sum_j w[t,j] z[pos(t,j)] in ascending j, no atomics
+//
+// FP4 codes are dequantised in registers (cvt.rn.f16x2.e2m1x2, times the UE4M3 scale via
+// cvt.rn.f16x2.e4m3x2: every product has <= 6 significant bits, exact in f16) and fed
+// to mma.sync.m16n8k16 (f32 accumulate).  Lane 4g+c of an MMA step s uses elements
+// 32c + 4s .. 32c + 4s + 3 of a 128-element k-block for both operands; the tensor core
+// sums over k in any order, so this shared permutation leaves the product unchanged.
+//
+// Kernels after the CSR are launched with programmatic dependent launch: each issues
+// the loads that depend only on the CSR (two or more kernels back, complete before its
+// predecessor passed its own griddepcontrol.wait) and then waits for its predecessor.
 #include "moe_internal.cuh"
 
 namespace moe {
 
 namespace {
 
-// Byte offset of 16-byte chunk `lc` of a staged f16 row: XOR-swizzled so that the
-// quarter-warp reading chunks 4c+u of rows g, g+1 touches eight distinct bank groups.
-__device__ __forceinline__ int swz_chunk(int lc) { return (lc ^ (((lc >> 3) & 1) << 1)) * 16; }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
-// Dequantise one MMA step's A fragment for a pair of rows (g, g+8): bytes 2s, 2s+1.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+               ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// Dequantise one MMA step's A fragment for rows (g, g+8): code bytes 2S, 2S+1 of the lane's
+// 16-byte piece of each row.
 template <int S>
 __device__ __forceinline__ void a_frag(const uint4& r0, const uint4& r1, uint32_t sc0,
                                        uint32_t sc1, uint32_t (&a)[4]) {
@@ -37,7 +58,7 @@ __device__ __forceinline__ void a_frag(const uint4& r0, const uint4& r1, uint32_
   a[3] = hmul2_u32(e2m1x2_to_f16x2(w1 >> (sh + 8)), sc1);
 }
 
-// Same for 8-byte (64-element k-block) lanes: bytes 2s, 2s+1 of a uint2.
+// Same for 64-element k-blocks: bytes 2S, 2S+1 of the lane's 8-byte piece.
 template <int S>
 __device__ __forceinline__ void a_frag64(const uint2& r0, const uint2& r1, uint32_t sc0,
                                          uint32_t sc1, uint32_t (&a)[4]) {
@@ -50,218 +71,219 @@ __device__ __forceinline__ void a_frag64(const uint2& r0, const uint2& r1, uint3
   a[3] = hmul2_u32(e2m1x2_to_f16x2(w1 >> (sh + 8)), sc1);
 }
 
+// Byte offset of 16-byte chunk `q` of row `r` in a shared code tile: with `swz` (rows a
+// multiple of 128 bytes) odd rows swap the two 64-byte halves of each 128-byte window, so
+// the quarter-warp reading the same chunk of rows g, g+1 hits distinct banks.
+__device__ __forceinline__ int wchunk(int r, int q, int row_bytes, bool swz) {
+  return r * row_bytes + ((swz ? (q ^ ((r & 1) << 2)) : q) << 4);
+}
+
+// Byte offset of 16-byte chunk `lc` of a staged f16 activation row: XOR-swizzled so the
+// quarter-warp reading chunks 4c+u of rows g, g+1 touches eight distinct bank groups.
+__device__ __forceinline__ int swz_chunk(int lc) { return (lc ^ (((lc >> 3) & 1) << 1)) * 16; }
+
+// ---------------------------------------------------------------------------
+// gather + f16 prescale of the activation rows of every CSR row (decode stage a3)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) x_gather_kernel(const uint16_t* __restrict__ x, int H, int k,
+                                                       const int32_t* __restrict__ pair_ids,
+                                                       const int32_t* __restrict__ offsets, int E,
+                                                       __half* __restrict__ xg,
+                                                       int32_t* __restrict__ xe) {
+  pdl_wait();
+  pdl_trigger();
+  const int pos = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (pos >= offsets[E]) return;
+  const uint16_t* row = x + (size_t)(pair_ids[pos] / k) * H;
+  float amax = 0.0f;
+  for (int c = lane * 8; c < H; c += 256) {
+    const uint4 v = *reinterpret_cast<const uint4*>(row + c);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      amax = fmaxf(amax, fabsf(__uint_as_float(w[i] << 16)));
+      amax = fmaxf(amax, fabsf(__uint_as_float(w[i] & 0xffff0000u)));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const int e = f16_prescale_exp(amax);
+  if (lane == 0) xe[pos] = e;
+  for (int c = lane * 8; c < H; c += 256) {
+    const uint4 v = *reinterpret_cast<const uint4*>(row + c);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2 hv = __floats2half2_rn(ldexpf(__uint_as_float(w[i] << 16), -e),
+                                           ldexpf(__uint_as_float(w[i] & 0xffff0000u), -e));
+      o[i] = *reinterpret_cast<const uint32_t*>(&hv);
+    }
+    *reinterpret_cast<uint4*>(xg + (size_t)pos * H + c) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// Same for h (f32 rows already in CSR order).
+__global__ void __launch_bounds__(256) h_prep_kernel(const float* __restrict__ h, int F,
+                                                     const int32_t* __restrict__ offsets, int E,
+                                                     __half* __restrict__ hg,
+                                                     int32_t* __restrict__ he) {
+  pdl_wait();
+  pdl_trigger();
+  const int pos = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (pos >= offsets[E]) return;
+  const float* row = h + (size_t)pos * F;
+  float amax = 0.0f;
+  for (int c = lane * 8; c < F; c += 256) {
+    const float4 a = *reinterpret_cast<const float4*>(row + c);
+    const float4 b = *reinterpret_cast<const float4*>(row + c + 4);
+    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))));
+    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w))));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const int e = f16_prescale_exp(amax);
+  if (lane == 0) he[pos] = e;
+  for (int c = lane * 8; c < F; c += 256) {
+    const float4 a = *reinterpret_cast<const float4*>(row + c);
+    const float4 b = *reinterpret_cast<const float4*>(row + c + 4);
+    __half2 h0 = __floats2half2_rn(ldexpf(a.x, -e), ldexpf(a.y, -e));
+    __half2 h1 = __floats2half2_rn(ldexpf(a.z, -e), ldexpf(a.w, -e));
+    __half2 h2 = __floats2half2_rn(ldexpf(b.x, -e), ldexpf(b.y, -e));
+    __half2 h3 = __floats2half2_rn(ldexpf(b.z, -e), ldexpf(b.w, -e));
+    *reinterpret_cast<uint4*>(hg + (size_t)pos * F + c) =
+        make_uint4(*reinterpret_cast<uint32_t*>(&h0), *reinterpret_cast<uint32_t*>(&h1),
+                   *reinterpret_cast<uint32_t*>(&h2), *reinterpret_cast<uint32_t*>(&h3));
+  }
+}
+
 // ---------------------------------------------------------------------------
 // gate/up + SiLU
 // ---------------------------------------------------------------------------
-// CTA = KS x RB warps: RB row blocks (16 gate rows + the matching 16 up rows each), the
-// H reduction split over KS warps and summed in shared memory in a fixed order.
-// grid = (ceil(F / (16 RB)), max_active).  Tokens of the expert are processed 8*NT at a time.
 struct GateUpArgs {
-  const uint16_t* x;      // bf16 [T][H]
+  const __half* xg;        // [P][H] gathered f16 activations
+  const int32_t* xe;       // [P]
   const uint8_t* codes;
   const uint8_t* scales;
-  int H, F, k;
+  int H, F;
   const int32_t* offsets;
-  const int32_t* pair_ids;
   const int32_t* active;
   const int32_t* n_active;
   float* h;
 };
 
-template <int KS, int RB, int NT>
-__global__ void __launch_bounds__(32 * KS * RB)
-decode_gate_up_kernel(const GateUpArgs args) {
-  extern __shared__ __align__(16) unsigned char smem[];
+// KMAX = ceil(H / 128 / 8): k-blocks per warp, their activation fragments held in registers.
+template <int KMAX>
+__global__ void __launch_bounds__(256, KMAX <= 2 ? 3 : 2) gate_up_kernel(const GateUpArgs args) {
+  extern __shared__ __align__(128) unsigned char smem[];
   const int a_idx = blockIdx.y;
-  if (a_idx >= *args.n_active) return;
+  const bool live_cta = a_idx < *args.n_active;
   const int H = args.H, F = args.F;
-  const int e = args.active[a_idx];
+  const int e = live_cta ? args.active[a_idx] : 0;
+  const int i0 = blockIdx.x * 16;
+  const int row_bytes = H / 2, srow = H / 16;
+  unsigned char* wc = smem;                               // [32][row_bytes] swizzled codes
+  unsigned char* ws = smem + 32 * row_bytes;              // [32][srow] scales
+  float* red = reinterpret_cast<float*>(ws + 32 * srow);  // [8 warps][32][8]
+
+  if (live_cta) {
+    // every thread issues its share of the 16-byte copies: rows 0..15 gate, 16..31 up
+    const size_t rows2F = (size_t)2 * F;
+    const int cpr = row_bytes / 16;                          // chunks per code row
+    for (int idx = threadIdx.x; idx < 32 * cpr; idx += 256) {
+      const int r = idx / cpr, q = idx - r * cpr;
+      const size_t wrow = (size_t)e * rows2F + (r < 16 ? i0 + r : F + i0 + r - 16);
+      cp_async16(wc + wchunk(r, q, row_bytes, true), args.codes + wrow * row_bytes + q * 16);
+    }
+    const int spr = srow / 16;
+    for (int idx = threadIdx.x; idx < 32 * spr; idx += 256) {
+      const int r = idx / spr, q = idx - r * spr;
+      const size_t wrow = (size_t)e * rows2F + (r < 16 ? i0 + r : F + i0 + r - 16);
+      cp_async16(ws + r * srow + q * 16, args.scales + wrow * srow + q * 16);
+    }
+  }
+  pdl_wait();                         // the gathered activations are complete
+  if (!live_cta) return;
   const int off = args.offsets[e];
   const int m = args.offsets[e + 1] - off;
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
-  const int kw = warp % KS, rbw = warp / KS;
-  const int i0 = (blockIdx.x * RB + rbw) * 16;     // first gate row of this warp
-  const bool rows_ok = i0 < F;
-
-  const int row_bytes = H / 2, srow_bytes = H / 16;
-  const size_t rows2F = (size_t)2 * F;
-  const uint8_t* cb = args.codes + (size_t)e * rows2F * row_bytes;
-  const uint8_t* sb = args.scales + (size_t)e * rows2F * srow_bytes;
-  const int ig = rows_ok ? i0 + g : 0;
-  const uint8_t* pg0 = cb + (size_t)ig * row_bytes + 16 * c;
-  const uint8_t* pg1 = pg0 + (size_t)8 * row_bytes;
-  const uint8_t* pu0 = pg0 + (size_t)F * row_bytes;
-  const uint8_t* pu1 = pu0 + (size_t)8 * row_bytes;
-  const uint8_t* sg0 = sb + (size_t)ig * srow_bytes + 2 * c;
-  const uint8_t* sg1 = sg0 + (size_t)8 * srow_bytes;
-  const uint8_t* su0 = sg0 + (size_t)F * srow_bytes;
-  const uint8_t* su1 = su0 + (size_t)8 * srow_bytes;
-
   const int nkb = H / 128;
-  const int kb_beg = kw * nkb / KS, kb_end = (kw + 1) * nkb / KS;
+  const int kb_beg = warp * nkb / 8, kb_end = (warp + 1) * nkb / 8;
+  cp_async_commit_wait_all();
+  __syncthreads();
 
-  const int xrow_bytes = H * 2 + 16;
-  unsigned char* xs = smem;                                        // [8NT][xrow_bytes]
-  int* slot_exp = reinterpret_cast<int*>(smem + 8 * NT * xrow_bytes);   // [8NT]
-  uint32_t* slot_amax = reinterpret_cast<uint32_t*>(slot_exp + 8 * NT);  // [8NT]
-  int* slot_tok = reinterpret_cast<int*>(slot_amax + 8 * NT);             // [8NT]
-  float* red = reinterpret_cast<float*>(smem + 8 * NT * xrow_bytes + 24 * NT * sizeof(int));
-
-  for (int tok0 = 0; tok0 < m; tok0 += 8 * NT) {
-    // prefetch the first k-block of weights before staging the activations
-    uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0, c2 = c0, c3 = c0;
-    uint32_t s0 = 0, s1 = 0, s2 = 0, s3 = 0;
-    if (rows_ok && kb_beg < kb_end) {
-      c0 = ldg_stream(pg0 + kb_beg * 64); c1 = ldg_stream(pg1 + kb_beg * 64);
-      c2 = ldg_stream(pu0 + kb_beg * 64); c3 = ldg_stream(pu1 + kb_beg * 64);
-      s0 = *reinterpret_cast<const uint16_t*>(sg0 + kb_beg * 8);
-      s1 = *reinterpret_cast<const uint16_t*>(sg1 + kb_beg * 8);
-      s2 = *reinterpret_cast<const uint16_t*>(su0 + kb_beg * 8);
-      s3 = *reinterpret_cast<const uint16_t*>(su1 + kb_beg * 8);
-    }
-    __syncthreads();   // previous pass done with xs
-    // stage the pass's activation rows (only the live ones): raw bf16 first, with each
-    // row's amax; dead slots keep stale data, which only reaches discarded output columns
-    const int live = min(8 * NT, m - tok0);
-    if (threadIdx.x < 8 * NT) {
-      slot_amax[threadIdx.x] = 0u;
-      slot_tok[threadIdx.x] =
-          threadIdx.x < live ? args.pair_ids[off + tok0 + threadIdx.x] / args.k : 0;
-    }
-    __syncthreads();
-    const int nchunk = H / 8;
-    for (int idx = threadIdx.x; idx < live * nchunk; idx += blockDim.x) {
-      const int slot = idx / nchunk, ch = idx - slot * nchunk;
-      const uint4 v =
-          *reinterpret_cast<const uint4*>(args.x + (size_t)slot_tok[slot] * H + ch * 8);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      uint32_t am = 0;
+  for (int tok0 = 0; tok0 < m; tok0 += 8) {
+    const int live = min(8, m - tok0);
+    // activation fragments of this warp's k-blocks, all requested up front
+    uint4 xb[KMAX][4];
+    const __half* xrow = args.xg + (size_t)(off + tok0 + g) * H + 32 * c;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        am = max(am, (w[i] << 16) & 0x7fffffffu);
-        am = max(am, w[i] & 0x7fff0000u);
+    for (int j = 0; j < KMAX; ++j)
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int kb = kb_beg + j;
+        xb[j][u] = (g < live && kb < kb_end)
+                       ? __ldg(reinterpret_cast<const uint4*>(xrow + kb * 128 + 8 * u))
+                       : make_uint4(0, 0, 0, 0);
       }
-      if (am) atomicMax(&slot_amax[slot], am);         // |x| as ordered integer bits
-      *reinterpret_cast<uint4*>(xs + slot * xrow_bytes + swz_chunk(ch)) = v;
-    }
-    __syncthreads();
-    if (threadIdx.x < 8 * NT)
-      slot_exp[threadIdx.x] = f16_prescale_exp(__uint_as_float(slot_amax[threadIdx.x]));
-    __syncthreads();
-    // convert in place to f16 times 2^-exp (same thread, same chunk as above)
-    for (int idx = threadIdx.x; idx < live * nchunk; idx += blockDim.x) {
-      const int slot = idx / nchunk, ch = idx - slot * nchunk;
-      uint4* q = reinterpret_cast<uint4*>(xs + slot * xrow_bytes + swz_chunk(ch));
-      const uint4 v = *q;
-      const int ex = slot_exp[slot];
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      uint32_t o[4];
+    float accg[4] = {0.f, 0.f, 0.f, 0.f}, accu[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const __half2 hv = __floats2half2_rn(ldexpf(__uint_as_float(w[i] << 16), -ex),
-                                             ldexpf(__uint_as_float(w[i] & 0xffff0000u), -ex));
-        o[i] = *reinterpret_cast<const uint32_t*>(&hv);
-      }
-      *q = make_uint4(o[0], o[1], o[2], o[3]);
-    }
-    __syncthreads();
-
-    float accg[NT][4], accu[NT][4];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int q = 0; q < 4; ++q) accg[nt][q] = accu[nt][q] = 0.0f;
-
-    if (rows_ok) {
-      for (int kb = kb_beg; kb < kb_end; ++kb) {
-        uint4 n0 = c0, n1 = c1, n2 = c2, n3 = c3;
-        uint32_t t0 = s0, t1 = s1, t2 = s2, t3 = s3;
-        if (kb + 1 < kb_end) {
-          n0 = ldg_stream(pg0 + (kb + 1) * 64); n1 = ldg_stream(pg1 + (kb + 1) * 64);
-          n2 = ldg_stream(pu0 + (kb + 1) * 64); n3 = ldg_stream(pu1 + (kb + 1) * 64);
-          t0 = *reinterpret_cast<const uint16_t*>(sg0 + (kb + 1) * 8);
-          t1 = *reinterpret_cast<const uint16_t*>(sg1 + (kb + 1) * 8);
-          t2 = *reinterpret_cast<const uint16_t*>(su0 + (kb + 1) * 8);
-          t3 = *reinterpret_cast<const uint16_t*>(su1 + (kb + 1) * 8);
-        }
-        const uint32_t f0 = e4m3x2_to_f16x2(s0), f1 = e4m3x2_to_f16x2(s1);
-        const uint32_t f2 = e4m3x2_to_f16x2(s2), f3 = e4m3x2_to_f16x2(s3);
-        // activation fragments for this k-block: 4 chunks of 16 B per n-tile
-        uint4 xb[NT][4];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            xb[nt][u] = *reinterpret_cast<const uint4*>(
-                xs + (nt * 8 + g) * xrow_bytes + swz_chunk(kb * 16 + 4 * c + u));
+    for (int j = 0; j < KMAX; ++j) {
+      const int kb = kb_beg + j;
+      if (kb < kb_end) {
+      const uint4 c0 = *reinterpret_cast<const uint4*>(wc + wchunk(g, kb * 4 + c, row_bytes, true));
+      const uint4 c1 = *reinterpret_cast<const uint4*>(wc + wchunk(g + 8, kb * 4 + c, row_bytes, true));
+      const uint4 c2 = *reinterpret_cast<const uint4*>(wc + wchunk(g + 16, kb * 4 + c, row_bytes, true));
+      const uint4 c3 = *reinterpret_cast<const uint4*>(wc + wchunk(g + 24, kb * 4 + c, row_bytes, true));
+      const unsigned char* sp = ws + g * srow + kb * 8 + 2 * c;
+      const uint32_t f0 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sp));
+      const uint32_t f1 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sp + 8 * srow));
+      const uint32_t f2 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sp + 16 * srow));
+      const uint32_t f3 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sp + 24 * srow));
 #define MOE_GU_STEP(S)                                                                     \
   {                                                                                        \
     uint32_t ag[4], au[4];                                                                 \
-    const uint32_t scg0 = (S < 4) ? bcast_lo(f0) : bcast_hi(f0);                           \
-    const uint32_t scg1 = (S < 4) ? bcast_lo(f1) : bcast_hi(f1);                           \
-    const uint32_t scu0 = (S < 4) ? bcast_lo(f2) : bcast_hi(f2);                           \
-    const uint32_t scu1 = (S < 4) ? bcast_lo(f3) : bcast_hi(f3);                           \
-    a_frag<S>(c0, c1, scg0, scg1, ag);                                                     \
-    a_frag<S>(c2, c3, scu0, scu1, au);                                                     \
-    _Pragma("unroll") for (int nt = 0; nt < NT; ++nt) {                                    \
-      const uint32_t b0 = (S & 1) ? xb[nt][S / 2].z : xb[nt][S / 2].x;                     \
-      const uint32_t b1 = (S & 1) ? xb[nt][S / 2].w : xb[nt][S / 2].y;                     \
-      mma_f16_16816(accg[nt], ag[0], ag[1], ag[2], ag[3], b0, b1);                         \
-      mma_f16_16816(accu[nt], au[0], au[1], au[2], au[3], b0, b1);                         \
-    }                                                                                      \
+    a_frag<S>(c0, c1, (S < 4) ? bcast_lo(f0) : bcast_hi(f0),                               \
+              (S < 4) ? bcast_lo(f1) : bcast_hi(f1), ag);                                  \
+    a_frag<S>(c2, c3, (S < 4) ? bcast_lo(f2) : bcast_hi(f2),                               \
+              (S < 4) ? bcast_lo(f3) : bcast_hi(f3), au);                                  \
+    const uint32_t b0 = (S & 1) ? xb[j][S / 2].z : xb[j][S / 2].x;                         \
+    const uint32_t b1 = (S & 1) ? xb[j][S / 2].w : xb[j][S / 2].y;                         \
+    mma_f16_16816(accg, ag[0], ag[1], ag[2], ag[3], b0, b1);                               \
+    mma_f16_16816(accu, au[0], au[1], au[2], au[3], b0, b1);                               \
   }
-        MOE_GU_STEP(0) MOE_GU_STEP(1) MOE_GU_STEP(2) MOE_GU_STEP(3)
-        MOE_GU_STEP(4) MOE_GU_STEP(5) MOE_GU_STEP(6) MOE_GU_STEP(7)
+      MOE_GU_STEP(0) MOE_GU_STEP(1) MOE_GU_STEP(2) MOE_GU_STEP(3)
+      MOE_GU_STEP(4) MOE_GU_STEP(5) MOE_GU_STEP(6) MOE_GU_STEP(7)
 #undef MOE_GU_STEP
-        c0 = n0; c1 = n1; c2 = n2; c3 = n3;
-        s0 = t0; s1 = t1; s2 = t2; s3 = t3;
       }
     }
-
-    // fixed-order reduction over the KS warps sharing a row block
-    if (KS > 1) {
-      float* mine = red + (((size_t)(kw * RB + rbw) * NT) * 32 + lane) * 8;
+    // fixed-order sum over the 8 warps' k ranges
+    float* mine = red + (warp * 32 + lane) * 8;
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
+    for (int q = 0; q < 4; ++q) { mine[q] = accg[q]; mine[4 + q] = accu[q]; }
+    __syncthreads();
+    if (warp == 0) {
+      float sg[4] = {0.f, 0.f, 0.f, 0.f}, su[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int w = 0; w < 8; ++w) {
+        const float* src = red + (w * 32 + lane) * 8;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          mine[nt * 256 + q] = accg[nt][q];
-          mine[nt * 256 + 4 + q] = accu[nt][q];
-        }
-      __syncthreads();
-      if (kw == 0) {
+        for (int q = 0; q < 4; ++q) { sg[q] += src[q]; su[q] += src[4 + q]; }
+      }
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) { accg[nt][q] = 0.0f; accu[nt][q] = 0.0f; }
-        for (int w = 0; w < KS; ++w) {
-          const float* src = red + (((size_t)(w * RB + rbw) * NT) * 32 + lane) * 8;
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              accg[nt][q] += src[nt * 256 + q];
-              accu[nt][q] += src[nt * 256 + 4 + q];
-            }
+      for (int q = 0; q < 4; ++q) {
+        const int n = 2 * c + (q & 1);
+        const int i = i0 + g + 8 * (q >> 1);
+        if (n < live) {
+          const int ex = args.xe[off + tok0 + n];
+          args.h[(size_t)(off + tok0 + n) * F + i] =
+              silu_f(ldexpf(sg[q], ex)) * ldexpf(su[q], ex);
         }
       }
     }
-    if (kw == 0 && rows_ok) {
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int n = nt * 8 + 2 * c + (q & 1);
-          const int i = i0 + g + 8 * (q >> 1);
-          if (tok0 + n < m) {
-            const int ex = slot_exp[n];
-            const float gv = ldexpf(accg[nt][q], ex), uv = ldexpf(accu[nt][q], ex);
-            args.h[(size_t)(off + tok0 + n) * F + i] = silu_f(gv) * uv;
-          }
-        }
-    }
+    __syncthreads();
   }
 }
 
@@ -269,7 +291,8 @@ decode_gate_up_kernel(const GateUpArgs args) {
 // down projection: z_p = W_down[e] h_p, rows of the per-pair partials in CSR order
 // ---------------------------------------------------------------------------
 struct DownArgs {
-  const float* h;
+  const __half* hg;        // [P][F]
+  const int32_t* he;       // [P]
   const uint8_t* codes;
   const uint8_t* scales;
   int H, F;
@@ -279,153 +302,105 @@ struct DownArgs {
   float* partial;
 };
 
-// CTA = WARPS warps of 16 output rows each; grid = (ceil(H / (16 WARPS)), max_active).
-// KB = 128 (uint4 lanes) when F % 128 == 0, else 64 (uint2 lanes).
-template <int WARPS, int NT, int KB>
-__global__ void __launch_bounds__(32 * WARPS)
-decode_down_kernel(const DownArgs args) {
-  extern __shared__ __align__(16) unsigned char smem[];
+// KB = 128 (16-byte lane pieces) when F % 128 == 0, else 64 (8-byte pieces).
+template <int KB>
+__global__ void __launch_bounds__(256, 3) down_kernel(const DownArgs args) {
+  extern __shared__ __align__(128) unsigned char smem[];
   const int a_idx = blockIdx.y;
-  if (a_idx >= *args.n_active) return;
+  const bool live_cta = a_idx < *args.n_active;
   const int H = args.H, F = args.F;
-  const int e = args.active[a_idx];
+  const int e = live_cta ? args.active[a_idx] : 0;
+  const int r0 = blockIdx.x * 128;
+  const int row_bytes = F / 2, srow = F / 16;
+  const bool swz = (row_bytes % 128) == 0;
+  unsigned char* wc = smem;                                // [128][row_bytes]
+  unsigned char* ws = smem + 128 * row_bytes;              // [128][srow]
+  const int hrow_bytes = F * 2 + 16;
+  unsigned char* hs = ws + ((128 * srow + 15) & ~15);      // [8][hrow_bytes]
+
+  if (live_cta) {
+    const int cpr = row_bytes / 16;
+    const unsigned char* src = args.codes + ((size_t)e * H + r0) * row_bytes;
+    for (int idx = threadIdx.x; idx < 128 * cpr; idx += 256) {
+      const int r = idx / cpr, q = idx - r * cpr;
+      cp_async16(wc + wchunk(r, q, row_bytes, swz), src + (size_t)r * row_bytes + q * 16);
+    }
+    const unsigned char* ssrc = args.scales + ((size_t)e * H + r0) * srow;
+    for (int idx = threadIdx.x; idx < 128 * srow / 16; idx += 256)
+      cp_async16(ws + idx * 16, ssrc + idx * 16);
+  }
+  pdl_wait();                         // h in f16 is complete
+  if (!live_cta) return;
   const int off = args.offsets[e];
   const int m = args.offsets[e + 1] - off;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
-  const int r0 = (blockIdx.x * WARPS + warp) * 16;
-  const bool rows_ok = r0 < H;
-  const int row_bytes = F / 2, srow_bytes = F / 16;
-  constexpr int LB = KB / 8;                       // code bytes per lane per k-block
-  const uint8_t* cb = args.codes + (size_t)e * H * row_bytes;
-  const uint8_t* sb = args.scales + (size_t)e * H * srow_bytes;
-  const int rg = rows_ok ? r0 + g : 0;
-  const uint8_t* p0 = cb + (size_t)rg * row_bytes + LB * c;
-  const uint8_t* p1 = p0 + (size_t)8 * row_bytes;
-  const uint8_t* q0 = sb + (size_t)rg * srow_bytes + (KB / 64) * c;
-  const uint8_t* q1 = q0 + (size_t)8 * srow_bytes;
   const int nkb = F / KB;
+  constexpr int LB = KB / 8;          // code bytes per lane per k-block
 
-  const int hrow_bytes = F * 2 + 16;
-  unsigned char* hs = smem;                                          // [8NT][hrow_bytes]
-  int* slot_exp = reinterpret_cast<int*>(smem + 8 * NT * hrow_bytes);
-
-  for (int tok0 = 0; tok0 < m; tok0 += 8 * NT) {
-    __syncthreads();
-    // stage h rows as f16 with a per-row power-of-two prescale (one warp per row)
-    const int nlive = min(8 * NT, m - tok0);
-    for (int slot = warp; slot < nlive; slot += WARPS) {
-      const bool live = true;
-      const float* hr = args.h + (size_t)(off + tok0 + slot) * F;
-      float amax = 0.0f;
-      if (live)
-        for (int i = lane * 4; i < F; i += 128) {
-          float4 v = *reinterpret_cast<const float4*>(hr + i);
-          amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
-        }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      const int ex = f16_prescale_exp(amax);
-      if (lane == 0) slot_exp[slot] = ex;
-      for (int ch = lane; ch < F / 8; ch += 32) {
-        uint4 o = make_uint4(0, 0, 0, 0);
-        if (live) {
-          float4 v0 = *reinterpret_cast<const float4*>(hr + ch * 8);
-          float4 v1 = *reinterpret_cast<const float4*>(hr + ch * 8 + 4);
-          __half2 h0 = __floats2half2_rn(ldexpf(v0.x, -ex), ldexpf(v0.y, -ex));
-          __half2 h1 = __floats2half2_rn(ldexpf(v0.z, -ex), ldexpf(v0.w, -ex));
-          __half2 h2 = __floats2half2_rn(ldexpf(v1.x, -ex), ldexpf(v1.y, -ex));
-          __half2 h3 = __floats2half2_rn(ldexpf(v1.z, -ex), ldexpf(v1.w, -ex));
-          o = make_uint4(*reinterpret_cast<uint32_t*>(&h0), *reinterpret_cast<uint32_t*>(&h1),
-                         *reinterpret_cast<uint32_t*>(&h2), *reinterpret_cast<uint32_t*>(&h3));
-        }
-        *reinterpret_cast<uint4*>(hs + slot * hrow_bytes + swz_chunk(ch)) = o;
-      }
+  for (int tok0 = 0; tok0 < m; tok0 += 8) {
+    const int live = min(8, m - tok0);
+    for (int idx = threadIdx.x; idx < live * (F / 8); idx += 256) {
+      const int slot = idx / (F / 8), ch = idx - slot * (F / 8);
+      cp_async16(hs + slot * hrow_bytes + swz_chunk(ch),
+                 args.hg + (size_t)(off + tok0 + slot) * F + ch * 8);
     }
+    cp_async_commit_wait_all();
     __syncthreads();
-    if (!rows_ok) continue;
-
-    float acc[NT][4];
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const int rw = warp * 16 + g;
+    for (int kb = 0; kb < nkb; ++kb) {
+      if (KB == 128) {
+        const uint4 a0 = *reinterpret_cast<const uint4*>(wc + wchunk(rw, kb * 4 + c, row_bytes, swz));
+        const uint4 a1 = *reinterpret_cast<const uint4*>(wc + wchunk(rw + 8, kb * 4 + c, row_bytes, swz));
+        const unsigned char* sp = ws + rw * srow + kb * 8 + 2 * c;
+        const uint32_t f0 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sp));
+        const uint32_t f1 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sp + 8 * srow));
+        uint4 xb[4];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int q = 0; q < 4; ++q) acc[nt][q] = 0.0f;
-
-    if (KB == 128) {
-      uint4 a0 = ldg_stream(p0), a1 = ldg_stream(p1);
-      uint32_t w0 = *reinterpret_cast<const uint16_t*>(q0);
-      uint32_t w1 = *reinterpret_cast<const uint16_t*>(q1);
-      for (int kb = 0; kb < nkb; ++kb) {
-        uint4 b0n = a0, b1n = a1;
-        uint32_t w0n = w0, w1n = w1;
-        if (kb + 1 < nkb) {
-          b0n = ldg_stream(p0 + (kb + 1) * (KB / 2));
-          b1n = ldg_stream(p1 + (kb + 1) * (KB / 2));
-          w0n = *reinterpret_cast<const uint16_t*>(q0 + (kb + 1) * (KB / 16));
-          w1n = *reinterpret_cast<const uint16_t*>(q1 + (kb + 1) * (KB / 16));
-        }
-        const uint32_t f0 = e4m3x2_to_f16x2(w0), f1 = e4m3x2_to_f16x2(w1);
-        uint4 xb[NT][4];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            xb[nt][u] = *reinterpret_cast<const uint4*>(
-                hs + (nt * 8 + g) * hrow_bytes + swz_chunk(kb * 16 + 4 * c + u));
+        for (int q = 0; q < 4; ++q)
+          xb[q] = *reinterpret_cast<const uint4*>(hs + g * hrow_bytes + swz_chunk(kb * 16 + 4 * c + q));
 #define MOE_DN_STEP(S)                                                                     \
   {                                                                                        \
     uint32_t af[4];                                                                        \
-    const uint32_t sc0 = (S < 4) ? bcast_lo(f0) : bcast_hi(f0);                            \
-    const uint32_t sc1 = (S < 4) ? bcast_lo(f1) : bcast_hi(f1);                            \
-    a_frag<S>(a0, a1, sc0, sc1, af);                                                       \
-    _Pragma("unroll") for (int nt = 0; nt < NT; ++nt) {                                    \
-      const uint32_t bb0 = (S & 1) ? xb[nt][S / 2].z : xb[nt][S / 2].x;                    \
-      const uint32_t bb1 = (S & 1) ? xb[nt][S / 2].w : xb[nt][S / 2].y;                    \
-      mma_f16_16816(acc[nt], af[0], af[1], af[2], af[3], bb0, bb1);                        \
-    }                                                                                      \
+    a_frag<S>(a0, a1, (S < 4) ? bcast_lo(f0) : bcast_hi(f0),                               \
+              (S < 4) ? bcast_lo(f1) : bcast_hi(f1), af);                                  \
+    mma_f16_16816(acc, af[0], af[1], af[2], af[3], (S & 1) ? xb[S / 2].z : xb[S / 2].x,     \
+                  (S & 1) ? xb[S / 2].w : xb[S / 2].y);                                    \
   }
         MOE_DN_STEP(0) MOE_DN_STEP(1) MOE_DN_STEP(2) MOE_DN_STEP(3)
         MOE_DN_STEP(4) MOE_DN_STEP(5) MOE_DN_STEP(6) MOE_DN_STEP(7)
 #undef MOE_DN_STEP
-        a0 = b0n; a1 = b1n; w0 = w0n; w1 = w1n;
-      }
-    } else {
-      for (int kb = 0; kb < nkb; ++kb) {
-        const uint2 a0 = ldg_stream64(p0 + kb * (KB / 2));
-        const uint2 a1 = ldg_stream64(p1 + kb * (KB / 2));
-        const uint32_t w0 = q0[kb * (KB / 16)], w1 = q1[kb * (KB / 16)];
-        const uint32_t f0 = bcast_lo(e4m3x2_to_f16x2(w0)), f1 = bcast_lo(e4m3x2_to_f16x2(w1));
-        uint4 xb[NT][2];
+      } else {
+        const unsigned char* rp = wc + rw * row_bytes + LB * c + kb * 32;
+        const uint2 a0 = *reinterpret_cast<const uint2*>(rp);
+        const uint2 a1 = *reinterpret_cast<const uint2*>(rp + 8 * row_bytes);
+        const unsigned char* sp = ws + rw * srow + kb * 4 + c;
+        const uint32_t f0 = bcast_lo(e4m3x2_to_f16x2(sp[0]));
+        const uint32_t f1 = bcast_lo(e4m3x2_to_f16x2(sp[8 * srow]));
+        uint4 xb[2];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int u = 0; u < 2; ++u)
-            xb[nt][u] = *reinterpret_cast<const uint4*>(
-                hs + (nt * 8 + g) * hrow_bytes + swz_chunk(kb * 8 + 2 * c + u));
+        for (int q = 0; q < 2; ++q)
+          xb[q] = *reinterpret_cast<const uint4*>(hs + g * hrow_bytes + swz_chunk(kb * 8 + 2 * c + q));
 #define MOE_DN64_STEP(S)                                                                   \
   {                                                                                        \
     uint32_t af[4];                                                                        \
     a_frag64<S>(a0, a1, f0, f1, af);                                                       \
-    _Pragma("unroll") for (int nt = 0; nt < NT; ++nt) {                                    \
-      const uint32_t bb0 = (S & 1) ? xb[nt][S / 2].z : xb[nt][S / 2].x;                    \
-      const uint32_t bb1 = (S & 1) ? xb[nt][S / 2].w : xb[nt][S / 2].y;                    \
-      mma_f16_16816(acc[nt], af[0], af[1], af[2], af[3], bb0, bb1);                        \
-    }                                                                                      \
+    mma_f16_16816(acc, af[0], af[1], af[2], af[3], (S & 1) ? xb[S / 2].z : xb[S / 2].x,     \
+                  (S & 1) ? xb[S / 2].w : xb[S / 2].y);                                    \
   }
         MOE_DN64_STEP(0) MOE_DN64_STEP(1) MOE_DN64_STEP(2) MOE_DN64_STEP(3)
 #undef MOE_DN64_STEP
       }
     }
-
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int n = nt * 8 + 2 * c + (q & 1);
-        const int r = r0 + g + 8 * (q >> 1);
-        if (tok0 + n < m)
-          args.partial[(size_t)(off + tok0 + n) * H + r] = ldexpf(acc[nt][q], slot_exp[n]);
-      }
+    for (int q = 0; q < 4; ++q) {
+      const int n = 2 * c + (q & 1);
+      const int r = r0 + rw + 8 * (q >> 1);
+      if (n < live)
+        args.partial[(size_t)(off + tok0 + n) * H + r] = ldexpf(acc[q], args.he[off + tok0 + n]);
+    }
+    __syncthreads();
   }
 }
 
@@ -435,6 +410,7 @@ decode_down_kernel(const DownArgs args) {
 __global__ void __launch_bounds__(256)
 combine_kernel(const float* __restrict__ w, const int32_t* __restrict__ pair_pos,
                const float* __restrict__ partial, int H, int k, float* __restrict__ y) {
+  pdl_wait();
   const int t = blockIdx.y;
   const int r = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
   if (r >= H) return;
@@ -452,30 +428,20 @@ combine_kernel(const float* __restrict__ w, const int32_t* __restrict__ pair_pos
   *reinterpret_cast<float4*>(y + (size_t)t * H + r) = acc;
 }
 
-template <int KS, int RB, int NT>
-cudaError_t run_gate_up(const GateUpArgs& a, int F, int max_active, cudaStream_t s) {
-  const int H = a.H;
-  const size_t smem = (size_t)8 * NT * (H * 2 + 16) + 24 * NT * sizeof(int) +
-                      (KS > 1 ? (size_t)KS * RB * NT * 32 * 8 * sizeof(float) : 0);
-  auto kern = decode_gate_up_kernel<KS, RB, NT>;
-  cudaError_t st = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)smem);
-  if (st != cudaSuccess) return st;
-  dim3 grid((F + 16 * RB - 1) / (16 * RB), max_active);
-  kern<<<grid, 32 * KS * RB, smem, s>>>(a);
-  return cudaGetLastError();
-}
-
-template <int WARPS, int NT, int KB>
-cudaError_t run_down(const DownArgs& a, int max_active, cudaStream_t s) {
-  const size_t smem = (size_t)8 * NT * (a.F * 2 + 16) + 8 * NT * sizeof(int);
-  auto kern = decode_down_kernel<WARPS, NT, KB>;
-  cudaError_t st = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)smem);
-  if (st != cudaSuccess) return st;
-  dim3 grid((a.H + 16 * WARPS - 1) / (16 * WARPS), max_active);
-  kern<<<grid, 32 * WARPS, smem, s>>>(a);
-  return cudaGetLastError();
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 }  // namespace
@@ -483,34 +449,55 @@ cudaError_t run_down(const DownArgs& a, int max_active, cudaStream_t s) {
 cudaError_t launch_decode_gate_up(const uint16_t* x_bf16, int T, int H, int F, int k,
                                   const moe_nvfp4_bank& b, moe_csr csr, const moe_ws_layout& L,
                                   char* ws, cudaStream_t s) {
-  GateUpArgs a{x_bf16, b.codes, b.scales, H, F, k, csr.expert_offsets, csr.pair_ids,
-               csr.active_experts, csr.n_active, reinterpret_cast<float*>(ws + L.h)};
+  const int kmax = (H / 128 + 7) / 8;
+  if (kmax > 4) return cudaErrorInvalidValue;
   const int P = T * k;
+  __half* xg = reinterpret_cast<__half*>(ws + L.xg);
+  int32_t* xe = reinterpret_cast<int32_t*>(ws + L.xe);
+  cudaError_t st = launch_pdl(x_gather_kernel, dim3((P + 7) / 8), dim3(256), 0, s, x_bf16, H, k,
+                              (const int32_t*)csr.pair_ids, (const int32_t*)csr.expert_offsets,
+                              b.E, xg, xe);
+  if (st != cudaSuccess) return st;
+  GateUpArgs a{xg, xe, b.codes, b.scales, H, F, csr.expert_offsets, csr.active_experts,
+               csr.n_active, reinterpret_cast<float*>(ws + L.h)};
   const int max_active = P < b.E ? P : b.E;
-  if (P <= 160) return run_gate_up<8, 1, 1>(a, F, max_active, s);
-  return run_gate_up<2, 4, 2>(a, F, max_active, s);
+  const size_t smem = 32 * (size_t)(H / 2) + 32 * (size_t)(H / 16) + 8 * 32 * 8 * sizeof(float);
+  auto kern = kmax <= 1 ? gate_up_kernel<1> : kmax == 2 ? gate_up_kernel<2>
+                                             : kmax == 3 ? gate_up_kernel<3> : gate_up_kernel<4>;
+  st = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (st != cudaSuccess) return st;
+  return launch_pdl(kern, dim3(F / 16, max_active), dim3(256), smem, s, a);
 }
 
 cudaError_t launch_decode_down(const moe_nvfp4_bank& b, moe_csr csr, int T, int H, int F, int k,
                                const moe_ws_layout& L, char* ws, cudaStream_t s) {
-  DownArgs a{reinterpret_cast<const float*>(ws + L.h), b.codes, b.scales, H, F,
-             csr.expert_offsets, csr.active_experts, csr.n_active,
-             reinterpret_cast<float*>(ws + L.partial)};
   const int P = T * k;
+  __half* hg = reinterpret_cast<__half*>(ws + L.hg);
+  int32_t* he = reinterpret_cast<int32_t*>(ws + L.he);
+  cudaError_t st = launch_pdl(h_prep_kernel, dim3((P + 7) / 8), dim3(256), 0, s,
+                              (const float*)(ws + L.h), F, (const int32_t*)csr.expert_offsets, b.E,
+                              hg, he);
+  if (st != cudaSuccess) return st;
+  DownArgs a{hg, he, b.codes, b.scales, H, F, csr.expert_offsets, csr.active_experts,
+             csr.n_active, reinterpret_cast<float*>(ws + L.partial)};
   const int max_active = P < b.E ? P : b.E;
+  const size_t smem = 128 * (size_t)(F / 2) + ((128 * (size_t)(F / 16) + 15) & ~size_t(15)) +
+                      8 * (size_t)(F * 2 + 16);
   if (F % 128 == 0) {
-    if (P <= 160) return run_down<4, 1, 128>(a, max_active, s);
-    return run_down<8, 2, 128>(a, max_active, s);
+    st = cudaFuncSetAttribute(down_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)smem);
+    if (st != cudaSuccess) return st;
+    return launch_pdl(down_kernel<128>, dim3(H / 128, max_active), dim3(256), smem, s, a);
   }
-  return run_down<4, 1, 64>(a, max_active, s);
+  st = cudaFuncSetAttribute(down_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (st != cudaSuccess) return st;
+  return launch_pdl(down_kernel<64>, dim3(H / 128, max_active), dim3(256), smem, s, a);
 }
 
 cudaError_t launch_combine(const float* w, int T, int H, int k, const moe_ws_layout& L, char* ws,
                            float* y, cudaStream_t s) {
-  dim3 grid((H / 4 + 255) / 256, T);
-  combine_kernel<<<grid, 256, 0, s>>>(w, reinterpret_cast<const int32_t*>(ws + L.pair_pos),
-                                      reinterpret_cast<const float*>(ws + L.partial), H, k, y);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3((H / 4 + 255) / 256, T), dim3(256), 0, s, w,
+                    (const int32_t*)(ws + L.pair_pos), (const float*)(ws + L.partial), H, k, y);
 }
 
 }  // namespace moe

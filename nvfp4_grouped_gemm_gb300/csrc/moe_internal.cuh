@@ -37,6 +37,8 @@ cudaError_t launch_prefill_gate_up(const uint16_t* x_bf16, int T, int H, int F, 
 cudaError_t launch_prefill_down(const moe_nvfp4_bank& b, moe_csr csr, int T, int H, int F, int k,
                                 const moe_ws_layout& L, char* ws, cudaStream_t s,
                                 bool* unsupported);
+cudaError_t launch_prefill_combine(const float* w, int T, int H, int F, int k,
+                                   const moe_ws_layout& L, char* ws, float* y, cudaStream_t s);
 cudaError_t launch_combine(const float* w, int T, int H, int k, const moe_ws_layout& L, char* ws,
                            float* y, cudaStream_t s);
 

@@ -19,6 +19,8 @@
 //
 // Every wait on an mbarrier is bounded by a 2 s %globaltimer budget; on expiry the CTA
 // sets MOE_DEVERR_TIMEOUT in the workspace error word, drains and frees its TMEM.
+#include <cmath>
+
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -39,29 +41,46 @@ __device__ __forceinline__ float ue4m3_val(int b) {
   return __uint_as_float((uint32_t)(e + 120) << 23 | (uint32_t)m << 20);   // (1+m/8)*2^(e-7)
 }
 
-// Nearest UE4M3 encoding to key/6 (key = block amax * 2^-s <= 2688), ties to even.
-__device__ __forceinline__ int ue4m3_code_of(float key) {
-  // thresholds t(j) = 6 * (v(j) + v(j+1)) / 2 between encodings j and j+1, j = 0..125
-  int lo = 0, hi = 126;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    const float t = 3.0f * (ue4m3_val(mid) + ue4m3_val(mid + 1));
-    if (t < key) lo = mid + 1; else hi = mid;
-  }
-  if (lo < 126 && 3.0f * (ue4m3_val(lo) + ue4m3_val(lo + 1)) == key && ((lo + 1) & 1) == 0)
-    ++lo;
-  return lo;
+// Decision threshold between UE4M3 encodings j and j+1, times 6: 3 * (v(j) + v(j+1)).
+__device__ __forceinline__ float ue4m3_thr6(int j) { return 3.0f * (ue4m3_val(j) + ue4m3_val(j + 1)); }
+
+// Threshold j "passed" by key: above it, or on it when the upper neighbour is the even code.
+__device__ __forceinline__ bool ue4m3_passed(float key, int j) {
+  const float t = ue4m3_thr6(j);
+  return key > t || (key == t && ((j + 1) & 1) == 0);
 }
 
-// E2M1 magnitude code of key / sbv (key = |v| * 2^-s), nearest with ties to the even code.
-__device__ __forceinline__ uint32_t e2m1_mag(float key, float sbv) {
-  const float mids[7] = {0.25f, 0.75f, 1.25f, 1.75f, 2.5f, 3.5f, 5.0f};
-  uint32_t c = 0;
-#pragma unroll
-  for (int j = 0; j < 7; ++j) {
-    const float t = mids[j] * sbv;
-    c += (key > t) || ((j & 1) && key == t);
+// Nearest UE4M3 encoding to key/6 (key = block amax * 2^-s <= 2688), ties to even: the
+// number of thresholds passed.  A first guess from the float bits of key/6 is corrected
+// by exact comparisons with the neighbouring thresholds.
+__device__ __forceinline__ int ue4m3_code_of(float key) {
+  const float r = key * (1.0f / 6.0f);
+  int cand;
+  if (r < 0.015625f) {
+    cand = (int)(r * 512.0f);                        // subnormal encodings m/8 * 2^-6
+  } else {
+    const uint32_t b = __float_as_uint(r);
+    const int e = (int)((b >> 23) & 0xff) - 127;       // -6 .. 8
+    cand = ((e + 7) << 3) | (int)((b >> 20) & 7);
   }
+  cand = min(max(cand, 0), 126);
+  while (cand < 126 && ue4m3_passed(key, cand)) ++cand;
+  while (cand > 0 && !ue4m3_passed(key, cand - 1)) --cand;
+  return cand;
+}
+
+// E2M1 magnitude code of key / sbv (key = |v| * 2^-s): the number of midpoints passed
+// (above midpoint j * sbv, or on it when the upper neighbour is even, i.e. j odd).
+__device__ __forceinline__ uint32_t e2m1_mag(float key, float sbv) {
+  // midpoints 0.25 0.75 1.25 1.75 | 2.5 3.5 | 5 between 0 .5 1 1.5 2 3 4 6
+  auto passed = [&](int j) {
+    const float mid = j < 4 ? 0.25f + 0.5f * (float)j : (j == 6 ? 5.0f : (float)j - 1.5f);
+    const float t = mid * sbv;
+    return key > t || ((j & 1) && key == t);
+  };
+  uint32_t c = passed(3) ? 4u : 0u;
+  c += passed((int)c + 1) ? 2u : 0u;
+  c += passed((int)c) ? 1u : 0u;
   return c;
 }
 
@@ -367,40 +386,45 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
 // ---------------------------------------------------------------------------
 // grouped block-scaled GEMM
 // ---------------------------------------------------------------------------
-// GATE_UP: A = Q(x) rows [P][H], B = gate rows and up rows of the expert, out h f32 [P][F].
-// DOWN:    A = Q(h) rows [P][F], B = down rows [H][F] of the expert, out partial f32 [P][H].
+// GATE_UP: A = Q(x) rows [P][H]; the B tile stacks BN/2 gate rows over the matching BN/2
+//          up rows of the expert, so one N=BN MMA yields g in accumulator columns
+//          [0, BN/2) and u in [BN/2, BN); out = h f32 [P][F] (BN/2 columns per tile).
+// DOWN:    A = Q(h) rows [P][F], B = BN down rows; out = z * 2^-(row exponent + cF) as f16
+//          [P][H] (the combine restores the scale; the bound |acc| <= F * 2688^2 keeps the
+//          value below 2^15).
 struct GemmArgs {
   const uint8_t* a_scales;      // [P][K/16]
   const int32_t* a_exp;         // [P]
   const uint8_t* b_scales;      // [E][rows][K/16]
   const int32_t* tiles;         // n_mtiles, then int4 list
-  float* out;                   // [P][out_cols]
+  void* out;                    // f32 [P][F] or f16 [P][H]
   uint32_t* err;
-  int P, K, rows_per_expert, n_tiles_n, out_cols, F;
+  int P, K, rows_per_expert, n_tiles_n, out_cols, F, down_shift;
 };
 
 template <int BN, bool GATE_UP>
 struct Cfg {
   static constexpr int BM = 128;
   static constexpr int KB = 128;                    // bytes of K per stage (256 elements)
-  static constexpr int NB = GATE_UP ? 2 : 1;        // B tiles per stage
   static constexpr int G = (BN + 127) / 128;        // 128-row scale-factor atoms per B tile
-  static constexpr int STAGES = 3;
+  static constexpr int STAGES = 4;
+  static constexpr int OUT_N = GATE_UP ? BN / 2 : BN;   // output columns per tile
   static constexpr int A_BYTES = BM * KB;
   static constexpr int B_BYTES = BN * KB;
   static constexpr int SFA_BYTES = 4 * 512;         // 4 k-steps x one atom
   static constexpr int SFB_BYTES = 4 * G * 512;
-  static constexpr int STAGE_BYTES = A_BYTES + NB * B_BYTES + SFA_BYTES + NB * SFB_BYTES;
-  static constexpr int ACC_COLS = NB * BN;
-  static constexpr int SF_COLS = 16 + NB * 16 * G;  // one stage's scale factors in TMEM
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+  static constexpr int ACC_COLS = 2 * BN;           // two accumulator buffers
+  static constexpr int SF_COLS = 16 + 16 * G;       // one stage's scale factors in TMEM
   // one scale-factor buffer per smem stage: a buffer is rewritten only after the stage's
   // empty barrier (committed behind the MMAs that read it) has completed
   static constexpr int TMEM_COLS_USED = ACC_COLS + STAGES * SF_COLS;
   static constexpr int TMEM_COLS = TMEM_COLS_USED <= 256 ? 256 : 512;
   static constexpr int THREADS = 320;               // 10 warps
   static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
-  static constexpr uint32_t TX_BYTES = A_BYTES + NB * B_BYTES;
+  static constexpr uint32_t TX_BYTES = A_BYTES + B_BYTES;
   static_assert(TMEM_COLS_USED <= 512, "TMEM budget");
+  static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
 };
 
 template <int BN, bool GATE_UP>
@@ -413,9 +437,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
   uint64_t* empty = full + C::STAGES;
-  uint64_t* acc_full = empty + C::STAGES;
-  uint64_t* acc_empty = acc_full + 1;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + 1);
+  uint64_t* acc_full = empty + C::STAGES;           // [2]
+  uint64_t* acc_empty = acc_full + 2;               // [2]
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -430,8 +454,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
       mbar_init(&full[s], 1 + 128);                  // TMA expect_tx + 128 scale threads
       mbar_init(&empty[s], 1);
     }
-    mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 4);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -454,7 +480,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
       int it = 0;
       for (int w = blockIdx.x; w < n_work && !*abort_flag; w += gridDim.x) {
         const int4 tile = tlist[w / args.n_tiles_n];
-        const int n0 = (w % args.n_tiles_n) * BN;
+        const int n0 = (w % args.n_tiles_n) * C::OUT_N;
         const int brow = tile.z * args.rows_per_expert + n0;
         for (int ks = 0; ks < k_stages; ++ks, ++it) {
           const int st = it % C::STAGES;
@@ -462,10 +488,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
           unsigned char* sb = smem + st * C::STAGE_BYTES;
           mbar_expect_tx(&full[st], C::TX_BYTES);
           tma_load_2d(sb, &tmap_a, ks * C::KB, tile.x, &full[st]);
-          tma_load_2d(sb + C::A_BYTES, &tmap_b, ks * C::KB, brow, &full[st]);
-          if (GATE_UP)
-            tma_load_2d(sb + C::A_BYTES + C::B_BYTES, &tmap_b, ks * C::KB, brow + args.F,
+          if (GATE_UP) {
+            tma_load_2d(sb + C::A_BYTES, &tmap_b, ks * C::KB, brow, &full[st]);
+            tma_load_2d(sb + C::A_BYTES + C::B_BYTES / 2, &tmap_b, ks * C::KB, brow + args.F,
                         &full[st]);
+          } else {
+            tma_load_2d(sb + C::A_BYTES, &tmap_b, ks * C::KB, brow, &full[st]);
+          }
         }
       }
       // drain: wait (bounded) until every issued stage has landed
@@ -486,8 +515,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
       constexpr uint32_t idesc = mxf4_idesc(128, BN);
       int it = 0, tcount = 0;
       for (int w = blockIdx.x; w < n_work && !*abort_flag; w += gridDim.x, ++tcount) {
-        if (!mbar_wait(acc_empty, (tcount & 1) ^ 1, abort_flag, args.err)) break;
+        const int ab = tcount & 1;
+        if (!mbar_wait(&acc_empty[ab], ((tcount >> 1) & 1) ^ 1, abort_flag, args.err)) break;
         tc_fence_after();
+        const uint32_t acc = acc_col + ab * BN;
         bool ok = true;
         for (int ks = 0; ks < k_stages; ++ks, ++it) {
           const int st = it % C::STAGES;
@@ -496,7 +527,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
           tc_fence_after();
           unsigned char* sb = smem + st * C::STAGE_BYTES;
           const uint32_t a_addr = smem_u32(sb);
-          const uint32_t sfa_smem = smem_u32(sb + C::A_BYTES + C::NB * C::B_BYTES);
+          const uint32_t b_addr = smem_u32(sb + C::A_BYTES);
+          const uint32_t sfa_smem = smem_u32(sb + C::A_BYTES + C::B_BYTES);
           const uint32_t sfb_smem = sfa_smem + C::SFA_BYTES;
           const uint32_t sfc = sf_col0 + st * C::SF_COLS;
           // scale factors: smem atoms -> TMEM (4 columns per 128-row atom)
@@ -504,26 +536,18 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
           for (int j = 0; j < 4; ++j)
             tc_cp_sf(sfc + 4 * j, smem_desc(sfa_smem + j * 512, 0, 128, 0));
 #pragma unroll
-          for (int b = 0; b < C::NB; ++b)
-#pragma unroll
-            for (int q = 0; q < 4 * C::G; ++q)
-              tc_cp_sf(sfc + 16 + b * 16 * C::G + 4 * q,
-                       smem_desc(sfb_smem + b * C::SFB_BYTES + q * 512, 0, 128, 0));
+          for (int q = 0; q < 4 * C::G; ++q)
+            tc_cp_sf(sfc + 16 + 4 * q, smem_desc(sfb_smem + q * 512, 0, 128, 0));
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const uint64_t adesc = smem_desc(a_addr + 32 * j, 16, 1024, 2);
-#pragma unroll
-            for (int b = 0; b < C::NB; ++b) {
-              const uint32_t b_addr = smem_u32(sb + C::A_BYTES + b * C::B_BYTES);
-              const uint64_t bdesc = smem_desc(b_addr + 32 * j, 16, 1024, 2);
-              tc_mma(acc_col + b * BN, adesc, bdesc, idesc, sfc + 4 * j,
-                     sfc + 16 + b * 16 * C::G + 4 * C::G * j, (ks | j) != 0);
-            }
+            const uint64_t bdesc = smem_desc(b_addr + 32 * j, 16, 1024, 2);
+            tc_mma(acc, adesc, bdesc, idesc, sfc + 4 * j, sfc + 16 + 4 * C::G * j, (ks | j) != 0);
           }
           tc_commit(&empty[st]);
         }
         if (!ok) break;
-        tc_commit(acc_full);
+        tc_commit(&acc_full[ab]);
       }
     }
   } else if (warp < 6) {
@@ -532,8 +556,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     int it = 0;
     for (int w = blockIdx.x; w < n_work && !*abort_flag; w += gridDim.x) {
       const int4 tile = tlist[w / args.n_tiles_n];
-      const int n0 = (w % args.n_tiles_n) * BN;
+      const int n0 = (w % args.n_tiles_n) * C::OUT_N;
       const int brow0 = tile.z * args.rows_per_expert + n0;
+      // the B rows this thread feeds: row n of the tile (gate_up: lower half gate, upper up)
+      const bool arow_ok = t < tile.y;
+      const uint8_t* asrc = args.a_scales + (size_t)(arow_ok ? tile.x + t : 0) * sfrow;
       bool ok = true;
       for (int ks = 0; ks < k_stages; ++ks, ++it) {
         const int st = it % C::STAGES;
@@ -541,32 +568,24 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
           ok = false;
           break;
         }
-        unsigned char* sfa = smem + st * C::STAGE_BYTES + C::A_BYTES + C::NB * C::B_BYTES;
+        unsigned char* sfa = smem + st * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES;
         unsigned char* sfb = sfa + C::SFA_BYTES;
-        {
-          const int m = t;                       // A row of the tile
-          const bool rv = m < tile.y;
-          const uint8_t* src = args.a_scales + (size_t)(rv ? tile.x + m : 0) * sfrow;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int byte = 16 * ks + 4 * j;
+          const bool v = arow_ok && byte < sfrow;
+          cp_async4(sfa + j * 512 + 16 * (t & 31) + 4 * (t >> 5), asrc + (v ? byte : 0), v);
+        }
+        for (int n = t; n < BN; n += 128) {
+          const int wrow = GATE_UP ? (n < BN / 2 ? brow0 + n : brow0 + args.F + n - BN / 2)
+                                   : brow0 + n;
+          const uint8_t* src = args.b_scales + (size_t)wrow * sfrow;
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const int byte = 16 * ks + 4 * j;
-            const bool v = rv && byte < sfrow;
-            cp_async4(sfa + j * 512 + 16 * (m & 31) + 4 * (m >> 5), src + (v ? byte : 0), v);
-          }
-        }
-#pragma unroll
-        for (int b = 0; b < C::NB; ++b) {
-          for (int n = t; n < BN; n += 128) {
-            const uint8_t* src = args.b_scales +
-                                 (size_t)(brow0 + (b ? args.F : 0) + n) * sfrow;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int byte = 16 * ks + 4 * j;
-              const bool v = byte < sfrow;
-              cp_async4(sfb + b * C::SFB_BYTES + (j * C::G + (n >> 7)) * 512 + 16 * (n & 31) +
-                            4 * ((n & 127) >> 5),
-                        src + (v ? byte : 0), v);
-            }
+            const bool v = byte < sfrow;
+            cp_async4(sfb + (j * C::G + (n >> 7)) * 512 + 16 * (n & 31) + 4 * ((n & 127) >> 5),
+                      src + (v ? byte : 0), v);
           }
         }
         cp_async_arrive(&full[st]);
@@ -578,39 +597,61 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     // ---------------- epilogue (warps 6..9 -> TMEM lane quarters 2,3,0,1) ----------------
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     int tcount = 0;
     for (int w = blockIdx.x; w < n_work && !*abort_flag; w += gridDim.x, ++tcount) {
+      const int ab = tcount & 1;
       const int4 tile = tlist[w / args.n_tiles_n];
-      const int n0 = (w % args.n_tiles_n) * BN;
-      if (!mbar_wait(acc_full, tcount & 1, abort_flag, args.err)) break;
-      tc_fence_after();
+      const int n0 = (w % args.n_tiles_n) * C::OUT_N;
       const bool valid = row < tile.y;
       const int pos = tile.x + row;
-      const int sx = valid ? args.a_exp[pos] : 0;
-      const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-      float* orow = args.out + (size_t)(valid ? pos : 0) * args.out_cols + n0;
+      const int sx = (GATE_UP && valid) ? args.a_exp[pos] : 0;
+      if (!mbar_wait(&acc_full[ab], (tcount >> 1) & 1, abort_flag, args.err)) break;
+      tc_fence_after();
+      const uint32_t acc = acc_col + ab * BN + lane_base;
+      if (GATE_UP) {
+        float* orow = reinterpret_cast<float*>(args.out) + (size_t)(valid ? pos : 0) * args.out_cols + n0;
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        float v[32];
-        tc_ld32(acc_col + lane_base + c * 32, v);
-        if (GATE_UP) {
-          float u[32];
-          tc_ld32(acc_col + lane_base + BN + c * 32, u);
+        for (int c = 0; c < BN / 64; ++c) {
+          float g[32], u[32];
+          tc_ld32(acc + c * 32, g);
+          tc_ld32(acc + BN / 2 + c * 32, u);
+          if (valid) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = silu_f(ldexpf(v[i], sx)) * ldexpf(u[i], sx);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = ldexpf(v[i], sx);
+            for (int i = 0; i < 32; i += 4) {
+              float4 o;
+              o.x = silu_f(ldexpf(g[i], sx)) * ldexpf(u[i], sx);
+              o.y = silu_f(ldexpf(g[i + 1], sx)) * ldexpf(u[i + 1], sx);
+              o.z = silu_f(ldexpf(g[i + 2], sx)) * ldexpf(u[i + 2], sx);
+              o.w = silu_f(ldexpf(g[i + 3], sx)) * ldexpf(u[i + 3], sx);
+              *reinterpret_cast<float4*>(orow + c * 32 + i) = o;
+            }
+          }
         }
-        if (valid) {
+      } else {
+        __half* orow = reinterpret_cast<__half*>(args.out) + (size_t)(valid ? pos : 0) * args.out_cols + n0;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tc_ld32(acc + c * 32, v);
+          if (valid) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4*>(orow + c * 32 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+            for (int i = 0; i < 32; i += 8) {
+              uint32_t pk[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const __half2 h2 = __floats2half2_rn(ldexpf(v[i + 2 * q], -args.down_shift),
+                                                     ldexpf(v[i + 2 * q + 1], -args.down_shift));
+                pk[q] = *reinterpret_cast<const uint32_t*>(&h2);
+              }
+              *reinterpret_cast<uint4*>(orow + c * 32 + i) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+          }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acc_empty);
+      if (lane == 0) mbar_arrive(&acc_empty[ab]);
     }
   }
 
@@ -622,6 +663,33 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "n"(C::TMEM_COLS) : "memory");
   }
+}
+
+// combine for the prefill path: y[t, :] = sum_j w[t, j] * f32(z16[pos_j, :]) * 2^(e_j + cF)
+__global__ void __launch_bounds__(256)
+combine_f16_kernel(const float* __restrict__ w, const int32_t* __restrict__ pair_pos,
+                   const __half* __restrict__ partial, const int32_t* __restrict__ hexp,
+                   int shift, int H, int k, float* __restrict__ y) {
+  const int t = blockIdx.y;
+  const int r = (blockIdx.x * blockDim.x + threadIdx.x) * 8;
+  if (r >= H) return;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int j = 0; j < k; ++j) {
+    const int pos = pair_pos[(size_t)t * k + j];
+    if (pos < 0) continue;
+    const float wj = ldexpf(w[(size_t)t * k + j], hexp[pos] + shift);
+    const uint4 z = *reinterpret_cast<const uint4*>(partial + (size_t)pos * H + r);
+    const uint32_t zz[4] = {z.x, z.y, z.z, z.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&zz[q]));
+      acc[2 * q] = fmaf(wj, f.x, acc[2 * q]);
+      acc[2 * q + 1] = fmaf(wj, f.y, acc[2 * q + 1]);
+    }
+  }
+  float4* out = reinterpret_cast<float4*>(y + (size_t)t * H + r);
+  out[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  out[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
 }
 
 // ---------------------------------------------------------------------------
@@ -686,7 +754,7 @@ cudaError_t launch_prefill_gate_up(const uint16_t* x_bf16, int T, int H, int F, 
                                    const moe_nvfp4_bank& b, moe_csr csr, const moe_ws_layout& L,
                                    char* ws, cudaStream_t s, bool* unsupported) {
   *unsupported = false;
-  if (H % 256 != 0 || (F % 128 != 0 && F != 64)) { *unsupported = true; return cudaSuccess; }
+  if (H % 256 != 0 || F % 64 != 0) { *unsupported = true; return cudaSuccess; }
   const int P = T * k;
   int32_t* tiles = reinterpret_cast<int32_t*>(ws + L.tiles);
   tiles_kernel<<<1, 1024, 0, s>>>(csr.expert_offsets, b.E, tiles);
@@ -700,14 +768,21 @@ cudaError_t launch_prefill_gate_up(const uint16_t* x_bf16, int T, int H, int F, 
                                               qc, qs, qe);
   if ((st = cudaGetLastError()) != cudaSuccess) return st;
   CUtensorMap ma, mb;
-  const int BN = (F % 128 == 0) ? 128 : 64;
+  constexpr int BN = 128;                           // 64 gate rows over 64 up rows
   if (!make_map(&ma, qc, H / 2, P, 128)) return cudaErrorInvalidValue;
-  if (!make_map(&mb, b.codes, H / 2, (uint64_t)b.E * 2 * F, BN)) return cudaErrorInvalidValue;
-  GemmArgs a{qs, qe, b.scales, tiles, reinterpret_cast<float*>(ws + L.h),
-             reinterpret_cast<uint32_t*>(ws + L.error_word), P, H, 2 * F, F / BN, F, F};
+  if (!make_map(&mb, b.codes, H / 2, (uint64_t)b.E * 2 * F, BN / 2)) return cudaErrorInvalidValue;
+  GemmArgs a{qs, qe, b.scales, tiles, ws + L.h, reinterpret_cast<uint32_t*>(ws + L.error_word),
+             P, H, 2 * F, F / (BN / 2), F, F, 0};
   const int max_tiles = P / 128 + (P < b.E ? P : b.E) + 1;
-  if (BN == 128) return run_gemm<128, true>(ma, mb, a, max_tiles, s);
-  return run_gemm<64, true>(ma, mb, a, max_tiles, s);
+  return run_gemm<BN, true>(ma, mb, a, max_tiles, s);
+}
+
+// Exponent c_F with F * 2688^2 * 2^-c_F < 2^15: the fixed shift of the f16 partials.
+int down_shift_for(int F) {
+  const double bound = (double)F * 2688.0 * 2688.0;
+  int c = 0;
+  while (std::ldexp(bound, -c) >= 32768.0) ++c;
+  return c;
 }
 
 cudaError_t launch_prefill_down(const moe_nvfp4_bank& b, moe_csr csr, int T, int H, int F, int k,
@@ -723,14 +798,25 @@ cudaError_t launch_prefill_down(const moe_nvfp4_bank& b, moe_csr csr, int T, int
                                               csr.expert_offsets, b.E, qc, qs, qe);
   cudaError_t st = cudaGetLastError();
   if (st != cudaSuccess) return st;
+  constexpr int BN = 128;
   CUtensorMap ma, mb;
   if (!make_map(&ma, qc, F / 2, P, 128)) return cudaErrorInvalidValue;
-  if (!make_map(&mb, b.codes, F / 2, (uint64_t)b.E * H, 256)) return cudaErrorInvalidValue;
-  GemmArgs a{qs, qe, b.scales, reinterpret_cast<const int32_t*>(ws + L.tiles),
-             reinterpret_cast<float*>(ws + L.partial),
-             reinterpret_cast<uint32_t*>(ws + L.error_word), P, F, H, H / 256, H, F};
+  if (!make_map(&mb, b.codes, F / 2, (uint64_t)b.E * H, BN)) return cudaErrorInvalidValue;
+  const int shift = down_shift_for(F);
+  GemmArgs a{qs, qe, b.scales, reinterpret_cast<const int32_t*>(ws + L.tiles), ws + L.partial,
+             reinterpret_cast<uint32_t*>(ws + L.error_word), P, F, H, H / BN, H, F, shift};
   const int max_tiles = P / 128 + (P < b.E ? P : b.E) + 1;
-  return run_gemm<256, false>(ma, mb, a, max_tiles, s);
+  return run_gemm<BN, false>(ma, mb, a, max_tiles, s);
+}
+
+cudaError_t launch_prefill_combine(const float* w, int T, int H, int F, int k,
+                                   const moe_ws_layout& L, char* ws, float* y, cudaStream_t s) {
+  dim3 grid((H / 8 + 255) / 256, T);
+  combine_f16_kernel<<<grid, 256, 0, s>>>(w, reinterpret_cast<const int32_t*>(ws + L.pair_pos),
+                                          reinterpret_cast<const __half*>(ws + L.partial),
+                                          reinterpret_cast<const int32_t*>(ws + L.qh_exp),
+                                          down_shift_for(F), H, k, y);
+  return cudaGetLastError();
 }
 
 }  // namespace moe

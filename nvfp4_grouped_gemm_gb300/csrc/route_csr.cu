@@ -107,16 +107,21 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* scratch, int* to
 }
 
 __global__ void __launch_bounds__(kCsrThreads, 1)
-build_csr_kernel(const int32_t* __restrict__ ids, int P, int E, int32_t* __restrict__ offsets,
+build_csr_kernel(const int32_t* __restrict__ ids_g, int P, int E, int32_t* __restrict__ offsets,
                  int32_t* __restrict__ pair_ids, int32_t* __restrict__ active,
                  int32_t* __restrict__ n_active, int32_t* __restrict__ pair_pos,
-                 uint32_t* __restrict__ err) {
+                 uint32_t* __restrict__ err, int ids_in_smem) {
   extern __shared__ int smem[];
   int* hist = smem;                           // [kCsrWarps][E]
   int* scratch = smem + kCsrWarps * E;        // [kCsrWarps]
+  int* ids_s = scratch + kCsrWarps;           // [P] when ids_in_smem
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int i = tid; i < kCsrWarps * E; i += kCsrThreads) hist[i] = 0;
+  // one coalesced pass over the ids; every later pass reads shared memory
+  if (ids_in_smem)
+    for (int p = tid; p < P; p += kCsrThreads) ids_s[p] = __ldg(ids_g + p);
   __syncthreads();
+  const int32_t* ids = ids_in_smem ? ids_s : ids_g;
 
   const int slice = (P + kCsrWarps - 1) / kCsrWarps;
   const int p_beg = min(P, warp * slice), p_end = min(P, p_beg + slice);
@@ -189,12 +194,15 @@ cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t*
 cudaError_t launch_build_csr(const int32_t* ids, int P, int k, int E, moe_csr csr,
                              int32_t* pair_pos, uint32_t* err, cudaStream_t s) {
   (void)k;
-  const size_t smem = (size_t)(kCsrWarps * E + kCsrWarps) * sizeof(int);
+  size_t smem = (size_t)(kCsrWarps * E + kCsrWarps) * sizeof(int);
+  const int ids_in_smem = smem + (size_t)P * sizeof(int) <= 200 * 1024 ? 1 : 0;
+  if (ids_in_smem) smem += (size_t)P * sizeof(int);
   cudaError_t st = cudaFuncSetAttribute(build_csr_kernel,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (st != cudaSuccess) return st;
   build_csr_kernel<<<1, kCsrThreads, smem, s>>>(ids, P, E, csr.expert_offsets, csr.pair_ids,
-                                                csr.active_experts, csr.n_active, pair_pos, err);
+                                                csr.active_experts, csr.n_active, pair_pos, err,
+                                                ids_in_smem);
   return cudaGetLastError();
 }
 

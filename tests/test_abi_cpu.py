@@ -58,7 +58,8 @@ def test_workspace_layout_host_logic(lib):
     Lp = moe.workspace_layout(4096, 4096, 640, 288, 8, moe.PATH_PREFILL)
     assert Lp["qx_codes"] > 0 and Lp["qh_codes"] > 0
     assert moe.workspace_bytes(0, H, F, E, k) == 0
-    assert moe.workspace_bytes(4, 100, F, E, k) == 0        # H % 128 != 0 unsupported
+    assert moe.workspace_bytes(4, 100, F, E, k) == 0        # H % 256 != 0 unsupported
+    assert moe.workspace_bytes(4, 8192, F, E, k) == 0       # H > 4096 unsupported
     assert moe.workspace_bytes(4, H, F, 8, 10) == 0         # k > E
 
 

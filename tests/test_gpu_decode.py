@@ -182,7 +182,7 @@ def test_csr_bit_exact_large(T, k, E):
     rng = np.random.default_rng(T + E)
     ids = synth.skewed_ids(rng, T, k, E)
     csr = moe.ExpertCSR(E, T * k)
-    ws = torch.zeros(moe.workspace_bytes(T, 128, 64, E, k, moe.PATH_DECODE), dtype=torch.uint8,
+    ws = torch.zeros(moe.workspace_bytes(T, 256, 64, E, k, moe.PATH_DECODE), dtype=torch.uint8,
                      device="cuda")
     moe.moe_build_expert_csr(torch.from_numpy(ids).cuda(), E, csr, ws)
     torch.cuda.synchronize()

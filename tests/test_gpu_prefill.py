@@ -166,3 +166,48 @@ def test_auto_path_switch():
     th = moe.prefill_min_pairs()
     assert moe.resolve_path(th // 8, 8) == moe.PATH_PREFILL
     assert moe.resolve_path(th // 8 - 1, 8) == moe.PATH_DECODE
+
+
+def _crafted_rows(H):
+    """Activation rows that sit exactly on Q's decision boundaries."""
+    rows = []
+    # block 0 sets sb = 448 at s = 0 (amax 2688); the rest hit every E2M1 midpoint exactly
+    r = np.zeros(H)
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]) * 448
+    r[0] = 2688.0
+    r[1:8] = mids
+    r[8:15] = -mids
+    r[15] = -0.0
+    # block 1: amax exactly on UE4M3 thresholds 3 * (v(j) + v(j+1)) for a few j
+    r[16] = 3.0 * (0.5 + 0.5625)          # between 0x30 and 0x31
+    r[17:32] = 0.1
+    r[32] = 3.0 * (0.015625 + 0.017578125)  # between 0x08 and 0x09
+    r[48] = 3.0 * (0.001953125 * 1 + 0.001953125 * 2)   # subnormal encodings 1 and 2
+    r[64:80] = 1e-30                        # far below the row scale: zero block scale
+    r[80:96] = -7.5e3                        # saturates against the row exponent
+    rows.append(r)
+    rows.append(np.zeros(H))                # all-zero row
+    rng = np.random.default_rng(5)
+    rows.append(rng.standard_normal(H) * 2.0 ** 40)
+    rows.append(rng.standard_normal(H) * 2.0 ** -40)
+    bits = synth.f32_to_bf16_bits(np.stack(rows).astype(np.float32))
+    return bits
+
+
+def test_quantiser_decision_boundaries():
+    base = synth.tiny(seed=2)
+    x_bits = _crafted_rows(base.H)
+    wl = synth.Workload("edges", 4, base.H, base.F, base.E, base.k, x_bits, base.gate_up,
+                        base.down, ids=np.array([[0, 1], [2, 3], [4, 5], [6, 7]], np.int32),
+                        weights=np.full((4, 2), 0.5, np.float32))
+    run = run_layer(wl, path=PF)
+    x = nvfp4.bf16_to_f64(x_bits)
+    cx, sx, ex = nvfp4.quantize(x)
+    P, H, k = wl.P, wl.H, wl.k
+    g_c = run.region("qx_codes", P * H // 2, np.uint8, (P, H // 2))
+    g_s = run.region("qx_scales", P * H // 16, np.uint8, (P, H // 16))
+    g_e = run.region("qx_exp", P * 4, np.int32, (P,))
+    p = np.arange(P)
+    assert np.array_equal(g_e[run.pair_pos[p]], ex[p // k])
+    assert np.array_equal(g_s[run.pair_pos[p]], sx[p // k])
+    assert np.array_equal(g_c[run.pair_pos[p]], cx[p // k])

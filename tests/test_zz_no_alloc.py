@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 def _csr_regular(ids, E):
     T, k = ids.shape
     csr = moe.ExpertCSR(E, T * k)
-    ws = torch.zeros(moe.workspace_bytes(T, 128, 64, E, k, moe.PATH_DECODE), dtype=torch.uint8,
+    ws = torch.zeros(moe.workspace_bytes(T, 256, 64, E, k, moe.PATH_DECODE), dtype=torch.uint8,
                      device="cuda")
     moe.moe_build_expert_csr(ids, E, csr, ws)
     return csr
