@@ -45,17 +45,20 @@ __device__ __forceinline__ void cp_async_commit_wait_all() {
 }
 
 // Dequantise one MMA step's A fragment for rows (g, g+8): code bytes 2S, 2S+1 of the lane's
-// 16-byte piece of each row.
+// 16-byte piece of each row.  The word holding them is converted whole (4 bytes, two
+// steps) by the caller; S selects the half.
 template <int S>
 __device__ __forceinline__ void a_frag(const uint4& r0, const uint4& r1, uint32_t sc0,
                                        uint32_t sc1, uint32_t (&a)[4]) {
   const uint32_t w0 = (S / 2 == 0) ? r0.x : (S / 2 == 1) ? r0.y : (S / 2 == 2) ? r0.z : r0.w;
   const uint32_t w1 = (S / 2 == 0) ? r1.x : (S / 2 == 1) ? r1.y : (S / 2 == 2) ? r1.z : r1.w;
-  const int sh = (S & 1) * 16;
-  a[0] = hmul2_u32(e2m1x2_to_f16x2(w0 >> sh), sc0);
-  a[1] = hmul2_u32(e2m1x2_to_f16x2(w1 >> sh), sc1);
-  a[2] = hmul2_u32(e2m1x2_to_f16x2(w0 >> (sh + 8)), sc0);
-  a[3] = hmul2_u32(e2m1x2_to_f16x2(w1 >> (sh + 8)), sc1);
+  uint32_t p0, p1, p2, p3, q0, q1, q2, q3;
+  e2m1x8_to_f16x2x4(w0, p0, p1, p2, p3);
+  e2m1x8_to_f16x2x4(w1, q0, q1, q2, q3);
+  a[0] = hmul2_u32((S & 1) ? p2 : p0, sc0);
+  a[1] = hmul2_u32((S & 1) ? q2 : q0, sc1);
+  a[2] = hmul2_u32((S & 1) ? p3 : p1, sc0);
+  a[3] = hmul2_u32((S & 1) ? q3 : q1, sc1);
 }
 
 // Same for 64-element k-blocks: bytes 2S, 2S+1 of the lane's 8-byte piece.
@@ -174,75 +177,93 @@ struct GateUpArgs {
   float* h;
 };
 
-// KMAX = ceil(H / 128 / 8): k-blocks per warp, their activation fragments held in registers.
+// Persistent: CTA c owns a contiguous range of work units u = (active expert, 16-row
+// block), ordered by expert.  Each unit's weight rows (16 gate + 16 up) land in one of two
+// shared buffers with 16-byte cp.async issued by every thread; the next unit's copy is in
+// flight while the current one is multiplied.  KMAX = ceil(H / 128 / 8): k-blocks per
+// warp, whose activation fragments stay in registers while the expert does not change.
 template <int KMAX>
-__global__ void __launch_bounds__(256, KMAX <= 2 ? 3 : 2) gate_up_kernel(const GateUpArgs args) {
+__global__ void __launch_bounds__(256, 2) gate_up_kernel(const GateUpArgs args) {
   extern __shared__ __align__(128) unsigned char smem[];
-  const int a_idx = blockIdx.y;
-  const bool live_cta = a_idx < *args.n_active;
   const int H = args.H, F = args.F;
-  const int e = live_cta ? args.active[a_idx] : 0;
-  const int i0 = blockIdx.x * 16;
   const int row_bytes = H / 2, srow = H / 16;
-  unsigned char* wc = smem;                               // [32][row_bytes] swizzled codes
-  unsigned char* ws = smem + 32 * row_bytes;              // [32][srow] scales
-  float* red = reinterpret_cast<float*>(ws + 32 * srow);  // [8 warps][32][8]
+  const int nrb = F / 16;
+  const int wbytes = (32 * row_bytes + 32 * srow + 127) & ~127;
+  float* red = reinterpret_cast<float*>(smem + 2 * wbytes);      // [8 warps][32][8]
+  const int n_units = *args.n_active * nrb;                        // CSR is complete
+  const int u_beg = (int)((long long)blockIdx.x * n_units / gridDim.x);
+  const int u_end = (int)((long long)(blockIdx.x + 1) * n_units / gridDim.x);
+  const size_t rows2F = (size_t)2 * F;
+  const int cpr = row_bytes / 16, spr = srow / 16;
 
-  if (live_cta) {
-    // every thread issues its share of the 16-byte copies: rows 0..15 gate, 16..31 up
-    const size_t rows2F = (size_t)2 * F;
-    const int cpr = row_bytes / 16;                          // chunks per code row
+  auto issue = [&](int u, int buf) {
+    const int e = args.active[u / nrb];
+    const int i0 = (u % nrb) * 16;
+    unsigned char* wc = smem + buf * wbytes;
+    unsigned char* ws = wc + 32 * row_bytes;
     for (int idx = threadIdx.x; idx < 32 * cpr; idx += 256) {
       const int r = idx / cpr, q = idx - r * cpr;
       const size_t wrow = (size_t)e * rows2F + (r < 16 ? i0 + r : F + i0 + r - 16);
       cp_async16(wc + wchunk(r, q, row_bytes, true), args.codes + wrow * row_bytes + q * 16);
     }
-    const int spr = srow / 16;
     for (int idx = threadIdx.x; idx < 32 * spr; idx += 256) {
       const int r = idx / spr, q = idx - r * spr;
       const size_t wrow = (size_t)e * rows2F + (r < 16 ? i0 + r : F + i0 + r - 16);
       cp_async16(ws + r * srow + q * 16, args.scales + wrow * srow + q * 16);
     }
-  }
-  pdl_wait();                         // the gathered activations are complete
-  if (!live_cta) return;
-  const int off = args.offsets[e];
-  const int m = args.offsets[e + 1] - off;
+  };
+
+  if (u_beg < u_end) issue(u_beg, 0);
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  pdl_wait();                                   // the gathered activations are complete
+
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
   const int nkb = H / 128;
   const int kb_beg = warp * nkb / 8, kb_end = (warp + 1) * nkb / 8;
-  cp_async_commit_wait_all();
-  __syncthreads();
+  uint4 xb[KMAX][4];
+  int cur_e = -1, cur_t0 = -1;
 
-  for (int tok0 = 0; tok0 < m; tok0 += 8) {
-    const int live = min(8, m - tok0);
-    // activation fragments of this warp's k-blocks, all requested up front
-    uint4 xb[KMAX][4];
-    const __half* xrow = args.xg + (size_t)(off + tok0 + g) * H + 32 * c;
+  for (int u = u_beg, i = 0; u < u_end; ++u, ++i) {
+    if (u + 1 < u_end) issue(u + 1, (i + 1) & 1);
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 1;" ::: "memory");
+    __syncthreads();
+    const unsigned char* wc = smem + (i & 1) * wbytes;
+    const unsigned char* ws = wc + 32 * row_bytes;
+    const int e = args.active[u / nrb];
+    const int i0 = (u % nrb) * 16;
+    const int off = args.offsets[e];
+    const int m = args.offsets[e + 1] - off;
+    for (int tok0 = 0; tok0 < m; tok0 += 8) {
+      const int live = min(8, m - tok0);
+      if (e != cur_e || tok0 != cur_t0) {
+        const __half* xrow = args.xg + (size_t)(off + tok0 + g) * H + 32 * c;
 #pragma unroll
-    for (int j = 0; j < KMAX; ++j)
+        for (int j = 0; j < KMAX; ++j)
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int kb = kb_beg + j;
-        xb[j][u] = (g < live && kb < kb_end)
-                       ? __ldg(reinterpret_cast<const uint4*>(xrow + kb * 128 + 8 * u))
-                       : make_uint4(0, 0, 0, 0);
+          for (int q = 0; q < 4; ++q) {
+            const int kb = kb_beg + j;
+            xb[j][q] = (g < live && kb < kb_end)
+                           ? __ldg(reinterpret_cast<const uint4*>(xrow + kb * 128 + 8 * q))
+                           : make_uint4(0, 0, 0, 0);
+          }
+        cur_e = e;
+        cur_t0 = tok0;
       }
-    float accg[4] = {0.f, 0.f, 0.f, 0.f}, accu[4] = {0.f, 0.f, 0.f, 0.f};
+      float accg[4] = {0.f, 0.f, 0.f, 0.f}, accu[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int j = 0; j < KMAX; ++j) {
-      const int kb = kb_beg + j;
-      if (kb < kb_end) {
-      const uint4 c0 = *reinterpret_cast<const uint4*>(wc + wchunk(g, kb * 4 + c, row_bytes, true));
-      const uint4 c1 = *reinterpret_cast<const uint4*>(wc + wchunk(g + 8, kb * 4 + c, row_bytes, true));
-      const uint4 c2 = *reinterpret_cast<const uint4*>(wc + wchunk(g + 16, kb * 4 + c, row_bytes, true));
-      const uint4 c3 = *reinterpret_cast<const uint4*>(wc + wchunk(g + 24, kb * 4 + c, row_bytes, true));
-      const unsigned char* sp = ws + g * srow + kb * 8 + 2 * c;
-      const uint32_t f0 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sp));
-      const uint32_t f1 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sp + 8 * srow));
-      const uint32_t f2 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sp + 16 * srow));
-      const uint32_t f3 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sp + 24 * srow));
+      for (int j = 0; j < KMAX; ++j) {
+        const int kb = kb_beg + j;
+        if (kb < kb_end) {
+          const uint4 c0 = *reinterpret_cast<const uint4*>(wc + wchunk(g, kb * 4 + c, row_bytes, true));
+          const uint4 c1 = *reinterpret_cast<const uint4*>(wc + wchunk(g + 8, kb * 4 + c, row_bytes, true));
+          const uint4 c2 = *reinterpret_cast<const uint4*>(wc + wchunk(g + 16, kb * 4 + c, row_bytes, true));
+          const uint4 c3 = *reinterpret_cast<const uint4*>(wc + wchunk(g + 24, kb * 4 + c, row_bytes, true));
+          const unsigned char* sp = ws + g * srow + kb * 8 + 2 * c;
+          const uint32_t f0 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sp));
+          const uint32_t f1 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sp + 8 * srow));
+          const uint32_t f2 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sp + 16 * srow));
+          const uint32_t f3 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sp + 24 * srow));
 #define MOE_GU_STEP(S)                                                                     \
   {                                                                                        \
     uint32_t ag[4], au[4];                                                                 \
@@ -255,36 +276,38 @@ __global__ void __launch_bounds__(256, KMAX <= 2 ? 3 : 2) gate_up_kernel(const G
     mma_f16_16816(accg, ag[0], ag[1], ag[2], ag[3], b0, b1);                               \
     mma_f16_16816(accu, au[0], au[1], au[2], au[3], b0, b1);                               \
   }
-      MOE_GU_STEP(0) MOE_GU_STEP(1) MOE_GU_STEP(2) MOE_GU_STEP(3)
-      MOE_GU_STEP(4) MOE_GU_STEP(5) MOE_GU_STEP(6) MOE_GU_STEP(7)
+          MOE_GU_STEP(0) MOE_GU_STEP(1) MOE_GU_STEP(2) MOE_GU_STEP(3)
+          MOE_GU_STEP(4) MOE_GU_STEP(5) MOE_GU_STEP(6) MOE_GU_STEP(7)
 #undef MOE_GU_STEP
-      }
-    }
-    // fixed-order sum over the 8 warps' k ranges
-    float* mine = red + (warp * 32 + lane) * 8;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) { mine[q] = accg[q]; mine[4 + q] = accu[q]; }
-    __syncthreads();
-    if (warp == 0) {
-      float sg[4] = {0.f, 0.f, 0.f, 0.f}, su[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int w = 0; w < 8; ++w) {
-        const float* src = red + (w * 32 + lane) * 8;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) { sg[q] += src[q]; su[q] += src[4 + q]; }
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int n = 2 * c + (q & 1);
-        const int i = i0 + g + 8 * (q >> 1);
-        if (n < live) {
-          const int ex = args.xe[off + tok0 + n];
-          args.h[(size_t)(off + tok0 + n) * F + i] =
-              silu_f(ldexpf(sg[q], ex)) * ldexpf(su[q], ex);
         }
       }
+      // fixed-order sum over the 8 warps' k ranges
+      float* mine = red + (warp * 32 + lane) * 8;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) { mine[q] = accg[q]; mine[4 + q] = accu[q]; }
+      __syncthreads();
+      if (warp == 0) {
+        float sg[4] = {0.f, 0.f, 0.f, 0.f}, su[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int w = 0; w < 8; ++w) {
+          const float* src = red + (w * 32 + lane) * 8;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) { sg[q] += src[q]; su[q] += src[4 + q]; }
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int n = 2 * c + (q & 1);
+          const int ii = i0 + g + 8 * (q >> 1);
+          if (n < live) {
+            const int ex = args.xe[off + tok0 + n];
+            args.h[(size_t)(off + tok0 + n) * F + ii] =
+                silu_f(ldexpf(sg[q], ex)) * ldexpf(su[q], ex);
+          }
+        }
+      }
+      __syncthreads();
     }
-    __syncthreads();
   }
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -302,24 +325,29 @@ struct DownArgs {
   float* partial;
 };
 
+// Persistent like the gate/up kernel: unit = (active expert, 128 output rows), two weight
+// buffers, the expert's h rows staged once while the expert does not change.
 // KB = 128 (16-byte lane pieces) when F % 128 == 0, else 64 (8-byte pieces).
 template <int KB>
-__global__ void __launch_bounds__(256, 3) down_kernel(const DownArgs args) {
+__global__ void __launch_bounds__(256, 2) down_kernel(const DownArgs args) {
   extern __shared__ __align__(128) unsigned char smem[];
-  const int a_idx = blockIdx.y;
-  const bool live_cta = a_idx < *args.n_active;
   const int H = args.H, F = args.F;
-  const int e = live_cta ? args.active[a_idx] : 0;
-  const int r0 = blockIdx.x * 128;
+  const int nrb = H / 128;
   const int row_bytes = F / 2, srow = F / 16;
   const bool swz = (row_bytes % 128) == 0;
-  unsigned char* wc = smem;                                // [128][row_bytes]
-  unsigned char* ws = smem + 128 * row_bytes;              // [128][srow]
+  const int wbytes = (128 * row_bytes + 128 * srow + 127) & ~127;
   const int hrow_bytes = F * 2 + 16;
-  unsigned char* hs = ws + ((128 * srow + 15) & ~15);      // [8][hrow_bytes]
+  unsigned char* hs = smem + 2 * wbytes;                            // [8][hrow_bytes]
+  const int n_units = *args.n_active * nrb;
+  const int u_beg = (int)((long long)blockIdx.x * n_units / gridDim.x);
+  const int u_end = (int)((long long)(blockIdx.x + 1) * n_units / gridDim.x);
+  const int cpr = row_bytes / 16;
 
-  if (live_cta) {
-    const int cpr = row_bytes / 16;
+  auto issue = [&](int u, int buf) {
+    const int e = args.active[u / nrb];
+    const int r0 = (u % nrb) * 128;
+    unsigned char* wc = smem + buf * wbytes;
+    unsigned char* ws = wc + 128 * row_bytes;
     const unsigned char* src = args.codes + ((size_t)e * H + r0) * row_bytes;
     for (int idx = threadIdx.x; idx < 128 * cpr; idx += 256) {
       const int r = idx / cpr, q = idx - r * cpr;
@@ -328,38 +356,59 @@ __global__ void __launch_bounds__(256, 3) down_kernel(const DownArgs args) {
     const unsigned char* ssrc = args.scales + ((size_t)e * H + r0) * srow;
     for (int idx = threadIdx.x; idx < 128 * srow / 16; idx += 256)
       cp_async16(ws + idx * 16, ssrc + idx * 16);
-  }
-  pdl_wait();                         // h in f16 is complete
-  if (!live_cta) return;
-  const int off = args.offsets[e];
-  const int m = args.offsets[e + 1] - off;
+  };
+
+  if (u_beg < u_end) issue(u_beg, 0);
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  pdl_wait();                                   // h in f16 is complete
+
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
   const int nkb = F / KB;
   constexpr int LB = KB / 8;          // code bytes per lane per k-block
+  int cur_e = -1, cur_t0 = -1;
 
-  for (int tok0 = 0; tok0 < m; tok0 += 8) {
-    const int live = min(8, m - tok0);
-    for (int idx = threadIdx.x; idx < live * (F / 8); idx += 256) {
-      const int slot = idx / (F / 8), ch = idx - slot * (F / 8);
-      cp_async16(hs + slot * hrow_bytes + swz_chunk(ch),
-                 args.hg + (size_t)(off + tok0 + slot) * F + ch * 8);
-    }
-    cp_async_commit_wait_all();
-    __syncthreads();
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    const int rw = warp * 16 + g;
-    for (int kb = 0; kb < nkb; ++kb) {
-      if (KB == 128) {
-        const uint4 a0 = *reinterpret_cast<const uint4*>(wc + wchunk(rw, kb * 4 + c, row_bytes, swz));
-        const uint4 a1 = *reinterpret_cast<const uint4*>(wc + wchunk(rw + 8, kb * 4 + c, row_bytes, swz));
-        const unsigned char* sp = ws + rw * srow + kb * 8 + 2 * c;
-        const uint32_t f0 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sp));
-        const uint32_t f1 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sp + 8 * srow));
-        uint4 xb[4];
+  for (int u = u_beg, i = 0; u < u_end; ++u, ++i) {
+    const int e = args.active[u / nrb];
+    const int r0 = (u % nrb) * 128;
+    const int off = args.offsets[e];
+    const int m = args.offsets[e + 1] - off;
+    const unsigned char* wc = smem + (i & 1) * wbytes;
+    const unsigned char* ws = wc + 128 * row_bytes;
+    for (int tok0 = 0; tok0 < m; tok0 += 8) {
+      const int live = min(8, m - tok0);
+      // stage the expert's h rows (copy group committed before the next unit's weights)
+      if (e != cur_e || tok0 != cur_t0) {
+        for (int idx = threadIdx.x; idx < live * (F / 8); idx += 256) {
+          const int slot = idx / (F / 8), ch = idx - slot * (F / 8);
+          cp_async16(hs + slot * hrow_bytes + swz_chunk(ch),
+                     args.hg + (size_t)(off + tok0 + slot) * F + ch * 8);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        cur_e = e;
+        cur_t0 = tok0;
+      }
+      if (tok0 == 0) {
+        // prefetch the next unit, then wait for everything but that prefetch
+        if (u + 1 < u_end) issue(u + 1, (i + 1) & 1);
+        asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 1;" ::: "memory");
+      } else {
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+      }
+      __syncthreads();
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      const int rw = warp * 16 + g;
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (KB == 128) {
+          const uint4 a0 = *reinterpret_cast<const uint4*>(wc + wchunk(rw, kb * 4 + c, row_bytes, swz));
+          const uint4 a1 = *reinterpret_cast<const uint4*>(wc + wchunk(rw + 8, kb * 4 + c, row_bytes, swz));
+          const unsigned char* sp = ws + rw * srow + kb * 8 + 2 * c;
+          const uint32_t f0 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sp));
+          const uint32_t f1 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sp + 8 * srow));
+          uint4 xb[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          xb[q] = *reinterpret_cast<const uint4*>(hs + g * hrow_bytes + swz_chunk(kb * 16 + 4 * c + q));
+          for (int q = 0; q < 4; ++q)
+            xb[q] = *reinterpret_cast<const uint4*>(hs + g * hrow_bytes + swz_chunk(kb * 16 + 4 * c + q));
 #define MOE_DN_STEP(S)                                                                     \
   {                                                                                        \
     uint32_t af[4];                                                                        \
@@ -368,20 +417,20 @@ __global__ void __launch_bounds__(256, 3) down_kernel(const DownArgs args) {
     mma_f16_16816(acc, af[0], af[1], af[2], af[3], (S & 1) ? xb[S / 2].z : xb[S / 2].x,     \
                   (S & 1) ? xb[S / 2].w : xb[S / 2].y);                                    \
   }
-        MOE_DN_STEP(0) MOE_DN_STEP(1) MOE_DN_STEP(2) MOE_DN_STEP(3)
-        MOE_DN_STEP(4) MOE_DN_STEP(5) MOE_DN_STEP(6) MOE_DN_STEP(7)
+          MOE_DN_STEP(0) MOE_DN_STEP(1) MOE_DN_STEP(2) MOE_DN_STEP(3)
+          MOE_DN_STEP(4) MOE_DN_STEP(5) MOE_DN_STEP(6) MOE_DN_STEP(7)
 #undef MOE_DN_STEP
-      } else {
-        const unsigned char* rp = wc + rw * row_bytes + LB * c + kb * 32;
-        const uint2 a0 = *reinterpret_cast<const uint2*>(rp);
-        const uint2 a1 = *reinterpret_cast<const uint2*>(rp + 8 * row_bytes);
-        const unsigned char* sp = ws + rw * srow + kb * 4 + c;
-        const uint32_t f0 = bcast_lo(e4m3x2_to_f16x2(sp[0]));
-        const uint32_t f1 = bcast_lo(e4m3x2_to_f16x2(sp[8 * srow]));
-        uint4 xb[2];
+        } else {
+          const unsigned char* rp = wc + rw * row_bytes + LB * c + kb * 32;
+          const uint2 a0 = *reinterpret_cast<const uint2*>(rp);
+          const uint2 a1 = *reinterpret_cast<const uint2*>(rp + 8 * row_bytes);
+          const unsigned char* sp = ws + rw * srow + kb * 4 + c;
+          const uint32_t f0 = bcast_lo(e4m3x2_to_f16x2(sp[0]));
+          const uint32_t f1 = bcast_lo(e4m3x2_to_f16x2(sp[8 * srow]));
+          uint4 xb[2];
 #pragma unroll
-        for (int q = 0; q < 2; ++q)
-          xb[q] = *reinterpret_cast<const uint4*>(hs + g * hrow_bytes + swz_chunk(kb * 8 + 2 * c + q));
+          for (int q = 0; q < 2; ++q)
+            xb[q] = *reinterpret_cast<const uint4*>(hs + g * hrow_bytes + swz_chunk(kb * 8 + 2 * c + q));
 #define MOE_DN64_STEP(S)                                                                   \
   {                                                                                        \
     uint32_t af[4];                                                                        \
@@ -389,19 +438,21 @@ __global__ void __launch_bounds__(256, 3) down_kernel(const DownArgs args) {
     mma_f16_16816(acc, af[0], af[1], af[2], af[3], (S & 1) ? xb[S / 2].z : xb[S / 2].x,     \
                   (S & 1) ? xb[S / 2].w : xb[S / 2].y);                                    \
   }
-        MOE_DN64_STEP(0) MOE_DN64_STEP(1) MOE_DN64_STEP(2) MOE_DN64_STEP(3)
+          MOE_DN64_STEP(0) MOE_DN64_STEP(1) MOE_DN64_STEP(2) MOE_DN64_STEP(3)
 #undef MOE_DN64_STEP
+        }
       }
-    }
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int n = 2 * c + (q & 1);
-      const int r = r0 + rw + 8 * (q >> 1);
-      if (n < live)
-        args.partial[(size_t)(off + tok0 + n) * H + r] = ldexpf(acc[q], args.he[off + tok0 + n]);
+      for (int q = 0; q < 4; ++q) {
+        const int n = 2 * c + (q & 1);
+        const int r = r0 + rw + 8 * (q >> 1);
+        if (n < live)
+          args.partial[(size_t)(off + tok0 + n) * H + r] = ldexpf(acc[q], args.he[off + tok0 + n]);
+      }
+      __syncthreads();
     }
-    __syncthreads();
   }
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -428,20 +479,15 @@ combine_kernel(const float* __restrict__ w, const int32_t* __restrict__ pair_pos
   *reinterpret_cast<float4*>(y + (size_t)t * H + r) = acc;
 }
 
-template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                       Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, args...);
+int sm_count() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
 }
 
 }  // namespace
@@ -460,13 +506,16 @@ cudaError_t launch_decode_gate_up(const uint16_t* x_bf16, int T, int H, int F, i
   if (st != cudaSuccess) return st;
   GateUpArgs a{xg, xe, b.codes, b.scales, H, F, csr.expert_offsets, csr.active_experts,
                csr.n_active, reinterpret_cast<float*>(ws + L.h)};
-  const int max_active = P < b.E ? P : b.E;
-  const size_t smem = 32 * (size_t)(H / 2) + 32 * (size_t)(H / 16) + 8 * 32 * 8 * sizeof(float);
+  const long long max_units = (long long)(P < b.E ? P : b.E) * (F / 16);
+  const size_t wbytes = (32 * (size_t)(H / 2) + 32 * (size_t)(H / 16) + 127) & ~size_t(127);
+  const size_t smem = 2 * wbytes + 8 * 32 * 8 * sizeof(float);
   auto kern = kmax <= 1 ? gate_up_kernel<1> : kmax == 2 ? gate_up_kernel<2>
                                              : kmax == 3 ? gate_up_kernel<3> : gate_up_kernel<4>;
   st = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (st != cudaSuccess) return st;
-  return launch_pdl(kern, dim3(F / 16, max_active), dim3(256), smem, s, a);
+  long long grid = 2LL * sm_count();
+  if (grid > max_units) grid = max_units;
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(256), smem, s, a);
 }
 
 cudaError_t launch_decode_down(const moe_nvfp4_bank& b, moe_csr csr, int T, int H, int F, int k,
@@ -480,18 +529,15 @@ cudaError_t launch_decode_down(const moe_nvfp4_bank& b, moe_csr csr, int T, int 
   if (st != cudaSuccess) return st;
   DownArgs a{hg, he, b.codes, b.scales, H, F, csr.expert_offsets, csr.active_experts,
              csr.n_active, reinterpret_cast<float*>(ws + L.partial)};
-  const int max_active = P < b.E ? P : b.E;
-  const size_t smem = 128 * (size_t)(F / 2) + ((128 * (size_t)(F / 16) + 15) & ~size_t(15)) +
-                      8 * (size_t)(F * 2 + 16);
-  if (F % 128 == 0) {
-    st = cudaFuncSetAttribute(down_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)smem);
-    if (st != cudaSuccess) return st;
-    return launch_pdl(down_kernel<128>, dim3(H / 128, max_active), dim3(256), smem, s, a);
-  }
-  st = cudaFuncSetAttribute(down_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const long long max_units = (long long)(P < b.E ? P : b.E) * (H / 128);
+  const size_t wbytes = (128 * (size_t)(F / 2) + 128 * (size_t)(F / 16) + 127) & ~size_t(127);
+  const size_t smem = 2 * wbytes + 8 * (size_t)(F * 2 + 16);
+  long long grid = 2LL * sm_count();
+  if (grid > max_units) grid = max_units;
+  auto kern = (F % 128 == 0) ? down_kernel<128> : down_kernel<64>;
+  st = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (st != cudaSuccess) return st;
-  return launch_pdl(down_kernel<64>, dim3(H / 128, max_active), dim3(256), smem, s, a);
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(256), smem, s, a);
 }
 
 cudaError_t launch_combine(const float* w, int T, int H, int k, const moe_ws_layout& L, char* ws,

@@ -407,7 +407,7 @@ struct Cfg {
   static constexpr int BM = 128;
   static constexpr int KB = 128;                    // bytes of K per stage (256 elements)
   static constexpr int G = (BN + 127) / 128;        // 128-row scale-factor atoms per B tile
-  static constexpr int STAGES = 4;
+  static constexpr int STAGES = 5;
   static constexpr int OUT_N = GATE_UP ? BN / 2 : BN;   // output columns per tile
   static constexpr int A_BYTES = BM * KB;
   static constexpr int B_BYTES = BN * KB;
@@ -552,47 +552,67 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     }
   } else if (warp < 6) {
     // ---------------- scale-factor loaders (128 threads) ----------------
+    // Thread t feeds A row t and B row t of every stage: 16 scale bytes each (the 4
+    // k-steps of the stage), loaded SFD stages ahead into registers and scattered into
+    // the 32x16-byte atoms once the stage's smem is free.
     const int t = threadIdx.x - 64;
-    int it = 0;
-    for (int w = blockIdx.x; w < n_work && !*abort_flag; w += gridDim.x) {
+    constexpr int SFD = 3;
+    const int n_it = ((n_work - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x) * k_stages;
+    auto load_sf = [&](int it2, uint4& va, uint4& vb) {
+      va = make_uint4(0, 0, 0, 0);
+      vb = make_uint4(0, 0, 0, 0);
+      if (it2 >= n_it) return;
+      const int w = blockIdx.x + (it2 / k_stages) * gridDim.x;
+      const int ks = it2 % k_stages;
       const int4 tile = tlist[w / args.n_tiles_n];
       const int n0 = (w % args.n_tiles_n) * C::OUT_N;
       const int brow0 = tile.z * args.rows_per_expert + n0;
-      // the B rows this thread feeds: row n of the tile (gate_up: lower half gate, upper up)
-      const bool arow_ok = t < tile.y;
-      const uint8_t* asrc = args.a_scales + (size_t)(arow_ok ? tile.x + t : 0) * sfrow;
-      bool ok = true;
-      for (int ks = 0; ks < k_stages; ++ks, ++it) {
-        const int st = it % C::STAGES;
-        if (!mbar_wait(&empty[st], ((it / C::STAGES) & 1) ^ 1, abort_flag, args.err)) {
-          ok = false;
-          break;
-        }
-        unsigned char* sfa = smem + st * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES;
-        unsigned char* sfb = sfa + C::SFA_BYTES;
+      const int byte0 = 16 * ks;
+      uint32_t a[4] = {0, 0, 0, 0}, b[4] = {0, 0, 0, 0};
+      if (t < tile.y) {
+        const uint8_t* src = args.a_scales + (size_t)(tile.x + t) * sfrow + byte0;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int byte = 16 * ks + 4 * j;
-          const bool v = arow_ok && byte < sfrow;
-          cp_async4(sfa + j * 512 + 16 * (t & 31) + 4 * (t >> 5), asrc + (v ? byte : 0), v);
-        }
-        for (int n = t; n < BN; n += 128) {
-          const int wrow = GATE_UP ? (n < BN / 2 ? brow0 + n : brow0 + args.F + n - BN / 2)
-                                   : brow0 + n;
-          const uint8_t* src = args.b_scales + (size_t)wrow * sfrow;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int byte = 16 * ks + 4 * j;
-            const bool v = byte < sfrow;
-            cp_async4(sfb + (j * C::G + (n >> 7)) * 512 + 16 * (n & 31) + 4 * ((n & 127) >> 5),
-                      src + (v ? byte : 0), v);
-          }
-        }
-        cp_async_arrive(&full[st]);
+        for (int j = 0; j < 4; ++j)
+          if (byte0 + 4 * j < sfrow) a[j] = __ldg(reinterpret_cast<const uint32_t*>(src + 4 * j));
       }
-      if (!ok) break;
+      if (t < BN) {
+        const int wrow = GATE_UP ? (t < BN / 2 ? brow0 + t : brow0 + args.F + t - BN / 2)
+                                 : brow0 + t;
+        const uint8_t* src = args.b_scales + (size_t)wrow * sfrow + byte0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (byte0 + 4 * j < sfrow) b[j] = __ldg(reinterpret_cast<const uint32_t*>(src + 4 * j));
+      }
+      va = make_uint4(a[0], a[1], a[2], a[3]);
+      vb = make_uint4(b[0], b[1], b[2], b[3]);
+    };
+    uint4 ra[SFD], rb[SFD];
+#pragma unroll
+    for (int d = 0; d < SFD; ++d) load_sf(d, ra[d], rb[d]);
+    for (int it = 0; it < n_it && !*abort_flag; ++it) {
+      const int st = it % C::STAGES;
+      const uint4 va = ra[0], vb = rb[0];
+#pragma unroll
+      for (int d = 0; d < SFD - 1; ++d) { ra[d] = ra[d + 1]; rb[d] = rb[d + 1]; }
+      load_sf(it + SFD, ra[SFD - 1], rb[SFD - 1]);
+      if (!mbar_wait(&empty[st], ((it / C::STAGES) & 1) ^ 1, abort_flag, args.err)) break;
+      uint32_t* sfa = reinterpret_cast<uint32_t*>(smem + st * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES);
+      uint32_t* sfb = sfa + C::SFA_BYTES / 4;
+      const int ai = 4 * (t & 31) + (t >> 5);          // u32 index of row t inside an atom
+      sfa[0 * 128 + ai] = va.x;
+      sfa[1 * 128 + ai] = va.y;
+      sfa[2 * 128 + ai] = va.z;
+      sfa[3 * 128 + ai] = va.w;
+      if (t < BN) {
+        sfb[(0 * C::G + (t >> 7)) * 128 + ai] = vb.x;
+        sfb[(1 * C::G + (t >> 7)) * 128 + ai] = vb.y;
+        sfb[(2 * C::G + (t >> 7)) * 128 + ai] = vb.z;
+        sfb[(3 * C::G + (t >> 7)) * 128 + ai] = vb.w;
+      }
+      // make the generic-proxy stores visible to tcgen05.cp, then arrive
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive(&full[st]);
     }
-    asm volatile("cp.async.wait_all;" ::: "memory");
   } else {
     // ---------------- epilogue (warps 6..9 -> TMEM lane quarters 2,3,0,1) ----------------
     const int quarter = warp & 3;

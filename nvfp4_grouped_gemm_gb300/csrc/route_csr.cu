@@ -23,21 +23,38 @@ __device__ __forceinline__ bool before(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
 }
 
-constexpr int kRouteMaxPerLane = kMaxE / 32;
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
-__global__ void route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
-                                  int32_t* __restrict__ ids, float* __restrict__ w) {
-  const int warps = blockDim.x / 32;
-  const int t = blockIdx.x * warps + threadIdx.x / 32;
+constexpr int kRouteWarps = 8;
+constexpr int kNone = 0x7fffffff;   // id of an empty candidate
+
+// a beats b: a is a candidate and either b is empty or a comes first in (logit desc, id asc)
+__device__ __forceinline__ bool beats(float av, int ai, float bv, int bi) {
+  return ai != kNone && (bi == kNone || before(av, ai, bv, bi));
+}
+
+// One warp per token; lane l holds experts l, l+32, ... (PL per lane, padded with empty
+// slots).  Round r picks the best candidate ordered strictly after round r-1's pick by a
+// tree over the lane's slots and a butterfly over the warp, so the dependency chain per
+// round is log2(PL) + 5 comparisons deep.
+template <int PL>
+__global__ void __launch_bounds__(kRouteWarps * 32)
+route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
+                  int32_t* __restrict__ ids, float* __restrict__ w) {
+  pdl_wait();
+  pdl_trigger();
+  const int t = blockIdx.x * kRouteWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
   const float* row = logits + (size_t)t * E;
-  // the token's logits, once, in registers: lane holds experts lane, lane+32, ...
-  float v[kRouteMaxPerLane];
+  float v[PL];
 #pragma unroll
-  for (int i = 0; i < kRouteMaxPerLane; ++i) {
+  for (int i = 0; i < PL; ++i) {
     const int e = lane + 32 * i;
-    v[i] = e < E ? __ldg(row + e) : -INFINITY;
+    v[i] = e < E ? __ldg(row + e) : 0.0f;
   }
   float prev_v = 0.0f;
   int prev_i = -1;
@@ -45,21 +62,27 @@ __global__ void route_topk_kernel(const float* __restrict__ logits, int T, int E
   float my_val = 0.0f;   // lane j < k keeps the j-th selected logit
   int my_id = 0;
   for (int r = 0; r < k; ++r) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
+    float cv[PL];
+    int ci[PL];
 #pragma unroll
-    for (int i = 0; i < kRouteMaxPerLane; ++i) {
+    for (int i = 0; i < PL; ++i) {
       const int e = lane + 32 * i;
-      if (e < E) {
-        const bool eligible = (prev_i < 0) || before(prev_v, prev_i, v[i], e);
-        if (eligible && (bi == 0x7fffffff || before(v[i], e, bv, bi))) { bv = v[i]; bi = e; }
-      }
+      const bool ok = e < E && (prev_i < 0 || before(prev_v, prev_i, v[i], e));
+      cv[i] = v[i];
+      ci[i] = ok ? e : kNone;
     }
+#pragma unroll
+    for (int s = PL / 2; s >= 1; s >>= 1)
+#pragma unroll
+      for (int i = 0; i < s; ++i)
+        if (beats(cv[i + s], ci[i + s], cv[i], ci[i])) { cv[i] = cv[i + s]; ci[i] = ci[i + s]; }
+    float bv = cv[0];
+    int bi = ci[0];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
       const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (oi != 0x7fffffff && (bi == 0x7fffffff || before(ov, oi, bv, bi))) { bv = ov; bi = oi; }
+      if (beats(ov, oi, bv, bi)) { bv = ov; bi = oi; }
     }
     prev_v = bv;
     prev_i = bi;
@@ -117,6 +140,8 @@ build_csr_kernel(const int32_t* __restrict__ ids_g, int P, int E, int32_t* __res
   int* ids_s = scratch + kCsrWarps;           // [P] when ids_in_smem
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int i = tid; i < kCsrWarps * E; i += kCsrThreads) hist[i] = 0;
+  pdl_wait();                                 // the expert ids are complete
+  pdl_trigger();
   // one coalesced pass over the ids; every later pass reads shared memory
   if (ids_in_smem)
     for (int p = tid; p < P; p += kCsrThreads) ids_s[p] = __ldg(ids_g + p);
@@ -185,10 +210,14 @@ build_csr_kernel(const int32_t* __restrict__ ids_g, int P, int E, int32_t* __res
 
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w,
                               cudaStream_t s) {
-  const int warps = 8;
-  dim3 grid((T + warps - 1) / warps);
-  route_topk_kernel<<<grid, warps * 32, 0, s>>>(logits, T, E, k, ids, w);
-  return cudaGetLastError();
+  const dim3 grid((T + kRouteWarps - 1) / kRouteWarps), block(kRouteWarps * 32);
+  const int pl = (E + 31) / 32;
+  if (pl <= 1) return launch_pdl(route_topk_kernel<1>, grid, block, 0, s, logits, T, E, k, ids, w);
+  if (pl <= 2) return launch_pdl(route_topk_kernel<2>, grid, block, 0, s, logits, T, E, k, ids, w);
+  if (pl <= 4) return launch_pdl(route_topk_kernel<4>, grid, block, 0, s, logits, T, E, k, ids, w);
+  if (pl <= 8) return launch_pdl(route_topk_kernel<8>, grid, block, 0, s, logits, T, E, k, ids, w);
+  if (pl <= 16) return launch_pdl(route_topk_kernel<16>, grid, block, 0, s, logits, T, E, k, ids, w);
+  return launch_pdl(route_topk_kernel<32>, grid, block, 0, s, logits, T, E, k, ids, w);
 }
 
 cudaError_t launch_build_csr(const int32_t* ids, int P, int k, int E, moe_csr csr,
@@ -200,10 +229,9 @@ cudaError_t launch_build_csr(const int32_t* ids, int P, int k, int E, moe_csr cs
   cudaError_t st = cudaFuncSetAttribute(build_csr_kernel,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (st != cudaSuccess) return st;
-  build_csr_kernel<<<1, kCsrThreads, smem, s>>>(ids, P, E, csr.expert_offsets, csr.pair_ids,
-                                                csr.active_experts, csr.n_active, pair_pos, err,
-                                                ids_in_smem);
-  return cudaGetLastError();
+  return launch_pdl(build_csr_kernel, dim3(1), dim3(kCsrThreads), smem, s, ids, P, E,
+                    csr.expert_offsets, csr.pair_ids, csr.active_experts, csr.n_active, pair_pos,
+                    err, ids_in_smem);
 }
 
 // ---------------------------------------------------------------------------
