@@ -44,23 +44,6 @@ __device__ __forceinline__ void cp_async_commit_wait_all() {
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
-// Dequantise one MMA step's A fragment for rows (g, g+8): code bytes 2S, 2S+1 of the lane's
-// 16-byte piece of each row.  The word holding them is converted whole (4 bytes, two
-// steps) by the caller; S selects the half.
-template <int S>
-__device__ __forceinline__ void a_frag(const uint4& r0, const uint4& r1, uint32_t sc0,
-                                       uint32_t sc1, uint32_t (&a)[4]) {
-  const uint32_t w0 = (S / 2 == 0) ? r0.x : (S / 2 == 1) ? r0.y : (S / 2 == 2) ? r0.z : r0.w;
-  const uint32_t w1 = (S / 2 == 0) ? r1.x : (S / 2 == 1) ? r1.y : (S / 2 == 2) ? r1.z : r1.w;
-  uint32_t p0, p1, p2, p3, q0, q1, q2, q3;
-  e2m1x8_to_f16x2x4(w0, p0, p1, p2, p3);
-  e2m1x8_to_f16x2x4(w1, q0, q1, q2, q3);
-  a[0] = hmul2_u32((S & 1) ? p2 : p0, sc0);
-  a[1] = hmul2_u32((S & 1) ? q2 : q0, sc1);
-  a[2] = hmul2_u32((S & 1) ? p3 : p1, sc0);
-  a[3] = hmul2_u32((S & 1) ? q3 : q1, sc1);
-}
-
 // Same for 64-element k-blocks: bytes 2S, 2S+1 of the lane's 8-byte piece.
 template <int S>
 __device__ __forceinline__ void a_frag64(const uint2& r0, const uint2& r1, uint32_t sc0,
@@ -99,29 +82,35 @@ __global__ void __launch_bounds__(256) x_gather_kernel(const uint16_t* __restric
   const int lane = threadIdx.x & 31;
   if (pos >= offsets[E]) return;
   const uint16_t* row = x + (size_t)(pair_ids[pos] / k) * H;
+  // the whole row in registers (H <= 4096: at most 16 pieces of 8 values per lane)
+  uint4 v[16];
   float amax = 0.0f;
-  for (int c = lane * 8; c < H; c += 256) {
-    const uint4 v = *reinterpret_cast<const uint4*>(row + c);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      amax = fmaxf(amax, fabsf(__uint_as_float(w[i] << 16)));
-      amax = fmaxf(amax, fabsf(__uint_as_float(w[i] & 0xffff0000u)));
+  for (int i = 0; i < 16; ++i) {
+    const int c = (lane + 32 * i) * 8;
+    v[i] = c < H ? *reinterpret_cast<const uint4*>(row + c) : make_uint4(0, 0, 0, 0);
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      amax = fmaxf(amax, fabsf(__uint_as_float(w[q] << 16)));
+      amax = fmaxf(amax, fabsf(__uint_as_float(w[q] & 0xffff0000u)));
     }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   const int e = f16_prescale_exp(amax);
   if (lane == 0) xe[pos] = e;
-  for (int c = lane * 8; c < H; c += 256) {
-    const uint4 v = *reinterpret_cast<const uint4*>(row + c);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int c = (lane + 32 * i) * 8;
+    if (c >= H) break;
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
     uint32_t o[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const __half2 hv = __floats2half2_rn(ldexpf(__uint_as_float(w[i] << 16), -e),
-                                           ldexpf(__uint_as_float(w[i] & 0xffff0000u), -e));
-      o[i] = *reinterpret_cast<const uint32_t*>(&hv);
+    for (int q = 0; q < 4; ++q) {
+      const __half2 hv = __floats2half2_rn(ldexpf(__uint_as_float(w[q] << 16), -e),
+                                           ldexpf(__uint_as_float(w[q] & 0xffff0000u), -e));
+      o[q] = *reinterpret_cast<const uint32_t*>(&hv);
     }
     *reinterpret_cast<uint4*>(xg + (size_t)pos * H + c) = make_uint4(o[0], o[1], o[2], o[3]);
   }
@@ -196,21 +185,21 @@ __global__ void __launch_bounds__(256, 2) gate_up_kernel(const GateUpArgs args) 
   const size_t rows2F = (size_t)2 * F;
   const int cpr = row_bytes / 16, spr = srow / 16;
 
+  // thread t copies row t/8 (rows 0..15 gate, 16..31 up), chunks t%8, t%8 + 8, ...
+  // (H % 256 == 0, so a code row has a multiple of 8 chunks); no divisions in the loop
+  const int my_r = threadIdx.x >> 3, my_q = threadIdx.x & 7;
   auto issue = [&](int u, int buf) {
     const int e = args.active[u / nrb];
     const int i0 = (u % nrb) * 16;
     unsigned char* wc = smem + buf * wbytes;
     unsigned char* ws = wc + 32 * row_bytes;
-    for (int idx = threadIdx.x; idx < 32 * cpr; idx += 256) {
-      const int r = idx / cpr, q = idx - r * cpr;
-      const size_t wrow = (size_t)e * rows2F + (r < 16 ? i0 + r : F + i0 + r - 16);
-      cp_async16(wc + wchunk(r, q, row_bytes, true), args.codes + wrow * row_bytes + q * 16);
-    }
-    for (int idx = threadIdx.x; idx < 32 * spr; idx += 256) {
-      const int r = idx / spr, q = idx - r * spr;
-      const size_t wrow = (size_t)e * rows2F + (r < 16 ? i0 + r : F + i0 + r - 16);
-      cp_async16(ws + r * srow + q * 16, args.scales + wrow * srow + q * 16);
-    }
+    const size_t wrow = (size_t)e * rows2F + (my_r < 16 ? i0 + my_r : F + i0 + my_r - 16);
+    const uint8_t* src = args.codes + wrow * row_bytes;
+    unsigned char* dst = wc + my_r * row_bytes;
+    const int swz = (my_r & 1) << 2;
+    for (int q = my_q; q < cpr; q += 8) cp_async16(dst + ((q ^ swz) << 4), src + q * 16);
+    const uint8_t* ssrc = args.scales + wrow * srow;
+    for (int q = my_q; q < spr; q += 8) cp_async16(ws + my_r * srow + q * 16, ssrc + q * 16);
   };
 
   if (u_beg < u_end) issue(u_beg, 0);
@@ -264,21 +253,30 @@ __global__ void __launch_bounds__(256, 2) gate_up_kernel(const GateUpArgs args) 
           const uint32_t f1 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sp + 8 * srow));
           const uint32_t f2 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sp + 16 * srow));
           const uint32_t f3 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sp + 24 * srow));
-#define MOE_GU_STEP(S)                                                                     \
-  {                                                                                        \
-    uint32_t ag[4], au[4];                                                                 \
-    a_frag<S>(c0, c1, (S < 4) ? bcast_lo(f0) : bcast_hi(f0),                               \
-              (S < 4) ? bcast_lo(f1) : bcast_hi(f1), ag);                                  \
-    a_frag<S>(c2, c3, (S < 4) ? bcast_lo(f2) : bcast_hi(f2),                               \
-              (S < 4) ? bcast_lo(f3) : bcast_hi(f3), au);                                  \
-    const uint32_t b0 = (S & 1) ? xb[j][S / 2].z : xb[j][S / 2].x;                         \
-    const uint32_t b1 = (S & 1) ? xb[j][S / 2].w : xb[j][S / 2].y;                         \
-    mma_f16_16816(accg, ag[0], ag[1], ag[2], ag[3], b0, b1);                               \
-    mma_f16_16816(accu, au[0], au[1], au[2], au[3], b0, b1);                               \
-  }
-          MOE_GU_STEP(0) MOE_GU_STEP(1) MOE_GU_STEP(2) MOE_GU_STEP(3)
-          MOE_GU_STEP(4) MOE_GU_STEP(5) MOE_GU_STEP(6) MOE_GU_STEP(7)
-#undef MOE_GU_STEP
+          // words 0,1 of a row use the scale of block 2c, words 2,3 that of block 2c+1
+          const uint32_t s0[2] = {bcast_lo(f0), bcast_hi(f0)}, s1[2] = {bcast_lo(f1), bcast_hi(f1)};
+          const uint32_t s2[2] = {bcast_lo(f2), bcast_hi(f2)}, s3[2] = {bcast_lo(f3), bcast_hi(f3)};
+          const uint32_t W0[4] = {c0.x, c0.y, c0.z, c0.w}, W1[4] = {c1.x, c1.y, c1.z, c1.w};
+          const uint32_t W2[4] = {c2.x, c2.y, c2.z, c2.w}, W3[4] = {c3.x, c3.y, c3.z, c3.w};
+#pragma unroll
+          for (int wi = 0; wi < 4; ++wi) {
+            // one word per row = two MMA steps (2wi, 2wi+1); each byte converted once
+            uint32_t g0[4], g1[4], u0[4], u1[4];
+            e2m1x8_to_f16x2x4(W0[wi], g0[0], g0[1], g0[2], g0[3]);
+            e2m1x8_to_f16x2x4(W1[wi], g1[0], g1[1], g1[2], g1[3]);
+            e2m1x8_to_f16x2x4(W2[wi], u0[0], u0[1], u0[2], u0[3]);
+            e2m1x8_to_f16x2x4(W3[wi], u1[0], u1[1], u1[2], u1[3]);
+            const int sb = wi >> 1;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t b0 = h ? xb[j][wi].z : xb[j][wi].x;
+              const uint32_t b1 = h ? xb[j][wi].w : xb[j][wi].y;
+              mma_f16_16816(accg, hmul2_u32(g0[2 * h], s0[sb]), hmul2_u32(g1[2 * h], s1[sb]),
+                            hmul2_u32(g0[2 * h + 1], s0[sb]), hmul2_u32(g1[2 * h + 1], s1[sb]), b0, b1);
+              mma_f16_16816(accu, hmul2_u32(u0[2 * h], s2[sb]), hmul2_u32(u1[2 * h], s3[sb]),
+                            hmul2_u32(u0[2 * h + 1], s2[sb]), hmul2_u32(u1[2 * h + 1], s3[sb]), b0, b1);
+            }
+          }
         }
       }
       // fixed-order sum over the 8 warps' k ranges
@@ -343,16 +341,17 @@ __global__ void __launch_bounds__(256, 2) down_kernel(const DownArgs args) {
   const int u_end = (int)((long long)(blockIdx.x + 1) * n_units / gridDim.x);
   const int cpr = row_bytes / 16;
 
+  // thread t copies row t/2, chunks t%2, t%2 + 2, ... of the unit's 128 rows
+  const int my_r = threadIdx.x >> 1, my_q = threadIdx.x & 1;
   auto issue = [&](int u, int buf) {
     const int e = args.active[u / nrb];
     const int r0 = (u % nrb) * 128;
     unsigned char* wc = smem + buf * wbytes;
     unsigned char* ws = wc + 128 * row_bytes;
-    const unsigned char* src = args.codes + ((size_t)e * H + r0) * row_bytes;
-    for (int idx = threadIdx.x; idx < 128 * cpr; idx += 256) {
-      const int r = idx / cpr, q = idx - r * cpr;
-      cp_async16(wc + wchunk(r, q, row_bytes, swz), src + (size_t)r * row_bytes + q * 16);
-    }
+    const unsigned char* src = args.codes + ((size_t)e * H + r0 + my_r) * row_bytes;
+    unsigned char* dst = wc + my_r * row_bytes;
+    const int sw = swz ? (my_r & 1) << 2 : 0;
+    for (int q = my_q; q < cpr; q += 2) cp_async16(dst + ((q ^ sw) << 4), src + q * 16);
     const unsigned char* ssrc = args.scales + ((size_t)e * H + r0) * srow;
     for (int idx = threadIdx.x; idx < 128 * srow / 16; idx += 256)
       cp_async16(ws + idx * 16, ssrc + idx * 16);
@@ -409,17 +408,20 @@ __global__ void __launch_bounds__(256, 2) down_kernel(const DownArgs args) {
 #pragma unroll
           for (int q = 0; q < 4; ++q)
             xb[q] = *reinterpret_cast<const uint4*>(hs + g * hrow_bytes + swz_chunk(kb * 16 + 4 * c + q));
-#define MOE_DN_STEP(S)                                                                     \
-  {                                                                                        \
-    uint32_t af[4];                                                                        \
-    a_frag<S>(a0, a1, (S < 4) ? bcast_lo(f0) : bcast_hi(f0),                               \
-              (S < 4) ? bcast_lo(f1) : bcast_hi(f1), af);                                  \
-    mma_f16_16816(acc, af[0], af[1], af[2], af[3], (S & 1) ? xb[S / 2].z : xb[S / 2].x,     \
-                  (S & 1) ? xb[S / 2].w : xb[S / 2].y);                                    \
-  }
-          MOE_DN_STEP(0) MOE_DN_STEP(1) MOE_DN_STEP(2) MOE_DN_STEP(3)
-          MOE_DN_STEP(4) MOE_DN_STEP(5) MOE_DN_STEP(6) MOE_DN_STEP(7)
-#undef MOE_DN_STEP
+          const uint32_t s0[2] = {bcast_lo(f0), bcast_hi(f0)}, s1[2] = {bcast_lo(f1), bcast_hi(f1)};
+          const uint32_t W0[4] = {a0.x, a0.y, a0.z, a0.w}, W1[4] = {a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+          for (int wi = 0; wi < 4; ++wi) {
+            uint32_t p0[4], p1[4];
+            e2m1x8_to_f16x2x4(W0[wi], p0[0], p0[1], p0[2], p0[3]);
+            e2m1x8_to_f16x2x4(W1[wi], p1[0], p1[1], p1[2], p1[3]);
+            const int sb = wi >> 1;
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              mma_f16_16816(acc, hmul2_u32(p0[2 * h], s0[sb]), hmul2_u32(p1[2 * h], s1[sb]),
+                            hmul2_u32(p0[2 * h + 1], s0[sb]), hmul2_u32(p1[2 * h + 1], s1[sb]),
+                            h ? xb[wi].z : xb[wi].x, h ? xb[wi].w : xb[wi].y);
+          }
         } else {
           const unsigned char* rp = wc + rw * row_bytes + LB * c + kb * 32;
           const uint2 a0 = *reinterpret_cast<const uint2*>(rp);

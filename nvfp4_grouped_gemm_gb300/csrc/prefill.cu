@@ -306,6 +306,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// Warp-wide bounded wait: lane 0 polls, the verdict is broadcast (keeps the polling
+// traffic on the shared-memory pipe 32x lower than every lane spinning).
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
+                                               volatile int* abort_flag, uint32_t* err) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag, err) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok) mbar_try(bar, parity);   // every lane observes the completed phase (acquire)
+  return ok != 0;
+}
+
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
                                             uint64_t* bar) {
   asm volatile(
@@ -595,7 +606,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
 #pragma unroll
       for (int d = 0; d < SFD - 1; ++d) { ra[d] = ra[d + 1]; rb[d] = rb[d + 1]; }
       load_sf(it + SFD, ra[SFD - 1], rb[SFD - 1]);
-      if (!mbar_wait(&empty[st], ((it / C::STAGES) & 1) ^ 1, abort_flag, args.err)) break;
+      if (!mbar_wait_warp(&empty[st], ((it / C::STAGES) & 1) ^ 1, abort_flag, args.err)) break;
       uint32_t* sfa = reinterpret_cast<uint32_t*>(smem + st * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES);
       uint32_t* sfb = sfa + C::SFA_BYTES / 4;
       const int ai = 4 * (t & 31) + (t >> 5);          // u32 index of row t inside an atom
@@ -626,7 +637,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
       const bool valid = row < tile.y;
       const int pos = tile.x + row;
       const int sx = (GATE_UP && valid) ? args.a_exp[pos] : 0;
-      if (!mbar_wait(&acc_full[ab], (tcount >> 1) & 1, abort_flag, args.err)) break;
+      if (!mbar_wait_warp(&acc_full[ab], (tcount >> 1) & 1, abort_flag, args.err)) break;
       tc_fence_after();
       const uint32_t acc = acc_col + ab * BN + lane_base;
       if (GATE_UP) {

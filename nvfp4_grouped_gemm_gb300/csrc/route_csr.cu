@@ -28,7 +28,6 @@ __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-constexpr int kRouteWarps = 8;
 constexpr int kNone = 0x7fffffff;   // id of an empty candidate
 
 // a beats b: a is a candidate and either b is empty or a comes first in (logit desc, id asc)
@@ -36,17 +35,17 @@ __device__ __forceinline__ bool beats(float av, int ai, float bv, int bi) {
   return ai != kNone && (bi == kNone || before(av, ai, bv, bi));
 }
 
-// One warp per token; lane l holds experts l, l+32, ... (PL per lane, padded with empty
-// slots).  Round r picks the best candidate ordered strictly after round r-1's pick by a
-// tree over the lane's slots and a butterfly over the warp, so the dependency chain per
-// round is log2(PL) + 5 comparisons deep.
+// One warp (one CTA) per token; lane l holds experts l, l+32, ... (PL per lane, padded).
+// Every untaken expert is ordered after the last pick, so each lane keeps the best of its
+// untaken experts; a round is a warp butterfly over those, after which only the winning
+// lane marks its slot taken and rescans its own PL slots.
 template <int PL>
-__global__ void __launch_bounds__(kRouteWarps * 32)
+__global__ void __launch_bounds__(32)
 route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
                   int32_t* __restrict__ ids, float* __restrict__ w) {
   pdl_wait();
   pdl_trigger();
-  const int t = blockIdx.x * kRouteWarps + (threadIdx.x >> 5);
+  const int t = blockIdx.x;
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
   const float* row = logits + (size_t)t * E;
@@ -56,38 +55,45 @@ route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
     const int e = lane + 32 * i;
     v[i] = e < E ? __ldg(row + e) : 0.0f;
   }
-  float prev_v = 0.0f;
-  int prev_i = -1;
-  float first_v = 0.0f;
-  float my_val = 0.0f;   // lane j < k keeps the j-th selected logit
-  int my_id = 0;
-  for (int r = 0; r < k; ++r) {
+  uint32_t taken = 0;
+  auto local_best = [&](float& bv, int& bi) {
     float cv[PL];
     int ci[PL];
 #pragma unroll
     for (int i = 0; i < PL; ++i) {
       const int e = lane + 32 * i;
-      const bool ok = e < E && (prev_i < 0 || before(prev_v, prev_i, v[i], e));
       cv[i] = v[i];
-      ci[i] = ok ? e : kNone;
+      ci[i] = (e < E && !((taken >> i) & 1u)) ? e : kNone;
     }
 #pragma unroll
     for (int s = PL / 2; s >= 1; s >>= 1)
 #pragma unroll
       for (int i = 0; i < s; ++i)
         if (beats(cv[i + s], ci[i + s], cv[i], ci[i])) { cv[i] = cv[i + s]; ci[i] = ci[i + s]; }
-    float bv = cv[0];
-    int bi = ci[0];
+    bv = cv[0];
+    bi = ci[0];
+  };
+  float lbv;
+  int lbi;
+  local_best(lbv, lbi);
+  float first_v = 0.0f;
+  float my_val = 0.0f;   // lane j < k keeps the j-th selected logit
+  int my_id = 0;
+  for (int r = 0; r < k; ++r) {
+    float bv = lbv;
+    int bi = lbi;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
       const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
       if (beats(ov, oi, bv, bi)) { bv = ov; bi = oi; }
     }
-    prev_v = bv;
-    prev_i = bi;
     if (r == 0) first_v = bv;
     if (lane == r) { my_val = bv; my_id = bi; }
+    if (bi != kNone && lane == (bi & 31)) {
+      taken |= 1u << (bi >> 5);
+      local_best(lbv, lbi);
+    }
   }
   const float ex = (lane < k) ? expf(my_val - first_v) : 0.0f;
   // sum in ascending j so every lane sees the same value
@@ -210,7 +216,7 @@ build_csr_kernel(const int32_t* __restrict__ ids_g, int P, int E, int32_t* __res
 
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w,
                               cudaStream_t s) {
-  const dim3 grid((T + kRouteWarps - 1) / kRouteWarps), block(kRouteWarps * 32);
+  const dim3 grid(T), block(32);
   const int pl = (E + 31) / 32;
   if (pl <= 1) return launch_pdl(route_topk_kernel<1>, grid, block, 0, s, logits, T, E, k, ids, w);
   if (pl <= 2) return launch_pdl(route_topk_kernel<2>, grid, block, 0, s, logits, T, E, k, ids, w);
