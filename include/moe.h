@@ -111,7 +111,7 @@ typedef struct moe_ws_layout {
   size_t qx_scales;    /* prefill: u8 [P][H/16] */
   size_t qx_exp;       /* prefill: i32 [P] row exponents */
   size_t qh_codes;     /* prefill: u8 [P][F/2]  Q(h) in CSR order */
-  size_t qh_scales;    /* prefill: u8 [P][F/16] */
+  size_t qh_scales;    /* prefill: u8 [P][S], S = F/16 rounded up to a multiple of 16 (bytes past F/16 unused) */
   size_t qh_exp;       /* prefill: i32 [P] */
   size_t partial;      /* per-pair down projections z, rows in CSR order: f32 [P][H] on the
                           decode path; on the prefill path f16 [P][H] holding

@@ -81,7 +81,7 @@ bool compute_layout(int T, int H, int F, int E, int k, int path, moe_ws_layout* 
     L->qx_scales = take(P * (H / 16));
     L->qx_exp = take(P * sizeof(int32_t));
     L->qh_codes = take(P * (F / 2));
-    L->qh_scales = take(P * (F / 16));
+    L->qh_scales = take(P * qh_scale_pitch(F));
     L->qh_exp = take(P * sizeof(int32_t));
     const size_t max_tiles = P / 128 + (size_t)(E < (int)P ? E : (int)P) + 1;
     L->tiles = take(16 + 16 * max_tiles);

@@ -17,6 +17,10 @@ constexpr size_t kAlign = 256;
 
 inline size_t align_up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a; }
 
+// Row pitch of the Q(h) block scales in the prefill workspace: F/16 rounded up to a
+// multiple of 16 bytes, so that the rows can be read by TMA.
+inline int qh_scale_pitch(int F) { return (F / 16 + 15) / 16 * 16; }
+
 // Workspace layout for one layer; pure function of the sizes (see moe_ws_layout).
 bool compute_layout(int T, int H, int F, int E, int k, int path, moe_ws_layout* L);
 int resolve_path(int T, int k, int path);

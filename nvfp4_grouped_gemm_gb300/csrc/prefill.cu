@@ -213,6 +213,7 @@ __global__ void __launch_bounds__(256) quant_x_kernel(const uint16_t* __restrict
 // Q(h): one warp per CSR row
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) quant_h_kernel(const float* __restrict__ h, int P, int F,
+                                                      int sf_pitch,
                                                       const int32_t* __restrict__ offsets, int E,
                                                       uint8_t* __restrict__ qc,
                                                       uint8_t* __restrict__ qs,
@@ -253,7 +254,7 @@ __global__ void __launch_bounds__(256) quant_h_kernel(const float* __restrict__ 
     }
     const int sbc = ue4m3_code_of(bmax);
     *reinterpret_cast<uint64_t*>(qc + (size_t)r * (F / 2) + b * 8) = quant_block(key, neg, sbc);
-    qs[(size_t)r * nblk + b] = (uint8_t)sbc;
+    qs[(size_t)r * sf_pitch + b] = (uint8_t)sbc;
   }
 }
 
@@ -404,15 +405,20 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
 //          [P][H] (the combine restores the scale; the bound |acc| <= F * 2688^2 keeps the
 //          value below 2^15).
 struct GemmArgs {
-  const uint8_t* a_scales;      // [P][K/16]
   const int32_t* a_exp;         // [P]
-  const uint8_t* b_scales;      // [E][rows][K/16]
   const int32_t* tiles;         // n_mtiles, then int4 list
   void* out;                    // f32 [P][F] or f16 [P][H]
   uint32_t* err;
   int P, K, rows_per_expert, n_tiles_n, out_cols, F, down_shift;
+  int b_sf_group;               // DOWN: g rows of the weight-scale plane per tensor-map row
 };
 
+// Scale factors reach shared memory through TMA, as row-major staging images beside the
+// code tiles: A rows [128][16 B] (the stage's 4 k-steps x 4 scales), B rows [BN][16 B]
+// (GATE_UP), or for DOWN g sub-row images [128/g][32 B] whose 16-byte windows start at
+// byte (s*K/16 + 16*ks) mod 16 (the weight-scale rows are K/16 bytes, not a multiple of
+// 16, so g consecutive rows form one tensor-map row).  Four warps transpose the staging
+// images into the 32x16-byte atoms tcgen05.cp reads; no thread waits on global memory.
 template <int BN, bool GATE_UP>
 struct Cfg {
   static constexpr int BM = 128;
@@ -424,7 +430,9 @@ struct Cfg {
   static constexpr int B_BYTES = BN * KB;
   static constexpr int SFA_BYTES = 4 * 512;         // 4 k-steps x one atom
   static constexpr int SFB_BYTES = 4 * G * 512;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+  static constexpr int SA_STG = BM * 16;            // A scale staging
+  static constexpr int SB_STG = GATE_UP ? BN * 16 : BN * 32;   // B scale staging (DOWN: 32-B windows)
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES + SA_STG + SB_STG;
   static constexpr int ACC_COLS = 2 * BN;           // two accumulator buffers
   static constexpr int SF_COLS = 16 + 16 * G;       // one stage's scale factors in TMEM
   // one scale-factor buffer per smem stage: a buffer is rewritten only after the stage's
@@ -433,25 +441,44 @@ struct Cfg {
   static constexpr int TMEM_COLS = TMEM_COLS_USED <= 256 ? 256 : 512;
   static constexpr int THREADS = 320;               // 10 warps
   static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
-  static constexpr uint32_t TX_BYTES = A_BYTES + B_BYTES;
   static_assert(TMEM_COLS_USED <= 512, "TMEM budget");
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
+  static_assert(SMEM <= 232448, "shared memory budget");
 };
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
 
 template <int BN, bool GATE_UP>
 __global__ void __launch_bounds__(320, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+            const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
             const GemmArgs args) {
   using C = Cfg<BN, GATE_UP>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
-  uint64_t* empty = full + C::STAGES;
+  uint64_t* sf_ready = full + C::STAGES;
+  uint64_t* empty = sf_ready + C::STAGES;
   uint64_t* acc_full = empty + C::STAGES;           // [2]
   uint64_t* acc_empty = acc_full + 2;               // [2]
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  // stage layout: A codes | B codes | SFA atoms | SFB atoms | A scale staging | B scale staging
+  constexpr int OFF_SFA = C::A_BYTES + C::B_BYTES;
+  constexpr int OFF_SFB = OFF_SFA + C::SFA_BYTES;
+  constexpr int OFF_SA = OFF_SFB + C::SFB_BYTES;
+  constexpr int OFF_SB = OFF_SA + C::SA_STG;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_mtiles = args.tiles[0];
@@ -462,7 +489,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&full[s], 1 + 128);                  // TMA expect_tx + 128 scale threads
+      mbar_init(&full[s], 1);                        // TMA expect_tx
+      mbar_init(&sf_ready[s], 4);                    // one arrive per transposing warp
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -488,25 +516,39 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
+      constexpr uint32_t tx = C::A_BYTES + C::B_BYTES + C::SA_STG + (GATE_UP ? C::SB_STG : 0);
+      const int g = args.b_sf_group;
+      const uint32_t tx_b_sf = GATE_UP ? 0u : (uint32_t)(g == 1 ? BN * 16 : BN * 32);
+      const int sub_rows = BN / g, sub_w = g == 1 ? 16 : 32;
       int it = 0;
+      int4 tile = blockIdx.x < n_work ? tlist[blockIdx.x / args.n_tiles_n] : make_int4(0, 0, 0, 0);
       for (int w = blockIdx.x; w < n_work && !*abort_flag; w += gridDim.x) {
-        const int4 tile = tlist[w / args.n_tiles_n];
+        const int wn = w + gridDim.x;                // next work's descriptor, fetched early
+        const int4 next = wn < n_work ? tlist[wn / args.n_tiles_n] : tile;
         const int n0 = (w % args.n_tiles_n) * C::OUT_N;
         const int brow = tile.z * args.rows_per_expert + n0;
         for (int ks = 0; ks < k_stages; ++ks, ++it) {
           const int st = it % C::STAGES;
           if (!mbar_wait(&empty[st], ((it / C::STAGES) & 1) ^ 1, abort_flag, args.err)) break;
           unsigned char* sb = smem + st * C::STAGE_BYTES;
-          mbar_expect_tx(&full[st], C::TX_BYTES);
+          mbar_expect_tx(&full[st], tx + tx_b_sf);
           tma_load_2d(sb, &tmap_a, ks * C::KB, tile.x, &full[st]);
+          tma_load_2d(sb + OFF_SA, &tmap_sfa, ks * 16, tile.x, &full[st]);
           if (GATE_UP) {
             tma_load_2d(sb + C::A_BYTES, &tmap_b, ks * C::KB, brow, &full[st]);
             tma_load_2d(sb + C::A_BYTES + C::B_BYTES / 2, &tmap_b, ks * C::KB, brow + args.F,
                         &full[st]);
+            tma_load_2d(sb + OFF_SB, &tmap_sfb, ks * 16, brow, &full[st]);
+            tma_load_2d(sb + OFF_SB + C::SB_STG / 2, &tmap_sfb, ks * 16, brow + args.F, &full[st]);
           } else {
             tma_load_2d(sb + C::A_BYTES, &tmap_b, ks * C::KB, brow, &full[st]);
+            for (int s2 = 0; s2 < g; ++s2) {
+              const int x = ((s2 * sfrow + 16 * ks) >> 4) << 4;
+              tma_load_2d(sb + OFF_SB + s2 * sub_rows * sub_w, &tmap_sfb, x, brow / g, &full[st]);
+            }
           }
         }
+        tile = next;
       }
       // drain: wait (bounded) until every issued stage has landed
       if (*abort_flag) {
@@ -533,14 +575,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         bool ok = true;
         for (int ks = 0; ks < k_stages; ++ks, ++it) {
           const int st = it % C::STAGES;
-          if (!mbar_wait(&full[st], (it / C::STAGES) & 1, abort_flag, args.err)) { ok = false; break; }
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          const uint32_t par = (it / C::STAGES) & 1;
+          if (!mbar_wait(&sf_ready[st], par, abort_flag, args.err) ||
+              !mbar_wait(&full[st], par, abort_flag, args.err)) { ok = false; break; }
           tc_fence_after();
           unsigned char* sb = smem + st * C::STAGE_BYTES;
           const uint32_t a_addr = smem_u32(sb);
           const uint32_t b_addr = smem_u32(sb + C::A_BYTES);
-          const uint32_t sfa_smem = smem_u32(sb + C::A_BYTES + C::B_BYTES);
-          const uint32_t sfb_smem = sfa_smem + C::SFA_BYTES;
+          const uint32_t sfa_smem = smem_u32(sb + OFF_SFA);
+          const uint32_t sfb_smem = smem_u32(sb + OFF_SFB);
           const uint32_t sfc = sf_col0 + st * C::SF_COLS;
           // scale factors: smem atoms -> TMEM (4 columns per 128-row atom)
 #pragma unroll
@@ -562,67 +605,49 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
       }
     }
   } else if (warp < 6) {
-    // ---------------- scale-factor loaders (128 threads) ----------------
-    // Thread t feeds A row t and B row t of every stage: 16 scale bytes each (the 4
-    // k-steps of the stage), loaded SFD stages ahead into registers and scattered into
-    // the 32x16-byte atoms once the stage's smem is free.
+    // ---------------- scale-factor transposers (128 threads) ----------------
+    // Thread t moves A row t and B row t of every stage from the staging images into the
+    // atoms: row t's 4 scales of k-step j go to u32 4*(t%32) + t/32 of atom j.  Scale bytes
+    // past the row's K/16 (the zero-filled tail of the last stage) are written as 0.
     const int t = threadIdx.x - 64;
-    constexpr int SFD = 3;
     const int n_it = ((n_work - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x) * k_stages;
-    auto load_sf = [&](int it2, uint4& va, uint4& vb) {
-      va = make_uint4(0, 0, 0, 0);
-      vb = make_uint4(0, 0, 0, 0);
-      if (it2 >= n_it) return;
-      const int w = blockIdx.x + (it2 / k_stages) * gridDim.x;
-      const int ks = it2 % k_stages;
-      const int4 tile = tlist[w / args.n_tiles_n];
-      const int n0 = (w % args.n_tiles_n) * C::OUT_N;
-      const int brow0 = tile.z * args.rows_per_expert + n0;
-      const int byte0 = 16 * ks;
-      uint32_t a[4] = {0, 0, 0, 0}, b[4] = {0, 0, 0, 0};
-      if (t < tile.y) {
-        const uint8_t* src = args.a_scales + (size_t)(tile.x + t) * sfrow + byte0;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (byte0 + 4 * j < sfrow) a[j] = __ldg(reinterpret_cast<const uint32_t*>(src + 4 * j));
-      }
-      if (t < BN) {
-        const int wrow = GATE_UP ? (t < BN / 2 ? brow0 + t : brow0 + args.F + t - BN / 2)
-                                 : brow0 + t;
-        const uint8_t* src = args.b_scales + (size_t)wrow * sfrow + byte0;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (byte0 + 4 * j < sfrow) b[j] = __ldg(reinterpret_cast<const uint32_t*>(src + 4 * j));
-      }
-      va = make_uint4(a[0], a[1], a[2], a[3]);
-      vb = make_uint4(b[0], b[1], b[2], b[3]);
-    };
-    uint4 ra[SFD], rb[SFD];
-#pragma unroll
-    for (int d = 0; d < SFD; ++d) load_sf(d, ra[d], rb[d]);
-    for (int it = 0; it < n_it && !*abort_flag; ++it) {
+    const int ai = 4 * (t & 31) + (t >> 5);
+    const int g = args.b_sf_group;
+    const int sub_rows = BN / g, sub_w = g == 1 ? 16 : 32;
+    const int bs = t % g, bi = t / g;
+    for (int it = 0; it < n_it; ++it) {
       const int st = it % C::STAGES;
-      const uint4 va = ra[0], vb = rb[0];
+      const int ks = it % k_stages;
+      if (!mbar_wait_warp(&full[st], (it / C::STAGES) & 1, abort_flag, args.err)) break;
+      const uint32_t sb = smem_u32(smem + st * C::STAGE_BYTES);
+      const int nvalid = min(4, (sfrow - 16 * ks) >> 2);   // u32 words of this stage in the row
+      const uint4 va4 = lds128(sb + OFF_SA + 16 * t);
+      uint32_t a[4] = {va4.x, va4.y, va4.z, va4.w};
+      uint32_t b[4];
+      if (GATE_UP) {
+        const uint4 vb4 = lds128(sb + OFF_SB + 16 * t);
+        b[0] = vb4.x; b[1] = vb4.y; b[2] = vb4.z; b[3] = vb4.w;
+      } else {
+        const int x = ((bs * sfrow + 16 * ks) >> 4) << 4;
+        const uint32_t src = sb + OFF_SB + bs * sub_rows * sub_w + bi * sub_w + (bs * sfrow + 16 * ks - x);
 #pragma unroll
-      for (int d = 0; d < SFD - 1; ++d) { ra[d] = ra[d + 1]; rb[d] = rb[d + 1]; }
-      load_sf(it + SFD, ra[SFD - 1], rb[SFD - 1]);
-      if (!mbar_wait_warp(&empty[st], ((it / C::STAGES) & 1) ^ 1, abort_flag, args.err)) break;
-      uint32_t* sfa = reinterpret_cast<uint32_t*>(smem + st * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES);
-      uint32_t* sfb = sfa + C::SFA_BYTES / 4;
-      const int ai = 4 * (t & 31) + (t >> 5);          // u32 index of row t inside an atom
-      sfa[0 * 128 + ai] = va.x;
-      sfa[1 * 128 + ai] = va.y;
-      sfa[2 * 128 + ai] = va.z;
-      sfa[3 * 128 + ai] = va.w;
-      if (t < BN) {
-        sfb[(0 * C::G + (t >> 7)) * 128 + ai] = vb.x;
-        sfb[(1 * C::G + (t >> 7)) * 128 + ai] = vb.y;
-        sfb[(2 * C::G + (t >> 7)) * 128 + ai] = vb.z;
-        sfb[(3 * C::G + (t >> 7)) * 128 + ai] = vb.w;
+        for (int j = 0; j < 4; ++j) b[j] = j < nvalid ? lds32(src + 4 * j) : 0u;
       }
-      // make the generic-proxy stores visible to tcgen05.cp, then arrive
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (j >= nvalid) a[j] = 0u;
+      uint32_t* sfa = reinterpret_cast<uint32_t*>(smem + st * C::STAGE_BYTES + OFF_SFA);
+      uint32_t* sfb = reinterpret_cast<uint32_t*>(smem + st * C::STAGE_BYTES + OFF_SFB);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) sfa[j * 128 + ai] = a[j];
+      if (t < BN) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sfb[(j * C::G + (t >> 7)) * 128 + ai] = b[j];
+      }
+      // make the generic-proxy stores visible to tcgen05.cp, then one arrive per warp
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive(&full[st]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sf_ready[st]);
     }
   } else {
     // ---------------- epilogue (warps 6..9 -> TMEM lane quarters 2,3,0,1) ----------------
@@ -739,17 +764,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2D u8 tensor map over [rows][row_bytes], box {128 bytes, box_rows}, 128-byte swizzle.
-bool make_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows,
-              uint32_t box_rows) {
+// 2D u8 tensor map over [rows][row_bytes] (row pitch `pitch`), box {box_w bytes, box_rows};
+// 128-byte swizzle for code tiles, none for scale staging.  Boxes reaching past row_bytes
+// or rows read zeros.
+bool make_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t pitch,
+              uint64_t rows, uint32_t box_w, uint32_t box_rows, bool swizzle) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {row_bytes, rows};
-  cuuint64_t strides[1] = {row_bytes};
-  cuuint32_t box[2] = {128, box_rows};
+  cuuint64_t strides[1] = {pitch};
+  cuuint32_t box[2] = {box_w, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -766,8 +794,8 @@ int num_sms() {
 }
 
 template <int BN, bool GATE_UP>
-cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& a,
-                     int max_tiles, cudaStream_t s) {
+cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msa,
+                     const CUtensorMap& msb, const GemmArgs& a, int max_tiles, cudaStream_t s) {
   using C = Cfg<BN, GATE_UP>;
   auto kern = gemm_kernel<BN, GATE_UP>;
   cudaError_t st = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -775,7 +803,7 @@ cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArg
   int grid = max_tiles * a.n_tiles_n;
   if (grid > num_sms()) grid = num_sms();
   if (grid < 1) grid = 1;
-  kern<<<grid, C::THREADS, C::SMEM, s>>>(ma, mb, a);
+  kern<<<grid, C::THREADS, C::SMEM, s>>>(ma, mb, msa, msb, a);
   return cudaGetLastError();
 }
 
@@ -798,14 +826,18 @@ cudaError_t launch_prefill_gate_up(const uint16_t* x_bf16, int T, int H, int F, 
                                               reinterpret_cast<const int32_t*>(ws + L.pair_pos),
                                               qc, qs, qe);
   if ((st = cudaGetLastError()) != cudaSuccess) return st;
-  CUtensorMap ma, mb;
+  CUtensorMap ma, mb, msa, msb;
   constexpr int BN = 128;                           // 64 gate rows over 64 up rows
-  if (!make_map(&ma, qc, H / 2, P, 128)) return cudaErrorInvalidValue;
-  if (!make_map(&mb, b.codes, H / 2, (uint64_t)b.E * 2 * F, BN / 2)) return cudaErrorInvalidValue;
-  GemmArgs a{qs, qe, b.scales, tiles, ws + L.h, reinterpret_cast<uint32_t*>(ws + L.error_word),
-             P, H, 2 * F, F / (BN / 2), F, F, 0};
+  const uint64_t wrows = (uint64_t)b.E * 2 * F;
+  if (!make_map(&ma, qc, H / 2, H / 2, P, 128, 128, true) ||
+      !make_map(&mb, b.codes, H / 2, H / 2, wrows, 128, BN / 2, true) ||
+      !make_map(&msa, qs, H / 16, H / 16, P, 16, 128, false) ||
+      !make_map(&msb, b.scales, H / 16, H / 16, wrows, 16, BN / 2, false))
+    return cudaErrorInvalidValue;
+  GemmArgs a{qe, tiles, ws + L.h, reinterpret_cast<uint32_t*>(ws + L.error_word),
+             P, H, 2 * F, F / (BN / 2), F, F, 0, 1};
   const int max_tiles = P / 128 + (P < b.E ? P : b.E) + 1;
-  return run_gemm<BN, true>(ma, mb, a, max_tiles, s);
+  return run_gemm<BN, true>(ma, mb, msa, msb, a, max_tiles, s);
 }
 
 // Exponent c_F with F * 2688^2 * 2^-c_F < 2^15: the fixed shift of the f16 partials.
@@ -825,19 +857,31 @@ cudaError_t launch_prefill_down(const moe_nvfp4_bank& b, moe_csr csr, int T, int
   uint8_t* qc = reinterpret_cast<uint8_t*>(ws + L.qh_codes);
   uint8_t* qs = reinterpret_cast<uint8_t*>(ws + L.qh_scales);
   int32_t* qe = reinterpret_cast<int32_t*>(ws + L.qh_exp);
-  quant_h_kernel<<<(P + 7) / 8, 256, 0, s>>>(reinterpret_cast<const float*>(ws + L.h), P, F,
+  const int sfh = qh_scale_pitch(F);
+  quant_h_kernel<<<(P + 7) / 8, 256, 0, s>>>(reinterpret_cast<const float*>(ws + L.h), P, F, sfh,
                                               csr.expert_offsets, b.E, qc, qs, qe);
   cudaError_t st = cudaGetLastError();
   if (st != cudaSuccess) return st;
   constexpr int BN = 128;
-  CUtensorMap ma, mb;
-  if (!make_map(&ma, qc, F / 2, P, 128)) return cudaErrorInvalidValue;
-  if (!make_map(&mb, b.codes, F / 2, (uint64_t)b.E * H, BN)) return cudaErrorInvalidValue;
+  // the weight-scale rows are F/16 bytes; g of them make a row pitch that is a multiple of 16
+  const int sfrow = F / 16;
+  int g = 1;
+  if (sfrow % 16 != 0)
+    for (g = 2; (g * sfrow) % 16 != 0 || g * sfrow < 32; g *= 2) {
+    }
+  const uint64_t wrows = (uint64_t)b.E * H;
+  CUtensorMap ma, mb, msa, msb;
+  if (!make_map(&ma, qc, F / 2, F / 2, P, 128, 128, true) ||
+      !make_map(&mb, b.codes, F / 2, F / 2, wrows, 128, BN, true) ||
+      !make_map(&msa, qs, sfh, sfh, P, 16, 128, false) ||
+      !make_map(&msb, b.scales, (uint64_t)g * sfrow, (uint64_t)g * sfrow, wrows / g,
+                g == 1 ? 16 : 32, BN / g, false))
+    return cudaErrorInvalidValue;
   const int shift = down_shift_for(F);
-  GemmArgs a{qs, qe, b.scales, reinterpret_cast<const int32_t*>(ws + L.tiles), ws + L.partial,
-             reinterpret_cast<uint32_t*>(ws + L.error_word), P, F, H, H / BN, H, F, shift};
+  GemmArgs a{qe, reinterpret_cast<const int32_t*>(ws + L.tiles), ws + L.partial,
+             reinterpret_cast<uint32_t*>(ws + L.error_word), P, F, H, H / BN, H, F, shift, g};
   const int max_tiles = P / 128 + (P < b.E ? P : b.E) + 1;
-  return run_gemm<BN, false>(ma, mb, a, max_tiles, s);
+  return run_gemm<BN, false>(ma, mb, msa, msb, a, max_tiles, s);
 }
 
 cudaError_t launch_prefill_combine(const float* w, int T, int H, int F, int k,

@@ -33,6 +33,11 @@ class DeviceRun:
         return self.ws_raw[off:off + nbytes].view(dtype).reshape(shape)
 
 
+def qh_scale_pitch(F: int) -> int:
+    """Row pitch of the Q(h) block scales in the prefill workspace (F/16 rounded up to 16)."""
+    return (F // 16 + 15) // 16 * 16
+
+
 def device_banks(wl, device="cuda"):
     return (moe.NvFp4Bank.from_numpy(wl.gate_up, device), moe.NvFp4Bank.from_numpy(wl.down, device))
 

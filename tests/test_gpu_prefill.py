@@ -18,7 +18,7 @@ import synth
 import oracle
 from oracle import nvfp4
 import nvfp4_grouped_gemm_gb300 as moe
-from gpu_util import run_layer, h_tolerance, assert_within, device_banks
+from gpu_util import run_layer, h_tolerance, assert_within, device_banks, qh_scale_pitch
 
 pytestmark = pytest.mark.gpu
 PF = moe.PATH_PREFILL
@@ -70,7 +70,8 @@ def _stages(wl, run, tokens):
     assert band_ratio <= 1.0, f"h error exceeds the quantisation band by {band_ratio:.3g}x"
     # (iii) Q(h) where the decision is not ambiguous
     q_c = _unpack(run.region("qh_codes", P * F // 2, np.uint8, (P, F // 2))[pos])
-    q_s = run.region("qh_scales", P * F // 16, np.uint8, (P, F // 16))[pos]
+    S = qh_scale_pitch(F)
+    q_s = run.region("qh_scales", P * S, np.uint8, (P, S))[pos, :F // 16]
     q_e = run.region("qh_exp", P * 4, np.int32, (P,))[pos]
     r_c = _unpack(res.qh[0][pairs])
     flagged = amb.flagged[pairs]
@@ -108,7 +109,8 @@ def _down_from_oracle_h(wl, run, res, tokens):
     wsn = ws.cpu().numpy()
     L = run.ws
     q_c = wsn[L["qh_codes"]:L["qh_codes"] + P * F // 2].reshape(P, F // 2)[pos]
-    q_s = wsn[L["qh_scales"]:L["qh_scales"] + P * F // 16].reshape(P, F // 16)[pos]
+    S = qh_scale_pitch(F)
+    q_s = wsn[L["qh_scales"]:L["qh_scales"] + P * S].reshape(P, S)[pos, :F // 16]
     assert np.array_equal(q_c, res.qh[0][pairs]), "Q(oracle h) codes"
     assert np.array_equal(q_s, res.qh[1][pairs]), "Q(oracle h) scales"
     yy = y.cpu().numpy()
