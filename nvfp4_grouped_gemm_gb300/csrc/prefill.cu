@@ -364,6 +364,10 @@ __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint3
       ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
       : "memory");
 }
+// Two k-steps' scale-factor atoms (32 rows x 16 B each, the second one LBO bytes after the
+// first) into 8 TMEM columns: lanes 0..31 receive the atoms (lanes 32..127 receive bytes
+// the MMA does not read).
+// One k-step's scale-factor atom (32 rows x 16 B) into 4 TMEM columns of every lane quarter.
 __device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
   asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
                : "memory");
@@ -566,6 +570,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       constexpr uint32_t idesc = mxf4_idesc(128, BN);
+      const uint32_t s0 = smem_u32(smem);
+      // descriptors of stage 0; stage st adds st * STAGE_BYTES to the start address field
+      const uint64_t a_desc0 = smem_desc(s0, 16, 1024, 2);
+      const uint64_t b_desc0 = smem_desc(s0 + C::A_BYTES, 16, 1024, 2);
+      const uint64_t sfa_desc0 = smem_desc(s0 + OFF_SFA, 0, 128, 0);
+      const uint64_t sfb_desc0 = smem_desc(s0 + OFF_SFB, 0, 128, 0);
       int it = 0, tcount = 0;
       for (int w = blockIdx.x; w < n_work && !*abort_flag; w += gridDim.x, ++tcount) {
         const int ab = tcount & 1;
@@ -573,32 +583,29 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         tc_fence_after();
         const uint32_t acc = acc_col + ab * BN;
         bool ok = true;
+        int st = it % C::STAGES;
+        uint32_t par = (it / C::STAGES) & 1;
         for (int ks = 0; ks < k_stages; ++ks, ++it) {
-          const int st = it % C::STAGES;
-          const uint32_t par = (it / C::STAGES) & 1;
-          if (!mbar_wait(&sf_ready[st], par, abort_flag, args.err) ||
-              !mbar_wait(&full[st], par, abort_flag, args.err)) { ok = false; break; }
+          // code tiles (TMA) and scale-factor atoms (transposers) of the stage
+          if (!mbar_wait(&full[st], par, abort_flag, args.err) ||
+              !mbar_wait(&sf_ready[st], par, abort_flag, args.err)) { ok = false; break; }
           tc_fence_after();
-          unsigned char* sb = smem + st * C::STAGE_BYTES;
-          const uint32_t a_addr = smem_u32(sb);
-          const uint32_t b_addr = smem_u32(sb + C::A_BYTES);
-          const uint32_t sfa_smem = smem_u32(sb + OFF_SFA);
-          const uint32_t sfb_smem = smem_u32(sb + OFF_SFB);
+          const uint64_t so = (uint64_t)((st * C::STAGE_BYTES) >> 4);
           const uint32_t sfc = sf_col0 + st * C::SF_COLS;
-          // scale factors: smem atoms -> TMEM (4 columns per 128-row atom)
+          // scale factors: smem atoms -> TMEM (k-step j at column 4j)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) tc_cp_sf(sfc + 4 * j, sfa_desc0 + so + ((j * 512) >> 4));
+#pragma unroll
+          for (int q = 0; q < 4 * C::G; ++q) tc_cp_sf(sfc + 16 + 4 * q, sfb_desc0 + so + ((q * 512) >> 4));
+          // k-steps past K (the zero-filled tail of the last stage) are skipped
+          const int nk = min(4, (sfrow - 16 * ks) >> 2);
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            tc_cp_sf(sfc + 4 * j, smem_desc(sfa_smem + j * 512, 0, 128, 0));
-#pragma unroll
-          for (int q = 0; q < 4 * C::G; ++q)
-            tc_cp_sf(sfc + 16 + 4 * q, smem_desc(sfb_smem + q * 512, 0, 128, 0));
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint64_t adesc = smem_desc(a_addr + 32 * j, 16, 1024, 2);
-            const uint64_t bdesc = smem_desc(b_addr + 32 * j, 16, 1024, 2);
-            tc_mma(acc, adesc, bdesc, idesc, sfc + 4 * j, sfc + 16 + 4 * C::G * j, (ks | j) != 0);
-          }
+            if (j < nk)
+              tc_mma(acc, a_desc0 + so + ((32 * j) >> 4), b_desc0 + so + ((32 * j) >> 4), idesc,
+                     sfc + 4 * j, sfc + 16 + 4 * C::G * j, (ks | j) != 0);
           tc_commit(&empty[st]);
+          if (++st == C::STAGES) { st = 0; par ^= 1u; }
         }
         if (!ok) break;
         tc_commit(&acc_full[ab]);
