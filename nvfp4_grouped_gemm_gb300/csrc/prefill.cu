@@ -367,11 +367,6 @@ __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint3
 // Two k-steps' scale-factor atoms (32 rows x 16 B each, the second one LBO bytes after the
 // first) into 8 TMEM columns: lanes 0..31 receive the atoms (lanes 32..127 receive bytes
 // the MMA does not read).
-// One k-step's scale-factor atom (32 rows x 16 B) into 4 TMEM columns of every lane quarter.
-__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
-               : "memory");
-}
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
@@ -382,6 +377,16 @@ __device__ __forceinline__ void tc_fence_before() {
 }
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// 16 consecutive 32-bit TMEM columns of this warp's 32 lanes (one value per lane each).
+__device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16};"
+      ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+        "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]),
+        "r"(v[14]), "r"(v[15])
+      : "memory");
 }
 __device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
@@ -421,22 +426,23 @@ struct GemmArgs {
 // code tiles: A rows [128][16 B] (the stage's 4 k-steps x 4 scales), B rows [BN][16 B]
 // (GATE_UP), or for DOWN g sub-row images [128/g][32 B] whose 16-byte windows start at
 // byte (s*K/16 + 16*ks) mod 16 (the weight-scale rows are K/16 bytes, not a multiple of
-// 16, so g consecutive rows form one tensor-map row).  Four warps transpose the staging
-// images into the 32x16-byte atoms tcgen05.cp reads; no thread waits on global memory.
+// 16, so g consecutive rows form one tensor-map row).  Four warps, one per TMEM lane
+// quarter, rearrange the staging images and store them into the stage's scale-factor
+// columns with tcgen05.st: lane r of every quarter holds, in columns 4j..4j+3, the k-step
+// j scales of rows r, r+32, r+64, r+96.  No thread waits on global memory, and the MMA
+// thread issues nothing but MMAs.
 template <int BN, bool GATE_UP>
 struct Cfg {
   static constexpr int BM = 128;
   static constexpr int KB = 128;                    // bytes of K per stage (256 elements)
   static constexpr int G = (BN + 127) / 128;        // 128-row scale-factor atoms per B tile
-  static constexpr int STAGES = 5;
+  static constexpr int STAGES = GATE_UP ? 6 : 5;
   static constexpr int OUT_N = GATE_UP ? BN / 2 : BN;   // output columns per tile
   static constexpr int A_BYTES = BM * KB;
   static constexpr int B_BYTES = BN * KB;
-  static constexpr int SFA_BYTES = 4 * 512;         // 4 k-steps x one atom
-  static constexpr int SFB_BYTES = 4 * G * 512;
   static constexpr int SA_STG = BM * 16;            // A scale staging
   static constexpr int SB_STG = GATE_UP ? BN * 16 : BN * 32;   // B scale staging (DOWN: 32-B windows)
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES + SA_STG + SB_STG;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SA_STG + SB_STG;
   static constexpr int ACC_COLS = 2 * BN;           // two accumulator buffers
   static constexpr int SF_COLS = 16 + 16 * G;       // one stage's scale factors in TMEM
   // one scale-factor buffer per smem stage: a buffer is rewritten only after the stage's
@@ -478,10 +484,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
   uint64_t* acc_empty = acc_full + 2;               // [2]
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-  // stage layout: A codes | B codes | SFA atoms | SFB atoms | A scale staging | B scale staging
-  constexpr int OFF_SFA = C::A_BYTES + C::B_BYTES;
-  constexpr int OFF_SFB = OFF_SFA + C::SFA_BYTES;
-  constexpr int OFF_SA = OFF_SFB + C::SFB_BYTES;
+  // stage layout: A codes | B codes | A scale staging | B scale staging
+  constexpr int OFF_SA = C::A_BYTES + C::B_BYTES;
   constexpr int OFF_SB = OFF_SA + C::SA_STG;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -574,8 +578,6 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
       // descriptors of stage 0; stage st adds st * STAGE_BYTES to the start address field
       const uint64_t a_desc0 = smem_desc(s0, 16, 1024, 2);
       const uint64_t b_desc0 = smem_desc(s0 + C::A_BYTES, 16, 1024, 2);
-      const uint64_t sfa_desc0 = smem_desc(s0 + OFF_SFA, 0, 128, 0);
-      const uint64_t sfb_desc0 = smem_desc(s0 + OFF_SFB, 0, 128, 0);
       int it = 0, tcount = 0;
       for (int w = blockIdx.x; w < n_work && !*abort_flag; w += gridDim.x, ++tcount) {
         const int ab = tcount & 1;
@@ -586,17 +588,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         int st = it % C::STAGES;
         uint32_t par = (it / C::STAGES) & 1;
         for (int ks = 0; ks < k_stages; ++ks, ++it) {
-          // code tiles (TMA) and scale-factor atoms (transposers) of the stage
+          // code tiles (TMA) and scale factors in TMEM (transposers) of the stage
           if (!mbar_wait(&full[st], par, abort_flag, args.err) ||
               !mbar_wait(&sf_ready[st], par, abort_flag, args.err)) { ok = false; break; }
           tc_fence_after();
           const uint64_t so = (uint64_t)((st * C::STAGE_BYTES) >> 4);
           const uint32_t sfc = sf_col0 + st * C::SF_COLS;
-          // scale factors: smem atoms -> TMEM (k-step j at column 4j)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) tc_cp_sf(sfc + 4 * j, sfa_desc0 + so + ((j * 512) >> 4));
-#pragma unroll
-          for (int q = 0; q < 4 * C::G; ++q) tc_cp_sf(sfc + 16 + 4 * q, sfb_desc0 + so + ((q * 512) >> 4));
           // k-steps past K (the zero-filled tail of the last stage) are skipped
           const int nk = min(4, (sfrow - 16 * ks) >> 2);
 #pragma unroll
@@ -612,47 +609,50 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
       }
     }
   } else if (warp < 6) {
-    // ---------------- scale-factor transposers (128 threads) ----------------
-    // Thread t moves A row t and B row t of every stage from the staging images into the
-    // atoms: row t's 4 scales of k-step j go to u32 4*(t%32) + t/32 of atom j.  Scale bytes
-    // past the row's K/16 (the zero-filled tail of the last stage) are written as 0.
-    const int t = threadIdx.x - 64;
+    // ---------------- scale-factor transposers (128 threads, one TMEM lane quarter each) ---
+    // Lane r of warp w writes TMEM lane 32*(w%4) + r: for k-step j, columns 4j + x hold the
+    // scale word of row r + 32x.  Scale bytes past the row's K/16 (the zero-filled tail of
+    // the last stage) are written as 0.
+    static_assert(C::G == 1, "one 128-row scale group per operand");
     const int n_it = ((n_work - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x) * k_stages;
-    const int ai = 4 * (t & 31) + (t >> 5);
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const int g = args.b_sf_group;
     const int sub_rows = BN / g, sub_w = g == 1 ? 16 : 32;
-    const int bs = t % g, bi = t / g;
     for (int it = 0; it < n_it; ++it) {
       const int st = it % C::STAGES;
       const int ks = it % k_stages;
       if (!mbar_wait_warp(&full[st], (it / C::STAGES) & 1, abort_flag, args.err)) break;
+      tc_fence_after();
       const uint32_t sb = smem_u32(smem + st * C::STAGE_BYTES);
-      const int nvalid = min(4, (sfrow - 16 * ks) >> 2);   // u32 words of this stage in the row
-      const uint4 va4 = lds128(sb + OFF_SA + 16 * t);
-      uint32_t a[4] = {va4.x, va4.y, va4.z, va4.w};
-      uint32_t b[4];
-      if (GATE_UP) {
-        const uint4 vb4 = lds128(sb + OFF_SB + 16 * t);
-        b[0] = vb4.x; b[1] = vb4.y; b[2] = vb4.z; b[3] = vb4.w;
-      } else {
-        const int x = ((bs * sfrow + 16 * ks) >> 4) << 4;
-        const uint32_t src = sb + OFF_SB + bs * sub_rows * sub_w + bi * sub_w + (bs * sfrow + 16 * ks - x);
+      const int nvalid = min(4, (sfrow - 16 * ks) >> 2);   // u32 words of this stage in a row
+      uint32_t va[16], vb[16];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) b[j] = j < nvalid ? lds32(src + 4 * j) : 0u;
+      for (int x = 0; x < 4; ++x) {
+        const int row = lane + 32 * x;
+        const uint4 a4 = lds128(sb + OFF_SA + 16 * row);
+        const uint32_t a[4] = {a4.x, a4.y, a4.z, a4.w};
+        uint32_t b[4];
+        if (GATE_UP) {
+          const uint4 b4 = lds128(sb + OFF_SB + 16 * row);
+          b[0] = b4.x; b[1] = b4.y; b[2] = b4.z; b[3] = b4.w;
+        } else {
+          const int bs = row % g, bi = row / g;
+          const int byte0 = bs * sfrow + 16 * ks;
+          const uint32_t src = sb + OFF_SB + bs * sub_rows * sub_w + bi * sub_w + (byte0 & 15);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) b[j] = j < nvalid ? lds32(src + 4 * j) : 0u;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          va[4 * j + x] = j < nvalid ? a[j] : 0u;
+          vb[4 * j + x] = b[j];
+        }
       }
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (j >= nvalid) a[j] = 0u;
-      uint32_t* sfa = reinterpret_cast<uint32_t*>(smem + st * C::STAGE_BYTES + OFF_SFA);
-      uint32_t* sfb = reinterpret_cast<uint32_t*>(smem + st * C::STAGE_BYTES + OFF_SFB);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) sfa[j * 128 + ai] = a[j];
-      if (t < BN) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) sfb[(j * C::G + (t >> 7)) * 128 + ai] = b[j];
-      }
-      // make the generic-proxy stores visible to tcgen05.cp, then one arrive per warp
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      const uint32_t sfc = sf_col0 + st * C::SF_COLS + lane_base;
+      tc_st16(sfc, va);
+      tc_st16(sfc + 16, vb);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sf_ready[st]);
     }
