@@ -388,20 +388,28 @@ __device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&v)[16])
         "r"(v[14]), "r"(v[15])
       : "memory");
 }
-__device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
+// Two groups of 32 consecutive 32-bit TMEM columns of this warp's lanes, then the wait:
+// one asm statement, so no use of the results can be scheduled before the wait.
+__device__ __forceinline__ void tc_ld32x2(uint32_t taddr0, uint32_t taddr1, float (&a)[32],
+                                          float (&b)[32]) {
+  uint32_t r[64];
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]),"=r"(r[1]),"=r"(r[2]),"=r"(r[3]),"=r"(r[4]),"=r"(r[5]),"=r"(r[6]),"=r"(r[7]),"=r"(r[8]),"=r"(r[9]),"=r"(r[10]),"=r"(r[11]),"=r"(r[12]),"=r"(r[13]),"=r"(r[14]),"=r"(r[15]),"=r"(r[16]),"=r"(r[17]),"=r"(r[18]),"=r"(r[19]),"=r"(r[20]),"=r"(r[21]),"=r"(r[22]),"=r"(r[23]),"=r"(r[24]),"=r"(r[25]),"=r"(r[26]),"=r"(r[27]),"=r"(r[28]),"=r"(r[29]),"=r"(r[30]),"=r"(r[31]),"=r"(r[32]),"=r"(r[33]),"=r"(r[34]),"=r"(r[35]),"=r"(r[36]),"=r"(r[37]),"=r"(r[38]),"=r"(r[39]),"=r"(r[40]),"=r"(r[41]),"=r"(r[42]),"=r"(r[43]),"=r"(r[44]),"=r"(r[45]),"=r"(r[46]),"=r"(r[47]),"=r"(r[48]),"=r"(r[49]),"=r"(r[50]),"=r"(r[51]),"=r"(r[52]),"=r"(r[53]),"=r"(r[54]),"=r"(r[55]),"=r"(r[56]),"=r"(r[57]),"=r"(r[58]),"=r"(r[59]),"=r"(r[60]),"=r"(r[61]),"=r"(r[62]),"=r"(r[63])
+      : "r"(taddr0), "r"(taddr1)
+      : "memory");
 #pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+  for (int i = 0; i < 32; ++i) {
+    a[i] = __uint_as_float(r[i]);
+    b[i] = __uint_as_float(r[32 + i]);
+  }
+}
+
+// 2^e as a float, exact for -149 <= e <= 127 (subnormal below -126).
+__device__ __forceinline__ float pow2f(int e) {
+  return e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(1u << (e + 149));
 }
 
 // ---------------------------------------------------------------------------
@@ -449,7 +457,8 @@ struct Cfg {
   // empty barrier (committed behind the MMAs that read it) has completed
   static constexpr int TMEM_COLS_USED = ACC_COLS + STAGES * SF_COLS;
   static constexpr int TMEM_COLS = TMEM_COLS_USED <= 256 ? 256 : 512;
-  static constexpr int THREADS = 320;               // 10 warps
+  static constexpr int EPI_WARPS = 8;               // two per TMEM lane quarter
+  static constexpr int THREADS = 32 * (6 + EPI_WARPS);   // TMA, MMA, 4 transposers, epilogue
   static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
   static_assert(TMEM_COLS_USED <= 512, "TMEM budget");
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
@@ -469,7 +478,7 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
 }
 
 template <int BN, bool GATE_UP>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(448, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
             const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
             const GemmArgs args) {
@@ -477,9 +486,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // full[s]: the stage's code tiles landed and its scale factors are in TMEM (TMA bytes +
+  // one arrive per transposer warp); stg_full[s]: the scale staging images landed.
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
-  uint64_t* sf_ready = full + C::STAGES;
-  uint64_t* empty = sf_ready + C::STAGES;
+  uint64_t* stg_full = full + C::STAGES;
+  uint64_t* empty = stg_full + C::STAGES;
   uint64_t* acc_full = empty + C::STAGES;           // [2]
   uint64_t* acc_empty = acc_full + 2;               // [2]
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + 2);
@@ -497,13 +508,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&full[s], 1);                        // TMA expect_tx
-      mbar_init(&sf_ready[s], 4);                    // one arrive per transposing warp
+      mbar_init(&full[s], 1 + 4);                    // TMA expect_tx + 4 transposer warps
+      mbar_init(&stg_full[s], 1);                    // TMA expect_tx
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 4);
+      mbar_init(&acc_empty[b], C::EPI_WARPS);
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -524,39 +535,50 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      constexpr uint32_t tx = C::A_BYTES + C::B_BYTES + C::SA_STG + (GATE_UP ? C::SB_STG : 0);
+      constexpr uint32_t tx_codes = C::A_BYTES + C::B_BYTES;
       const int g = args.b_sf_group;
-      const uint32_t tx_b_sf = GATE_UP ? 0u : (uint32_t)(g == 1 ? BN * 16 : BN * 32);
+      const uint32_t tx_stg = C::SA_STG + (GATE_UP ? C::SB_STG : (uint32_t)(g == 1 ? BN * 16 : BN * 32));
       const int sub_rows = BN / g, sub_w = g == 1 ? 16 : 32;
       int it = 0;
+      // work descriptors are fetched two works ahead (a DOWN work is only a few stages)
+      const int w1 = blockIdx.x + gridDim.x;
       int4 tile = blockIdx.x < n_work ? tlist[blockIdx.x / args.n_tiles_n] : make_int4(0, 0, 0, 0);
+      int4 next = w1 < n_work ? tlist[w1 / args.n_tiles_n] : tile;
       for (int w = blockIdx.x; w < n_work && !*abort_flag; w += gridDim.x) {
-        const int wn = w + gridDim.x;                // next work's descriptor, fetched early
-        const int4 next = wn < n_work ? tlist[wn / args.n_tiles_n] : tile;
+        const int w2 = w + 2 * gridDim.x;
+        const int4 next2 = w2 < n_work ? tlist[w2 / args.n_tiles_n] : next;
         const int n0 = (w % args.n_tiles_n) * C::OUT_N;
         const int brow = tile.z * args.rows_per_expert + n0;
         for (int ks = 0; ks < k_stages; ++ks, ++it) {
           const int st = it % C::STAGES;
           if (!mbar_wait(&empty[st], ((it / C::STAGES) & 1) ^ 1, abort_flag, args.err)) break;
           unsigned char* sb = smem + st * C::STAGE_BYTES;
-          mbar_expect_tx(&full[st], tx + tx_b_sf);
+          mbar_expect_tx(&stg_full[st], tx_stg);
+          mbar_expect_tx(&full[st], tx_codes);
+          // scale staging first: the transposers can start while the code tiles stream in
+          tma_load_2d(sb + OFF_SA, &tmap_sfa, ks * 16, tile.x, &stg_full[st]);
+          if (GATE_UP) {
+            tma_load_2d(sb + OFF_SB, &tmap_sfb, ks * 16, brow, &stg_full[st]);
+            tma_load_2d(sb + OFF_SB + C::SB_STG / 2, &tmap_sfb, ks * 16, brow + args.F,
+                        &stg_full[st]);
+          } else {
+            for (int s2 = 0; s2 < g; ++s2) {
+              const int x = ((s2 * sfrow + 16 * ks) >> 4) << 4;
+              tma_load_2d(sb + OFF_SB + s2 * sub_rows * sub_w, &tmap_sfb, x, brow / g,
+                          &stg_full[st]);
+            }
+          }
           tma_load_2d(sb, &tmap_a, ks * C::KB, tile.x, &full[st]);
-          tma_load_2d(sb + OFF_SA, &tmap_sfa, ks * 16, tile.x, &full[st]);
           if (GATE_UP) {
             tma_load_2d(sb + C::A_BYTES, &tmap_b, ks * C::KB, brow, &full[st]);
             tma_load_2d(sb + C::A_BYTES + C::B_BYTES / 2, &tmap_b, ks * C::KB, brow + args.F,
                         &full[st]);
-            tma_load_2d(sb + OFF_SB, &tmap_sfb, ks * 16, brow, &full[st]);
-            tma_load_2d(sb + OFF_SB + C::SB_STG / 2, &tmap_sfb, ks * 16, brow + args.F, &full[st]);
           } else {
             tma_load_2d(sb + C::A_BYTES, &tmap_b, ks * C::KB, brow, &full[st]);
-            for (int s2 = 0; s2 < g; ++s2) {
-              const int x = ((s2 * sfrow + 16 * ks) >> 4) << 4;
-              tma_load_2d(sb + OFF_SB + s2 * sub_rows * sub_w, &tmap_sfb, x, brow / g, &full[st]);
-            }
           }
         }
         tile = next;
+        next = next2;
       }
       // drain: wait (bounded) until every issued stage has landed
       if (*abort_flag) {
@@ -564,7 +586,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
           if (it <= s) continue;
           const int last = s + ((it - 1 - s) / C::STAGES) * C::STAGES;   // last issue on s
           const uint64_t t0 = global_ns();
-          while (!mbar_try(&full[s], (last / C::STAGES) & 1) &&
+          // full also needs the transposers, which may have stopped: its wait is bounded
+          while ((!mbar_try(&stg_full[s], (last / C::STAGES) & 1) ||
+                  !mbar_try(&full[s], (last / C::STAGES) & 1)) &&
                  global_ns() - t0 < 100000000ull) {
           }
         }
@@ -589,8 +613,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         uint32_t par = (it / C::STAGES) & 1;
         for (int ks = 0; ks < k_stages; ++ks, ++it) {
           // code tiles (TMA) and scale factors in TMEM (transposers) of the stage
-          if (!mbar_wait(&full[st], par, abort_flag, args.err) ||
-              !mbar_wait(&sf_ready[st], par, abort_flag, args.err)) { ok = false; break; }
+          if (!mbar_wait(&full[st], par, abort_flag, args.err)) { ok = false; break; }
           tc_fence_after();
           const uint64_t so = (uint64_t)((st * C::STAGE_BYTES) >> 4);
           const uint32_t sfc = sf_col0 + st * C::SF_COLS;
@@ -621,7 +644,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     for (int it = 0; it < n_it; ++it) {
       const int st = it % C::STAGES;
       const int ks = it % k_stages;
-      if (!mbar_wait_warp(&full[st], (it / C::STAGES) & 1, abort_flag, args.err)) break;
+      if (!mbar_wait_warp(&stg_full[st], (it / C::STAGES) & 1, abort_flag, args.err)) break;
       tc_fence_after();
       const uint32_t sb = smem_u32(smem + st * C::STAGE_BYTES);
       const int nvalid = min(4, (sfrow - 16 * ks) >> 2);   // u32 words of this stage in a row
@@ -654,11 +677,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sf_ready[st]);
+      if (lane == 0) mbar_arrive(&full[st]);
     }
   } else {
-    // ---------------- epilogue (warps 6..9 -> TMEM lane quarters 2,3,0,1) ----------------
+    // ---------------- epilogue (warps 6..13: lane quarter warp % 4, column half) ----------
+    static_assert(C::THREADS == 448 && C::EPI_WARPS == 8, "epilogue warp map");
     const int quarter = warp & 3;
+    const int half = (warp - 6) >> 2;
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     int tcount = 0;
@@ -668,48 +693,54 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
       const int n0 = (w % args.n_tiles_n) * C::OUT_N;
       const bool valid = row < tile.y;
       const int pos = tile.x + row;
-      const int sx = (GATE_UP && valid) ? args.a_exp[pos] : 0;
+      const int sx = GATE_UP ? (valid ? args.a_exp[pos] : 0) : -args.down_shift;
+      // x * 2^sx is one exact-power-of-two multiply when 2^sx is a float, else ldexpf
+      const bool fast = sx >= -149 && sx <= 127;
+      const float m = fast ? pow2f(sx) : 0.0f;
       if (!mbar_wait_warp(&acc_full[ab], (tcount >> 1) & 1, abort_flag, args.err)) break;
       tc_fence_after();
       const uint32_t acc = acc_col + ab * BN + lane_base;
       if (GATE_UP) {
+        // this warp: accumulator columns [32*half, +32) (gate) and BN/2 + the same (up)
         float* orow = reinterpret_cast<float*>(args.out) + (size_t)(valid ? pos : 0) * args.out_cols + n0;
-#pragma unroll 1
-        for (int c = 0; c < BN / 64; ++c) {
-          float g[32], u[32];
-          tc_ld32(acc + c * 32, g);
-          tc_ld32(acc + BN / 2 + c * 32, u);
-          if (valid) {
+        static_assert(BN / 64 == 2, "one 32-column chunk per epilogue warp");
+        float g[32], u[32];
+        tc_ld32x2(acc + half * 32, acc + BN / 2 + half * 32, g, u);
+        if (valid) {
 #pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-              float4 o;
-              o.x = silu_f(ldexpf(g[i], sx)) * ldexpf(u[i], sx);
-              o.y = silu_f(ldexpf(g[i + 1], sx)) * ldexpf(u[i + 1], sx);
-              o.z = silu_f(ldexpf(g[i + 2], sx)) * ldexpf(u[i + 2], sx);
-              o.w = silu_f(ldexpf(g[i + 3], sx)) * ldexpf(u[i + 3], sx);
-              *reinterpret_cast<float4*>(orow + c * 32 + i) = o;
+          for (int i = 0; i < 32; i += 4) {
+            float o[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float gg = fast ? g[i + q] * m : ldexpf(g[i + q], sx);
+              const float uu = fast ? u[i + q] * m : ldexpf(u[i + q], sx);
+              o[q] = silu_f(gg) * uu;
             }
+            *reinterpret_cast<float4*>(orow + half * 32 + i) = make_float4(o[0], o[1], o[2], o[3]);
           }
         }
       } else {
+        // this warp: accumulator columns [64*half, +64) -> f16 partials
         __half* orow = reinterpret_cast<__half*>(args.out) + (size_t)(valid ? pos : 0) * args.out_cols + n0;
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          float v[32];
-          tc_ld32(acc + c * 32, v);
-          if (valid) {
+        static_assert(BN / 32 == 4, "two 32-column chunks per epilogue warp");
+        float v[2][32];
+        tc_ld32x2(acc + half * 64, acc + half * 64 + 32, v[0], v[1]);
+        if (valid) {
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
 #pragma unroll
             for (int i = 0; i < 32; i += 8) {
               uint32_t pk[4];
 #pragma unroll
               for (int q = 0; q < 4; ++q) {
-                const __half2 h2 = __floats2half2_rn(ldexpf(v[i + 2 * q], -args.down_shift),
-                                                     ldexpf(v[i + 2 * q + 1], -args.down_shift));
+                const float a0 = fast ? v[c][i + 2 * q] * m : ldexpf(v[c][i + 2 * q], sx);
+                const float a1 = fast ? v[c][i + 2 * q + 1] * m : ldexpf(v[c][i + 2 * q + 1], sx);
+                const __half2 h2 = __floats2half2_rn(a0, a1);
                 pk[q] = *reinterpret_cast<const uint32_t*>(&h2);
               }
-              *reinterpret_cast<uint4*>(orow + c * 32 + i) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              *reinterpret_cast<uint4*>(orow + half * 64 + c * 32 + i) =
+                  make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
-          }
         }
       }
       tc_fence_before();
