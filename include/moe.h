@@ -118,8 +118,6 @@ typedef struct moe_ws_layout {
                           z * 2^-(qh_exp[row] + c_F), c_F the smallest shift with
                           F * 2688^2 * 2^-c_F < 2^15 */
   size_t tiles;        /* prefill: i32 count, pad to 16 B, then int4 {row0, rows, expert, 0} per M-tile */
-  size_t counters;     /* decode: i32 per-call counters (unit queues, per-expert and per-(token,
-                          64-row chunk) arrivals), zeroed by each gate/up call */
 } moe_ws_layout;
 
 /* Limits (MOE_ERR_UNSUPPORTED beyond them): 1 <= k <= min(E, 32); E <= 1024;

@@ -76,7 +76,6 @@ bool compute_layout(int T, int H, int F, int E, int k, int path, moe_ws_layout* 
     L->xe = take(P * sizeof(int32_t));
     L->hg = take(P * F * 2);
     L->he = take(P * sizeof(int32_t));
-    L->counters = take(sizeof(int32_t) * (size_t)decode_counter_count(T, H, E < (int)P ? E : (int)P));
   } else {
     L->qx_codes = take(P * (H / 2));
     L->qx_scales = take(P * (H / 16));
@@ -211,7 +210,9 @@ moe_status moe_grouped_down_combine_nvfp4(const moe_nvfp4_bank* w_down, moe_csr 
     if (ce != cudaSuccess) return MOE_ERR_CUDA;
     return from_cuda(launch_prefill_combine(topk_w, T, H, F, k, L, w, y, s));
   }
-  return from_cuda(launch_decode_down(*w_down, csr, topk_w, T, H, F, k, L, w, y, s));
+  ce = launch_decode_down(*w_down, csr, T, H, F, k, L, w, s);
+  if (ce != cudaSuccess) return MOE_ERR_CUDA;
+  return from_cuda(launch_combine(topk_w, T, H, k, L, w, y, s));
 }
 
 moe_status moe_get_device_error(const void* ws, void* stream, int32_t* code) {

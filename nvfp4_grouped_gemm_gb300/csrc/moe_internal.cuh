@@ -34,12 +34,10 @@ cudaError_t launch_build_csr(const int32_t* ids, int P, int k, int E, moe_csr cs
 cudaError_t launch_decode_gate_up(const uint16_t* x_bf16, int T, int H, int F, int k,
                                   const moe_nvfp4_bank& b, moe_csr csr, const moe_ws_layout& L,
                                   char* ws, cudaStream_t s);
-cudaError_t launch_decode_down(const moe_nvfp4_bank& b, moe_csr csr, const float* w, int T, int H,
-                               int F, int k, const moe_ws_layout& L, char* ws, float* y,
-                               cudaStream_t s);
-// Number of int32 counters the decode path keeps in the workspace (A = bound on the
-// number of active experts).
-int decode_counter_count(int T, int H, int A);
+cudaError_t launch_decode_down(const moe_nvfp4_bank& b, moe_csr csr, int T, int H, int F, int k,
+                               const moe_ws_layout& L, char* ws, cudaStream_t s);
+cudaError_t launch_combine(const float* w, int T, int H, int k, const moe_ws_layout& L, char* ws,
+                           float* y, cudaStream_t s);
 cudaError_t launch_prefill_gate_up(const uint16_t* x_bf16, int T, int H, int F, int k,
                                    const moe_nvfp4_bank& b, moe_csr csr, const moe_ws_layout& L,
                                    char* ws, cudaStream_t s, bool* unsupported);
