@@ -148,7 +148,8 @@ moe_status moe_route_topk(const float* logits, int32_t T, int32_t E, int32_t k,
  * expert that keeps ascending p within an expert (placement by prefix sums, not by
  * atomic arrival order, so the result is bit-exact and deterministic). topk_ids i32
  * [T][k]. Writes `csr` and the workspace's pair_pos; ids outside [0, E) set
- * MOE_DEVERR_EXPERT_ID and are left out. */
+ * MOE_DEVERR_EXPERT_ID and are left out. From T*k >= 4096 pairs it also keeps per-chunk
+ * counts in the workspace's h region (which the gate/up call overwrites afterwards). */
 moe_status moe_build_expert_csr(const int32_t* topk_ids, int32_t T, int32_t k, int32_t E,
                                 moe_csr csr, void* ws, size_t ws_bytes, void* stream);
 

@@ -151,10 +151,15 @@ moe_status moe_build_expert_csr(const int32_t* topk_ids, int32_t T, int32_t k, i
   if (!compute_layout(T, 256, 64, E, k, MOE_PATH_DECODE, &L)) return MOE_ERR_UNSUPPORTED;
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MOE_ERR_WORKSPACE;
   if (ws_bytes < L.pair_pos + (size_t)T * k * sizeof(int32_t)) return MOE_ERR_WORKSPACE;
+  // many pairs: the grid-wide build keeps per-chunk counts in the h region (written only
+  // later, by the gate/up call); it needs that much workspace
+  const size_t scratch = csr_scratch_bytes(T * k, E);
+  if (scratch && ws_bytes < L.h + scratch) return MOE_ERR_WORKSPACE;
   char* w = static_cast<char*>(ws);
   return from_cuda(launch_build_csr(topk_ids, T * k, k, E, csr,
                                     reinterpret_cast<int32_t*>(w + L.pair_pos),
                                     reinterpret_cast<uint32_t*>(w + L.error_word),
+                                    scratch ? reinterpret_cast<int32_t*>(w + L.h) : nullptr,
                                     static_cast<cudaStream_t>(stream)));
 }
 

@@ -29,8 +29,12 @@ int resolve_path(int T, int k, int path);
 // Launchers (return cudaGetLastError() of the launch sequence).
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w,
                               cudaStream_t s);
+// With `scratch` (csr_scratch_bytes(P, E) bytes, nonzero from kCsrGridMinPairs pairs)
+// the CSR is built by three grid-wide kernels, else by one CTA.
+constexpr int kCsrGridMinPairs = 4096;
+size_t csr_scratch_bytes(int P, int E);
 cudaError_t launch_build_csr(const int32_t* ids, int P, int k, int E, moe_csr csr,
-                             int32_t* pair_pos, uint32_t* err, cudaStream_t s);
+                             int32_t* pair_pos, uint32_t* err, int32_t* scratch, cudaStream_t s);
 cudaError_t launch_decode_gate_up(const uint16_t* x_bf16, int T, int H, int F, int k,
                                   const moe_nvfp4_bank& b, moe_csr csr, const moe_ws_layout& L,
                                   char* ws, cudaStream_t s);

@@ -11,6 +11,11 @@
 // expert in earlier slices), pass C walks each slice in ascending p and places pairs with
 // a warp-level match so that equal experts keep ascending p.  Placement never depends on
 // the order atomics happen to arrive in, so the output is bit-exact.
+//
+// For many pairs the same three passes run over the whole grid: csr_count_kernel counts
+// each 2048-pair chunk's pairs per expert, csr_scan_kernel turns the [chunk][expert]
+// counts into each chunk's first row per expert (plus the offsets and the active list),
+// csr_place_kernel places each chunk's pairs as above within the chunk.
 #include <mutex>
 
 #include "moe_internal.cuh"
@@ -212,6 +217,110 @@ build_csr_kernel(const int32_t* __restrict__ ids_g, int P, int E, int32_t* __res
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// grid-wide CSR for many pairs
+// ---------------------------------------------------------------------------
+constexpr int kChunkPairs = 2048;
+constexpr int kChunkThreads = 256;
+constexpr int kChunkWarps = kChunkThreads / 32;
+
+__global__ void __launch_bounds__(kChunkThreads)
+csr_count_kernel(const int32_t* __restrict__ ids, int P, int E, int32_t* __restrict__ cnt,
+                 int32_t* __restrict__ pair_pos, uint32_t* __restrict__ err) {
+  extern __shared__ int hist[];                // [E]
+  for (int i = threadIdx.x; i < E; i += kChunkThreads) hist[i] = 0;
+  pdl_wait();                                  // the expert ids are complete
+  pdl_trigger();
+  __syncthreads();
+  const int p0 = blockIdx.x * kChunkPairs, p1 = min(P, p0 + kChunkPairs);
+  bool bad = false;
+  for (int p = p0 + (int)threadIdx.x; p < p1; p += kChunkThreads) {
+    const int e = __ldg(ids + p);
+    if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
+    else { bad = true; pair_pos[p] = -1; }
+  }
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(err, (uint32_t)MOE_DEVERR_EXPERT_ID);
+  __syncthreads();
+  for (int i = threadIdx.x; i < E; i += kChunkThreads) cnt[(size_t)blockIdx.x * E + i] = hist[i];
+}
+
+// One CTA of kCsrThreads: thread e turns expert e's per-chunk counts into chunk starts.
+__global__ void __launch_bounds__(kCsrThreads, 1)
+csr_scan_kernel(int32_t* __restrict__ cnt, int n_chunks, int E, int32_t* __restrict__ offsets,
+                int32_t* __restrict__ active, int32_t* __restrict__ n_active) {
+  __shared__ int scratch[kCsrWarps];
+  pdl_wait();
+  pdl_trigger();
+  const int e = threadIdx.x;
+  int tot = 0;
+  if (e < E)
+    for (int b = 0; b < n_chunks; ++b) {
+      const int c = cnt[(size_t)b * E + e];
+      cnt[(size_t)b * E + e] = tot;
+      tot += c;
+    }
+  int total, act_total;
+  const int off = block_exclusive_scan(e < E ? tot : 0, scratch, &total);
+  const int act = block_exclusive_scan((e < E && tot > 0) ? 1 : 0, scratch, &act_total);
+  if (e < E) {
+    offsets[e] = off;
+    if (tot > 0) active[act] = e;
+    for (int b = 0; b < n_chunks; ++b) cnt[(size_t)b * E + e] += off;
+  }
+  if (e == 0) {
+    offsets[E] = total;
+    *n_active = act_total;
+  }
+}
+
+__global__ void __launch_bounds__(kChunkThreads)
+csr_place_kernel(const int32_t* __restrict__ ids, int P, int E, const int32_t* __restrict__ cnt,
+                 int32_t* __restrict__ pair_ids, int32_t* __restrict__ pair_pos) {
+  extern __shared__ int wh[];                  // [kChunkWarps][E]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < kChunkWarps * E; i += kChunkThreads) wh[i] = 0;
+  pdl_wait();                                  // the chunk starts are complete
+  pdl_trigger();
+  __syncthreads();
+  const int p0 = blockIdx.x * kChunkPairs, p1 = min(P, p0 + kChunkPairs);
+  const int slice = (p1 - p0 + kChunkWarps - 1) / kChunkWarps;
+  const int s0 = min(p1, p0 + warp * slice), s1 = min(p1, s0 + slice);
+  int* my = wh + warp * E;
+  for (int p = s0 + lane; p < s1; p += 32) {
+    const int e = __ldg(ids + p);
+    if (e >= 0 && e < E) atomicAdd(&my[e], 1);
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += kChunkThreads) {
+    int run = cnt[(size_t)blockIdx.x * E + e];
+    for (int w = 0; w < kChunkWarps; ++w) {
+      const int c = wh[w * E + e];
+      wh[w * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  for (int base = s0; base < s1; base += 32) {
+    const int p = base + lane;
+    const bool in = p < s1;
+    int e = in ? __ldg(ids + p) : -1;
+    const bool valid = in && e >= 0 && e < E;
+    if (!valid) e = -1 - lane;                 // unique key: matches nobody
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const unsigned lower = peers & ((1u << lane) - 1u);
+    const int start = valid ? my[e] : 0;
+    __syncwarp();
+    if (valid) {
+      const int pos = start + __popc(lower);
+      pair_ids[pos] = p;
+      pair_pos[p] = pos;
+      if (lower == 0) my[e] = start + __popc(peers);
+    }
+    __syncwarp();
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w,
@@ -226,9 +335,28 @@ cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t*
   return launch_pdl(route_topk_kernel<32>, grid, block, 0, s, logits, T, E, k, ids, w);
 }
 
+size_t csr_scratch_bytes(int P, int E) {
+  if (P < kCsrGridMinPairs) return 0;
+  return (size_t)((P + kChunkPairs - 1) / kChunkPairs) * E * sizeof(int32_t);
+}
+
 cudaError_t launch_build_csr(const int32_t* ids, int P, int k, int E, moe_csr csr,
-                             int32_t* pair_pos, uint32_t* err, cudaStream_t s) {
+                             int32_t* pair_pos, uint32_t* err, int32_t* scratch, cudaStream_t s) {
   (void)k;
+  if (P >= kCsrGridMinPairs && scratch) {
+    const int nb = (P + kChunkPairs - 1) / kChunkPairs;
+    cudaError_t st = launch_pdl(csr_count_kernel, dim3(nb), dim3(kChunkThreads),
+                                (size_t)E * sizeof(int), s, ids, P, E, scratch, pair_pos, err);
+    if (st != cudaSuccess) return st;
+    st = launch_pdl(csr_scan_kernel, dim3(1), dim3(kCsrThreads), 0, s, scratch, nb, E,
+                    csr.expert_offsets, csr.active_experts, csr.n_active);
+    if (st != cudaSuccess) return st;
+    const size_t smem = (size_t)kChunkWarps * E * sizeof(int);
+    st = cudaFuncSetAttribute(csr_place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (st != cudaSuccess) return st;
+    return launch_pdl(csr_place_kernel, dim3(nb), dim3(kChunkThreads), smem, s, ids, P, E,
+                      (const int32_t*)scratch, csr.pair_ids, pair_pos);
+  }
   size_t smem = (size_t)(kCsrWarps * E + kCsrWarps) * sizeof(int);
   const int ids_in_smem = smem + (size_t)P * sizeof(int) <= 200 * 1024 ? 1 : 0;
   if (ids_in_smem) smem += (size_t)P * sizeof(int);
@@ -290,6 +418,6 @@ extern "C" moe_status moe_build_expert_csr_static(const int32_t* topk_ids, int32
   // and never read back by this entry point, so nothing needs clearing between calls
   cudaError_t st = launch_build_csr(topk_ids, T * k, k, E, csr, scratch,
                                     reinterpret_cast<uint32_t*>(scratch + kStaticMaxPairs),
-                                    static_cast<cudaStream_t>(stream));
+                                    nullptr, static_cast<cudaStream_t>(stream));
   return st == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

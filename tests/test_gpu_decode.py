@@ -126,6 +126,31 @@ def test_single_token_single_expert():
     _check_layer(one, run)
 
 
+def test_csr_many_pairs_with_invalid_ids():
+    """The grid-wide CSR (thousands of pairs) skips and flags out-of-range ids, keeps the
+    rest in ascending pair order, and writes -1 as their CSR position."""
+    T, k, E = 700, 8, 96
+    rng = np.random.default_rng(5)
+    ids = synth.skewed_ids(rng, T, k, E)
+    bad = rng.choice(T * k, size=37, replace=False)
+    ids.reshape(-1)[bad[:20]] = E + 3
+    ids.reshape(-1)[bad[20:]] = -1
+    csr = moe.ExpertCSR(E, T * k)
+    ws = torch.zeros(moe.workspace_bytes(T, 256, 64, E, k, moe.PATH_DECODE), dtype=torch.uint8,
+                     device="cuda")
+    moe.moe_build_expert_csr(torch.from_numpy(ids).cuda(), E, csr, ws)
+    torch.cuda.synchronize()
+    ref = oracle.build_expert_csr(ids, E)
+    assert np.array_equal(csr.expert_offsets.cpu().numpy(), ref.offsets)
+    assert np.array_equal(csr.pair_ids.cpu().numpy()[:int(ref.offsets[-1])], ref.pair_ids)
+    assert int(csr.n_active.item()) == ref.n_active
+    assert np.array_equal(csr.active_experts.cpu().numpy()[:ref.n_active], ref.active)
+    L = moe.workspace_layout(T, 256, 64, E, k, moe.PATH_DECODE)
+    pos = ws[L["pair_pos"]:L["pair_pos"] + 4 * T * k].view(torch.int32).cpu().numpy()
+    assert np.array_equal(pos, ref.pair_pos)
+    assert moe.get_device_error(ws) & moe.DEVERR_EXPERT_ID
+
+
 def test_invalid_expert_ids_are_flagged_and_skipped():
     wl = synth.tiny(seed=4)
     ids = np.array([[1, 3], [99, 3], [-2, 0], [7, 7]], np.int32)
@@ -177,7 +202,8 @@ def test_route_ties_to_lower_id():
     assert np.allclose(w.cpu().numpy(), ref_w, rtol=2e-6)
 
 
-@pytest.mark.parametrize("T,k,E", [(4096, 8, 288), (1, 1, 1), (3, 7, 1024), (2048, 1, 64)])
+@pytest.mark.parametrize("T,k,E", [(4096, 8, 288), (1, 1, 1), (3, 7, 1024), (2048, 1, 64),
+                                   (1000, 5, 1024), (600, 7, 7)])
 def test_csr_bit_exact_large(T, k, E):
     rng = np.random.default_rng(T + E)
     ids = synth.skewed_ids(rng, T, k, E)
