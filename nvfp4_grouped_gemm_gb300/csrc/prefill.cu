@@ -85,6 +85,17 @@ __device__ __forceinline__ uint32_t e2m1_mag(float key, float sbv) {
 }
 
 // Row exponent: smallest s with amax <= 2688 * 2^s (2688 = 0.65625 * 2^12).
+// 2^e as a float, exact for -149 <= e <= 127 (subnormal below -126).
+__device__ __forceinline__ float pow2f(int e) {
+  return e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(1u << (e + 149));
+}
+
+// |v| * 2^-s: one multiply by the exact power of two when 2^-s is a float (the same
+// correctly rounded value as ldexpf), else ldexpf.
+__device__ __forceinline__ float scale_down(float v, int s, bool fast, float m) {
+  return fast ? v * m : ldexpf(v, -s);
+}
+
 __device__ __forceinline__ int row_exp_of(float amax) {
   if (!(amax > 0.0f)) return 0;
   int ea;
@@ -154,6 +165,8 @@ __global__ void __launch_bounds__(1024) tiles_kernel(const int32_t* __restrict__
 // ---------------------------------------------------------------------------
 // Q(x): one warp per token, the result copied to each of the token's CSR rows
 // ---------------------------------------------------------------------------
+// Lane l takes blocks l, l+32, ...: one pass for the row amax, a second (from L1) for the
+// block scales and codes.
 __global__ void __launch_bounds__(256) quant_x_kernel(const uint16_t* __restrict__ x, int T, int H,
                                                       int k, const int32_t* __restrict__ pair_pos,
                                                       uint8_t* __restrict__ qc,
@@ -167,7 +180,7 @@ __global__ void __launch_bounds__(256) quant_x_kernel(const uint16_t* __restrict
   float amax = 0.0f;
   for (int b = lane; b < nblk; b += 32) {
     const uint4* p = reinterpret_cast<const uint4*>(row + b * 16);
-    const uint4 v0 = p[0], v1 = p[1];
+    const uint4 v0 = __ldg(p), v1 = __ldg(p + 1);
     const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -178,40 +191,48 @@ __global__ void __launch_bounds__(256) quant_x_kernel(const uint16_t* __restrict
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   const int s = row_exp_of(amax);
-  int pos[kMaxK];
-  for (int j = 0; j < k; ++j) pos[j] = pair_pos[(size_t)t * k + j];
-  if (lane == 0)
-    for (int j = 0; j < k; ++j)
-      if (pos[j] >= 0) qe[pos[j]] = s;
-  for (int b = lane; b < nblk; b += 32) {
-    const uint4* p = reinterpret_cast<const uint4*>(row + b * 16);
-    const uint4 v0 = p[0], v1 = p[1];
-    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    float key[16];
-    uint32_t neg = 0;
-    float bmax = 0.0f;
+  const bool fast = s >= -127 && s <= 149;
+  const float m = fast ? pow2f(-s) : 0.0f;
+  // lane j < k holds the CSR row of pair (t, j) (k <= 32)
+  const int mypos = lane < k ? pair_pos[(size_t)t * k + lane] : -1;
+  if (mypos >= 0) qe[mypos] = s;
+  for (int b0 = 0; b0 < nblk; b0 += 32) {          // warp-uniform
+    const int b = b0 + lane;
+    const bool has = b < nblk;
+    uint64_t codes = 0;
+    int sbc = 0;
+    if (has) {
+      const uint4* p = reinterpret_cast<const uint4*>(row + b * 16);
+      const uint4 v0 = __ldg(p), v1 = __ldg(p + 1);
+      const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+      float key[16];
+      uint32_t neg = 0;
+      float bmax = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
-      key[2 * i] = ldexpf(fabsf(lo), -s);
-      key[2 * i + 1] = ldexpf(fabsf(hi), -s);
-      neg |= (lo < 0.0f ? 1u : 0u) << (2 * i);
-      neg |= (hi < 0.0f ? 1u : 0u) << (2 * i + 1);
-      bmax = fmaxf(bmax, fmaxf(key[2 * i], key[2 * i + 1]));
+      for (int i = 0; i < 8; ++i) {
+        const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
+        key[2 * i] = scale_down(fabsf(lo), s, fast, m);
+        key[2 * i + 1] = scale_down(fabsf(hi), s, fast, m);
+        neg |= (lo < 0.0f ? 1u : 0u) << (2 * i);
+        neg |= (hi < 0.0f ? 1u : 0u) << (2 * i + 1);
+        bmax = fmaxf(bmax, fmaxf(key[2 * i], key[2 * i + 1]));
+      }
+      sbc = ue4m3_code_of(bmax);
+      codes = quant_block(key, neg, sbc);
     }
-    const int sbc = ue4m3_code_of(bmax);
-    const uint64_t codes = quant_block(key, neg, sbc);
     for (int j = 0; j < k; ++j) {
-      if (pos[j] < 0) continue;
-      *reinterpret_cast<uint64_t*>(qc + (size_t)pos[j] * (H / 2) + b * 8) = codes;
-      qs[(size_t)pos[j] * nblk + b] = (uint8_t)sbc;
+      const int pj = __shfl_sync(0xffffffffu, mypos, j);
+      if (!has || pj < 0) continue;
+      *reinterpret_cast<uint64_t*>(qc + (size_t)pj * (H / 2) + b * 8) = codes;
+      qs[(size_t)pj * nblk + b] = (uint8_t)sbc;
     }
   }
 }
 
 // ---------------------------------------------------------------------------
-// Q(h): one warp per CSR row
+// Q(h): one warp per CSR row, the row's blocks in registers as for Q(x)
 // ---------------------------------------------------------------------------
+template <int NB>
 __global__ void __launch_bounds__(256) quant_h_kernel(const float* __restrict__ h, int P, int F,
                                                       int sf_pitch,
                                                       const int32_t* __restrict__ offsets, int E,
@@ -223,33 +244,42 @@ __global__ void __launch_bounds__(256) quant_h_kernel(const float* __restrict__ 
   if (r >= P || r >= offsets[E]) return;
   const float* row = h + (size_t)r * F;
   const int nblk = F / 16;
+  float4 v[NB][4];
   float amax = 0.0f;
-  for (int b = lane; b < nblk; b += 32) {
-    const float4* p = reinterpret_cast<const float4*>(row + b * 16);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float4 v = p[q];
-      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+  for (int i = 0; i < NB; ++i) {
+    const int b = lane + 32 * i;
+    if (b < nblk) {
+      const float4* p = reinterpret_cast<const float4*>(row + b * 16);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        v[i][q] = __ldcs(p + q);
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[i][q].x), fabsf(v[i][q].y)),
+                                 fmaxf(fabsf(v[i][q].z), fabsf(v[i][q].w))));
+      }
     }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   const int s = row_exp_of(amax);
+  const bool fast = s >= -127 && s <= 149;
+  const float m = fast ? pow2f(-s) : 0.0f;
   if (lane == 0) qe[r] = s;
-  for (int b = lane; b < nblk; b += 32) {
-    const float4* p = reinterpret_cast<const float4*>(row + b * 16);
+#pragma unroll
+  for (int i = 0; i < NB; ++i) {
+    const int b = lane + 32 * i;
+    if (b >= nblk) break;
     float key[16];
     uint32_t neg = 0;
     float bmax = 0.0f;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const float4 v = p[q];
-      const float vv[4] = {v.x, v.y, v.z, v.w};
+      const float vv[4] = {v[i][q].x, v[i][q].y, v[i][q].z, v[i][q].w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        key[4 * q + i] = ldexpf(fabsf(vv[i]), -s);
-        neg |= (vv[i] < 0.0f ? 1u : 0u) << (4 * q + i);
-        bmax = fmaxf(bmax, key[4 * q + i]);
+      for (int e = 0; e < 4; ++e) {
+        key[4 * q + e] = scale_down(fabsf(vv[e]), s, fast, m);
+        neg |= (vv[e] < 0.0f ? 1u : 0u) << (4 * q + e);
+        bmax = fmaxf(bmax, key[4 * q + e]);
       }
     }
     const int sbc = ue4m3_code_of(bmax);
@@ -405,11 +435,6 @@ __device__ __forceinline__ void tc_ld32x2(uint32_t taddr0, uint32_t taddr1, floa
     a[i] = __uint_as_float(r[i]);
     b[i] = __uint_as_float(r[32 + i]);
   }
-}
-
-// 2^e as a float, exact for -149 <= e <= 127 (subnormal below -126).
-__device__ __forceinline__ float pow2f(int e) {
-  return e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(1u << (e + 149));
 }
 
 // ---------------------------------------------------------------------------
@@ -896,8 +921,14 @@ cudaError_t launch_prefill_down(const moe_nvfp4_bank& b, moe_csr csr, int T, int
   uint8_t* qs = reinterpret_cast<uint8_t*>(ws + L.qh_scales);
   int32_t* qe = reinterpret_cast<int32_t*>(ws + L.qh_exp);
   const int sfh = qh_scale_pitch(F);
-  quant_h_kernel<<<(P + 7) / 8, 256, 0, s>>>(reinterpret_cast<const float*>(ws + L.h), P, F, sfh,
-                                              csr.expert_offsets, b.E, qc, qs, qe);
+  {
+    const int nb = (F / 16 + 31) / 32;           // blocks per lane
+    if (nb > 8) { *unsupported = true; return cudaSuccess; }
+    auto kq = nb <= 1 ? quant_h_kernel<1> : nb <= 2 ? quant_h_kernel<2>
+            : nb <= 4 ? quant_h_kernel<4> : quant_h_kernel<8>;
+    kq<<<(P + 7) / 8, 256, 0, s>>>(reinterpret_cast<const float*>(ws + L.h), P, F, sfh,
+                                   csr.expert_offsets, b.E, qc, qs, qe);
+  }
   cudaError_t st = cudaGetLastError();
   if (st != cudaSuccess) return st;
   constexpr int BN = 128;
