@@ -69,22 +69,6 @@ __device__ __forceinline__ int ue4m3_code_of(float key) {
   return cand;
 }
 
-// E2M1 magnitude code of key / sbv (key = |v| * 2^-s): the number of midpoints passed
-// (above midpoint j * sbv, or on it when the upper neighbour is even, i.e. j odd).
-__device__ __forceinline__ uint32_t e2m1_mag(float key, float sbv) {
-  // midpoints 0.25 0.75 1.25 1.75 | 2.5 3.5 | 5 between 0 .5 1 1.5 2 3 4 6
-  auto passed = [&](int j) {
-    const float mid = j < 4 ? 0.25f + 0.5f * (float)j : (j == 6 ? 5.0f : (float)j - 1.5f);
-    const float t = mid * sbv;
-    return key > t || ((j & 1) && key == t);
-  };
-  uint32_t c = passed(3) ? 4u : 0u;
-  c += passed((int)c + 1) ? 2u : 0u;
-  c += passed((int)c) ? 1u : 0u;
-  return c;
-}
-
-// Row exponent: smallest s with amax <= 2688 * 2^s (2688 = 0.65625 * 2^12).
 // 2^e as a float, exact for -149 <= e <= 127 (subnormal below -126).
 __device__ __forceinline__ float pow2f(int e) {
   return e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(1u << (e + 149));
@@ -96,6 +80,7 @@ __device__ __forceinline__ float scale_down(float v, int s, bool fast, float m) 
   return fast ? v * m : ldexpf(v, -s);
 }
 
+// Row exponent: smallest s with amax <= 2688 * 2^s (2688 = 0.65625 * 2^12).
 __device__ __forceinline__ int row_exp_of(float amax) {
   if (!(amax > 0.0f)) return 0;
   int ea;
@@ -104,13 +89,24 @@ __device__ __forceinline__ int row_exp_of(float amax) {
 }
 
 // Quantise 16 values (already |v| * 2^-s in `key`, signs in `neg`) with block code sbc.
+// The E2M1 magnitude code of key / scale is the number of midpoints passed between the
+// values 0 .5 1 1.5 2 3 4 6 (midpoints .25 .75 1.25 1.75 2.5 3.5 5).  The seven decision
+// thresholds midpoint * scale are exact f32 products, formed once per block; a key passes
+// an even-indexed threshold when above it and an odd-indexed one when at or above it, so
+// a tie goes to the even code.
 __device__ __forceinline__ uint64_t quant_block(const float (&key)[16], uint32_t negmask, int sbc) {
   if (sbc == 0) return 0ull;
   const float sbv = ue4m3_val(sbc);
+  const float t0 = 0.25f * sbv, t1 = 0.75f * sbv, t2 = 1.25f * sbv, t3 = 1.75f * sbv;
+  const float t4 = 2.5f * sbv, t5 = 3.5f * sbv, t6 = 5.0f * sbv;
   uint64_t out = 0;
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    uint64_t c = e2m1_mag(key[i], sbv) | (((negmask >> i) & 1u) << 3);
+    const float v = key[i];
+    const uint32_t mag = (uint32_t)(v > t0) + (uint32_t)(v >= t1) + (uint32_t)(v > t2) +
+                         (uint32_t)(v >= t3) + (uint32_t)(v > t4) + (uint32_t)(v >= t5) +
+                         (uint32_t)(v > t6);
+    uint64_t c = mag | (((negmask >> i) & 1u) << 3);
     out |= c << (4 * i);
   }
   return out;
