@@ -759,8 +759,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 const __half2 h2 = __floats2half2_rn(a0, a1);
                 pk[q] = *reinterpret_cast<const uint32_t*>(&h2);
               }
-              *reinterpret_cast<uint4*>(orow + half * 64 + c * 32 + i) =
-                  make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              // streaming store: the partials are read once, by the combine
+              __stcs(reinterpret_cast<uint4*>(orow + half * 64 + c * 32 + i),
+                     make_uint4(pk[0], pk[1], pk[2], pk[3]));
             }
         }
       }
