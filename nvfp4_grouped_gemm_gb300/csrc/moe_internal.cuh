@@ -48,6 +48,12 @@ cudaError_t launch_prefill_gate_up(const uint16_t* x_bf16, int T, int H, int F, 
 cudaError_t launch_prefill_down(const moe_nvfp4_bank& b, moe_csr csr, int T, int H, int F, int k,
                                 const moe_ws_layout& L, char* ws, cudaStream_t s,
                                 bool* unsupported);
+cudaError_t launch_quant_x(const uint16_t* x_bf16, int T, int H, int k, const int32_t* pair_pos,
+                           uint8_t* qc, uint8_t* qs, int32_t* qe, cudaStream_t s);
+cudaError_t launch_quant_h(const float* h, int P, int F, int sf_pitch, const int32_t* offsets,
+                           int E, uint8_t* qc, uint8_t* qs, int32_t* qe, cudaStream_t s);
+// Exponent c_F with F * 2688^2 * 2^-c_F < 2^15: the fixed shift of the f16 partials.
+int down_shift_for(int F);
 cudaError_t launch_prefill_combine(const float* w, int T, int H, int F, int k,
                                    const moe_ws_layout& L, char* ws, float* y, cudaStream_t s);
 // Launch with programmatic dependent launch allowed: the kernel may start while its
@@ -72,6 +78,12 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 // ---------------------------------------------------------------------------
 // Device helpers
 // ---------------------------------------------------------------------------
+
+// 2^e as a float, exact for -149 <= e <= 127 (subnormal below -126).
+__device__ __forceinline__ float pow2f(int e) {
+  return e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(1u << (e + 149));
+}
+
 
 // Two E2M1 codes (one byte, low nibble = even element) to an f16x2 (low half = even).
 __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {

@@ -1,0 +1,287 @@
+// Prefill activations and combine:
+//
+//   quant_x_kernel      Q(x): each token's bf16 row to NVFP4 with a power-of-two row scale,
+//                       written to every CSR row of the token's pairs
+//   quant_h_kernel      Q(h) per CSR row
+//   combine_f16_kernel  y[t] = sum_j w[t,j] * z16[pos_j] * 2^(e_j + c_F), ascending j
+//
+// The quantiser Q (the pages never quantise activations; block-scaled FP4 x FP4 needs it):
+// s = smallest integer with amax_row <= 6*448*2^s; block scale = the UE4M3 value nearest
+// to amax_16 / (6*2^s) (ties to the even encoding); code = the E2M1 value nearest to
+// v / (scale*2^s), saturating at 6, ties to even, sign bit iff v < 0.  Every decision is
+// an exact float32 comparison of |v|*2^-s against midpoint*scale products.
+#include <cmath>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+
+namespace {
+
+// ---------------------------------------------------------------------------
+// number formats (device side, written from the format definitions)
+// ---------------------------------------------------------------------------
+
+// Value of UE4M3 encoding b (0 <= b <= 0x7E).
+__device__ __forceinline__ float ue4m3_val(int b) {
+  const int e = b >> 3, m = b & 7;
+  if (e == 0) return (float)m * (1.0f / 512.0f);                    // m/8 * 2^-6
+  return __uint_as_float((uint32_t)(e + 120) << 23 | (uint32_t)m << 20);   // (1+m/8)*2^(e-7)
+}
+
+// Decision threshold between UE4M3 encodings j and j+1, times 6: 3 * (v(j) + v(j+1)).
+__device__ __forceinline__ float ue4m3_thr6(int j) { return 3.0f * (ue4m3_val(j) + ue4m3_val(j + 1)); }
+
+// Threshold j "passed" by key: above it, or on it when the upper neighbour is the even code.
+__device__ __forceinline__ bool ue4m3_passed(float key, int j) {
+  const float t = ue4m3_thr6(j);
+  return key > t || (key == t && ((j + 1) & 1) == 0);
+}
+
+// Nearest UE4M3 encoding to key/6 (key = block amax * 2^-s <= 2688), ties to even: the
+// number of thresholds passed.  A first guess from the float bits of key/6 is corrected
+// by exact comparisons with the neighbouring thresholds.
+__device__ __forceinline__ int ue4m3_code_of(float key) {
+  const float r = key * (1.0f / 6.0f);
+  int cand;
+  if (r < 0.015625f) {
+    cand = (int)(r * 512.0f);                        // subnormal encodings m/8 * 2^-6
+  } else {
+    const uint32_t b = __float_as_uint(r);
+    const int e = (int)((b >> 23) & 0xff) - 127;       // -6 .. 8
+    cand = ((e + 7) << 3) | (int)((b >> 20) & 7);
+  }
+  cand = min(max(cand, 0), 126);
+  while (cand < 126 && ue4m3_passed(key, cand)) ++cand;
+  while (cand > 0 && !ue4m3_passed(key, cand - 1)) --cand;
+  return cand;
+}
+
+// |v| * 2^-s: one multiply by the exact power of two when 2^-s is a float (the same
+// correctly rounded value as ldexpf), else ldexpf.
+__device__ __forceinline__ float scale_down(float v, int s, bool fast, float m) {
+  return fast ? v * m : ldexpf(v, -s);
+}
+
+// Row exponent: smallest s with amax <= 2688 * 2^s (2688 = 0.65625 * 2^12).
+__device__ __forceinline__ int row_exp_of(float amax) {
+  if (!(amax > 0.0f)) return 0;
+  int ea;
+  const float m = frexpf(amax, &ea);
+  return ea - 12 + (m > 0.65625f ? 1 : 0);
+}
+
+// Quantise 16 values (already |v| * 2^-s in `key`, signs in `neg`) with block code sbc.
+// The E2M1 magnitude code of key / scale is the number of midpoints passed between the
+// values 0 .5 1 1.5 2 3 4 6 (midpoints .25 .75 1.25 1.75 2.5 3.5 5).  The seven decision
+// thresholds midpoint * scale are exact f32 products, formed once per block; a key passes
+// an even-indexed threshold when above it and an odd-indexed one when at or above it, so
+// a tie goes to the even code.
+__device__ __forceinline__ uint64_t quant_block(const float (&key)[16], uint32_t negmask, int sbc) {
+  if (sbc == 0) return 0ull;
+  const float sbv = ue4m3_val(sbc);
+  const float t0 = 0.25f * sbv, t1 = 0.75f * sbv, t2 = 1.25f * sbv, t3 = 1.75f * sbv;
+  const float t4 = 2.5f * sbv, t5 = 3.5f * sbv, t6 = 5.0f * sbv;
+  uint64_t out = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float v = key[i];
+    const uint32_t mag = (uint32_t)(v > t0) + (uint32_t)(v >= t1) + (uint32_t)(v > t2) +
+                         (uint32_t)(v >= t3) + (uint32_t)(v > t4) + (uint32_t)(v >= t5) +
+                         (uint32_t)(v > t6);
+    uint64_t c = mag | (((negmask >> i) & 1u) << 3);
+    out |= c << (4 * i);
+  }
+  return out;
+}
+
+// ---------------------------------------------------------------------------
+// Q(x): one warp per token, the result copied to each of the token's CSR rows
+// ---------------------------------------------------------------------------
+// Lane l takes blocks l, l+32, ...: one pass for the row amax, a second (from L1) for the
+// block scales and codes.
+__global__ void __launch_bounds__(256) quant_x_kernel(const uint16_t* __restrict__ x, int T, int H,
+                                                      int k, const int32_t* __restrict__ pair_pos,
+                                                      uint8_t* __restrict__ qc,
+                                                      uint8_t* __restrict__ qs,
+                                                      int32_t* __restrict__ qe) {
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const uint16_t* row = x + (size_t)t * H;
+  const int nblk = H / 16;
+  float amax = 0.0f;
+  for (int b = lane; b < nblk; b += 32) {
+    const uint4* p = reinterpret_cast<const uint4*>(row + b * 16);
+    const uint4 v0 = __ldg(p), v1 = __ldg(p + 1);
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      amax = fmaxf(amax, fabsf(__uint_as_float(w[i] << 16)));
+      amax = fmaxf(amax, fabsf(__uint_as_float(w[i] & 0xffff0000u)));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const int s = row_exp_of(amax);
+  const bool fast = s >= -127 && s <= 149;
+  const float m = fast ? pow2f(-s) : 0.0f;
+  // lane j < k holds the CSR row of pair (t, j) (k <= 32)
+  const int mypos = lane < k ? pair_pos[(size_t)t * k + lane] : -1;
+  if (mypos >= 0) qe[mypos] = s;
+  for (int b0 = 0; b0 < nblk; b0 += 32) {          // warp-uniform
+    const int b = b0 + lane;
+    const bool has = b < nblk;
+    uint64_t codes = 0;
+    int sbc = 0;
+    if (has) {
+      const uint4* p = reinterpret_cast<const uint4*>(row + b * 16);
+      const uint4 v0 = __ldg(p), v1 = __ldg(p + 1);
+      const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+      float key[16];
+      uint32_t neg = 0;
+      float bmax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
+        key[2 * i] = scale_down(fabsf(lo), s, fast, m);
+        key[2 * i + 1] = scale_down(fabsf(hi), s, fast, m);
+        neg |= (lo < 0.0f ? 1u : 0u) << (2 * i);
+        neg |= (hi < 0.0f ? 1u : 0u) << (2 * i + 1);
+        bmax = fmaxf(bmax, fmaxf(key[2 * i], key[2 * i + 1]));
+      }
+      sbc = ue4m3_code_of(bmax);
+      codes = quant_block(key, neg, sbc);
+    }
+    for (int j = 0; j < k; ++j) {
+      const int pj = __shfl_sync(0xffffffffu, mypos, j);
+      if (!has || pj < 0) continue;
+      *reinterpret_cast<uint64_t*>(qc + (size_t)pj * (H / 2) + b * 8) = codes;
+      qs[(size_t)pj * nblk + b] = (uint8_t)sbc;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Q(h): one warp per CSR row, the row's blocks in registers as for Q(x)
+// ---------------------------------------------------------------------------
+template <int NB>
+__global__ void __launch_bounds__(256) quant_h_kernel(const float* __restrict__ h, int P, int F,
+                                                      int sf_pitch,
+                                                      const int32_t* __restrict__ offsets, int E,
+                                                      uint8_t* __restrict__ qc,
+                                                      uint8_t* __restrict__ qs,
+                                                      int32_t* __restrict__ qe) {
+  const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= P || r >= offsets[E]) return;
+  const float* row = h + (size_t)r * F;
+  const int nblk = F / 16;
+  float4 v[NB][4];
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < NB; ++i) {
+    const int b = lane + 32 * i;
+    if (b < nblk) {
+      const float4* p = reinterpret_cast<const float4*>(row + b * 16);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        v[i][q] = __ldcs(p + q);
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[i][q].x), fabsf(v[i][q].y)),
+                                 fmaxf(fabsf(v[i][q].z), fabsf(v[i][q].w))));
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const int s = row_exp_of(amax);
+  const bool fast = s >= -127 && s <= 149;
+  const float m = fast ? pow2f(-s) : 0.0f;
+  if (lane == 0) qe[r] = s;
+#pragma unroll
+  for (int i = 0; i < NB; ++i) {
+    const int b = lane + 32 * i;
+    if (b >= nblk) break;
+    float key[16];
+    uint32_t neg = 0;
+    float bmax = 0.0f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float vv[4] = {v[i][q].x, v[i][q].y, v[i][q].z, v[i][q].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        key[4 * q + e] = scale_down(fabsf(vv[e]), s, fast, m);
+        neg |= (vv[e] < 0.0f ? 1u : 0u) << (4 * q + e);
+        bmax = fmaxf(bmax, key[4 * q + e]);
+      }
+    }
+    const int sbc = ue4m3_code_of(bmax);
+    *reinterpret_cast<uint64_t*>(qc + (size_t)r * (F / 2) + b * 8) = quant_block(key, neg, sbc);
+    qs[(size_t)r * sf_pitch + b] = (uint8_t)sbc;
+  }
+}
+
+// combine for the prefill path: y[t, :] = sum_j w[t, j] * f32(z16[pos_j, :]) * 2^(e_j + cF)
+__global__ void __launch_bounds__(256)
+combine_f16_kernel(const float* __restrict__ w, const int32_t* __restrict__ pair_pos,
+                   const __half* __restrict__ partial, const int32_t* __restrict__ hexp,
+                   int shift, int H, int k, float* __restrict__ y) {
+  const int t = blockIdx.y;
+  const int r = (blockIdx.x * blockDim.x + threadIdx.x) * 8;
+  if (r >= H) return;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int j = 0; j < k; ++j) {
+    const int pos = pair_pos[(size_t)t * k + j];
+    if (pos < 0) continue;
+    const float wj = ldexpf(w[(size_t)t * k + j], hexp[pos] + shift);
+    const uint4 z = *reinterpret_cast<const uint4*>(partial + (size_t)pos * H + r);
+    const uint32_t zz[4] = {z.x, z.y, z.z, z.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&zz[q]));
+      acc[2 * q] = fmaf(wj, f.x, acc[2 * q]);
+      acc[2 * q + 1] = fmaf(wj, f.y, acc[2 * q + 1]);
+    }
+  }
+  float4* out = reinterpret_cast<float4*>(y + (size_t)t * H + r);
+  out[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  out[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+}
+
+}  // namespace
+
+cudaError_t launch_quant_x(const uint16_t* x_bf16, int T, int H, int k, const int32_t* pair_pos,
+                           uint8_t* qc, uint8_t* qs, int32_t* qe, cudaStream_t s) {
+  quant_x_kernel<<<(T + 7) / 8, 256, 0, s>>>(x_bf16, T, H, k, pair_pos, qc, qs, qe);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_h(const float* h, int P, int F, int sf_pitch, const int32_t* offsets,
+                           int E, uint8_t* qc, uint8_t* qs, int32_t* qe, cudaStream_t s) {
+  const int nb = (F / 16 + 31) / 32;             // blocks per lane
+  if (nb > 8) return cudaErrorInvalidValue;
+  auto kq = nb <= 1 ? quant_h_kernel<1> : nb <= 2 ? quant_h_kernel<2>
+          : nb <= 4 ? quant_h_kernel<4> : quant_h_kernel<8>;
+  kq<<<(P + 7) / 8, 256, 0, s>>>(h, P, F, sf_pitch, offsets, E, qc, qs, qe);
+  return cudaGetLastError();
+}
+
+// Exponent c_F with F * 2688^2 * 2^-c_F < 2^15: the fixed shift of the f16 partials.
+int down_shift_for(int F) {
+  const double bound = (double)F * 2688.0 * 2688.0;
+  int c = 0;
+  while (std::ldexp(bound, -c) >= 32768.0) ++c;
+  return c;
+}
+
+cudaError_t launch_prefill_combine(const float* w, int T, int H, int F, int k,
+                                   const moe_ws_layout& L, char* ws, float* y, cudaStream_t s) {
+  dim3 grid((H / 8 + 255) / 256, T);
+  combine_f16_kernel<<<grid, 256, 0, s>>>(w, reinterpret_cast<const int32_t*>(ws + L.pair_pos),
+                                          reinterpret_cast<const __half*>(ws + L.partial),
+                                          reinterpret_cast<const int32_t*>(ws + L.qh_exp),
+                                          down_shift_for(F), H, k, y);
+  return cudaGetLastError();
+}
+
+}  // namespace moe
