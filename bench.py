@@ -532,9 +532,8 @@ def run_ours(args):
         else:
             cpu = {"error": info["error"][-200:]}
 
-    # decode: [route], csr, x_gather, gate_up, h_prep, down, combine; prefill: [route], csr,
-    # tiles, Q(x), gate/up GEMM, Q(h), down GEMM, combine
-    launches_per_step = (7 if lgs else 6) if not prefill else (8 if lgs else 7)
+    # the library's own count of the kernels the CSR, gate/up and down calls launch, plus routing
+    launches_per_step = moe.kernel_launches(wl.T, wl.H, wl.F, wl.E, wl.k, path) + (1 if lgs else 0)
     line = {
         "metric": metric_name(args.workload), "value": value, "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_ms / args.steps,

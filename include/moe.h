@@ -135,6 +135,11 @@ int32_t moe_prefill_min_pairs(void);
 /* The path a call with these arguments runs (DECODE or PREFILL). */
 int32_t moe_resolve_path(int32_t T, int32_t k, int32_t path);
 
+/* Number of kernels one layer with these sizes launches in moe_build_expert_csr,
+ * moe_grouped_gate_up_silu_nvfp4 and moe_grouped_down_combine_nvfp4 together (add one
+ * for moe_route_topk); 0 if the sizes are invalid. */
+int32_t moe_kernel_launches(int32_t T, int32_t H, int32_t F, int32_t E, int32_t k, int32_t path);
+
 /* Top-k routing of router logits (the pages' probes start from already-routed pairs;
  * this is the router that produces them). For each token t: the k experts with the largest
  * logits[t, :] in descending order, ties broken towards the lower expert id, comparing

@@ -15,7 +15,7 @@ from . import _native
 from ._native import PATH_AUTO, PATH_DECODE, PATH_PREFILL, DEVERR_EXPERT_ID, DEVERR_TIMEOUT  # noqa
 
 __all__ = ["MoeError", "NvFp4Bank", "ExpertCSR", "workspace_bytes", "workspace_layout",
-           "resolve_path", "prefill_min_pairs", "moe_route_topk", "moe_build_expert_csr",
+           "resolve_path", "prefill_min_pairs", "kernel_launches", "moe_route_topk", "moe_build_expert_csr",
            "moe_build_expert_csr_static",
            "moe_grouped_gate_up_silu_nvfp4", "moe_grouped_down_combine_nvfp4",
            "get_device_error", "MoeLayer", "PATH_AUTO", "PATH_DECODE", "PATH_PREFILL"]
@@ -90,6 +90,11 @@ def workspace_layout(T: int, H: int, F: int, E: int, k: int, path: int = PATH_AU
 
 def resolve_path(T: int, k: int, path: int = PATH_AUTO) -> int:
     return int(_native.load().moe_resolve_path(T, k, path))
+
+
+def kernel_launches(T: int, H: int, F: int, E: int, k: int, path: int = PATH_AUTO) -> int:
+    """Kernels launched per layer by the CSR, gate/up and down calls (add 1 for routing)."""
+    return int(_native.load().moe_kernel_launches(T, H, F, E, k, path))
 
 
 def prefill_min_pairs() -> int:

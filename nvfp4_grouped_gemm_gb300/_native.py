@@ -38,6 +38,7 @@ SIGNATURES = [
     ("moe_workspace_layout", c_i32, [c_i32] * 6 + [ctypes.POINTER(WsLayout)]),
     ("moe_prefill_min_pairs", c_i32, []),
     ("moe_resolve_path", c_i32, [c_i32] * 3),
+    ("moe_kernel_launches", c_i32, [c_i32] * 6),
     ("moe_route_topk", c_i32, [c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp]),
     ("moe_build_expert_csr", c_i32, [c_vp, c_i32, c_i32, c_i32, CSR, c_vp, c_size, c_vp]),
     ("moe_grouped_gate_up_silu_nvfp4", c_i32,

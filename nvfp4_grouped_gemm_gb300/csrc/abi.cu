@@ -115,6 +115,16 @@ int32_t moe_prefill_min_pairs(void) { return kPrefillMinPairs; }
 
 int32_t moe_resolve_path(int32_t T, int32_t k, int32_t path) { return resolve_path(T, k, path); }
 
+int32_t moe_kernel_launches(int32_t T, int32_t H, int32_t F, int32_t E, int32_t k, int32_t path) {
+  moe_ws_layout L;
+  if (!compute_layout(T, H, F, E, k, path, &L)) return 0;
+  const int P = T * k;
+  const int csr = csr_scratch_bytes(P, E) ? 3 : 1;   // grid-wide build or one CTA
+  if (resolve_path(T, k, path) == MOE_PATH_DECODE)
+    return csr + 2 /* x gather, gate/up */ + 3 /* h prep, down, combine */;
+  return csr + 3 /* tiles, Q(x), gate/up GEMM */ + 3 /* Q(h), down GEMM, combine */;
+}
+
 const char* moe_status_string(moe_status s) {
   switch (s) {
     case MOE_OK: return "MOE_OK";
@@ -210,10 +220,9 @@ moe_status moe_grouped_down_combine_nvfp4(const moe_nvfp4_bank* w_down, moe_csr 
   cudaError_t ce;
   if (p == MOE_PATH_PREFILL) {
     bool unsup = false;
-    ce = launch_prefill_down(*w_down, csr, T, H, F, k, L, w, s, &unsup);
+    ce = launch_prefill_down(*w_down, csr, topk_w, T, H, F, k, L, w, y, s, &unsup);
     if (unsup) return MOE_ERR_UNSUPPORTED;
-    if (ce != cudaSuccess) return MOE_ERR_CUDA;
-    return from_cuda(launch_prefill_combine(topk_w, T, H, F, k, L, w, y, s));
+    return from_cuda(ce);
   }
   ce = launch_decode_down(*w_down, csr, T, H, F, k, L, w, s);
   if (ce != cudaSuccess) return MOE_ERR_CUDA;

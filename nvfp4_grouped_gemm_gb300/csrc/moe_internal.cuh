@@ -45,16 +45,17 @@ cudaError_t launch_combine(const float* w, int T, int H, int k, const moe_ws_lay
 cudaError_t launch_prefill_gate_up(const uint16_t* x_bf16, int T, int H, int F, int k,
                                    const moe_nvfp4_bank& b, moe_csr csr, const moe_ws_layout& L,
                                    char* ws, cudaStream_t s, bool* unsupported);
-cudaError_t launch_prefill_down(const moe_nvfp4_bank& b, moe_csr csr, int T, int H, int F, int k,
-                                const moe_ws_layout& L, char* ws, cudaStream_t s,
-                                bool* unsupported);
+// Q(h), the down GEMM and the combine.
+cudaError_t launch_prefill_down(const moe_nvfp4_bank& b, moe_csr csr, const float* w, int T, int H,
+                                int F, int k, const moe_ws_layout& L, char* ws, float* y,
+                                cudaStream_t s, bool* unsupported);
 cudaError_t launch_quant_x(const uint16_t* x_bf16, int T, int H, int k, const int32_t* pair_pos,
                            uint8_t* qc, uint8_t* qs, int32_t* qe, cudaStream_t s);
 cudaError_t launch_quant_h(const float* h, int P, int F, int sf_pitch, const int32_t* offsets,
                            int E, uint8_t* qc, uint8_t* qs, int32_t* qe, cudaStream_t s);
 // Exponent c_F with F * 2688^2 * 2^-c_F < 2^15: the fixed shift of the f16 partials.
 int down_shift_for(int F);
-cudaError_t launch_prefill_combine(const float* w, int T, int H, int F, int k,
+cudaError_t launch_prefill_combine(const float* w, int T, int H, int F, int k, int c0, int HS,
                                    const moe_ws_layout& L, char* ws, float* y, cudaStream_t s);
 // Launch with programmatic dependent launch allowed: the kernel may start while its
 // predecessor in the stream finishes, and must execute griddepcontrol.wait before it

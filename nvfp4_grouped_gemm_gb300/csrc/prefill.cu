@@ -137,6 +137,21 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       ::"r"(smem_u32(dst)), "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
+// Same with an L2 cache policy (weights: evict first, so that the activation tiles and the
+// partials written meanwhile keep their L2 lines).
+__device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* map, int x, int y,
+                                                 uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;"
+      ::"r"(smem_u32(dst)), "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
 
 __device__ __forceinline__ void cp_async4(void* dst, const void* src, bool valid) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;"
@@ -234,6 +249,7 @@ struct GemmArgs {
   uint32_t* err;
   int P, K, rows_per_expert, n_tiles_n, out_cols, F, down_shift;
   int b_sf_group;               // DOWN: g rows of the weight-scale plane per tensor-map row
+  int n_base;                   // first N-tile of this launch (output columns are relative to it)
 };
 
 // Scale factors reach shared memory through TMA, as row-major staging images beside the
@@ -344,6 +360,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
       constexpr uint32_t tx_codes = C::A_BYTES + C::B_BYTES;
       const int g = args.b_sf_group;
       const uint32_t tx_stg = C::SA_STG + (GATE_UP ? C::SB_STG : (uint32_t)(g == 1 ? BN * 16 : BN * 32));
+      const uint64_t wpol = l2_evict_first_policy();
       const int sub_rows = BN / g, sub_w = g == 1 ? 16 : 32;
       int it = 0;
       // work descriptors are fetched two works ahead (a DOWN work is only a few stages)
@@ -354,7 +371,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         const int w2 = w + 2 * gridDim.x;
         const int4 next2 = w2 < n_work ? tlist[w2 / args.n_tiles_n] : next;
         const int n0 = (w % args.n_tiles_n) * C::OUT_N;
-        const int brow = tile.z * args.rows_per_expert + n0;
+        const int brow = tile.z * args.rows_per_expert + args.n_base * C::OUT_N + n0;
         for (int ks = 0; ks < k_stages; ++ks, ++it) {
           const int st = it % C::STAGES;
           if (!mbar_wait(&empty[st], ((it / C::STAGES) & 1) ^ 1, abort_flag, args.err)) break;
@@ -376,11 +393,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
           }
           tma_load_2d(sb, &tmap_a, ks * C::KB, tile.x, &full[st]);
           if (GATE_UP) {
-            tma_load_2d(sb + C::A_BYTES, &tmap_b, ks * C::KB, brow, &full[st]);
-            tma_load_2d(sb + C::A_BYTES + C::B_BYTES / 2, &tmap_b, ks * C::KB, brow + args.F,
-                        &full[st]);
+            tma_load_2d_hint(sb + C::A_BYTES, &tmap_b, ks * C::KB, brow, &full[st], wpol);
+            tma_load_2d_hint(sb + C::A_BYTES + C::B_BYTES / 2, &tmap_b, ks * C::KB, brow + args.F,
+                             &full[st], wpol);
           } else {
-            tma_load_2d(sb + C::A_BYTES, &tmap_b, ks * C::KB, brow, &full[st]);
+            tma_load_2d_hint(sb + C::A_BYTES, &tmap_b, ks * C::KB, brow, &full[st], wpol);
           }
         }
         tile = next;
@@ -544,9 +561,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 const __half2 h2 = __floats2half2_rn(a0, a1);
                 pk[q] = *reinterpret_cast<const uint32_t*>(&h2);
               }
-              // streaming store: the partials are read once, by the combine
-              __stcs(reinterpret_cast<uint4*>(orow + half * 64 + c * 32 + i),
-                     make_uint4(pk[0], pk[1], pk[2], pk[3]));
+              *reinterpret_cast<uint4*>(orow + half * 64 + c * 32 + i) =
+                  make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
         }
       }
@@ -652,14 +668,14 @@ cudaError_t launch_prefill_gate_up(const uint16_t* x_bf16, int T, int H, int F, 
       !make_map(&msb, b.scales, H / 16, H / 16, wrows, 16, BN / 2, false))
     return cudaErrorInvalidValue;
   GemmArgs a{qe, tiles, ws + L.h, reinterpret_cast<uint32_t*>(ws + L.error_word),
-             P, H, 2 * F, F / (BN / 2), F, F, 0, 1};
+             P, H, 2 * F, F / (BN / 2), F, F, 0, 1, 0};
   const int max_tiles = P / 128 + (P < b.E ? P : b.E) + 1;
   return run_gemm<BN, true>(ma, mb, msa, msb, a, max_tiles, s);
 }
 
-cudaError_t launch_prefill_down(const moe_nvfp4_bank& b, moe_csr csr, int T, int H, int F, int k,
-                                const moe_ws_layout& L, char* ws, cudaStream_t s,
-                                bool* unsupported) {
+cudaError_t launch_prefill_down(const moe_nvfp4_bank& b, moe_csr csr, const float* w, int T, int H,
+                                int F, int k, const moe_ws_layout& L, char* ws, float* y,
+                                cudaStream_t s, bool* unsupported) {
   *unsupported = false;
   if (H % 256 != 0 || F % 64 != 0) { *unsupported = true; return cudaSuccess; }
   const int P = T * k;
@@ -687,10 +703,13 @@ cudaError_t launch_prefill_down(const moe_nvfp4_bank& b, moe_csr csr, int T, int
                 g == 1 ? 16 : 32, BN / g, false))
     return cudaErrorInvalidValue;
   const int shift = down_shift_for(F);
-  GemmArgs a{qe, reinterpret_cast<const int32_t*>(ws + L.tiles), ws + L.partial,
-             reinterpret_cast<uint32_t*>(ws + L.error_word), P, F, H, H / BN, H, F, shift, g};
   const int max_tiles = P / 128 + (P < b.E ? P : b.E) + 1;
-  return run_gemm<BN, false>(ma, mb, msa, msb, a, max_tiles, s);
+  // (splitting the output columns so that each slice's partials stay in L2 for the combine
+  // was measured slower: every extra GEMM launch costs more than the HBM round trip saves)
+  GemmArgs a{qe, reinterpret_cast<const int32_t*>(ws + L.tiles), ws + L.partial,
+             reinterpret_cast<uint32_t*>(ws + L.error_word), P, F, H, H / BN, H, F, shift, g, 0};
+  if ((st = run_gemm<BN, false>(ma, mb, msa, msb, a, max_tiles, s)) != cudaSuccess) return st;
+  return launch_prefill_combine(w, T, H, F, k, 0, H, L, ws, y, s);
 }
 
 }  // namespace moe

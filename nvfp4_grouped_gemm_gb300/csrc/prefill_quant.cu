@@ -82,16 +82,18 @@ __device__ __forceinline__ uint64_t quant_block(const float (&key)[16], uint32_t
   const float sbv = ue4m3_val(sbc);
   const float t0 = 0.25f * sbv, t1 = 0.75f * sbv, t2 = 1.25f * sbv, t3 = 1.75f * sbv;
   const float t4 = 2.5f * sbv, t5 = 3.5f * sbv, t6 = 5.0f * sbv;
-  uint64_t out = 0;
+  // thresholds are increasing, so the count is found by a three-step search
+  uint32_t lo = 0, hi = 0;
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const float v = key[i];
-    const uint32_t mag = (uint32_t)(v > t0) + (uint32_t)(v >= t1) + (uint32_t)(v > t2) +
-                         (uint32_t)(v >= t3) + (uint32_t)(v > t4) + (uint32_t)(v >= t5) +
-                         (uint32_t)(v > t6);
-    uint64_t c = mag | (((negmask >> i) & 1u) << 3);
-    out |= c << (4 * i);
+    const bool b2 = v >= t3;
+    const bool b1 = v >= (b2 ? t5 : t1);
+    const bool b0 = v > (b2 ? (b1 ? t6 : t4) : (b1 ? t2 : t0));
+    const uint32_t c = (b2 ? 4u : 0u) | (b1 ? 2u : 0u) | (b0 ? 1u : 0u) | (((negmask >> i) & 1u) << 3);
+    if (i < 8) lo |= c << (4 * i); else hi |= c << (4 * (i - 8));
   }
+  const uint64_t out = (uint64_t)lo | ((uint64_t)hi << 32);
   return out;
 }
 
@@ -222,30 +224,51 @@ __global__ void __launch_bounds__(256) quant_h_kernel(const float* __restrict__ 
 }
 
 // combine for the prefill path: y[t, :] = sum_j w[t, j] * f32(z16[pos_j, :]) * 2^(e_j + cF)
+// The token's k positions and scaled weights are read once into shared memory; the
+// partial rows are then loaded four pairs at a time and summed in ascending j.
+// Columns [c0, c0 + HS) of y from a partial slice [P][HS].
 __global__ void __launch_bounds__(256)
 combine_f16_kernel(const float* __restrict__ w, const int32_t* __restrict__ pair_pos,
                    const __half* __restrict__ partial, const int32_t* __restrict__ hexp,
-                   int shift, int H, int k, float* __restrict__ y) {
+                   int shift, int H, int c0, int HS, int k, float* __restrict__ y) {
+  __shared__ int s_pos[kMaxK];
+  __shared__ float s_w[kMaxK];
   const int t = blockIdx.y;
-  const int r = (blockIdx.x * blockDim.x + threadIdx.x) * 8;
-  if (r >= H) return;
+  if (threadIdx.x < k) {
+    const int pos = pair_pos[(size_t)t * k + threadIdx.x];
+    s_pos[threadIdx.x] = pos;
+    s_w[threadIdx.x] = pos >= 0 ? ldexpf(w[(size_t)t * k + threadIdx.x], hexp[pos] + shift) : 0.0f;
+  }
+  __syncthreads();
+  const int r = (blockIdx.x * blockDim.x + threadIdx.x) * 8;   // column within the slice
+  if (r >= HS) return;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int j = 0; j < k; ++j) {
-    const int pos = pair_pos[(size_t)t * k + j];
-    if (pos < 0) continue;
-    const float wj = ldexpf(w[(size_t)t * k + j], hexp[pos] + shift);
-    const uint4 z = *reinterpret_cast<const uint4*>(partial + (size_t)pos * H + r);
-    const uint32_t zz[4] = {z.x, z.y, z.z, z.w};
+  for (int j0 = 0; j0 < k; j0 += 4) {
+    uint4 z[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&zz[q]));
-      acc[2 * q] = fmaf(wj, f.x, acc[2 * q]);
-      acc[2 * q + 1] = fmaf(wj, f.y, acc[2 * q + 1]);
+      const int j = j0 + q;
+      const int pos = j < k ? s_pos[j] : -1;
+      z[q] = pos >= 0 ? __ldcs(reinterpret_cast<const uint4*>(partial + (size_t)pos * HS + r))
+                      : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int j = j0 + q;
+      if (j >= k || s_pos[j] < 0) continue;
+      const float wj = s_w[j];
+      const uint32_t zz[4] = {z[q].x, z[q].y, z[q].z, z[q].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&zz[e]));
+        acc[2 * e] = fmaf(wj, f.x, acc[2 * e]);
+        acc[2 * e + 1] = fmaf(wj, f.y, acc[2 * e + 1]);
+      }
     }
   }
-  float4* out = reinterpret_cast<float4*>(y + (size_t)t * H + r);
-  out[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-  out[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  float4* out = reinterpret_cast<float4*>(y + (size_t)t * H + c0 + r);
+  __stcs(out, make_float4(acc[0], acc[1], acc[2], acc[3]));
+  __stcs(out + 1, make_float4(acc[4], acc[5], acc[6], acc[7]));
 }
 
 }  // namespace
@@ -274,13 +297,13 @@ int down_shift_for(int F) {
   return c;
 }
 
-cudaError_t launch_prefill_combine(const float* w, int T, int H, int F, int k,
+cudaError_t launch_prefill_combine(const float* w, int T, int H, int F, int k, int c0, int HS,
                                    const moe_ws_layout& L, char* ws, float* y, cudaStream_t s) {
-  dim3 grid((H / 8 + 255) / 256, T);
+  dim3 grid((HS / 8 + 255) / 256, T);
   combine_f16_kernel<<<grid, 256, 0, s>>>(w, reinterpret_cast<const int32_t*>(ws + L.pair_pos),
                                           reinterpret_cast<const __half*>(ws + L.partial),
                                           reinterpret_cast<const int32_t*>(ws + L.qh_exp),
-                                          down_shift_for(F), H, k, y);
+                                          down_shift_for(F), H, c0, HS, k, y);
   return cudaGetLastError();
 }
 
