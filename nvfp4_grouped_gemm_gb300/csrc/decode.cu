@@ -26,6 +26,7 @@
 // the loads that depend only on the CSR (two or more kernels back, complete before its
 // predecessor passed its own griddepcontrol.wait) and then waits for its predecessor.
 #include "moe_internal.cuh"
+#include "tma_sync.cuh"
 
 namespace moe {
 
@@ -481,6 +482,202 @@ combine_kernel(const float* __restrict__ w, const int32_t* __restrict__ pair_pos
   *reinterpret_cast<float4*>(y + (size_t)t * H + r) = acc;
 }
 
+// ---------------------------------------------------------------------------
+// gate/up + SiLU, TMA-fed warp units
+// ---------------------------------------------------------------------------
+// One CTA per SM: warp 0 streams tiles with TMA into a ring of shared-memory stages; each
+// of the NW other warps owns two stages and multiplies whole units alone (no CTA barrier,
+// no cross-warp sum).  A unit = (active expert, 8 gate rows + the matching 8 up rows);
+// one m16n8k16 MMA carries the gate rows in M rows 0..7 and the up rows in 8..15, so each
+// lane holds a gate and an up value of the same (row, pair) and writes h itself.  A stage
+// is one of the unit's NH K-chunks of KC = H/2/NH bytes per row, fetched by two 4-D TMA
+// boxes: codes {128 B, 8 rows, gate/up, nb = KC/128 K-boxes} (SWIZZLE_128B, so the
+// quarter-warp reads of rows g..g+7 hit distinct banks) land as [K-box][gate, up][row][128 B],
+// scales {16 B, 8 rows, gate/up, nb} as [K-box][gate, up][row][16 B].  The first unit of a
+// warp is CTA unit w, the next w + NW, ...; a unit with more than 8 pairs is streamed
+// once per group of 8 pairs.
+constexpr int kTmaWarps = 8;                  // consumer warps
+constexpr int kTmaSlots = 2;                  // stages per consumer warp
+
+struct GuTmaArgs {
+  const __half* xg;
+  const int32_t* xe;
+  int H, F, nh, nb;                           // K-chunks per unit, 128-byte boxes per chunk
+  const int32_t* offsets;
+  const int32_t* active;
+  const int32_t* n_active;
+  float* h;
+  uint32_t* err;
+};
+
+__host__ __device__ constexpr int gu_stage_bytes(int nb) {
+  return ((2 * nb * 1024 + 2 * 8 * nb * 16) + 1023) / 1024 * 1024;
+}
+// byte offsets inside a stage
+__device__ __forceinline__ uint32_t gu_code_off(int kbox, int mat, int row, int chunk16) {
+  return kbox * 2048 + mat * 1024 + row * 128 + ((chunk16 ^ row) << 4);
+}
+__device__ __forceinline__ uint32_t gu_scale_off(int nb, int kbox, int mat, int row) {
+  return 2 * nb * 1024 + kbox * 256 + mat * 128 + row * 16;
+}
+
+__global__ void __launch_bounds__(32 * (1 + kTmaWarps), 1)
+gate_up_tma_kernel(const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_s,
+                   const GuTmaArgs args) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int nb = args.nb, nh = args.nh;
+  const int stage_bytes = gu_stage_bytes(nb);
+  constexpr int NSLOT = kTmaWarps * kTmaSlots;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NSLOT * stage_bytes);
+  uint64_t* empty = full + NSLOT;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + NSLOT);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int H = args.H, F = args.F;
+  const int nrb = F / 8;                                   // units per expert
+  const int sc_bytes = nb * 16;                            // scale bytes per row and stage
+  (void)sc_bytes;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NSLOT; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  pdl_wait();                                              // gathered activations are ready
+  pdl_trigger();
+  const int n_units = *args.n_active * nrb;
+  const int u_beg = (int)((long long)blockIdx.x * n_units / gridDim.x);
+  const int u_end = (int)((long long)(blockIdx.x + 1) * n_units / gridDim.x);
+
+  if (warp == 0) {
+    // ---------------- TMA producer: round robin over the consumer warps ----------------
+    if (lane == 0) {
+      const uint32_t tx = (uint32_t)(2 * nb * 1024 + 2 * 8 * sc_bytes);
+      int cu[kTmaWarps], cp[kTmaWarps], ch[kTmaWarps], cq[kTmaWarps];   // unit, pass, chunk, stages
+      for (int w = 0; w < kTmaWarps; ++w) { cu[w] = u_beg + w; cp[w] = 0; ch[w] = 0; cq[w] = 0; }
+      bool more = true, ok = true;
+      while (more && ok) {
+        more = false;
+        for (int w = 0; w < kTmaWarps && ok; ++w) {
+          if (cu[w] >= u_end) continue;
+          more = true;
+          const int slot = w * kTmaSlots + (cq[w] & 1);
+          if (!mbar_wait(&empty[slot], ((cq[w] >> 1) & 1) ^ 1, abort_flag, args.err)) { ok = false; break; }
+          const int u = cu[w];
+          const int e = args.active[u / nrb];
+          unsigned char* sb = smem + slot * stage_bytes;
+          mbar_expect_tx(&full[slot], tx);
+          // coordinates {byte in K-box, row of the matrix, 2e (gate) .. 2e+1 (up), K-box}
+          tma_load_4d(sb, &tmap_c, 0, (u % nrb) * 8, 2 * e, ch[w] * nb, &full[slot]);
+          tma_load_4d(sb + 2 * nb * 1024, &tmap_s, 0, (u % nrb) * 8, 2 * e, ch[w] * nb, &full[slot]);
+          ++cq[w];
+          if (++ch[w] == nh) {
+            ch[w] = 0;
+            const int m = args.offsets[e + 1] - args.offsets[e];
+            if (++cp[w] * 8 >= m) { cp[w] = 0; cu[w] += kTmaWarps; }
+          }
+        }
+      }
+      if (!ok) {
+        // drain, bounded: every issued stage has landed before the CTA exits
+        for (int w = 0; w < kTmaWarps; ++w)
+          for (int par = 0; par < 2; ++par) {
+            if (cq[w] <= par) continue;
+            const int last = par + ((cq[w] - 1 - par) / 2) * 2;     // last stage issued on the slot
+            const uint64_t t0 = global_ns();
+            while (!mbar_try(&full[w * kTmaSlots + par], (uint32_t)((last >> 1) & 1)) &&
+                   global_ns() - t0 < 100000000ull) {
+            }
+          }
+      }
+    }
+  } else {
+    // ---------------- consumer warp ----------------
+    const int cw = warp - 1;
+    const int g = lane >> 2, c = lane & 3;
+    int q = 0;                                             // stages consumed
+    for (int u = u_beg + cw; u < u_end && !*abort_flag; u += kTmaWarps) {
+      const int e = args.active[u / nrb];
+      const int i0 = (u % nrb) * 8;
+      const int off = args.offsets[e];
+      const int m = args.offsets[e + 1] - off;
+      bool ok = true;
+      for (int tok0 = 0; tok0 < m && ok; tok0 += 8) {
+        const int live = min(8, m - tok0);
+        const __half* xrow = args.xg + (size_t)(off + tok0 + (g < live ? g : 0)) * H + 32 * c;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        uint4 xb[4];
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq)
+          xb[qq] = g < live ? __ldg(reinterpret_cast<const uint4*>(xrow + 8 * qq)) : make_uint4(0, 0, 0, 0);
+        for (int hc = 0; hc < nh; ++hc, ++q) {
+          const int slot = cw * kTmaSlots + (q & 1);
+          if (!mbar_wait_warp(&full[slot], (q >> 1) & 1, abort_flag, args.err)) { ok = false; break; }
+          const uint32_t sb = smem_u32(smem + slot * stage_bytes);
+          for (int kl = 0; kl < 2 * nb; ++kl) {             // 128-element k-blocks of the chunk
+            const int kbg = hc * 2 * nb + kl;               // k-block within the row
+            uint4 xn[4];
+            const bool nxt = g < live && kbg + 1 < H / 128;
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq)
+              xn[qq] = nxt ? __ldg(reinterpret_cast<const uint4*>(xrow + (kbg + 1) * 128 + 8 * qq))
+                           : make_uint4(0, 0, 0, 0);
+            const int chunk = ((kl & 1) << 2) + c;           // 16-byte chunk within the K-box row
+            const int kbox = kl >> 1;
+            uint4 WGv, WUv;
+            asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(WGv.x), "=r"(WGv.y), "=r"(WGv.z), "=r"(WGv.w) : "r"(sb + gu_code_off(kbox, 0, g, chunk)));
+            asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(WUv.x), "=r"(WUv.y), "=r"(WUv.z), "=r"(WUv.w) : "r"(sb + gu_code_off(kbox, 1, g, chunk)));
+            // the K-box's 16 scale bytes per row: 8 for each of its two 128-element k-blocks
+            unsigned short s16g, s16u;
+            const uint32_t so = ((kl & 1) << 3) + 2 * c;
+            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(s16g) : "r"(sb + gu_scale_off(nb, kbox, 0, g) + so));
+            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(s16u) : "r"(sb + gu_scale_off(nb, kbox, 1, g) + so));
+            const uint32_t fg = e4m3x2_to_f16x2(s16g), fu = e4m3x2_to_f16x2(s16u);
+            const uint32_t s_g[2] = {bcast_lo(fg), bcast_hi(fg)};
+            const uint32_t s_u[2] = {bcast_lo(fu), bcast_hi(fu)};
+            const uint32_t WG[4] = {WGv.x, WGv.y, WGv.z, WGv.w};
+            const uint32_t WU[4] = {WUv.x, WUv.y, WUv.z, WUv.w};
+#pragma unroll
+            for (int wi = 0; wi < 4; ++wi) {
+              uint32_t gq[4], uq[4];
+              e2m1x8_to_f16x2x4(WG[wi], gq[0], gq[1], gq[2], gq[3]);
+              e2m1x8_to_f16x2x4(WU[wi], uq[0], uq[1], uq[2], uq[3]);
+              const int sbk = wi >> 1;
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh)
+                mma_f16_16816(acc, hmul2_u32(gq[2 * hh], s_g[sbk]), hmul2_u32(uq[2 * hh], s_u[sbk]),
+                              hmul2_u32(gq[2 * hh + 1], s_g[sbk]), hmul2_u32(uq[2 * hh + 1], s_u[sbk]),
+                              hh ? xb[wi].z : xb[wi].x, hh ? xb[wi].w : xb[wi].y);
+            }
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) xb[qq] = xn[qq];
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[slot]);
+        }
+        if (!ok) break;
+        // acc[0..1]: gate row i0+g, pairs 2c, 2c+1; acc[2..3]: up row i0+g, same pairs
+#pragma unroll
+        for (int qq = 0; qq < 2; ++qq) {
+          const int n = 2 * c + qq;
+          if (n < live) {
+            const int pos = off + tok0 + n;
+            const int ex = args.xe[pos];
+            args.h[(size_t)pos * F + i0 + g] = silu_f(ldexpf(acc[qq], ex)) * ldexpf(acc[2 + qq], ex);
+          }
+        }
+      }
+      if (!ok) break;
+    }
+  }
+  __syncthreads();
+}
+
 int sm_count() {
   static int n = 0;
   if (!n) {
@@ -506,6 +703,36 @@ cudaError_t launch_decode_gate_up(const uint16_t* x_bf16, int T, int H, int F, i
                               (const int32_t*)csr.pair_ids, (const int32_t*)csr.expert_offsets,
                               b.E, xg, xe);
   if (st != cudaSuccess) return st;
+  {
+    // TMA-fed warp units: K-chunks of at most 5 boxes of 128 bytes per row
+    const int n256 = H / 256;
+    int nh = 1;
+    while (n256 % nh != 0 || n256 / nh > 5) ++nh;
+    const int nb = n256 / nh;
+    const size_t smem = (size_t)kTmaWarps * kTmaSlots * gu_stage_bytes(nb) + 1024 + 512;
+    // the banks as [K-box][E*2 matrices][F rows][bytes of the K-box] (row pitch H/2 or H/16)
+    CUtensorMap mc, ms;
+    const uint64_t cdims[4] = {128, (uint64_t)F, 2 * (uint64_t)b.E, (uint64_t)n256};
+    const uint64_t cstr[3] = {(uint64_t)H / 2, (uint64_t)F * (H / 2), 128};
+    const uint32_t cbox[4] = {128, 8, 2, (uint32_t)nb};
+    const uint64_t sdims[4] = {16, (uint64_t)F, 2 * (uint64_t)b.E, (uint64_t)n256};
+    const uint64_t sstr[3] = {(uint64_t)H / 16, (uint64_t)F * (H / 16), 16};
+    const uint32_t sbox[4] = {16, 8, 2, (uint32_t)nb};
+    if (smem <= 232448 && make_map4(&mc, b.codes, cdims, cstr, cbox, true) &&
+        make_map4(&ms, b.scales, sdims, sstr, sbox, false)) {
+      GuTmaArgs ta{xg, xe, H, F, nh, nb, csr.expert_offsets, csr.active_experts, csr.n_active,
+                   reinterpret_cast<float*>(ws + L.h), reinterpret_cast<uint32_t*>(ws + L.error_word)};
+      st = cudaFuncSetAttribute(gate_up_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)smem);
+      if (st != cudaSuccess) return st;
+      const long long units = (long long)(P < b.E ? P : b.E) * (F / 8);
+      long long grid = sm_count();
+      if (grid * kTmaWarps > units) grid = (units + kTmaWarps - 1) / kTmaWarps;
+      if (grid < 1) grid = 1;
+      return launch_pdl(gate_up_tma_kernel, dim3((unsigned)grid), dim3(32 * (1 + kTmaWarps)), smem,
+                        s, mc, ms, ta);
+    }
+  }
   GateUpArgs a{xg, xe, b.codes, b.scales, H, F, csr.expert_offsets, csr.active_experts,
                csr.n_active, reinterpret_cast<float*>(ws + L.h)};
   const long long max_units = (long long)(P < b.E ? P : b.E) * (F / 16);
