@@ -496,8 +496,9 @@ combine_kernel(const float* __restrict__ w, const int32_t* __restrict__ pair_pos
 // scales {16 B, 8 rows, gate/up, nb} as [K-box][gate, up][row][16 B].  The first unit of a
 // warp is CTA unit w, the next w + NW, ...; a unit with more than 8 pairs is streamed
 // once per group of 8 pairs.
-constexpr int kTmaWarps = 8;                  // consumer warps
+constexpr int kTmaWarps = 16;                 // consumer warps
 constexpr int kTmaSlots = 2;                  // stages per consumer warp
+constexpr int kTmaProd = 4;                   // producer warps, each feeding kTmaWarps/kTmaProd
 
 struct GuTmaArgs {
   const __half* xg;
@@ -521,7 +522,7 @@ __device__ __forceinline__ uint32_t gu_scale_off(int nb, int kbox, int mat, int 
   return 2 * nb * 1024 + kbox * 256 + mat * 128 + row * 16;
 }
 
-__global__ void __launch_bounds__(32 * (1 + kTmaWarps), 1)
+__global__ void __launch_bounds__(32 * (kTmaProd + kTmaWarps), 1)
 gate_up_tma_kernel(const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_s,
                    const GuTmaArgs args) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -554,43 +555,48 @@ gate_up_tma_kernel(const __grid_constant__ CUtensorMap tmap_c, const __grid_cons
   const int u_beg = (int)((long long)blockIdx.x * n_units / gridDim.x);
   const int u_end = (int)((long long)(blockIdx.x + 1) * n_units / gridDim.x);
 
-  if (warp == 0) {
-    // ---------------- TMA producer: round robin over the consumer warps ----------------
+  constexpr int PER = kTmaWarps / kTmaProd;               // consumer warps per producer
+  if (warp < kTmaProd) {
+    // ---------------- TMA producers: warp p feeds consumers p*PER .. p*PER+PER-1 ----------------
     if (lane == 0) {
       const uint32_t tx = (uint32_t)(2 * nb * 1024 + 2 * 8 * sc_bytes);
-      int cu[kTmaWarps], cp[kTmaWarps], ch[kTmaWarps], cq[kTmaWarps];   // unit, pass, chunk, stages
-      for (int w = 0; w < kTmaWarps; ++w) { cu[w] = u_beg + w; cp[w] = 0; ch[w] = 0; cq[w] = 0; }
+      const int w0 = warp * PER;
+      int cu[PER], cp[PER], ch[PER], cq[PER];              // unit, pass, chunk, stages
+      for (int i = 0; i < PER; ++i) { cu[i] = u_beg + w0 + i; cp[i] = 0; ch[i] = 0; cq[i] = 0; }
       bool more = true, ok = true;
       while (more && ok) {
         more = false;
-        for (int w = 0; w < kTmaWarps && ok; ++w) {
-          if (cu[w] >= u_end) continue;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+          if (!ok) break;
+          const int w = w0 + i;
+          if (cu[i] >= u_end) continue;
           more = true;
-          const int slot = w * kTmaSlots + (cq[w] & 1);
-          if (!mbar_wait(&empty[slot], ((cq[w] >> 1) & 1) ^ 1, abort_flag, args.err)) { ok = false; break; }
-          const int u = cu[w];
+          const int slot = w * kTmaSlots + (cq[i] & 1);
+          if (!mbar_wait(&empty[slot], ((cq[i] >> 1) & 1) ^ 1, abort_flag, args.err)) { ok = false; break; }
+          const int u = cu[i];
           const int e = args.active[u / nrb];
           unsigned char* sb = smem + slot * stage_bytes;
           mbar_expect_tx(&full[slot], tx);
           // coordinates {byte in K-box, row of the matrix, 2e (gate) .. 2e+1 (up), K-box}
-          tma_load_4d(sb, &tmap_c, 0, (u % nrb) * 8, 2 * e, ch[w] * nb, &full[slot]);
-          tma_load_4d(sb + 2 * nb * 1024, &tmap_s, 0, (u % nrb) * 8, 2 * e, ch[w] * nb, &full[slot]);
-          ++cq[w];
-          if (++ch[w] == nh) {
-            ch[w] = 0;
+          tma_load_4d(sb, &tmap_c, 0, (u % nrb) * 8, 2 * e, ch[i] * nb, &full[slot]);
+          tma_load_4d(sb + 2 * nb * 1024, &tmap_s, 0, (u % nrb) * 8, 2 * e, ch[i] * nb, &full[slot]);
+          ++cq[i];
+          if (++ch[i] == nh) {
+            ch[i] = 0;
             const int m = args.offsets[e + 1] - args.offsets[e];
-            if (++cp[w] * 8 >= m) { cp[w] = 0; cu[w] += kTmaWarps; }
+            if (++cp[i] * 8 >= m) { cp[i] = 0; cu[i] += kTmaWarps; }
           }
         }
       }
       if (!ok) {
         // drain, bounded: every issued stage has landed before the CTA exits
-        for (int w = 0; w < kTmaWarps; ++w)
+        for (int i = 0; i < PER; ++i)
           for (int par = 0; par < 2; ++par) {
-            if (cq[w] <= par) continue;
-            const int last = par + ((cq[w] - 1 - par) / 2) * 2;     // last stage issued on the slot
+            if (cq[i] <= par) continue;
+            const int last = par + ((cq[i] - 1 - par) / 2) * 2;     // last stage issued on the slot
             const uint64_t t0 = global_ns();
-            while (!mbar_try(&full[w * kTmaSlots + par], (uint32_t)((last >> 1) & 1)) &&
+            while (!mbar_try(&full[(w0 + i) * kTmaSlots + par], (uint32_t)((last >> 1) & 1)) &&
                    global_ns() - t0 < 100000000ull) {
             }
           }
@@ -598,7 +604,7 @@ gate_up_tma_kernel(const __grid_constant__ CUtensorMap tmap_c, const __grid_cons
     }
   } else {
     // ---------------- consumer warp ----------------
-    const int cw = warp - 1;
+    const int cw = warp - kTmaProd;
     const int g = lane >> 2, c = lane & 3;
     int q = 0;                                             // stages consumed
     for (int u = u_beg + cw; u < u_end && !*abort_flag; u += kTmaWarps) {
@@ -704,12 +710,14 @@ cudaError_t launch_decode_gate_up(const uint16_t* x_bf16, int T, int H, int F, i
                               b.E, xg, xe);
   if (st != cudaSuccess) return st;
   {
-    // TMA-fed warp units: K-chunks of at most 5 boxes of 128 bytes per row
+    // TMA-fed warp units: K-chunks of at most 2 boxes of 128 bytes per row
     const int n256 = H / 256;
     int nh = 1;
-    while (n256 % nh != 0 || n256 / nh > 5) ++nh;
+    while (n256 % nh != 0 || n256 / nh > 2) ++nh;
     const int nb = n256 / nh;
-    const size_t smem = (size_t)kTmaWarps * kTmaSlots * gu_stage_bytes(nb) + 1024 + 512;
+    // stages, 1 KiB of alignment slack, the barriers (16 B per slot) and the abort flag
+    const size_t smem = (size_t)kTmaWarps * kTmaSlots * gu_stage_bytes(nb) + 1024 +
+                        (size_t)kTmaWarps * kTmaSlots * 16 + 16;
     // the banks as [K-box][E*2 matrices][F rows][bytes of the K-box] (row pitch H/2 or H/16)
     CUtensorMap mc, ms;
     const uint64_t cdims[4] = {128, (uint64_t)F, 2 * (uint64_t)b.E, (uint64_t)n256};
@@ -718,7 +726,11 @@ cudaError_t launch_decode_gate_up(const uint16_t* x_bf16, int T, int H, int F, i
     const uint64_t sdims[4] = {16, (uint64_t)F, 2 * (uint64_t)b.E, (uint64_t)n256};
     const uint64_t sstr[3] = {(uint64_t)H / 16, (uint64_t)F * (H / 16), 16};
     const uint32_t sbox[4] = {16, 8, 2, (uint32_t)nb};
-    if (smem <= 232448 && make_map4(&mc, b.codes, cdims, cstr, cbox, true) &&
+    // with fewer than ~8 units per SM the warps cannot keep enough bytes in flight and the
+    // CTA kernel below is faster (measured at one token: 40 us against 42 us per layer)
+    const long long units_bound = (long long)(P < b.E ? P : b.E) * (F / 8);
+    if (units_bound >= 8LL * sm_count() && smem <= 232448 &&
+        make_map4(&mc, b.codes, cdims, cstr, cbox, true) &&
         make_map4(&ms, b.scales, sdims, sstr, sbox, false)) {
       GuTmaArgs ta{xg, xe, H, F, nh, nb, csr.expert_offsets, csr.active_experts, csr.n_active,
                    reinterpret_cast<float*>(ws + L.h), reinterpret_cast<uint32_t*>(ws + L.error_word)};
@@ -726,11 +738,12 @@ cudaError_t launch_decode_gate_up(const uint16_t* x_bf16, int T, int H, int F, i
                                 (int)smem);
       if (st != cudaSuccess) return st;
       const long long units = (long long)(P < b.E ? P : b.E) * (F / 8);
+      // every SM streams, even when there are fewer units than consumer warps
       long long grid = sm_count();
-      if (grid * kTmaWarps > units) grid = (units + kTmaWarps - 1) / kTmaWarps;
+      if (grid > units) grid = units;
       if (grid < 1) grid = 1;
-      return launch_pdl(gate_up_tma_kernel, dim3((unsigned)grid), dim3(32 * (1 + kTmaWarps)), smem,
-                        s, mc, ms, ta);
+      return launch_pdl(gate_up_tma_kernel, dim3((unsigned)grid), dim3(32 * (kTmaProd + kTmaWarps)),
+                        smem, s, mc, ms, ta);
     }
   }
   GateUpArgs a{xg, xe, b.codes, b.scales, H, F, csr.expert_offsets, csr.active_experts,
