@@ -684,6 +684,182 @@ gate_up_tma_kernel(const __grid_constant__ CUtensorMap tmap_c, const __grid_cons
   __syncthreads();
 }
 
+// ---------------------------------------------------------------------------
+// down, bulk-copy-fed warp units
+// ---------------------------------------------------------------------------
+// Same organisation as gate_up_tma_kernel for the down projection: a unit = (active
+// expert, 16 output rows) over the whole F, fetched as one stage by two contiguous bulk
+// copies (the unit's rows are consecutive: 16 x F/2 code bytes, then 16 x F/16 scale
+// bytes).  With F/2 bytes per row the quarter-warp reads of rows g, g+1 at 64 kb + 16 c
+// fall in different bank halves whenever F/2 is an odd multiple of 64 bytes.
+struct DnTmaArgs {
+  const __half* hg;
+  const int32_t* he;
+  const uint8_t* codes;
+  const uint8_t* scales;
+  int H, F;
+  const int32_t* offsets;
+  const int32_t* active;
+  const int32_t* n_active;
+  float* partial;
+  uint32_t* err;
+};
+
+__host__ __device__ constexpr int dn_stage_bytes(int F) {
+  return ((16 * (F / 2) + 16 * (F / 16)) + 1023) / 1024 * 1024;
+}
+
+__global__ void __launch_bounds__(32 * (kTmaProd + kTmaWarps), 1)
+down_tma_kernel(const DnTmaArgs args) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int H = args.H, F = args.F;
+  const int stage_bytes = dn_stage_bytes(F);
+  const int row_bytes = F / 2, srow = F / 16;
+  const uint32_t codes_bytes = 16 * row_bytes, scale_bytes = 16 * srow;
+  constexpr int NSLOT = kTmaWarps * kTmaSlots;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NSLOT * stage_bytes);
+  uint64_t* empty = full + NSLOT;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + NSLOT);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nrb = H / 16;                                  // units per expert
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NSLOT; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  const int n_units = *args.n_active * nrb;              // the CSR is complete
+  const int u_beg = (int)((long long)blockIdx.x * n_units / gridDim.x);
+  const int u_end = (int)((long long)(blockIdx.x + 1) * n_units / gridDim.x);
+  constexpr int PER = kTmaWarps / kTmaProd;
+
+  if (warp < kTmaProd) {
+    // ---------------- producers: warp p feeds consumers p*PER .. p*PER+PER-1 ----------------
+    // the weights do not depend on the previous kernel, so the copies start before its end
+    if (lane == 0) {
+      const int w0 = warp * PER;
+      int cu[PER], cp[PER], cq[PER];                       // unit, pass, stages
+      for (int i = 0; i < PER; ++i) { cu[i] = u_beg + w0 + i; cp[i] = 0; cq[i] = 0; }
+      bool more = true, ok = true;
+      while (more && ok) {
+        more = false;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+          if (!ok) break;
+          const int w = w0 + i;
+          if (cu[i] >= u_end) continue;
+          more = true;
+          const int slot = w * kTmaSlots + (cq[i] & 1);
+          if (!mbar_wait(&empty[slot], ((cq[i] >> 1) & 1) ^ 1, abort_flag, args.err)) { ok = false; break; }
+          const int u = cu[i];
+          const int e = args.active[u / nrb];
+          const size_t r0 = (size_t)e * H + (u % nrb) * 16;
+          unsigned char* sb = smem + slot * stage_bytes;
+          mbar_expect_tx(&full[slot], codes_bytes + scale_bytes);
+          bulk_load(sb, args.codes + r0 * row_bytes, codes_bytes, &full[slot]);
+          bulk_load(sb + codes_bytes, args.scales + r0 * srow, scale_bytes, &full[slot]);
+          ++cq[i];
+          const int m = args.offsets[e + 1] - args.offsets[e];
+          if (++cp[i] * 8 >= m) { cp[i] = 0; cu[i] += kTmaWarps; }
+        }
+      }
+      if (!ok) {
+        for (int i = 0; i < PER; ++i)
+          for (int par = 0; par < 2; ++par) {
+            if (cq[i] <= par) continue;
+            const int last = par + ((cq[i] - 1 - par) / 2) * 2;
+            const uint64_t t0 = global_ns();
+            while (!mbar_try(&full[(w0 + i) * kTmaSlots + par], (uint32_t)((last >> 1) & 1)) &&
+                   global_ns() - t0 < 100000000ull) {
+            }
+          }
+      }
+    }
+    pdl_wait();
+    pdl_trigger();
+  } else {
+    // ---------------- consumer warp ----------------
+    pdl_wait();                                            // h in f16 is complete
+    pdl_trigger();
+    const int cw = warp - kTmaProd;
+    const int g = lane >> 2, c = lane & 3;
+    const int nkb = F / 128;
+    int q = 0;
+    for (int u = u_beg + cw; u < u_end && !*abort_flag; u += kTmaWarps) {
+      const int e = args.active[u / nrb];
+      const int r0 = (u % nrb) * 16;
+      const int off = args.offsets[e];
+      const int m = args.offsets[e + 1] - off;
+      bool ok = true;
+      for (int tok0 = 0; tok0 < m && ok; tok0 += 8, ++q) {
+        const int live = min(8, m - tok0);
+        const __half* hrow = args.hg + (size_t)(off + tok0 + (g < live ? g : 0)) * F + 32 * c;
+        const int slot = cw * kTmaSlots + (q & 1);
+        if (!mbar_wait_warp(&full[slot], (q >> 1) & 1, abort_flag, args.err)) { ok = false; break; }
+        const uint32_t sb = smem_u32(smem + slot * stage_bytes);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        uint4 xb[4];
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq)
+          xb[qq] = g < live ? __ldg(reinterpret_cast<const uint4*>(hrow + 8 * qq)) : make_uint4(0, 0, 0, 0);
+        for (int kb = 0; kb < nkb; ++kb) {
+          uint4 xn[4];
+          const bool nxt = g < live && kb + 1 < nkb;
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq)
+            xn[qq] = nxt ? __ldg(reinterpret_cast<const uint4*>(hrow + (kb + 1) * 128 + 8 * qq))
+                         : make_uint4(0, 0, 0, 0);
+          uint4 A0, A1;
+          const uint32_t a0 = sb + g * row_bytes + kb * 64 + 16 * c;
+          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(A0.x), "=r"(A0.y), "=r"(A0.z), "=r"(A0.w) : "r"(a0));
+          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(A1.x), "=r"(A1.y), "=r"(A1.z), "=r"(A1.w) : "r"(a0 + 8 * row_bytes));
+          unsigned short s0, s1;
+          const uint32_t sa = sb + codes_bytes + g * srow + kb * 8 + 2 * c;
+          asm volatile("ld.shared.u16 %0, [%1];" : "=h"(s0) : "r"(sa));
+          asm volatile("ld.shared.u16 %0, [%1];" : "=h"(s1) : "r"(sa + 8 * srow));
+          const uint32_t f0 = e4m3x2_to_f16x2(s0), f1 = e4m3x2_to_f16x2(s1);
+          const uint32_t sc0[2] = {bcast_lo(f0), bcast_hi(f0)};
+          const uint32_t sc1[2] = {bcast_lo(f1), bcast_hi(f1)};
+          const uint32_t W0[4] = {A0.x, A0.y, A0.z, A0.w}, W1[4] = {A1.x, A1.y, A1.z, A1.w};
+#pragma unroll
+          for (int wi = 0; wi < 4; ++wi) {
+            uint32_t p0[4], p1[4];
+            e2m1x8_to_f16x2x4(W0[wi], p0[0], p0[1], p0[2], p0[3]);
+            e2m1x8_to_f16x2x4(W1[wi], p1[0], p1[1], p1[2], p1[3]);
+            const int sbk = wi >> 1;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+              mma_f16_16816(acc, hmul2_u32(p0[2 * hh], sc0[sbk]), hmul2_u32(p1[2 * hh], sc1[sbk]),
+                            hmul2_u32(p0[2 * hh + 1], sc0[sbk]), hmul2_u32(p1[2 * hh + 1], sc1[sbk]),
+                            hh ? xb[wi].z : xb[wi].x, hh ? xb[wi].w : xb[wi].y);
+          }
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) xb[qq] = xn[qq];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+        // acc[q]: row r0 + g + 8(q>>1), pair 2c + (q&1)
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+          const int n = 2 * c + (qq & 1);
+          if (n < live) {
+            const int pos = off + tok0 + n;
+            args.partial[(size_t)pos * H + r0 + g + 8 * (qq >> 1)] = ldexpf(acc[qq], args.he[pos]);
+          }
+        }
+      }
+      if (!ok) break;
+    }
+  }
+  __syncthreads();
+}
+
 int sm_count() {
   static int n = 0;
   if (!n) {
@@ -769,6 +945,24 @@ cudaError_t launch_decode_down(const moe_nvfp4_bank& b, moe_csr csr, int T, int 
                               (const float*)(ws + L.h), F, (const int32_t*)csr.expert_offsets, b.E,
                               hg, he);
   if (st != cudaSuccess) return st;
+  {
+    // bulk-copy-fed warp units when there are enough of them and the rows fit the loop
+    const size_t smem = (size_t)kTmaWarps * kTmaSlots * dn_stage_bytes(F) + 1024 +
+                        (size_t)kTmaWarps * kTmaSlots * 16 + 16;
+    const long long units = (long long)(P < b.E ? P : b.E) * (H / 16);
+    if (F % 128 == 0 && units >= 8LL * sm_count() && smem <= 232448 &&
+        (reinterpret_cast<uintptr_t>(b.codes) & 15) == 0 && (reinterpret_cast<uintptr_t>(b.scales) & 15) == 0) {
+      DnTmaArgs ta{hg, he, b.codes, b.scales, H, F, csr.expert_offsets, csr.active_experts,
+                   csr.n_active, reinterpret_cast<float*>(ws + L.partial),
+                   reinterpret_cast<uint32_t*>(ws + L.error_word)};
+      st = cudaFuncSetAttribute(down_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (st != cudaSuccess) return st;
+      long long grid = sm_count();
+      if (grid > units) grid = units;
+      return launch_pdl(down_tma_kernel, dim3((unsigned)grid), dim3(32 * (kTmaProd + kTmaWarps)),
+                        smem, s, ta);
+    }
+  }
   DownArgs a{hg, he, b.codes, b.scales, H, F, csr.expert_offsets, csr.active_experts,
              csr.n_active, reinterpret_cast<float*>(ws + L.partial)};
   const long long max_units = (long long)(P < b.E ? P : b.E) * (H / 128);
