@@ -463,7 +463,7 @@ def run_ours(args):
         gu_bytes = [uniq[b] * gu_bytes_per_expert for (b, _) in brk]
         ach = sum(gu_bytes) / (sum(gu_ms) * 1e-3) / 1e9
         alg = sum(gu_bytes) / len(gu_bytes)
-        ratio = recorded_traffic(args.workload, "gate_up_kernel")
+        ratio = recorded_traffic(args.workload, "gate_up_tma_kernel")
         roof = {"bound": "hbm", "kernel": "decode gate_up+SiLU (moe_grouped_gate_up_silu_nvfp4)",
                 "achieved": ach, "peak": pk, "unit": "GB/s", "frac": ach / pk,
                 "traffic": None if ratio is None else ratio * alg, "peak_source": pk_src,
