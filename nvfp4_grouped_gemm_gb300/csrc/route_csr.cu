@@ -110,6 +110,55 @@ route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
   }
 }
 
+// One CTA per token for wider routers: a bitonic sort in shared memory of the N (a power
+// of two >= E) keys (logit, id) in the same order (logit descending, then id ascending;
+// padding keys of -inf with ids past E sort last); the first k keys are the picks and the
+// weights are formed exactly as in route_topk_kernel.
+template <int N>
+__global__ void __launch_bounds__(N / 2)
+route_sort_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ ids,
+                  float* __restrict__ w) {
+  __shared__ float sv[N];
+  __shared__ int si[N];
+  pdl_wait();
+  pdl_trigger();
+  const int t = blockIdx.x;
+  const int tid = threadIdx.x;
+  const float* row = logits + (size_t)t * E;
+  for (int i = tid; i < N; i += N / 2) {
+    sv[i] = i < E ? __ldg(row + i) : -INFINITY;
+    si[i] = i;
+  }
+  __syncthreads();
+  for (int size = 2; size <= N; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const int i = 2 * stride * (tid / stride) + (tid & (stride - 1));
+      const int j = i + stride;
+      const bool up = (i & size) == 0;          // this block ends ordered best-first
+      const float vi = sv[i], vj = sv[j];
+      const int ii = si[i], ij = si[j];
+      if (before(vj, ij, vi, ii) == up) {
+        sv[i] = vj; sv[j] = vi;
+        si[i] = ij; si[j] = ii;
+      }
+      __syncthreads();
+    }
+  }
+  if (tid < 32) {
+    const int lane = tid;
+    const float first_v = sv[0];
+    const float my_val = lane < k ? sv[lane] : 0.0f;
+    const float ex = (lane < k) ? expf(my_val - first_v) : 0.0f;
+    // sum in ascending j so every lane sees the same value
+    float denom = 0.0f;
+    for (int j = 0; j < k; ++j) denom += __shfl_sync(0xffffffffu, ex, j);
+    if (lane < k) {
+      ids[(size_t)t * k + lane] = si[lane];
+      w[(size_t)t * k + lane] = ex / denom;
+    }
+  }
+}
+
 constexpr int kCsrThreads = 1024;
 constexpr int kCsrWarps = kCsrThreads / 32;
 
@@ -327,6 +376,13 @@ cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t*
                               cudaStream_t s) {
   const dim3 grid(T), block(32);
   const int pl = (E + 31) / 32;
+  // wider routers: sort per token (the warp version runs k dependent rounds of shuffles)
+  if (E > 64) {
+    if (E <= 128) return launch_pdl(route_sort_kernel<128>, grid, dim3(64), 0, s, logits, T, E, k, ids, w);
+    if (E <= 256) return launch_pdl(route_sort_kernel<256>, grid, dim3(128), 0, s, logits, T, E, k, ids, w);
+    if (E <= 512) return launch_pdl(route_sort_kernel<512>, grid, dim3(256), 0, s, logits, T, E, k, ids, w);
+    return launch_pdl(route_sort_kernel<1024>, grid, dim3(512), 0, s, logits, T, E, k, ids, w);
+  }
   if (pl <= 1) return launch_pdl(route_topk_kernel<1>, grid, block, 0, s, logits, T, E, k, ids, w);
   if (pl <= 2) return launch_pdl(route_topk_kernel<2>, grid, block, 0, s, logits, T, E, k, ids, w);
   if (pl <= 4) return launch_pdl(route_topk_kernel<4>, grid, block, 0, s, logits, T, E, k, ids, w);
