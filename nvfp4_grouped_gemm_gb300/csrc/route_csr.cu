@@ -370,6 +370,59 @@ csr_place_kernel(const int32_t* __restrict__ ids, int P, int E, const int32_t* _
   }
 }
 
+// Few pairs (P <= kCsrSmallPairs): one histogram and one scan; pair p's place among the
+// pairs of its expert is the number of earlier pairs with the same expert.
+constexpr int kCsrSmallPairs = 256;
+
+__global__ void __launch_bounds__(kCsrThreads, 1)
+csr_small_kernel(const int32_t* __restrict__ ids_g, int P, int E, int32_t* __restrict__ offsets,
+                 int32_t* __restrict__ pair_ids, int32_t* __restrict__ active,
+                 int32_t* __restrict__ n_active, int32_t* __restrict__ pair_pos,
+                 uint32_t* __restrict__ err) {
+  __shared__ int hist[kMaxE];
+  __shared__ int ids_s[kCsrSmallPairs];
+  __shared__ int scratch[kCsrWarps];
+  const int tid = threadIdx.x;
+  if (tid < E) hist[tid] = 0;
+  pdl_wait();                                 // the expert ids are complete
+  pdl_trigger();
+  int e = -1;
+  bool valid = false;
+  if (tid < P) {
+    e = __ldg(ids_g + tid);
+    valid = e >= 0 && e < E;
+    ids_s[tid] = valid ? e : -1;
+    if (!valid) {
+      pair_pos[tid] = -1;
+      atomicOr(err, (uint32_t)MOE_DEVERR_EXPERT_ID);
+    }
+  }
+  __syncthreads();
+  if (valid) atomicAdd(&hist[e], 1);
+  __syncthreads();
+  const int cnt = tid < E ? hist[tid] : 0;
+  int total, act_total;
+  const int off = block_exclusive_scan(cnt, scratch, &total);
+  const int act = block_exclusive_scan((tid < E && cnt > 0) ? 1 : 0, scratch, &act_total);
+  if (tid < E) {
+    offsets[tid] = off;
+    hist[tid] = off;
+    if (cnt > 0) active[act] = tid;
+  }
+  if (tid == 0) {
+    offsets[E] = total;
+    *n_active = act_total;
+  }
+  __syncthreads();
+  if (valid) {
+    int rank = 0;
+    for (int q = 0; q < tid; ++q) rank += ids_s[q] == e;
+    const int pos = hist[e] + rank;
+    pair_ids[pos] = tid;
+    pair_pos[tid] = pos;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w,
@@ -399,6 +452,9 @@ size_t csr_scratch_bytes(int P, int E) {
 cudaError_t launch_build_csr(const int32_t* ids, int P, int k, int E, moe_csr csr,
                              int32_t* pair_pos, uint32_t* err, int32_t* scratch, cudaStream_t s) {
   (void)k;
+  if (P <= kCsrSmallPairs)
+    return launch_pdl(csr_small_kernel, dim3(1), dim3(kCsrThreads), 0, s, ids, P, E,
+                      csr.expert_offsets, csr.pair_ids, csr.active_experts, csr.n_active, pair_pos, err);
   if (P >= kCsrGridMinPairs && scratch) {
     const int nb = (P + kChunkPairs - 1) / kChunkPairs;
     cudaError_t st = launch_pdl(csr_count_kernel, dim3(nb), dim3(kChunkThreads),
