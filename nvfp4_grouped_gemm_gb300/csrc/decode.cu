@@ -549,8 +549,8 @@ gate_up_tma_kernel(const __grid_constant__ CUtensorMap tmap_c, const __grid_cons
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  pdl_wait();                                              // gathered activations are ready
-  pdl_trigger();
+  // the producers read only the CSR (complete two kernels back) and the weights, so they
+  // start streaming before the gathered activations are ready; the consumers wait
   const int n_units = *args.n_active * nrb;
   const int u_beg = (int)((long long)blockIdx.x * n_units / gridDim.x);
   const int u_end = (int)((long long)(blockIdx.x + 1) * n_units / gridDim.x);
@@ -558,6 +558,7 @@ gate_up_tma_kernel(const __grid_constant__ CUtensorMap tmap_c, const __grid_cons
   constexpr int PER = kTmaWarps / kTmaProd;               // consumer warps per producer
   if (warp < kTmaProd) {
     // ---------------- TMA producers: warp p feeds consumers p*PER .. p*PER+PER-1 ----------------
+    pdl_trigger();
     if (lane == 0) {
       const uint32_t tx = (uint32_t)(2 * nb * 1024 + 2 * 8 * sc_bytes);
       const int w0 = warp * PER;
@@ -604,6 +605,8 @@ gate_up_tma_kernel(const __grid_constant__ CUtensorMap tmap_c, const __grid_cons
     }
   } else {
     // ---------------- consumer warp ----------------
+    pdl_wait();                                            // gathered activations are ready
+    pdl_trigger();
     const int cw = warp - kTmaProd;
     const int g = lane >> 2, c = lane & 3;
     int q = 0;                                             // stages consumed
