@@ -121,7 +121,9 @@ typedef struct moe_ws_layout {
 } moe_ws_layout;
 
 /* Limits (MOE_ERR_UNSUPPORTED beyond them): 1 <= k <= min(E, 32); E <= 1024;
- * H % 256 == 0 and H <= 4096; F % 64 == 0; T*k < 2^31 / max(H, F). */
+ * H % 256 == 0 and H <= 4096; F % 64 == 0; T*k < 2^31 / max(H, F); F <= 1408 on the
+ * DECODE path and F <= 4096 on the PREFILL path (the path AUTO resolves to counts;
+ * moe_workspace_bytes returns 0 for such sizes). */
 
 /* Workspace size in bytes for one layer with these sizes (0 if the sizes are invalid). */
 size_t moe_workspace_bytes(int32_t T, int32_t H, int32_t F, int32_t E, int32_t k, int32_t path);
@@ -162,7 +164,11 @@ moe_status moe_build_expert_csr(const int32_t* topk_ids, int32_t T, int32_t k, i
  * expert's 2F x H NVFP4 rows are read from HBM once per call whatever its number of
  * pairs (the union-of-experts gather of "moe_union_probe.rs"). x_bf16 bf16 [T][H]
  * (16-byte aligned); w_gate_up: rows = 2F, in_f = H. Result h f32 [P][F] in the
- * workspace, rows in CSR order. */
+ * workspace, rows in CSR order. Reads the CSR and the workspace's pair_pos written by
+ * moe_build_expert_csr on this workspace. The DECODE path starts reading x_bf16 before
+ * the CSR kernel has finished (its rows do not depend on the routing), so x_bf16 must be
+ * complete in stream order when the call is made: a kernel that writes it and is launched
+ * with programmatic dependent launch must not signal its dependents before its last write. */
 moe_status moe_grouped_gate_up_silu_nvfp4(const void* x_bf16, int32_t T, int32_t H, int32_t F,
                                           int32_t k, const moe_nvfp4_bank* w_gate_up,
                                           moe_csr csr, int32_t path, void* ws, size_t ws_bytes,
@@ -193,7 +199,9 @@ moe_status moe_grouped_down_combine_nvfp4(const moe_nvfp4_bank* w_down, moe_csr 
  * the one array: calls that can overlap on the GPU (different streams, or different host
  * threads, on the same device) race, so serialise them. Invalid expert ids are left out
  * as in moe_build_expert_csr, but no error word is reported: expert_offsets[E] < T*k
- * tells the caller that some were dropped. */
+ * tells the caller that some were dropped. The layer calls (gate/up, down/combine) also
+ * read the per-pair positions that moe_build_expert_csr writes into their workspace, so
+ * they need that entry point; this one serves callers that want the CSR alone. */
 moe_status moe_build_expert_csr_static(const int32_t* topk_ids, int32_t T, int32_t k, int32_t E,
                                        moe_csr csr, void* stream);
 

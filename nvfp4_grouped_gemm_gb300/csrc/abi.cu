@@ -55,10 +55,20 @@ int resolve_path(int T, int k, int path) {
   return (long long)T * k >= kPrefillMinPairs ? MOE_PATH_PREFILL : MOE_PATH_DECODE;
 }
 
+// The per-path limit on F (the path AUTO resolves to for these sizes).
+moe_status path_supported(int T, int F, int k, int path) {
+  if (path != MOE_PATH_AUTO && path != MOE_PATH_DECODE && path != MOE_PATH_PREFILL)
+    return MOE_ERR_INVALID_ARG;
+  const int p = resolve_path(T, k, path);
+  if (p == MOE_PATH_DECODE && F > kDecodeMaxF) return MOE_ERR_UNSUPPORTED;
+  if (p == MOE_PATH_PREFILL && F > kPrefillMaxF) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
 bool compute_layout(int T, int H, int F, int E, int k, int path, moe_ws_layout* L) {
   std::memset(L, 0, sizeof(*L));
   if (sizes_supported(T, H, F, E, k) != MOE_OK) return false;
-  if (path != MOE_PATH_AUTO && path != MOE_PATH_DECODE && path != MOE_PATH_PREFILL) return false;
+  if (path_supported(T, F, k, path) != MOE_OK) return false;
   path = resolve_path(T, k, path);
   const size_t P = (size_t)T * k;
   size_t o = 0;
@@ -107,6 +117,7 @@ moe_status moe_workspace_layout(int32_t T, int32_t H, int32_t F, int32_t E, int3
   if (!out) return MOE_ERR_INVALID_ARG;
   moe_status st = sizes_supported(T, H, F, E, k);
   if (st != MOE_OK) return st;
+  if ((st = path_supported(T, F, k, path)) != MOE_OK) return st;
   if (!compute_layout(T, H, F, E, k, path, out)) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
@@ -182,6 +193,7 @@ moe_status moe_grouped_gate_up_silu_nvfp4(const void* x_bf16, int32_t T, int32_t
   const int E = w_gate_up->E;
   moe_status st = sizes_supported(T, H, F, E, k);
   if (st != MOE_OK) return st;
+  if ((st = path_supported(T, F, k, path)) != MOE_OK) return st;
   if ((st = check_bank(w_gate_up, E, 2 * F, H)) != MOE_OK) return st;
   if ((st = check_csr(csr)) != MOE_OK) return st;
   moe_ws_layout L;
@@ -209,6 +221,7 @@ moe_status moe_grouped_down_combine_nvfp4(const moe_nvfp4_bank* w_down, moe_csr 
   const int E = w_down->E;
   moe_status st = sizes_supported(T, H, F, E, k);
   if (st != MOE_OK) return st;
+  if ((st = path_supported(T, F, k, path)) != MOE_OK) return st;
   if ((st = check_bank(w_down, E, H, F)) != MOE_OK) return st;
   if ((st = check_csr(csr)) != MOE_OK) return st;
   moe_ws_layout L;

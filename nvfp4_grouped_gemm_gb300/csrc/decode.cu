@@ -5,7 +5,8 @@
 //
 //   x_gather_kernel   CSR row r <- token x row as f16 times 2^-e (e from the row's amax,
 //                     so the largest magnitude lands in [2^14, 2^15): exact for bf16
-//                     values in f16's normal range)
+//                     values in f16's normal range); one warp per pair, the row read and
+//                     converted before the wait and stored at the pair's CSR row after it
 //   gate_up_kernel    CTA = (active expert, 16 gate rows + the matching 16 up rows); the
 //                     CTA's weight bytes land in shared memory with 16-byte cp.async
 //                     issued by every thread up front, the activation fragments come
@@ -72,24 +73,24 @@ __device__ __forceinline__ int swz_chunk(int lc) { return (lc ^ (((lc >> 3) & 1)
 // ---------------------------------------------------------------------------
 // gather + f16 prescale of the activation rows of every CSR row (decode stage a3)
 // ---------------------------------------------------------------------------
+// One warp per pair p = t*k + j.  The token's row depends only on x, so it is read and
+// converted before the wait; after it, the row goes to the pair's CSR row pair_pos[p].
+template <int NP>
 __global__ void __launch_bounds__(256) x_gather_kernel(const uint16_t* __restrict__ x, int H, int k,
-                                                       const int32_t* __restrict__ pair_ids,
-                                                       const int32_t* __restrict__ offsets, int E,
+                                                       int P, const int32_t* __restrict__ pair_pos,
                                                        __half* __restrict__ xg,
                                                        int32_t* __restrict__ xe) {
-  pdl_wait();
-  pdl_trigger();
-  const int pos = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int p = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (pos >= offsets[E]) return;
-  const uint16_t* row = x + (size_t)(pair_ids[pos] / k) * H;
-  // the whole row in registers (H <= 4096: at most 16 pieces of 8 values per lane)
-  uint4 v[16];
+  const bool has = p < P;
+  const uint16_t* row = x + (size_t)(has ? p / k : 0) * H;
+  // the whole row in registers (H <= 256 * NP: NP pieces of 8 values per lane)
+  uint4 v[NP];
   float amax = 0.0f;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
+  for (int i = 0; i < NP; ++i) {
     const int c = (lane + 32 * i) * 8;
-    v[i] = c < H ? *reinterpret_cast<const uint4*>(row + c) : make_uint4(0, 0, 0, 0);
+    v[i] = has && c < H ? *reinterpret_cast<const uint4*>(row + c) : make_uint4(0, 0, 0, 0);
     const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -100,24 +101,36 @@ __global__ void __launch_bounds__(256) x_gather_kernel(const uint16_t* __restric
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   const int e = f16_prescale_exp(amax);
-  if (lane == 0) xe[pos] = e;
+  // times 2^-e as two power-of-two factors (each a normal float for every e of a bf16 row)
+  const float s1 = pow2f(-e / 2), s2 = pow2f(-e - (-e / 2));
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int c = (lane + 32 * i) * 8;
-    if (c >= H) break;
-    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-    uint32_t o[4];
+  for (int i = 0; i < NP; ++i) {
+    uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const __half2 hv = __floats2half2_rn(ldexpf(__uint_as_float(w[q] << 16), -e),
-                                           ldexpf(__uint_as_float(w[q] & 0xffff0000u), -e));
-      o[q] = *reinterpret_cast<const uint32_t*>(&hv);
+      const __half2 hv = __floats2half2_rn((__uint_as_float(w[q] << 16) * s1) * s2,
+                                           (__uint_as_float(w[q] & 0xffff0000u) * s1) * s2);
+      w[q] = *reinterpret_cast<const uint32_t*>(&hv);
     }
-    *reinterpret_cast<uint4*>(xg + (size_t)pos * H + c) = make_uint4(o[0], o[1], o[2], o[3]);
+    v[i] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  pdl_wait();                                  // pair_pos is complete
+  pdl_trigger();
+  if (!has) return;
+  const int pos = pair_pos[p];
+  if (pos < 0) return;                         // invalid expert id: the pair has no row
+  if (lane == 0) xe[pos] = e;
+#pragma unroll
+  for (int i = 0; i < NP; ++i) {
+    const int c = (lane + 32 * i) * 8;
+    if (c >= H) break;
+    *reinterpret_cast<uint4*>(xg + (size_t)pos * H + c) = v[i];
   }
 }
 
-// Same for h (f32 rows already in CSR order).
+// Same for h (f32 rows already in CSR order), F <= 128*NR: the row stays in registers, so
+// h is read once.
+template <int NR>
 __global__ void __launch_bounds__(256) h_prep_kernel(const float* __restrict__ h, int F,
                                                      const int32_t* __restrict__ offsets, int E,
                                                      __half* __restrict__ hg,
@@ -128,27 +141,26 @@ __global__ void __launch_bounds__(256) h_prep_kernel(const float* __restrict__ h
   const int lane = threadIdx.x & 31;
   if (pos >= offsets[E]) return;
   const float* row = h + (size_t)pos * F;
+  float4 v[NR];
   float amax = 0.0f;
-  for (int c = lane * 8; c < F; c += 256) {
-    const float4 a = *reinterpret_cast<const float4*>(row + c);
-    const float4 b = *reinterpret_cast<const float4*>(row + c + 4);
-    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))));
-    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w))));
+#pragma unroll
+  for (int i = 0; i < NR; ++i) {
+    const int c = 4 * lane + 128 * i;
+    v[i] = c < F ? *reinterpret_cast<const float4*>(row + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   const int e = f16_prescale_exp(amax);
   if (lane == 0) he[pos] = e;
-  for (int c = lane * 8; c < F; c += 256) {
-    const float4 a = *reinterpret_cast<const float4*>(row + c);
-    const float4 b = *reinterpret_cast<const float4*>(row + c + 4);
-    __half2 h0 = __floats2half2_rn(ldexpf(a.x, -e), ldexpf(a.y, -e));
-    __half2 h1 = __floats2half2_rn(ldexpf(a.z, -e), ldexpf(a.w, -e));
-    __half2 h2 = __floats2half2_rn(ldexpf(b.x, -e), ldexpf(b.y, -e));
-    __half2 h3 = __floats2half2_rn(ldexpf(b.z, -e), ldexpf(b.w, -e));
-    *reinterpret_cast<uint4*>(hg + (size_t)pos * F + c) =
-        make_uint4(*reinterpret_cast<uint32_t*>(&h0), *reinterpret_cast<uint32_t*>(&h1),
-                   *reinterpret_cast<uint32_t*>(&h2), *reinterpret_cast<uint32_t*>(&h3));
+#pragma unroll
+  for (int i = 0; i < NR; ++i) {
+    const int c = 4 * lane + 128 * i;
+    if (c >= F) break;
+    const __half2 h0 = __floats2half2_rn(ldexpf(v[i].x, -e), ldexpf(v[i].y, -e));
+    const __half2 h1 = __floats2half2_rn(ldexpf(v[i].z, -e), ldexpf(v[i].w, -e));
+    *reinterpret_cast<uint2*>(hg + (size_t)pos * F + c) =
+        make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
   }
 }
 
@@ -464,20 +476,40 @@ __global__ void __launch_bounds__(256, 2) down_kernel(const DownArgs args) {
 __global__ void __launch_bounds__(256)
 combine_kernel(const float* __restrict__ w, const int32_t* __restrict__ pair_pos,
                const float* __restrict__ partial, int H, int k, float* __restrict__ y) {
-  pdl_wait();
+  __shared__ int s_pos[kMaxK];
+  __shared__ float s_w[kMaxK];
+  // positions and weights come from the CSR and the router, complete two or more kernels
+  // back; only the partial rows need the wait
   const int t = blockIdx.y;
+  if (threadIdx.x < k) {
+    s_pos[threadIdx.x] = pair_pos[(size_t)t * k + threadIdx.x];
+    s_w[threadIdx.x] = w[(size_t)t * k + threadIdx.x];
+  }
+  __syncthreads();
+  pdl_wait();
   const int r = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
   if (r >= H) return;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int j = 0; j < k; ++j) {
-    const int pos = pair_pos[(size_t)t * k + j];
-    if (pos < 0) continue;
-    const float wj = w[(size_t)t * k + j];
-    const float4 z = *reinterpret_cast<const float4*>(partial + (size_t)pos * H + r);
-    acc.x = fmaf(wj, z.x, acc.x);
-    acc.y = fmaf(wj, z.y, acc.y);
-    acc.z = fmaf(wj, z.z, acc.z);
-    acc.w = fmaf(wj, z.w, acc.w);
+  // the partial rows are loaded four pairs at a time and summed in ascending j
+  for (int j0 = 0; j0 < k; j0 += 4) {
+    float4 z[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int j = j0 + q;
+      const int pos = j < k ? s_pos[j] : -1;
+      z[q] = pos >= 0 ? __ldcs(reinterpret_cast<const float4*>(partial + (size_t)pos * H + r))
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int j = j0 + q;
+      if (j >= k || s_pos[j] < 0) continue;
+      const float wj = s_w[j];
+      acc.x = fmaf(wj, z[q].x, acc.x);
+      acc.y = fmaf(wj, z[q].y, acc.y);
+      acc.z = fmaf(wj, z[q].z, acc.z);
+      acc.w = fmaf(wj, z[q].w, acc.w);
+    }
   }
   *reinterpret_cast<float4*>(y + (size_t)t * H + r) = acc;
 }
@@ -522,13 +554,15 @@ __device__ __forceinline__ uint32_t gu_scale_off(int nb, int kbox, int mat, int 
   return 2 * nb * 1024 + kbox * 256 + mat * 128 + row * 16;
 }
 
+template <int NB>
 __global__ void __launch_bounds__(32 * (kTmaProd + kTmaWarps), 1)
 gate_up_tma_kernel(const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_s,
                    const GuTmaArgs args) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int nb = args.nb, nh = args.nh;
+  constexpr int nb = NB;                                   // 128-byte K-boxes per stage
+  const int nh = args.nh;
   const int stage_bytes = gu_stage_bytes(nb);
   constexpr int NSLOT = kTmaWarps * kTmaSlots;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + NSLOT * stage_bytes);
@@ -628,6 +662,7 @@ gate_up_tma_kernel(const __grid_constant__ CUtensorMap tmap_c, const __grid_cons
           const int slot = cw * kTmaSlots + (q & 1);
           if (!mbar_wait_warp(&full[slot], (q >> 1) & 1, abort_flag, args.err)) { ok = false; break; }
           const uint32_t sb = smem_u32(smem + slot * stage_bytes);
+#pragma unroll
           for (int kl = 0; kl < 2 * nb; ++kl) {             // 128-element k-blocks of the chunk
             const int kbg = hc * 2 * nb + kl;               // k-block within the row
             uint4 xn[4];
@@ -884,9 +919,11 @@ cudaError_t launch_decode_gate_up(const uint16_t* x_bf16, int T, int H, int F, i
   const int P = T * k;
   __half* xg = reinterpret_cast<__half*>(ws + L.xg);
   int32_t* xe = reinterpret_cast<int32_t*>(ws + L.xe);
-  cudaError_t st = launch_pdl(x_gather_kernel, dim3((P + 7) / 8), dim3(256), 0, s, x_bf16, H, k,
-                              (const int32_t*)csr.pair_ids, (const int32_t*)csr.expert_offsets,
-                              b.E, xg, xe);
+  const int np = H / 256;                         // 16-byte pieces per lane
+  auto xk = np <= 4 ? x_gather_kernel<4> : np <= 8 ? x_gather_kernel<8>
+          : np <= 12 ? x_gather_kernel<12> : x_gather_kernel<16>;
+  cudaError_t st = launch_pdl(xk, dim3((P + 7) / 8), dim3(256), 0, s, x_bf16, H, k,
+                              P, (const int32_t*)(ws + L.pair_pos), xg, xe);
   if (st != cudaSuccess) return st;
   {
     // TMA-fed warp units: K-chunks of at most 2 boxes of 128 bytes per row
@@ -913,7 +950,8 @@ cudaError_t launch_decode_gate_up(const uint16_t* x_bf16, int T, int H, int F, i
         make_map4(&ms, b.scales, sdims, sstr, sbox, false)) {
       GuTmaArgs ta{xg, xe, H, F, nh, nb, csr.expert_offsets, csr.active_experts, csr.n_active,
                    reinterpret_cast<float*>(ws + L.h), reinterpret_cast<uint32_t*>(ws + L.error_word)};
-      st = cudaFuncSetAttribute(gate_up_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      auto gk = nb == 1 ? gate_up_tma_kernel<1> : gate_up_tma_kernel<2>;
+      st = cudaFuncSetAttribute(gk, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)smem);
       if (st != cudaSuccess) return st;
       const long long units = (long long)(P < b.E ? P : b.E) * (F / 8);
@@ -921,7 +959,7 @@ cudaError_t launch_decode_gate_up(const uint16_t* x_bf16, int T, int H, int F, i
       long long grid = sm_count();
       if (grid > units) grid = units;
       if (grid < 1) grid = 1;
-      return launch_pdl(gate_up_tma_kernel, dim3((unsigned)grid), dim3(32 * (kTmaProd + kTmaWarps)),
+      return launch_pdl(gk, dim3((unsigned)grid), dim3(32 * (kTmaProd + kTmaWarps)),
                         smem, s, mc, ms, ta);
     }
   }
@@ -944,9 +982,12 @@ cudaError_t launch_decode_down(const moe_nvfp4_bank& b, moe_csr csr, int T, int 
   const int P = T * k;
   __half* hg = reinterpret_cast<__half*>(ws + L.hg);
   int32_t* he = reinterpret_cast<int32_t*>(ws + L.he);
-  cudaError_t st = launch_pdl(h_prep_kernel, dim3((P + 7) / 8), dim3(256), 0, s,
-                              (const float*)(ws + L.h), F, (const int32_t*)csr.expert_offsets, b.E,
-                              hg, he);
+  const int nr = (F + 127) / 128;                 // float4 per lane
+  if (nr > 16) return cudaErrorInvalidValue;      // F <= 1408 on this path
+  auto hk = nr <= 2 ? h_prep_kernel<2> : nr <= 5 ? h_prep_kernel<5> : nr <= 8 ? h_prep_kernel<8>
+                                                                    : h_prep_kernel<16>;
+  cudaError_t st = launch_pdl(hk, dim3((P + 7) / 8), dim3(256), 0, s, (const float*)(ws + L.h), F,
+                              (const int32_t*)csr.expert_offsets, b.E, hg, he);
   if (st != cudaSuccess) return st;
   {
     // bulk-copy-fed warp units when there are enough of them and the rows fit the loop

@@ -14,6 +14,10 @@ namespace moe {
 constexpr int kMaxE = 1024;
 constexpr int kMaxK = 32;
 constexpr int kPrefillMinPairs = 2048;
+// Largest F per path: the decode down kernel keeps two 128-row weight tiles and eight f16
+// h rows in shared memory; the prefill Q(h) kernel holds a row of h in registers.
+constexpr int kDecodeMaxF = 1408;
+constexpr int kPrefillMaxF = 4096;
 constexpr size_t kAlign = 256;
 
 inline size_t align_up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a; }

@@ -1,9 +1,12 @@
 // Top-k routing and the expert-first CSR.
 //
-// route_topk_kernel: one warp per token.  Round r selects the largest (logit, -id) pair
-// among those ordered strictly after the pair selected in round r-1, so no element is
-// ever removed or overwritten and ties resolve to the lower id exactly as the float32
-// comparison dictates.
+// route_merge_kernel: one CTA per token, one expert per thread.  Each (logit, id) pair
+// becomes a 64-bit key whose unsigned order is the routing order (logit descending, then
+// id ascending; -0 and +0 share a key, as the float32 comparison makes them equal).  Every
+// warp sorts its 32 keys with a shuffle bitonic sort; the sorted lists are then merged
+// pairwise through shared memory (the best 32 of two descending lists a, b are
+// max(a[i], b[31-i]), a bitonic sequence that five shuffle steps sort), so warp 0 ends with
+// the best 32 keys in order and k <= 32 of them are the picks.
 //
 // build_csr_kernel: one CTA.  The P pairs are cut into 32 contiguous slices, one per warp.
 // Pass A counts each slice's pairs per expert in shared memory, pass B turns the
@@ -24,136 +27,85 @@ namespace moe {
 
 namespace {
 
-__device__ __forceinline__ bool before(float va, int ia, float vb, int ib) {
-  return va > vb || (va == vb && ia < ib);
-}
-
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-constexpr int kNone = 0x7fffffff;   // id of an empty candidate
-
-// a beats b: a is a candidate and either b is empty or a comes first in (logit desc, id asc)
-__device__ __forceinline__ bool beats(float av, int ai, float bv, int bi) {
-  return ai != kNone && (bi == kNone || before(av, ai, bv, bi));
+// Routing key: unsigned order = (logit descending, id ascending); 0 is below every key.
+__device__ __forceinline__ unsigned long long route_key(float v, int id) {
+  const uint32_t u = (v == 0.0f) ? 0u : __float_as_uint(v);
+  const uint32_t o = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((unsigned long long)o << 32) | (0xffffffffu - (uint32_t)id);
+}
+__device__ __forceinline__ float key_logit(unsigned long long key) {
+  const uint32_t o = (uint32_t)(key >> 32);
+  return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
+}
+__device__ __forceinline__ int key_id(unsigned long long key) {
+  return (int)(0xffffffffu - (uint32_t)key);
+}
+__device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) {
+  return a > b ? a : b;
+}
+__device__ __forceinline__ unsigned long long umin64(unsigned long long a, unsigned long long b) {
+  return a < b ? a : b;
 }
 
-// One warp (one CTA) per token; lane l holds experts l, l+32, ... (PL per lane, padded).
-// Every untaken expert is ordered after the last pick, so each lane keeps the best of its
-// untaken experts; a round is a warp butterfly over those, after which only the winning
-// lane marks its slot taken and rescans its own PL slots.
-template <int PL>
-__global__ void __launch_bounds__(32)
-route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
-                  int32_t* __restrict__ ids, float* __restrict__ w) {
-  pdl_wait();
-  pdl_trigger();
-  const int t = blockIdx.x;
-  const int lane = threadIdx.x & 31;
-  if (t >= T) return;
-  const float* row = logits + (size_t)t * E;
-  float v[PL];
+// Sort a bitonic sequence held one key per lane into descending lane order.
+__device__ __forceinline__ unsigned long long bitonic_merge_desc(unsigned long long key, int lane) {
 #pragma unroll
-  for (int i = 0; i < PL; ++i) {
-    const int e = lane + 32 * i;
-    v[i] = e < E ? __ldg(row + e) : 0.0f;
+  for (int stride = 16; stride > 0; stride >>= 1) {
+    const unsigned long long o = __shfl_xor_sync(0xffffffffu, key, stride);
+    key = (lane & stride) == 0 ? umax64(key, o) : umin64(key, o);
   }
-  uint32_t taken = 0;
-  auto local_best = [&](float& bv, int& bi) {
-    float cv[PL];
-    int ci[PL];
-#pragma unroll
-    for (int i = 0; i < PL; ++i) {
-      const int e = lane + 32 * i;
-      cv[i] = v[i];
-      ci[i] = (e < E && !((taken >> i) & 1u)) ? e : kNone;
-    }
-#pragma unroll
-    for (int s = PL / 2; s >= 1; s >>= 1)
-#pragma unroll
-      for (int i = 0; i < s; ++i)
-        if (beats(cv[i + s], ci[i + s], cv[i], ci[i])) { cv[i] = cv[i + s]; ci[i] = ci[i + s]; }
-    bv = cv[0];
-    bi = ci[0];
-  };
-  float lbv;
-  int lbi;
-  local_best(lbv, lbi);
-  float first_v = 0.0f;
-  float my_val = 0.0f;   // lane j < k keeps the j-th selected logit
-  int my_id = 0;
-  for (int r = 0; r < k; ++r) {
-    float bv = lbv;
-    int bi = lbi;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (beats(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-    }
-    if (r == 0) first_v = bv;
-    if (lane == r) { my_val = bv; my_id = bi; }
-    if (bi != kNone && lane == (bi & 31)) {
-      taken |= 1u << (bi >> 5);
-      local_best(lbv, lbi);
-    }
-  }
-  const float ex = (lane < k) ? expf(my_val - first_v) : 0.0f;
-  // sum in ascending j so every lane sees the same value
-  float denom = 0.0f;
-  for (int j = 0; j < k; ++j) denom += __shfl_sync(0xffffffffu, ex, j);
-  if (lane < k) {
-    ids[(size_t)t * k + lane] = my_id;
-    w[(size_t)t * k + lane] = ex / denom;
-  }
+  return key;
 }
 
-// One CTA per token for wider routers: a bitonic sort in shared memory of the N (a power
-// of two >= E) keys (logit, id) in the same order (logit descending, then id ascending;
-// padding keys of -inf with ids past E sort last); the first k keys are the picks and the
-// weights are formed exactly as in route_topk_kernel.
-template <int N>
-__global__ void __launch_bounds__(N / 2)
-route_sort_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ ids,
-                  float* __restrict__ w) {
-  __shared__ float sv[N];
-  __shared__ int si[N];
-  pdl_wait();
-  pdl_trigger();
-  const int t = blockIdx.x;
-  const int tid = threadIdx.x;
-  const float* row = logits + (size_t)t * E;
-  for (int i = tid; i < N; i += N / 2) {
-    sv[i] = i < E ? __ldg(row + i) : -INFINITY;
-    si[i] = i;
-  }
-  __syncthreads();
-  for (int size = 2; size <= N; size <<= 1) {
+// Descending sort of one key per lane.  Before the last size, blocks alternate between
+// descending ((lane & size) == 0) and ascending, so each pair of blocks is bitonic.
+__device__ __forceinline__ unsigned long long warp_sort_desc(unsigned long long key, int lane) {
+#pragma unroll
+  for (int size = 2; size < 32; size <<= 1) {
+#pragma unroll
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      const int i = 2 * stride * (tid / stride) + (tid & (stride - 1));
-      const int j = i + stride;
-      const bool up = (i & size) == 0;          // this block ends ordered best-first
-      const float vi = sv[i], vj = sv[j];
-      const int ii = si[i], ij = si[j];
-      if (before(vj, ij, vi, ii) == up) {
-        sv[i] = vj; sv[j] = vi;
-        si[i] = ij; si[j] = ii;
-      }
-      __syncthreads();
+      const unsigned long long o = __shfl_xor_sync(0xffffffffu, key, stride);
+      const bool keep_max = ((lane & stride) == 0) == ((lane & size) == 0);
+      key = keep_max ? umax64(key, o) : umin64(key, o);
     }
   }
-  if (tid < 32) {
-    const int lane = tid;
-    const float first_v = sv[0];
-    const float my_val = lane < k ? sv[lane] : 0.0f;
-    const float ex = (lane < k) ? expf(my_val - first_v) : 0.0f;
+  return bitonic_merge_desc(key, lane);
+}
+
+// blockDim.x = 32 * ceil(E / 32) threads (E <= 1024); thread e holds expert e.
+__global__ void __launch_bounds__(1024)
+route_merge_kernel(const float* __restrict__ logits, int T, int E, int k,
+                   int32_t* __restrict__ ids, float* __restrict__ w) {
+  __shared__ unsigned long long lists[2][32][32];
+  pdl_wait();
+  pdl_trigger();
+  const int t = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int e = threadIdx.x;
+  unsigned long long key = e < E ? route_key(__ldg(logits + (size_t)t * E + e), e) : 0ull;
+  key = warp_sort_desc(key, lane);
+  // merge tree: at stride s the warps w = 0 mod 2s take in warp w + s's list
+  int buf = 0;
+  for (int s = 1; s < nw; s <<= 1) {
+    lists[buf][warp][lane] = key;
+    __syncthreads();
+    if ((warp & (2 * s - 1)) == 0 && warp + s < nw)
+      key = bitonic_merge_desc(umax64(key, lists[buf][warp + s][31 - lane]), lane);
+    buf ^= 1;
+  }
+  if (warp == 0) {
+    const float first_v = key_logit(__shfl_sync(0xffffffffu, key, 0));
+    const float ex = (lane < k) ? expf(key_logit(key) - first_v) : 0.0f;
     // sum in ascending j so every lane sees the same value
     float denom = 0.0f;
     for (int j = 0; j < k; ++j) denom += __shfl_sync(0xffffffffu, ex, j);
     if (lane < k) {
-      ids[(size_t)t * k + lane] = si[lane];
+      ids[(size_t)t * k + lane] = key_id(key);
       w[(size_t)t * k + lane] = ex / denom;
     }
   }
@@ -427,21 +379,8 @@ csr_small_kernel(const int32_t* __restrict__ ids_g, int P, int E, int32_t* __res
 
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w,
                               cudaStream_t s) {
-  const dim3 grid(T), block(32);
-  const int pl = (E + 31) / 32;
-  // wider routers: sort per token (the warp version runs k dependent rounds of shuffles)
-  if (E > 64) {
-    if (E <= 128) return launch_pdl(route_sort_kernel<128>, grid, dim3(64), 0, s, logits, T, E, k, ids, w);
-    if (E <= 256) return launch_pdl(route_sort_kernel<256>, grid, dim3(128), 0, s, logits, T, E, k, ids, w);
-    if (E <= 512) return launch_pdl(route_sort_kernel<512>, grid, dim3(256), 0, s, logits, T, E, k, ids, w);
-    return launch_pdl(route_sort_kernel<1024>, grid, dim3(512), 0, s, logits, T, E, k, ids, w);
-  }
-  if (pl <= 1) return launch_pdl(route_topk_kernel<1>, grid, block, 0, s, logits, T, E, k, ids, w);
-  if (pl <= 2) return launch_pdl(route_topk_kernel<2>, grid, block, 0, s, logits, T, E, k, ids, w);
-  if (pl <= 4) return launch_pdl(route_topk_kernel<4>, grid, block, 0, s, logits, T, E, k, ids, w);
-  if (pl <= 8) return launch_pdl(route_topk_kernel<8>, grid, block, 0, s, logits, T, E, k, ids, w);
-  if (pl <= 16) return launch_pdl(route_topk_kernel<16>, grid, block, 0, s, logits, T, E, k, ids, w);
-  return launch_pdl(route_topk_kernel<32>, grid, block, 0, s, logits, T, E, k, ids, w);
+  const int nw = (E + 31) / 32;
+  return launch_pdl(route_merge_kernel, dim3(T), dim3(32 * nw), 0, s, logits, T, E, k, ids, w);
 }
 
 size_t csr_scratch_bytes(int P, int E) {

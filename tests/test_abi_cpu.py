@@ -61,6 +61,11 @@ def test_workspace_layout_host_logic(lib):
     assert moe.workspace_bytes(4, 100, F, E, k) == 0        # H % 256 != 0 unsupported
     assert moe.workspace_bytes(4, 8192, F, E, k) == 0       # H > 4096 unsupported
     assert moe.workspace_bytes(4, H, F, 8, 10) == 0         # k > E
+    # per-path F limits: decode up to 1408, prefill up to 4096
+    assert moe.workspace_bytes(4, H, 1408, E, k, moe.PATH_DECODE) > 0
+    assert moe.workspace_bytes(4, H, 1472, E, k, moe.PATH_DECODE) == 0
+    assert moe.workspace_bytes(4, H, 1472, E, k, moe.PATH_PREFILL) > 0
+    assert moe.workspace_bytes(4, H, 4160, E, k, moe.PATH_PREFILL) == 0
 
 
 def test_path_resolution(lib):
@@ -93,6 +98,10 @@ def test_host_validation_rejects_before_launch(lib):
     # workspace too small
     assert lib.moe_grouped_gate_up_silu_nvfp4(16, 4, 256, 64, 2, ctypes.byref(bank), good, 0,
                                               256, 16, None) == 3
+    # F beyond the decode path's limit
+    wide = _native.Bank(16, 16, 16, 2 * 2048, 256)
+    assert lib.moe_grouped_gate_up_silu_nvfp4(16, 4, 256, 2048, 2, ctypes.byref(wide), good, 1,
+                                              256, 1 << 30, None) == 2
     dbank = _native.Bank(16, 16, 16, 256, 64)
     assert lib.moe_grouped_down_combine_nvfp4(ctypes.byref(dbank), good, 16, 4, 256, 64, 2, 0,
                                               None, 256, 1 << 20, None) == 1

@@ -126,6 +126,15 @@ def test_single_token_single_expert():
     _check_layer(one, run)
 
 
+@pytest.mark.parametrize("F", [1024, 1408])
+def test_wide_ff_decode(F):
+    """ff widths up to the decode path's largest (wider h rows held in registers)."""
+    wl = synth.logits_workload(f"wide_F{F}", 3, 256, F, 8, 2, seed=11)
+    run = run_layer(wl)
+    assert run.err == 0
+    _check_layer(wl, run)
+
+
 def test_csr_many_pairs_with_invalid_ids():
     """The grid-wide CSR (thousands of pairs) skips and flags out-of-range ids, keeps the
     rest in ascending pair order, and writes -1 as their CSR position."""
@@ -190,9 +199,12 @@ def test_many_pairs_on_one_expert():
     _check_layer(many, run, tokens=[0, 13, 39])
 
 
-def test_route_ties_to_lower_id():
-    T, E, k = 64, 512, 10
-    rng = np.random.default_rng(11)
+@pytest.mark.parametrize("T,E,k", [(64, 512, 10), (33, 7, 3), (40, 33, 32), (17, 64, 8),
+                                   (50, 100, 6), (29, 300, 16), (12, 1024, 32), (5, 997, 1)])
+def test_route_ties_to_lower_id(T, E, k):
+    """Every router width (one warp up to 32 warps merged) against the oracle, on logits
+    with many exact ties, signed zeros among them."""
+    rng = np.random.default_rng(11 + E)
     logits = np.round(rng.standard_normal((T, E)) * 2).astype(np.float32)   # many exact ties
     ids = torch.zeros(T, k, dtype=torch.int32, device="cuda")
     w = torch.zeros(T, k, dtype=torch.float32, device="cuda")
