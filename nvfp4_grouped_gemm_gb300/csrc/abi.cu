@@ -81,19 +81,23 @@ bool compute_layout(int T, int H, int F, int E, int k, int path, moe_ws_layout* 
   L->pair_pos = take(P * sizeof(int32_t));
   L->h = take(P * F * sizeof(float));
   L->partial = take(P * H * sizeof(float));
-  if (path == MOE_PATH_DECODE) {
+  if (path == MOE_PATH_DECODE && !decode_sliced((long long)P)) {
     L->xg = take(P * H * 2);
     L->xe = take(P * sizeof(int32_t));
     L->hg = take(P * F * 2);
     L->he = take(P * sizeof(int32_t));
   } else {
-    L->qx_codes = take(P * (H / 2));
-    L->qx_scales = take(P * (H / 16));
-    L->qx_exp = take(P * sizeof(int32_t));
-    L->qh_codes = take(P * (F / 2));
-    L->qh_scales = take(P * qh_scale_pitch(F));
-    L->qh_exp = take(P * sizeof(int32_t));
-    const size_t max_tiles = P / 128 + (size_t)(E < (int)P ? E : (int)P) + 1;
+    // operand rows per pair: the sliced decode form keeps kDecodeSlices slices of each row
+    const bool sl = path == MOE_PATH_DECODE;
+    const size_t R = P * (sl ? kDecodeSlices : 1);
+    L->qx_codes = take(R * (H / 2));
+    L->qx_scales = take(R * (H / 16));
+    L->qx_exp = take(R * sizeof(int32_t));
+    L->qh_codes = take(R * (F / 2));
+    L->qh_scales = take(R * qh_scale_pitch(F));
+    L->qh_exp = take(R * sizeof(int32_t));
+    // tiles: 128 rows, or 32 rows (eight pairs' slices) in the sliced decode form
+    const size_t max_tiles = R / (sl ? 32 : 128) + (size_t)(E < (int)P ? E : (int)P) + 1;
     L->tiles = take(16 + 16 * max_tiles);
   }
   L->total = o;
@@ -132,7 +136,8 @@ int32_t moe_kernel_launches(int32_t T, int32_t H, int32_t F, int32_t E, int32_t 
   const int P = T * k;
   const int csr = csr_scratch_bytes(P, E) ? 3 : 1;   // grid-wide build or one CTA
   if (resolve_path(T, k, path) == MOE_PATH_DECODE)
-    return csr + 2 /* x gather, gate/up */ + 3 /* h prep, down, combine */;
+    return decode_sliced(P) ? csr + 3 /* tiles, x slices, gate/up */ + 3 /* h slices, down, combine */
+                            : csr + 2 /* x gather, gate/up */ + 3 /* h prep, down, combine */;
   return csr + 3 /* tiles, Q(x), gate/up GEMM */ + 3 /* Q(h), down GEMM, combine */;
 }
 
@@ -208,6 +213,9 @@ moe_status moe_grouped_gate_up_silu_nvfp4(const void* x_bf16, int32_t T, int32_t
     if (unsup) return MOE_ERR_UNSUPPORTED;
     return from_cuda(ce);
   }
+  if (decode_sliced((long long)T * k))
+    return from_cuda(launch_sliced_gate_up(static_cast<const uint16_t*>(x_bf16), T, H, F, k,
+                                           *w_gate_up, csr, L, static_cast<char*>(ws), s));
   return from_cuda(launch_decode_gate_up(static_cast<const uint16_t*>(x_bf16), T, H, F, k,
                                          *w_gate_up, csr, L, static_cast<char*>(ws), s));
 }
@@ -237,7 +245,8 @@ moe_status moe_grouped_down_combine_nvfp4(const moe_nvfp4_bank* w_down, moe_csr 
     if (unsup) return MOE_ERR_UNSUPPORTED;
     return from_cuda(ce);
   }
-  ce = launch_decode_down(*w_down, csr, T, H, F, k, L, w, s);
+  ce = decode_sliced((long long)T * k) ? launch_sliced_down(*w_down, csr, T, H, F, k, L, w, s)
+                                       : launch_decode_down(*w_down, csr, T, H, F, k, L, w, s);
   if (ce != cudaSuccess) return MOE_ERR_CUDA;
   return from_cuda(launch_combine(topk_w, T, H, k, L, w, y, s));
 }

@@ -18,6 +18,15 @@ constexpr int kPrefillMinPairs = 2048;
 // h rows in shared memory; the prefill Q(h) kernel holds a row of h in registers.
 constexpr int kDecodeMaxF = 1408;
 constexpr int kPrefillMaxF = 4096;
+// Slices per activation row in the decode form of the tensor-core path.
+constexpr int kDecodeSlices = 4;
+// The decode path runs the sliced tensor-core GEMMs from this many pairs on (below it, the
+// TMA-fed mma.sync kernels of decode.cu, whose fixed costs are lower).
+#ifndef MOE_SLICED_MIN_PAIRS
+#define MOE_SLICED_MIN_PAIRS 512
+#endif
+constexpr int kSlicedMinPairs = MOE_SLICED_MIN_PAIRS;
+inline bool decode_sliced(long long P) { return P >= kSlicedMinPairs; }
 constexpr size_t kAlign = 256;
 
 inline size_t align_up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a; }
@@ -46,6 +55,14 @@ cudaError_t launch_decode_down(const moe_nvfp4_bank& b, moe_csr csr, int T, int 
                                const moe_ws_layout& L, char* ws, cudaStream_t s);
 cudaError_t launch_combine(const float* w, int T, int H, int k, const moe_ws_layout& L, char* ws,
                            float* y, cudaStream_t s);
+// Tile list over the CSR (prefill.cu): rpp operand rows per pair, tiles of tile_rows rows.
+cudaError_t launch_tiles(const int32_t* offsets, int E, int rpp, int tile_rows, int32_t* tiles,
+                         cudaStream_t s);
+cudaError_t launch_sliced_gate_up(const uint16_t* x_bf16, int T, int H, int F, int k,
+                                  const moe_nvfp4_bank& b, moe_csr csr, const moe_ws_layout& L,
+                                  char* ws, cudaStream_t s);
+cudaError_t launch_sliced_down(const moe_nvfp4_bank& b, moe_csr csr, int T, int H, int F, int k,
+                               const moe_ws_layout& L, char* ws, cudaStream_t s);
 cudaError_t launch_prefill_gate_up(const uint16_t* x_bf16, int T, int H, int F, int k,
                                    const moe_nvfp4_bank& b, moe_csr csr, const moe_ws_layout& L,
                                    char* ws, cudaStream_t s, bool* unsupported);
@@ -59,8 +76,19 @@ cudaError_t launch_quant_h(const float* h, int P, int F, int sf_pitch, const int
                            int E, uint8_t* qc, uint8_t* qs, int32_t* qe, cudaStream_t s);
 // Exponent c_F with F * 2688^2 * 2^-c_F < 2^15: the fixed shift of the f16 partials.
 int down_shift_for(int F);
+cudaError_t launch_slice_x(const uint16_t* x_bf16, int T, int H, int k, const int32_t* pair_pos,
+                           uint8_t* qc, uint8_t* qs, int32_t* qe, cudaStream_t s);
+cudaError_t launch_slice_h(const float* h, int P, int F, int sf_pitch, const int32_t* offsets,
+                           int E, uint8_t* qc, uint8_t* qs, int32_t* qe, cudaStream_t s);
 cudaError_t launch_prefill_combine(const float* w, int T, int H, int F, int k, int c0, int HS,
                                    const moe_ws_layout& L, char* ws, float* y, cudaStream_t s);
+// Programmatic dependent launch, device side: wait for the predecessor grid (complete,
+// its memory visible), or allow the successor grid to start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Launch with programmatic dependent launch allowed: the kernel may start while its
 // predecessor in the stream finishes, and must execute griddepcontrol.wait before it
 // reads anything that predecessor writes.

@@ -19,6 +19,7 @@
 
 #include "moe_internal.cuh"
 #include "tma_sync.cuh"
+#include "tcgen05.cuh"
 
 namespace moe {
 
@@ -30,15 +31,20 @@ namespace {
 constexpr int kTileRows = 128;
 
 // tiles region: int n_mtiles, pad to 16 B, then int4 {row0, rows, expert, 0} per M-tile.
+// A pair owns `rpp` consecutive operand rows (1, or the activation slices of the decode
+// form); an expert's rows are cut into tiles of `tile_rows`.
 __global__ void __launch_bounds__(1024) tiles_kernel(const int32_t* __restrict__ offsets, int E,
+                                                     int rpp, int tile_rows,
                                                      int32_t* __restrict__ tiles) {
   __shared__ int scratch[32];
+  pdl_wait();                                       // the CSR offsets are complete
+  pdl_trigger();
   const int e = threadIdx.x;
   const int lane = e & 31, warp = e >> 5;
   int cnt = 0, off = 0;
   if (e < E) {
-    off = offsets[e];
-    cnt = (offsets[e + 1] - off + kTileRows - 1) / kTileRows;
+    off = offsets[e] * rpp;
+    cnt = (offsets[e + 1] * rpp - off + tile_rows - 1) / tile_rows;
   }
   int x = cnt;
 #pragma unroll
@@ -61,10 +67,10 @@ __global__ void __launch_bounds__(1024) tiles_kernel(const int32_t* __restrict__
   const int base = (warp ? scratch[warp - 1] : 0) + x - cnt;
   int4* list = reinterpret_cast<int4*>(tiles + 4);
   if (e < E) {
-    const int m = offsets[e + 1] - off;
+    const int m = offsets[e + 1] * rpp - off;
     for (int i = 0; i < cnt; ++i) {
-      const int r = m - i * kTileRows;
-      list[base + i] = make_int4(off + i * kTileRows, r < kTileRows ? r : kTileRows, e, 0);
+      const int r = m - i * tile_rows;
+      list[base + i] = make_int4(off + i * tile_rows, r < tile_rows ? r : tile_rows, e, 0);
     }
   }
   if (threadIdx.x == 0) tiles[0] = scratch[31];
@@ -80,77 +86,6 @@ __device__ __forceinline__ void cp_async4(void* dst, const void* src, bool valid
 __device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
-}
-
-// Shared-memory matrix descriptor (tcgen05): start >> 4, LBO >> 4, SBO >> 4, version 1,
-// swizzle mode in bits 61..63 (0 none, 2 = 128-byte).
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo,
-                                              uint32_t swz) {
-  uint64_t d = 0;
-  d |= (uint64_t)((addr & 0x3FFFF) >> 4);
-  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
-  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)(swz & 7) << 61;
-  return d;
-}
-
-// Instruction descriptor, kind::mxf4nvf4: A/B E2M1 (1), K-major, N>>3 at 17, UE4M3 scales
-// (bit 23 = 0), M>>4 at 24, scale-factor ids 0, dense K = 64.
-__host__ __device__ constexpr uint32_t mxf4_idesc(int M, int N) {
-  return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
-                                       uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X "
-      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}"
-      ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
-      : "memory");
-}
-// Two k-steps' scale-factor atoms (32 rows x 16 B each, the second one LBO bytes after the
-// first) into 8 TMEM columns: lanes 0..31 receive the atoms (lanes 32..127 receive bytes
-// the MMA does not read).
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-      ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-// 16 consecutive 32-bit TMEM columns of this warp's 32 lanes (one value per lane each).
-__device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&v)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
-      "%13,%14,%15,%16};"
-      ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
-        "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]),
-        "r"(v[14]), "r"(v[15])
-      : "memory");
-}
-// Two groups of 32 consecutive 32-bit TMEM columns of this warp's lanes, then the wait:
-// one asm statement, so no use of the results can be scheduled before the wait.
-__device__ __forceinline__ void tc_ld32x2(uint32_t taddr0, uint32_t taddr1, float (&a)[32],
-                                          float (&b)[32]) {
-  uint32_t r[64];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]),"=r"(r[1]),"=r"(r[2]),"=r"(r[3]),"=r"(r[4]),"=r"(r[5]),"=r"(r[6]),"=r"(r[7]),"=r"(r[8]),"=r"(r[9]),"=r"(r[10]),"=r"(r[11]),"=r"(r[12]),"=r"(r[13]),"=r"(r[14]),"=r"(r[15]),"=r"(r[16]),"=r"(r[17]),"=r"(r[18]),"=r"(r[19]),"=r"(r[20]),"=r"(r[21]),"=r"(r[22]),"=r"(r[23]),"=r"(r[24]),"=r"(r[25]),"=r"(r[26]),"=r"(r[27]),"=r"(r[28]),"=r"(r[29]),"=r"(r[30]),"=r"(r[31]),"=r"(r[32]),"=r"(r[33]),"=r"(r[34]),"=r"(r[35]),"=r"(r[36]),"=r"(r[37]),"=r"(r[38]),"=r"(r[39]),"=r"(r[40]),"=r"(r[41]),"=r"(r[42]),"=r"(r[43]),"=r"(r[44]),"=r"(r[45]),"=r"(r[46]),"=r"(r[47]),"=r"(r[48]),"=r"(r[49]),"=r"(r[50]),"=r"(r[51]),"=r"(r[52]),"=r"(r[53]),"=r"(r[54]),"=r"(r[55]),"=r"(r[56]),"=r"(r[57]),"=r"(r[58]),"=r"(r[59]),"=r"(r[60]),"=r"(r[61]),"=r"(r[62]),"=r"(r[63])
-      : "r"(taddr0), "r"(taddr1)
-      : "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    a[i] = __uint_as_float(r[i]);
-    b[i] = __uint_as_float(r[32 + i]);
-  }
 }
 
 // ---------------------------------------------------------------------------
@@ -206,18 +141,6 @@ struct Cfg {
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
-
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
-}
 
 template <int BN, bool GATE_UP>
 __global__ void __launch_bounds__(448, 1)
@@ -528,7 +451,7 @@ cudaError_t launch_prefill_gate_up(const uint16_t* x_bf16, int T, int H, int F, 
   if (H % 256 != 0 || F % 64 != 0) { *unsupported = true; return cudaSuccess; }
   const int P = T * k;
   int32_t* tiles = reinterpret_cast<int32_t*>(ws + L.tiles);
-  tiles_kernel<<<1, 1024, 0, s>>>(csr.expert_offsets, b.E, tiles);
+  tiles_kernel<<<1, 1024, 0, s>>>(csr.expert_offsets, b.E, 1, kTileRows, tiles);
   cudaError_t st = cudaGetLastError();
   if (st != cudaSuccess) return st;
   uint8_t* qc = reinterpret_cast<uint8_t*>(ws + L.qx_codes);
@@ -588,6 +511,11 @@ cudaError_t launch_prefill_down(const moe_nvfp4_bank& b, moe_csr csr, const floa
              reinterpret_cast<uint32_t*>(ws + L.error_word), P, F, H, H / BN, H, F, shift, g, 0};
   if ((st = run_gemm<BN, false>(ma, mb, msa, msb, a, max_tiles, s)) != cudaSuccess) return st;
   return launch_prefill_combine(w, T, H, F, k, 0, H, L, ws, y, s);
+}
+
+cudaError_t launch_tiles(const int32_t* offsets, int E, int rpp, int tile_rows, int32_t* tiles,
+                         cudaStream_t s) {
+  return launch_pdl(tiles_kernel, dim3(1), dim3(1024), 0, s, offsets, E, rpp, tile_rows, tiles);
 }
 
 }  // namespace moe

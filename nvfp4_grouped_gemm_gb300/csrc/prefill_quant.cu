@@ -223,6 +223,160 @@ __global__ void __launch_bounds__(256) quant_h_kernel(const float* __restrict__ 
   }
 }
 
+// ---------------------------------------------------------------------------
+// Activation slices for the decode form of the tensor-core path: a row v is written as
+// NS rows q_0..q_{NS-1}, each the quantiser Q of what the earlier ones left over
+// (q_i = Q(v - q_0 - ... - q_{i-1}), exact f32 residuals), so that sum_i q_i approximates v
+// to about 6^-NS of each block's largest magnitude.  The GEMM multiplies every slice and
+// sums the NS accumulator rows of a pair in its epilogue.  One thread per 16-value block.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float e2m1_mag(uint32_t m) {      // magnitude code 0..7
+  return m < 2 ? 0.5f * (float)m : __uint_as_float(((m >> 1) + 126u) << 23 | (m & 1u) << 22);
+}
+
+// Row max of |v| over the CTA (one value per thread in `x`); `red` holds one slot per warp.
+__device__ __forceinline__ float cta_max(float x, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = x;
+  __syncthreads();
+  float m = 0.0f;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) m = fmaxf(m, red[w]);
+  return m;
+}
+
+// One slice of a quarter block: the 4 residual values r of this thread (elements 4q..4q+3
+// of a 16-value block whose other quarters sit in the neighbouring lanes q^1, q^2).  Row
+// exponent from row_amax, block scale from the block's max key (shared by the 4 lanes), E2M1
+// codes as in quant_block; r becomes the remainder.  Returns the 4 codes as 16 bits.
+__device__ __forceinline__ uint32_t slice_quarter(float (&r)[4], float row_amax, int& s_out,
+                                                  int& sbc_out) {
+  const int s = row_exp_of(row_amax);
+  const bool fast = s >= -127 && s <= 149;
+  const float m = fast ? pow2f(-s) : 0.0f;
+  float key[4];
+  float bmax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    key[i] = scale_down(fabsf(r[i]), s, fast, m);
+    bmax = fmaxf(bmax, key[i]);
+  }
+  bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 1));
+  bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 2));
+  const int sbc = ue4m3_code_of(bmax);
+  uint32_t codes = 0;
+  if (sbc != 0) {
+    const float sbv = ue4m3_val(sbc);
+    const float t0 = 0.25f * sbv, t1 = 0.75f * sbv, t2 = 1.25f * sbv, t3 = 1.75f * sbv;
+    const float t4 = 2.5f * sbv, t5 = 3.5f * sbv, t6 = 5.0f * sbv;
+    const bool up_fast = s >= -126 && s <= 127;
+    const float p = up_fast ? pow2f(s) : 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float v = key[i];
+      // the same three-step threshold search as quant_block (ties to the even code)
+      const bool b2 = v >= t3;
+      const bool b1 = v >= (b2 ? t5 : t1);
+      const bool b0 = v > (b2 ? (b1 ? t6 : t4) : (b1 ? t2 : t0));
+      const uint32_t mag = (b2 ? 4u : 0u) | (b1 ? 2u : 0u) | (b0 ? 1u : 0u);
+      const bool neg = r[i] < 0.0f;
+      codes |= (mag | (neg ? 8u : 0u)) << (4 * i);
+      const float qv = e2m1_mag(mag) * sbv;               // exact: <= 6 significant bits
+      const float qs = up_fast ? qv * p : ldexpf(qv, s);
+      r[i] = neg ? r[i] + qs : r[i] - qs;
+    }
+  }
+  s_out = s;
+  sbc_out = sbc;
+  return codes;
+}
+
+// x: one CTA per token, four threads per 16-value block (thread 4b + q holds elements
+// 16b + 4q .. +3).  The slices depend only on x, so they are formed before the wait; after it
+// they are written to the NS rows of each of the token's pairs (rows pair_pos * NS + i).
+template <int NS>
+__global__ void __launch_bounds__(1024) slice_x_kernel(const uint16_t* __restrict__ x, int H, int k,
+                                                       const int32_t* __restrict__ pair_pos,
+                                                       uint8_t* __restrict__ qc,
+                                                       uint8_t* __restrict__ qs,
+                                                       int32_t* __restrict__ qe) {
+  __shared__ float red[NS][32];
+  __shared__ int s_pos[kMaxK];
+  const int t = blockIdx.x, tid = threadIdx.x;
+  const int b = tid >> 2, q = tid & 3;
+  const int nblk = H / 16;
+  const bool has = b < nblk;
+  float r[4];
+  {
+    const uint2 w = has ? __ldg(reinterpret_cast<const uint2*>(x + (size_t)t * H + 16 * b + 4 * q))
+                        : make_uint2(0, 0);
+    r[0] = __uint_as_float(w.x << 16);
+    r[1] = __uint_as_float(w.x & 0xffff0000u);
+    r[2] = __uint_as_float(w.y << 16);
+    r[3] = __uint_as_float(w.y & 0xffff0000u);
+  }
+  uint32_t codes[NS];
+  int sbc[NS], sx[NS];
+#pragma unroll
+  for (int i = 0; i < NS; ++i) {
+    const float a = fmaxf(fmaxf(fabsf(r[0]), fabsf(r[1])), fmaxf(fabsf(r[2]), fabsf(r[3])));
+    codes[i] = slice_quarter(r, cta_max(a, red[i]), sx[i], sbc[i]);
+  }
+  pdl_wait();                                       // pair_pos is complete
+  pdl_trigger();
+  // the token's k positions, read once (all loads in flight together)
+  if (tid < k) s_pos[tid] = pair_pos[(size_t)t * k + tid];
+  __syncthreads();
+  if (!has) return;
+  for (int j = 0; j < k; ++j) {
+    const int pos = s_pos[j];
+    if (pos < 0) continue;
+#pragma unroll
+    for (int i = 0; i < NS; ++i) {
+      const size_t row = (size_t)pos * NS + i;
+      *reinterpret_cast<uint16_t*>(qc + row * (H / 2) + 8 * b + 2 * q) = (uint16_t)codes[i];
+      if (q == 0) qs[row * nblk + b] = (uint8_t)sbc[i];
+      if (tid == 0) qe[row] = sx[i];
+    }
+  }
+}
+
+// h: one CTA per CSR row (f32 h, rows in CSR order), rows r * NS + i, four threads per block.
+template <int NS>
+__global__ void __launch_bounds__(1024) slice_h_kernel(const float* __restrict__ h, int F,
+                                                       int sf_pitch,
+                                                       const int32_t* __restrict__ offsets, int E,
+                                                       uint8_t* __restrict__ qc,
+                                                       uint8_t* __restrict__ qs,
+                                                       int32_t* __restrict__ qe) {
+  __shared__ float red[NS][32];
+  pdl_wait();
+  pdl_trigger();
+  const int row0 = blockIdx.x, tid = threadIdx.x;
+  if (row0 >= offsets[E]) return;                  // uniform over the CTA
+  const int b = tid >> 2, q = tid & 3;
+  const int nblk = F / 16;
+  const bool has = b < nblk;
+  float r[4];
+  {
+    const float4 v = has ? __ldcs(reinterpret_cast<const float4*>(h + (size_t)row0 * F + 16 * b + 4 * q))
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+    r[0] = v.x; r[1] = v.y; r[2] = v.z; r[3] = v.w;
+  }
+#pragma unroll
+  for (int i = 0; i < NS; ++i) {
+    const float a = fmaxf(fmaxf(fabsf(r[0]), fabsf(r[1])), fmaxf(fabsf(r[2]), fabsf(r[3])));
+    int s, sbc;
+    const uint32_t c = slice_quarter(r, cta_max(a, red[i]), s, sbc);
+    if (has) {
+      const size_t row = (size_t)row0 * NS + i;
+      *reinterpret_cast<uint16_t*>(qc + row * (F / 2) + 8 * b + 2 * q) = (uint16_t)c;
+      if (q == 0) qs[row * sf_pitch + b] = (uint8_t)sbc;
+      if (tid == 0) qe[row] = s;
+    }
+  }
+}
+
 // combine for the prefill path: y[t, :] = sum_j w[t, j] * f32(z16[pos_j, :]) * 2^(e_j + cF)
 // The token's k positions and scaled weights are read once into shared memory; the
 // partial rows are then loaded four pairs at a time and summed in ascending j.
@@ -277,6 +431,22 @@ cudaError_t launch_quant_x(const uint16_t* x_bf16, int T, int H, int k, const in
                            uint8_t* qc, uint8_t* qs, int32_t* qe, cudaStream_t s) {
   quant_x_kernel<<<(T + 7) / 8, 256, 0, s>>>(x_bf16, T, H, k, pair_pos, qc, qs, qe);
   return cudaGetLastError();
+}
+
+cudaError_t launch_slice_x(const uint16_t* x_bf16, int T, int H, int k, const int32_t* pair_pos,
+                           uint8_t* qc, uint8_t* qs, int32_t* qe, cudaStream_t s) {
+  const int threads = (H / 4 + 31) / 32 * 32;      // four per 16-value block
+  if (threads > 1024) return cudaErrorInvalidValue;
+  return launch_pdl(slice_x_kernel<kDecodeSlices>, dim3(T), dim3(threads), 0, s, x_bf16, H, k,
+                    pair_pos, qc, qs, qe);
+}
+
+cudaError_t launch_slice_h(const float* h, int P, int F, int sf_pitch, const int32_t* offsets,
+                           int E, uint8_t* qc, uint8_t* qs, int32_t* qe, cudaStream_t s) {
+  const int threads = (F / 4 + 31) / 32 * 32;
+  if (threads > 1024) return cudaErrorInvalidValue;
+  return launch_pdl(slice_h_kernel<kDecodeSlices>, dim3(P), dim3(threads), 0, s, h, F, sf_pitch,
+                    offsets, E, qc, qs, qe);
 }
 
 cudaError_t launch_quant_h(const float* h, int P, int F, int sf_pitch, const int32_t* offsets,

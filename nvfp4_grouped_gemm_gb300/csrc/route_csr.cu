@@ -27,10 +27,6 @@ namespace moe {
 
 namespace {
 
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void pdl_trigger() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
 
 // Routing key: unsigned order = (logit descending, id ascending); 0 is below every key.
 __device__ __forceinline__ unsigned long long route_key(float v, int id) {

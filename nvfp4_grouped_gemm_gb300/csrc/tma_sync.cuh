@@ -124,6 +124,22 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t p
   return r == CUDA_SUCCESS;
 }
 
+// 3-D u8 tensor map (dims[0] innermost, strides in bytes of dims 1..2) with box `box`.
+bool make_map3(CUtensorMap* map, const void* base, const uint64_t (&dims)[3],
+               const uint64_t (&strides)[2], const uint32_t (&box)[3], bool swizzle) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+  cuuint64_t st[2] = {strides[0], strides[1]};
+  cuuint32_t bx[3] = {box[0], box[1], box[2]};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), d, st, bx, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 4-D u8 tensor map (dims[0] innermost, strides in bytes of dims 1..3) with box `box`.
 bool make_map4(CUtensorMap* map, const void* base, const uint64_t (&dims)[4],
                const uint64_t (&strides)[3], const uint32_t (&box)[4], bool swizzle) {
@@ -140,6 +156,15 @@ bool make_map4(CUtensorMap* map, const void* base, const uint64_t (&dims)[4],
   return r == CUDA_SUCCESS;
 }
 
+// 3-D tiled load with an L2 cache policy.
+__device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* map, int x0, int x1,
+                                                 int x2, uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;"
+      ::"r"(smem_u32(dst)), "l"(map), "r"(x0), "r"(x1), "r"(x2), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
 __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int x0, int x1,
                                             int x2, int x3, uint64_t* bar) {
   asm volatile(

@@ -117,6 +117,20 @@ def test_split_batch_bit_identical():
         assert np.array_equal(y, full[lo:hi])
 
 
+def test_split_batch_bit_identical_sliced():
+    """The same split check on the sliced tensor-core form (both halves at >= 512 pairs):
+    a pair's slices depend only on its token and each output column is reduced on its own,
+    so how pairs share tiles does not change a bit."""
+    wl = synth.verify(128)
+    gu, dn = device_banks(wl)
+    full = run_layer(wl, banks=(gu, dn), fetch=False).y
+    for lo, hi in ((0, 64), (64, 128)):
+        part = synth.Workload(wl.name, hi - lo, wl.H, wl.F, wl.E, wl.k, wl.x_bits[lo:hi],
+                              wl.gate_up, wl.down, logits=wl.logits[lo:hi])
+        y = run_layer(part, banks=(gu, dn), fetch=False).y
+        assert np.array_equal(y, full[lo:hi])
+
+
 def test_single_token_single_expert():
     """k = 1, T = 1: the smallest layer."""
     wl = synth.tiny(seed=3)
@@ -197,6 +211,39 @@ def test_many_pairs_on_one_expert():
                           ids=ids, weights=w)
     run = run_layer(many)
     _check_layer(many, run, tokens=[0, 13, 39])
+
+
+@pytest.mark.parametrize("T,H,F,E,k", [(64, 256, 64, 16, 8),      # one k-step for down
+                                       (80, 256, 128, 7, 7),      # 80 pairs per expert: 10 tiles
+                                       (52, 512, 1408, 32, 10)])  # widest decode F
+def test_sliced_path_shapes(T, H, F, E, k):
+    """From 512 pairs the decode path runs the sliced tensor-core GEMMs: ragged tiles, an
+    expert spread over many 8-pair tiles, a down projection of one 64-wide k-step, and the
+    widest F (its weight-scale rows staged whole)."""
+    assert T * k >= 512
+    wl = synth.logits_workload(f"sliced_{T}_{H}_{F}", T, H, F, E, k, seed=21)
+    run = run_layer(wl)
+    assert run.err == 0
+    _check_layer(wl, run)
+
+
+def test_sliced_path_invalid_ids_and_duplicates():
+    """Invalid ids are skipped and flagged; a token may name one expert twice (sliced form)."""
+    T, k, E = 64, 8, 40
+    wl = synth.logits_workload("sliced_bad", T, 256, 128, E, k, seed=5)
+    rng = np.random.default_rng(5)
+    ids = rng.integers(0, E, size=(T, k)).astype(np.int32)
+    ids[3, 2] = E + 7
+    ids[10, 0] = -1
+    ids[20, 5] = ids[20, 6]
+    w = rng.uniform(0.05, 1.0, size=(T, k)).astype(np.float32)
+    bad = synth.Workload("sliced_bad", T, wl.H, wl.F, E, k, wl.x_bits, wl.gate_up, wl.down,
+                         ids=ids, weights=w)
+    run = run_layer(bad)
+    assert run.err & moe.DEVERR_EXPERT_ID
+    res = oracle.ffn(bad.x_bits, ids, w.astype(np.float64), bad.gate_up, bad.down)
+    _check_csr(run, ids, E)
+    assert_within(run.y, res.y, oracle.tolerance(res.tsum), "y")
 
 
 @pytest.mark.parametrize("T,E,k", [(64, 512, 10), (33, 7, 3), (40, 33, 32), (17, 64, 8),
