@@ -203,3 +203,39 @@ def test_expert_bytes_match_page_traffic(golden_dir):
 
 def test_useful_flops_prefill():
     assert oracle.useful_flops(32768, 4096, 640) == 515_396_075_520
+
+
+def test_four_residual_slices_stay_far_inside_the_decode_tolerance():
+    """The sliced decode form replaces each activation row v by q_0 + q_1 + q_2 + q_3, where
+    q_i = Q(v - q_0 - ... - q_{i-1}) with the pages' NVFP4 quantiser Q.  Modelled here with
+    the oracle's Q and f64 arithmetic on a small decode layer: the y error of slicing both x
+    and h stays below 5% of the per-element tolerance (each extra slice gains about 6x), while
+    one slice alone (plain W4A4) does not fit."""
+    wl = synth.logits_workload("slices", 4, 512, 128, 32, 4, seed=2)
+    ids, w = oracle.route_topk(wl.logits, wl.k)
+    ref = oracle.ffn(wl.x_bits, ids, w, wl.gate_up, wl.down)
+    tol = oracle.tolerance(ref.tsum)
+    x = nvfp4.bf16_to_f64(wl.x_bits)
+    Wgu = nvfp4.dequant(wl.gate_up.codes, wl.gate_up.scales)
+    Wd = nvfp4.dequant(wl.down.codes, wl.down.scales)
+
+    def sliced(v, n):
+        acc = np.zeros_like(v)
+        for _ in range(n):
+            c, s, e = nvfp4.quantize(v - acc)
+            acc = acc + nvfp4.dequant_q(c, s, e)
+        return acc
+
+    def layer(n):
+        xa = sliced(x, n)
+        y = np.zeros((wl.T, wl.H))
+        for t in range(wl.T):
+            for j in range(wl.k):
+                e = ids[t, j]
+                gu = Wgu[e] @ xa[t]
+                h = gu[:wl.F] / (1.0 + np.exp(-gu[:wl.F])) * gu[wl.F:]
+                y[t] += w[t, j] * (Wd[e] @ sliced(h[None, :], n)[0])
+        return np.abs(y - ref.y) / tol
+
+    assert layer(4).max() < 0.05
+    assert layer(1).max() > 1.0
