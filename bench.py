@@ -463,8 +463,12 @@ def run_ours(args):
         gu_bytes = [uniq[b] * gu_bytes_per_expert for (b, _) in brk]
         ach = sum(gu_bytes) / (sum(gu_ms) * 1e-3) / 1e9
         alg = sum(gu_bytes) / len(gu_bytes)
-        ratio = recorded_traffic(args.workload, "gate_up_tma_kernel")
-        roof = {"bound": "hbm", "kernel": "decode gate_up+SiLU (moe_grouped_gate_up_silu_nvfp4)",
+        # from 512 pairs the decode call runs the sliced tensor-core form
+        sliced = wl.P >= 512
+        ratio = (recorded_traffic([args.workload, "verify_T128"], "sliced_gemm_kernel<1>") if sliced
+                 else recorded_traffic([args.workload, "decode_T8"], "gate_up_tma_kernel"))
+        roof = {"bound": "hbm", "kernel": "decode gate_up+SiLU (moe_grouped_gate_up_silu_nvfp4; " +
+                ("x slices + tcgen05 sliced GEMM)" if sliced else "x staging + TMA-fed mma.sync kernel)"),
                 "achieved": ach, "peak": pk, "unit": "GB/s", "frac": ach / pk,
                 "traffic": None if ratio is None else ratio * alg, "peak_source": pk_src,
                 "algorithmic_bytes_per_launch": alg}
