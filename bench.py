@@ -141,7 +141,10 @@ class ClockSampler:
 # CPU baseline: the oracle as it stands, on a bounded sample, in a fresh process
 # ---------------------------------------------------------------------------
 
-def cpu_baseline(workload: str, tokens: int, seed: int = 0, threads: int = 1):
+def cpu_baseline(workload: str, tokens: int, seed: int = 0, threads: int = 1,
+                 budget_s: float = 10.0):
+    """Time the oracle on windows of `tokens` tokens of the workload, taken in turn (and
+    repeated) until about `budget_s` seconds of CPU work have been measured."""
     env = dict(os.environ)
     for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[v] = str(threads)
@@ -149,19 +152,25 @@ def cpu_baseline(workload: str, tokens: int, seed: int = 0, threads: int = 1):
         "import json,sys,time; sys.path.insert(0, %r)\n"
         "import numpy as np, synth, oracle\n"
         "wl = synth.by_name(%r, %d)\n"
-        "toks = np.arange(min(%d, wl.T))\n"
-        "t0 = time.perf_counter()\n"
-        "if wl.logits is not None:\n"
-        "    ids, w = oracle.route_topk(wl.logits[toks], wl.k)\n"
-        "else:\n"
-        "    ids, w = wl.ids[toks], wl.weights[toks].astype(np.float64)\n"
-        "sub = synth.Workload(wl.name, len(toks), wl.H, wl.F, wl.E, wl.k, wl.x_bits[toks], wl.gate_up, wl.down)\n"
+        "n = min(%d, wl.T); budget = %r\n"
         "mode = 'prefill' if wl.name.startswith('prefill') else 'decode'\n"
-        "res = oracle.ffn(sub.x_bits, ids, w, sub.gate_up, sub.down, mode=mode)\n"
-        "dt = time.perf_counter() - t0\n"
-        "U = len(np.unique(ids))\n"
-        "print(json.dumps({'seconds': dt, 'unique': int(U), 'pairs': int(ids.size), 'tokens': int(len(toks))}))\n"
-    ) % (ROOT, workload, seed, tokens)
+        "tot = {'seconds': 0.0, 'unique': 0, 'pairs': 0, 'tokens': 0, 'windows': 0}\n"
+        "start = 0\n"
+        "while tot['seconds'] < budget:\n"
+        "    toks = (start + np.arange(n)) %% wl.T\n"
+        "    start = (start + n) %% wl.T\n"
+        "    t0 = time.perf_counter()\n"
+        "    if wl.logits is not None:\n"
+        "        ids, w = oracle.route_topk(wl.logits[toks], wl.k)\n"
+        "    else:\n"
+        "        ids, w = wl.ids[toks], wl.weights[toks].astype(np.float64)\n"
+        "    sub = synth.Workload(wl.name, len(toks), wl.H, wl.F, wl.E, wl.k, wl.x_bits[toks], wl.gate_up, wl.down)\n"
+        "    oracle.ffn(sub.x_bits, ids, w, sub.gate_up, sub.down, mode=mode)\n"
+        "    tot['seconds'] += time.perf_counter() - t0\n"
+        "    tot['unique'] += int(len(np.unique(ids))); tot['pairs'] += int(ids.size)\n"
+        "    tot['tokens'] += int(len(toks)); tot['windows'] += 1\n"
+        "print(json.dumps(tot))\n"
+    ) % (ROOT, workload, seed, tokens, budget_s)
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
                        timeout=600)
     if r.returncode != 0:
@@ -530,9 +539,10 @@ def run_ours(args):
         if "error" not in info:
             v, u = cpu_value(args.workload, info, wl.H, wl.F)
             cpu = {"value": v, "unit": u, "cores": 1, "kind": "oracle",
-                   "sample": f"{info['tokens']} token(s), {info['pairs']} pairs, "
-                             f"{info['unique']} experts of {workload_desc(wl)}; float64 numpy oracle, "
-                             f"{info['seconds']:.2f} s"}
+                   "sample": f"{info['windows']} windows of {args.cpu_sample_tokens} token(s) "
+                             f"({info['tokens']} tokens, {info['pairs']} pairs, {info['unique']} "
+                             f"expert streams in total) of {workload_desc(wl)}; float64 numpy "
+                             f"oracle, 1 thread, {info['seconds']:.1f} s"}
         else:
             cpu = {"error": info["error"][-200:]}
 
