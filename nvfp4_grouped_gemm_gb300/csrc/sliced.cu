@@ -40,14 +40,15 @@ namespace {
 
 constexpr int kSliceTile = 32;                     // B rows per tile: 8 pairs x 4 slices
 
-// A stage carries 256 bytes of K per row (512 elements, eight k-steps of 64) as two
-// 128-byte-wide sub-tiles, so the MMA thread's per-stage costs (barrier wait, commit) are
-// paid once per eight MMAs.
+// A stage carries KSUB x 128 bytes of K per row as 128-byte-wide sub-tiles, so the MMA
+// thread's per-stage costs (barrier wait, commit) are paid once per 4*KSUB MMAs: two
+// sub-tiles for gate/up (K = H), three for down, whose F/2-byte rows (320 at F = 640) then
+// fit one stage per work.
 template <bool GATE_UP>
 struct SCfg {
   static constexpr int NB = kSliceTile;           // MMA N
   static constexpr int KB = 128;                  // bytes of K per sub-tile (256 elements)
-  static constexpr int KSUB = 2;                  // sub-tiles per stage
+  static constexpr int KSUB = GATE_UP ? 2 : 3;    // sub-tiles per stage
   static constexpr int KSTEPS = 4 * KSUB;         // k-steps of 64 per stage
   static constexpr int A_SUB = 128 * KB;          // weight rows
   static constexpr int B_SUB = NB * KB;           // slice rows
@@ -57,9 +58,9 @@ struct SCfg {
   // whole F/16-byte scale rows of the 128 rows (g consecutive rows form one tensor-map row
   // whose pitch is a multiple of 16), 128 * F/16 <= 11264 bytes for F <= 1408
   static constexpr int SA_STG = GATE_UP ? 128 * 16 * KSUB : 11264;
-  static constexpr int SB_STG = NB * 16 * KSUB;   // slice-scale staging [NB][32 B]
+  static constexpr int SB_STG = NB * 16 * KSUB;   // slice-scale staging [NB][16*KSUB B]
   static constexpr int STAGE_BYTES = (A_BYTES + B_BYTES + SA_STG + SB_STG + 1023) / 1024 * 1024;
-  static constexpr int STAGES = GATE_UP ? 5 : 4;
+  static constexpr int STAGES = GATE_UP ? 5 : 3;
   static constexpr int ACC_COLS = 2 * NB;          // two accumulator buffers
   static constexpr int SF_COLS = 8 * KSTEPS;       // per stage: 4 columns per k-step for A and for B
   static constexpr int TMEM_COLS = 512;
@@ -82,6 +83,7 @@ struct SlicedArgs {
   int out_cols;                // F or H
   int F;                       // gate/up: row offset of the up rows; down: unused
   int a_sf_group;              // down: g weight-scale rows per tensor-map row
+  int sb_w;                    // bytes per slice-scale staging row: min(16*KSUB, scale pitch)
 };
 
 __device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&a)[32]) {
@@ -159,7 +161,7 @@ sliced_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
     if (lane == 0) {
       constexpr uint32_t tx_codes = C::A_BYTES + C::B_BYTES;
       const int g = GATE_UP ? 1 : args.a_sf_group;
-      const uint32_t tx_stg = (uint32_t)(GATE_UP ? C::SA_STG : 128 * sfrow) + C::SB_STG;
+      const uint32_t tx_stg = (uint32_t)(GATE_UP ? C::SA_STG : 128 * sfrow) + (uint32_t)(C::NB * args.sb_w);
       const uint64_t wpol = l2_evict_first_policy();
       int it = 0;
       // work descriptors are fetched two works ahead
@@ -288,7 +290,9 @@ sliced_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
       }
 #pragma unroll
       for (int q = 0; q < KW / 4; ++q) {
-        const uint4 b4 = lds128(sb + OFF_SB + 4 * KW * lane + 16 * q);
+        // staging rows are sb_w bytes; words past them are past the row's K (nvalid)
+        const uint4 b4 = 16 * q < args.sb_w ? lds128(sb + OFF_SB + args.sb_w * lane + 16 * q)
+                                            : make_uint4(0, 0, 0, 0);
         const uint32_t b[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
@@ -394,12 +398,13 @@ cudaError_t launch_sliced_gate_up(const uint16_t* x_bf16, int T, int H, int F, i
   uint8_t* qc = reinterpret_cast<uint8_t*>(ws + L.qx_codes);
   uint8_t* qs = reinterpret_cast<uint8_t*>(ws + L.qx_scales);
   int32_t* qe = reinterpret_cast<int32_t*>(ws + L.qx_exp);
+  // the slices of x depend only on x: they are formed while the CSR kernel still runs, and
+  // only their stores wait for it; the tile list follows
+  cudaError_t st = launch_slice_x(x_bf16, T, H, k, reinterpret_cast<const int32_t*>(ws + L.pair_pos),
+                                  qc, qs, qe, s);
+  if (st != cudaSuccess) return st;
   int32_t* tiles = reinterpret_cast<int32_t*>(ws + L.tiles);
-  cudaError_t st = launch_tiles(csr.expert_offsets, b.E, NS, kSliceTile, tiles, s);
-  if (st != cudaSuccess) return st;
-  // the slices of x are formed while the tile list is built; only their stores wait
-  st = launch_slice_x(x_bf16, T, H, k, reinterpret_cast<const int32_t*>(ws + L.pair_pos), qc, qs, qe, s);
-  if (st != cudaSuccess) return st;
+  if ((st = launch_tiles(csr.expert_offsets, b.E, NS, kSliceTile, tiles, s)) != cudaSuccess) return st;
   // weights: [K bytes][gate, up][row], so the box {128 B, 2, 64} lands gate row i and up row i
   // as shared-memory rows 2i and 2i+1; the row extent stops F rows short of the bank so the
   // up coordinate (row + F) stays inside it
@@ -408,6 +413,7 @@ cudaError_t launch_sliced_gate_up(const uint16_t* x_bf16, int T, int H, int F, i
   const uint64_t cdims[3] = {(uint64_t)H / 2, 2, wrows};
   const uint64_t cstr[2] = {(uint64_t)F * (H / 2), (uint64_t)H / 2};
   const uint32_t cbox[3] = {128, 2, 64};
+  const int sbw = 16 * SCfg<true>::KSUB < H / 16 ? 16 * SCfg<true>::KSUB : H / 16;
   const uint64_t sdims[3] = {(uint64_t)H / 16, 2, wrows};
   const uint64_t sstr[2] = {(uint64_t)F * (H / 16), (uint64_t)H / 16};
   const uint32_t sbox[3] = {32, 2, 64};
@@ -415,10 +421,10 @@ cudaError_t launch_sliced_gate_up(const uint16_t* x_bf16, int T, int H, int F, i
   if (!make_map3(&ma, b.codes, cdims, cstr, cbox, true) ||
       !make_map(&mb, qc, H / 2, H / 2, rows, 128, kSliceTile, true) ||
       !make_map3(&msa, b.scales, sdims, sstr, sbox, false) ||
-      !make_map(&msb, qs, H / 16, H / 16, rows, 32, kSliceTile, false))
+      !make_map(&msb, qs, H / 16, H / 16, rows, sbw, kSliceTile, false))
     return cudaErrorInvalidValue;
   SlicedArgs a{qe, tiles, reinterpret_cast<float*>(ws + L.h),
-               reinterpret_cast<uint32_t*>(ws + L.error_word), H, 2 * F, F / 64, F, F, 1};
+               reinterpret_cast<uint32_t*>(ws + L.error_word), H, 2 * F, F / 64, F, F, 1, sbw};
   const int max_tiles = (int)(rows / kSliceTile) + (P < b.E ? P : b.E) + 1;
   return run_sliced<true>(ma, mb, msa, msb, a, max_tiles, s);
 }
@@ -443,16 +449,17 @@ cudaError_t launch_sliced_down(const moe_nvfp4_bank& b, moe_csr csr, int T, int 
   if (128 % g != 0 || g * sfrow > 256 || 128 * sfrow > 11264) return cudaErrorInvalidValue;
   const uint64_t rows = (uint64_t)P * NS;
   const uint64_t wrows = (uint64_t)b.E * H;
+  const int sbw = 16 * SCfg<false>::KSUB < sfh ? 16 * SCfg<false>::KSUB : sfh;
   CUtensorMap ma, mb, msa, msb;
   if (!make_map(&ma, b.codes, F / 2, F / 2, wrows, 128, 128, true) ||
       !make_map(&mb, qc, F / 2, F / 2, rows, 128, kSliceTile, true) ||
       !make_map(&msa, b.scales, (uint64_t)g * sfrow, (uint64_t)g * sfrow, wrows / g,
                 g * sfrow, 128 / g, false) ||
-      !make_map(&msb, qs, sfh, sfh, rows, 32, kSliceTile, false))
+      !make_map(&msb, qs, sfh, sfh, rows, sbw, kSliceTile, false))
     return cudaErrorInvalidValue;
   SlicedArgs a{qe, reinterpret_cast<const int32_t*>(ws + L.tiles),
                reinterpret_cast<float*>(ws + L.partial),
-               reinterpret_cast<uint32_t*>(ws + L.error_word), F, H, H / 128, H, F, g};
+               reinterpret_cast<uint32_t*>(ws + L.error_word), F, H, H / 128, H, F, g, sbw};
   const int max_tiles = (int)(rows / kSliceTile) + (P < b.E ? P : b.E) + 1;
   return run_sliced<false>(ma, mb, msa, msb, a, max_tiles, s);
 }
