@@ -472,8 +472,8 @@ def run_ours(args):
         gu_bytes = [uniq[b] * gu_bytes_per_expert for (b, _) in brk]
         ach = sum(gu_bytes) / (sum(gu_ms) * 1e-3) / 1e9
         alg = sum(gu_bytes) / len(gu_bytes)
-        # from 512 pairs the decode call runs the sliced tensor-core form
-        sliced = wl.P >= 512
+        # from moe.decode_tensor_core_min_pairs() pairs the decode call runs the sliced form
+        sliced = wl.P >= moe.decode_tensor_core_min_pairs()
         ratio = (recorded_traffic([args.workload, "verify_T128"], "sliced_gemm_kernel<1>") if sliced
                  else recorded_traffic([args.workload, "decode_T8"], "gate_up_tma_kernel"))
         roof = {"bound": "hbm", "kernel": "decode gate_up+SiLU (moe_grouped_gate_up_silu_nvfp4; " +

@@ -134,6 +134,11 @@ moe_status moe_workspace_layout(int32_t T, int32_t H, int32_t F, int32_t E, int3
 
 /* Path AUTO resolves to: PREFILL if T*k >= this value, else DECODE. */
 int32_t moe_prefill_min_pairs(void);
+/* On the DECODE path, from this many pairs (T*k) on the gate/up and down calls run the
+ * tensor-core form: each activation row (x, then h) as four residual NVFP4 slices
+ * multiplied by the block-scaled FP4 tensor cores; below it, the exact-f16 activations
+ * against weights dequantised in registers. Both stay within the stated tolerance. */
+int32_t moe_decode_tensor_core_min_pairs(void);
 /* The path a call with these arguments runs (DECODE or PREFILL). */
 int32_t moe_resolve_path(int32_t T, int32_t k, int32_t path);
 

@@ -14,7 +14,7 @@ import torch
 from . import _native
 from ._native import PATH_AUTO, PATH_DECODE, PATH_PREFILL, DEVERR_EXPERT_ID, DEVERR_TIMEOUT  # noqa
 
-__all__ = ["MoeError", "NvFp4Bank", "ExpertCSR", "workspace_bytes", "workspace_layout",
+__all__ = ["MoeError", "NvFp4Bank", "ExpertCSR", "workspace_bytes", "workspace_layout", "decode_tensor_core_min_pairs",
            "resolve_path", "prefill_min_pairs", "kernel_launches", "moe_route_topk", "moe_build_expert_csr",
            "moe_build_expert_csr_static",
            "moe_grouped_gate_up_silu_nvfp4", "moe_grouped_down_combine_nvfp4",
@@ -99,6 +99,11 @@ def kernel_launches(T: int, H: int, F: int, E: int, k: int, path: int = PATH_AUT
 
 def prefill_min_pairs() -> int:
     return int(_native.load().moe_prefill_min_pairs())
+
+
+def decode_tensor_core_min_pairs() -> int:
+    """Pairs (T*k) from which the decode path runs its tensor-core (sliced) form."""
+    return int(_native.load().moe_decode_tensor_core_min_pairs())
 
 
 def moe_route_topk(logits: torch.Tensor, k: int, topk_ids: torch.Tensor, topk_w: torch.Tensor,

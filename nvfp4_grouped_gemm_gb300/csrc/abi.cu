@@ -128,6 +128,8 @@ moe_status moe_workspace_layout(int32_t T, int32_t H, int32_t F, int32_t E, int3
 
 int32_t moe_prefill_min_pairs(void) { return kPrefillMinPairs; }
 
+int32_t moe_decode_tensor_core_min_pairs(void) { return kSlicedMinPairs; }
+
 int32_t moe_resolve_path(int32_t T, int32_t k, int32_t path) { return resolve_path(T, k, path); }
 
 int32_t moe_kernel_launches(int32_t T, int32_t H, int32_t F, int32_t E, int32_t k, int32_t path) {

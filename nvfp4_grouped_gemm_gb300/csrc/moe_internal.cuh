@@ -23,7 +23,7 @@ constexpr int kDecodeSlices = 4;
 // The decode path runs the sliced tensor-core GEMMs from this many pairs on (below it, the
 // TMA-fed mma.sync kernels of decode.cu, whose fixed costs are lower).
 #ifndef MOE_SLICED_MIN_PAIRS
-#define MOE_SLICED_MIN_PAIRS 512
+#define MOE_SLICED_MIN_PAIRS 256
 #endif
 constexpr int kSlicedMinPairs = MOE_SLICED_MIN_PAIRS;
 inline bool decode_sliced(long long P) { return P >= kSlicedMinPairs; }

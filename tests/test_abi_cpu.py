@@ -109,13 +109,14 @@ def test_host_validation_rejects_before_launch(lib):
 
 def test_kernel_launch_count_host_logic(lib):
     """The per-layer kernel count the library reports follows its own launch plan: decode
-    below 512 pairs runs x-gather, gate/up, h-prep, down and combine after the CSR; from 512
+    below 256 pairs runs x-gather, gate/up, h-prep, down and combine after the CSR; from 256
     pairs it runs tiles, x slices, the gate/up GEMM, h slices, the down GEMM and the combine;
     prefill runs tiles, Q(x), the gate/up GEMM, Q(h), the down GEMM and the combine; the CSR
     is one kernel below 4096 pairs and three from there on."""
     assert moe.kernel_launches(8, 2560, 640, 512, 10) == 1 + 5
-    assert moe.kernel_launches(51, 2560, 640, 256, 10) == 1 + 5
-    assert moe.kernel_launches(52, 2560, 640, 256, 10) == 1 + 6
+    assert moe.decode_tensor_core_min_pairs() == 256
+    assert moe.kernel_launches(25, 2560, 640, 256, 10) == 1 + 5
+    assert moe.kernel_launches(26, 2560, 640, 256, 10) == 1 + 6
     assert moe.kernel_launches(128, 2560, 640, 256, 10) == 1 + 6
     assert moe.kernel_launches(4096, 4096, 640, 288, 8) == 3 + 6
     assert moe.kernel_launches(4, 256, 64, 16, 2, moe.PATH_PREFILL) == 1 + 6

@@ -118,7 +118,7 @@ def test_split_batch_bit_identical():
 
 
 def test_split_batch_bit_identical_sliced():
-    """The same split check on the sliced tensor-core form (both halves at >= 512 pairs):
+    """The same split check on the sliced tensor-core form (both halves at >= 256 pairs):
     a pair's slices depend only on its token and each output column is reduced on its own,
     so how pairs share tiles does not change a bit."""
     wl = synth.verify(128)
@@ -217,10 +217,10 @@ def test_many_pairs_on_one_expert():
                                        (80, 256, 128, 7, 7),      # 80 pairs per expert: 10 tiles
                                        (52, 512, 1408, 32, 10)])  # widest decode F
 def test_sliced_path_shapes(T, H, F, E, k):
-    """From 512 pairs the decode path runs the sliced tensor-core GEMMs: ragged tiles, an
+    """From 256 pairs the decode path runs the sliced tensor-core GEMMs: ragged tiles, an
     expert spread over many 8-pair tiles, a down projection of one 64-wide k-step, and the
     widest F (its weight-scale rows staged whole)."""
-    assert T * k >= 512
+    assert T * k >= moe.decode_tensor_core_min_pairs()
     wl = synth.logits_workload(f"sliced_{T}_{H}_{F}", T, H, F, E, k, seed=21)
     run = run_layer(wl)
     assert run.err == 0
