@@ -245,24 +245,26 @@ __device__ __forceinline__ float cta_max(float x, float* red) {
   return m;
 }
 
-// One slice of a quarter block: the 4 residual values r of this thread (elements 4q..4q+3
-// of a 16-value block whose other quarters sit in the neighbouring lanes q^1, q^2).  Row
-// exponent from row_amax, block scale from the block's max key (shared by the 4 lanes), E2M1
-// codes as in quant_block; r becomes the remainder.  Returns the 4 codes as 16 bits.
-__device__ __forceinline__ uint32_t slice_quarter(float (&r)[4], float row_amax, int& s_out,
-                                                  int& sbc_out) {
+// One slice of part of a block: the EPT residual values r of this thread (elements
+// EPT*q .. EPT*q + EPT-1 of a 16-value block whose other parts sit in the neighbouring lanes).
+// Row exponent from row_amax, block scale from the block's max key (shared by the block's
+// lanes), E2M1 codes as in quant_block; r becomes the remainder.  Returns the EPT codes as
+// 4*EPT bits.
+template <int EPT>
+__device__ __forceinline__ uint32_t slice_part(float (&r)[EPT], float row_amax, int& s_out,
+                                               int& sbc_out) {
   const int s = row_exp_of(row_amax);
   const bool fast = s >= -127 && s <= 149;
   const float m = fast ? pow2f(-s) : 0.0f;
-  float key[4];
+  float key[EPT];
   float bmax = 0.0f;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
+  for (int i = 0; i < EPT; ++i) {
     key[i] = scale_down(fabsf(r[i]), s, fast, m);
     bmax = fmaxf(bmax, key[i]);
   }
-  bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 1));
-  bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 2));
+#pragma unroll
+  for (int o = 1; o < 16 / EPT; o <<= 1) bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, o));
   const int sbc = ue4m3_code_of(bmax);
   uint32_t codes = 0;
   if (sbc != 0) {
@@ -272,7 +274,7 @@ __device__ __forceinline__ uint32_t slice_quarter(float (&r)[4], float row_amax,
     const bool up_fast = s >= -126 && s <= 127;
     const float p = up_fast ? pow2f(s) : 0.0f;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < EPT; ++i) {
       const float v = key[i];
       // the same three-step threshold search as quant_block (ties to the even code)
       const bool b2 = v >= t3;
@@ -291,36 +293,45 @@ __device__ __forceinline__ uint32_t slice_quarter(float (&r)[4], float row_amax,
   return codes;
 }
 
-// x: one CTA per token, four threads per 16-value block (thread 4b + q holds elements
-// 16b + 4q .. +3).  The slices depend only on x, so they are formed before the wait; after it
-// they are written to the NS rows of each of the token's pairs (rows pair_pos * NS + i).
+// Elements per thread in the slice kernels: a 16-value block is shared by two lanes.
+constexpr int kSliceEPT = 8;
+
+// x: one CTA per token, 16/EPT threads per 16-value block (thread (16/EPT)*b + q holds
+// elements 16b + EPT*q ..).  The slices depend only on x, so they are formed before the
+// wait; after it they are written to the NS rows of each of the token's pairs (rows
+// pair_pos * NS + i).
 template <int NS>
 __global__ void __launch_bounds__(1024) slice_x_kernel(const uint16_t* __restrict__ x, int H, int k,
                                                        const int32_t* __restrict__ pair_pos,
                                                        uint8_t* __restrict__ qc,
                                                        uint8_t* __restrict__ qs,
                                                        int32_t* __restrict__ qe) {
+  constexpr int EPT = kSliceEPT, TPB = 16 / EPT;
   __shared__ float red[NS][32];
   __shared__ int s_pos[kMaxK];
   const int t = blockIdx.x, tid = threadIdx.x;
-  const int b = tid >> 2, q = tid & 3;
+  const int b = tid / TPB, q = tid % TPB;
   const int nblk = H / 16;
   const bool has = b < nblk;
-  float r[4];
+  float r[EPT];
   {
-    const uint2 w = has ? __ldg(reinterpret_cast<const uint2*>(x + (size_t)t * H + 16 * b + 4 * q))
-                        : make_uint2(0, 0);
-    r[0] = __uint_as_float(w.x << 16);
-    r[1] = __uint_as_float(w.x & 0xffff0000u);
-    r[2] = __uint_as_float(w.y << 16);
-    r[3] = __uint_as_float(w.y & 0xffff0000u);
+    const uint4 w = has ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H + 16 * b + EPT * q))
+                        : make_uint4(0, 0, 0, 0);
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      r[2 * i] = __uint_as_float(ww[i] << 16);
+      r[2 * i + 1] = __uint_as_float(ww[i] & 0xffff0000u);
+    }
   }
   uint32_t codes[NS];
   int sbc[NS], sx[NS];
 #pragma unroll
   for (int i = 0; i < NS; ++i) {
-    const float a = fmaxf(fmaxf(fabsf(r[0]), fabsf(r[1])), fmaxf(fabsf(r[2]), fabsf(r[3])));
-    codes[i] = slice_quarter(r, cta_max(a, red[i]), sx[i], sbc[i]);
+    float a = 0.0f;
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) a = fmaxf(a, fabsf(r[e]));
+    codes[i] = slice_part<EPT>(r, cta_max(a, red[i]), sx[i], sbc[i]);
   }
   pdl_wait();                                       // pair_pos is complete
   pdl_trigger();
@@ -334,14 +345,14 @@ __global__ void __launch_bounds__(1024) slice_x_kernel(const uint16_t* __restric
 #pragma unroll
     for (int i = 0; i < NS; ++i) {
       const size_t row = (size_t)pos * NS + i;
-      *reinterpret_cast<uint16_t*>(qc + row * (H / 2) + 8 * b + 2 * q) = (uint16_t)codes[i];
+      *reinterpret_cast<uint32_t*>(qc + row * (H / 2) + 8 * b + (EPT / 2) * q) = codes[i];
       if (q == 0) qs[row * nblk + b] = (uint8_t)sbc[i];
       if (tid == 0) qe[row] = sx[i];
     }
   }
 }
 
-// h: one CTA per CSR row (f32 h, rows in CSR order), rows r * NS + i, four threads per block.
+// h: one CTA per CSR row (f32 h, rows in CSR order), rows r * NS + i.
 template <int NS>
 __global__ void __launch_bounds__(1024) slice_h_kernel(const float* __restrict__ h, int F,
                                                        int sf_pitch,
@@ -349,28 +360,34 @@ __global__ void __launch_bounds__(1024) slice_h_kernel(const float* __restrict__
                                                        uint8_t* __restrict__ qc,
                                                        uint8_t* __restrict__ qs,
                                                        int32_t* __restrict__ qe) {
+  constexpr int EPT = kSliceEPT, TPB = 16 / EPT;
   __shared__ float red[NS][32];
   pdl_wait();
   pdl_trigger();
   const int row0 = blockIdx.x, tid = threadIdx.x;
   if (row0 >= offsets[E]) return;                  // uniform over the CTA
-  const int b = tid >> 2, q = tid & 3;
+  const int b = tid / TPB, q = tid % TPB;
   const int nblk = F / 16;
   const bool has = b < nblk;
-  float r[4];
+  float r[EPT];
   {
-    const float4 v = has ? __ldcs(reinterpret_cast<const float4*>(h + (size_t)row0 * F + 16 * b + 4 * q))
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
-    r[0] = v.x; r[1] = v.y; r[2] = v.z; r[3] = v.w;
+    const float4* p = reinterpret_cast<const float4*>(h + (size_t)row0 * F + 16 * b + EPT * q);
+#pragma unroll
+    for (int i = 0; i < EPT / 4; ++i) {
+      const float4 v = has ? __ldcs(p + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+      r[4 * i] = v.x; r[4 * i + 1] = v.y; r[4 * i + 2] = v.z; r[4 * i + 3] = v.w;
+    }
   }
 #pragma unroll
   for (int i = 0; i < NS; ++i) {
-    const float a = fmaxf(fmaxf(fabsf(r[0]), fabsf(r[1])), fmaxf(fabsf(r[2]), fabsf(r[3])));
+    float a = 0.0f;
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) a = fmaxf(a, fabsf(r[e]));
     int s, sbc;
-    const uint32_t c = slice_quarter(r, cta_max(a, red[i]), s, sbc);
+    const uint32_t c = slice_part<EPT>(r, cta_max(a, red[i]), s, sbc);
     if (has) {
       const size_t row = (size_t)row0 * NS + i;
-      *reinterpret_cast<uint16_t*>(qc + row * (F / 2) + 8 * b + 2 * q) = (uint16_t)c;
+      *reinterpret_cast<uint32_t*>(qc + row * (F / 2) + 8 * b + (EPT / 2) * q) = c;
       if (q == 0) qs[row * sf_pitch + b] = (uint8_t)sbc;
       if (tid == 0) qe[row] = s;
     }
@@ -435,7 +452,7 @@ cudaError_t launch_quant_x(const uint16_t* x_bf16, int T, int H, int k, const in
 
 cudaError_t launch_slice_x(const uint16_t* x_bf16, int T, int H, int k, const int32_t* pair_pos,
                            uint8_t* qc, uint8_t* qs, int32_t* qe, cudaStream_t s) {
-  const int threads = (H / 4 + 31) / 32 * 32;      // four per 16-value block
+  const int threads = (H / kSliceEPT + 31) / 32 * 32;
   if (threads > 1024) return cudaErrorInvalidValue;
   return launch_pdl(slice_x_kernel<kDecodeSlices>, dim3(T), dim3(threads), 0, s, x_bf16, H, k,
                     pair_pos, qc, qs, qe);
@@ -443,7 +460,7 @@ cudaError_t launch_slice_x(const uint16_t* x_bf16, int T, int H, int k, const in
 
 cudaError_t launch_slice_h(const float* h, int P, int F, int sf_pitch, const int32_t* offsets,
                            int E, uint8_t* qc, uint8_t* qs, int32_t* qe, cudaStream_t s) {
-  const int threads = (F / 4 + 31) / 32 * 32;
+  const int threads = (F / kSliceEPT + 31) / 32 * 32;
   if (threads > 1024) return cudaErrorInvalidValue;
   return launch_pdl(slice_h_kernel<kDecodeSlices>, dim3(P), dim3(threads), 0, s, h, F, sf_pitch,
                     offsets, E, qc, qs, qe);
