@@ -210,6 +210,17 @@ moe_status moe_grouped_down_combine_nvfp4(const moe_nvfp4_bank* w_down, moe_csr 
 moe_status moe_build_expert_csr_static(const int32_t* topk_ids, int32_t T, int32_t k, int32_t E,
                                        moe_csr csr, void* stream);
 
+/* Weight-layout import (not on the per-layer path): rows stored the way the pages' banks
+ * are ("moe_sk_repro.rs", mk_bank: 64 values per 36-byte block; "moe_sel_census.rs", BLK:
+ * 4 UE4M3 sub-scales + 32 code bytes) into the planar planes this library reads. Each
+ * row of in_f weights is in_f/64 blocks; a block is its 4 scale bytes (scale i for weights
+ * 16i..16i+15 of the block) followed by its 32 code bytes (low nibble = even weight).
+ * blob u8 [rows][in_f/64*36] (4-byte aligned) -> codes u8 [rows][in_f/2] (16-byte aligned),
+ * scales u8 [rows][in_f/16] (4-byte aligned); all device pointers, caller-owned; rows is
+ * E times the rows of one expert for a whole bank. in_f % 64 == 0. Async on `stream`. */
+moe_status moe_nvfp4_from_interleaved(const uint8_t* blob, int64_t rows, int32_t in_f,
+                                      uint8_t* codes, uint8_t* scales, void* stream);
+
 /* Human-readable name of a status (static string, never NULL). */
 const char* moe_status_string(moe_status status);
 

@@ -57,6 +57,22 @@ class NvFp4Bank:
         self._c = _native.Bank(codes.data_ptr(), scales.data_ptr(), self.E, self.rows, self.in_f)
 
     @classmethod
+    def from_interleaved(cls, blob: torch.Tensor, E: int, rows: int, in_f: int,
+                         stream=None) -> "NvFp4Bank":
+        """A bank from the pages' interleaved storage: blob u8 [E, rows, in_f/64*36] on the
+        device (36-byte blocks of 4 UE4M3 scales then 32 code bytes), converted on the GPU."""
+        if blob.dtype != torch.uint8 or not blob.is_contiguous() or not blob.is_cuda:
+            raise TypeError("blob must be a contiguous uint8 CUDA tensor")
+        if blob.numel() != E * rows * (in_f // 64) * 36 or in_f % 64:
+            raise ValueError("blob size does not match E * rows * in_f/64 * 36")
+        codes = torch.empty(E, rows, in_f // 2, dtype=torch.uint8, device=blob.device)
+        scales = torch.empty(E, rows, in_f // 16, dtype=torch.uint8, device=blob.device)
+        _check(_native.load().moe_nvfp4_from_interleaved(_ptr(blob), E * rows, in_f, _ptr(codes),
+                                                         _ptr(scales), _stream(stream)),
+               "moe_nvfp4_from_interleaved")
+        return cls(codes, scales)
+
+    @classmethod
     def from_numpy(cls, bank, device="cuda") -> "NvFp4Bank":
         return cls(torch.from_numpy(bank.codes).to(device), torch.from_numpy(bank.scales).to(device))
 

@@ -38,6 +38,7 @@ SIGNATURES = [
     ("moe_workspace_layout", c_i32, [c_i32] * 6 + [ctypes.POINTER(WsLayout)]),
     ("moe_prefill_min_pairs", c_i32, []),
     ("moe_decode_tensor_core_min_pairs", c_i32, []),
+    ("moe_nvfp4_from_interleaved", c_i32, [c_vp, ctypes.c_int64, c_i32, c_vp, c_vp, c_vp]),
     ("moe_resolve_path", c_i32, [c_i32] * 3),
     ("moe_kernel_launches", c_i32, [c_i32] * 6),
     ("moe_route_topk", c_i32, [c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp]),

@@ -194,3 +194,28 @@ def quantize(v: np.ndarray):
 def dequant_q(codes: np.ndarray, scales: np.ndarray, s: np.ndarray) -> np.ndarray:
     """Value of a Q result: E2M1(code) * UE4M3(scale) * 2^s."""
     return np.ldexp(dequant(codes, scales), np.asarray(s)[..., None])
+
+
+def from_interleaved(blob: np.ndarray, in_f: int):
+    """Planar (codes, scales) of rows stored as 36-byte blocks per 64 weights.
+
+    The pages' own banks use this storage: "NVFP4 stores 64 values per 36-byte block"
+    ("moe_sk_repro.rs", `fn main`, `mk_bank`, row bytes in_f / 64 * 36) and "4 UE4M3
+    sub-scales + 32 code bytes" per block ("moe_sel_census.rs", constant `BLK`).  Reading
+    of the order the pages leave open: the block's 4 scale bytes come first (scale i
+    covers weights 16i .. 16i+15 of the block), then its 32 code bytes (two codes per
+    byte, low nibble = even weight, as in the planar layout).
+
+    blob: uint8 [..., in_f / 64 * 36].  Returns codes uint8 [..., in_f / 2] and scales
+    uint8 [..., in_f / 16].
+    """
+    blob = np.asarray(blob, dtype=np.uint8)
+    if in_f % 64:
+        raise ValueError("in_f must be a multiple of 64")
+    nblk = in_f // 64
+    if blob.shape[-1] != nblk * 36:
+        raise ValueError("row length must be in_f / 64 * 36 bytes")
+    b = blob.reshape(blob.shape[:-1] + (nblk, 36))
+    scales = b[..., :4].reshape(blob.shape[:-1] + (in_f // 16,))
+    codes = b[..., 4:].reshape(blob.shape[:-1] + (in_f // 2,))
+    return codes.copy(), scales.copy()

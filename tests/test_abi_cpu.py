@@ -102,6 +102,11 @@ def test_host_validation_rejects_before_launch(lib):
     wide = _native.Bank(16, 16, 16, 2 * 2048, 256)
     assert lib.moe_grouped_gate_up_silu_nvfp4(16, 4, 256, 2048, 2, ctypes.byref(wide), good, 1,
                                               256, 1 << 30, None) == 2
+    # interleaved import: null, in_f not a multiple of 64, misaligned codes
+    assert lib.moe_nvfp4_from_interleaved(None, 4, 128, 16, 16, None) == 1
+    assert lib.moe_nvfp4_from_interleaved(16, 4, 96, 16, 16, None) == 1
+    assert lib.moe_nvfp4_from_interleaved(16, 4, 128, 24, 16, None) == 1
+    assert lib.moe_nvfp4_from_interleaved(16, 0, 128, 16, 16, None) == 1
     dbank = _native.Bank(16, 16, 16, 256, 64)
     assert lib.moe_grouped_down_combine_nvfp4(ctypes.byref(dbank), good, 16, 4, 256, 64, 2, 0,
                                               None, 256, 1 << 20, None) == 1

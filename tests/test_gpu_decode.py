@@ -131,6 +131,36 @@ def test_split_batch_bit_identical_sliced():
         assert np.array_equal(y, full[lo:hi])
 
 
+def test_interleaved_banks_import_bit_exact_and_run_the_same_layer():
+    """Banks stored the pages' way (36-byte blocks: 4 scales then 32 code bytes per 64
+    weights) convert on the GPU to exactly the oracle's planar bytes, and a layer on the
+    converted banks is bit-identical to one on banks converted by the oracle."""
+    from oracle import nvfp4
+    wl = synth.decode(8)
+
+    def interleave(bank):
+        E, rows, half = bank.codes.shape
+        in_f = half * 2
+        c = bank.codes.reshape(E, rows, in_f // 64, 32)
+        s = bank.scales.reshape(E, rows, in_f // 64, 4)
+        return np.concatenate([s, c], axis=-1).reshape(E, rows, in_f // 64 * 36), in_f
+
+    banks = []
+    for bank in (wl.gate_up, wl.down):
+        blob, in_f = interleave(bank)
+        E, rows = blob.shape[:2]
+        dev = moe.NvFp4Bank.from_interleaved(torch.from_numpy(np.ascontiguousarray(blob)).cuda(),
+                                             E, rows, in_f)
+        torch.cuda.synchronize()
+        ref_c, ref_s = nvfp4.from_interleaved(blob, in_f)
+        assert np.array_equal(dev.codes.cpu().numpy(), ref_c)
+        assert np.array_equal(dev.scales.cpu().numpy(), ref_s)
+        banks.append(dev)
+    y_imp = run_layer(wl, banks=tuple(banks), fetch=False).y
+    y_ref = run_layer(wl, fetch=False).y
+    assert np.array_equal(y_imp, y_ref)
+
+
 def test_single_token_single_expert():
     """k = 1, T = 1: the smallest layer."""
     wl = synth.tiny(seed=3)

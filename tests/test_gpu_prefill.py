@@ -137,6 +137,17 @@ def test_prefill_small(seed):
     _down_from_oracle_h(wl, run, res, toks)
 
 
+@pytest.mark.parametrize("T", [1, 8])
+def test_prefill_numerics_at_decode_sizes(T):
+    """The PREFILL path (NVFP4 x and h, FP4 x FP4 tensor-core GEMMs) chosen explicitly at
+    decode batch sizes: one T sweep can keep the prefill semantics across the AUTO switch,
+    checked stage by stage like the large cases."""
+    wl = synth.decode(T)
+    run = run_layer(wl, path=PF)
+    assert run.err == 0
+    res, info = _stages(wl, run, np.arange(T))
+
+
 def test_prefill_full_size_sampled():
     """The prefill workload at full size (4096 tokens, 32768 pairs, 288 experts)."""
     wl = synth.prefill()

@@ -196,3 +196,24 @@ def test_quantize_roundtrip_error_bound():
     # scaling a row by a power of two leaves codes and block scales unchanged
     c2, sc2, s2 = nvfp4.quantize(v * 2.0 ** 7)
     assert np.array_equal(c, c2) and np.array_equal(sc, sc2) and np.array_equal(s2, s + 7)
+
+
+def test_interleaved_block_import_matches_hand_written_fixture(golden_dir):
+    """The pages' 36-byte blocks (4 scales + 32 code bytes per 64 weights) become the planar
+    code and scale rows written out by hand, and dequantise to the values the block means."""
+    rows = {}
+    for line in open(os.path.join(golden_dir, "interleaved_block.txt")):
+        if line.strip() and not line.startswith("#"):
+            f = line.split()
+            rows[f[0]] = np.frombuffer(bytes.fromhex("".join(f[1:])), np.uint8)
+    assert rows["interleaved"].size == 2 * 36
+    codes, scales = nvfp4.from_interleaved(rows["interleaved"], 128)
+    assert np.array_equal(codes, rows["codes"])
+    assert np.array_equal(scales, rows["scales"])
+    w = nvfp4.dequant(codes[None, None, :], scales[None, None, :])[0, 0]
+    # block 0: code w%16 times scales 1, 0.5, 0.25, 0.125 per 16 weights
+    assert w[0] == 0.0 and w[7] == 6.0 and w[15] == -6.0 and w[17] == 0.25 and w[33] == 0.125 and w[40] == 0.0
+    # block 1: even weights 0.5, odd weights 1.0, times 2^-6, 2^-5, 2^-4, 448
+    assert w[64] == 0.5 / 64 and w[65] == 1.0 / 64 and w[80] == 0.5 / 32 and w[127] == 448.0
+    with pytest.raises(ValueError):
+        nvfp4.from_interleaved(rows["interleaved"][:70], 128)
