@@ -76,11 +76,16 @@ enum { MOE_PATH_AUTO = 0, MOE_PATH_DECODE = 1, MOE_PATH_PREFILL = 2 };
 enum { MOE_DEVERR_EXPERT_ID = 1, MOE_DEVERR_TIMEOUT = 2 };
 
 /* One NVFP4 weight bank. gate_up: rows = 2F (gate rows 0..F-1, up rows F..2F-1),
- * in_f = H. down: rows = H, in_f = F. */
+ * in_f = H. down: rows = H, in_f = F. A weight is E2M1(code) x UE4M3(scale of its
+ * 16-group), times alpha[e] when `alpha` is not NULL: an optional per-expert float32
+ * second-level scale (the two-level scaling of ModelOpt NVFP4 checkpoints, "ModelOpt
+ * group-16" on page 4; device array [E], finite, caller-owned). On the PREFILL path the
+ * down bank's alpha must stay <= 2 (its f16 partials are scaled for |alpha| <= 2). */
 typedef struct moe_nvfp4_bank {
   const uint8_t* codes;
   const uint8_t* scales;
   int32_t E, rows, in_f;
+  const float* alpha;
 } moe_nvfp4_bank;
 
 /* Expert-first CSR written by moe_build_expert_csr (all device arrays, caller-owned):

@@ -9,6 +9,7 @@ from __future__ import annotations
 import ctypes
 from typing import Optional
 
+import numpy as np
 import torch
 
 from . import _native
@@ -43,22 +44,29 @@ def _stream(stream) -> Optional[int]:
 
 
 class NvFp4Bank:
-    """Planar NVFP4 bank on the device: codes u8 [E, rows, in_f/2], scales u8 [E, rows, in_f/16]."""
+    """Planar NVFP4 bank on the device: codes u8 [E, rows, in_f/2], scales u8 [E, rows, in_f/16],
+    and optionally alpha f32 [E], a per-expert second-level scale of the weights."""
 
-    def __init__(self, codes: torch.Tensor, scales: torch.Tensor):
+    def __init__(self, codes: torch.Tensor, scales: torch.Tensor,
+                 alpha: Optional[torch.Tensor] = None):
         if codes.dtype != torch.uint8 or scales.dtype != torch.uint8:
             raise TypeError("codes and scales must be uint8")
         if codes.dim() != 3 or scales.dim() != 3:
             raise ValueError("bank planes are [E, rows, bytes]")
         if not (codes.is_contiguous() and scales.is_contiguous()):
             raise ValueError("bank planes must be contiguous")
-        self.codes, self.scales = codes, scales
+        if alpha is not None:
+            if alpha.dtype != torch.float32 or alpha.numel() != codes.shape[0] or \
+                    not alpha.is_contiguous() or alpha.device != codes.device:
+                raise ValueError("alpha must be a contiguous float32 [E] tensor beside the codes")
+        self.codes, self.scales, self.alpha = codes, scales, alpha
         self.E, self.rows, self.in_f = codes.shape[0], codes.shape[1], codes.shape[2] * 2
-        self._c = _native.Bank(codes.data_ptr(), scales.data_ptr(), self.E, self.rows, self.in_f)
+        self._c = _native.Bank(codes.data_ptr(), scales.data_ptr(), self.E, self.rows, self.in_f,
+                               alpha.data_ptr() if alpha is not None else None)
 
     @classmethod
     def from_interleaved(cls, blob: torch.Tensor, E: int, rows: int, in_f: int,
-                         stream=None) -> "NvFp4Bank":
+                         alpha: Optional[torch.Tensor] = None, stream=None) -> "NvFp4Bank":
         """A bank from the pages' interleaved storage: blob u8 [E, rows, in_f/64*36] on the
         device (36-byte blocks of 4 UE4M3 scales then 32 code bytes), converted on the GPU."""
         if blob.dtype != torch.uint8 or not blob.is_contiguous() or not blob.is_cuda:
@@ -70,11 +78,14 @@ class NvFp4Bank:
         _check(_native.load().moe_nvfp4_from_interleaved(_ptr(blob), E * rows, in_f, _ptr(codes),
                                                          _ptr(scales), _stream(stream)),
                "moe_nvfp4_from_interleaved")
-        return cls(codes, scales)
+        return cls(codes, scales, alpha)
 
     @classmethod
     def from_numpy(cls, bank, device="cuda") -> "NvFp4Bank":
-        return cls(torch.from_numpy(bank.codes).to(device), torch.from_numpy(bank.scales).to(device))
+        alpha = getattr(bank, "alpha", None)
+        return cls(torch.from_numpy(bank.codes).to(device), torch.from_numpy(bank.scales).to(device),
+                   None if alpha is None else torch.from_numpy(
+                       np.ascontiguousarray(alpha, dtype=np.float32)).to(device))
 
     def nbytes(self) -> int:
         return self.codes.numel() + self.scales.numel()

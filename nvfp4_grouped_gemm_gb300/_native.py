@@ -18,7 +18,8 @@ DEVERR_EXPERT_ID, DEVERR_TIMEOUT = 1, 2
 
 
 class Bank(ctypes.Structure):
-    _fields_ = [("codes", c_vp), ("scales", c_vp), ("E", c_i32), ("rows", c_i32), ("in_f", c_i32)]
+    _fields_ = [("codes", c_vp), ("scales", c_vp), ("E", c_i32), ("rows", c_i32), ("in_f", c_i32),
+                ("alpha", c_vp)]
 
 
 class CSR(ctypes.Structure):

@@ -173,6 +173,7 @@ struct GateUpArgs {
   const int32_t* active;
   const int32_t* n_active;
   float* h;
+  const float* alpha = nullptr;   // [E] per-expert second-level weight scale, or none
 };
 
 // Persistent: CTA c owns a contiguous range of work units u = (active expert, 16-row
@@ -306,8 +307,9 @@ __global__ void __launch_bounds__(256, 2) gate_up_kernel(const GateUpArgs args) 
           const int ii = i0 + g + 8 * (q >> 1);
           if (n < live) {
             const int ex = args.xe[off + tok0 + n];
+            const float al = args.alpha ? __ldg(args.alpha + e) : 1.0f;
             args.h[(size_t)(off + tok0 + n) * F + ii] =
-                silu_f(ldexpf(sg[q], ex)) * ldexpf(su[q], ex);
+                silu_f(al * ldexpf(sg[q], ex)) * (al * ldexpf(su[q], ex));
           }
         }
       }
@@ -330,6 +332,7 @@ struct DownArgs {
   const int32_t* active;
   const int32_t* n_active;
   float* partial;
+  const float* alpha = nullptr;   // [E] per-expert second-level weight scale, or none
 };
 
 // Persistent like the gate/up kernel: unit = (active expert, 128 output rows), two weight
@@ -458,7 +461,8 @@ __global__ void __launch_bounds__(256, 2) down_kernel(const DownArgs args) {
         const int n = 2 * c + (q & 1);
         const int r = r0 + rw + 8 * (q >> 1);
         if (n < live)
-          args.partial[(size_t)(off + tok0 + n) * H + r] = ldexpf(acc[q], args.he[off + tok0 + n]);
+          args.partial[(size_t)(off + tok0 + n) * H + r] =
+              (args.alpha ? __ldg(args.alpha + e) : 1.0f) * ldexpf(acc[q], args.he[off + tok0 + n]);
       }
       __syncthreads();
     }
@@ -537,6 +541,7 @@ struct GuTmaArgs {
   const int32_t* n_active;
   float* h;
   uint32_t* err;
+  const float* alpha = nullptr;   // [E] per-expert second-level weight scale, or none
 };
 
 __host__ __device__ constexpr int gu_stage_bytes(int nb) {
@@ -708,7 +713,9 @@ gate_up_tma_kernel(const __grid_constant__ CUtensorMap tmap_c, const __grid_cons
           if (n < live) {
             const int pos = off + tok0 + n;
             const int ex = args.xe[pos];
-            args.h[(size_t)pos * F + i0 + g] = silu_f(ldexpf(acc[qq], ex)) * ldexpf(acc[2 + qq], ex);
+            const float al = args.alpha ? __ldg(args.alpha + e) : 1.0f;
+            args.h[(size_t)pos * F + i0 + g] =
+                silu_f(al * ldexpf(acc[qq], ex)) * (al * ldexpf(acc[2 + qq], ex));
           }
         }
       }
@@ -737,6 +744,7 @@ struct DnTmaArgs {
   const int32_t* n_active;
   float* partial;
   uint32_t* err;
+  const float* alpha = nullptr;   // [E] per-expert second-level weight scale, or none
 };
 
 __host__ __device__ constexpr int dn_stage_bytes(int F) {
@@ -884,7 +892,8 @@ down_tma_kernel(const DnTmaArgs args) {
           const int n = 2 * c + (qq & 1);
           if (n < live) {
             const int pos = off + tok0 + n;
-            args.partial[(size_t)pos * H + r0 + g + 8 * (qq >> 1)] = ldexpf(acc[qq], args.he[pos]);
+            args.partial[(size_t)pos * H + r0 + g + 8 * (qq >> 1)] =
+                (args.alpha ? __ldg(args.alpha + e) : 1.0f) * ldexpf(acc[qq], args.he[pos]);
           }
         }
       }
@@ -946,6 +955,7 @@ cudaError_t launch_decode_gate_up(const uint16_t* x_bf16, int T, int H, int F, i
         make_map4(&ms, b.scales, sdims, sstr, sbox, false)) {
       GuTmaArgs ta{xg, xe, H, F, nh, nb, csr.expert_offsets, csr.active_experts, csr.n_active,
                    reinterpret_cast<float*>(ws + L.h), reinterpret_cast<uint32_t*>(ws + L.error_word)};
+      ta.alpha = b.alpha;
       auto gk = nb == 1 ? gate_up_tma_kernel<1> : gate_up_tma_kernel<2>;
       st = cudaFuncSetAttribute(gk, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)smem);
@@ -961,6 +971,7 @@ cudaError_t launch_decode_gate_up(const uint16_t* x_bf16, int T, int H, int F, i
   }
   GateUpArgs a{xg, xe, b.codes, b.scales, H, F, csr.expert_offsets, csr.active_experts,
                csr.n_active, reinterpret_cast<float*>(ws + L.h)};
+  a.alpha = b.alpha;
   const long long max_units = (long long)(P < b.E ? P : b.E) * (F / 16);
   const size_t wbytes = (32 * (size_t)(H / 2) + 32 * (size_t)(H / 16) + 127) & ~size_t(127);
   const size_t smem = 2 * wbytes + 8 * 32 * 8 * sizeof(float);
@@ -995,6 +1006,7 @@ cudaError_t launch_decode_down(const moe_nvfp4_bank& b, moe_csr csr, int T, int 
       DnTmaArgs ta{hg, he, b.codes, b.scales, H, F, csr.expert_offsets, csr.active_experts,
                    csr.n_active, reinterpret_cast<float*>(ws + L.partial),
                    reinterpret_cast<uint32_t*>(ws + L.error_word)};
+      ta.alpha = b.alpha;
       st = cudaFuncSetAttribute(down_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (st != cudaSuccess) return st;
       long long grid = sm_count();
@@ -1005,6 +1017,7 @@ cudaError_t launch_decode_down(const moe_nvfp4_bank& b, moe_csr csr, int T, int 
   }
   DownArgs a{hg, he, b.codes, b.scales, H, F, csr.expert_offsets, csr.active_experts,
              csr.n_active, reinterpret_cast<float*>(ws + L.partial)};
+  a.alpha = b.alpha;
   const long long max_units = (long long)(P < b.E ? P : b.E) * (H / 128);
   const size_t wbytes = (128 * (size_t)(F / 2) + 128 * (size_t)(F / 16) + 127) & ~size_t(127);
   const size_t smem = 2 * wbytes + 8 * (size_t)(F * 2 + 16);

@@ -105,6 +105,7 @@ struct GemmArgs {
   int P, K, rows_per_expert, n_tiles_n, out_cols, F, down_shift;
   int b_sf_group;               // DOWN: g rows of the weight-scale plane per tensor-map row
   int n_base;                   // first N-tile of this launch (output columns are relative to it)
+  const float* alpha = nullptr; // [E] per-expert second-level weight scale, or none
 };
 
 // Scale factors reach shared memory through TMA, as row-major staging images beside the
@@ -363,6 +364,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
       // x * 2^sx is one exact-power-of-two multiply when 2^sx is a float, else ldexpf
       const bool fast = sx >= -149 && sx <= 127;
       const float m = fast ? pow2f(sx) : 0.0f;
+      const float al = args.alpha ? __ldg(args.alpha + tile.z) : 1.0f;
       if (!mbar_wait_warp(&acc_full[ab], (tcount >> 1) & 1, abort_flag, args.err)) break;
       tc_fence_after();
       const uint32_t acc = acc_col + ab * BN + lane_base;
@@ -378,8 +380,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
             float o[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const float gg = fast ? g[i + q] * m : ldexpf(g[i + q], sx);
-              const float uu = fast ? u[i + q] * m : ldexpf(u[i + q], sx);
+              const float gg = al * (fast ? g[i + q] * m : ldexpf(g[i + q], sx));
+              const float uu = al * (fast ? u[i + q] * m : ldexpf(u[i + q], sx));
               o[q] = silu_f(gg) * uu;
             }
             *reinterpret_cast<float4*>(orow + half * 32 + i) = make_float4(o[0], o[1], o[2], o[3]);
@@ -399,8 +401,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
               uint32_t pk[4];
 #pragma unroll
               for (int q = 0; q < 4; ++q) {
-                const float a0 = fast ? v[c][i + 2 * q] * m : ldexpf(v[c][i + 2 * q], sx);
-                const float a1 = fast ? v[c][i + 2 * q + 1] * m : ldexpf(v[c][i + 2 * q + 1], sx);
+                const float a0 = al * (fast ? v[c][i + 2 * q] * m : ldexpf(v[c][i + 2 * q], sx));
+                const float a1 = al * (fast ? v[c][i + 2 * q + 1] * m : ldexpf(v[c][i + 2 * q + 1], sx));
                 const __half2 h2 = __floats2half2_rn(a0, a1);
                 pk[q] = *reinterpret_cast<const uint32_t*>(&h2);
               }
@@ -470,6 +472,7 @@ cudaError_t launch_prefill_gate_up(const uint16_t* x_bf16, int T, int H, int F, 
     return cudaErrorInvalidValue;
   GemmArgs a{qe, tiles, ws + L.h, reinterpret_cast<uint32_t*>(ws + L.error_word),
              P, H, 2 * F, F / (BN / 2), F, F, 0, 1, 0};
+  a.alpha = b.alpha;
   const int max_tiles = P / 128 + (P < b.E ? P : b.E) + 1;
   return run_gemm<BN, true>(ma, mb, msa, msb, a, max_tiles, s);
 }
@@ -509,6 +512,7 @@ cudaError_t launch_prefill_down(const moe_nvfp4_bank& b, moe_csr csr, const floa
   // was measured slower: every extra GEMM launch costs more than the HBM round trip saves)
   GemmArgs a{qe, reinterpret_cast<const int32_t*>(ws + L.tiles), ws + L.partial,
              reinterpret_cast<uint32_t*>(ws + L.error_word), P, F, H, H / BN, H, F, shift, g, 0};
+  a.alpha = b.alpha;
   if ((st = run_gemm<BN, false>(ma, mb, msa, msb, a, max_tiles, s)) != cudaSuccess) return st;
   return launch_prefill_combine(w, T, H, F, k, 0, H, L, ws, y, s);
 }

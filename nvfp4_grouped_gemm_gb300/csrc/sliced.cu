@@ -84,6 +84,7 @@ struct SlicedArgs {
   int F;                       // gate/up: row offset of the up rows; down: unused
   int a_sf_group;              // down: g weight-scale rows per tensor-map row
   int sb_w;                    // bytes per slice-scale staging row: min(16*KSUB, scale pitch)
+  const float* alpha = nullptr;   // [E] per-expert second-level weight scale, or none
 };
 
 __device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&a)[32]) {
@@ -339,6 +340,11 @@ sliced_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
         for (int s = 0; s < 4; ++s) a += ldexpf(v[4 * p + s], __shfl_sync(0xffffffffu, ex, 4 * p + s));
         z[p] = a;
       }
+      if (args.alpha) {
+        const float al = __ldg(args.alpha + tile.z);
+#pragma unroll
+        for (int p = 0; p < 8; ++p) z[p] *= al;
+      }
       const int np = tile.y >> 2;                           // pairs in the tile
       const int pos0 = tile.x >> 2;                         // CSR row of the tile's first pair
       if (GATE_UP) {
@@ -425,6 +431,7 @@ cudaError_t launch_sliced_gate_up(const uint16_t* x_bf16, int T, int H, int F, i
     return cudaErrorInvalidValue;
   SlicedArgs a{qe, tiles, reinterpret_cast<float*>(ws + L.h),
                reinterpret_cast<uint32_t*>(ws + L.error_word), H, 2 * F, F / 64, F, F, 1, sbw};
+  a.alpha = b.alpha;
   const int max_tiles = (int)(rows / kSliceTile) + (P < b.E ? P : b.E) + 1;
   return run_sliced<true>(ma, mb, msa, msb, a, max_tiles, s);
 }
@@ -460,6 +467,7 @@ cudaError_t launch_sliced_down(const moe_nvfp4_bank& b, moe_csr csr, int T, int 
   SlicedArgs a{qe, reinterpret_cast<const int32_t*>(ws + L.tiles),
                reinterpret_cast<float*>(ws + L.partial),
                reinterpret_cast<uint32_t*>(ws + L.error_word), F, H, H / 128, H, F, g, sbw};
+  a.alpha = b.alpha;
   const int max_tiles = (int)(rows / kSliceTile) + (P < b.E ? P : b.E) + 1;
   return run_sliced<false>(ma, mb, msa, msb, a, max_tiles, s);
 }

@@ -124,6 +124,16 @@ class FFNResult:
     h_used: Optional[np.ndarray] = None  # the h fed to the down projection, [P, F]
 
 
+def _expert_weights(bank, e: int) -> np.ndarray:
+    """Expert e's weights in float64: E2M1(code) x UE4M3(scale), times the bank's per-expert
+    second-level scale alpha[e] when it has one.  The pages name "ModelOpt group-16" NVFP4
+    checkpoints (page 4, setup), whose weights carry such a float32 scale per tensor; they
+    never print it, so a bank without alpha means alpha = 1."""
+    wt = nvfp4.dequant(bank.codes[e], bank.scales[e])
+    alpha = getattr(bank, "alpha", None)
+    return wt if alpha is None else wt * float(np.float32(alpha[e]))
+
+
 def ffn(x_bits: np.ndarray, ids: np.ndarray, w: np.ndarray, gate_up, down,
         mode: str = "decode", tokens: Optional[np.ndarray] = None,
         qh_override: Optional[tuple] = None) -> FFNResult:
@@ -177,7 +187,7 @@ def ffn(x_bits: np.ndarray, ids: np.ndarray, w: np.ndarray, gate_up, down,
     for e in np.unique(flat_ids[sel]):
         pe = sel[flat_ids[sel] == e]                       # this expert's pairs, ascending p
         a = a_tok[pe // k]                                  # [m, H]
-        wgu = nvfp4.dequant(gate_up.codes[e], gate_up.scales[e])   # [2F, H]
+        wgu = _expert_weights(gate_up, e)                           # [2F, H]
         wg, wu = wgu[:F], wgu[F:]
         g = a @ wg.T
         u = a @ wu.T
@@ -197,7 +207,7 @@ def ffn(x_bits: np.ndarray, ids: np.ndarray, w: np.ndarray, gate_up, down,
         else:
             hq = h
         h_used[pe] = hq
-        wd = nvfp4.dequant(down.codes[e], down.scales[e])           # [H, F]
+        wd = _expert_weights(down, e)                               # [H, F]
         z[pe] = hq @ wd.T
         s_abs[pe] = np.abs(hq) @ np.abs(wd).T
     y = np.zeros((T, H))
@@ -331,6 +341,6 @@ def prefill_allowance(res: FFNResult, amb: QAmbiguity, down, ids: np.ndarray,
             if not 0 <= e < E or not amb.flagged[p].any():
                 continue
             idx = np.nonzero(amb.flagged[p])[0]
-            wd = np.abs(nvfp4.dequant(down.codes[e], down.scales[e]))[:, idx]
+            wd = np.abs(_expert_weights(down, e))[:, idx]
             extra[t] += abs(float(w[t, j])) * (wd @ amb.delta[p, idx])
     return extra

@@ -43,9 +43,11 @@ SCALE_HI = 0x30  # UE4M3 encoding of 0.5
 
 @dataclasses.dataclass
 class Bank:
-    """One NVFP4 weight bank, planar: codes [E, rows, in_f//2], scales [E, rows, in_f//16]."""
+    """One NVFP4 weight bank, planar: codes [E, rows, in_f//2], scales [E, rows, in_f//16],
+    and optionally alpha [E] float32 (a per-expert second-level scale)."""
     codes: np.ndarray
     scales: np.ndarray
+    alpha: Optional[np.ndarray] = None
 
     @property
     def E(self) -> int:

@@ -161,6 +161,22 @@ def test_interleaved_banks_import_bit_exact_and_run_the_same_layer():
     assert np.array_equal(y_imp, y_ref)
 
 
+@pytest.mark.parametrize("shape", ["decode_T8", "sliced"])
+def test_per_expert_alpha(shape):
+    """Banks with a per-expert float32 second-level scale alpha (both decode forms)."""
+    if shape == "decode_T8":
+        wl = synth.decode(8)
+    else:
+        wl = synth.logits_workload("alpha_sliced", 32, 256, 128, 16, 8, seed=8)
+        assert wl.P >= moe.decode_tensor_core_min_pairs()
+    rng = np.random.default_rng(12)
+    for bank in (wl.gate_up, wl.down):
+        bank.alpha = rng.uniform(0.25, 1.75, size=bank.E).astype(np.float32)
+    run = run_layer(wl)
+    assert run.err == 0
+    _check_layer(wl, run)
+
+
 def test_single_token_single_expert():
     """k = 1, T = 1: the smallest layer."""
     wl = synth.tiny(seed=3)

@@ -148,6 +148,17 @@ def test_prefill_numerics_at_decode_sizes(T):
     res, info = _stages(wl, run, np.arange(T))
 
 
+def test_prefill_per_expert_alpha():
+    """Prefill with a per-expert second-level scale alpha on both banks (down's <= 2)."""
+    wl = synth.prefill(seed=3, T=256)
+    rng = np.random.default_rng(13)
+    wl.gate_up.alpha = rng.uniform(0.25, 1.75, size=wl.E).astype(np.float32)
+    wl.down.alpha = rng.uniform(0.25, 1.75, size=wl.E).astype(np.float32)
+    run = run_layer(wl, path=PF)
+    assert run.err == 0
+    _stages(wl, run, np.arange(0, 256, 41))
+
+
 def test_prefill_full_size_sampled():
     """The prefill workload at full size (4096 tokens, 32768 pairs, 288 experts)."""
     wl = synth.prefill()

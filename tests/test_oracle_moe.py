@@ -239,3 +239,27 @@ def test_four_residual_slices_stay_far_inside_the_decode_tolerance():
 
     assert layer(4).max() < 0.05
     assert layer(1).max() > 1.0
+
+
+def test_alpha_power_of_two_equals_scaled_block_scales():
+    """A per-expert second-level scale alpha = 2^j gives the same weights as raising every
+    UE4M3 block scale of that expert by j binades (+8j in the encoding, exact while the scale
+    stays a normal UE4M3 value): the oracle's y is identical bit for bit."""
+    wl = synth.tiny(seed=5)
+    ids, w = oracle.route_topk(wl.logits, wl.k)
+    j = np.array([1, 2, 0, 1] * (wl.E // 4))
+    alpha = (2.0 ** j).astype(np.float32)
+
+    def with_alpha(bank):
+        return synth.Bank(bank.codes, bank.scales, alpha=alpha)
+
+    def folded(bank):
+        s = bank.scales.astype(np.int64) + 8 * j[:, None, None]
+        assert s.max() <= 0x7E and bank.scales.min() >= 0x08
+        return synth.Bank(bank.codes, s.astype(np.uint8))
+
+    a = oracle.ffn(wl.x_bits, ids, w, with_alpha(wl.gate_up), with_alpha(wl.down))
+    f = oracle.ffn(wl.x_bits, ids, w, folded(wl.gate_up), folded(wl.down))
+    assert np.array_equal(a.y, f.y) and np.array_equal(a.tsum, f.tsum)
+    plain = oracle.ffn(wl.x_bits, ids, w, wl.gate_up, wl.down)
+    assert not np.allclose(a.y, plain.y)
