@@ -552,8 +552,11 @@ def run_ours(args):
         "metric": metric_name(args.workload), "value": value, "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "nvfp4 weights (e2m1 x ue4m3) * f16 activations, f32 accumulate" if not prefill
-                 else "nvfp4 x nvfp4 block-scaled (e2m1, ue4m3), f32 accumulate",
+        "dtype": ("nvfp4 x nvfp4 block-scaled (e2m1, ue4m3), f32 accumulate" if prefill else
+                  "nvfp4 weights x 4 residual nvfp4 slices of each activation row, block-scaled "
+                  "tensor cores, f32 accumulate"
+                  if wl.P >= moe.decode_tensor_core_min_pairs() else
+                  "nvfp4 weights (e2m1 x ue4m3) * f16 activations, f32 accumulate"),
         "data": "synthetic",
         "config": {"workload": workload_desc(wl),
                    "l2": "flushed before every step (512 MiB write, then 512 MiB read)",
