@@ -555,7 +555,9 @@ __device__ __forceinline__ uint32_t gu_scale_off(int nb, int kbox, int mat, int 
   return 2 * nb * 1024 + kbox * 256 + mat * 128 + row * 16;
 }
 
-template <int NB>
+// ALPHA: the bank has per-expert second-level scales (a separate instance, so the common
+// case keeps every register for the K loop).
+template <int NB, bool ALPHA>
 __global__ void __launch_bounds__(32 * (kTmaProd + kTmaWarps), 1)
 gate_up_tma_kernel(const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_s,
                    const GuTmaArgs args) {
@@ -713,7 +715,7 @@ gate_up_tma_kernel(const __grid_constant__ CUtensorMap tmap_c, const __grid_cons
           if (n < live) {
             const int pos = off + tok0 + n;
             const int ex = args.xe[pos];
-            const float al = args.alpha ? __ldg(args.alpha + e) : 1.0f;
+            const float al = ALPHA ? __ldg(args.alpha + args.active[u / nrb]) : 1.0f;
             args.h[(size_t)pos * F + i0 + g] =
                 silu_f(al * ldexpf(acc[qq], ex)) * (al * ldexpf(acc[2 + qq], ex));
           }
@@ -956,7 +958,8 @@ cudaError_t launch_decode_gate_up(const uint16_t* x_bf16, int T, int H, int F, i
       GuTmaArgs ta{xg, xe, H, F, nh, nb, csr.expert_offsets, csr.active_experts, csr.n_active,
                    reinterpret_cast<float*>(ws + L.h), reinterpret_cast<uint32_t*>(ws + L.error_word)};
       ta.alpha = b.alpha;
-      auto gk = nb == 1 ? gate_up_tma_kernel<1> : gate_up_tma_kernel<2>;
+      auto gk = b.alpha ? (nb == 1 ? gate_up_tma_kernel<1, true> : gate_up_tma_kernel<2, true>)
+                        : (nb == 1 ? gate_up_tma_kernel<1, false> : gate_up_tma_kernel<2, false>);
       st = cudaFuncSetAttribute(gk, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)smem);
       if (st != cudaSuccess) return st;
