@@ -43,8 +43,10 @@
  * NVFP4 bank layout (planar, row-major):
  *   codes  u8 [E][rows][in_f/2]  two E2M1 codes per byte, low nibble = even element
  *   scales u8 [E][rows][in_f/16] one UE4M3 byte per 16 consecutive elements of a row
- *   value(e, r, c) = E2M1(code) * UE4M3(scale[e][r][c/16]); scale bytes must be <= 0x7E.
- *   Both planes must be 16-byte aligned.
+ *   value(e, r, c) = E2M1(code) * UE4M3(scale[e][r][c/16]) (* alpha[e] when the bank has a
+ *   per-expert second-level scale); scale bytes must be <= 0x7E.
+ *   Both planes must be 16-byte aligned. Banks stored as the pages' interleaved 36-byte
+ *   blocks convert with moe_nvfp4_from_interleaved.
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H
@@ -65,11 +67,15 @@ typedef enum moe_status {
   MOE_ERR_TIMEOUT = 5        /* a bounded device wait gave up (device error word) */
 } moe_status;
 
-/* Path selection: DECODE multiplies the exact bf16 activations by the dequantised
- * weights and keeps h in float32; PREFILL quantises x and h to NVFP4 (per-row power-of-two
- * scale, UE4M3 per 16, E2M1 codes; nearest-even) and runs block-scaled FP4 tensor-core
- * GEMMs. AUTO picks PREFILL when T*k >= moe_prefill_min_pairs(). The two paths differ
- * in numerics by design. */
+/* Path selection: DECODE keeps the bf16 activations and a float32 h. Below
+ * moe_decode_tensor_core_min_pairs() pairs it multiplies them exactly (as f16 with a
+ * power-of-two row prescale) by weights dequantised in registers. From that many pairs it
+ * writes each activation row as four residual NVFP4 slices for the block-scaled FP4
+ * tensor cores; the sum of the slices is the row to ~6^-4 of each 16-block's largest
+ * magnitude, far inside the tolerance. PREFILL quantises x and h to NVFP4 once (per-row
+ * power-of-two scale, UE4M3 per 16, E2M1 codes; nearest-even) and runs block-scaled FP4
+ * tensor-core GEMMs. AUTO picks PREFILL when T*k >= moe_prefill_min_pairs(). The paths
+ * differ in numerics by design. */
 enum { MOE_PATH_AUTO = 0, MOE_PATH_DECODE = 1, MOE_PATH_PREFILL = 2 };
 
 /* Bits of the device error word. */
