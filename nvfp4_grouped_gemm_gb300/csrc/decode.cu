@@ -490,18 +490,18 @@ combine_kernel(const float* __restrict__ w, const int32_t* __restrict__ pair_pos
   const int r = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
   if (r >= H) return;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  // the partial rows are loaded four pairs at a time and summed in ascending j
-  for (int j0 = 0; j0 < k; j0 += 4) {
-    float4 z[4];
+  // the partial rows are loaded eight pairs at a time and summed in ascending j
+  for (int j0 = 0; j0 < k; j0 += 8) {
+    float4 z[8];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < 8; ++q) {
       const int j = j0 + q;
       const int pos = j < k ? s_pos[j] : -1;
       z[q] = pos >= 0 ? __ldcs(reinterpret_cast<const float4*>(partial + (size_t)pos * H + r))
                       : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < 8; ++q) {
       const int j = j0 + q;
       if (j >= k || s_pos[j] < 0) continue;
       const float wj = s_w[j];

@@ -396,7 +396,7 @@ __global__ void __launch_bounds__(1024) slice_h_kernel(const float* __restrict__
 
 // combine for the prefill path: y[t, :] = sum_j w[t, j] * f32(z16[pos_j, :]) * 2^(e_j + cF)
 // The token's k positions and scaled weights are read once into shared memory; the
-// partial rows are then loaded four pairs at a time and summed in ascending j.
+// partial rows are then loaded eight pairs at a time and summed in ascending j.
 // Columns [c0, c0 + HS) of y from a partial slice [P][HS].
 __global__ void __launch_bounds__(256)
 combine_f16_kernel(const float* __restrict__ w, const int32_t* __restrict__ pair_pos,
@@ -414,17 +414,17 @@ combine_f16_kernel(const float* __restrict__ w, const int32_t* __restrict__ pair
   const int r = (blockIdx.x * blockDim.x + threadIdx.x) * 8;   // column within the slice
   if (r >= HS) return;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int j0 = 0; j0 < k; j0 += 4) {
-    uint4 z[4];
+  for (int j0 = 0; j0 < k; j0 += 8) {
+    uint4 z[8];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < 8; ++q) {
       const int j = j0 + q;
       const int pos = j < k ? s_pos[j] : -1;
       z[q] = pos >= 0 ? __ldcs(reinterpret_cast<const uint4*>(partial + (size_t)pos * HS + r))
                       : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < 8; ++q) {
       const int j = j0 + q;
       if (j >= k || s_pos[j] < 0) continue;
       const float wj = s_w[j];
