@@ -1,4 +1,6 @@
-// Decode path: few pairs per expert, memory-bound on the NVFP4 weight bytes.
+// Decode path below the tensor-core switch (fewer than moe_decode_tensor_core_min_pairs()
+// pairs; from there on sliced.cu): few pairs per expert, memory-bound on the NVFP4 weight
+// bytes.
 //
 // The grid is indexed by active expert, not by pair, so every active expert's rows are
 // streamed from HBM exactly once per call (the union-of-experts gather).  Kernels:
@@ -15,7 +17,11 @@
 //   h_prep_kernel     CSR row r of h (f32) -> f16 times 2^-e, as for x
 //   down_kernel       CTA = (active expert, 128 output rows), weights and the expert's h
 //                     rows in shared memory, warp w owns 16 rows over the whole F
-//   combine_kernel    y[t] = sum_j w[t,j] z[pos(t,j)] in ascending j, no atomics
+//   gate_up_tma_kernel, down_tma_kernel   from 8 units per SM on: one CTA per SM, four
+//                     producer warps feed a TMA / bulk-copy ring, sixteen consumer warps
+//                     each multiply whole units (8 gate + 8 up rows, or 16 down rows)
+//   combine_kernel    y[t] = sum_j w[t,j] z[pos(t,j)] in ascending j, no atomics (also the
+//                     combine of the sliced form)
 //
 // FP4 codes are dequantised in registers (cvt.rn.f16x2.e2m1x2, times the UE4M3 scale via
 // cvt.rn.f16x2.e4m3x2: every product has <= 6 significant bits, exact in f16) and fed

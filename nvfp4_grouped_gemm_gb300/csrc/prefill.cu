@@ -76,17 +76,7 @@ __global__ void __launch_bounds__(1024) tiles_kernel(const int32_t* __restrict__
   if (threadIdx.x == 0) tiles[0] = scratch[31];
 }
 
-// ---------------------------------------------------------------------------
-// PTX wrappers: mbarrier, TMA, cp.async, tcgen05
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void cp_async4(void* dst, const void* src, bool valid) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;"
-               ::"r"(smem_u32(dst)), "l"(src), "r"(valid ? 4 : 0) : "memory");
-}
-__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
+// (mbarrier and TMA wrappers: tma_sync.cuh; tcgen05 wrappers: tcgen05.cuh)
 
 // ---------------------------------------------------------------------------
 // grouped block-scaled GEMM

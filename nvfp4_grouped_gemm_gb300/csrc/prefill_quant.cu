@@ -1,8 +1,10 @@
-// Prefill activations and combine:
+// Activation quantisers and the prefill combine:
 //
 //   quant_x_kernel      Q(x): each token's bf16 row to NVFP4 with a power-of-two row scale,
 //                       written to every CSR row of the token's pairs
 //   quant_h_kernel      Q(h) per CSR row
+//   slice_x_kernel, slice_h_kernel   the decode tensor-core form's four residual slices
+//                       of each x row (per token, written to its pairs' rows) and h row
 //   combine_f16_kernel  y[t] = sum_j w[t,j] * z16[pos_j] * 2^(e_j + c_F), ascending j
 //
 // The quantiser Q (the pages never quantise activations; block-scaled FP4 x FP4 needs it):
