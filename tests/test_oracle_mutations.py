@@ -120,3 +120,37 @@ def test_planted_silu_sign_is_caught(monkeypatch):
     monkeypatch.setattr(moe, "silu", lambda g: g / (1.0 + np.exp(g)))
     with pytest.raises(AssertionError):
         tm.test_ffn_matches_brute_force_tiny()
+
+
+def test_planted_interleaved_order_swap_is_caught(monkeypatch, golden_dir):
+    """Codes read before the scales in a 36-byte block."""
+    def bad(blob, in_f):
+        b = np.asarray(blob, np.uint8)
+        nblk = in_f // 64
+        r = b.reshape(b.shape[:-1] + (nblk, 36))
+        return (r[..., :32].reshape(b.shape[:-1] + (in_f // 2,)).copy(),
+                r[..., 32:].reshape(b.shape[:-1] + (in_f // 16,)).copy())
+    monkeypatch.setattr(nvfp4, "from_interleaved", bad)
+    with pytest.raises(AssertionError):
+        fmt.test_interleaved_block_import_matches_hand_written_fixture(golden_dir)
+
+
+def test_planted_ignored_alpha_is_caught(monkeypatch):
+    """The per-expert second-level scale dropped from the weights."""
+    monkeypatch.setattr(moe, "_expert_weights",
+                        lambda bank, e: nvfp4.dequant(bank.codes[e], bank.scales[e]))
+    with pytest.raises(AssertionError):
+        tm.test_alpha_power_of_two_equals_scaled_block_scales()
+
+
+def test_planted_alpha_applied_twice_is_caught(monkeypatch):
+    """The per-expert scale applied to the weights twice."""
+    orig = moe._expert_weights
+
+    def bad(bank, e):
+        alpha = getattr(bank, "alpha", None)
+        w = orig(bank, e)
+        return w if alpha is None else w * float(alpha[e])
+    monkeypatch.setattr(moe, "_expert_weights", bad)
+    with pytest.raises(AssertionError):
+        tm.test_alpha_power_of_two_equals_scaled_block_scales()
