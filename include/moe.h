@@ -133,8 +133,10 @@ typedef struct moe_ws_layout {
 
 /* Limits (MOE_ERR_UNSUPPORTED beyond them): 1 <= k <= min(E, 32); E <= 1024;
  * H % 256 == 0 and H <= 4096; F % 64 == 0; T*k < 2^31 / max(H, F); F <= 1408 on the
- * DECODE path and F <= 4096 on the PREFILL path (the path AUTO resolves to counts;
- * moe_workspace_bytes returns 0 for such sizes). */
+ * DECODE path, and from moe_decode_tensor_core_min_pairs() pairs on also F not in
+ * {1088, 1216, 1344} (their weight-scale rows do not fit the down GEMM's staging); F <= 4096
+ * on the PREFILL path (the path AUTO resolves to counts; moe_workspace_bytes returns 0 for
+ * such sizes). */
 
 /* Workspace size in bytes for one layer with these sizes (0 if the sizes are invalid). */
 size_t moe_workspace_bytes(int32_t T, int32_t H, int32_t F, int32_t E, int32_t k, int32_t path);

@@ -56,11 +56,25 @@ int resolve_path(int T, int k, int path) {
 }
 
 // The per-path limit on F (the path AUTO resolves to for these sizes).
+// The sliced down GEMM stages each weight row's F/16 scale bytes whole, through a tensor
+// map whose rows are g consecutive scale rows (g the smallest power of two with g*F/16 a
+// multiple of 16 and at least 32 bytes); a tensor-map box row holds at most 256 bytes.
+bool sliced_down_supported(int F) {
+  const int sfrow = F / 16;
+  int g = 1;
+  if (sfrow % 16 != 0)
+    for (g = 2; (g * sfrow) % 16 != 0 || g * sfrow < 32; g *= 2) {
+    }
+  return 128 % g == 0 && g * sfrow <= 256 && 128 * sfrow <= 11264;
+}
+
 moe_status path_supported(int T, int F, int k, int path) {
   if (path != MOE_PATH_AUTO && path != MOE_PATH_DECODE && path != MOE_PATH_PREFILL)
     return MOE_ERR_INVALID_ARG;
   const int p = resolve_path(T, k, path);
   if (p == MOE_PATH_DECODE && F > kDecodeMaxF) return MOE_ERR_UNSUPPORTED;
+  if (p == MOE_PATH_DECODE && decode_sliced((long long)T * k) && !sliced_down_supported(F))
+    return MOE_ERR_UNSUPPORTED;                    // F = 1088, 1216, 1344
   if (p == MOE_PATH_PREFILL && F > kPrefillMaxF) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }

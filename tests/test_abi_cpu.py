@@ -66,6 +66,12 @@ def test_workspace_layout_host_logic(lib):
     assert moe.workspace_bytes(4, H, 1472, E, k, moe.PATH_DECODE) == 0
     assert moe.workspace_bytes(4, H, 1472, E, k, moe.PATH_PREFILL) > 0
     assert moe.workspace_bytes(4, H, 4160, E, k, moe.PATH_PREFILL) == 0
+    # the tensor-core decode form (from 256 pairs) cannot stage F = 1088, 1216, 1344
+    for f in range(64, 1409, 64):
+        small = moe.workspace_bytes(4, H, f, E, k, moe.PATH_DECODE)
+        wide = moe.workspace_bytes(64, H, f, E, k, moe.PATH_DECODE)
+        assert small > 0
+        assert (wide == 0) == (f in (1088, 1216, 1344)), f
 
 
 def test_path_resolution(lib):
