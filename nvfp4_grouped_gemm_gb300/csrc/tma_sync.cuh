@@ -57,7 +57,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
-// Warp-wide bounded wait: lane 0 polls, the verdict is broadcast (keeps the polling
+// Warp-wide bounded wait: lane 0 polls, the result is broadcast (keeps the polling
 // traffic on the shared-memory pipe 32x lower than every lane spinning).
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
                                                volatile int* abort_flag, uint32_t* err) {
