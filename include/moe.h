@@ -84,8 +84,8 @@ enum { MOE_DEVERR_EXPERT_ID = 1, MOE_DEVERR_TIMEOUT = 2 };
 /* One NVFP4 weight bank. gate_up: rows = 2F (gate rows 0..F-1, up rows F..2F-1),
  * in_f = H. down: rows = H, in_f = F. A weight is E2M1(code) x UE4M3(scale of its
  * 16-group), times alpha[e] when `alpha` is not NULL: an optional per-expert float32
- * second-level scale (the two-level scaling of ModelOpt NVFP4 checkpoints, "ModelOpt
- * group-16" on page 4; device array [E], finite, caller-owned). On the PREFILL path the
+ * second-level scale (the two-level scaling of the ModelOpt NVFP4 checkpoints page 4 runs;
+ * device array [E], finite, caller-owned). On the PREFILL path the
  * down bank's alpha must stay <= 2 (its f16 partials are scaled for |alpha| <= 2). */
 typedef struct moe_nvfp4_bank {
   const uint8_t* codes;
@@ -224,8 +224,9 @@ moe_status moe_build_expert_csr_static(const int32_t* topk_ids, int32_t T, int32
                                        moe_csr csr, void* stream);
 
 /* Weight-layout import (not on the per-layer path): rows stored the way the pages' banks
- * are ("moe_sk_repro.rs", mk_bank: 64 values per 36-byte block; "moe_sel_census.rs", BLK:
- * 4 UE4M3 sub-scales + 32 code bytes) into the planar planes this library reads. Each
+ * are (mk_bank of "moe_sk_repro.rs" gives every 64 weights a 36-byte block; the BLK
+ * constant of "moe_sel_census.rs" splits it into four UE4M3 scale bytes and thirty-two code
+ * bytes) into the planar planes this library reads. Each
  * row of in_f weights is in_f/64 blocks; a block is its 4 scale bytes (scale i for weights
  * 16i..16i+15 of the block) followed by its 32 code bytes (low nibble = even weight).
  * blob u8 [rows][in_f/64*36] (4-byte aligned) -> codes u8 [rows][in_f/2] (16-byte aligned),

@@ -126,9 +126,9 @@ class FFNResult:
 
 def _expert_weights(bank, e: int) -> np.ndarray:
     """Expert e's weights in float64: E2M1(code) x UE4M3(scale), times the bank's per-expert
-    second-level scale alpha[e] when it has one.  The pages name "ModelOpt group-16" NVFP4
-    checkpoints (page 4, setup), whose weights carry such a float32 scale per tensor; they
-    never print it, so a bank without alpha means alpha = 1."""
+    second-level scale alpha[e] when it has one.  Page 4's setup runs ModelOpt NVFP4
+    checkpoints with 16-weight groups, whose weights carry such a float32 scale per tensor;
+    the pages never print it, so a bank without alpha means alpha = 1."""
     wt = nvfp4.dequant(bank.codes[e], bank.scales[e])
     alpha = getattr(bank, "alpha", None)
     return wt if alpha is None else wt * float(np.float32(alpha[e]))

@@ -5,9 +5,9 @@ baseline may import this package; the product path never does.
 
 Formats (the weight value is E2M1 code x UE4M3 scale of its 16-group):
 
-* E2M1 ("E2M1 codes with one UE4M3 scale per 16 weights", "moe_sel_census.rs"
-  header constants, and "moe_union_probe.rs": a row is in_f/2 code bytes +
-  in_f/16 ue4m3 scale bytes).  4-bit code c: sign s = c>>3, exponent e =
+* E2M1 (4-bit codes with a UE4M3 scale for every group of 16 weights, per the
+  header constants of "moe_sel_census.rs"; "moe_union_probe.rs" counts a row as
+  in_f/2 code bytes plus in_f/16 UE4M3 scale bytes).  4-bit code c: sign s = c>>3, exponent e =
   (c>>1)&3, mantissa m = c&1; value (-1)^s * (m/2 if e == 0 else (1+m/2)*2^(e-1)).
   Magnitudes {0, 0.5, 1, 1.5, 2, 3, 4, 6}; code 8 is -0.
 * UE4M3 scale byte b (bit 7 must be 0, 0x7F is NaN and rejected): e = (b>>3)&15,
@@ -199,9 +199,10 @@ def dequant_q(codes: np.ndarray, scales: np.ndarray, s: np.ndarray) -> np.ndarra
 def from_interleaved(blob: np.ndarray, in_f: int):
     """Planar (codes, scales) of rows stored as 36-byte blocks per 64 weights.
 
-    The pages' own banks use this storage: "NVFP4 stores 64 values per 36-byte block"
-    ("moe_sk_repro.rs", `fn main`, `mk_bank`, row bytes in_f / 64 * 36) and "4 UE4M3
-    sub-scales + 32 code bytes" per block ("moe_sel_census.rs", constant `BLK`).  Reading
+    The pages' own banks use this storage: `mk_bank` in `fn main` of "moe_sk_repro.rs"
+    sizes a row at 36 bytes for every 64 weights (row bytes in_f / 64 * 36), and the
+    `BLK` constant of "moe_sel_census.rs" splits such a block into four UE4M3 scale bytes
+    and thirty-two code bytes.  Reading
     of the order the pages leave open: the block's 4 scale bytes come first (scale i
     covers weights 16i .. 16i+15 of the block), then its 32 code bytes (two codes per
     byte, low nibble = even weight, as in the planar layout).

@@ -135,7 +135,8 @@ def test_ffn_invariant_under_pair_order_and_expert_relabel():
 
 def test_ffn_split_tokens_invariance():
     """Computing two halves of the batch separately gives the same rows (page 4's
-    "shared N160 + N160 versus full N320" check, read as a split of the batch)."""
+    numeric-check table compares a 320-row batch run as two 160-row halves with the
+    whole; read as a split of the batch)."""
     w = synth.decode(T=4)
     sub = synth.Bank(w.gate_up.codes, w.gate_up.scales)
     ids, ww = oracle.route_topk(w.logits, w.k)
