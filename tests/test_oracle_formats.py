@@ -217,3 +217,22 @@ def test_interleaved_block_import_matches_hand_written_fixture(golden_dir):
     assert w[64] == 0.5 / 64 and w[65] == 1.0 / 64 and w[80] == 0.5 / 32 and w[127] == 448.0
     with pytest.raises(ValueError):
         nvfp4.from_interleaved(rows["interleaved"][:70], 128)
+
+
+def test_quantize_power_of_two_and_sign_invariance():
+    """Q commutes with exact rescaling and negation: Q(2^j v) has v's codes and block scales
+    and row exponent s + j (the row scale is a power of two, so every decision is the same
+    comparison); Q(-v) flips exactly the sign bit of every code of a nonzero value."""
+    rng = np.random.default_rng(17)
+    v = rng.standard_normal((6, 64)) * np.exp2(rng.integers(-30, 30, size=(6, 1)))
+    v[0, :16] = 0.0                                         # a zero block
+    c0, s0, e0 = nvfp4.quantize(v)
+    for j in (-40, -3, 1, 7, 60):
+        c, s, e = nvfp4.quantize(np.ldexp(v, j))
+        assert np.array_equal(c, c0) and np.array_equal(s, s0) and np.array_equal(e, e0 + j)
+    cn, sn, en = nvfp4.quantize(-v)
+    assert np.array_equal(sn, s0) and np.array_equal(en, e0)
+    lo, hi = c0 & 0xF, c0 >> 4
+    nlo, nhi = cn & 0xF, cn >> 4
+    nz_lo, nz_hi = v[:, 0::2] != 0, v[:, 1::2] != 0
+    assert np.array_equal(nlo[nz_lo], lo[nz_lo] ^ 8) and np.array_equal(nhi[nz_hi], hi[nz_hi] ^ 8)
