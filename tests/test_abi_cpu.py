@@ -3,6 +3,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 import nvfp4_grouped_gemm_gb300 as moe
@@ -132,3 +133,27 @@ def test_kernel_launch_count_host_logic(lib):
     assert moe.kernel_launches(4096, 4096, 640, 288, 8) == 3 + 6
     assert moe.kernel_launches(4, 256, 64, 16, 2, moe.PATH_PREFILL) == 1 + 6
     assert moe.kernel_launches(0, 256, 64, 16, 2) == 0
+
+
+@pytest.mark.parametrize("path,rpp,tile_rows", [(moe.PATH_PREFILL, 1, 128), (moe.PATH_DECODE, 4, 32)])
+def test_tile_list_always_fits_its_workspace_region(lib, path, rpp, tile_rows):
+    """The M-tile list (a count, then one 16-byte record per tile) never outgrows the
+    workspace region the layout gives it: an expert with m pairs needs ceil(m*rpp/tile_rows)
+    tiles, at most m*rpp/tile_rows + 1, and at most min(E, P) experts are active."""
+    rng = np.random.default_rng(23)
+    H, F = 256, 64
+    for _ in range(200):
+        E = int(rng.integers(1, 1025))
+        k = int(rng.integers(1, min(E, 32) + 1))
+        T = int(rng.integers(1, 600))
+        if path == moe.PATH_DECODE and T * k < moe.decode_tensor_core_min_pairs():
+            T = (moe.decode_tensor_core_min_pairs() + k - 1) // k
+        P = T * k
+        L = moe.workspace_layout(T, H, F, E, k, path)
+        ends = sorted(v for n, v in L.items() if n != "total" and v > L["tiles"]) + [L["total"]]
+        region = ends[0] - L["tiles"]
+        skew = rng.uniform(0.5, 3.0)
+        ids = np.minimum((rng.uniform(size=P) ** skew * E).astype(np.int64), E - 1)
+        counts = np.bincount(ids, minlength=E)
+        tiles = int(np.sum((counts * rpp + tile_rows - 1) // tile_rows))
+        assert 16 + 16 * tiles <= region, (T, k, E, tiles, region)
