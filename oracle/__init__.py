@@ -11,12 +11,13 @@ and ``--impl reference`` legs may import it.  It shares no code with the CUDA
 library or its Python binding; the only module both sides use is ``synth``,
 which draws the seeded inputs and holds none of the method's arithmetic.
 
-Parity status: every function here has at least one external pin except the
-numerical values of the device's float32 accumulations, which are checked only
-to within the stated tolerance ("parity unpinned" beyond it), and the prefill
-quantisation band ``H_BAND``, which is derived from the float32 accumulation
-bound rather than pinned.
+Parity status: every function here has at least one external pin.  The
+numerical values of the device's float32 accumulations are checked to within
+the stated tolerance ("parity unpinned" beyond it); the prefill quantisation
+band (``moe.h_band``) models a float32 accumulation in 64-element K-steps and is
+pinned against a float32 emulation of that accumulation.
 """
 from . import nvfp4, moe  # noqa: F401
 from .moe import (route_topk, build_expert_csr, ffn, tolerance, unique_expert_bytes,  # noqa: F401
-                  useful_flops, qh_ambiguity, prefill_allowance, TOL_REL, TOL_ABS)
+                  useful_flops, qh_ambiguity, prefill_allowance, h_band, down_combine,
+                  accumulation_scale, TOL_REL, TOL_ABS)

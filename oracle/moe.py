@@ -122,6 +122,8 @@ class FFNResult:
     qx: Optional[tuple] = None  # prefill: Q(x) per token (codes, scales, s)
     qh: Optional[tuple] = None  # prefill: Q(f32(h)) per pair (codes, scales, s)
     h_used: Optional[np.ndarray] = None  # the h fed to the down projection, [P, F]
+    g_acc: Optional[np.ndarray] = None   # prefill: float64 [P, F] accumulation scale of g
+    u_acc: Optional[np.ndarray] = None   # prefill: float64 [P, F] accumulation scale of u
 
 
 def _expert_weights(bank, e: int) -> np.ndarray:
@@ -180,6 +182,8 @@ def ffn(x_bits: np.ndarray, ids: np.ndarray, w: np.ndarray, gate_up, down,
     ga = np.zeros((P, F))
     ua = np.zeros((P, F))
     h_used = np.zeros((P, F))
+    g_acc = np.zeros((P, F)) if mode == "prefill" else None
+    u_acc = np.zeros((P, F)) if mode == "prefill" else None
     qh_c = np.zeros((P, F // 2), np.uint8)
     qh_s = np.zeros((P, F // 16), np.uint8)
     qh_e = np.zeros(P, np.int64)
@@ -197,6 +201,8 @@ def ffn(x_bits: np.ndarray, ids: np.ndarray, w: np.ndarray, gate_up, down,
         h = silu(g) * u
         hh[pe] = h
         if mode == "prefill":
+            acc = accumulation_scale(a, wgu)
+            g_acc[pe], u_acc[pe] = acc[:, :F], acc[:, F:]
             if qh_override is not None:
                 c, s, ex = (qh_override[0][pe], qh_override[1][pe], qh_override[2][pe])
             else:
@@ -221,7 +227,31 @@ def ffn(x_bits: np.ndarray, ids: np.ndarray, w: np.ndarray, gate_up, down,
                 y[t] += wf[t, j] * z[p]
                 tsum[t] += abs(wf[t, j]) * s_abs[p]
     return FFNResult(y, tsum, z, s_abs, hh, gg, uu, ga, ua, qx=qx,
-                     qh=(qh_c, qh_s, qh_e) if mode == "prefill" else None, h_used=h_used)
+                     qh=(qh_c, qh_s, qh_e) if mode == "prefill" else None, h_used=h_used,
+                     g_acc=g_acc, u_acc=u_acc)
+
+
+def down_combine(h_used: np.ndarray, ids: np.ndarray, w: np.ndarray, down,
+                 tokens: np.ndarray):
+    """Steps 4-6 alone: z_p = W_down[e] h_used[p], y[t] = sum_j w[t, j] z_{t*k+j} in j order,
+    and the tolerance scale tsum, for given per-pair down-projection inputs h_used [P, F]
+    (pair order).  Returns (y, tsum), both float64 [T, H] (rows of other tokens zero)."""
+    T, k = ids.shape
+    E, H = down.codes.shape[0], down.codes.shape[1]
+    y = np.zeros((T, H))
+    tsum = np.zeros((T, H))
+    wd = {}
+    for t in np.asarray(tokens, dtype=np.int64):
+        for j in range(k):                                 # fixed j order
+            e = int(ids[t, j])
+            if not 0 <= e < E:
+                continue
+            if e not in wd:
+                wd[e] = _expert_weights(down, e)
+            hp = h_used[t * k + j]
+            y[t] += float(w[t, j]) * (wd[e] @ hp)
+            tsum[t] += abs(float(w[t, j])) * (np.abs(wd[e]) @ np.abs(hp))
+    return y, tsum
 
 
 def tolerance(tsum: np.ndarray, extra: Optional[np.ndarray] = None) -> np.ndarray:
@@ -248,11 +278,37 @@ def useful_flops(P: int, H: int, F: int) -> int:
 # Prefill: which Q(h) decisions a float32 device accumulation may take either way
 # ---------------------------------------------------------------------------
 
-# Bound on the relative error of a float32 accumulation of K products that a
-# tensor core performs in K/64 steps, one rounding of the running sum per step:
-# (K/64) * 2^-24 with K <= 4096 gives 2^-18; twice that leaves room for one more
-# rounding per step inside the instruction.
-H_BAND = 2.0 ** -17
+# The block-scaled FP4 tensor-core product consumes K in steps of 64 elements (one
+# instruction: four 16-element groups, each with its pair of UE4M3 scales) and adds each
+# step's sum into a float32 accumulator.  The products themselves are exact in float32
+# (an E2M1 x UE4M3 operand has at most 6 significant bits, a product of two at most 12).
+ACC_STEP = 64
+# Roundings charged per step: one of the step's own sum and one of the running sum, each at
+# most 2^-24 of the rounded magnitude (round to nearest).  This is an assumption about the
+# device's arithmetic; the tests pin it against a float32 emulation of the accumulation and
+# check the device's h against it.
+ACC_ROUNDINGS = 2
+UNIT_ROUNDOFF = 2.0 ** -24
+
+
+def accumulation_scale(a: np.ndarray, w: np.ndarray, step: int = ACC_STEP) -> np.ndarray:
+    """Sum over the K-steps of |S_j| + |A_j| for every dot product a[m] . w[n].
+
+    S_j is the exact sum of step j's products and A_j = S_1 + ... + S_j the exact running
+    sum after it.  A float32 accumulation that rounds each S_j and each A_j once (round to
+    nearest) is off the exact dot product by at most 2^-24 times this scale, to first order.
+    a [m, K], w [n, K] (float64, exact operand values), K a multiple of `step`; returns
+    [m, n].
+    """
+    m, K = a.shape
+    n = w.shape[0]
+    if K % step:
+        raise ValueError("K must be a multiple of the accumulation step")
+    J = K // step
+    # S[j] = a[:, step j] @ w[:, step j].T, one matrix product per step
+    S = np.matmul(a.reshape(m, J, step).transpose(1, 0, 2), w.reshape(n, J, step).transpose(1, 2, 0))
+    A = np.cumsum(S, axis=0)
+    return np.abs(S).sum(axis=0) + np.abs(A).sum(axis=0)
 
 
 @dataclasses.dataclass
@@ -260,6 +316,7 @@ class QAmbiguity:
     flagged: np.ndarray        # bool [P, F]: some Q decision for the element lies within the band
     delta: np.ndarray          # float64 [P, F]: bound on |deq(Q(h')) - deq(Q(h))| where flagged
     band: np.ndarray           # float64 [P, F]: the error band eps_i assumed for h_i
+    zero_sign: np.ndarray = None   # bool [P, F]: a zero code whose sign bit may differ
 
 
 def _silu_prime(g):
@@ -267,64 +324,86 @@ def _silu_prime(g):
     return sg * (1.0 + g * (1.0 - sg))
 
 
-def qh_ambiguity(res: FFNResult, pairs: np.ndarray, beta: float = H_BAND) -> QAmbiguity:
-    """Flag the elements of Q(h) whose code could differ for an h within the band.
+def h_band(res: FFNResult, widen: float = 1.0) -> np.ndarray:
+    """Error band eps_i of a device float32 h_i = silu(g_i) * u_i around the exact value.
 
-    The band for h_i is eps_i = beta * (|silu'(g)| |u| G_abs + |silu(g)| U_abs)
-    + 2^-22 |h_i| + 2^-26 amax_row, G_abs/U_abs being the sums of absolute products of
-    the gate and up dot products.  The last term covers values far below every
-    decision of their row: a float32 SiLU underflows to 0 for g below about -88, where
-    the float64 value is ~1e-38; no threshold of Q lies below 2^-22 amax_row except the
-    zero-scale one near 2^-19 amax_row, so the floor cannot hide a decision.  An element is flagged if its row exponent, its block scale
-    or its own code changes between the two ends of the band.  A flagged
-    element's dequantised value then moves by at most
-    |deq' - h'| + |h' - h| + |h - deq| <= 1.375 unit' + eps + 1.375 unit, a
-    rounding error being at most half the largest E2M1 gap (1 unit) plus the
-    saturation overshoot (3/8 unit); with unit' <= unit_hi this is bounded by
-    3 unit_hi + eps, unit_hi being the block's unit at the upper end of the band
+    eps = widen * ACC_ROUNDINGS * 2^-24 * (|silu'(g)| |u| g_acc + |silu(g)| u_acc)
+          + 2^-22 |h| + 2^-120 |u| + 2^-140.
+    The first term propagates the accumulation bound of g and u (accumulation_scale) to h
+    to first order; the second covers the float32 epilogue (exp, divide, multiplies: a few
+    roundings of h).  The last two cover float32 underflow, where relative bounds fail: a
+    float32 SiLU is 0 for g below about -88.7 (exp(-g) overflows), while the exact
+    |silu(g)| = |g| e^g there is below 2^-121; results below 2^-126 are subnormal, with an
+    absolute error of at most 2^-150 per operation.
+    """
+    if res.g_acc is None:
+        raise ValueError("the band needs a prefill-mode result (accumulation scales)")
+    g, u = res.g, res.u
+    eps = widen * ACC_ROUNDINGS * UNIT_ROUNDOFF * (np.abs(_silu_prime(g)) * np.abs(u) * res.g_acc
+                                                   + np.abs(silu(g)) * res.u_acc)
+    eps = eps + 2.0 ** -22 * np.abs(res.h)
+    eps = eps + 2.0 ** -120 * np.abs(u) + 2.0 ** -140
+    return eps
+
+
+def qh_ambiguity(res: FFNResult, pairs: np.ndarray, widen: float = 1.0) -> QAmbiguity:
+    """Flag the elements of Q(h) whose decisions could differ for any h' with
+    |h'_i - h_i| <= eps_i (h_band).
+
+    The row exponent follows the row's largest magnitude, which for such h' lies in
+    [max_i (|h_i| - eps_i), max_i (|h_i| + eps_i)]; a block scale likewise follows its
+    block's largest magnitude.  An element is flagged if its row exponent, its block scale
+    or its own E2M1 magnitude code changes inside these intervals.  A flagged element's
+    dequantised value moves by at most |deq' - h'| + |h' - h| + |h - deq| <= 1.375 unit'
+    + eps + 1.375 unit, a rounding error being at most half the largest E2M1 gap (1 unit)
+    plus the saturation overshoot (3/8 unit); with unit' <= unit_hi this is bounded by
+    3 unit_hi + eps, unit_hi being the block's unit at the upper end of the interval
     (twice that when the row exponent itself may move).
+
+    Separately, ``zero_sign`` marks elements whose code has magnitude 0 at both ends but
+    whose sign may differ (|h_i| <= eps_i): the sign bit of a zero code follows the sign
+    of h', which the band does not fix, and the value (+0 or -0) is the same either way.
     """
     P, F = res.h.shape
-    g, u = res.g, res.u
-    eps = beta * (np.abs(_silu_prime(g)) * np.abs(u) * res.g_abs + np.abs(silu(g)) * res.u_abs)
-    eps = eps + 2.0 ** -22 * np.abs(res.h)
-    eps = eps + 2.0 ** -26 * np.abs(res.h).max(axis=1, keepdims=True)
+    eps = h_band(res, widen)
     flagged = np.zeros((P, F), dtype=bool)
+    zero_sign = np.zeros((P, F), dtype=bool)
     delta = np.zeros((P, F))
     mids6 = nvfp4._UE4M3_MID6
     for p in pairs:
         v = res.h[p].astype(np.float32).astype(np.float64)
         a = np.abs(v)
         e = eps[p]
-        emax = e.max()
+        lo = np.maximum(a - e, 0.0)
+        hi = a + e
         s = nvfp4.row_exponent(np.array([a.max()]))[0]
-        s_lo = nvfp4.row_exponent(np.array([max(a.max() - emax, 0.0)]))[0]
-        s_hi = nvfp4.row_exponent(np.array([a.max() + emax]))[0]
+        s_lo = nvfp4.row_exponent(np.array([lo.max()]))[0]
+        s_hi = nvfp4.row_exponent(np.array([hi.max()]))[0]
         row_amb = (s_lo != s) or (s_hi != s)
         ab = np.ldexp(a, -s).reshape(-1, 16)
-        eb = np.ldexp(e, -s).reshape(-1, 16)
-        bmax = ab.max(axis=1)
-        bemax = eb.max(axis=1)
-        sb_c = nvfp4.nearest_even(bmax, mids6)
-        sb_lo = nvfp4.nearest_even(np.maximum(bmax - bemax, 0.0), mids6)
-        sb_hi = nvfp4.nearest_even(bmax + bemax, mids6)
+        lob = np.ldexp(lo, -s).reshape(-1, 16)
+        hib = np.ldexp(hi, -s).reshape(-1, 16)
+        sb_c = nvfp4.nearest_even(ab.max(axis=1), mids6)
+        sb_lo = nvfp4.nearest_even(lob.max(axis=1), mids6)
+        sb_hi = nvfp4.nearest_even(hib.max(axis=1), mids6)
         blk_amb = (sb_lo != sb_c) | (sb_hi != sb_c)
         sbv = nvfp4.UE4M3_TABLE[sb_c][:, None]
         thr = nvfp4._E2M1_MIDS[None, None, :] * sbv[..., None]        # [nb, 1, 7]
+
         def mag(x):
             return ((x[..., None] > thr) | ((x[..., None] == thr) &
                     (np.arange(7) % 2 == 1))).sum(axis=-1)
-        el_amb = (mag(np.maximum(ab - eb, 0.0)) != mag(ab + eb))
-        # a code of magnitude 0 may take either sign
-        el_amb |= (ab <= eb) & (sbv > 0)
+        m_lo, m_hi = mag(lob), mag(hib)
+        el_amb = m_lo != m_hi
         unit = np.ldexp(nvfp4.UE4M3_TABLE[np.minimum(sb_hi, 0x7E)], s)[:, None] * np.ones((1, 16))
         f = el_amb | blk_amb[:, None]
         if row_amb:
             f[:] = True
             unit = unit * 2.0
         flagged[p] = f.reshape(-1)
+        zero_sign[p] = (~f & (m_hi == 0) & (lob == 0.0)).reshape(-1)
         delta[p] = np.where(f, 3.0 * unit + e.reshape(-1, 16), 0.0).reshape(-1)
-    return QAmbiguity(flagged, delta, eps)
+    return QAmbiguity(flagged, delta, eps, zero_sign)
 
 
 def prefill_allowance(res: FFNResult, amb: QAmbiguity, down, ids: np.ndarray,
@@ -334,13 +413,15 @@ def prefill_allowance(res: FFNResult, amb: QAmbiguity, down, ids: np.ndarray,
     k = ids.shape[1]
     E = down.codes.shape[0]
     extra = np.zeros((T, H))
+    absd = {}
     for t in tokens:
         for j in range(k):
             p = t * k + j
             e = int(ids[t, j])
             if not 0 <= e < E or not amb.flagged[p].any():
                 continue
+            if e not in absd:
+                absd[e] = np.abs(_expert_weights(down, e))
             idx = np.nonzero(amb.flagged[p])[0]
-            wd = np.abs(_expert_weights(down, e))[:, idx]
-            extra[t] += abs(float(w[t, j])) * (wd @ amb.delta[p, idx])
+            extra[t] += abs(float(w[t, j])) * (absd[e][:, idx] @ amb.delta[p, idx])
     return extra

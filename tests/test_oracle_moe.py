@@ -172,8 +172,8 @@ def test_prefill_ambiguity_covers_perturbations():
     ids, ww = oracle.route_topk(w.logits, w.k)
     res = oracle.ffn(w.x_bits, ids, ww, w.gate_up, w.down, mode="prefill")
     P = w.P
-    band_scale = 300       # widen the band so that flags actually occur on a tiny case
-    amb = oracle.qh_ambiguity(res, np.arange(P), beta=oracle.moe.H_BAND * band_scale)
+    # widen the band so that flags actually occur on a tiny case
+    amb = oracle.qh_ambiguity(res, np.arange(P), widen=3e4)
     base = nvfp4.dequant_q(*res.qh)
     rng = np.random.default_rng(0)
     hit = 0
@@ -264,3 +264,30 @@ def test_alpha_power_of_two_equals_scaled_block_scales():
     assert np.array_equal(a.y, f.y) and np.array_equal(a.tsum, f.tsum)
     plain = oracle.ffn(wl.x_bits, ids, w, wl.gate_up, wl.down)
     assert not np.allclose(a.y, plain.y)
+
+
+def test_hash_router_csr_statistics():
+    """The pages' hash router ("moe_sk_repro.rs", fn route) through the oracle's CSR, at the
+    page's own sizes (E=288, top-8, t in {512, 2048, 4096}; fn main prints n_active, max_m,
+    mean_m and pad128 for them, in that format): n_active 288; max_m 56 / 265 / 494; mean_m
+    14.2 / 56.9 / 113.8; pad128 (rows of 128-row tiles over useful rows) 9.00 / 2.30 /
+    1.39x.  These figures were computed once from the router's definition and are stored
+    here; the hash's own first value is pinned by its arithmetic (p = 0 hashes to 0, so
+    u = 0 and the expert is 0), and the skew by the closed form P(e < j) = (j/E)^(1/1.35)."""
+    E, k = 288, 8
+    expect = {512: (288, 56, 14.2, 9.00), 2048: (288, 265, 56.9, 2.30), 4096: (288, 494, 113.8, 1.39)}
+    for t, (n_active, max_m, mean_m, pad) in expect.items():
+        ids = np.array([synth.hash_route(p, E) for p in range(t * k)], np.int32).reshape(t, k)
+        csr = oracle.build_expert_csr(ids, E)
+        ms = np.diff(csr.offsets.astype(np.int64))
+        ms = ms[ms > 0]
+        assert csr.n_active == n_active
+        assert ms.max() == max_m
+        assert round(ms.mean(), 1) == mean_m
+        assert round(float(((ms + 127) // 128 * 128).sum() / ms.sum()), 2) == pad
+    assert synth.hash_route(0, E) == 0
+    ids = np.array([synth.hash_route(p, E) for p in range(32768)])
+    for j in (1, 10, 72, 144):
+        p = (j / E) ** (1 / 1.35)
+        sd = np.sqrt(p * (1 - p) / ids.size)
+        assert abs(np.mean(ids < j) - p) < 5 * sd
