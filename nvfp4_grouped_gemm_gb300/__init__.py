@@ -152,7 +152,13 @@ def moe_build_expert_csr_static(topk_ids: torch.Tensor, E: int, csr: ExpertCSR,
                                 stream=None) -> None:
     """The CSR without a workspace (scratch in a fixed device array inside the library);
     for callers that cannot allocate device memory. T*k <= 65536."""
+    if topk_ids.dtype != torch.int32 or not topk_ids.is_contiguous() or topk_ids.dim() != 2:
+        raise TypeError("topk_ids must be a contiguous int32 [T, k] tensor")
+    if not topk_ids.is_cuda or topk_ids.device.index != torch.cuda.current_device():
+        raise ValueError("topk_ids must be on the current CUDA device")
     T, k = topk_ids.shape
+    if csr.E != E or csr.pair_ids.numel() < T * k or csr.expert_offsets.device != topk_ids.device:
+        raise ValueError("csr must be sized for E experts and T*k pairs on the same device")
     _check(_native.load().moe_build_expert_csr_static(_ptr(topk_ids), T, k, E, csr._c,
                                                       _stream(stream)),
            "moe_build_expert_csr_static")
