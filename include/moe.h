@@ -128,7 +128,10 @@ typedef struct moe_ws_layout {
                           decode path; on the prefill path f16 [P][H] holding
                           z * 2^-(qh_exp[row] + c_F), c_F the smallest shift with
                           F * 2688^2 * 2^-c_F < 2^15 */
-  size_t tiles;        /* prefill: i32 count, pad to 16 B, then int4 {row0, rows, expert, 0} per M-tile */
+  size_t tiles;        /* 128-row M-tiles of the prefill GEMMs (written by the CSR call): i32
+                          count, pad to 16 B, then int4 {row0, rows, expert, 0} per tile */
+  size_t slice_tiles;  /* the same for the sliced decode GEMMs: 32-row tiles over the 4 slice
+                          rows of every pair (row0 and rows count slice rows) */
 } moe_ws_layout;
 
 /* Limits (MOE_ERR_UNSUPPORTED beyond them): 1 <= k <= min(E, 32); E <= 1024;
@@ -172,9 +175,11 @@ moe_status moe_route_topk(const float* logits, int32_t T, int32_t E, int32_t k,
 /* Expert-first CSR of the P = T*k pairs ("moe_sk_repro.rs", fn main): a counting sort by
  * expert that keeps ascending p within an expert (placement by prefix sums, not by
  * atomic arrival order, so the result is bit-exact and deterministic). topk_ids i32
- * [T][k]. Writes `csr` and the workspace's pair_pos; ids outside [0, E) set
- * MOE_DEVERR_EXPERT_ID and are left out. From T*k >= 4096 pairs it also keeps per-chunk
- * counts in the workspace's h region (which the gate/up call overwrites afterwards). */
+ * [T][k]. Writes `csr` and the workspace's pair_pos and both tile lists (tiles,
+ * slice_tiles); ids outside [0, E) set MOE_DEVERR_EXPERT_ID and are left out. ws must hold
+ * at least the regions before h (moe_workspace_layout with any H, F, path: they do not
+ * depend on them). From T*k >= 4096 pairs it also keeps per-chunk counts in the
+ * workspace's h region (which the gate/up call overwrites afterwards). */
 moe_status moe_build_expert_csr(const int32_t* topk_ids, int32_t T, int32_t k, int32_t E,
                                 moe_csr csr, void* ws, size_t ws_bytes, void* stream);
 
@@ -202,10 +207,9 @@ moe_status moe_grouped_down_combine_nvfp4(const moe_nvfp4_bank* w_down, moe_csr 
                                           size_t ws_bytes, void* stream);
 
 /* moe_build_expert_csr without a workspace, for callers that cannot allocate device
- * memory: a plugin or engine that owns every device allocation and hands kernels only its
- * own tensors, code issuing work inside a CUDA stream capture that must not call
- * cudaMalloc (which may also synchronise the device), or latency-critical loops where an
- * allocation's implicit synchronisation is unacceptable. The paper the method comes from
+ * memory: a host engine or plugin that owns every device allocation and hands kernels only
+ * its own tensors, or code on a path where a device allocation is not allowed because
+ * cudaMalloc may block and synchronise the whole device. The paper the method comes from
  * has no counterpart to this entry point; it is an addition of this library.
  *
  * Same inputs and CSR outputs as moe_build_expert_csr (bit-identical results). Its scratch
@@ -213,13 +217,15 @@ moe_status moe_grouped_down_combine_nvfp4(const moe_nvfp4_bank* w_down, moe_csr 
  * per GPU that loads the library, held until the process exits; nothing is allocated or
  * freed. Limits: T * k <= 65536 (else MOE_ERR_UNSUPPORTED), plus the limits above.
  * The first call on each device looks up the array's device address (once per device, on
- * the current device); make that first call before any stream capture. All calls share
- * the one array: calls that can overlap on the GPU (different streams, or different host
- * threads, on the same device) race, so serialise them. Invalid expert ids are left out
- * as in moe_build_expert_csr, but no error word is reported: expert_offsets[E] < T*k
- * tells the caller that some were dropped. The layer calls (gate/up, down/combine) also
- * read the per-pair positions that moe_build_expert_csr writes into their workspace, so
- * they need that entry point; this one serves callers that want the CSR alone. */
+ * the current device) and keeps it for the life of that device's primary context: make
+ * that first call before any stream capture, and do not call this entry point again on a
+ * device after resetting it (cudaDeviceReset). All calls share the one array: calls that
+ * can overlap on the GPU (different streams, or different host threads, on the same
+ * device) race, so serialise them. Invalid expert ids are left out as in
+ * moe_build_expert_csr, but no error word is reported: expert_offsets[E] < T*k tells the
+ * caller that some were dropped. The layer calls (gate/up, down/combine) also read the
+ * per-pair positions that moe_build_expert_csr writes into their workspace, so they need
+ * that entry point; this one serves callers that want the CSR alone. */
 moe_status moe_build_expert_csr_static(const int32_t* topk_ids, int32_t T, int32_t k, int32_t E,
                                        moe_csr csr, void* stream);
 

@@ -1,9 +1,23 @@
 // Host side of the C ABI: argument validation, workspace layout and kernel launches.
+#include <atomic>
 #include <cstring>
 
 #include "moe_internal.cuh"
 
 namespace moe {
+
+int num_sms() {
+  constexpr int kCachedDevices = 64;
+  static std::atomic<int> cache[kCachedDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  int n = (dev >= 0 && dev < kCachedDevices) ? cache[dev].load(std::memory_order_relaxed) : 0;
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    n = 1;
+  if (dev >= 0 && dev < kCachedDevices) cache[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
 
 namespace {
 
@@ -93,6 +107,10 @@ bool compute_layout(int T, int H, int F, int E, int k, int path, moe_ws_layout* 
   };
   L->error_word = take(sizeof(uint32_t));
   L->pair_pos = take(P * sizeof(int32_t));
+  // both tile lists, written by the CSR call whatever the path (their place depends only on
+  // P and E, so the CSR call finds them without knowing H, F or the path)
+  L->tiles = take(tile_list_bytes((long long)P, 1, kTileRows, E));
+  L->slice_tiles = take(tile_list_bytes((long long)P, kDecodeSlices, kSliceTileRows, E));
   L->h = take(P * F * sizeof(float));
   L->partial = take(P * H * sizeof(float));
   if (path == MOE_PATH_DECODE && !decode_sliced((long long)P)) {
@@ -110,9 +128,6 @@ bool compute_layout(int T, int H, int F, int E, int k, int path, moe_ws_layout* 
     L->qh_codes = take(R * (F / 2));
     L->qh_scales = take(R * qh_scale_pitch(F));
     L->qh_exp = take(R * sizeof(int32_t));
-    // tiles: 128 rows, or 32 rows (eight pairs' slices) in the sliced decode form
-    const size_t max_tiles = R / (sl ? 32 : 128) + (size_t)(E < (int)P ? E : (int)P) + 1;
-    L->tiles = take(16 + 16 * max_tiles);
   }
   L->total = o;
   return true;
@@ -152,9 +167,9 @@ int32_t moe_kernel_launches(int32_t T, int32_t H, int32_t F, int32_t E, int32_t 
   const int P = T * k;
   const int csr = csr_scratch_bytes(P, E) ? 3 : 1;   // grid-wide build or one CTA
   if (resolve_path(T, k, path) == MOE_PATH_DECODE)
-    return decode_sliced(P) ? csr + 3 /* tiles, x slices, gate/up */ + 3 /* h slices, down, combine */
+    return decode_sliced(P) ? csr + 2 /* x slices, gate/up */ + 3 /* h slices, down, combine */
                             : csr + 2 /* x gather, gate/up */ + 3 /* h prep, down, combine */;
-  return csr + 3 /* tiles, Q(x), gate/up GEMM */ + 3 /* Q(h), down GEMM, combine */;
+  return csr + 2 /* Q(x), gate/up GEMM */ + 3 /* Q(h), down GEMM, combine */;
 }
 
 const char* moe_status_string(moe_status s) {
@@ -192,7 +207,7 @@ moe_status moe_build_expert_csr(const int32_t* topk_ids, int32_t T, int32_t k, i
   moe_ws_layout L;
   if (!compute_layout(T, 256, 64, E, k, MOE_PATH_DECODE, &L)) return MOE_ERR_UNSUPPORTED;
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MOE_ERR_WORKSPACE;
-  if (ws_bytes < L.pair_pos + (size_t)T * k * sizeof(int32_t)) return MOE_ERR_WORKSPACE;
+  if (ws_bytes < L.h) return MOE_ERR_WORKSPACE;            // error word, pair_pos, tile lists
   // many pairs: the grid-wide build keeps per-chunk counts in the h region (written only
   // later, by the gate/up call); it needs that much workspace
   const size_t scratch = csr_scratch_bytes(T * k, E);
@@ -202,6 +217,8 @@ moe_status moe_build_expert_csr(const int32_t* topk_ids, int32_t T, int32_t k, i
                                     reinterpret_cast<int32_t*>(w + L.pair_pos),
                                     reinterpret_cast<uint32_t*>(w + L.error_word),
                                     scratch ? reinterpret_cast<int32_t*>(w + L.h) : nullptr,
+                                    reinterpret_cast<int32_t*>(w + L.tiles),
+                                    reinterpret_cast<int32_t*>(w + L.slice_tiles),
                                     static_cast<cudaStream_t>(stream)));
 }
 

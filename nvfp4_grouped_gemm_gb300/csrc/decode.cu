@@ -911,17 +911,6 @@ down_tma_kernel(const DnTmaArgs args) {
   __syncthreads();
 }
 
-int sm_count() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 1;
-  }
-  return n;
-}
-
 }  // namespace
 
 cudaError_t launch_decode_gate_up(const uint16_t* x_bf16, int T, int H, int F, int k,
@@ -958,7 +947,7 @@ cudaError_t launch_decode_gate_up(const uint16_t* x_bf16, int T, int H, int F, i
     // with fewer than ~8 units per SM the warps cannot keep enough bytes in flight and the
     // CTA kernel below is faster (measured at one token: 40 us against 42 us per layer)
     const long long units_bound = (long long)(P < b.E ? P : b.E) * (F / 8);
-    if (units_bound >= 8LL * sm_count() && smem <= 232448 &&
+    if (units_bound >= 8LL * num_sms() && smem <= 232448 &&
         make_map4(&mc, b.codes, cdims, cstr, cbox, true) &&
         make_map4(&ms, b.scales, sdims, sstr, sbox, false)) {
       GuTmaArgs ta{xg, xe, H, F, nh, nb, csr.expert_offsets, csr.active_experts, csr.n_active,
@@ -971,7 +960,7 @@ cudaError_t launch_decode_gate_up(const uint16_t* x_bf16, int T, int H, int F, i
       if (st != cudaSuccess) return st;
       const long long units = (long long)(P < b.E ? P : b.E) * (F / 8);
       // every SM streams, even when there are fewer units than consumer warps
-      long long grid = sm_count();
+      long long grid = num_sms();
       if (grid > units) grid = units;
       if (grid < 1) grid = 1;
       return launch_pdl(gk, dim3((unsigned)grid), dim3(32 * (kTmaProd + kTmaWarps)),
@@ -988,7 +977,7 @@ cudaError_t launch_decode_gate_up(const uint16_t* x_bf16, int T, int H, int F, i
                                              : kmax == 3 ? gate_up_kernel<3> : gate_up_kernel<4>;
   st = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (st != cudaSuccess) return st;
-  long long grid = 2LL * sm_count();
+  long long grid = 2LL * num_sms();
   if (grid > max_units) grid = max_units;
   return launch_pdl(kern, dim3((unsigned)grid), dim3(256), smem, s, a);
 }
@@ -1010,7 +999,7 @@ cudaError_t launch_decode_down(const moe_nvfp4_bank& b, moe_csr csr, int T, int 
     const size_t smem = (size_t)kTmaWarps * kTmaSlots * dn_stage_bytes(F) + 1024 +
                         (size_t)kTmaWarps * kTmaSlots * 16 + 16;
     const long long units = (long long)(P < b.E ? P : b.E) * (H / 16);
-    if (F % 128 == 0 && units >= 8LL * sm_count() && smem <= 232448 &&
+    if (F % 128 == 0 && units >= 8LL * num_sms() && smem <= 232448 &&
         (reinterpret_cast<uintptr_t>(b.codes) & 15) == 0 && (reinterpret_cast<uintptr_t>(b.scales) & 15) == 0) {
       DnTmaArgs ta{hg, he, b.codes, b.scales, H, F, csr.expert_offsets, csr.active_experts,
                    csr.n_active, reinterpret_cast<float*>(ws + L.partial),
@@ -1018,7 +1007,7 @@ cudaError_t launch_decode_down(const moe_nvfp4_bank& b, moe_csr csr, int T, int 
       ta.alpha = b.alpha;
       st = cudaFuncSetAttribute(down_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (st != cudaSuccess) return st;
-      long long grid = sm_count();
+      long long grid = num_sms();
       if (grid > units) grid = units;
       return launch_pdl(down_tma_kernel, dim3((unsigned)grid), dim3(32 * (kTmaProd + kTmaWarps)),
                         smem, s, ta);
@@ -1030,7 +1019,7 @@ cudaError_t launch_decode_down(const moe_nvfp4_bank& b, moe_csr csr, int T, int 
   const long long max_units = (long long)(P < b.E ? P : b.E) * (H / 128);
   const size_t wbytes = (128 * (size_t)(F / 2) + 128 * (size_t)(F / 16) + 127) & ~size_t(127);
   const size_t smem = 2 * wbytes + 8 * (size_t)(F * 2 + 16);
-  long long grid = 2LL * sm_count();
+  long long grid = 2LL * num_sms();
   if (grid > max_units) grid = max_units;
   auto kern = (F % 128 == 0) ? down_kernel<128> : down_kernel<64>;
   st = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

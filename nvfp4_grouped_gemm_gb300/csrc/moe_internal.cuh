@@ -28,8 +28,22 @@ constexpr int kDecodeSlices = 4;
 constexpr int kSlicedMinPairs = MOE_SLICED_MIN_PAIRS;
 inline bool decode_sliced(long long P) { return P >= kSlicedMinPairs; }
 constexpr size_t kAlign = 256;
+// Tile lists over the CSR: the prefill GEMMs cut an expert's rows into 128-row M-tiles; the
+// sliced decode GEMMs cut its slice rows (kDecodeSlices per pair) into 32-row tiles.
+constexpr int kTileRows = 128;
+constexpr int kSliceTileRows = 32;
+// Bytes of a tile list (count, pad to 16 B, then one int4 {row0, rows, expert, 0} per tile)
+// for P pairs of rpp operand rows each: at most P*rpp/tile_rows full tiles plus one partial
+// tile per active expert (at most min(E, P) of them).
+inline size_t tile_list_bytes(long long P, int rpp, int tile_rows, int E) {
+  const long long active = E < P ? E : P;
+  return (size_t)(16 + 16 * (P * rpp / tile_rows + active + 1));
+}
 
 inline size_t align_up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a; }
+
+// Number of SMs of the current device (cached per device; grids are sized from it).
+int num_sms();
 
 // Row pitch of the Q(h) block scales in the prefill workspace: F/16 rounded up to a
 // multiple of 16 bytes, so that the rows can be read by TMA.
@@ -46,8 +60,10 @@ cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t*
 // the CSR is built by three grid-wide kernels, else by one CTA.
 constexpr int kCsrGridMinPairs = 4096;
 size_t csr_scratch_bytes(int P, int E);
+// `tiles` / `slice_tiles` (either may be null) receive the two tile lists.
 cudaError_t launch_build_csr(const int32_t* ids, int P, int k, int E, moe_csr csr,
-                             int32_t* pair_pos, uint32_t* err, int32_t* scratch, cudaStream_t s);
+                             int32_t* pair_pos, uint32_t* err, int32_t* scratch, int32_t* tiles,
+                             int32_t* slice_tiles, cudaStream_t s);
 cudaError_t launch_decode_gate_up(const uint16_t* x_bf16, int T, int H, int F, int k,
                                   const moe_nvfp4_bank& b, moe_csr csr, const moe_ws_layout& L,
                                   char* ws, cudaStream_t s);
@@ -55,9 +71,6 @@ cudaError_t launch_decode_down(const moe_nvfp4_bank& b, moe_csr csr, int T, int 
                                const moe_ws_layout& L, char* ws, cudaStream_t s);
 cudaError_t launch_combine(const float* w, int T, int H, int k, const moe_ws_layout& L, char* ws,
                            float* y, cudaStream_t s);
-// Tile list over the CSR (prefill.cu): rpp operand rows per pair, tiles of tile_rows rows.
-cudaError_t launch_tiles(const int32_t* offsets, int E, int rpp, int tile_rows, int32_t* tiles,
-                         cudaStream_t s);
 cudaError_t launch_sliced_gate_up(const uint16_t* x_bf16, int T, int H, int F, int k,
                                   const moe_nvfp4_bank& b, moe_csr csr, const moe_ws_layout& L,
                                   char* ws, cudaStream_t s);
@@ -76,12 +89,12 @@ cudaError_t launch_quant_h(const float* h, int P, int F, int sf_pitch, const int
                            int E, uint8_t* qc, uint8_t* qs, int32_t* qe, cudaStream_t s);
 // Exponent c_F with F * 2688^2 * 2^-c_F < 2^15: the fixed shift of the f16 partials.
 int down_shift_for(int F);
+cudaError_t launch_prefill_combine(const float* w, int T, int H, int F, int k, int c0, int HS,
+                                   const moe_ws_layout& L, char* ws, float* y, cudaStream_t s);
 cudaError_t launch_slice_x(const uint16_t* x_bf16, int T, int H, int k, const int32_t* pair_pos,
                            uint8_t* qc, uint8_t* qs, int32_t* qe, cudaStream_t s);
 cudaError_t launch_slice_h(const float* h, int P, int F, int sf_pitch, const int32_t* offsets,
                            int E, uint8_t* qc, uint8_t* qs, int32_t* qe, cudaStream_t s);
-cudaError_t launch_prefill_combine(const float* w, int T, int H, int F, int k, int c0, int HS,
-                                   const moe_ws_layout& L, char* ws, float* y, cudaStream_t s);
 // Programmatic dependent launch, device side: wait for the predecessor grid (complete,
 // its memory visible), or allow the successor grid to start launching.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

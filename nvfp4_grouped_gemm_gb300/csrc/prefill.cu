@@ -1,7 +1,7 @@
 // Prefill path: hundreds of pairs per expert, a dense grouped contraction on the
-// block-scaled FP4 tensor cores (tcgen05.mma kind::mxf4nvf4, UE4M3 scale per 16).
+// block-scaled FP4 tensor cores (tcgen05.mma kind::mxf4nvf4, UE4M3 scale per 16), over the
+// 128-row M-tiles (expert, first CSR row, rows) the CSR call lists.
 //
-//   tiles_kernel    128-row M-tiles (expert, first CSR row, rows) from the CSR offsets
 //   gemm_kernel     persistent, warp-specialised grouped GEMM over (M-tile, N-tile) work:
 //                   TMA (SWIZZLE_128B) feeds FP4 code tiles and row-major images of the
 //                   UE4M3 scale factors, four warps write the scale factors into TMEM
@@ -25,57 +25,6 @@ namespace moe {
 
 namespace {
 
-// ---------------------------------------------------------------------------
-// M-tile list
-// ---------------------------------------------------------------------------
-constexpr int kTileRows = 128;
-
-// tiles region: int n_mtiles, pad to 16 B, then int4 {row0, rows, expert, 0} per M-tile.
-// A pair owns `rpp` consecutive operand rows (1, or the activation slices of the decode
-// form); an expert's rows are cut into tiles of `tile_rows`.
-__global__ void __launch_bounds__(1024) tiles_kernel(const int32_t* __restrict__ offsets, int E,
-                                                     int rpp, int tile_rows,
-                                                     int32_t* __restrict__ tiles) {
-  __shared__ int scratch[32];
-  pdl_wait();                                       // the CSR offsets are complete
-  pdl_trigger();
-  const int e = threadIdx.x;
-  const int lane = e & 31, warp = e >> 5;
-  int cnt = 0, off = 0;
-  if (e < E) {
-    off = offsets[e] * rpp;
-    cnt = (offsets[e + 1] * rpp - off + tile_rows - 1) / tile_rows;
-  }
-  int x = cnt;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) scratch[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int s = scratch[lane];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += y;
-    }
-    scratch[lane] = s;
-  }
-  __syncthreads();
-  const int base = (warp ? scratch[warp - 1] : 0) + x - cnt;
-  int4* list = reinterpret_cast<int4*>(tiles + 4);
-  if (e < E) {
-    const int m = offsets[e + 1] * rpp - off;
-    for (int i = 0; i < cnt; ++i) {
-      const int r = m - i * tile_rows;
-      list[base + i] = make_int4(off + i * tile_rows, r < tile_rows ? r : tile_rows, e, 0);
-    }
-  }
-  if (threadIdx.x == 0) tiles[0] = scratch[31];
-}
-
 // (mbarrier and TMA wrappers: tma_sync.cuh; tcgen05 wrappers: tcgen05.cuh)
 
 // ---------------------------------------------------------------------------
@@ -96,7 +45,19 @@ struct GemmArgs {
   int b_sf_group;               // DOWN: g rows of the weight-scale plane per tensor-map row
   int n_base;                   // first N-tile of this launch (output columns are relative to it)
   const float* alpha = nullptr; // [E] per-expert second-level weight scale, or none
+  // Works are taken in groups of `n_group` N-tiles: all M-tiles of group 0, then of group 1,
+  // ...; within a group M-tiles in list order, N fastest (n_group = n_tiles_n: one group).
+  int n_group = 0;
 };
+
+// M-tile index and N-tile index of work w (see GemmArgs::n_group).
+__device__ __forceinline__ void work_mn(int w, int n_mtiles, int ng, int& m, int& n) {
+  const int per = n_mtiles * ng;
+  const int g = w / per;
+  const int r = w - g * per;
+  m = r / ng;
+  n = g * ng + (r - m * ng);
+}
 
 // Scale factors reach shared memory through TMA, as row-major staging images beside the
 // code tiles: A rows [128][16 B] (the stage's 4 k-steps x 4 scales), B rows [BN][16 B]
@@ -198,13 +159,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
       const int sub_rows = BN / g, sub_w = g == 1 ? 16 : 32;
       int it = 0;
       // work descriptors are fetched two works ahead (a DOWN work is only a few stages)
+      const int ng = args.n_group;
+      auto mtile_of = [&](int w) { int m, n; work_mn(w, n_mtiles, ng, m, n); return tlist[m]; };
       const int w1 = blockIdx.x + gridDim.x;
-      int4 tile = blockIdx.x < n_work ? tlist[blockIdx.x / args.n_tiles_n] : make_int4(0, 0, 0, 0);
-      int4 next = w1 < n_work ? tlist[w1 / args.n_tiles_n] : tile;
+      int4 tile = blockIdx.x < n_work ? mtile_of(blockIdx.x) : make_int4(0, 0, 0, 0);
+      int4 next = w1 < n_work ? mtile_of(w1) : tile;
       for (int w = blockIdx.x; w < n_work && !*abort_flag; w += gridDim.x) {
         const int w2 = w + 2 * gridDim.x;
-        const int4 next2 = w2 < n_work ? tlist[w2 / args.n_tiles_n] : next;
-        const int n0 = (w % args.n_tiles_n) * C::OUT_N;
+        const int4 next2 = w2 < n_work ? mtile_of(w2) : next;
+        int wm, wn;
+        work_mn(w, n_mtiles, ng, wm, wn);
+        const int n0 = wn * C::OUT_N;
         const int brow = tile.z * args.rows_per_expert + args.n_base * C::OUT_N + n0;
         for (int ks = 0; ks < k_stages; ++ks, ++it) {
           const int st = it % C::STAGES;
@@ -346,8 +311,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     int tcount = 0;
     for (int w = blockIdx.x; w < n_work && !*abort_flag; w += gridDim.x, ++tcount) {
       const int ab = tcount & 1;
-      const int4 tile = tlist[w / args.n_tiles_n];
-      const int n0 = (w % args.n_tiles_n) * C::OUT_N;
+      int wm, wn;
+      work_mn(w, n_mtiles, args.n_group, wm, wn);
+      const int4 tile = tlist[wm];
+      const int n0 = wn * C::OUT_N;
       const bool valid = row < tile.y;
       const int pos = tile.x + row;
       const int sx = GATE_UP ? (valid ? args.a_exp[pos] : 0) : -args.down_shift;
@@ -364,6 +331,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         static_assert(BN / 64 == 2, "one 32-column chunk per epilogue warp");
         float g[32], u[32];
         tc_ld32x2(acc + half * 32, acc + BN / 2 + half * 32, g, u);
+        // the values are in registers: hand the accumulator buffer back to the MMA thread
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[ab]);
         if (valid) {
 #pragma unroll
           for (int i = 0; i < 32; i += 4) {
@@ -383,6 +354,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         static_assert(BN / 32 == 4, "two 32-column chunks per epilogue warp");
         float v[2][32];
         tc_ld32x2(acc + half * 64, acc + half * 64 + 32, v[0], v[1]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[ab]);
         if (valid) {
 #pragma unroll
           for (int c = 0; c < 2; ++c)
@@ -401,9 +375,6 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
             }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[ab]);
     }
   }
 
@@ -442,15 +413,13 @@ cudaError_t launch_prefill_gate_up(const uint16_t* x_bf16, int T, int H, int F, 
   *unsupported = false;
   if (H % 256 != 0 || F % 64 != 0) { *unsupported = true; return cudaSuccess; }
   const int P = T * k;
+  // the 128-row M-tile list was written by the CSR call
   int32_t* tiles = reinterpret_cast<int32_t*>(ws + L.tiles);
-  tiles_kernel<<<1, 1024, 0, s>>>(csr.expert_offsets, b.E, 1, kTileRows, tiles);
-  cudaError_t st = cudaGetLastError();
-  if (st != cudaSuccess) return st;
   uint8_t* qc = reinterpret_cast<uint8_t*>(ws + L.qx_codes);
   uint8_t* qs = reinterpret_cast<uint8_t*>(ws + L.qx_scales);
   int32_t* qe = reinterpret_cast<int32_t*>(ws + L.qx_exp);
-  st = launch_quant_x(x_bf16, T, H, k, reinterpret_cast<const int32_t*>(ws + L.pair_pos), qc, qs,
-                      qe, s);
+  cudaError_t st = launch_quant_x(x_bf16, T, H, k,
+                                  reinterpret_cast<const int32_t*>(ws + L.pair_pos), qc, qs, qe, s);
   if (st != cudaSuccess) return st;
   CUtensorMap ma, mb, msa, msb;
   constexpr int BN = 128;                           // 64 gate rows over 64 up rows
@@ -463,6 +432,7 @@ cudaError_t launch_prefill_gate_up(const uint16_t* x_bf16, int T, int H, int F, 
   GemmArgs a{qe, tiles, ws + L.h, reinterpret_cast<uint32_t*>(ws + L.error_word),
              P, H, 2 * F, F / (BN / 2), F, F, 0, 1, 0};
   a.alpha = b.alpha;
+  a.n_group = a.n_tiles_n;                          // one group: M-tiles in order, N fastest
   const int max_tiles = P / 128 + (P < b.E ? P : b.E) + 1;
   return run_gemm<BN, true>(ma, mb, msa, msb, a, max_tiles, s);
 }
@@ -498,18 +468,12 @@ cudaError_t launch_prefill_down(const moe_nvfp4_bank& b, moe_csr csr, const floa
     return cudaErrorInvalidValue;
   const int shift = down_shift_for(F);
   const int max_tiles = P / 128 + (P < b.E ? P : b.E) + 1;
-  // (splitting the output columns so that each slice's partials stay in L2 for the combine
-  // was measured slower: every extra GEMM launch costs more than the HBM round trip saves)
   GemmArgs a{qe, reinterpret_cast<const int32_t*>(ws + L.tiles), ws + L.partial,
              reinterpret_cast<uint32_t*>(ws + L.error_word), P, F, H, H / BN, H, F, shift, g, 0};
   a.alpha = b.alpha;
+  a.n_group = a.n_tiles_n;                          // one group: M-tiles in order, N fastest
   if ((st = run_gemm<BN, false>(ma, mb, msa, msb, a, max_tiles, s)) != cudaSuccess) return st;
   return launch_prefill_combine(w, T, H, F, k, 0, H, L, ws, y, s);
-}
-
-cudaError_t launch_tiles(const int32_t* offsets, int E, int rpp, int tile_rows, int32_t* tiles,
-                         cudaStream_t s) {
-  return launch_pdl(tiles_kernel, dim3(1), dim3(1024), 0, s, offsets, E, rpp, tile_rows, tiles);
 }
 
 }  // namespace moe

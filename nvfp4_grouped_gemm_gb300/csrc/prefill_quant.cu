@@ -1,103 +1,20 @@
-// Activation quantisers and the prefill combine:
+// Activation quantisers (the quantiser Q itself is in quant.cuh) and the prefill combine:
 //
 //   quant_x_kernel      Q(x): each token's bf16 row to NVFP4 with a power-of-two row scale,
 //                       written to every CSR row of the token's pairs
 //   quant_h_kernel      Q(h) per CSR row
-//   slice_x_kernel, slice_h_kernel   the decode tensor-core form's four residual slices
-//                       of each x row (per token, written to its pairs' rows) and h row
 //   combine_f16_kernel  y[t] = sum_j w[t,j] * z16[pos_j] * 2^(e_j + c_F), ascending j
-//
-// The quantiser Q (the pages never quantise activations; block-scaled FP4 x FP4 needs it):
-// s = smallest integer with amax_row <= 6*448*2^s; block scale = the UE4M3 value nearest
-// to amax_16 / (6*2^s) (ties to the even encoding); code = the E2M1 value nearest to
-// v / (scale*2^s), saturating at 6, ties to even, sign bit iff v < 0.  Every decision is
-// an exact float32 comparison of |v|*2^-s against midpoint*scale products.
+//   slice_x_kernel, slice_h_kernel   the decode tensor-core form's four residual slices
+//                       of each x row (per pair or per token, written to the pairs' rows)
+//                       and h row
 #include <cmath>
 
 #include "moe_internal.cuh"
+#include "quant.cuh"
 
 namespace moe {
 
 namespace {
-
-// ---------------------------------------------------------------------------
-// number formats (device side, written from the format definitions)
-// ---------------------------------------------------------------------------
-
-// Value of UE4M3 encoding b (0 <= b <= 0x7E).
-__device__ __forceinline__ float ue4m3_val(int b) {
-  const int e = b >> 3, m = b & 7;
-  if (e == 0) return (float)m * (1.0f / 512.0f);                    // m/8 * 2^-6
-  return __uint_as_float((uint32_t)(e + 120) << 23 | (uint32_t)m << 20);   // (1+m/8)*2^(e-7)
-}
-
-// Decision threshold between UE4M3 encodings j and j+1, times 6: 3 * (v(j) + v(j+1)).
-__device__ __forceinline__ float ue4m3_thr6(int j) { return 3.0f * (ue4m3_val(j) + ue4m3_val(j + 1)); }
-
-// Threshold j "passed" by key: above it, or on it when the upper neighbour is the even code.
-__device__ __forceinline__ bool ue4m3_passed(float key, int j) {
-  const float t = ue4m3_thr6(j);
-  return key > t || (key == t && ((j + 1) & 1) == 0);
-}
-
-// Nearest UE4M3 encoding to key/6 (key = block amax * 2^-s <= 2688), ties to even: the
-// number of thresholds passed.  A first guess from the float bits of key/6 is corrected
-// by exact comparisons with the neighbouring thresholds.
-__device__ __forceinline__ int ue4m3_code_of(float key) {
-  const float r = key * (1.0f / 6.0f);
-  int cand;
-  if (r < 0.015625f) {
-    cand = (int)(r * 512.0f);                        // subnormal encodings m/8 * 2^-6
-  } else {
-    const uint32_t b = __float_as_uint(r);
-    const int e = (int)((b >> 23) & 0xff) - 127;       // -6 .. 8
-    cand = ((e + 7) << 3) | (int)((b >> 20) & 7);
-  }
-  cand = min(max(cand, 0), 126);
-  while (cand < 126 && ue4m3_passed(key, cand)) ++cand;
-  while (cand > 0 && !ue4m3_passed(key, cand - 1)) --cand;
-  return cand;
-}
-
-// |v| * 2^-s: one multiply by the exact power of two when 2^-s is a float (the same
-// correctly rounded value as ldexpf), else ldexpf.
-__device__ __forceinline__ float scale_down(float v, int s, bool fast, float m) {
-  return fast ? v * m : ldexpf(v, -s);
-}
-
-// Row exponent: smallest s with amax <= 2688 * 2^s (2688 = 0.65625 * 2^12).
-__device__ __forceinline__ int row_exp_of(float amax) {
-  if (!(amax > 0.0f)) return 0;
-  int ea;
-  const float m = frexpf(amax, &ea);
-  return ea - 12 + (m > 0.65625f ? 1 : 0);
-}
-
-// Quantise 16 values (already |v| * 2^-s in `key`, signs in `neg`) with block code sbc.
-// The E2M1 magnitude code of key / scale is the number of midpoints passed between the
-// values 0 .5 1 1.5 2 3 4 6 (midpoints .25 .75 1.25 1.75 2.5 3.5 5).  The seven decision
-// thresholds midpoint * scale are exact f32 products, formed once per block; a key passes
-// an even-indexed threshold when above it and an odd-indexed one when at or above it, so
-// a tie goes to the even code.
-__device__ __forceinline__ uint64_t quant_block(const float (&key)[16], uint32_t negmask, int sbc) {
-  if (sbc == 0) return 0ull;
-  const float sbv = ue4m3_val(sbc);
-  const float t0 = 0.25f * sbv, t1 = 0.75f * sbv, t2 = 1.25f * sbv, t3 = 1.75f * sbv;
-  const float t4 = 2.5f * sbv, t5 = 3.5f * sbv, t6 = 5.0f * sbv;
-  // thresholds are increasing, so the count is found by a three-step search
-  uint32_t lo = 0, hi = 0;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const float v = key[i];
-    const bool b2 = v >= t3;
-    const bool b1 = v >= (b2 ? t5 : t1);
-    const bool b0 = v > (b2 ? (b1 ? t6 : t4) : (b1 ? t2 : t0));
-    const uint32_t c = (b2 ? 4u : 0u) | (b1 ? 2u : 0u) | (b0 ? 1u : 0u) | (((negmask >> i) & 1u) << 3);
-    if (i < 8) lo |= c << (4 * i); else hi |= c << (4 * (i - 8));
-  }
-  const uint64_t out = (uint64_t)lo | ((uint64_t)hi << 32);
-  return out;
-}
 
 // ---------------------------------------------------------------------------
 // Q(x): one warp per token, the result copied to each of the token's CSR rows
@@ -298,11 +215,13 @@ __device__ __forceinline__ uint32_t slice_part(float (&r)[EPT], float row_amax, 
 // Elements per thread in the slice kernels: a 16-value block is shared by two lanes.
 constexpr int kSliceEPT = 8;
 
-// x: one CTA per token, 16/EPT threads per 16-value block (thread (16/EPT)*b + q holds
-// elements 16b + EPT*q ..).  The slices depend only on x, so they are formed before the
-// wait; after it they are written to the NS rows of each of the token's pairs (rows
-// pair_pos * NS + i).
-template <int NS>
+// x: 16/EPT threads per 16-value block (thread (16/EPT)*b + q holds elements 16b + EPT*q
+// ..).  PER_PAIR: one CTA per pair p = t*k + j, which forms the slices of its token's row
+// and writes them to its own pair's NS rows (pair_pos * NS + i); the k CTAs of a token
+// repeat the work, spreading it over k times more SMs when there are few tokens.
+// Otherwise one CTA per token, writing to all k of its pairs' rows.  The slices depend only
+// on x, so they are formed before the wait; only the stores wait for the CSR.
+template <int NS, bool PER_PAIR>
 __global__ void __launch_bounds__(1024) slice_x_kernel(const uint16_t* __restrict__ x, int H, int k,
                                                        const int32_t* __restrict__ pair_pos,
                                                        uint8_t* __restrict__ qc,
@@ -311,7 +230,7 @@ __global__ void __launch_bounds__(1024) slice_x_kernel(const uint16_t* __restric
   constexpr int EPT = kSliceEPT, TPB = 16 / EPT;
   __shared__ float red[NS][32];
   __shared__ int s_pos[kMaxK];
-  const int t = blockIdx.x, tid = threadIdx.x;
+  const int t = PER_PAIR ? blockIdx.x / k : blockIdx.x, tid = threadIdx.x;
   const int b = tid / TPB, q = tid % TPB;
   const int nblk = H / 16;
   const bool has = b < nblk;
@@ -337,13 +256,14 @@ __global__ void __launch_bounds__(1024) slice_x_kernel(const uint16_t* __restric
   }
   pdl_wait();                                       // pair_pos is complete
   pdl_trigger();
-  // the token's k positions, read once (all loads in flight together)
-  if (tid < k) s_pos[tid] = pair_pos[(size_t)t * k + tid];
+  const int npairs = PER_PAIR ? 1 : k;
+  // the positions of this CTA's pairs, read once (all loads in flight together)
+  if (tid < npairs) s_pos[tid] = pair_pos[PER_PAIR ? (size_t)blockIdx.x : (size_t)t * k + tid];
   __syncthreads();
   if (!has) return;
-  for (int j = 0; j < k; ++j) {
+  for (int j = 0; j < npairs; ++j) {
     const int pos = s_pos[j];
-    if (pos < 0) continue;
+    if (pos < 0) continue;                          // invalid expert id: the pair has no rows
 #pragma unroll
     for (int i = 0; i < NS; ++i) {
       const size_t row = (size_t)pos * NS + i;
@@ -456,8 +376,13 @@ cudaError_t launch_slice_x(const uint16_t* x_bf16, int T, int H, int k, const in
                            uint8_t* qc, uint8_t* qs, int32_t* qe, cudaStream_t s) {
   const int threads = (H / kSliceEPT + 31) / 32 * 32;
   if (threads > 1024) return cudaErrorInvalidValue;
-  return launch_pdl(slice_x_kernel<kDecodeSlices>, dim3(T), dim3(threads), 0, s, x_bf16, H, k,
-                    pair_pos, qc, qs, qe);
+  // one CTA per pair while that keeps at most ~4 CTAs per SM: few tokens alone would leave
+  // most SMs idle (the k-fold repeated work is cheaper than the idle SMs up to there)
+  if ((long long)T * k <= 4LL * num_sms())
+    return launch_pdl(slice_x_kernel<kDecodeSlices, true>, dim3(T * k), dim3(threads), 0, s,
+                      x_bf16, H, k, pair_pos, qc, qs, qe);
+  return launch_pdl(slice_x_kernel<kDecodeSlices, false>, dim3(T), dim3(threads), 0, s, x_bf16,
+                    H, k, pair_pos, qc, qs, qe);
 }
 
 cudaError_t launch_slice_h(const float* h, int P, int F, int sf_pitch, const int32_t* offsets,
@@ -467,7 +392,6 @@ cudaError_t launch_slice_h(const float* h, int P, int F, int sf_pitch, const int
   return launch_pdl(slice_h_kernel<kDecodeSlices>, dim3(P), dim3(threads), 0, s, h, F, sf_pitch,
                     offsets, E, qc, qs, qe);
 }
-
 cudaError_t launch_quant_h(const float* h, int P, int F, int sf_pitch, const int32_t* offsets,
                            int E, uint8_t* qc, uint8_t* qs, int32_t* qe, cudaStream_t s) {
   const int nb = (F / 16 + 31) / 32;             // blocks per lane
@@ -476,9 +400,7 @@ cudaError_t launch_quant_h(const float* h, int P, int F, int sf_pitch, const int
           : nb <= 4 ? quant_h_kernel<4> : quant_h_kernel<8>;
   kq<<<(P + 7) / 8, 256, 0, s>>>(h, P, F, sf_pitch, offsets, E, qc, qs, qe);
   return cudaGetLastError();
-}
-
-// Exponent c_F with F * 2688^2 * 2^-c_F < 2^15: the fixed shift of the f16 partials.
+}// Exponent c_F with F * 2688^2 * 2^-c_F < 2^15: the fixed shift of the f16 partials.
 int down_shift_for(int F) {
   const double bound = (double)F * 2688.0 * 2688.0;
   int c = 0;

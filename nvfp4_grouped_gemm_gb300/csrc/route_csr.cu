@@ -137,11 +137,39 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* scratch, int* to
   return base + x - v;
 }
 
+// The tile list of one operand layout, one expert per thread (threads tid < E hold their
+// expert's count and offset): an expert's cnt * rpp operand rows starting at off * rpp are
+// cut into tiles of tile_rows rows, listed in expert order.  Every thread of the CTA must
+// call it (it scans across the block).
+__device__ __forceinline__ void write_tile_list(int E, int cnt, int off, int rpp, int tile_rows,
+                                                int32_t* __restrict__ tiles, int* scratch) {
+  const int e = threadIdx.x;
+  const int m = e < E ? cnt * rpp : 0;
+  const int nt = (m + tile_rows - 1) / tile_rows;
+  int total;
+  const int base = block_exclusive_scan(nt, scratch, &total);
+  int4* list = reinterpret_cast<int4*>(tiles + 4);
+  for (int i = 0; i < nt; ++i) {
+    const int r = m - i * tile_rows;
+    list[base + i] = make_int4(off * rpp + i * tile_rows, r < tile_rows ? r : tile_rows, e, 0);
+  }
+  if (threadIdx.x == 0) tiles[0] = total;
+}
+
+// Both tile lists (the prefill GEMMs' 128-row M-tiles, the sliced decode GEMMs' 32-row
+// tiles over kDecodeSlices rows per pair), when the caller passed their regions.
+__device__ __forceinline__ void write_tile_lists(int E, int cnt, int off, int32_t* tiles,
+                                                 int32_t* slice_tiles, int* scratch) {
+  if (tiles) write_tile_list(E, cnt, off, 1, kTileRows, tiles, scratch);
+  if (slice_tiles) write_tile_list(E, cnt, off, kDecodeSlices, kSliceTileRows, slice_tiles, scratch);
+}
+
 __global__ void __launch_bounds__(kCsrThreads, 1)
 build_csr_kernel(const int32_t* __restrict__ ids_g, int P, int E, int32_t* __restrict__ offsets,
                  int32_t* __restrict__ pair_ids, int32_t* __restrict__ active,
                  int32_t* __restrict__ n_active, int32_t* __restrict__ pair_pos,
-                 uint32_t* __restrict__ err, int ids_in_smem) {
+                 uint32_t* __restrict__ err, int ids_in_smem, int32_t* tiles,
+                 int32_t* slice_tiles) {
   extern __shared__ int smem[];
   int* hist = smem;                           // [kCsrWarps][E]
   int* scratch = smem + kCsrWarps * E;        // [kCsrWarps]
@@ -191,6 +219,7 @@ build_csr_kernel(const int32_t* __restrict__ ids_g, int P, int E, int32_t* __res
     offsets[E] = total;
     *n_active = act_total;
   }
+  write_tile_lists(E, cnt, off, tiles, slice_tiles, scratch);
   __syncthreads();
 
   // pass C: stable placement within each slice
@@ -245,7 +274,8 @@ csr_count_kernel(const int32_t* __restrict__ ids, int P, int E, int32_t* __restr
 // One CTA of kCsrThreads: thread e turns expert e's per-chunk counts into chunk starts.
 __global__ void __launch_bounds__(kCsrThreads, 1)
 csr_scan_kernel(int32_t* __restrict__ cnt, int n_chunks, int E, int32_t* __restrict__ offsets,
-                int32_t* __restrict__ active, int32_t* __restrict__ n_active) {
+                int32_t* __restrict__ active, int32_t* __restrict__ n_active, int32_t* tiles,
+                int32_t* slice_tiles) {
   __shared__ int scratch[kCsrWarps];
   pdl_wait();
   pdl_trigger();
@@ -269,6 +299,7 @@ csr_scan_kernel(int32_t* __restrict__ cnt, int n_chunks, int E, int32_t* __restr
     offsets[E] = total;
     *n_active = act_total;
   }
+  write_tile_lists(E, tot, off, tiles, slice_tiles, scratch);
 }
 
 __global__ void __launch_bounds__(kChunkThreads)
@@ -326,7 +357,7 @@ __global__ void __launch_bounds__(kCsrThreads, 1)
 csr_small_kernel(const int32_t* __restrict__ ids_g, int P, int E, int32_t* __restrict__ offsets,
                  int32_t* __restrict__ pair_ids, int32_t* __restrict__ active,
                  int32_t* __restrict__ n_active, int32_t* __restrict__ pair_pos,
-                 uint32_t* __restrict__ err) {
+                 uint32_t* __restrict__ err, int32_t* tiles, int32_t* slice_tiles) {
   __shared__ int hist[kMaxE];
   __shared__ int ids_s[kCsrSmallPairs];
   __shared__ int scratch[kCsrWarps];
@@ -361,6 +392,7 @@ csr_small_kernel(const int32_t* __restrict__ ids_g, int P, int E, int32_t* __res
     offsets[E] = total;
     *n_active = act_total;
   }
+  write_tile_lists(E, cnt, off, tiles, slice_tiles, scratch);
   __syncthreads();
   if (valid) {
     int rank = 0;
@@ -385,18 +417,20 @@ size_t csr_scratch_bytes(int P, int E) {
 }
 
 cudaError_t launch_build_csr(const int32_t* ids, int P, int k, int E, moe_csr csr,
-                             int32_t* pair_pos, uint32_t* err, int32_t* scratch, cudaStream_t s) {
+                             int32_t* pair_pos, uint32_t* err, int32_t* scratch, int32_t* tiles,
+                             int32_t* slice_tiles, cudaStream_t s) {
   (void)k;
   if (P <= kCsrSmallPairs)
     return launch_pdl(csr_small_kernel, dim3(1), dim3(kCsrThreads), 0, s, ids, P, E,
-                      csr.expert_offsets, csr.pair_ids, csr.active_experts, csr.n_active, pair_pos, err);
+                      csr.expert_offsets, csr.pair_ids, csr.active_experts, csr.n_active, pair_pos,
+                      err, tiles, slice_tiles);
   if (P >= kCsrGridMinPairs && scratch) {
     const int nb = (P + kChunkPairs - 1) / kChunkPairs;
     cudaError_t st = launch_pdl(csr_count_kernel, dim3(nb), dim3(kChunkThreads),
                                 (size_t)E * sizeof(int), s, ids, P, E, scratch, pair_pos, err);
     if (st != cudaSuccess) return st;
     st = launch_pdl(csr_scan_kernel, dim3(1), dim3(kCsrThreads), 0, s, scratch, nb, E,
-                    csr.expert_offsets, csr.active_experts, csr.n_active);
+                    csr.expert_offsets, csr.active_experts, csr.n_active, tiles, slice_tiles);
     if (st != cudaSuccess) return st;
     const size_t smem = (size_t)kChunkWarps * E * sizeof(int);
     st = cudaFuncSetAttribute(csr_place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -412,7 +446,7 @@ cudaError_t launch_build_csr(const int32_t* ids, int P, int k, int E, moe_csr cs
   if (st != cudaSuccess) return st;
   return launch_pdl(build_csr_kernel, dim3(1), dim3(kCsrThreads), smem, s, ids, P, E,
                     csr.expert_offsets, csr.pair_ids, csr.active_experts, csr.n_active, pair_pos,
-                    err, ids_in_smem);
+                    err, ids_in_smem, tiles, slice_tiles);
 }
 
 // ---------------------------------------------------------------------------
@@ -465,6 +499,6 @@ extern "C" moe_status moe_build_expert_csr_static(const int32_t* topk_ids, int32
   // and never read back by this entry point, so nothing needs clearing between calls
   cudaError_t st = launch_build_csr(topk_ids, T * k, k, E, csr, scratch,
                                     reinterpret_cast<uint32_t*>(scratch + kStaticMaxPairs),
-                                    nullptr, static_cast<cudaStream_t>(stream));
+                                    nullptr, nullptr, nullptr, static_cast<cudaStream_t>(stream));
   return st == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

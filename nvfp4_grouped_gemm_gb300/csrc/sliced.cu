@@ -38,7 +38,7 @@ namespace moe {
 
 namespace {
 
-constexpr int kSliceTile = 32;                     // B rows per tile: 8 pairs x 4 slices
+constexpr int kSliceTile = kSliceTileRows;         // B rows per tile: 8 pairs x 4 slices
 
 // A stage carries KSUB x 128 bytes of K per row as 128-byte-wide sub-tiles, so the MMA
 // thread's per-stage costs (barrier wait, commit) are paid once per 4*KSUB MMAs: two
@@ -87,6 +87,7 @@ struct SlicedArgs {
   const float* alpha = nullptr;   // [E] per-expert second-level weight scale, or none
 };
 
+
 __device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&a)[32]) {
   uint32_t r[32];
   asm volatile(
@@ -123,7 +124,10 @@ sliced_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
   constexpr int OFF_SB = OFF_SA + C::SA_STG;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  pdl_wait();                                       // tiles, slices (and h) are complete
+  // The tile list comes from the CSR call, complete before this grid started (the kernel
+  // before this one waited for it before letting this grid launch); the slices (and their
+  // exponents) come from the kernel just before, which the producer and the epilogue wait
+  // for where they first read them.
   const int n_tiles = args.tiles[0];
   const int4* tlist = reinterpret_cast<const int4*>(args.tiles + 4);
   const int n_work = n_tiles * args.n_tiles_n;
@@ -153,6 +157,8 @@ sliced_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the next kernel may launch now: it waits for this grid before reading what it writes
+  pdl_trigger();
   const uint32_t tmem = *tmem_holder;
   const uint32_t acc_col = tmem;
   const uint32_t sf_col0 = tmem + C::ACC_COLS;
@@ -164,6 +170,28 @@ sliced_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
       const int g = GATE_UP ? 1 : args.a_sf_group;
       const uint32_t tx_stg = (uint32_t)(GATE_UP ? C::SA_STG : 128 * sfrow) + (uint32_t)(C::NB * args.sb_w);
       const uint64_t wpol = l2_evict_first_policy();
+      // The slice half of a stage (B codes and B scale staging) reads what the previous
+      // kernel writes; the weight half depends only on the tile list.  The weight halves of
+      // the first STAGES stages are issued before waiting for the previous kernel, so the
+      // weight stream starts while the slices are still being formed.
+      auto issue_b = [&](int st, int ks, int row0, int nsub) {
+        unsigned char* sb = smem + st * C::STAGE_BYTES;
+        tma_load_2d(sb + OFF_SB, &tmap_sfb, ks * 16 * C::KSUB, row0, &stg_full[st]);
+#pragma unroll
+        for (int q = 0; q < C::KSUB; ++q)
+          if (q < nsub)
+            tma_load_2d(sb + OFF_B + q * C::B_SUB, &tmap_b, (ks * C::KSUB + q) * C::KB, row0,
+                        &full[st]);
+      };
+      int pend_st[C::STAGES], pend_ks[C::STAGES], pend_row[C::STAGES], pend_nsub[C::STAGES];
+      int npend = 0;
+      bool waited = false;
+      auto flush_pending = [&]() {
+        pdl_wait();
+        for (int i = 0; i < npend; ++i) issue_b(pend_st[i], pend_ks[i], pend_row[i], pend_nsub[i]);
+        npend = 0;
+        waited = true;
+      };
       int it = 0;
       // work descriptors are fetched two works ahead
       const int w1 = blockIdx.x + gridDim.x;
@@ -186,7 +214,6 @@ sliced_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
             tma_load_3d_hint(sb + OFF_SA, &tmap_sfa, ks * 16 * C::KSUB, 0, wrow, &stg_full[st], wpol);
           else
             tma_load_2d_hint(sb + OFF_SA, &tmap_sfa, 0, wrow / g, &stg_full[st], wpol);
-          tma_load_2d(sb + OFF_SB, &tmap_sfb, ks * 16 * C::KSUB, tile.x, &stg_full[st]);
 #pragma unroll
           for (int q = 0; q < C::KSUB; ++q) {
             if (q >= nsub) break;
@@ -195,12 +222,19 @@ sliced_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
               tma_load_3d_hint(sb + q * C::A_SUB, &tmap_a, x, 0, wrow, &full[st], wpol);
             else
               tma_load_2d_hint(sb + q * C::A_SUB, &tmap_a, x, wrow, &full[st], wpol);
-            tma_load_2d(sb + OFF_B + q * C::B_SUB, &tmap_b, x, tile.x, &full[st]);
+          }
+          if (waited) {
+            issue_b(st, ks, tile.x, nsub);
+          } else {
+            pend_st[npend] = st; pend_ks[npend] = ks; pend_row[npend] = tile.x; pend_nsub[npend] = nsub;
+            if (++npend == C::STAGES) flush_pending();
           }
         }
         tile = next;
         next = next2;
       }
+      // every issued stage gets its slice half (also when the loop ended early)
+      if (!waited) flush_pending();
       // drain: wait (bounded) until every issued stage has landed
       if (*abort_flag) {
         for (int s = 0; s < C::STAGES; ++s) {
@@ -317,6 +351,7 @@ sliced_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
     }
   } else {
     // ---------------- epilogue (warps 6..9, one TMEM lane quarter each) ----------------
+    pdl_wait();                                              // the slice exponents are complete
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;                     // weight row of the tile
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
@@ -405,12 +440,12 @@ cudaError_t launch_sliced_gate_up(const uint16_t* x_bf16, int T, int H, int F, i
   uint8_t* qs = reinterpret_cast<uint8_t*>(ws + L.qx_scales);
   int32_t* qe = reinterpret_cast<int32_t*>(ws + L.qx_exp);
   // the slices of x depend only on x: they are formed while the CSR kernel still runs, and
-  // only their stores wait for it; the tile list follows
+  // only their stores wait for it
   cudaError_t st = launch_slice_x(x_bf16, T, H, k, reinterpret_cast<const int32_t*>(ws + L.pair_pos),
                                   qc, qs, qe, s);
   if (st != cudaSuccess) return st;
-  int32_t* tiles = reinterpret_cast<int32_t*>(ws + L.tiles);
-  if ((st = launch_tiles(csr.expert_offsets, b.E, NS, kSliceTile, tiles, s)) != cudaSuccess) return st;
+  // the 32-row tile list over the slice rows was written by the CSR call
+  int32_t* tiles = reinterpret_cast<int32_t*>(ws + L.slice_tiles);
   // weights: [K bytes][gate, up][row], so the box {128 B, 2, 64} lands gate row i and up row i
   // as shared-memory rows 2i and 2i+1; the row extent stops F rows short of the bank so the
   // up coordinate (row + F) stays inside it
@@ -464,7 +499,7 @@ cudaError_t launch_sliced_down(const moe_nvfp4_bank& b, moe_csr csr, int T, int 
                 g * sfrow, 128 / g, false) ||
       !make_map(&msb, qs, sfh, sfh, rows, sbw, kSliceTile, false))
     return cudaErrorInvalidValue;
-  SlicedArgs a{qe, reinterpret_cast<const int32_t*>(ws + L.tiles),
+  SlicedArgs a{qe, reinterpret_cast<const int32_t*>(ws + L.slice_tiles),
                reinterpret_cast<float*>(ws + L.partial),
                reinterpret_cast<uint32_t*>(ws + L.error_word), F, H, H / 128, H, F, g, sbw};
   a.alpha = b.alpha;

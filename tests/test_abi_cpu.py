@@ -122,24 +122,28 @@ def test_host_validation_rejects_before_launch(lib):
 def test_kernel_launch_count_host_logic(lib):
     """The per-layer kernel count the library reports follows its own launch plan: decode
     below 256 pairs runs x-gather, gate/up, h-prep, down and combine after the CSR; from 256
-    pairs it runs tiles, x slices, the gate/up GEMM, h slices, the down GEMM and the combine;
-    prefill runs tiles, Q(x), the gate/up GEMM, Q(h), the down GEMM and the combine; the CSR
-    is one kernel below 4096 pairs and three from there on."""
+    pairs it runs x slices, the gate/up GEMM, h slices, the down GEMM and the combine;
+    prefill runs Q(x), the gate/up GEMM, Q(h), the down GEMM and the combine (the CSR call
+    writes the tile lists of both tensor-core forms); the CSR is one kernel below 4096 pairs
+    and three from there on."""
     assert moe.kernel_launches(8, 2560, 640, 512, 10) == 1 + 5
     assert moe.decode_tensor_core_min_pairs() == 256
     assert moe.kernel_launches(25, 2560, 640, 256, 10) == 1 + 5
-    assert moe.kernel_launches(26, 2560, 640, 256, 10) == 1 + 6
-    assert moe.kernel_launches(128, 2560, 640, 256, 10) == 1 + 6
-    assert moe.kernel_launches(4096, 4096, 640, 288, 8) == 3 + 6
-    assert moe.kernel_launches(4, 256, 64, 16, 2, moe.PATH_PREFILL) == 1 + 6
+    assert moe.kernel_launches(26, 2560, 640, 256, 10) == 1 + 5
+    assert moe.kernel_launches(128, 2560, 640, 256, 10) == 1 + 5
+    assert moe.kernel_launches(4096, 4096, 640, 288, 8) == 3 + 5
+    assert moe.kernel_launches(4, 256, 64, 16, 2, moe.PATH_PREFILL) == 1 + 5
     assert moe.kernel_launches(0, 256, 64, 16, 2) == 0
 
 
-@pytest.mark.parametrize("path,rpp,tile_rows", [(moe.PATH_PREFILL, 1, 128), (moe.PATH_DECODE, 4, 32)])
-def test_tile_list_always_fits_its_workspace_region(lib, path, rpp, tile_rows):
-    """The M-tile list (a count, then one 16-byte record per tile) never outgrows the
+@pytest.mark.parametrize("path,rpp,tile_rows,region_name",
+                         [(moe.PATH_PREFILL, 1, 128, "tiles"), (moe.PATH_DECODE, 4, 32, "slice_tiles")])
+def test_tile_list_always_fits_its_workspace_region(lib, path, rpp, tile_rows, region_name):
+    """Each tile list (a count, then one 16-byte record per tile) never outgrows the
     workspace region the layout gives it: an expert with m pairs needs ceil(m*rpp/tile_rows)
-    tiles, at most m*rpp/tile_rows + 1, and at most min(E, P) experts are active."""
+    tiles, at most m*rpp/tile_rows + 1, and at most min(E, P) experts are active.  Both
+    regions sit before h at offsets that depend only on P and E (the CSR call writes them
+    without knowing H, F or the path)."""
     rng = np.random.default_rng(23)
     H, F = 256, 64
     for _ in range(200):
@@ -150,8 +154,13 @@ def test_tile_list_always_fits_its_workspace_region(lib, path, rpp, tile_rows):
             T = (moe.decode_tensor_core_min_pairs() + k - 1) // k
         P = T * k
         L = moe.workspace_layout(T, H, F, E, k, path)
-        ends = sorted(v for n, v in L.items() if n != "total" and v > L["tiles"]) + [L["total"]]
-        region = ends[0] - L["tiles"]
+        L2 = moe.workspace_layout(T, 4096, 640, E, k, moe.PATH_PREFILL if path == moe.PATH_DECODE
+                                  else moe.PATH_DECODE)
+        for n in ("error_word", "pair_pos", "tiles", "slice_tiles", "h"):
+            assert L[n] == L2[n]
+        start = L[region_name]
+        ends = sorted(v for n, v in L.items() if n != "total" and v > start) + [L["total"]]
+        region = ends[0] - start
         skew = rng.uniform(0.5, 3.0)
         ids = np.minimum((rng.uniform(size=P) ** skew * E).astype(np.int64), E - 1)
         counts = np.bincount(ids, minlength=E)
