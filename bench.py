@@ -47,6 +47,9 @@ def parse():
     ap.add_argument("--batches", type=int, default=8, help="distinct input batches rotated")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=1)
+    ap.add_argument("--no-subresults", dest="subresults", action="store_false",
+                    help="time only --workload (by default N=1 also times " +
+                    ", ".join(("prefill", "verify_T128", "decode_T1", "union_U60")) + ")")
     return ap.parse_args()
 
 
@@ -178,6 +181,73 @@ def cpu_baseline(workload: str, tokens: int, seed: int = 0, threads: int = 1,
     return json.loads(r.stdout.strip().splitlines()[-1])
 
 
+def _oracle_window_worker(job):
+    """One window of the oracle in a spawned worker (BLAS pinned to one thread)."""
+    workload, seed, toks = job
+    import synth
+    import oracle
+    global _WL, _WL_KEY
+    if _WL is None or _WL_KEY != (workload, seed):
+        _WL, _WL_KEY = synth.by_name(workload, seed), (workload, seed)
+    wl = _WL
+    toks = np.asarray(toks)
+    if wl.logits is not None:
+        ids, w = oracle.route_topk(wl.logits[toks], wl.k)
+    else:
+        ids, w = wl.ids[toks], wl.weights[toks].astype(np.float64)
+    mode = "prefill" if is_prefill(wl.name) else "decode"
+    oracle.ffn(wl.x_bits[toks], ids, w, wl.gate_up, wl.down, mode=mode)
+    return int(len(np.unique(ids))), int(ids.size), int(len(toks))
+
+
+_WL, _WL_KEY = None, None
+
+
+def _pool_init():
+    global _WL, _WL_KEY
+    _WL, _WL_KEY = None, None
+
+
+def cpu_baseline_all_cores(workload: str, tokens: int, seed: int = 0, budget_s: float = 10.0):
+    """The oracle on every host core: one spawned process per core, each running whole
+    windows of `tokens` tokens (BLAS pinned to one thread per process), about `budget_s`
+    seconds of wall time after the workers have drawn the workload."""
+    import multiprocessing as mp
+    cores = os.cpu_count() or 1
+    env_keep = {v: os.environ.get(v) for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS",
+                                                "MKL_NUM_THREADS")}
+    for v in env_keep:
+        os.environ[v] = "1"
+    try:
+        import synth
+        T = synth.by_name(workload, seed).T
+        ctx = mp.get_context("spawn")
+        with ctx.Pool(cores, initializer=_pool_init) as pool:
+            # every worker draws the workload once (not timed), then a timed calibration round
+            warm = [(workload, seed, [(i * tokens + j) % T for j in range(tokens)])
+                    for i in range(cores)]
+            pool.map(_oracle_window_worker, warm, chunksize=1)
+            t0 = time.perf_counter()
+            pool.map(_oracle_window_worker, warm, chunksize=1)
+            per_round = max(time.perf_counter() - t0, 1e-3)
+            rounds = max(1, int(budget_s / per_round))
+            jobs = [(workload, seed, [(i * tokens + j) % T for j in range(tokens)])
+                    for i in range(cores * rounds)]
+            t0 = time.perf_counter()
+            res = pool.map(_oracle_window_worker, jobs, chunksize=1)
+            secs = time.perf_counter() - t0
+    except Exception as e:                       # reported in the line, never fatal
+        return {"error": repr(e)}
+    finally:
+        for v, old in env_keep.items():
+            if old is None:
+                os.environ.pop(v, None)
+            else:
+                os.environ[v] = old
+    return {"seconds": secs, "unique": sum(r[0] for r in res), "pairs": sum(r[1] for r in res),
+            "tokens": sum(r[2] for r in res), "windows": len(res), "cores": cores}
+
+
 def cpu_value(workload, info, H, F):
     import oracle
     if is_prefill(workload):
@@ -295,24 +365,22 @@ def metric_name(workload):
 # our arm
 # ---------------------------------------------------------------------------
 
-def run_ours(args):
+SUBRESULT_WORKLOADS = ("prefill", "verify_T128", "decode_T1", "union_U60")
+
+
+def measure(name, steps, warmup, batches, dev, rank, world):
+    """Time one workload: the whole layer as one CUDA graph per step (L2 flushed before
+    each), the layer split in three graphs for the breakdown and the roofline of the
+    dominant kernel, and the end-to-end call with host buffers.  Returns a dict of the
+    line's keys (everything but the CPU baseline and the clocks)."""
     import torch
-    import torch.distributed as dist
 
     import synth
     import oracle
     import nvfp4_grouped_gemm_gb300 as moe
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-
-    wl = synth.by_name(args.workload, seed=rank)
-    prefill = is_prefill(args.workload)
+    wl = synth.by_name(name, seed=rank)
+    prefill = is_prefill(name)
     path = moe.PATH_PREFILL if prefill else moe.PATH_DECODE
     gu = moe.NvFp4Bank.from_numpy(wl.gate_up, dev)
     dn = moe.NvFp4Bank.from_numpy(wl.down, dev)
@@ -320,7 +388,7 @@ def run_ours(args):
 
     # distinct batches of the same shape, rotated step by step
     rng = np.random.default_rng(1000 + rank)
-    nb = max(1, args.batches)
+    nb = max(1, batches)
     xs, lgs, idss, wss = [], [], [], []
     for b in range(nb):
         x = synth.f32_to_bf16_bits(rng.standard_normal((wl.T, wl.H), dtype=np.float32))
@@ -338,14 +406,11 @@ def run_ours(args):
     flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_out = torch.empty((), dtype=torch.float32, device=dev)
 
-    class _Flush:
+    def flush():
         """Write a buffer 4x the L2, then read another one: the write evicts everything,
         the read leaves only clean lines so no dirty write-back spills into the next step."""
-        @staticmethod
-        def zero_():
-            flush_w.zero_()
-            torch.sum(flush_r, dim=0, out=flush_out)
-    flush = _Flush
+        flush_w.zero_()
+        torch.sum(flush_r, dim=0, out=flush_out)
     bufs = layer.buffers(wl.T, path)
 
     def pre(b):           # route + CSR
@@ -392,7 +457,7 @@ def run_ours(args):
         for i in range(warm + n_steps):
             b = i % nb
             with torch.cuda.stream(stream):
-                flush.zero_()
+                flush()
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
@@ -402,27 +467,24 @@ def run_ours(args):
                 evs.append((b, e0, e1))
         return evs
 
-    timed(0, args.warmup)
+    timed(0, warmup)
     torch.cuda.synchronize(dev)
-    sampler = ClockSampler(local)
-    sampler.start()
     if world > 1:
+        import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize(dev)
     t_wall0 = time.perf_counter()
-    evs = timed(args.steps, 0)
+    evs = timed(steps, 0)
     torch.cuda.synchronize(dev)
     if world > 1:
         dist.barrier()
     t_wall = time.perf_counter() - t_wall0
-    clocks = sampler.stop()
 
     step_ms = [e0.elapsed_time(e1) for (_, e0, e1) in evs]
-    tot_ms = sum(step_ms)
+    tot_ms = max_over_ranks(sum(step_ms), dev)
     uniq_steps = [uniq[b] for (b, _, _) in evs]
-    tot_ms = max_over_ranks(tot_ms, dev)
     if prefill:
-        value = weak_scaling_value(flops_per_step * args.steps, world, tot_ms * 1e-3) / 1e12
+        value = weak_scaling_value(flops_per_step * steps, world, tot_ms * 1e-3) / 1e12
         unit = "TFLOP/s"
     else:
         value = weak_scaling_value(sum(u * per_expert for u in uniq_steps), world,
@@ -431,10 +493,10 @@ def run_ours(args):
 
     # per-kernel breakdown: the same layer as three graphs, L2 flushed before each step
     brk = []
-    for i in range(args.warmup + args.steps):
+    for i in range(warmup + steps):
         b = i % nb
         with torch.cuda.stream(stream):
-            flush.zero_()
+            flush()
             ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
             ev[0].record(stream)
             split_g[b][0].replay()
@@ -443,7 +505,7 @@ def run_ours(args):
             ev[2].record(stream)
             split_g[b][2].replay()
             ev[3].record(stream)
-        if i >= args.warmup:
+        if i >= warmup:
             brk.append((b, ev))
     torch.cuda.synchronize(dev)
     pre_ms = [ev[0].elapsed_time(ev[1]) for (_, ev) in brk]
@@ -451,14 +513,15 @@ def run_ours(args):
     dn_ms = [ev[2].elapsed_time(ev[3]) for (_, ev) in brk]
 
     peaks, _src = load_peaks()
+    pk, pk_src = peak_hbm(peaks)
+    extra = {}
     if prefill:
         # the gate/up GEMM streams every expert's gate/up bytes, reads Q(x) and writes h
         alg = (wl.E * 2 * wl.F * (wl.H // 2 + wl.H // 16) + wl.P * (wl.H // 2 + wl.H // 16)
                + wl.P * wl.F * 4)
         gu_s = float(np.mean(gu_ms)) * 1e-3
-        pk, pk_src = peak_hbm(peaks)
         fpk, fpk_src = peak_fp4(peaks, sustained=False)
-        ratio = recorded_traffic([args.workload, "prefill_T1024"], "gemm_kernel<128,1>")
+        ratio = recorded_traffic([name, "prefill_T1024"], "gemm_kernel<128,1>")
         gu_flops = wl.P * 2 * (2 * wl.F * wl.H)
         roof = {"bound": "hbm", "kernel": "prefill gate_up (graph of tiles + Q(x) + tcgen05 "
                 "block-scaled GEMM)", "achieved": alg / gu_s / 1e9, "peak": pk, "unit": "GB/s",
@@ -467,23 +530,33 @@ def run_ours(args):
                 "algorithmic_bytes_per_launch": alg,
                 "tensor": {"achieved_tflops": gu_flops / gu_s / 1e12, "peak_tflops": fpk,
                            "frac": gu_flops / gu_s / 1e12 / fpk, "peak_source": fpk_src}}
+        # the layer against the FP4 peak and against the rate its algorithmic bytes allow
+        # (every weight once, x in, y out) at the measured HBM bandwidth
+        layer_bytes = (wl.E * per_expert + wl.T * wl.H * 2 + wl.T * wl.H * 4)
+        attainable = pk * 1e9 * flops_per_step / layer_bytes / 1e12
+        extra["layer_roof"] = {"fp4_peak_tflops": fpk, "frac_of_fp4_peak": value / fpk,
+                               "fp4_peak_source": fpk_src,
+                               "attainable_tflops": attainable,
+                               "frac_of_attainable": value / attainable,
+                               "attainable_basis": f"{pk:.0f} GB/s ({pk_src}) x "
+                               f"{flops_per_step / layer_bytes:.1f} FLOP per algorithmic byte "
+                               f"({layer_bytes / 1e9:.3f} GB: weights once, x, y)"}
     else:
-        pk, pk_src = peak_hbm(peaks)
         gu_bytes = [uniq[b] * gu_bytes_per_expert for (b, _) in brk]
         ach = sum(gu_bytes) / (sum(gu_ms) * 1e-3) / 1e9
         alg = sum(gu_bytes) / len(gu_bytes)
         # from moe.decode_tensor_core_min_pairs() pairs the decode call runs the sliced form
         sliced = wl.P >= moe.decode_tensor_core_min_pairs()
-        ratio = (recorded_traffic([args.workload, "verify_T128"], "sliced_gemm_kernel<1>") if sliced
-                 else recorded_traffic([args.workload, "decode_T8"], "gate_up_tma_kernel"))
+        ratio = (recorded_traffic([name, "verify_T128"], "sliced_gemm_kernel<1>") if sliced
+                 else recorded_traffic([name, "decode_T8"], "gate_up_tma_kernel"))
         roof = {"bound": "hbm", "kernel": "decode gate_up+SiLU (moe_grouped_gate_up_silu_nvfp4; " +
                 ("x slices + tcgen05 sliced GEMM)" if sliced else "x staging + TMA-fed mma.sync kernel)"),
                 "achieved": ach, "peak": pk, "unit": "GB/s", "frac": ach / pk,
                 "traffic": None if ratio is None else ratio * alg, "peak_source": pk_src,
                 "algorithmic_bytes_per_launch": alg}
+        extra["layer_roof"] = {"frac_of_hbm": value / pk, "peak_source": pk_src}
 
     # end to end through the public API: pinned host inputs in, host result out, per step
-    e2e = None
     x_h = [xx.cpu().pin_memory() for xx in xs]
     l_h = [ll.cpu().pin_memory() for ll in lgs] if lgs else None
     i_h = [ii.cpu().pin_memory() for ii in idss] if idss else None
@@ -500,10 +573,10 @@ def run_ours(args):
         return layer.forward(x_d, ids=i_d, w=w_d, path=path, stream=stream)
     g_e2e = capture(e2e_layer)
     e2e_ms = []
-    for i in range(args.warmup + args.steps):
+    for i in range(warmup + steps):
         b = i % nb
         with torch.cuda.stream(stream):
-            flush.zero_()
+            flush()
             a0 = torch.cuda.Event(enable_timing=True)
             a1 = torch.cuda.Event(enable_timing=True)
             a0.record(stream)
@@ -516,24 +589,83 @@ def run_ours(args):
             g_e2e.replay()
             y_h.copy_(bufs["y"], non_blocking=True)
             a1.record(stream)
-        if i >= args.warmup:
+        if i >= warmup:
             e2e_ms.append((b, a0, a1))
     torch.cuda.synchronize(dev)
-    e_tot = sum(a0.elapsed_time(a1) for (_, a0, a1) in e2e_ms)
+    e_tot = max_over_ranks(sum(a0.elapsed_time(a1) for (_, a0, a1) in e2e_ms), dev)
     if prefill:
-        e_val = flops_per_step * len(e2e_ms) / (e_tot * 1e-3) / 1e12
+        e_val = weak_scaling_value(flops_per_step * len(e2e_ms), world, e_tot * 1e-3) / 1e12
     else:
-        e_val = sum(uniq[b] * per_expert for (b, _, _) in e2e_ms) / (e_tot * 1e-3) / 1e9
+        e_val = weak_scaling_value(sum(uniq[b] * per_expert for (b, _, _) in e2e_ms), world,
+                                   e_tot * 1e-3) / 1e9
     h2d = xs[0].numel() * 2 + (lgs[0].numel() * 4 if lgs else idss[0].numel() * 4 + wss[0].numel() * 4)
     e2e = {"value": e_val, "unit": unit, "h2d_bytes_per_step": int(h2d),
            "d2h_bytes_per_step": int(wl.T * wl.H * 4), "ms_per_step": e_tot / len(e2e_ms)}
+
+    # the library's own count of the kernels the CSR, gate/up and down calls launch, plus routing
+    launches_per_step = moe.kernel_launches(wl.T, wl.H, wl.F, wl.E, wl.k, path) + (1 if lgs else 0)
+    out = {
+        "workload": name, "wl": wl, "value": value, "unit": unit, "steps": steps,
+        "ms_per_step": tot_ms / steps,
+        "dtype": ("nvfp4 x nvfp4 block-scaled (e2m1, ue4m3), f32 accumulate" if prefill else
+                  "nvfp4 weights x 4 residual nvfp4 slices of each activation row, block-scaled "
+                  "tensor cores, f32 accumulate"
+                  if wl.P >= moe.decode_tensor_core_min_pairs() else
+                  "nvfp4 weights (e2m1 x ue4m3) * f16 activations, f32 accumulate"),
+        "config": {"workload": workload_desc(wl),
+                   "l2": "flushed before every step (512 MiB write, then 512 MiB read)",
+                   "batches_rotated": nb, "unique_experts_mean": float(np.mean(uniq_steps)),
+                   "path": "prefill" if prefill else "decode"},
+        "roofline": roof, "e2e": e2e,
+        "gpu_launches": launches_per_step * steps,
+        "breakdown_ms": {"route+csr": float(np.mean(pre_ms)), "gate_up": float(np.mean(gu_ms)),
+                         "down+combine": float(np.mean(dn_ms)),
+                         "note": "three graphs per step, L2 flushed before each step"},
+        "wall_s": t_wall,
+    }
+    out.update(extra)
+    # release this workload's device memory before the next one
+    del layer, gu, dn, bufs, full_g, split_g, g_e2e, xs, lgs, idss, wss, flush_w, flush_r
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    main = measure(args.workload, args.steps, args.warmup, args.batches, dev, rank, world)
+    clocks = sampler.stop()
+    subs = []
+    if args.subresults and world == 1:
+        for name in SUBRESULT_WORKLOADS:
+            if name == args.workload:
+                continue
+            sub_steps = max(3, min(args.steps, 10 if is_prefill(name) else 20))
+            sampler = ClockSampler(local)
+            sampler.start()
+            r = measure(name, sub_steps, max(3, args.warmup), args.batches, dev, rank, world)
+            r["clocks"] = sampler.stop()
+            subs.append(r)
 
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return
 
-    cpu = None
+    wl = main["wl"]
+    cpu, cpu_all = None, None
     if not args.no_cpu_baseline and world == 1:
         info = cpu_baseline(args.workload, args.cpu_sample_tokens)
         if "error" not in info:
@@ -545,33 +677,41 @@ def run_ours(args):
                              f"oracle, 1 thread, {info['seconds']:.1f} s"}
         else:
             cpu = {"error": info["error"][-200:]}
+        info = cpu_baseline_all_cores(args.workload, args.cpu_sample_tokens)
+        if "error" not in info:
+            v, u = cpu_value(args.workload, info, wl.H, wl.F)
+            cpu_all = {"value": v, "unit": u, "cores": info["cores"], "kind": "oracle",
+                       "sample": f"{info['windows']} windows of {args.cpu_sample_tokens} token(s) "
+                                 f"({info['tokens']} tokens, {info['pairs']} pairs, "
+                                 f"{info['unique']} expert streams in total) of "
+                                 f"{workload_desc(wl)}; float64 numpy oracle, one spawned "
+                                 f"process per core ({info['cores']} cores, os.cpu_count()), "
+                                 f"1 BLAS thread each, {info['seconds']:.1f} s wall"}
+        else:
+            cpu_all = {"error": info["error"][-200:]}
 
-    # the library's own count of the kernels the CSR, gate/up and down calls launch, plus routing
-    launches_per_step = moe.kernel_launches(wl.T, wl.H, wl.F, wl.E, wl.k, path) + (1 if lgs else 0)
+    def keys(r):
+        d = {k: r[k] for k in ("value", "unit", "ms_per_step", "dtype", "config", "roofline",
+                               "e2e", "breakdown_ms", "layer_roof") if k in r}
+        d["metric"] = metric_name(r["workload"])
+        d["steps"] = r["steps"]
+        if "clocks" in r:
+            d["clocks"] = r["clocks"]
+        return d
+
     line = {
-        "metric": metric_name(args.workload), "value": value, "unit": unit, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_ms / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": ("nvfp4 x nvfp4 block-scaled (e2m1, ue4m3), f32 accumulate" if prefill else
-                  "nvfp4 weights x 4 residual nvfp4 slices of each activation row, block-scaled "
-                  "tensor cores, f32 accumulate"
-                  if wl.P >= moe.decode_tensor_core_min_pairs() else
-                  "nvfp4 weights (e2m1 x ue4m3) * f16 activations, f32 accumulate"),
-        "data": "synthetic",
-        "config": {"workload": workload_desc(wl),
-                   "l2": "flushed before every step (512 MiB write, then 512 MiB read)",
-                   "batches_rotated": nb, "unique_experts_mean": float(np.mean(uniq_steps)),
-                   "path": "prefill" if prefill else "decode"},
-        "roofline": roof,
-        "cpu_baseline": cpu,
-        "e2e": e2e,
-        "gpu_launches": launches_per_step * args.steps,
-        "clocks": clocks,
-        "breakdown_ms": {"route+csr": float(np.mean(pre_ms)), "gate_up": float(np.mean(gu_ms)),
-                         "down+combine": float(np.mean(dn_ms)),
-                         "note": "three graphs per step, L2 flushed before each step"},
+        "metric": metric_name(args.workload), "value": main["value"], "unit": main["unit"],
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": main["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": main["dtype"], "data": "synthetic",
+        "config": main["config"], "roofline": main["roofline"],
+        "layer_roof": main.get("layer_roof"),
+        "cpu_baseline": cpu, "cpu_baseline_all_cores": cpu_all,
+        "e2e": main["e2e"], "gpu_launches": main["gpu_launches"], "clocks": clocks,
+        "breakdown_ms": main["breakdown_ms"],
         "timing": "one CUDA graph per step (the whole layer), CUDA events around each replay",
-        "wall_s": t_wall,
+        "wall_s": main["wall_s"],
+        "subresults": [keys(r) for r in subs],
     }
     print(json.dumps(line))
     if world > 1:
