@@ -88,7 +88,10 @@ struct Cfg {
   static constexpr int TMEM_COLS = TMEM_COLS_USED <= 256 ? 256 : 512;
   static constexpr int EPI_WARPS = 8;               // two per TMEM lane quarter
   static constexpr int THREADS = 32 * (6 + EPI_WARPS);   // TMA, MMA, 4 transposers, epilogue
-  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+  // DOWN: per epilogue warp a 4 KB staging image of its 32 x 64 f16 block of partials,
+  // written to global memory by one TMA store (128-byte swizzle, 1024-byte aligned)
+  static constexpr int OUT_STG = GATE_UP ? 0 : 8 * 4096;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + OUT_STG + 1024 /*align*/ + 256 /*barriers*/;
   static_assert(TMEM_COLS_USED <= 512, "TMEM budget");
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
   static_assert(SMEM <= 232448, "shared memory budget");
@@ -98,14 +101,15 @@ template <int BN, bool GATE_UP>
 __global__ void __launch_bounds__(448, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
             const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
-            const GemmArgs args) {
+            const __grid_constant__ CUtensorMap tmap_out, const GemmArgs args) {
   using C = Cfg<BN, GATE_UP>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   // full[s]: the stage's code tiles landed and its scale factors are in TMEM (TMA bytes +
   // one arrive per transposer warp); stg_full[s]: the scale staging images landed.
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  unsigned char* out_stg = smem + C::STAGES * C::STAGE_BYTES;   // DOWN: [8 warps][4 KB]
+  uint64_t* full = reinterpret_cast<uint64_t*>(out_stg + C::OUT_STG);
   uint64_t* stg_full = full + C::STAGES;
   uint64_t* empty = stg_full + C::STAGES;
   uint64_t* acc_full = empty + C::STAGES;           // [2]
@@ -357,25 +361,54 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[ab]);
-        if (valid) {
+        uint4 pk[8];                                   // the row's 64 values as f16, 8 x 16 B
 #pragma unroll
-          for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
-            for (int i = 0; i < 32; i += 8) {
-              uint32_t pk[4];
+          for (int i = 0; i < 32; i += 8) {
+            uint32_t q4[4];
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const float a0 = al * (fast ? v[c][i + 2 * q] * m : ldexpf(v[c][i + 2 * q], sx));
-                const float a1 = al * (fast ? v[c][i + 2 * q + 1] * m : ldexpf(v[c][i + 2 * q + 1], sx));
-                const __half2 h2 = __floats2half2_rn(a0, a1);
-                pk[q] = *reinterpret_cast<const uint32_t*>(&h2);
-              }
-              *reinterpret_cast<uint4*>(orow + half * 64 + c * 32 + i) =
-                  make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            for (int q = 0; q < 4; ++q) {
+              const float a0 = al * (fast ? v[c][i + 2 * q] * m : ldexpf(v[c][i + 2 * q], sx));
+              const float a1 = al * (fast ? v[c][i + 2 * q + 1] * m : ldexpf(v[c][i + 2 * q + 1], sx));
+              const __half2 h2 = __floats2half2_rn(a0, a1);
+              q4[q] = *reinterpret_cast<const uint32_t*>(&h2);
             }
+            pk[c * 4 + i / 8] = make_uint4(q4[0], q4[1], q4[2], q4[3]);
+          }
+        // A warp whose 32 rows are all valid stores them through shared memory with one TMA
+        // store, which keeps these 4 KB off the load/store path the transposer warps need; the
+        // rows of a ragged last M-tile that end inside this warp's quarter are stored directly
+        // (a 32-row box would reach into the next expert's rows).
+        if (tile.y - quarter * 32 >= 32) {
+          unsigned char* stg = out_stg + (warp - 6) * 4096;
+          const uint32_t sa = smem_u32(stg);
+          if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+          __syncwarp();
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t adr = sa + lane * 128 + ((c ^ (lane & 7)) << 4);
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(adr), "r"(pk[c].x),
+                         "r"(pk[c].y), "r"(pk[c].z), "r"(pk[c].w) : "memory");
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) {
+            const int x = (n0 + half * 64) * 2;                     // bytes
+            const int y = tile.x + quarter * 32;
+            asm volatile(
+                "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+                ::"l"(&tmap_out), "r"(x), "r"(y), "r"(sa) : "memory");
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+          }
+        } else if (valid) {
+#pragma unroll
+          for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(orow + half * 64 + c * 8) = pk[c];
         }
       }
     }
+    // every TMA store of the partials has finished reading shared memory
+    if (!GATE_UP && lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   }
 
   tc_fence_before();
@@ -393,7 +426,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
 // ---------------------------------------------------------------------------
 template <int BN, bool GATE_UP>
 cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msa,
-                     const CUtensorMap& msb, const GemmArgs& a, int max_tiles, cudaStream_t s) {
+                     const CUtensorMap& msb, const CUtensorMap& mo, const GemmArgs& a, int max_tiles,
+                     cudaStream_t s) {
   using C = Cfg<BN, GATE_UP>;
   auto kern = gemm_kernel<BN, GATE_UP>;
   cudaError_t st = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -401,7 +435,7 @@ cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtenso
   int grid = max_tiles * a.n_tiles_n;
   if (grid > num_sms()) grid = num_sms();
   if (grid < 1) grid = 1;
-  kern<<<grid, C::THREADS, C::SMEM, s>>>(ma, mb, msa, msb, a);
+  kern<<<grid, C::THREADS, C::SMEM, s>>>(ma, mb, msa, msb, mo, a);
   return cudaGetLastError();
 }
 
@@ -434,7 +468,7 @@ cudaError_t launch_prefill_gate_up(const uint16_t* x_bf16, int T, int H, int F, 
   a.alpha = b.alpha;
   a.n_group = a.n_tiles_n;                          // one group: M-tiles in order, N fastest
   const int max_tiles = P / 128 + (P < b.E ? P : b.E) + 1;
-  return run_gemm<BN, true>(ma, mb, msa, msb, a, max_tiles, s);
+  return run_gemm<BN, true>(ma, mb, msa, msb, ma /* unused */, a, max_tiles, s);
 }
 
 cudaError_t launch_prefill_down(const moe_nvfp4_bank& b, moe_csr csr, const float* w, int T, int H,
@@ -472,7 +506,11 @@ cudaError_t launch_prefill_down(const moe_nvfp4_bank& b, moe_csr csr, const floa
              reinterpret_cast<uint32_t*>(ws + L.error_word), P, F, H, H / BN, H, F, shift, g, 0};
   a.alpha = b.alpha;
   a.n_group = a.n_tiles_n;                          // one group: M-tiles in order, N fastest
-  if ((st = run_gemm<BN, false>(ma, mb, msa, msb, a, max_tiles, s)) != cudaSuccess) return st;
+  // the f16 partials [P][H]: box {64 columns, 32 rows}, 128-byte swizzle
+  CUtensorMap mo;
+  if (!make_map(&mo, ws + L.partial, (uint64_t)H * 2, (uint64_t)H * 2, P, 128, 32, true))
+    return cudaErrorInvalidValue;
+  if ((st = run_gemm<BN, false>(ma, mb, msa, msb, mo, a, max_tiles, s)) != cudaSuccess) return st;
   return launch_prefill_combine(w, T, H, F, k, 0, H, L, ws, y, s);
 }
 
