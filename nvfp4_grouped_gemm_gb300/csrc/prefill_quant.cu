@@ -1,7 +1,7 @@
 // Activation quantisers (the quantiser Q itself is in quant.cuh) and the prefill combine:
 //
-//   quant_x_kernel      Q(x): each token's bf16 row to NVFP4 with a power-of-two row scale,
-//                       written to every CSR row of the token's pairs
+//   quant_x_kernel      Q(x): each token's bf16 row to NVFP4 with a power-of-two row scale
+//                       (one CTA per token), written to every CSR row of the token's pairs
 //   quant_h_kernel      Q(h) per CSR row
 //   combine_f16_kernel  y[t] = sum_j w[t,j] * z16[pos_j] * 2^(e_j + c_F), ascending j
 //   slice_x_kernel, slice_h_kernel   the decode tensor-core form's four residual slices
@@ -17,69 +17,67 @@ namespace moe {
 namespace {
 
 // ---------------------------------------------------------------------------
-// Q(x): one warp per token, the result copied to each of the token's CSR rows
+// Q(x): one CTA per token, one thread per 16-value block (H <= 16 * blockDim.x), the
+// result copied to each of the token's CSR rows
 // ---------------------------------------------------------------------------
-// Lane l takes blocks l, l+32, ...: one pass for the row amax, a second (from L1) for the
-// block scales and codes.
 __global__ void __launch_bounds__(256) quant_x_kernel(const uint16_t* __restrict__ x, int T, int H,
                                                       int k, const int32_t* __restrict__ pair_pos,
                                                       uint8_t* __restrict__ qc,
                                                       uint8_t* __restrict__ qs,
                                                       int32_t* __restrict__ qe) {
-  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (t >= T) return;
-  const uint16_t* row = x + (size_t)t * H;
+  __shared__ float red[8];
+  __shared__ int s_pos[kMaxK];
+  const int t = blockIdx.x, b = threadIdx.x;
+  const int lane = b & 31, warp = b >> 5;
   const int nblk = H / 16;
+  const bool has = b < nblk;
+  if (b < k) s_pos[b] = pair_pos[(size_t)t * k + b];
+  uint32_t w[8];
+  {
+    const uint4* p = reinterpret_cast<const uint4*>(x + (size_t)t * H + b * 16);
+    const uint4 v0 = has ? __ldg(p) : make_uint4(0, 0, 0, 0);
+    const uint4 v1 = has ? __ldg(p + 1) : make_uint4(0, 0, 0, 0);
+    w[0] = v0.x; w[1] = v0.y; w[2] = v0.z; w[3] = v0.w;
+    w[4] = v1.x; w[5] = v1.y; w[6] = v1.z; w[7] = v1.w;
+  }
   float amax = 0.0f;
-  for (int b = lane; b < nblk; b += 32) {
-    const uint4* p = reinterpret_cast<const uint4*>(row + b * 16);
-    const uint4 v0 = __ldg(p), v1 = __ldg(p + 1);
-    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      amax = fmaxf(amax, fabsf(__uint_as_float(w[i] << 16)));
-      amax = fmaxf(amax, fabsf(__uint_as_float(w[i] & 0xffff0000u)));
-    }
+  for (int i = 0; i < 8; ++i) {
+    amax = fmaxf(amax, fabsf(__uint_as_float(w[i] << 16)));
+    amax = fmaxf(amax, fabsf(__uint_as_float(w[i] & 0xffff0000u)));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if (lane == 0) red[warp] = amax;
+  __syncthreads();
+  amax = 0.0f;
+  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) amax = fmaxf(amax, red[i]);
   const int s = row_exp_of(amax);
   const bool fast = s >= -127 && s <= 149;
   const float m = fast ? pow2f(-s) : 0.0f;
-  // lane j < k holds the CSR row of pair (t, j) (k <= 32)
-  const int mypos = lane < k ? pair_pos[(size_t)t * k + lane] : -1;
-  if (mypos >= 0) qe[mypos] = s;
-  for (int b0 = 0; b0 < nblk; b0 += 32) {          // warp-uniform
-    const int b = b0 + lane;
-    const bool has = b < nblk;
-    uint64_t codes = 0;
-    int sbc = 0;
-    if (has) {
-      const uint4* p = reinterpret_cast<const uint4*>(row + b * 16);
-      const uint4 v0 = __ldg(p), v1 = __ldg(p + 1);
-      const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-      float key[16];
-      uint32_t neg = 0;
-      float bmax = 0.0f;
+  if (!has) return;
+  float key[16];
+  uint32_t neg = 0;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
-        key[2 * i] = scale_down(fabsf(lo), s, fast, m);
-        key[2 * i + 1] = scale_down(fabsf(hi), s, fast, m);
-        neg |= (lo < 0.0f ? 1u : 0u) << (2 * i);
-        neg |= (hi < 0.0f ? 1u : 0u) << (2 * i + 1);
-        bmax = fmaxf(bmax, fmaxf(key[2 * i], key[2 * i + 1]));
-      }
-      sbc = ue4m3_code_of(bmax);
-      codes = quant_block(key, neg, sbc);
-    }
-    for (int j = 0; j < k; ++j) {
-      const int pj = __shfl_sync(0xffffffffu, mypos, j);
-      if (!has || pj < 0) continue;
-      *reinterpret_cast<uint64_t*>(qc + (size_t)pj * (H / 2) + b * 8) = codes;
-      qs[(size_t)pj * nblk + b] = (uint8_t)sbc;
-    }
+  for (int i = 0; i < 8; ++i) {
+    const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
+    key[2 * i] = fabsf(lo);
+    key[2 * i + 1] = fabsf(hi);
+    neg |= (lo < 0.0f ? 1u : 0u) << (2 * i);
+    neg |= (hi < 0.0f ? 1u : 0u) << (2 * i + 1);
+  }
+  scale_down_n(key, s, fast, m);
+  float bmax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, key[i]);
+  const int sbc = ue4m3_code_of(bmax);
+  const uint64_t codes = quant_block(key, neg, sbc);
+  for (int j = 0; j < k; ++j) {
+    const int pj = s_pos[j];
+    if (pj < 0) continue;                          // invalid expert id: the pair has no row
+    *reinterpret_cast<uint64_t*>(qc + (size_t)pj * (H / 2) + b * 8) = codes;
+    qs[(size_t)pj * nblk + b] = (uint8_t)sbc;
+    if (b == 0) qe[pj] = s;
   }
 }
 
@@ -125,17 +123,19 @@ __global__ void __launch_bounds__(256) quant_h_kernel(const float* __restrict__ 
     if (b >= nblk) break;
     float key[16];
     uint32_t neg = 0;
-    float bmax = 0.0f;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const float vv[4] = {v[i][q].x, v[i][q].y, v[i][q].z, v[i][q].w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        key[4 * q + e] = scale_down(fabsf(vv[e]), s, fast, m);
+        key[4 * q + e] = fabsf(vv[e]);
         neg |= (vv[e] < 0.0f ? 1u : 0u) << (4 * q + e);
-        bmax = fmaxf(bmax, key[4 * q + e]);
       }
     }
+    scale_down_n(key, s, fast, m);
+    float bmax = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) bmax = fmaxf(bmax, key[e]);
     const int sbc = ue4m3_code_of(bmax);
     *reinterpret_cast<uint64_t*>(qc + (size_t)r * (F / 2) + b * 8) = quant_block(key, neg, sbc);
     qs[(size_t)r * sf_pitch + b] = (uint8_t)sbc;
@@ -176,12 +176,12 @@ __device__ __forceinline__ uint32_t slice_part(float (&r)[EPT], float row_amax, 
   const bool fast = s >= -127 && s <= 149;
   const float m = fast ? pow2f(-s) : 0.0f;
   float key[EPT];
+#pragma unroll
+  for (int i = 0; i < EPT; ++i) key[i] = fabsf(r[i]);
+  scale_down_n(key, s, fast, m);
   float bmax = 0.0f;
 #pragma unroll
-  for (int i = 0; i < EPT; ++i) {
-    key[i] = scale_down(fabsf(r[i]), s, fast, m);
-    bmax = fmaxf(bmax, key[i]);
-  }
+  for (int i = 0; i < EPT; ++i) bmax = fmaxf(bmax, key[i]);
 #pragma unroll
   for (int o = 1; o < 16 / EPT; o <<= 1) bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, o));
   const int sbc = ue4m3_code_of(bmax);
@@ -190,8 +190,10 @@ __device__ __forceinline__ uint32_t slice_part(float (&r)[EPT], float row_amax, 
     const float sbv = ue4m3_val(sbc);
     const float t0 = 0.25f * sbv, t1 = 0.75f * sbv, t2 = 1.25f * sbv, t3 = 1.75f * sbv;
     const float t4 = 2.5f * sbv, t5 = 3.5f * sbv, t6 = 5.0f * sbv;
-    const bool up_fast = s >= -126 && s <= 127;
-    const float p = up_fast ? pow2f(s) : 0.0f;
+    // each code's value times 2^s, removed from the residual: the values are formed first,
+    // then scaled by one exact power-of-two multiply (ldexpf only when 2^s is not a float)
+    float qv[EPT];
+    uint32_t negs = 0;
 #pragma unroll
     for (int i = 0; i < EPT; ++i) {
       const float v = key[i];
@@ -201,11 +203,13 @@ __device__ __forceinline__ uint32_t slice_part(float (&r)[EPT], float row_amax, 
       const bool b0 = v > (b2 ? (b1 ? t6 : t4) : (b1 ? t2 : t0));
       const uint32_t mag = (b2 ? 4u : 0u) | (b1 ? 2u : 0u) | (b0 ? 1u : 0u);
       const bool neg = r[i] < 0.0f;
+      negs |= (neg ? 1u : 0u) << i;
       codes |= (mag | (neg ? 8u : 0u)) << (4 * i);
-      const float qv = e2m1_mag(mag) * sbv;               // exact: <= 6 significant bits
-      const float qs = up_fast ? qv * p : ldexpf(qv, s);
-      r[i] = neg ? r[i] + qs : r[i] - qs;
+      qv[i] = e2m1_mag(mag) * sbv;                        // exact: <= 6 significant bits
     }
+    scale_down_n(qv, -s, s >= -126 && s <= 127, s >= -126 && s <= 127 ? pow2f(s) : 0.0f);
+#pragma unroll
+    for (int i = 0; i < EPT; ++i) r[i] = ((negs >> i) & 1u) ? r[i] + qv[i] : r[i] - qv[i];
   }
   s_out = s;
   sbc_out = sbc;
@@ -368,7 +372,9 @@ combine_f16_kernel(const float* __restrict__ w, const int32_t* __restrict__ pair
 
 cudaError_t launch_quant_x(const uint16_t* x_bf16, int T, int H, int k, const int32_t* pair_pos,
                            uint8_t* qc, uint8_t* qs, int32_t* qe, cudaStream_t s) {
-  quant_x_kernel<<<(T + 7) / 8, 256, 0, s>>>(x_bf16, T, H, k, pair_pos, qc, qs, qe);
+  const int threads = (H / 16 + 31) / 32 * 32;     // one thread per 16-value block
+  if (threads > 256) return cudaErrorInvalidValue;
+  quant_x_kernel<<<T, threads, 0, s>>>(x_bf16, T, H, k, pair_pos, qc, qs, qe);
   return cudaGetLastError();
 }
 

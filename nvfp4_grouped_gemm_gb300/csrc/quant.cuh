@@ -53,10 +53,19 @@ __device__ __forceinline__ int ue4m3_code_of(float key) {
   return cand;
 }
 
-// |v| * 2^-s: one multiply by the exact power of two when 2^-s is a float (the same
-// correctly rounded value as ldexpf), else ldexpf.
-__device__ __forceinline__ float scale_down(float v, int s, bool fast, float m) {
-  return fast ? v * m : ldexpf(v, -s);
+// key[i] * 2^-s in place: one multiply by the exact power of two m = 2^-s when that is a
+// float (the same correctly rounded value as ldexpf), else ldexpf.  The choice is made once
+// for the whole array, so the common case is a plain multiply per element (a per-element
+// select could let the compiler evaluate the long ldexpf path for every element).
+template <int N>
+__device__ __forceinline__ void scale_down_n(float (&key)[N], int s, bool fast, float m) {
+  if (fast) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) key[i] *= m;
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; ++i) key[i] = ldexpf(key[i], -s);
+  }
 }
 
 // Row exponent: smallest s with amax <= 2688 * 2^s (2688 = 0.65625 * 2^12).
