@@ -422,6 +422,422 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
 }
 
 // ---------------------------------------------------------------------------
+// down GEMM with the activation tile resident (K = F <= 256 * KS)
+// ---------------------------------------------------------------------------
+// Work comes in chunks: one M-tile (128 CSR rows of Q(h)) x up to kChunkN consecutive
+// N-tiles of 128 down rows.  The chunk's A tile (KS k-stages of 128 B codes per row, with
+// their scale staging) is loaded once and its scale factors go to TMEM once; only the
+// weights then stream, through a ring of B stages (codes + scale staging, 20 KiB), so
+// more weight bytes are in flight per SM than with A re-read every stage.  A, its scale
+// staging and its TMEM scale factors are double-buffered: chunk i uses buffer i % 2, and
+// the producer loads chunk i+1's A right after chunk i's first N-tile of weights, a whole
+// chunk before the MMAs need it (an A tile takes about 2 us to land even from L2 while the
+// weights stream).  The epilogue stages its partials in 2 KiB per warp (two 32-column TMA
+// stores, 64-byte swizzle), which leaves room for five B stages.  Warp roles and outputs
+// are those of gemm_kernel<128, false>.
+constexpr int kChunkN = 4;
+constexpr int kResidentKS = 3;                      // k-stages of A held (F <= 768)
+
+struct DCfg {
+  static constexpr int KS = kResidentKS;
+  static constexpr int BN = 128;
+  static constexpr int KB = 128;                    // bytes of K per k-stage (256 elements)
+  static constexpr int A_CODES = 128 * KB;          // per k-stage
+  static constexpr int A_SA = 128 * 16;             // per k-stage: scale staging [128][16 B]
+  static constexpr int A_BUF = KS * A_CODES;        // one A buffer's codes
+  static constexpr int SA_BUF = KS * A_SA;          // one A buffer's scale staging
+  static constexpr int A_BYTES = 2 * (A_BUF + SA_BUF);
+  static constexpr int B_CODES = BN * KB;
+  static constexpr int B_SB = BN * 32;              // 32-byte windows of g-grouped scale rows
+  static constexpr int STAGE_BYTES = B_CODES + B_SB;
+  static constexpr int OUT_STG = 8 * 2048;          // per epilogue warp: 32 rows x 32 f16
+  static constexpr int STAGES = (232448 - 1024 - 512 - OUT_STG - A_BYTES) / STAGE_BYTES;
+  static constexpr int ACC_COLS = 2 * BN;
+  static constexpr int SFA_COLS = KS * 16;          // 4 columns per k-step, per buffer
+  static constexpr int SFB_COLS = 16;               // per stage
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int EPI_WARPS = 8;
+  static constexpr int THREADS = 32 * (6 + EPI_WARPS);
+  static constexpr int SMEM = A_BYTES + STAGES * STAGE_BYTES + OUT_STG + 512 + 1024;
+  static_assert(STAGES >= 5, "B ring depth");
+  static_assert(ACC_COLS + 2 * SFA_COLS + STAGES * SFB_COLS <= TMEM_COLS, "TMEM budget");
+  static_assert(A_BUF % 1024 == 0 && (2 * A_BUF + 2 * SA_BUF) % 1024 == 0 &&
+                STAGE_BYTES % 1024 == 0, "alignment");
+  static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+// chunk c -> M-tile and its N-tile range [n_lo, n_hi)
+__device__ __forceinline__ void chunk_range(int c, int nr, int n_tiles_n, int& m, int& n_lo,
+                                            int& n_hi) {
+  m = c / nr;
+  n_lo = (c - m * nr) * kChunkN;
+  n_hi = min(n_tiles_n, n_lo + kChunkN);
+}
+
+__global__ void __launch_bounds__(448, 1)
+down_resident_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                     const __grid_constant__ CUtensorMap tmap_b,
+                     const __grid_constant__ CUtensorMap tmap_sfa,
+                     const __grid_constant__ CUtensorMap tmap_sfb,
+                     const __grid_constant__ CUtensorMap tmap_out, const GemmArgs args) {
+  using C = DCfg;
+  constexpr int BN = C::BN, KS = C::KS;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // layout: A codes [2][KS][16 KiB] | A scale staging [2][KS][2 KiB] | B ring | epilogue staging
+  unsigned char* a_codes = smem;
+  unsigned char* a_sa = smem + 2 * C::A_BUF;
+  unsigned char* bring = smem + C::A_BYTES;
+  unsigned char* out_stg = bring + C::STAGES * C::STAGE_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(out_stg + C::OUT_STG);   // B codes + B SF in TMEM
+  uint64_t* stg_full = full + C::STAGES;            // B scale staging landed
+  uint64_t* empty = stg_full + C::STAGES;
+  uint64_t* acc_full = empty + C::STAGES;           // [2]
+  uint64_t* acc_empty = acc_full + 2;               // [2]
+  uint64_t* a_full = acc_empty + 2;                 // [2] A codes of buffer b landed
+  uint64_t* a_stg = a_full + 2;                     // [2] A scale staging of buffer b landed
+  uint64_t* a_sf = a_stg + 2;                       // [2] A scale factors of buffer b in TMEM
+  uint64_t* a_empty = a_sf + 2;                     // [2] the MMAs reading buffer b are done
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(a_empty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  static_assert((3 * C::STAGES + 12) * 8 + 8 <= 512, "barrier area");
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_mtiles = args.tiles[0];
+  const int4* tlist = reinterpret_cast<const int4*>(args.tiles + 4);
+  const int nr = (args.n_tiles_n + kChunkN - 1) / kChunkN;
+  const int n_chunk = n_mtiles * nr;
+  const int k_stages = (args.K / 2 + C::KB - 1) / C::KB;   // <= KS (checked by the host)
+  const int sfrow = args.K / 16;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1 + 4);
+      mbar_init(&stg_full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], C::EPI_WARPS);
+      mbar_init(&a_full[b], 1);                      // TMA expect_tx
+      mbar_init(&a_stg[b], 1);                       // TMA expect_tx
+      mbar_init(&a_sf[b], 4);                        // 4 transposer warps
+      mbar_init(&a_empty[b], 1);                     // MMA commit
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(smem_u32(tmem_holder)), "n"(C::TMEM_COLS) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const uint32_t acc_col = tmem;
+  const uint32_t sfa_col0 = tmem + C::ACC_COLS;                // A scale factors, 2 buffers
+  const uint32_t sfb_col0 = sfa_col0 + 2 * C::SFA_COLS;        // per-stage B scale factors
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      const int g = args.b_sf_group;
+      const int sub_rows = BN / g, sub_w = g == 1 ? 16 : 32;
+      const uint32_t tx_sb = (uint32_t)(g == 1 ? BN * 16 : BN * 32);
+      const uint64_t wpol = l2_evict_first_policy();
+      int it = 0, ca = 0;                          // B stage sequence, chunk sequence
+      int a_cnt = 0;                               // A tiles issued
+      bool ok = true;
+      // A of the chunk with sequence number q (chunk blockIdx.x + q * gridDim.x) into buffer
+      // q % 2, once the MMAs of chunk q - 2 (its last reader) are done
+      auto load_a = [&](int q) -> bool {
+        const int c = blockIdx.x + q * gridDim.x;
+        if (c >= n_chunk) return true;
+        int m, n_lo, n_hi;
+        chunk_range(c, nr, args.n_tiles_n, m, n_lo, n_hi);
+        const int4 tile = tlist[m];
+        const int b = q & 1;
+        if (!mbar_wait(&a_empty[b], ((q >> 1) & 1) ^ 1, abort_flag, args.err)) return false;
+        mbar_expect_tx(&a_stg[b], (uint32_t)(k_stages * C::A_SA));
+        for (int ks = 0; ks < k_stages; ++ks)
+          tma_load_2d(a_sa + b * C::SA_BUF + ks * C::A_SA, &tmap_sfa, ks * 16, tile.x, &a_stg[b]);
+        mbar_expect_tx(&a_full[b], (uint32_t)(k_stages * C::A_CODES));
+        for (int ks = 0; ks < k_stages; ++ks)
+          tma_load_2d(a_codes + b * C::A_BUF + ks * C::A_CODES, &tmap_a, ks * C::KB, tile.x,
+                      &a_full[b]);
+        ++a_cnt;
+        return true;
+      };
+      ok = load_a(0);
+      for (int c = blockIdx.x; c < n_chunk && ok && !*abort_flag; c += gridDim.x, ++ca) {
+        int m, n_lo, n_hi;
+        chunk_range(c, nr, args.n_tiles_n, m, n_lo, n_hi);
+        const int4 tile = tlist[m];
+        for (int n = n_lo; n < n_hi && ok; ++n) {
+          const int brow = tile.z * args.rows_per_expert + n * BN;
+          for (int ks = 0; ks < k_stages; ++ks, ++it) {
+            const int st = it % C::STAGES;
+            if (!mbar_wait(&empty[st], ((it / C::STAGES) & 1) ^ 1, abort_flag, args.err)) {
+              ok = false;
+              break;
+            }
+            unsigned char* sb = bring + st * C::STAGE_BYTES;
+            mbar_expect_tx(&stg_full[st], tx_sb);
+            mbar_expect_tx(&full[st], C::B_CODES);
+            for (int s2 = 0; s2 < g; ++s2) {
+              const int x = ((s2 * sfrow + 16 * ks) >> 4) << 4;
+              tma_load_2d(sb + C::B_CODES + s2 * sub_rows * sub_w, &tmap_sfb, x, brow / g,
+                          &stg_full[st]);
+            }
+            tma_load_2d_hint(sb, &tmap_b, ks * C::KB, brow, &full[st], wpol);
+          }
+          // the next chunk's A, after this chunk's first N-tile of weights
+          if (n == n_lo && ok) ok = load_a(ca + 1);
+        }
+      }
+      // drain: wait (bounded) until every issued copy has landed
+      if (!ok || *abort_flag) {
+        const uint64_t t0 = global_ns();
+        for (int s = 0; s < C::STAGES; ++s) {
+          if (it <= s) continue;
+          const int last = s + ((it - 1 - s) / C::STAGES) * C::STAGES;
+          while ((!mbar_try(&stg_full[s], (last / C::STAGES) & 1) ||
+                  !mbar_try(&full[s], (last / C::STAGES) & 1)) &&
+                 global_ns() - t0 < 100000000ull) {
+          }
+        }
+        for (int q = a_cnt - 2; q < a_cnt; ++q) {
+          if (q < 0) continue;
+          const uint32_t par = (q >> 1) & 1;
+          while ((!mbar_try(&a_stg[q & 1], par) || !mbar_try(&a_full[q & 1], par)) &&
+                 global_ns() - t0 < 100000000ull) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = mxf4_idesc(128, BN);
+      const uint64_t a_desc0 = smem_desc(smem_u32(a_codes), 16, 1024, 2);
+      const uint64_t b_desc0 = smem_desc(smem_u32(bring), 16, 1024, 2);
+      int it = 0, tcount = 0, ca = 0;
+      bool ok = true;
+      for (int c = blockIdx.x; c < n_chunk && ok && !*abort_flag; c += gridDim.x, ++ca) {
+        int m, n_lo, n_hi;
+        chunk_range(c, nr, args.n_tiles_n, m, n_lo, n_hi);
+        const int b = ca & 1;
+        const uint32_t par = (ca >> 1) & 1;
+        // the chunk's A codes landed and its scale factors are in TMEM (buffer b)
+        if (!mbar_wait(&a_sf[b], par, abort_flag, args.err) ||
+            !mbar_wait(&a_full[b], par, abort_flag, args.err))
+          break;
+        tc_fence_after();
+        const uint32_t sfa_col = sfa_col0 + b * C::SFA_COLS;
+        const uint64_t a_base = a_desc0 + (uint64_t)((b * C::A_BUF) >> 4);
+        for (int n = n_lo; n < n_hi && ok; ++n, ++tcount) {
+          const int ab = tcount & 1;
+          if (!mbar_wait(&acc_empty[ab], ((tcount >> 1) & 1) ^ 1, abort_flag, args.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t acc = acc_col + ab * BN;
+          for (int ks = 0; ks < k_stages; ++ks, ++it) {
+            const int st = it % C::STAGES;
+            if (!mbar_wait(&full[st], (it / C::STAGES) & 1, abort_flag, args.err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t ao = (uint64_t)((ks * C::A_CODES) >> 4);
+            const uint64_t bo = (uint64_t)((st * C::STAGE_BYTES) >> 4);
+            const uint32_t sfb = sfb_col0 + st * C::SFB_COLS;
+            const int nk = min(4, (sfrow - 16 * ks) >> 2);   // k-steps past K are skipped
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (j < nk)
+                tc_mma(acc, a_base + ao + ((32 * j) >> 4), b_desc0 + bo + ((32 * j) >> 4), idesc,
+                       sfa_col + 16 * ks + 4 * j, sfb + 4 * j, (ks | j) != 0);
+            tc_commit(&empty[st]);
+          }
+          if (!ok) break;
+          tc_commit(&acc_full[ab]);
+        }
+        // buffer b (codes, staging, TMEM scale factors) may be refilled once these are done
+        tc_commit(&a_empty[b]);
+      }
+    }
+  } else if (warp < 6) {
+    // ---------------- scale-factor transposers (128 threads, one TMEM lane quarter each) ---
+    // The weight scale factors of every B stage, as in gemm_kernel; and the A scale factors
+    // of each chunk once, into TMEM buffer q % 2 (lane r of every quarter holds, in columns
+    // 16 ks + 4 j + x, the k-step (ks, j) scales of row r + 32 x), in the producer's order:
+    // chunk 0's first, chunk q+1's after chunk q's first N-tile of weights.  A chunk's
+    // staging lands only after the MMAs that read that buffer before are done.
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const int g = args.b_sf_group;
+    const int sub_rows = BN / g, sub_w = g == 1 ? 16 : 32;
+    auto write_sfa = [&](int q) -> bool {
+      const int c = blockIdx.x + q * gridDim.x;
+      if (c >= n_chunk) return true;
+      const int b = q & 1;
+      if (!mbar_wait_warp(&a_stg[b], (q >> 1) & 1, abort_flag, args.err)) return false;
+      tc_fence_after();
+      for (int ks = 0; ks < KS; ++ks) {
+        const int nvalid = ks < k_stages ? min(4, (sfrow - 16 * ks) >> 2) : 0;
+        uint32_t va[16];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const uint4 a4 = ks < k_stages
+                               ? lds128(smem_u32(a_sa + b * C::SA_BUF + ks * C::A_SA) + 16 * (lane + 32 * x))
+                               : make_uint4(0, 0, 0, 0);
+          const uint32_t a[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) va[4 * j + x] = j < nvalid ? a[j] : 0u;
+        }
+        tc_st16(sfa_col0 + b * C::SFA_COLS + 16 * ks + lane_base, va);
+      }
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&a_sf[b]);
+      return true;
+    };
+    bool ok = write_sfa(0);
+    int it = 0, ca = 0;
+    for (int c = blockIdx.x; c < n_chunk && ok; c += gridDim.x, ++ca) {
+      int m, n_lo, n_hi;
+      chunk_range(c, nr, args.n_tiles_n, m, n_lo, n_hi);
+      for (int n = n_lo; n < n_hi && ok; ++n) {
+        for (int ks = 0; ks < k_stages; ++ks, ++it) {
+          const int st = it % C::STAGES;
+          if (!mbar_wait_warp(&stg_full[st], (it / C::STAGES) & 1, abort_flag, args.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sb = smem_u32(bring + st * C::STAGE_BYTES + C::B_CODES);
+          const int nvalid = min(4, (sfrow - 16 * ks) >> 2);
+          uint32_t vb[16];
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            const int row = lane + 32 * x;
+            const int bs = row % g, bi = row / g;
+            const int byte0 = bs * sfrow + 16 * ks;
+            const uint32_t src = sb + bs * sub_rows * sub_w + bi * sub_w + (byte0 & 15);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) vb[4 * j + x] = j < nvalid ? lds32(src + 4 * j) : 0u;
+          }
+          tc_st16(sfb_col0 + st * C::SFB_COLS + lane_base, vb);
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&full[st]);
+        }
+        if (n == n_lo && ok) ok = write_sfa(ca + 1);
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 6..13: lane quarter warp % 4, column half) ----------
+    const int quarter = warp & 3;
+    const int half = (warp - 6) >> 2;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    const int sx = -args.down_shift;
+    const bool fast = sx >= -149 && sx <= 127;
+    const float mul = fast ? pow2f(sx) : 0.0f;
+    int tcount = 0;
+    bool ok = true;
+    for (int c = blockIdx.x; c < n_chunk && ok; c += gridDim.x) {
+      int m, n_lo, n_hi;
+      chunk_range(c, nr, args.n_tiles_n, m, n_lo, n_hi);
+      const int4 tile = tlist[m];
+      const bool valid = row < tile.y;
+      const int pos = tile.x + row;
+      const float al = args.alpha ? __ldg(args.alpha + tile.z) : 1.0f;
+      for (int n = n_lo; n < n_hi; ++n, ++tcount) {
+        const int ab = tcount & 1;
+        const int n0 = n * BN;
+        if (!mbar_wait_warp(&acc_full[ab], (tcount >> 1) & 1, abort_flag, args.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t acc = acc_col + ab * BN + lane_base;
+        __half* orow = reinterpret_cast<__half*>(args.out) + (size_t)(valid ? pos : 0) * args.out_cols + n0;
+        float v[2][32];
+        tc_ld32x2(acc + half * 64, acc + half * 64 + 32, v[0], v[1]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[ab]);
+        uint4 pk[8];                                   // the row's 64 values as f16, 8 x 16 B
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            uint32_t q4[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float a0 = al * (fast ? v[cc][i + 2 * q] * mul : ldexpf(v[cc][i + 2 * q], sx));
+              const float a1 = al * (fast ? v[cc][i + 2 * q + 1] * mul : ldexpf(v[cc][i + 2 * q + 1], sx));
+              const __half2 h2 = __floats2half2_rn(a0, a1);
+              q4[q] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+            pk[cc * 4 + i / 8] = make_uint4(q4[0], q4[1], q4[2], q4[3]);
+          }
+        // full 32-row quarters through shared memory, 32 columns at a time (one TMA store
+        // each; 64-byte swizzle: 16-byte chunk c of row r at r*64 + 16*(c ^ ((r >> 1) & 3)),
+        // conflict-free); the rows of a ragged last M-tile that end inside this quarter
+        // directly (a box would reach the next expert's rows)
+        if (tile.y - quarter * 32 >= 32) {
+          const uint32_t sa = smem_u32(out_stg + (warp - 6) * 2048);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+            __syncwarp();
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+              const uint4 v4 = pk[hh * 4 + cc];
+              const uint32_t adr = sa + lane * 64 + ((cc ^ ((lane >> 1) & 3)) << 4);
+              asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(adr), "r"(v4.x),
+                           "r"(v4.y), "r"(v4.z), "r"(v4.w) : "memory");
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) {
+              const int x = (n0 + half * 64 + hh * 32) * 2;
+              const int y = tile.x + quarter * 32;
+              asm volatile(
+                  "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+                  ::"l"(&tmap_out), "r"(x), "r"(y), "r"(sa) : "memory");
+              asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            }
+          }
+        } else if (valid) {
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc) *reinterpret_cast<uint4*>(orow + half * 64 + cc * 8) = pk[cc];
+        }
+      }
+    }
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "n"(C::TMEM_COLS) : "memory");
+  }
+}
+
+// ---------------------------------------------------------------------------
 // host helpers
 // ---------------------------------------------------------------------------
 template <int BN, bool GATE_UP>
@@ -433,6 +849,20 @@ cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtenso
   cudaError_t st = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (st != cudaSuccess) return st;
   int grid = max_tiles * a.n_tiles_n;
+  if (grid > num_sms()) grid = num_sms();
+  if (grid < 1) grid = 1;
+  kern<<<grid, C::THREADS, C::SMEM, s>>>(ma, mb, msa, msb, mo, a);
+  return cudaGetLastError();
+}
+
+cudaError_t run_down_resident(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msa,
+                              const CUtensorMap& msb, const CUtensorMap& mo, const GemmArgs& a,
+                              int max_tiles, cudaStream_t s) {
+  using C = DCfg;
+  auto kern = down_resident_kernel;
+  cudaError_t st = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (st != cudaSuccess) return st;
+  int grid = max_tiles * ((a.n_tiles_n + kChunkN - 1) / kChunkN);
   if (grid > num_sms()) grid = num_sms();
   if (grid < 1) grid = 1;
   kern<<<grid, C::THREADS, C::SMEM, s>>>(ma, mb, msa, msb, mo, a);
@@ -510,7 +940,18 @@ cudaError_t launch_prefill_down(const moe_nvfp4_bank& b, moe_csr csr, const floa
   CUtensorMap mo;
   if (!make_map(&mo, ws + L.partial, (uint64_t)H * 2, (uint64_t)H * 2, P, 128, 32, true))
     return cudaErrorInvalidValue;
-  if ((st = run_gemm<BN, false>(ma, mb, msa, msb, mo, a, max_tiles, s)) != cudaSuccess) return st;
+  // K = F of up to kResidentKS k-stages (F <= 768): the Q(h) tile stays resident and only
+  // the weights stream; beyond that the general kernel re-reads both operands per stage
+  if ((F / 2 + 127) / 128 <= kResidentKS) {
+    // its epilogue stores 32 columns per box: {64 bytes, 32 rows}, 64-byte swizzle
+    CUtensorMap mo32;
+    if (!make_map(&mo32, ws + L.partial, (uint64_t)H * 2, (uint64_t)H * 2, P, 64, 32,
+                  CU_TENSOR_MAP_SWIZZLE_64B))
+      return cudaErrorInvalidValue;
+    st = run_down_resident(ma, mb, msa, msb, mo32, a, max_tiles, s);
+  } else
+    st = run_gemm<BN, false>(ma, mb, msa, msb, mo, a, max_tiles, s);
+  if (st != cudaSuccess) return st;
   return launch_prefill_combine(w, T, H, F, k, 0, H, L, ws, y, s);
 }
 

@@ -112,7 +112,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // 128-byte swizzle for code tiles, none for scale staging.  Boxes reaching past row_bytes
 // or rows read zeros.
 bool make_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t pitch,
-              uint64_t rows, uint32_t box_w, uint32_t box_rows, bool swizzle) {
+              uint64_t rows, uint32_t box_w, uint32_t box_rows, CUtensorMapSwizzle swizzle) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {row_bytes, rows};
@@ -120,10 +120,14 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t p
   cuuint32_t box[2] = {box_w, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+bool make_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t pitch,
+              uint64_t rows, uint32_t box_w, uint32_t box_rows, bool swizzle) {
+  return make_map(map, base, row_bytes, pitch, rows, box_w, box_rows,
+                  swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 // 3-D u8 tensor map (dims[0] innermost, strides in bytes of dims 1..2) with box `box`.

@@ -184,6 +184,19 @@ def test_prefill_numerics_at_decode_sizes(T):
     res, info = _stages(wl, run, np.arange(T))
 
 
+@pytest.mark.parametrize("F", [768, 832, 1152])
+def test_prefill_ff_widths(F):
+    """The down GEMM's forms across F: the Q(h) tile held in shared memory for up to three
+    k-stages (F = 768, all three full) and re-read every stage beyond that (F = 832 with a
+    half-empty last stage, F = 1152); two M-tiles per expert, every token checked."""
+    wl = synth.logits_workload(f"prefill_F{F}", 256, 512, F, 4, 4, seed=5)
+    run = run_layer(wl, path=PF)
+    assert run.err == 0
+    toks = np.arange(wl.T)
+    res, info = _stages(wl, run, toks)
+    _down_from_oracle_h(wl, run, res, toks)
+
+
 def test_prefill_per_expert_alpha():
     """Prefill with a per-expert second-level scale alpha on both banks (down's <= 2)."""
     wl = synth.prefill(seed=3, T=256)
