@@ -196,6 +196,16 @@ def test_wide_ff_decode(F):
     _check_layer(wl, run)
 
 
+@pytest.mark.parametrize("T", [4, 8])
+def test_decode_largest_E_k_and_H(T):
+    """The largest router width, top-k and hidden size a layer takes (E = 1024, k = 32,
+    H = 4096): 128 pairs run the mma.sync kernels, 256 pairs the sliced tensor-core form."""
+    wl = synth.logits_workload(f"limits_T{T}", T, 4096, 256, 1024, 32, seed=23)
+    run = run_layer(wl)
+    assert run.err == 0
+    _check_layer(wl, run)
+
+
 def test_csr_many_pairs_with_invalid_ids():
     """The grid-wide CSR (thousands of pairs) skips and flags out-of-range ids, keeps the
     rest in ascending pair order, and writes -1 as their CSR position."""

@@ -197,6 +197,17 @@ def test_prefill_ff_widths(F):
     _down_from_oracle_h(wl, run, res, toks)
 
 
+def test_prefill_largest_ff_and_hidden():
+    """The prefill path at its largest F and H (F = H = 4096): Q(h) of 256 blocks per row
+    and the general down GEMM over 16 k-stages; every token checked."""
+    wl = synth.logits_workload("prefill_F4096", 32, 4096, 4096, 16, 4, seed=29)
+    run = run_layer(wl, path=PF)
+    assert run.err == 0
+    toks = np.arange(wl.T)
+    res, info = _stages(wl, run, toks)
+    _down_from_oracle_h(wl, run, res, toks)
+
+
 def test_prefill_per_expert_alpha():
     """Prefill with a per-expert second-level scale alpha on both banks (down's <= 2)."""
     wl = synth.prefill(seed=3, T=256)
