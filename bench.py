@@ -482,6 +482,9 @@ def measure(name, steps, warmup, batches, dev, rank, world):
 
     step_ms = [e0.elapsed_time(e1) for (_, e0, e1) in evs]
     tot_ms = max_over_ranks(sum(step_ms), dev)
+    med_ms = statistics.median(step_ms)
+    step_stats = {"median_ms": med_ms, "min_ms": min(step_ms), "max_ms": max(step_ms),
+                  "spread": (max(step_ms) - min(step_ms)) / med_ms if med_ms > 0 else 0.0}
     uniq_steps = [uniq[b] for (b, _, _) in evs]
     if prefill:
         value = weak_scaling_value(flops_per_step * steps, world, tot_ms * 1e-3) / 1e12
@@ -614,9 +617,10 @@ def measure(name, steps, warmup, batches, dev, rank, world):
                   "nvfp4 weights (e2m1 x ue4m3) * f16 activations, f32 accumulate"),
         "config": {"workload": workload_desc(wl),
                    "l2": "flushed before every step (512 MiB write, then 512 MiB read)",
+                   "l2_bytes": int(torch.cuda.get_device_properties(dev).L2_cache_size),
                    "batches_rotated": nb, "unique_experts_mean": float(np.mean(uniq_steps)),
                    "path": "prefill" if prefill else "decode"},
-        "roofline": roof, "e2e": e2e,
+        "roofline": roof, "e2e": e2e, "step_stats": step_stats,
         "gpu_launches": launches_per_step * steps,
         "breakdown_ms": {"route+csr": float(np.mean(pre_ms)), "gate_up": float(np.mean(gu_ms)),
                          "down+combine": float(np.mean(dn_ms)),
@@ -652,7 +656,8 @@ def run_ours(args):
         for name in SUBRESULT_WORKLOADS:
             if name == args.workload:
                 continue
-            sub_steps = max(3, min(args.steps, 10 if is_prefill(name) else 20))
+            # at least 20 timed steps for prefill and 50 for decode, after the warm-up
+            sub_steps = 20 if is_prefill(name) else 50
             sampler = ClockSampler(local)
             sampler.start()
             r = measure(name, sub_steps, max(3, args.warmup), args.batches, dev, rank, world)
@@ -692,7 +697,7 @@ def run_ours(args):
 
     def keys(r):
         d = {k: r[k] for k in ("value", "unit", "ms_per_step", "dtype", "config", "roofline",
-                               "e2e", "breakdown_ms", "layer_roof") if k in r}
+                               "e2e", "breakdown_ms", "layer_roof", "step_stats") if k in r}
         d["metric"] = metric_name(r["workload"])
         d["steps"] = r["steps"]
         if "clocks" in r:
@@ -708,7 +713,7 @@ def run_ours(args):
         "layer_roof": main.get("layer_roof"),
         "cpu_baseline": cpu, "cpu_baseline_all_cores": cpu_all,
         "e2e": main["e2e"], "gpu_launches": main["gpu_launches"], "clocks": clocks,
-        "breakdown_ms": main["breakdown_ms"],
+        "breakdown_ms": main["breakdown_ms"], "step_stats": main["step_stats"],
         "timing": "one CUDA graph per step (the whole layer), CUDA events around each replay",
         "wall_s": main["wall_s"],
         "subresults": [keys(r) for r in subs],

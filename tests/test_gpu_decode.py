@@ -206,6 +206,29 @@ def test_decode_largest_E_k_and_H(T):
     _check_layer(wl, run)
 
 
+@pytest.mark.parametrize("name,path", [("decode_T8", moe.PATH_DECODE), ("verify_T32", moe.PATH_DECODE),
+                                       ("prefill_T64", moe.PATH_PREFILL)])
+def test_expert_relabel_bit_identical(name, path):
+    """Relabelling the experts (bank e' = bank pi^-1(e'), ids -> pi(ids)) reorders the CSR
+    and the work but not any pair's arithmetic: y is bit-identical, on the mma.sync and
+    sliced decode forms and on the prefill path."""
+    wl = synth.by_name(name, seed=3)
+    ids = wl.ids if wl.ids is not None else oracle.route_topk(wl.logits, wl.k)[0]
+    w = wl.weights if wl.weights is not None else oracle.route_topk(wl.logits, wl.k)[1].astype(np.float32)
+    base = synth.Workload(name, wl.T, wl.H, wl.F, wl.E, wl.k, wl.x_bits, wl.gate_up, wl.down,
+                          ids=np.ascontiguousarray(ids, np.int32), weights=np.ascontiguousarray(w, np.float32))
+    y0 = run_layer(base, path=path, fetch=False).y
+    pi = np.random.default_rng(31).permutation(wl.E)
+    inv = np.argsort(pi)
+
+    def relabel(bank):
+        return type(bank)(bank.codes[inv], bank.scales[inv], None if bank.alpha is None else bank.alpha[inv])
+    moved = synth.Workload(name, wl.T, wl.H, wl.F, wl.E, wl.k, wl.x_bits, relabel(wl.gate_up),
+                           relabel(wl.down), ids=pi[base.ids].astype(np.int32), weights=base.weights)
+    y1 = run_layer(moved, path=path, fetch=False).y
+    assert np.array_equal(y0, y1)
+
+
 def test_csr_many_pairs_with_invalid_ids():
     """The grid-wide CSR (thousands of pairs) skips and flags out-of-range ids, keeps the
     rest in ascending pair order, and writes -1 as their CSR position."""
