@@ -229,6 +229,37 @@ def test_expert_relabel_bit_identical(name, path):
     assert np.array_equal(y0, y1)
 
 
+@pytest.mark.parametrize("name,path", [("decode_T8", moe.PATH_DECODE), ("verify_T32", moe.PATH_DECODE),
+                                       ("prefill_T64", moe.PATH_PREFILL)])
+def test_pinned_host_buffers_passed_to_the_calls(name, path):
+    """The calls take pinned host memory for x, the router logits (or ids and weights) and
+    y: the kernels read and write it over the host link, and y equals the device-buffer
+    run bit for bit."""
+    wl = synth.by_name(name, seed=7)
+    gu, dn = device_banks(wl)
+    layer = moe.MoeLayer(gu, dn, wl.k)
+    b = layer.buffers(wl.T, path)
+    x_d = torch.from_numpy(wl.x_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    x_h = x_d.cpu().pin_memory()
+    y_h = torch.empty(wl.T, wl.H, dtype=torch.float32).pin_memory()
+    if wl.logits is not None:
+        l_d = torch.from_numpy(wl.logits).cuda()
+        y_dev = layer.forward(x_d, logits=l_d, path=path).clone()
+        moe.moe_route_topk(l_d.cpu().pin_memory(), wl.k, b["ids"], b["w"])
+        ids_t, w_t = b["ids"], b["w"]
+    else:
+        i_d = torch.from_numpy(np.ascontiguousarray(wl.ids, np.int32)).cuda()
+        w_d = torch.from_numpy(np.ascontiguousarray(wl.weights, np.float32)).cuda()
+        y_dev = layer.forward(x_d, ids=i_d, w=w_d, path=path).clone()
+        ids_t, w_t = i_d.cpu().pin_memory(), w_d.cpu().pin_memory()
+    moe.moe_build_expert_csr(ids_t, wl.E, b["csr"], b["ws"])
+    moe.moe_grouped_gate_up_silu_nvfp4(x_h, wl.k, wl.F, gu, b["csr"], b["ws"], path)
+    moe.moe_grouped_down_combine_nvfp4(dn, b["csr"], w_t, wl.T, wl.H, wl.F, wl.k, y_h, b["ws"], path)
+    torch.cuda.synchronize()
+    assert torch.equal(y_h, y_dev.cpu())
+    assert moe.get_device_error(b["ws"]) == 0
+
+
 def test_csr_many_pairs_with_invalid_ids():
     """The grid-wide CSR (thousands of pairs) skips and flags out-of-range ids, keeps the
     rest in ascending pair order, and writes -1 as their CSR position."""
