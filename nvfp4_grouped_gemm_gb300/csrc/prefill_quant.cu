@@ -31,7 +31,6 @@ __global__ void __launch_bounds__(256) quant_x_kernel(const uint16_t* __restrict
   const int lane = b & 31, warp = b >> 5;
   const int nblk = H / 16;
   const bool has = b < nblk;
-  if (b < k) s_pos[b] = pair_pos[(size_t)t * k + b];
   uint32_t w[8];
   {
     const uint4* p = reinterpret_cast<const uint4*>(x + (size_t)t * H + b * 16);
@@ -55,7 +54,6 @@ __global__ void __launch_bounds__(256) quant_x_kernel(const uint16_t* __restrict
   const int s = row_exp_of(amax);
   const bool fast = s >= -127 && s <= 149;
   const float m = fast ? pow2f(-s) : 0.0f;
-  if (!has) return;
   float key[16];
   uint32_t neg = 0;
 #pragma unroll
@@ -72,6 +70,13 @@ __global__ void __launch_bounds__(256) quant_x_kernel(const uint16_t* __restrict
   for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, key[i]);
   const int sbc = ue4m3_code_of(bmax);
   const uint64_t codes = quant_block(key, neg, sbc);
+  // the codes depend on x alone and are formed while the CSR kernel runs; where they go
+  // (the token's CSR rows) waits for it
+  pdl_wait();
+  pdl_trigger();
+  if (b < k) s_pos[b] = pair_pos[(size_t)t * k + b];
+  __syncthreads();
+  if (!has) return;
   for (int j = 0; j < k; ++j) {
     const int pj = s_pos[j];
     if (pj < 0) continue;                          // invalid expert id: the pair has no row
@@ -374,8 +379,8 @@ cudaError_t launch_quant_x(const uint16_t* x_bf16, int T, int H, int k, const in
                            uint8_t* qc, uint8_t* qs, int32_t* qe, cudaStream_t s) {
   const int threads = (H / 16 + 31) / 32 * 32;     // one thread per 16-value block
   if (threads > 256) return cudaErrorInvalidValue;
-  quant_x_kernel<<<T, threads, 0, s>>>(x_bf16, T, H, k, pair_pos, qc, qs, qe);
-  return cudaGetLastError();
+  return launch_pdl(quant_x_kernel, dim3(T), dim3(threads), 0, s, x_bf16, T, H, k, pair_pos, qc,
+                    qs, qe);
 }
 
 cudaError_t launch_slice_x(const uint16_t* x_bf16, int T, int H, int k, const int32_t* pair_pos,
