@@ -326,11 +326,13 @@ def test_many_pairs_on_one_expert():
 
 @pytest.mark.parametrize("T,H,F,E,k", [(64, 256, 64, 16, 8),      # one k-step for down
                                        (80, 256, 128, 7, 7),      # 80 pairs per expert: 10 tiles
+                                       (40, 512, 384, 24, 8),     # K/2 = 192: 1.5 sub-tiles
                                        (52, 512, 1408, 32, 10)])  # widest decode F
 def test_sliced_path_shapes(T, H, F, E, k):
     """From 256 pairs the decode path runs the sliced tensor-core GEMMs: ragged tiles, an
-    expert spread over many 8-pair tiles, a down projection of one 64-wide k-step, and the
-    widest F (its weight-scale rows staged whole)."""
+    expert spread over many 8-pair tiles, a down projection of one 64-wide k-step, a down
+    row ending halfway into its second 128-byte sub-tile (F = 384; the zero-filled half's
+    k-steps are skipped), and the widest F (its weight-scale rows staged whole)."""
     assert T * k >= moe.decode_tensor_core_min_pairs()
     wl = synth.logits_workload(f"sliced_{T}_{H}_{F}", T, H, F, E, k, seed=21)
     run = run_layer(wl)
