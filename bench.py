@@ -518,6 +518,40 @@ def measure(name, steps, warmup, batches, dev, rank, world):
     peaks, _src = load_peaks()
     pk, pk_src = peak_hbm(peaks)
     extra = {}
+    if not prefill and moe.decode_layer_supported(wl.T, wl.H, wl.F, wl.E, wl.k):
+        # the same layer and batches through the one-kernel call (moe_decode_layer_nvfp4),
+        # timed the same way; the line's value is the four-call layer's
+        def one_kernel(b):
+            if lgs:
+                layer.forward_fused(xs[b], logits=lgs[b], stream=stream)
+            else:
+                layer.forward_fused(xs[b], ids=idss[b], w=wss[b], stream=stream)
+        with torch.cuda.stream(stream):
+            for b in range(nb):
+                one_kernel(b)
+            stream.synchronize()
+        one_g = [capture(lambda b=b: one_kernel(b)) for b in range(nb)]
+        one_ev = []
+        for i in range(warmup + steps):
+            b = i % nb
+            with torch.cuda.stream(stream):
+                flush()
+                c0 = torch.cuda.Event(enable_timing=True)
+                c1 = torch.cuda.Event(enable_timing=True)
+                c0.record(stream)
+                one_g[b].replay()
+                c1.record(stream)
+            if i >= warmup:
+                one_ev.append((b, c0, c1))
+        torch.cuda.synchronize(dev)
+        o_ms = [c0.elapsed_time(c1) for (_, c0, c1) in one_ev]
+        extra["one_kernel_layer"] = {
+            "value": sum(uniq[b] * per_expert for (b, _, _) in one_ev) / (sum(o_ms) * 1e-3) / 1e9,
+            "unit": "GB/s", "ms_per_step": sum(o_ms) / len(o_ms),
+            "median_ms": statistics.median(o_ms), "gpu_launches_per_step": 1,
+            "note": "moe_decode_layer_nvfp4 (routing, CSR, gate/up, down and combine in one "
+                    "cooperative kernel) on the same batches, L2 flushed before each step"}
+        del one_g
     if prefill:
         # the gate/up GEMM streams every expert's gate/up bytes, reads Q(x) and writes h
         alg = (wl.E * 2 * wl.F * (wl.H // 2 + wl.H // 16) + wl.P * (wl.H // 2 + wl.H // 16)
@@ -746,7 +780,8 @@ def run_ours(args):
 
     def keys(r):
         d = {k: r[k] for k in ("value", "unit", "ms_per_step", "dtype", "config", "roofline",
-                               "e2e", "breakdown_ms", "layer_roof", "step_stats") if k in r}
+                               "e2e", "breakdown_ms", "layer_roof", "step_stats",
+                               "one_kernel_layer") if k in r}
         d["metric"] = metric_name(r["workload"])
         d["steps"] = r["steps"]
         if "clocks" in r:
@@ -763,6 +798,7 @@ def run_ours(args):
         "cpu_baseline": cpu, "cpu_baseline_all_cores": cpu_all,
         "e2e": main["e2e"], "gpu_launches": main["gpu_launches"], "clocks": clocks,
         "breakdown_ms": main["breakdown_ms"], "step_stats": main["step_stats"],
+        "one_kernel_layer": main.get("one_kernel_layer"),
         "timing": "one CUDA graph per step (the whole layer), CUDA events around each replay",
         "wall_s": main["wall_s"],
         "subresults": [keys(r) for r in subs],

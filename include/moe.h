@@ -9,6 +9,9 @@
  *   moe_grouped_gate_up_silu_nvfp4  per expert: h = silu(W_gate a) * (W_up a)
  *   moe_grouped_down_combine_nvfp4  per expert: z = W_down h, then y[t] = sum_j w[t,j] z[t*k+j]
  *
+ * or, for decode batches within moe_decode_layer_supported, the same four steps in one
+ * call and one kernel (moe_decode_layer_nvfp4).
+ *
  * Sources of the definitions (the pages the method is taken from):
  *   - "moe_sk_repro.rs" (fn main): pairs p = t*k + j grouped by expert in ascending p
  *     (buckets / ex_ids / ex_off / ex_pairs), token of a pair = p / k, three grouped
@@ -132,6 +135,8 @@ typedef struct moe_ws_layout {
                           count, pad to 16 B, then int4 {row0, rows, expert, 0} per tile */
   size_t slice_tiles;  /* the same for the sliced decode GEMMs: 32-row tiles over the 4 slice
                           rows of every pair (row0 and rows count slice rows) */
+  size_t sync;         /* decode below moe_decode_tensor_core_min_pairs() pairs: u64 [6] sync
+                          words of moe_decode_layer_nvfp4 (call counter, barrier counters) */
 } moe_ws_layout;
 
 /* Limits (MOE_ERR_UNSUPPORTED beyond them): 1 <= k <= min(E, 32); E <= 1024;
@@ -205,6 +210,37 @@ moe_status moe_grouped_down_combine_nvfp4(const moe_nvfp4_bank* w_down, moe_csr 
                                           const float* topk_w, int32_t T, int32_t H, int32_t F,
                                           int32_t k, int32_t path, float* y, void* ws,
                                           size_t ws_bytes, void* stream);
+
+/* The whole decode layer in one call and one kernel: routing (or given picks), the CSR,
+ * gate/up + SiLU, down and the combine of the four calls above. topk_ids and topk_w are
+ * bit-identical to moe_route_topk's; every other step runs the arithmetic of the DECODE
+ * path's TMA-fed kernels, so y is bit-identical to the four calls wherever those run them
+ * (from 8 units per SM: min(T*k, E) * F/8 gate/up and min(T*k, E) * H/16 down units),
+ * and agrees with them to rounding below that. One cooperative grid of one CTA per SM: every CTA routes the T tokens and
+ * builds the CSR itself, the weight stream runs from the gate/up rows straight into the
+ * down rows, and the steps are ordered by four grid-wide barriers, each wait bounded
+ * (MOE_DEVERR_TIMEOUT on expiry). Sizes: moe_decode_layer_supported (T <= 32 tokens,
+ * T*k below moe_decode_tensor_core_min_pairs(), H % 256 == 0, F % 128 == 0
+ * and F <= 640, plus the limits above), else MOE_ERR_UNSUPPORTED.
+ *   logits   f32 [T][E] (finite): routed as moe_route_topk does, the picks and weights
+ *            written to topk_ids / topk_w; or NULL: topk_ids i32 [T][k] and topk_w f32
+ *            [T][k] are inputs (ids outside [0, E) set MOE_DEVERR_EXPERT_ID and are left
+ *            out, as in moe_build_expert_csr).
+ *   x_bf16   bf16 [T][H], 16-byte aligned; w_gate_up rows = 2F, in_f = H; w_down rows = H,
+ *            in_f = F (same E); y f32 [T][H], 16-byte aligned, overwritten.
+ *   ws       moe_workspace_bytes(T, H, F, E, k, MOE_PATH_DECODE) bytes, zero-filled once
+ *            after allocation like every workspace: its sync words hold a call counter and
+ *            barrier counters that only grow, so no call resets them. A call whose wait
+ *            gave up (MOE_DEVERR_TIMEOUT) marks them, and later calls on that workspace then
+ *            only report MOE_DEVERR_TIMEOUT until it is zero-filled again. The call writes
+ *            the regions the DECODE path uses (not a csr). */
+moe_status moe_decode_layer_nvfp4(const float* logits, int32_t* topk_ids, float* topk_w,
+                                  const void* x_bf16, int32_t T, int32_t H, int32_t F, int32_t k,
+                                  const moe_nvfp4_bank* w_gate_up, const moe_nvfp4_bank* w_down,
+                                  float* y, void* ws, size_t ws_bytes, void* stream);
+
+/* 1 if moe_decode_layer_nvfp4 takes these sizes, else 0. */
+int32_t moe_decode_layer_supported(int32_t T, int32_t H, int32_t F, int32_t E, int32_t k);
 
 /* moe_build_expert_csr without a workspace, for callers that cannot allocate device
  * memory: a host engine or plugin that owns every device allocation and hands kernels only

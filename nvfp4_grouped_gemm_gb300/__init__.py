@@ -181,6 +181,25 @@ def moe_grouped_down_combine_nvfp4(w_down: NvFp4Bank, csr: ExpertCSR, topk_w: to
         ws.numel() * ws.element_size(), _stream(stream)), "moe_grouped_down_combine_nvfp4")
 
 
+def decode_layer_supported(T: int, H: int, F: int, E: int, k: int) -> bool:
+    """Whether moe_decode_layer_nvfp4 (the one-kernel decode layer) takes these sizes."""
+    return bool(_native.load().moe_decode_layer_supported(T, H, F, E, k))
+
+
+def moe_decode_layer_nvfp4(x_bf16: torch.Tensor, k: int, w_gate_up: NvFp4Bank,
+                           w_down: NvFp4Bank, y: torch.Tensor, ws: torch.Tensor,
+                           topk_ids: torch.Tensor, topk_w: torch.Tensor,
+                           logits: Optional[torch.Tensor] = None, stream=None) -> None:
+    """The whole decode layer in one kernel.  With ``logits`` the picks and weights are
+    written to ``topk_ids`` / ``topk_w``; without, they are read from them."""
+    T, H = x_bf16.shape
+    _check(_native.load().moe_decode_layer_nvfp4(
+        _ptr(logits) if logits is not None else None, _ptr(topk_ids), _ptr(topk_w),
+        _ptr(x_bf16), T, H, w_down.in_f, k, ctypes.byref(w_gate_up._c), ctypes.byref(w_down._c),
+        _ptr(y), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+        "moe_decode_layer_nvfp4")
+
+
 def get_device_error(ws: torch.Tensor, stream=None) -> int:
     code = ctypes.c_int32(0)
     st = _native.load().moe_get_device_error(_ptr(ws), _stream(stream), ctypes.byref(code))
@@ -235,4 +254,20 @@ class MoeLayer:
                                        path, stream)
         moe_grouped_down_combine_nvfp4(self.down, b["csr"], w, T, self.H, self.F, self.k, b["y"],
                                        b["ws"], path, stream)
+        return b["y"]
+
+    def forward_fused(self, x_bf16: torch.Tensor, logits: Optional[torch.Tensor] = None,
+                      ids: Optional[torch.Tensor] = None, w: Optional[torch.Tensor] = None,
+                      stream=None) -> torch.Tensor:
+        """The same layer through moe_decode_layer_nvfp4 (one kernel; decode sizes within
+        decode_layer_supported).  Uses the DECODE buffers; with logits the picks and
+        weights land in buffers()["ids"] / ["w"]."""
+        T = x_bf16.shape[0]
+        b = self.buffers(T, PATH_DECODE)
+        if logits is None and (ids is None or w is None):
+            raise ValueError("pass logits, or ids and w")
+        if logits is not None:
+            ids, w = b["ids"], b["w"]
+        moe_decode_layer_nvfp4(x_bf16, self.k, self.gate_up, self.down, b["y"], b["ws"], ids, w,
+                               logits=logits, stream=stream)
         return b["y"]

@@ -30,7 +30,7 @@ class CSR(ctypes.Structure):
 class WsLayout(ctypes.Structure):
     _fields_ = [(n, c_size) for n in (
         "total", "error_word", "pair_pos", "h", "xg", "xe", "hg", "he", "qx_codes", "qx_scales", "qx_exp",
-        "qh_codes", "qh_scales", "qh_exp", "partial", "tiles", "slice_tiles")]
+        "qh_codes", "qh_scales", "qh_exp", "partial", "tiles", "slice_tiles", "sync")]
 
 
 # (name, restype, argtypes) of every exported entry point declared in include/moe.h
@@ -50,6 +50,10 @@ SIGNATURES = [
      [ctypes.POINTER(Bank), CSR, c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_size,
       c_vp]),
     ("moe_build_expert_csr_static", c_i32, [c_vp, c_i32, c_i32, c_i32, CSR, c_vp]),
+    ("moe_decode_layer_nvfp4", c_i32,
+     [c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32, ctypes.POINTER(Bank),
+      ctypes.POINTER(Bank), c_vp, c_vp, c_size, c_vp]),
+    ("moe_decode_layer_supported", c_i32, [c_i32] * 5),
     ("moe_status_string", ctypes.c_char_p, [c_i32]),
     ("moe_get_device_error", c_i32, [c_vp, c_vp, ctypes.POINTER(c_i32)]),
 ]

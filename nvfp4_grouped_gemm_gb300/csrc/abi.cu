@@ -118,6 +118,7 @@ bool compute_layout(int T, int H, int F, int E, int k, int path, moe_ws_layout* 
     L->xe = take(P * sizeof(int32_t));
     L->hg = take(P * F * 2);
     L->he = take(P * sizeof(int32_t));
+    L->sync = take(decode_layer_sync_bytes());
   } else {
     // operand rows per pair: the sliced decode form keeps kDecodeSlices slices of each row
     const bool sl = path == MOE_PATH_DECODE;
@@ -282,6 +283,34 @@ moe_status moe_grouped_down_combine_nvfp4(const moe_nvfp4_bank* w_down, moe_csr 
                                        : launch_decode_down(*w_down, csr, T, H, F, k, L, w, s);
   if (ce != cudaSuccess) return MOE_ERR_CUDA;
   return from_cuda(launch_combine(topk_w, T, H, k, L, w, y, s));
+}
+
+int32_t moe_decode_layer_supported(int32_t T, int32_t H, int32_t F, int32_t E, int32_t k) {
+  if (sizes_supported(T, H, F, E, k) != MOE_OK) return 0;
+  if (path_supported(T, F, k, MOE_PATH_DECODE) != MOE_OK) return 0;
+  return decode_layer_supported(T, H, F, E, k) ? 1 : 0;
+}
+
+moe_status moe_decode_layer_nvfp4(const float* logits, int32_t* topk_ids, float* topk_w,
+                                  const void* x_bf16, int32_t T, int32_t H, int32_t F, int32_t k,
+                                  const moe_nvfp4_bank* w_gate_up, const moe_nvfp4_bank* w_down,
+                                  float* y, void* ws, size_t ws_bytes, void* stream) {
+  if (!topk_ids || !topk_w || !y || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+  if (!x_bf16 || !aligned16(x_bf16)) return MOE_ERR_INVALID_ARG;
+  if (!w_gate_up || !w_down) return MOE_ERR_INVALID_ARG;
+  const int E = w_gate_up->E;
+  moe_status st = sizes_supported(T, H, F, E, k);
+  if (st != MOE_OK) return st;
+  if ((st = check_bank(w_gate_up, E, 2 * F, H)) != MOE_OK) return st;
+  if ((st = check_bank(w_down, E, H, F)) != MOE_OK) return st;
+  if (!moe_decode_layer_supported(T, H, F, E, k)) return MOE_ERR_UNSUPPORTED;
+  moe_ws_layout L;
+  if (!compute_layout(T, H, F, E, k, MOE_PATH_DECODE, &L)) return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(ws, ws_bytes, L)) != MOE_OK) return st;
+  return from_cuda(launch_decode_layer(logits, topk_ids, topk_w,
+                                       static_cast<const uint16_t*>(x_bf16), T, H, F, k,
+                                       *w_gate_up, *w_down, L, static_cast<char*>(ws), y,
+                                       static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_get_device_error(const void* ws, void* stream, int32_t* code) {

@@ -32,8 +32,7 @@
 // Kernels after the CSR are launched with programmatic dependent launch: each issues
 // the loads that depend only on the CSR (two or more kernels back, complete before its
 // predecessor passed its own griddepcontrol.wait) and then waits for its predecessor.
-#include "moe_internal.cuh"
-#include "tma_sync.cuh"
+#include "decode_units.cuh"
 
 namespace moe {
 
@@ -85,49 +84,16 @@ __global__ void __launch_bounds__(256) x_gather_kernel(const uint16_t* __restric
   const int p = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   const bool has = p < P;
-  const uint16_t* row = x + (size_t)(has ? p / k : 0) * H;
   // the whole row in registers (H <= 256 * NP: NP pieces of 8 values per lane)
   uint4 v[NP];
-  float amax = 0.0f;
-#pragma unroll
-  for (int i = 0; i < NP; ++i) {
-    const int c = (lane + 32 * i) * 8;
-    v[i] = has && c < H ? *reinterpret_cast<const uint4*>(row + c) : make_uint4(0, 0, 0, 0);
-    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      amax = fmaxf(amax, fabsf(__uint_as_float(w[q] << 16)));
-      amax = fmaxf(amax, fabsf(__uint_as_float(w[q] & 0xffff0000u)));
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  const int e = f16_prescale_exp(amax);
-  // times 2^-e as two power-of-two factors (each a normal float for every e of a bf16 row)
-  const float s1 = pow2f(-e / 2), s2 = pow2f(-e - (-e / 2));
-#pragma unroll
-  for (int i = 0; i < NP; ++i) {
-    uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const __half2 hv = __floats2half2_rn((__uint_as_float(w[q] << 16) * s1) * s2,
-                                           (__uint_as_float(w[q] & 0xffff0000u) * s1) * s2);
-      w[q] = *reinterpret_cast<const uint32_t*>(&hv);
-    }
-    v[i] = make_uint4(w[0], w[1], w[2], w[3]);
-  }
+  const int e = x_row_f16<NP>(x + (size_t)(has ? p / k : 0) * H, has, H, lane, v);
   pdl_wait();                                  // pair_pos is complete
   pdl_trigger();
   if (!has) return;
   const int pos = pair_pos[p];
   if (pos < 0) return;                         // invalid expert id: the pair has no row
   if (lane == 0) xe[pos] = e;
-#pragma unroll
-  for (int i = 0; i < NP; ++i) {
-    const int c = (lane + 32 * i) * 8;
-    if (c >= H) break;
-    *reinterpret_cast<uint4*>(xg + (size_t)pos * H + c) = v[i];
-  }
+  x_row_store<NP>(v, H, lane, xg + (size_t)pos * H);
 }
 
 // Same for h (f32 rows already in CSR order), F <= 128*NR: the row stays in registers, so
@@ -140,30 +106,8 @@ __global__ void __launch_bounds__(256) h_prep_kernel(const float* __restrict__ h
   pdl_wait();
   pdl_trigger();
   const int pos = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
   if (pos >= offsets[E]) return;
-  const float* row = h + (size_t)pos * F;
-  float4 v[NR];
-  float amax = 0.0f;
-#pragma unroll
-  for (int i = 0; i < NR; ++i) {
-    const int c = 4 * lane + 128 * i;
-    v[i] = c < F ? *reinterpret_cast<const float4*>(row + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  const int e = f16_prescale_exp(amax);
-  if (lane == 0) he[pos] = e;
-#pragma unroll
-  for (int i = 0; i < NR; ++i) {
-    const int c = 4 * lane + 128 * i;
-    if (c >= F) break;
-    const __half2 h0 = __floats2half2_rn(ldexpf(v[i].x, -e), ldexpf(v[i].y, -e));
-    const __half2 h1 = __floats2half2_rn(ldexpf(v[i].z, -e), ldexpf(v[i].w, -e));
-    *reinterpret_cast<uint2*>(hg + (size_t)pos * F + c) =
-        make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
-  }
+  h_row_f16<NR>(h + (size_t)pos * F, F, threadIdx.x & 31, hg + (size_t)pos * F, he + pos);
 }
 
 // ---------------------------------------------------------------------------
@@ -495,71 +439,16 @@ combine_kernel(const float* __restrict__ w, const int32_t* __restrict__ pair_pos
   pdl_wait();
   const int r = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
   if (r >= H) return;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  // the partial rows are loaded eight pairs at a time and summed in ascending j
-  for (int j0 = 0; j0 < k; j0 += 8) {
-    float4 z[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int j = j0 + q;
-      const int pos = j < k ? s_pos[j] : -1;
-      z[q] = pos >= 0 ? __ldcs(reinterpret_cast<const float4*>(partial + (size_t)pos * H + r))
-                      : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int j = j0 + q;
-      if (j >= k || s_pos[j] < 0) continue;
-      const float wj = s_w[j];
-      acc.x = fmaf(wj, z[q].x, acc.x);
-      acc.y = fmaf(wj, z[q].y, acc.y);
-      acc.z = fmaf(wj, z[q].z, acc.z);
-      acc.w = fmaf(wj, z[q].w, acc.w);
-    }
-  }
-  *reinterpret_cast<float4*>(y + (size_t)t * H + r) = acc;
+  *reinterpret_cast<float4*>(y + (size_t)t * H + r) = combine4(partial, s_pos, s_w, k, H, r);
 }
 
 // ---------------------------------------------------------------------------
-// gate/up + SiLU, TMA-fed warp units
+// gate/up + SiLU and down, TMA-fed warp units (decode_units.cuh)
 // ---------------------------------------------------------------------------
-// One CTA per SM: warp 0 streams tiles with TMA into a ring of shared-memory stages; each
-// of the NW other warps owns two stages and multiplies whole units alone (no CTA barrier,
-// no cross-warp sum).  A unit = (active expert, 8 gate rows + the matching 8 up rows);
-// one m16n8k16 MMA carries the gate rows in M rows 0..7 and the up rows in 8..15, so each
-// lane holds a gate and an up value of the same (row, pair) and writes h itself.  A stage
-// is one of the unit's NH K-chunks of KC = H/2/NH bytes per row, fetched by two 4-D TMA
-// boxes: codes {128 B, 8 rows, gate/up, nb = KC/128 K-boxes} (SWIZZLE_128B, so the
-// quarter-warp reads of rows g..g+7 hit distinct banks) land as [K-box][gate, up][row][128 B],
-// scales {16 B, 8 rows, gate/up, nb} as [K-box][gate, up][row][16 B].  The first unit of a
-// warp is CTA unit w, the next w + NW, ...; a unit with more than 8 pairs is streamed
-// once per group of 8 pairs.
-constexpr int kTmaWarps = 16;                 // consumer warps
-constexpr int kTmaSlots = 2;                  // stages per consumer warp
-constexpr int kTmaProd = 4;                   // producer warps, each feeding kTmaWarps/kTmaProd
-
-struct GuTmaArgs {
-  const __half* xg;
-  const int32_t* xe;
-  int H, F, nh, nb;                           // K-chunks per unit, 128-byte boxes per chunk
-  const int32_t* offsets;
-  const int32_t* active;
-  const int32_t* n_active;
-  float* h;
-  uint32_t* err;
-  const float* alpha = nullptr;   // [E] per-expert second-level weight scale, or none
-};
-
-__host__ __device__ constexpr int gu_stage_bytes(int nb) {
-  return ((2 * nb * 1024 + 2 * 8 * nb * 16) + 1023) / 1024 * 1024;
-}
-// byte offsets inside a stage
-__device__ __forceinline__ uint32_t gu_code_off(int kbox, int mat, int row, int chunk16) {
-  return kbox * 2048 + mat * 1024 + row * 128 + ((chunk16 ^ row) << 4);
-}
-__device__ __forceinline__ uint32_t gu_scale_off(int nb, int kbox, int mat, int row) {
-  return 2 * nb * 1024 + kbox * 256 + mat * 128 + row * 16;
-}
+// One CTA per SM: kTmaProd producer warps stream the units' stages with TMA into the rings
+// of the kTmaWarps consumer warps (kTmaSlots stages each), and each consumer multiplies
+// whole units alone (no CTA barrier, no cross-warp sum).  The CTA takes a contiguous range
+// of the units (expert-major); its consumer w takes units w, w + kTmaWarps, ...
 
 // ALPHA: the bank has per-expert second-level scales (a separate instance, so the common
 // case keeps every register for the K loop).
@@ -570,18 +459,13 @@ gate_up_tma_kernel(const __grid_constant__ CUtensorMap tmap_c, const __grid_cons
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  constexpr int nb = NB;                                   // 128-byte K-boxes per stage
-  const int nh = args.nh;
-  const int stage_bytes = gu_stage_bytes(nb);
+  const int stage_bytes = gu_stage_bytes(NB);
   constexpr int NSLOT = kTmaWarps * kTmaSlots;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + NSLOT * stage_bytes);
   uint64_t* empty = full + NSLOT;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + NSLOT);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int H = args.H, F = args.F;
-  const int nrb = F / 8;                                   // units per expert
-  const int sc_bytes = nb * 16;                            // scale bytes per row and stage
-  (void)sc_bytes;
+  const int nrb = args.F / 8;                              // units per expert
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NSLOT; ++i) {
@@ -603,177 +487,53 @@ gate_up_tma_kernel(const __grid_constant__ CUtensorMap tmap_c, const __grid_cons
     // ---------------- TMA producers: warp p feeds consumers p*PER .. p*PER+PER-1 ----------------
     pdl_trigger();
     if (lane == 0) {
-      const uint32_t tx = (uint32_t)(2 * nb * 1024 + 2 * 8 * sc_bytes);
       const int w0 = warp * PER;
-      int cu[PER], cp[PER], ch[PER], cq[PER];              // unit, pass, chunk, stages
-      for (int i = 0; i < PER; ++i) { cu[i] = u_beg + w0 + i; cp[i] = 0; ch[i] = 0; cq[i] = 0; }
+      GuCursor cur[PER];
+      for (int i = 0; i < PER; ++i) cur[i] = GuCursor{u_beg + w0 + i, 0, 0, 0};
       bool more = true, ok = true;
       while (more && ok) {
         more = false;
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
           if (!ok) break;
-          const int w = w0 + i;
-          if (cu[i] >= u_end) continue;
+          if (cur[i].u >= u_end) continue;
           more = true;
-          const int slot = w * kTmaSlots + (cq[i] & 1);
-          if (!mbar_wait(&empty[slot], ((cq[i] >> 1) & 1) ^ 1, abort_flag, args.err)) { ok = false; break; }
-          const int u = cu[i];
-          const int e = args.active[u / nrb];
-          unsigned char* sb = smem + slot * stage_bytes;
-          mbar_expect_tx(&full[slot], tx);
-          // coordinates {byte in K-box, row of the matrix, 2e (gate) .. 2e+1 (up), K-box}
-          tma_load_4d(sb, &tmap_c, 0, (u % nrb) * 8, 2 * e, ch[i] * nb, &full[slot]);
-          tma_load_4d(sb + 2 * nb * 1024, &tmap_s, 0, (u % nrb) * 8, 2 * e, ch[i] * nb, &full[slot]);
-          ++cq[i];
-          if (++ch[i] == nh) {
-            ch[i] = 0;
-            const int m = args.offsets[e + 1] - args.offsets[e];
-            if (++cp[i] * 8 >= m) { cp[i] = 0; cu[i] += kTmaWarps; }
-          }
+          ok = gu_issue(args, &tmap_c, &tmap_s, cur[i], kTmaWarps, smem, stage_bytes, full, empty,
+                        Ring{(w0 + i) * kTmaSlots, 1}, abort_flag);
         }
       }
-      if (!ok) {
-        // drain, bounded: every issued stage has landed before the CTA exits
-        for (int i = 0; i < PER; ++i)
-          for (int par = 0; par < 2; ++par) {
-            if (cq[i] <= par) continue;
-            const int last = par + ((cq[i] - 1 - par) / 2) * 2;     // last stage issued on the slot
-            const uint64_t t0 = global_ns();
-            while (!mbar_try(&full[(w0 + i) * kTmaSlots + par], (uint32_t)((last >> 1) & 1)) &&
-                   global_ns() - t0 < 100000000ull) {
-            }
-          }
-      }
+      // drain, bounded: every issued stage has landed before the CTA exits
+      if (!ok)
+        for (int i = 0; i < PER; ++i) ring_drain(full, Ring{(w0 + i) * kTmaSlots, 1}, cur[i].q);
     }
   } else {
     // ---------------- consumer warp ----------------
     pdl_wait();                                            // gathered activations are ready
     pdl_trigger();
     const int cw = warp - kTmaProd;
-    const int g = lane >> 2, c = lane & 3;
+    const Ring ring{cw * kTmaSlots, 1};
     int q = 0;                                             // stages consumed
-    for (int u = u_beg + cw; u < u_end && !*abort_flag; u += kTmaWarps) {
-      const int e = args.active[u / nrb];
-      const int i0 = (u % nrb) * 8;
-      const int off = args.offsets[e];
-      const int m = args.offsets[e + 1] - off;
-      bool ok = true;
-      for (int tok0 = 0; tok0 < m && ok; tok0 += 8) {
-        const int live = min(8, m - tok0);
-        const __half* xrow = args.xg + (size_t)(off + tok0 + (g < live ? g : 0)) * H + 32 * c;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        uint4 xb[4];
-#pragma unroll
-        for (int qq = 0; qq < 4; ++qq)
-          xb[qq] = g < live ? __ldg(reinterpret_cast<const uint4*>(xrow + 8 * qq)) : make_uint4(0, 0, 0, 0);
-        for (int hc = 0; hc < nh; ++hc, ++q) {
-          const int slot = cw * kTmaSlots + (q & 1);
-          if (!mbar_wait_warp(&full[slot], (q >> 1) & 1, abort_flag, args.err)) { ok = false; break; }
-          const uint32_t sb = smem_u32(smem + slot * stage_bytes);
-#pragma unroll
-          for (int kl = 0; kl < 2 * nb; ++kl) {             // 128-element k-blocks of the chunk
-            const int kbg = hc * 2 * nb + kl;               // k-block within the row
-            uint4 xn[4];
-            const bool nxt = g < live && kbg + 1 < H / 128;
-#pragma unroll
-            for (int qq = 0; qq < 4; ++qq)
-              xn[qq] = nxt ? __ldg(reinterpret_cast<const uint4*>(xrow + (kbg + 1) * 128 + 8 * qq))
-                           : make_uint4(0, 0, 0, 0);
-            const int chunk = ((kl & 1) << 2) + c;           // 16-byte chunk within the K-box row
-            const int kbox = kl >> 1;
-            uint4 WGv, WUv;
-            asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(WGv.x), "=r"(WGv.y), "=r"(WGv.z), "=r"(WGv.w) : "r"(sb + gu_code_off(kbox, 0, g, chunk)));
-            asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(WUv.x), "=r"(WUv.y), "=r"(WUv.z), "=r"(WUv.w) : "r"(sb + gu_code_off(kbox, 1, g, chunk)));
-            // the K-box's 16 scale bytes per row: 8 for each of its two 128-element k-blocks
-            unsigned short s16g, s16u;
-            const uint32_t so = ((kl & 1) << 3) + 2 * c;
-            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(s16g) : "r"(sb + gu_scale_off(nb, kbox, 0, g) + so));
-            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(s16u) : "r"(sb + gu_scale_off(nb, kbox, 1, g) + so));
-            const uint32_t fg = e4m3x2_to_f16x2(s16g), fu = e4m3x2_to_f16x2(s16u);
-            const uint32_t s_g[2] = {bcast_lo(fg), bcast_hi(fg)};
-            const uint32_t s_u[2] = {bcast_lo(fu), bcast_hi(fu)};
-            const uint32_t WG[4] = {WGv.x, WGv.y, WGv.z, WGv.w};
-            const uint32_t WU[4] = {WUv.x, WUv.y, WUv.z, WUv.w};
-#pragma unroll
-            for (int wi = 0; wi < 4; ++wi) {
-              uint32_t gq[4], uq[4];
-              e2m1x8_to_f16x2x4(WG[wi], gq[0], gq[1], gq[2], gq[3]);
-              e2m1x8_to_f16x2x4(WU[wi], uq[0], uq[1], uq[2], uq[3]);
-              const int sbk = wi >> 1;
-#pragma unroll
-              for (int hh = 0; hh < 2; ++hh)
-                mma_f16_16816(acc, hmul2_u32(gq[2 * hh], s_g[sbk]), hmul2_u32(uq[2 * hh], s_u[sbk]),
-                              hmul2_u32(gq[2 * hh + 1], s_g[sbk]), hmul2_u32(uq[2 * hh + 1], s_u[sbk]),
-                              hh ? xb[wi].z : xb[wi].x, hh ? xb[wi].w : xb[wi].y);
-            }
-#pragma unroll
-            for (int qq = 0; qq < 4; ++qq) xb[qq] = xn[qq];
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&empty[slot]);
-        }
-        if (!ok) break;
-        // acc[0..1]: gate row i0+g, pairs 2c, 2c+1; acc[2..3]: up row i0+g, same pairs
-#pragma unroll
-        for (int qq = 0; qq < 2; ++qq) {
-          const int n = 2 * c + qq;
-          if (n < live) {
-            const int pos = off + tok0 + n;
-            const int ex = args.xe[pos];
-            const float al = ALPHA ? __ldg(args.alpha + args.active[u / nrb]) : 1.0f;
-            args.h[(size_t)pos * F + i0 + g] =
-                silu_f(al * ldexpf(acc[qq], ex)) * (al * ldexpf(acc[2 + qq], ex));
-          }
-        }
-      }
-      if (!ok) break;
-    }
+    for (int u = u_beg + cw; u < u_end && !*abort_flag; u += kTmaWarps)
+      if (!gu_consume_unit<NB, ALPHA>(args, u, smem, stage_bytes, full, empty, ring, q, abort_flag))
+        break;
   }
   __syncthreads();
 }
 
-// ---------------------------------------------------------------------------
-// down, bulk-copy-fed warp units
-// ---------------------------------------------------------------------------
-// Same organisation as gate_up_tma_kernel for the down projection: a unit = (active
-// expert, 16 output rows) over the whole F, fetched as one stage by two contiguous bulk
-// copies (the unit's rows are consecutive: 16 x F/2 code bytes, then 16 x F/16 scale
-// bytes).  With F/2 bytes per row the quarter-warp reads of rows g, g+1 at 64 kb + 16 c
-// fall in different bank halves whenever F/2 is an odd multiple of 64 bytes.
-struct DnTmaArgs {
-  const __half* hg;
-  const int32_t* he;
-  const uint8_t* codes;
-  const uint8_t* scales;
-  int H, F;
-  const int32_t* offsets;
-  const int32_t* active;
-  const int32_t* n_active;
-  float* partial;
-  uint32_t* err;
-  const float* alpha = nullptr;   // [E] per-expert second-level weight scale, or none
-};
-
-__host__ __device__ constexpr int dn_stage_bytes(int F) {
-  return ((16 * (F / 2) + 16 * (F / 16)) + 1023) / 1024 * 1024;
-}
-
+// The down projection in the same organisation: a unit = (active expert, 16 output rows)
+// over the whole F, one stage per group of 8 pairs.
 __global__ void __launch_bounds__(32 * (kTmaProd + kTmaWarps), 1)
 down_tma_kernel(const DnTmaArgs args) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int H = args.H, F = args.F;
-  const int stage_bytes = dn_stage_bytes(F);
-  const int row_bytes = F / 2, srow = F / 16;
-  const uint32_t codes_bytes = 16 * row_bytes, scale_bytes = 16 * srow;
+  const int stage_bytes = dn_stage_bytes(args.F);
   constexpr int NSLOT = kTmaWarps * kTmaSlots;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + NSLOT * stage_bytes);
   uint64_t* empty = full + NSLOT;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + NSLOT);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nrb = H / 16;                                  // units per expert
+  const int nrb = args.H / 16;                             // units per expert
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NSLOT; ++i) {
@@ -794,42 +554,22 @@ down_tma_kernel(const DnTmaArgs args) {
     // the weights do not depend on the previous kernel, so the copies start before its end
     if (lane == 0) {
       const int w0 = warp * PER;
-      int cu[PER], cp[PER], cq[PER];                       // unit, pass, stages
-      for (int i = 0; i < PER; ++i) { cu[i] = u_beg + w0 + i; cp[i] = 0; cq[i] = 0; }
+      DnCursor cur[PER];
+      for (int i = 0; i < PER; ++i) cur[i] = DnCursor{u_beg + w0 + i, 0, 0};
       bool more = true, ok = true;
       while (more && ok) {
         more = false;
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
           if (!ok) break;
-          const int w = w0 + i;
-          if (cu[i] >= u_end) continue;
+          if (cur[i].u >= u_end) continue;
           more = true;
-          const int slot = w * kTmaSlots + (cq[i] & 1);
-          if (!mbar_wait(&empty[slot], ((cq[i] >> 1) & 1) ^ 1, abort_flag, args.err)) { ok = false; break; }
-          const int u = cu[i];
-          const int e = args.active[u / nrb];
-          const size_t r0 = (size_t)e * H + (u % nrb) * 16;
-          unsigned char* sb = smem + slot * stage_bytes;
-          mbar_expect_tx(&full[slot], codes_bytes + scale_bytes);
-          bulk_load(sb, args.codes + r0 * row_bytes, codes_bytes, &full[slot]);
-          bulk_load(sb + codes_bytes, args.scales + r0 * srow, scale_bytes, &full[slot]);
-          ++cq[i];
-          const int m = args.offsets[e + 1] - args.offsets[e];
-          if (++cp[i] * 8 >= m) { cp[i] = 0; cu[i] += kTmaWarps; }
+          ok = dn_issue(args, cur[i], kTmaWarps, smem, stage_bytes, full, empty,
+                        Ring{(w0 + i) * kTmaSlots, 1}, abort_flag);
         }
       }
-      if (!ok) {
-        for (int i = 0; i < PER; ++i)
-          for (int par = 0; par < 2; ++par) {
-            if (cq[i] <= par) continue;
-            const int last = par + ((cq[i] - 1 - par) / 2) * 2;
-            const uint64_t t0 = global_ns();
-            while (!mbar_try(&full[(w0 + i) * kTmaSlots + par], (uint32_t)((last >> 1) & 1)) &&
-                   global_ns() - t0 < 100000000ull) {
-            }
-          }
-      }
+      if (!ok)
+        for (int i = 0; i < PER; ++i) ring_drain(full, Ring{(w0 + i) * kTmaSlots, 1}, cur[i].q);
     }
     pdl_wait();
     pdl_trigger();
@@ -838,75 +578,10 @@ down_tma_kernel(const DnTmaArgs args) {
     pdl_wait();                                            // h in f16 is complete
     pdl_trigger();
     const int cw = warp - kTmaProd;
-    const int g = lane >> 2, c = lane & 3;
-    const int nkb = F / 128;
+    const Ring ring{cw * kTmaSlots, 1};
     int q = 0;
-    for (int u = u_beg + cw; u < u_end && !*abort_flag; u += kTmaWarps) {
-      const int e = args.active[u / nrb];
-      const int r0 = (u % nrb) * 16;
-      const int off = args.offsets[e];
-      const int m = args.offsets[e + 1] - off;
-      bool ok = true;
-      for (int tok0 = 0; tok0 < m && ok; tok0 += 8, ++q) {
-        const int live = min(8, m - tok0);
-        const __half* hrow = args.hg + (size_t)(off + tok0 + (g < live ? g : 0)) * F + 32 * c;
-        const int slot = cw * kTmaSlots + (q & 1);
-        if (!mbar_wait_warp(&full[slot], (q >> 1) & 1, abort_flag, args.err)) { ok = false; break; }
-        const uint32_t sb = smem_u32(smem + slot * stage_bytes);
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        uint4 xb[4];
-#pragma unroll
-        for (int qq = 0; qq < 4; ++qq)
-          xb[qq] = g < live ? __ldg(reinterpret_cast<const uint4*>(hrow + 8 * qq)) : make_uint4(0, 0, 0, 0);
-        for (int kb = 0; kb < nkb; ++kb) {
-          uint4 xn[4];
-          const bool nxt = g < live && kb + 1 < nkb;
-#pragma unroll
-          for (int qq = 0; qq < 4; ++qq)
-            xn[qq] = nxt ? __ldg(reinterpret_cast<const uint4*>(hrow + (kb + 1) * 128 + 8 * qq))
-                         : make_uint4(0, 0, 0, 0);
-          uint4 A0, A1;
-          const uint32_t a0 = sb + g * row_bytes + kb * 64 + 16 * c;
-          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(A0.x), "=r"(A0.y), "=r"(A0.z), "=r"(A0.w) : "r"(a0));
-          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(A1.x), "=r"(A1.y), "=r"(A1.z), "=r"(A1.w) : "r"(a0 + 8 * row_bytes));
-          unsigned short s0, s1;
-          const uint32_t sa = sb + codes_bytes + g * srow + kb * 8 + 2 * c;
-          asm volatile("ld.shared.u16 %0, [%1];" : "=h"(s0) : "r"(sa));
-          asm volatile("ld.shared.u16 %0, [%1];" : "=h"(s1) : "r"(sa + 8 * srow));
-          const uint32_t f0 = e4m3x2_to_f16x2(s0), f1 = e4m3x2_to_f16x2(s1);
-          const uint32_t sc0[2] = {bcast_lo(f0), bcast_hi(f0)};
-          const uint32_t sc1[2] = {bcast_lo(f1), bcast_hi(f1)};
-          const uint32_t W0[4] = {A0.x, A0.y, A0.z, A0.w}, W1[4] = {A1.x, A1.y, A1.z, A1.w};
-#pragma unroll
-          for (int wi = 0; wi < 4; ++wi) {
-            uint32_t p0[4], p1[4];
-            e2m1x8_to_f16x2x4(W0[wi], p0[0], p0[1], p0[2], p0[3]);
-            e2m1x8_to_f16x2x4(W1[wi], p1[0], p1[1], p1[2], p1[3]);
-            const int sbk = wi >> 1;
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh)
-              mma_f16_16816(acc, hmul2_u32(p0[2 * hh], sc0[sbk]), hmul2_u32(p1[2 * hh], sc1[sbk]),
-                            hmul2_u32(p0[2 * hh + 1], sc0[sbk]), hmul2_u32(p1[2 * hh + 1], sc1[sbk]),
-                            hh ? xb[wi].z : xb[wi].x, hh ? xb[wi].w : xb[wi].y);
-          }
-#pragma unroll
-          for (int qq = 0; qq < 4; ++qq) xb[qq] = xn[qq];
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
-        // acc[q]: row r0 + g + 8(q>>1), pair 2c + (q&1)
-#pragma unroll
-        for (int qq = 0; qq < 4; ++qq) {
-          const int n = 2 * c + (qq & 1);
-          if (n < live) {
-            const int pos = off + tok0 + n;
-            args.partial[(size_t)pos * H + r0 + g + 8 * (qq >> 1)] =
-                (args.alpha ? __ldg(args.alpha + e) : 1.0f) * ldexpf(acc[qq], args.he[pos]);
-          }
-        }
-      }
-      if (!ok) break;
-    }
+    for (int u = u_beg + cw; u < u_end && !*abort_flag; u += kTmaWarps)
+      if (!dn_consume_unit(args, u, smem, stage_bytes, full, empty, ring, q, abort_flag)) break;
   }
   __syncthreads();
 }

@@ -71,6 +71,13 @@ cudaError_t launch_decode_down(const moe_nvfp4_bank& b, moe_csr csr, int T, int 
                                const moe_ws_layout& L, char* ws, cudaStream_t s);
 cudaError_t launch_combine(const float* w, int T, int H, int k, const moe_ws_layout& L, char* ws,
                            float* y, cudaStream_t s);
+// The one-kernel decode layer (decode_layer.cu).
+bool decode_layer_supported(int T, int H, int F, int E, int k);
+size_t decode_layer_sync_bytes();
+cudaError_t launch_decode_layer(const float* logits, int32_t* ids, float* w, const uint16_t* x,
+                                int T, int H, int F, int k, const moe_nvfp4_bank& gu,
+                                const moe_nvfp4_bank& dn, const moe_ws_layout& L, char* ws,
+                                float* y, cudaStream_t s);
 cudaError_t launch_sliced_gate_up(const uint16_t* x_bf16, int T, int H, int F, int k,
                                   const moe_nvfp4_bank& b, moe_csr csr, const moe_ws_layout& L,
                                   char* ws, cudaStream_t s);
@@ -191,6 +198,21 @@ __device__ __forceinline__ uint2 ldg_stream64(const void* p) {
 }
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+
+// Routing key: unsigned order = (logit descending, id ascending); 0 is below every key.
+// -0 and +0 share a key, as the float32 comparison makes them equal.
+__device__ __forceinline__ unsigned long long route_key(float v, int id) {
+  const uint32_t u = (v == 0.0f) ? 0u : __float_as_uint(v);
+  const uint32_t o = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((unsigned long long)o << 32) | (0xffffffffu - (uint32_t)id);
+}
+__device__ __forceinline__ float key_logit(unsigned long long key) {
+  const uint32_t o = (uint32_t)(key >> 32);
+  return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
+}
+__device__ __forceinline__ int key_id(unsigned long long key) {
+  return (int)(0xffffffffu - (uint32_t)key);
+}
 
 // Exponent e with |v| * 2^-e in [2^14, 2^15) for v != 0 (0 for v == 0): the power-of-two
 // prescale that maps a row's largest magnitude into the top binade below f16's 2^15.

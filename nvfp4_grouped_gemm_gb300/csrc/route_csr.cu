@@ -28,19 +28,6 @@ namespace moe {
 namespace {
 
 
-// Routing key: unsigned order = (logit descending, id ascending); 0 is below every key.
-__device__ __forceinline__ unsigned long long route_key(float v, int id) {
-  const uint32_t u = (v == 0.0f) ? 0u : __float_as_uint(v);
-  const uint32_t o = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-  return ((unsigned long long)o << 32) | (0xffffffffu - (uint32_t)id);
-}
-__device__ __forceinline__ float key_logit(unsigned long long key) {
-  const uint32_t o = (uint32_t)(key >> 32);
-  return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
-}
-__device__ __forceinline__ int key_id(unsigned long long key) {
-  return (int)(0xffffffffu - (uint32_t)key);
-}
 __device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) {
   return a > b ? a : b;
 }
