@@ -237,6 +237,8 @@ build_csr_kernel(const int32_t* __restrict__ ids_g, int P, int E, int32_t* __res
 constexpr int kChunkPairs = 2048;
 constexpr int kChunkThreads = 256;
 constexpr int kChunkWarps = kChunkThreads / 32;
+static_assert(kChunkPairs % kChunkThreads == 0 && kChunkPairs % (32 * kChunkWarps) == 0,
+              "whole register batches of ids per thread and per warp slice");
 
 __global__ void __launch_bounds__(kChunkThreads)
 csr_count_kernel(const int32_t* __restrict__ ids, int P, int E, int32_t* __restrict__ cnt,
@@ -248,8 +250,19 @@ csr_count_kernel(const int32_t* __restrict__ ids, int P, int E, int32_t* __restr
   __syncthreads();
   const int p0 = blockIdx.x * kChunkPairs, p1 = min(P, p0 + kChunkPairs);
   bool bad = false;
-  for (int p = p0 + (int)threadIdx.x; p < p1; p += kChunkThreads) {
-    const int e = __ldg(ids + p);
+  // the thread's ids loaded together, then counted
+  constexpr int kPerThread = kChunkPairs / kChunkThreads;
+  int ev[kPerThread];
+#pragma unroll
+  for (int i = 0; i < kPerThread; ++i) {
+    const int p = p0 + (int)threadIdx.x + i * kChunkThreads;
+    ev[i] = p < p1 ? __ldg(ids + p) : 0;
+  }
+#pragma unroll
+  for (int i = 0; i < kPerThread; ++i) {
+    const int p = p0 + (int)threadIdx.x + i * kChunkThreads;
+    if (p >= p1) continue;
+    const int e = ev[i];
     if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
     else { bad = true; pair_pos[p] = -1; }
   }
@@ -267,20 +280,45 @@ csr_scan_kernel(int32_t* __restrict__ cnt, int n_chunks, int E, int32_t* __restr
   pdl_wait();
   pdl_trigger();
   const int e = threadIdx.x;
+  // Up to kScanRegChunks chunks the expert's counts are loaded together into registers (the
+  // loads are independent, one round trip instead of one per chunk) and written once, as
+  // chunk starts, after the offsets are known; beyond that the counts are rewritten in two
+  // passes over memory.
+  constexpr int kScanRegChunks = 32;
+  int c[kScanRegChunks];
+  const bool in_regs = n_chunks <= kScanRegChunks;
   int tot = 0;
-  if (e < E)
-    for (int b = 0; b < n_chunks; ++b) {
-      const int c = cnt[(size_t)b * E + e];
-      cnt[(size_t)b * E + e] = tot;
-      tot += c;
+  if (e < E) {
+    if (in_regs) {
+#pragma unroll
+      for (int b = 0; b < kScanRegChunks; ++b) c[b] = b < n_chunks ? cnt[(size_t)b * E + e] : 0;
+#pragma unroll
+      for (int b = 0; b < kScanRegChunks; ++b) {
+        const int v = c[b];
+        c[b] = tot;
+        tot += v;
+      }
+    } else {
+      for (int b = 0; b < n_chunks; ++b) {
+        const int v = cnt[(size_t)b * E + e];
+        cnt[(size_t)b * E + e] = tot;
+        tot += v;
+      }
     }
+  }
   int total, act_total;
   const int off = block_exclusive_scan(e < E ? tot : 0, scratch, &total);
   const int act = block_exclusive_scan((e < E && tot > 0) ? 1 : 0, scratch, &act_total);
   if (e < E) {
     offsets[e] = off;
     if (tot > 0) active[act] = e;
-    for (int b = 0; b < n_chunks; ++b) cnt[(size_t)b * E + e] += off;
+    if (in_regs) {
+#pragma unroll
+      for (int b = 0; b < kScanRegChunks; ++b)
+        if (b < n_chunks) cnt[(size_t)b * E + e] = c[b] + off;
+    } else {
+      for (int b = 0; b < n_chunks; ++b) cnt[(size_t)b * E + e] += off;
+    }
   }
   if (e == 0) {
     offsets[E] = total;
@@ -295,17 +333,28 @@ csr_place_kernel(const int32_t* __restrict__ ids, int P, int E, const int32_t* _
   extern __shared__ int wh[];                  // [kChunkWarps][E]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int i = tid; i < kChunkWarps * E; i += kChunkThreads) wh[i] = 0;
-  pdl_wait();                                  // the chunk starts are complete
-  pdl_trigger();
   __syncthreads();
   const int p0 = blockIdx.x * kChunkPairs, p1 = min(P, p0 + kChunkPairs);
   const int slice = (p1 - p0 + kChunkWarps - 1) / kChunkWarps;
   const int s0 = min(p1, p0 + warp * slice), s1 = min(p1, s0 + slice);
   int* my = wh + warp * E;
-  for (int p = s0 + lane; p < s1; p += 32) {
-    const int e = __ldg(ids + p);
-    if (e >= 0 && e < E) atomicAdd(&my[e], 1);
+  // The ids were complete before the count kernel passed its wait (two kernels back), so
+  // the warp's slice is loaded (into registers, once) and counted before the wait for the
+  // chunk starts.
+  constexpr int kPerLane = kChunkPairs / kChunkWarps / 32;
+  int ev[kPerLane];
+#pragma unroll
+  for (int i = 0; i < kPerLane; ++i) {
+    const int p = s0 + lane + 32 * i;
+    ev[i] = p < s1 ? __ldg(ids + p) : -1;
   }
+#pragma unroll
+  for (int i = 0; i < kPerLane; ++i) {
+    const int e = ev[i];
+    if (s0 + lane + 32 * i < s1 && e >= 0 && e < E) atomicAdd(&my[e], 1);
+  }
+  pdl_wait();                                  // the chunk starts are complete
+  pdl_trigger();
   __syncthreads();
   for (int e = tid; e < E; e += kChunkThreads) {
     int run = cnt[(size_t)blockIdx.x * E + e];
@@ -316,10 +365,11 @@ csr_place_kernel(const int32_t* __restrict__ ids, int P, int E, const int32_t* _
     }
   }
   __syncthreads();
-  for (int base = s0; base < s1; base += 32) {
-    const int p = base + lane;
+#pragma unroll
+  for (int i = 0; i < kPerLane; ++i) {
+    const int p = s0 + lane + 32 * i;
     const bool in = p < s1;
-    int e = in ? __ldg(ids + p) : -1;
+    int e = ev[i];
     const bool valid = in && e >= 0 && e < E;
     if (!valid) e = -1 - lane;                 // unique key: matches nobody
     const unsigned peers = __match_any_sync(0xffffffffu, e);
@@ -337,7 +387,8 @@ csr_place_kernel(const int32_t* __restrict__ ids, int P, int E, const int32_t* _
 }
 
 // Few pairs (P <= kCsrSmallPairs): one histogram and one scan; pair p's place among the
-// pairs of its expert is the number of earlier pairs with the same expert.
+// pairs of its expert is the number of earlier pairs with the same expert, counted by one
+// warp that walks the pairs in groups of 32.
 constexpr int kCsrSmallPairs = 256;
 
 __global__ void __launch_bounds__(kCsrThreads, 1)
@@ -381,12 +432,25 @@ csr_small_kernel(const int32_t* __restrict__ ids_g, int P, int E, int32_t* __res
   }
   write_tile_lists(E, cnt, off, tiles, slice_tiles, scratch);
   __syncthreads();
-  if (valid) {
-    int rank = 0;
-    for (int q = 0; q < tid; ++q) rank += ids_s[q] == e;
-    const int pos = hist[e] + rank;
-    pair_ids[pos] = tid;
-    pair_pos[tid] = pos;
+  // one warp places the pairs 32 at a time in ascending p: equal experts in a group are
+  // matched and ranked by lane, hist[e] (the expert's next row) advances by the group
+  if (tid < 32) {
+    for (int p0 = 0; p0 < P; p0 += 32) {
+      const int p = p0 + tid;
+      const int ep = p < P ? ids_s[p] : -1;
+      const bool v = ep >= 0;
+      const unsigned peers = __match_any_sync(0xffffffffu, v ? ep : -1 - tid);
+      const unsigned lower = peers & ((1u << tid) - 1u);
+      const int start = v ? hist[ep] : 0;
+      __syncwarp();
+      if (v) {
+        const int pos = start + __popc(lower);
+        pair_ids[pos] = p;
+        pair_pos[p] = pos;
+        if (lower == 0) hist[ep] = start + __popc(peers);
+      }
+      __syncwarp();
+    }
   }
 }
 
