@@ -328,8 +328,13 @@ def recorded_traffic(workloads, kernel: str):
         wl, kern, src, sha, dram, alg = f[:6]
         if wl not in workloads or kern != kernel:
             continue
+        # a kernel whose code spans several files lists them joined by commas; the sha256 is
+        # taken over their bytes in that order
         try:
-            now = hashlib.sha256(open(os.path.join(ROOT, src), "rb").read()).hexdigest()
+            h = hashlib.sha256()
+            for part in src.split(","):
+                h.update(open(os.path.join(ROOT, part), "rb").read())
+            now = h.hexdigest()
         except OSError:
             return None
         if now != sha:
