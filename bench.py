@@ -687,11 +687,118 @@ def measure(name, steps, warmup, batches, dev, rank, world):
         full_g[0].replay()
     torch.cuda.synchronize(dev)
     same = bool(torch.equal(y_hz, bufs["y"].cpu()))
-    e2e = {"value": z_val, "unit": unit, "h2d_bytes_per_step": int(h2d),
-           "d2h_bytes_per_step": int(wl.T * wl.H * 4), "ms_per_step": z_tot / len(z_ms),
-           "how": "pinned host buffers passed to the calls (inputs read and y written by the "
-                  "kernels over the host link, one graph replay per step)",
-           "y_equals_device_run": same, "with_copies": e2e_copies}
+    e2e_zero_copy = {"value": z_val, "unit": unit, "ms_per_step": z_tot / len(z_ms),
+                     "how": "pinned host buffers passed to the calls (inputs read and y written "
+                            "by the kernels over the host link), one step at a time, L2 flushed "
+                            "before each step",
+                     "y_equals_device_run": same}
+
+    # End to end, steps pipelined: while step i's layer runs, step i+1's inputs are copied in
+    # and step i-1's y copied out (a copy-in, a compute and a copy-out stream, two buffer
+    # sets, events between them). Every step still moves its own inputs and result between
+    # pinned host memory and the device inside the timed region, which spans all K steps.
+    # No L2 flush between steps: the weights the steps stream exceed the L2.
+    lay2 = [layer, moe.MoeLayer(gu, dn, wl.k)]
+    sets = []
+    for si in range(2):
+        lay = lay2[si]
+        xd = torch.empty_like(xs[0])
+        ld = torch.empty_like(lgs[0]) if lgs else None
+        idd = torch.empty_like(idss[0]) if idss else None
+        wdd = torch.empty_like(wss[0]) if wss else None
+
+        def fwd(lay=lay, xd=xd, ld=ld, idd=idd, wdd=wdd):
+            if lgs:
+                return lay.forward(xd, logits=ld, path=path, stream=stream)
+            return lay.forward(xd, ids=idd, w=wdd, path=path, stream=stream)
+        with torch.cuda.stream(stream):
+            xd.copy_(xs[0])
+            if lgs:
+                ld.copy_(lgs[0])
+            else:
+                idd.copy_(idss[0])
+                wdd.copy_(wss[0])
+            fwd()
+        stream.synchronize()
+        sets.append({"x": xd, "l": ld, "i": idd, "w": wdd, "y": lay.buffers(wl.T, path)["y"],
+                     "g": capture(fwd)})
+    y_hp = [torch.empty(wl.T, wl.H, dtype=torch.float32).pin_memory() for _ in range(2)]
+    s_in = torch.cuda.Stream(device=dev)
+    s_out = torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_lay = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+
+    def pipeline(n, start_ev):
+        s_in.wait_event(start_ev)
+        for i in range(n):
+            b, si = i % nb, i % 2
+            st = sets[si]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev_lay[si])        # the set's last layer has read its inputs
+                st["x"].copy_(x_h[b], non_blocking=True)
+                if lgs:
+                    st["l"].copy_(l_h[b], non_blocking=True)
+                else:
+                    st["i"].copy_(i_h[b], non_blocking=True)
+                    st["w"].copy_(w_h[b], non_blocking=True)
+                ev_in[si].record(s_in)
+            stream.wait_event(ev_in[si])
+            if i >= 2:
+                stream.wait_event(ev_out[si])          # the set's last y has been read out
+            with torch.cuda.stream(stream):
+                st["g"].replay()
+                ev_lay[si].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_lay[si])
+                y_hp[si].copy_(st["y"], non_blocking=True)
+                ev_out[si].record(s_out)
+        stream.wait_event(ev_out[(n - 1) % 2])
+        if n >= 2:
+            stream.wait_event(ev_out[(n - 2) % 2])
+
+    for n_run, keep in ((warmup, False), (steps, True)):
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        p0 = torch.cuda.Event(enable_timing=True)
+        p1 = torch.cuda.Event(enable_timing=True)
+        p0.record(stream)
+        pipeline(n_run, p0)
+        p1.record(stream)
+        torch.cuda.synchronize(dev)
+    p_tot = max_over_ranks(p0.elapsed_time(p1), dev)
+    n_last = steps - 1
+    p_units = [uniq[i % nb] for i in range(steps)]
+    if prefill:
+        p_val = weak_scaling_value(flops_per_step * steps, world, p_tot * 1e-3) / 1e12
+    else:
+        p_val = weak_scaling_value(sum(u * per_expert for u in p_units), world, p_tot * 1e-3) / 1e9
+    # the last step's host result equals that batch's device-buffer layer, bit for bit
+    with torch.cuda.stream(stream):
+        full_g[n_last % nb].replay()
+    torch.cuda.synchronize(dev)
+    p_same = bool(torch.equal(y_hp[n_last % 2], bufs["y"].cpu()))
+    e2e_pipelined = {"value": p_val, "unit": unit, "ms_per_step": p_tot / steps,
+                     "how": "K steps pipelined: each step's inputs copied in from pinned host "
+                            "memory and its y copied out to pinned host memory inside the "
+                            "timed region, overlapping the neighbouring steps' layers (copy-in, "
+                            "compute and copy-out streams, two buffer sets); whole-region CUDA "
+                            "events; no L2 flush between steps (the streamed weights exceed "
+                            "the L2)",
+                     "y_equals_device_run": p_same}
+    # the line's end-to-end figure is the faster of the two ways a caller can run the layer
+    # on host data (pinned host buffers passed straight to the calls, or copies overlapped
+    # with the neighbouring steps); both are kept, with the serialised-copy run
+    best = e2e_pipelined if e2e_pipelined["ms_per_step"] < e2e_zero_copy["ms_per_step"] \
+        else e2e_zero_copy
+    e2e = {"value": best["value"], "unit": unit, "h2d_bytes_per_step": int(h2d),
+           "d2h_bytes_per_step": int(wl.T * wl.H * 4), "ms_per_step": best["ms_per_step"],
+           "how": ("pipelined copies: " if best is e2e_pipelined else "zero copy: ") + best["how"],
+           "y_equals_device_run": best["y_equals_device_run"], "pipelined": e2e_pipelined,
+           "zero_copy": e2e_zero_copy, "with_copies": e2e_copies}
+    del sets, lay2
 
     # the library's own count of the kernels the CSR, gate/up and down calls launch, plus routing
     launches_per_step = moe.kernel_launches(wl.T, wl.H, wl.F, wl.E, wl.k, path) + (1 if lgs else 0)
