@@ -89,48 +89,51 @@ __global__ void __launch_bounds__(256) quant_x_kernel(const uint16_t* __restrict
 // ---------------------------------------------------------------------------
 // Q(h): one warp per CSR row, the row's blocks in registers as for Q(x)
 // ---------------------------------------------------------------------------
-template <int NB>
+// LPR lanes per row (32 / LPR rows per warp), lane l of a row taking its blocks l, l + LPR,
+// ...: LPR is chosen so that the row's F/16 blocks fill every lane in every pass
+// (F = 640: 8 lanes x 5 blocks), since the per-block work is ALU-bound.  Two passes over
+// the row: the largest magnitude (reduced over the row's lanes), then each block read again
+// (from L1) and quantised, so that no lane holds more than one block.
+template <int LPR>
 __global__ void __launch_bounds__(256) quant_h_kernel(const float* __restrict__ h, int P, int F,
                                                       int sf_pitch,
                                                       const int32_t* __restrict__ offsets, int E,
                                                       uint8_t* __restrict__ qc,
                                                       uint8_t* __restrict__ qs,
                                                       int32_t* __restrict__ qe) {
-  const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  static_assert(LPR >= 4 && LPR <= 32 && (LPR & (LPR - 1)) == 0, "lanes per row");
   const int lane = threadIdx.x & 31;
-  if (r >= P || r >= offsets[E]) return;
+  const int sub = lane % LPR;
+  const int r = (blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * (32 / LPR) + lane / LPR;
+  const bool valid = r < P && r < offsets[E];
   const float* row = h + (size_t)r * F;
   const int nblk = F / 16;
-  float4 v[NB][4];
   float amax = 0.0f;
-#pragma unroll
-  for (int i = 0; i < NB; ++i) {
-    const int b = lane + 32 * i;
-    if (b < nblk) {
+  if (valid)
+    for (int b = sub; b < nblk; b += LPR) {
       const float4* p = reinterpret_cast<const float4*>(row + b * 16);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        v[i][q] = __ldcs(p + q);
-        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[i][q].x), fabsf(v[i][q].y)),
-                                 fmaxf(fabsf(v[i][q].z), fabsf(v[i][q].w))));
+        const float4 v = __ldg(p + q);
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
       }
     }
-  }
+  // the row's lanes are LPR consecutive lanes starting at a multiple of LPR
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  for (int o = LPR / 2; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if (!valid) return;
   const int s = row_exp_of(amax);
   const bool fast = s >= -127 && s <= 149;
   const float m = fast ? pow2f(-s) : 0.0f;
-  if (lane == 0) qe[r] = s;
-#pragma unroll
-  for (int i = 0; i < NB; ++i) {
-    const int b = lane + 32 * i;
-    if (b >= nblk) break;
+  if (sub == 0) qe[r] = s;
+  for (int b = sub; b < nblk; b += LPR) {
+    const float4* p = reinterpret_cast<const float4*>(row + b * 16);
     float key[16];
     uint32_t neg = 0;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const float vv[4] = {v[i][q].x, v[i][q].y, v[i][q].z, v[i][q].w};
+      const float4 v4 = __ldcs(p + q);
+      const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         key[4 * q + e] = fabsf(vv[e]);
@@ -405,11 +408,18 @@ cudaError_t launch_slice_h(const float* h, int P, int F, int sf_pitch, const int
 }
 cudaError_t launch_quant_h(const float* h, int P, int F, int sf_pitch, const int32_t* offsets,
                            int E, uint8_t* qc, uint8_t* qs, int32_t* qe, cudaStream_t s) {
-  const int nb = (F / 16 + 31) / 32;             // blocks per lane
-  if (nb > 8) return cudaErrorInvalidValue;
-  auto kq = nb <= 1 ? quant_h_kernel<1> : nb <= 2 ? quant_h_kernel<2>
-          : nb <= 4 ? quant_h_kernel<4> : quant_h_kernel<8>;
-  kq<<<(P + 7) / 8, 256, 0, s>>>(h, P, F, sf_pitch, offsets, E, qc, qs, qe);
+  // lanes per row: the fewest idle lane-passes (lanes x passes - blocks), ties to more lanes
+  const int nblk = F / 16;
+  int lpr = 32, waste = 32 * ((nblk + 31) / 32) - nblk;
+  for (int c = 16; c >= 4; c /= 2) {
+    const int w = c * ((nblk + c - 1) / c) - nblk;
+    if (w < waste) { lpr = c; waste = w; }
+  }
+  const int rows_per_cta = 8 * (32 / lpr);
+  auto kq = lpr == 4 ? quant_h_kernel<4> : lpr == 8 ? quant_h_kernel<8>
+          : lpr == 16 ? quant_h_kernel<16> : quant_h_kernel<32>;
+  kq<<<(P + rows_per_cta - 1) / rows_per_cta, 256, 0, s>>>(h, P, F, sf_pitch, offsets, E, qc, qs,
+                                                           qe);
   return cudaGetLastError();
 }// Exponent c_F with F * 2688^2 * 2^-c_F < 2^15: the fixed shift of the f16 partials.
 int down_shift_for(int F) {
