@@ -338,6 +338,8 @@ csr_place_kernel(const int32_t* __restrict__ ids, int P, int E, const int32_t* _
   const int slice = (p1 - p0 + kChunkWarps - 1) / kChunkWarps;
   const int s0 = min(p1, p0 + warp * slice), s1 = min(p1, s0 + slice);
   int* my = wh + warp * E;
+  // the next kernel may launch now (it waits for this grid before it reads what it writes)
+  pdl_trigger();
   // The ids were complete before the count kernel passed its wait (two kernels back), so
   // the warp's slice is loaded (into registers, once) and counted before the wait for the
   // chunk starts.
@@ -354,7 +356,6 @@ csr_place_kernel(const int32_t* __restrict__ ids, int P, int E, const int32_t* _
     if (s0 + lane + 32 * i < s1 && e >= 0 && e < E) atomicAdd(&my[e], 1);
   }
   pdl_wait();                                  // the chunk starts are complete
-  pdl_trigger();
   __syncthreads();
   for (int e = tid; e < E; e += kChunkThreads) {
     int run = cnt[(size_t)blockIdx.x * E + e];
