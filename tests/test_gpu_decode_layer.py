@@ -173,3 +173,39 @@ def test_layer_kernel_two_layers_back_to_back():
     yb, _ = _same_as_per_call(b)
     ya2, _ = _same_as_per_call(a)
     assert np.array_equal(_bits(ya), _bits(ya2))
+
+
+def test_layer_kernel_wait_runs_out_then_reports_until_zeroed():
+    """The kernel's bounded waits, made to run out without a fault: the workspace's call
+    counter is set far ahead of the barrier counters (as in a workspace left by another
+    run), so no count the grid reaches satisfies a wait. The waits give up after their 2 s
+    budget, the call sets MOE_DEVERR_TIMEOUT and marks the sync words, the next call only
+    reports it, and after the workspace is zero-filled again the layer is back to normal."""
+    import time
+    wl = synth.decode(1)
+    banks = device_banks(wl)
+    layer = moe.MoeLayer(*banks, wl.k)
+    x = _x(wl)
+    lg = torch.from_numpy(wl.logits).cuda()
+    y_ok = layer.forward_fused(x, logits=lg).cpu().numpy().copy()
+    b = layer.buffers(wl.T, moe.PATH_DECODE)
+    assert moe.get_device_error(b["ws"]) == 0
+    L = moe.workspace_layout(wl.T, wl.H, wl.F, wl.E, wl.k, moe.PATH_DECODE)
+    sync = b["ws"][L["sync"]:L["sync"] + 48].view(torch.int64)
+    assert int(sync[0]) == 1                       # one completed call: the epoch advanced
+    sync[0] = 1000                                 # barrier targets no count can reach
+    t0 = time.time()
+    layer.forward_fused(x, logits=lg)
+    torch.cuda.synchronize()
+    assert time.time() - t0 < 30
+    assert moe.get_device_error(b["ws"]) & moe.DEVERR_TIMEOUT
+    assert int(sync[5]) != 0                       # the sync words are marked
+    t0 = time.time()
+    layer.forward_fused(x, logits=lg)              # reports it without waiting
+    torch.cuda.synchronize()
+    assert time.time() - t0 < 1.0
+    assert moe.get_device_error(b["ws"]) & moe.DEVERR_TIMEOUT
+    b["ws"].zero_()
+    y = layer.forward_fused(x, logits=lg).cpu().numpy()
+    assert moe.get_device_error(b["ws"]) == 0
+    assert np.array_equal(_bits(y), _bits(y_ok))
