@@ -389,3 +389,34 @@ def test_csr_bit_exact_large(T, k, E):
     assert np.array_equal(csr.pair_ids.cpu().numpy()[:T * k], ref.pair_ids)
     assert int(csr.n_active.item()) == ref.n_active
     assert np.array_equal(csr.active_experts.cpu().numpy()[:ref.n_active], ref.active)
+
+
+@pytest.mark.parametrize("name", ["verify_T32", "sliced_F384"])
+def test_sliced_h_slices_bit_exact_against_the_oracle(name):
+    """The four residual slices of h the sliced form writes (codes, block scales, row
+    exponents of every slice row) equal the oracle's q_i = Q(v - q_0 - ... - q_{i-1}) of the
+    GPU's own h rows, bit for bit (the residuals are exact in float32 as in float64)."""
+    from oracle import nvfp4
+    if name == "verify_T32":
+        wl = synth.verify(32)
+    else:
+        wl = synth.logits_workload("sliced_F384", 40, 512, 384, 24, 8, seed=21)
+    assert wl.P >= moe.decode_tensor_core_min_pairs()
+    run = run_layer(wl)
+    assert run.err == 0
+    L, F, NS = run.ws, wl.F, 4
+    R = wl.P * NS
+    pitch = (F // 16 + 15) // 16 * 16
+    n_valid = int(run.offsets[-1])
+    codes = run.ws_raw[L["qh_codes"]:L["qh_codes"] + R * F // 2].reshape(R, F // 2)
+    scales = run.ws_raw[L["qh_scales"]:L["qh_scales"] + R * pitch].reshape(R, pitch)[:, :F // 16]
+    exps = run.ws_raw[L["qh_exp"]:L["qh_exp"] + 4 * R].view(np.int32)
+    v = run.h_csr[:n_valid].astype(np.float64)
+    acc = np.zeros_like(v)
+    for i in range(NS):
+        c, sc, e = nvfp4.quantize(v - acc)
+        rows = np.arange(n_valid) * NS + i
+        assert np.array_equal(codes[rows], c), f"slice {i} codes"
+        assert np.array_equal(scales[rows], sc), f"slice {i} scales"
+        assert np.array_equal(exps[rows], e.astype(np.int32)), f"slice {i} exponents"
+        acc = acc + nvfp4.dequant_q(c, sc, e)
