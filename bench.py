@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--batches", type=int, default=8, help="distinct input batches rotated")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=1)
+    ap.add_argument("--sf-prepack", default="off", choices=["on", "off"],
+                    help="give the layer banks with prepacked scale factors (moe_nvfp4_prepack_sf)")
     ap.add_argument("--no-subresults", dest="subresults", action="store_false",
                     help="time only --workload (by default N=1 also times " +
                     ", ".join(("prefill", "verify_T128", "decode_T1", "union_U60")) + ")")
@@ -373,7 +375,7 @@ def metric_name(workload):
 SUBRESULT_WORKLOADS = ("prefill", "verify_T128", "decode_T1", "union_U60")
 
 
-def measure(name, steps, warmup, batches, dev, rank, world):
+def measure(name, steps, warmup, batches, dev, rank, world, sf_prepack=False):
     """Time one workload: the whole layer as one CUDA graph per step (L2 flushed before
     each), the layer split in three graphs for the breakdown and the roofline of the
     dominant kernel, and the end-to-end call with host buffers.  Returns a dict of the
@@ -389,6 +391,8 @@ def measure(name, steps, warmup, batches, dev, rank, world):
     path = moe.PATH_PREFILL if prefill else moe.PATH_DECODE
     gu = moe.NvFp4Bank.from_numpy(wl.gate_up, dev)
     dn = moe.NvFp4Bank.from_numpy(wl.down, dev)
+    if sf_prepack:
+        gu, dn = gu.prepack_sf(True), dn.prepack_sf(False)
     layer = moe.MoeLayer(gu, dn, wl.k)
 
     # distinct batches of the same shape, rotated step by step
@@ -814,7 +818,8 @@ def measure(name, steps, warmup, batches, dev, rank, world):
                    "l2": "flushed before every step (512 MiB write, then 512 MiB read)",
                    "l2_bytes": int(torch.cuda.get_device_properties(dev).L2_cache_size),
                    "batches_rotated": nb, "unique_experts_mean": float(np.mean(uniq_steps)),
-                   "path": "prefill" if prefill else "decode"},
+                   "path": "prefill" if prefill else "decode",
+                   "sf_prepack": bool(sf_prepack)},
         "roofline": roof, "e2e": e2e, "step_stats": step_stats,
         "gpu_launches": launches_per_step * steps,
         "breakdown_ms": {"route+csr": float(np.mean(pre_ms)), "gate_up": float(np.mean(gu_ms)),
@@ -844,7 +849,8 @@ def run_ours(args):
 
     sampler = ClockSampler(local)
     sampler.start()
-    main = measure(args.workload, args.steps, args.warmup, args.batches, dev, rank, world)
+    pk = args.sf_prepack == "on"
+    main = measure(args.workload, args.steps, args.warmup, args.batches, dev, rank, world, pk)
     clocks = sampler.stop()
     subs = []
     if args.subresults and world == 1:
@@ -855,7 +861,7 @@ def run_ours(args):
             sub_steps = 20 if is_prefill(name) else 50
             sampler = ClockSampler(local)
             sampler.start()
-            r = measure(name, sub_steps, max(3, args.warmup), args.batches, dev, rank, world)
+            r = measure(name, sub_steps, max(3, args.warmup), args.batches, dev, rank, world, pk)
             r["clocks"] = sampler.stop()
             subs.append(r)
 

@@ -95,7 +95,20 @@ typedef struct moe_nvfp4_bank {
   const uint8_t* scales;
   int32_t E, rows, in_f;
   const float* alpha;
+  /* Optional: the scale plane rewritten by moe_nvfp4_prepack_sf (device, 16-byte aligned,
+   * caller-owned) and the order it was written in; NULL and MOE_SF_ATOMS_NONE when the
+   * bank has none. The tensor-core GEMMs (DECODE from moe_decode_tensor_core_min_pairs()
+   * pairs, PREFILL) then copy each stage's weight scale factors straight into tensor memory
+   * instead of rearranging `scales`; the results are bit-identical either way. `scales`
+   * stays required (the other DECODE kernels read it). */
+  const uint8_t* sf_atoms;
+  int32_t sf_atoms_order;
 } moe_nvfp4_bank;
+
+/* Row orders of a prepacked scale plane: a gate/up bank's 128-row tiles interleave gate
+ * row i and up row i (tile t, row m: gate row 64t + m/2 for even m, up row 64t + m/2 for
+ * odd m); a down bank's tiles are rows 128t .. 128t + 127. */
+enum { MOE_SF_ATOMS_NONE = 0, MOE_SF_ATOMS_GATE_UP = 1, MOE_SF_ATOMS_ROWS = 2 };
 
 /* Expert-first CSR written by moe_build_expert_csr (all device arrays, caller-owned):
  *   expert_offsets i32 [E+1]  exclusive prefix sum of per-expert pair counts
@@ -276,6 +289,24 @@ moe_status moe_build_expert_csr_static(const int32_t* topk_ids, int32_t T, int32
  * E times the rows of one expert for a whole bank. in_f % 64 == 0. Async on `stream`. */
 moe_status moe_nvfp4_from_interleaved(const uint8_t* blob, int64_t rows, int32_t in_f,
                                       uint8_t* codes, uint8_t* scales, void* stream);
+
+/* Scale-factor prepack (not on the per-layer path). The block-scaled MMA
+ * (tcgen05.mma kind::mxf4nvf4, scale_vec::4X: one UE4M3 scale per 16 E2M1 weights, the
+ * scaling the pages' NVFP4 format defines) reads a 128-row operand's scale factors for one
+ * K-step of 64 weights from tensor memory: lane r, column x holds the four scale bytes of
+ * row 32x + r. This writes a bank's planar scale plane in that order, one 512-byte atom per
+ * (expert, 128-row tile, K-step): sf_atoms[((e * rows/128 + t) * in_f/64 + j) * 512 + 16r +
+ * 4x + b] = scale byte 4j + b of tile row 32x + r (the tile rows of `order`, above), so a
+ * GEMM stage's atoms are one contiguous copy that tcgen05.cp moves into tensor memory.
+ *   scales    u8 [E][rows][in_f/16] (16-byte aligned, device)
+ *   sf_atoms  u8 [moe_nvfp4_sf_atoms_bytes(E, rows, in_f)] (16-byte aligned, device,
+ *             caller-owned; the same size as `scales`)
+ *   order     MOE_SF_ATOMS_GATE_UP (rows = 2F) or MOE_SF_ATOMS_ROWS
+ * Requires in_f % 64 == 0 and rows % 128 == 0; MOE_ERR_INVALID_ARG otherwise, for a null
+ * or misaligned pointer, or for `bytes` below the size. Async on `stream`. */
+size_t moe_nvfp4_sf_atoms_bytes(int32_t E, int32_t rows, int32_t in_f);
+moe_status moe_nvfp4_prepack_sf(const uint8_t* scales, int32_t E, int32_t rows, int32_t in_f,
+                                int32_t order, uint8_t* sf_atoms, size_t bytes, void* stream);
 
 /* Human-readable name of a status (static string, never NULL). */
 const char* moe_status_string(moe_status status);

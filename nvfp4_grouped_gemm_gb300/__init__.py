@@ -14,6 +14,7 @@ import torch
 
 from . import _native
 from ._native import PATH_AUTO, PATH_DECODE, PATH_PREFILL, DEVERR_EXPERT_ID, DEVERR_TIMEOUT  # noqa
+from ._native import SF_ATOMS_NONE, SF_ATOMS_GATE_UP, SF_ATOMS_ROWS  # noqa
 
 __all__ = ["MoeError", "NvFp4Bank", "ExpertCSR", "workspace_bytes", "workspace_layout", "decode_tensor_core_min_pairs",
            "resolve_path", "prefill_min_pairs", "kernel_launches", "moe_route_topk", "moe_build_expert_csr",
@@ -48,7 +49,8 @@ class NvFp4Bank:
     and optionally alpha f32 [E], a per-expert second-level scale of the weights."""
 
     def __init__(self, codes: torch.Tensor, scales: torch.Tensor,
-                 alpha: Optional[torch.Tensor] = None):
+                 alpha: Optional[torch.Tensor] = None, sf_atoms: Optional[torch.Tensor] = None,
+                 sf_atoms_order: int = 0):
         if codes.dtype != torch.uint8 or scales.dtype != torch.uint8:
             raise TypeError("codes and scales must be uint8")
         if codes.dim() != 3 or scales.dim() != 3:
@@ -59,10 +61,32 @@ class NvFp4Bank:
             if alpha.dtype != torch.float32 or alpha.numel() != codes.shape[0] or \
                     not alpha.is_contiguous() or alpha.device != codes.device:
                 raise ValueError("alpha must be a contiguous float32 [E] tensor beside the codes")
+        if sf_atoms is not None and (sf_atoms.dtype != torch.uint8 or not sf_atoms.is_contiguous()
+                                     or sf_atoms.device != codes.device):
+            raise ValueError("sf_atoms must be a contiguous uint8 tensor beside the codes")
         self.codes, self.scales, self.alpha = codes, scales, alpha
+        self.sf_atoms = sf_atoms
+        self.sf_atoms_order = sf_atoms_order if sf_atoms is not None else _native.SF_ATOMS_NONE
         self.E, self.rows, self.in_f = codes.shape[0], codes.shape[1], codes.shape[2] * 2
         self._c = _native.Bank(codes.data_ptr(), scales.data_ptr(), self.E, self.rows, self.in_f,
-                               alpha.data_ptr() if alpha is not None else None)
+                               alpha.data_ptr() if alpha is not None else None,
+                               sf_atoms.data_ptr() if sf_atoms is not None else None,
+                               self.sf_atoms_order)
+
+    def prepack_sf(self, gate_up: bool, stream=None) -> "NvFp4Bank":
+        """The same bank with its scale plane also written as tensor-memory atoms
+        (moe_nvfp4_prepack_sf) in the row order of the gate/up call (gate_up=True) or of the
+        down call. The tensor-core GEMMs then copy each stage's weight scale factors straight
+        into tensor memory; results are bit-identical to the bank without them."""
+        order = _native.SF_ATOMS_GATE_UP if gate_up else _native.SF_ATOMS_ROWS
+        lib = _native.load()
+        n = lib.moe_nvfp4_sf_atoms_bytes(self.E, self.rows, self.in_f)
+        if n == 0:
+            raise ValueError("prepacking needs rows % 128 == 0 and in_f % 64 == 0")
+        atoms = torch.empty(n, dtype=torch.uint8, device=self.codes.device)
+        _check(lib.moe_nvfp4_prepack_sf(_ptr(self.scales), self.E, self.rows, self.in_f, order,
+                                        _ptr(atoms), n, _stream(stream)), "moe_nvfp4_prepack_sf")
+        return NvFp4Bank(self.codes, self.scales, self.alpha, sf_atoms=atoms, sf_atoms_order=order)
 
     @classmethod
     def from_interleaved(cls, blob: torch.Tensor, E: int, rows: int, in_f: int,

@@ -17,9 +17,12 @@ PATH_AUTO, PATH_DECODE, PATH_PREFILL = 0, 1, 2
 DEVERR_EXPERT_ID, DEVERR_TIMEOUT = 1, 2
 
 
+SF_ATOMS_NONE, SF_ATOMS_GATE_UP, SF_ATOMS_ROWS = 0, 1, 2
+
+
 class Bank(ctypes.Structure):
     _fields_ = [("codes", c_vp), ("scales", c_vp), ("E", c_i32), ("rows", c_i32), ("in_f", c_i32),
-                ("alpha", c_vp)]
+                ("alpha", c_vp), ("sf_atoms", c_vp), ("sf_atoms_order", c_i32)]
 
 
 class CSR(ctypes.Structure):
@@ -40,6 +43,8 @@ SIGNATURES = [
     ("moe_prefill_min_pairs", c_i32, []),
     ("moe_decode_tensor_core_min_pairs", c_i32, []),
     ("moe_nvfp4_from_interleaved", c_i32, [c_vp, ctypes.c_int64, c_i32, c_vp, c_vp, c_vp]),
+    ("moe_nvfp4_sf_atoms_bytes", c_size, [c_i32] * 3),
+    ("moe_nvfp4_prepack_sf", c_i32, [c_vp, c_i32, c_i32, c_i32, c_i32, c_vp, c_size, c_vp]),
     ("moe_resolve_path", c_i32, [c_i32] * 3),
     ("moe_kernel_launches", c_i32, [c_i32] * 6),
     ("moe_route_topk", c_i32, [c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp]),

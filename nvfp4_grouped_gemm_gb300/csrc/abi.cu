@@ -39,11 +39,15 @@ moe_status sizes_supported(int T, int H, int F, int E, int k) {
   return MOE_OK;
 }
 
-moe_status check_bank(const moe_nvfp4_bank* b, int E_expected, int rows, int in_f) {
+// A prepacked scale plane (sf_atoms) must be 16-byte aligned and written in the row order
+// of the call it is passed to: `order`.
+moe_status check_bank(const moe_nvfp4_bank* b, int E_expected, int rows, int in_f, int order) {
   if (!b || !b->codes || !b->scales) return MOE_ERR_INVALID_ARG;
   if (!aligned16(b->codes) || !aligned16(b->scales)) return MOE_ERR_INVALID_ARG;
   if (b->rows != rows || b->in_f != in_f || b->E <= 0) return MOE_ERR_INVALID_ARG;
   if (E_expected > 0 && b->E != E_expected) return MOE_ERR_INVALID_ARG;
+  if (b->sf_atoms && (!aligned16(b->sf_atoms) || b->sf_atoms_order != order))
+    return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
 
@@ -233,7 +237,7 @@ moe_status moe_grouped_gate_up_silu_nvfp4(const void* x_bf16, int32_t T, int32_t
   moe_status st = sizes_supported(T, H, F, E, k);
   if (st != MOE_OK) return st;
   if ((st = path_supported(T, F, k, path)) != MOE_OK) return st;
-  if ((st = check_bank(w_gate_up, E, 2 * F, H)) != MOE_OK) return st;
+  if ((st = check_bank(w_gate_up, E, 2 * F, H, MOE_SF_ATOMS_GATE_UP)) != MOE_OK) return st;
   if ((st = check_csr(csr)) != MOE_OK) return st;
   moe_ws_layout L;
   if (!compute_layout(T, H, F, E, k, path, &L)) return MOE_ERR_INVALID_ARG;
@@ -264,7 +268,7 @@ moe_status moe_grouped_down_combine_nvfp4(const moe_nvfp4_bank* w_down, moe_csr 
   moe_status st = sizes_supported(T, H, F, E, k);
   if (st != MOE_OK) return st;
   if ((st = path_supported(T, F, k, path)) != MOE_OK) return st;
-  if ((st = check_bank(w_down, E, H, F)) != MOE_OK) return st;
+  if ((st = check_bank(w_down, E, H, F, MOE_SF_ATOMS_ROWS)) != MOE_OK) return st;
   if ((st = check_csr(csr)) != MOE_OK) return st;
   moe_ws_layout L;
   if (!compute_layout(T, H, F, E, k, path, &L)) return MOE_ERR_INVALID_ARG;
@@ -301,8 +305,8 @@ moe_status moe_decode_layer_nvfp4(const float* logits, int32_t* topk_ids, float*
   const int E = w_gate_up->E;
   moe_status st = sizes_supported(T, H, F, E, k);
   if (st != MOE_OK) return st;
-  if ((st = check_bank(w_gate_up, E, 2 * F, H)) != MOE_OK) return st;
-  if ((st = check_bank(w_down, E, H, F)) != MOE_OK) return st;
+  if ((st = check_bank(w_gate_up, E, 2 * F, H, MOE_SF_ATOMS_GATE_UP)) != MOE_OK) return st;
+  if ((st = check_bank(w_down, E, H, F, MOE_SF_ATOMS_ROWS)) != MOE_OK) return st;
   if (!moe_decode_layer_supported(T, H, F, E, k)) return MOE_ERR_UNSUPPORTED;
   moe_ws_layout L;
   if (!compute_layout(T, H, F, E, k, MOE_PATH_DECODE, &L)) return MOE_ERR_INVALID_ARG;

@@ -30,9 +30,10 @@ namespace {
 // ---------------------------------------------------------------------------
 // grouped block-scaled GEMM
 // ---------------------------------------------------------------------------
-// GATE_UP: A = Q(x) rows [P][H]; the B tile stacks BN/2 gate rows over the matching BN/2
-//          up rows of the expert, so one N=BN MMA yields g in accumulator columns
-//          [0, BN/2) and u in [BN/2, BN); out = h f32 [P][F] (BN/2 columns per tile).
+// GATE_UP: A = Q(x) rows [P][H]; the B tile interleaves BN/2 gate rows with the matching
+//          up rows of the expert (gate row i, up row i as tile rows 2i, 2i+1: a 3-D tensor
+//          map {bytes, gate/up, row}), so one N=BN MMA yields g_i and u_i in accumulator
+//          columns 2i and 2i+1; out = h f32 [P][F] (BN/2 columns per tile).
 // DOWN:    A = Q(h) rows [P][F], B = BN down rows; out = z * 2^-(row exponent + cF) as f16
 //          [P][H] (the combine restores the scale; the bound |acc| <= F * 2688^2 keeps the
 //          value below 2^15).
@@ -48,6 +49,10 @@ struct GemmArgs {
   // Works are taken in groups of `n_group` N-tiles: all M-tiles of group 0, then of group 1,
   // ...; within a group M-tiles in list order, N fastest (n_group = n_tiles_n: one group).
   int n_group = 0;
+  // PACKED kernels: the weights' scale factors as 512-byte tensor-memory atoms, one per
+  // (expert, 128-row tile, k-step of 64), b_tiles tiles per expert and kst k-steps per row
+  const uint8_t* b_atoms = nullptr;
+  int b_tiles = 0, kst = 0;
 };
 
 // M-tile index and N-tile index of work w (see GemmArgs::n_group).
@@ -97,7 +102,11 @@ struct Cfg {
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-template <int BN, bool GATE_UP>
+// PACKED: the weights' scale factors come as prepacked atoms (GemmArgs::b_atoms), one
+// contiguous copy per stage beside the A staging; one thread of the first transposer warp
+// moves them into TMEM with tcgen05.cp and commits the copies to the stage's full barrier,
+// so the MMA thread still issues nothing but MMAs; the transposer warps handle only A's.
+template <int BN, bool GATE_UP, bool PACKED>
 __global__ void __launch_bounds__(448, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
             const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
@@ -129,7 +138,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&full[s], 1 + 4);                    // TMA expect_tx + 4 transposer warps
+      // TMA expect_tx + 4 transposer warps (+ PACKED: the commit of the atom copies)
+      mbar_init(&full[s], PACKED ? 1 + 4 + 1 : 1 + 4);
       mbar_init(&stg_full[s], 1);                    // TMA expect_tx
       mbar_init(&empty[s], 1);
     }
@@ -158,7 +168,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     if (lane == 0) {
       constexpr uint32_t tx_codes = C::A_BYTES + C::B_BYTES;
       const int g = args.b_sf_group;
-      const uint32_t tx_stg = C::SA_STG + (GATE_UP ? C::SB_STG : (uint32_t)(g == 1 ? BN * 16 : BN * 32));
+      const uint32_t tx_stg =
+          C::SA_STG + (PACKED ? 0u : GATE_UP ? C::SB_STG : (uint32_t)(g == 1 ? BN * 16 : BN * 32));
       const uint64_t wpol = l2_evict_first_policy();
       const int sub_rows = BN / g, sub_w = g == 1 ? 16 : 32;
       int it = 0;
@@ -179,14 +190,18 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
           const int st = it % C::STAGES;
           if (!mbar_wait(&empty[st], ((it / C::STAGES) & 1) ^ 1, abort_flag, args.err)) break;
           unsigned char* sb = smem + st * C::STAGE_BYTES;
-          mbar_expect_tx(&stg_full[st], tx_stg);
+          const int nk = PACKED ? min(4, args.kst - 4 * ks) : 0;   // atoms of the stage
+          mbar_expect_tx(&stg_full[st], tx_stg + 512u * nk);
           mbar_expect_tx(&full[st], tx_codes);
           // scale staging first: the transposers can start while the code tiles stream in
           tma_load_2d(sb + OFF_SA, &tmap_sfa, ks * 16, tile.x, &stg_full[st]);
-          if (GATE_UP) {
-            tma_load_2d(sb + OFF_SB, &tmap_sfb, ks * 16, brow, &stg_full[st]);
-            tma_load_2d(sb + OFF_SB + C::SB_STG / 2, &tmap_sfb, ks * 16, brow + args.F,
-                        &stg_full[st]);
+          if (PACKED) {
+            const int t = args.n_base + wn;                 // the weight tile of this work
+            bulk_load(sb + OFF_SB,
+                      args.b_atoms + ((size_t)(tile.z * args.b_tiles + t) * args.kst + 4 * ks) * 512,
+                      512u * nk, &stg_full[st]);
+          } else if (GATE_UP) {
+            tma_load_3d_hint(sb + OFF_SB, &tmap_sfb, ks * 16, 0, brow, &stg_full[st], wpol);
           } else {
             for (int s2 = 0; s2 < g; ++s2) {
               const int x = ((s2 * sfrow + 16 * ks) >> 4) << 4;
@@ -195,13 +210,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
             }
           }
           tma_load_2d(sb, &tmap_a, ks * C::KB, tile.x, &full[st]);
-          if (GATE_UP) {
+          if (GATE_UP)
+            tma_load_3d_hint(sb + C::A_BYTES, &tmap_b, ks * C::KB, 0, brow, &full[st], wpol);
+          else
             tma_load_2d_hint(sb + C::A_BYTES, &tmap_b, ks * C::KB, brow, &full[st], wpol);
-            tma_load_2d_hint(sb + C::A_BYTES + C::B_BYTES / 2, &tmap_b, ks * C::KB, brow + args.F,
-                             &full[st], wpol);
-          } else {
-            tma_load_2d_hint(sb + C::A_BYTES, &tmap_b, ks * C::KB, brow, &full[st], wpol);
-          }
         }
         tile = next;
         next = next2;
@@ -261,7 +273,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     // ---------------- scale-factor transposers (128 threads, one TMEM lane quarter each) ---
     // Lane r of warp w writes TMEM lane 32*(w%4) + r: for k-step j, columns 4j + x hold the
     // scale word of row r + 32x.  Scale bytes past the row's K/16 (the zero-filled tail of
-    // the last stage) are written as 0.
+    // the last stage) are written as 0.  PACKED: A's only.
     static_assert(C::G == 1, "one 128-row scale group per operand");
     const int n_it = ((n_work - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x) * k_stages;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
@@ -274,14 +286,22 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
       tc_fence_after();
       const uint32_t sb = smem_u32(smem + st * C::STAGE_BYTES);
       const int nvalid = min(4, (sfrow - 16 * ks) >> 2);   // u32 words of this stage in a row
+      if (PACKED && warp == 2 && lane == 0) {
+        // the weight atoms into the stage's B columns, completing on full[st]
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (j < nvalid) tc_cp_sf(sf_col0 + st * C::SF_COLS + 16 + 4 * j, sb + OFF_SB + 512 * j);
+        tc_commit(&full[st]);
+      }
       uint32_t va[16], vb[16];
 #pragma unroll
       for (int x = 0; x < 4; ++x) {
         const int row = lane + 32 * x;
         const uint4 a4 = lds128(sb + OFF_SA + 16 * row);
         const uint32_t a[4] = {a4.x, a4.y, a4.z, a4.w};
-        uint32_t b[4];
-        if (GATE_UP) {
+        uint32_t b[4] = {0u, 0u, 0u, 0u};
+        if (PACKED) {
+        } else if (GATE_UP) {
           const uint4 b4 = lds128(sb + OFF_SB + 16 * row);
           b[0] = b4.x; b[1] = b4.y; b[2] = b4.z; b[3] = b4.w;
         } else {
@@ -299,7 +319,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
       }
       const uint32_t sfc = sf_col0 + st * C::SF_COLS + lane_base;
       tc_st16(sfc, va);
-      tc_st16(sfc + 16, vb);
+      if (!PACKED) tc_st16(sfc + 16, vb);
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
       __syncwarp();
@@ -330,11 +350,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
       tc_fence_after();
       const uint32_t acc = acc_col + ab * BN + lane_base;
       if (GATE_UP) {
-        // this warp: accumulator columns [32*half, +32) (gate) and BN/2 + the same (up)
+        // this warp: accumulator columns [64*half, +64) = (g_i, u_i) of h columns
+        // [32*half, +32)
         float* orow = reinterpret_cast<float*>(args.out) + (size_t)(valid ? pos : 0) * args.out_cols + n0;
-        static_assert(BN / 64 == 2, "one 32-column chunk per epilogue warp");
-        float g[32], u[32];
-        tc_ld32x2(acc + half * 32, acc + BN / 2 + half * 32, g, u);
+        static_assert(BN / 64 == 2, "one 32-column chunk of h per epilogue warp");
+        float gu[2][32];
+        tc_ld32x2(acc + half * 64, acc + half * 64 + 32, gu[0], gu[1]);
         // the values are in registers: hand the accumulator buffer back to the MMA thread
         tc_fence_before();
         __syncwarp();
@@ -345,8 +366,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
             float o[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const float gg = al * (fast ? g[i + q] * m : ldexpf(g[i + q], sx));
-              const float uu = al * (fast ? u[i + q] * m : ldexpf(u[i + q], sx));
+              const float* v = gu[(i + q) >> 4] + 2 * ((i + q) & 15);
+              const float gg = al * (fast ? v[0] * m : ldexpf(v[0], sx));
+              const float uu = al * (fast ? v[1] * m : ldexpf(v[1], sx));
               o[q] = silu_f(gg) * uu;
             }
             *reinterpret_cast<float4*>(orow + half * 32 + i) = make_float4(o[0], o[1], o[2], o[3]);
@@ -474,6 +496,7 @@ __device__ __forceinline__ void chunk_range(int c, int nr, int n_tiles_n, int& m
   n_hi = min(n_tiles_n, n_lo + kChunkN);
 }
 
+template <bool PACKED>
 __global__ void __launch_bounds__(448, 1)
 down_resident_kernel(const __grid_constant__ CUtensorMap tmap_a,
                      const __grid_constant__ CUtensorMap tmap_b,
@@ -513,7 +536,9 @@ down_resident_kernel(const __grid_constant__ CUtensorMap tmap_a,
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&full[s], 1 + 4);
+      // PACKED: the stage's codes and scale-factor atoms, both TMA bytes; otherwise the
+      // codes and one arrive per transposer warp
+      mbar_init(&full[s], PACKED ? 1 : 1 + 4);
       mbar_init(&stg_full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -586,12 +611,21 @@ down_resident_kernel(const __grid_constant__ CUtensorMap tmap_a,
               break;
             }
             unsigned char* sb = bring + st * C::STAGE_BYTES;
-            mbar_expect_tx(&stg_full[st], tx_sb);
-            mbar_expect_tx(&full[st], C::B_CODES);
-            for (int s2 = 0; s2 < g; ++s2) {
-              const int x = ((s2 * sfrow + 16 * ks) >> 4) << 4;
-              tma_load_2d(sb + C::B_CODES + s2 * sub_rows * sub_w, &tmap_sfb, x, brow / g,
-                          &stg_full[st]);
+            if (PACKED) {
+              // the stage's k-steps of atoms: one contiguous copy
+              const int nk = min(4, args.kst - 4 * ks);
+              mbar_expect_tx(&full[st], (uint32_t)(C::B_CODES + 512 * nk));
+              bulk_load(sb + C::B_CODES,
+                        args.b_atoms + ((size_t)(tile.z * args.b_tiles + n) * args.kst + 4 * ks) * 512,
+                        512u * nk, &full[st]);
+            } else {
+              mbar_expect_tx(&stg_full[st], tx_sb);
+              mbar_expect_tx(&full[st], C::B_CODES);
+              for (int s2 = 0; s2 < g; ++s2) {
+                const int x = ((s2 * sfrow + 16 * ks) >> 4) << 4;
+                tma_load_2d(sb + C::B_CODES + s2 * sub_rows * sub_w, &tmap_sfb, x, brow / g,
+                            &stg_full[st]);
+              }
             }
             tma_load_2d_hint(sb, &tmap_b, ks * C::KB, brow, &full[st], wpol);
           }
@@ -605,7 +639,7 @@ down_resident_kernel(const __grid_constant__ CUtensorMap tmap_a,
         for (int s = 0; s < C::STAGES; ++s) {
           if (it <= s) continue;
           const int last = s + ((it - 1 - s) / C::STAGES) * C::STAGES;
-          while ((!mbar_try(&stg_full[s], (last / C::STAGES) & 1) ||
+          while (((!PACKED && !mbar_try(&stg_full[s], (last / C::STAGES) & 1)) ||
                   !mbar_try(&full[s], (last / C::STAGES) & 1)) &&
                  global_ns() - t0 < 100000000ull) {
           }
@@ -658,6 +692,12 @@ down_resident_kernel(const __grid_constant__ CUtensorMap tmap_a,
             const uint64_t bo = (uint64_t)((st * C::STAGE_BYTES) >> 4);
             const uint32_t sfb = sfb_col0 + st * C::SFB_COLS;
             const int nk = min(4, (sfrow - 16 * ks) >> 2);   // k-steps past K are skipped
+            if (PACKED) {
+              const uint32_t atoms = smem_u32(bring + st * C::STAGE_BYTES + C::B_CODES);
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                if (j < nk) tc_cp_sf(sfb + 4 * j, atoms + 512 * j);
+            }
 #pragma unroll
             for (int j = 0; j < 4; ++j)
               if (j < nk)
@@ -710,7 +750,10 @@ down_resident_kernel(const __grid_constant__ CUtensorMap tmap_a,
     };
     bool ok = write_sfa(0);
     int it = 0, ca = 0;
-    for (int c = blockIdx.x; c < n_chunk && ok; c += gridDim.x, ++ca) {
+    // PACKED: the weight scale factors reach TMEM by tcgen05.cp; only the chunks' A remain
+    if (PACKED)
+      for (int q = 1; ok && blockIdx.x + q * gridDim.x < n_chunk; ++q) ok = write_sfa(q);
+    for (int c = blockIdx.x; c < n_chunk && ok && !PACKED; c += gridDim.x, ++ca) {
       int m, n_lo, n_hi;
       chunk_range(c, nr, args.n_tiles_n, m, n_lo, n_hi);
       for (int n = n_lo; n < n_hi && ok; ++n) {
@@ -845,7 +888,7 @@ cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtenso
                      const CUtensorMap& msb, const CUtensorMap& mo, const GemmArgs& a, int max_tiles,
                      cudaStream_t s) {
   using C = Cfg<BN, GATE_UP>;
-  auto kern = gemm_kernel<BN, GATE_UP>;
+  auto kern = a.b_atoms ? gemm_kernel<BN, GATE_UP, true> : gemm_kernel<BN, GATE_UP, false>;
   cudaError_t st = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (st != cudaSuccess) return st;
   int grid = max_tiles * a.n_tiles_n;
@@ -859,7 +902,7 @@ cudaError_t run_down_resident(const CUtensorMap& ma, const CUtensorMap& mb, cons
                               const CUtensorMap& msb, const CUtensorMap& mo, const GemmArgs& a,
                               int max_tiles, cudaStream_t s) {
   using C = DCfg;
-  auto kern = down_resident_kernel;
+  auto kern = a.b_atoms ? down_resident_kernel<true> : down_resident_kernel<false>;
   cudaError_t st = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (st != cudaSuccess) return st;
   int grid = max_tiles * ((a.n_tiles_n + kChunkN - 1) / kChunkN);
@@ -886,16 +929,30 @@ cudaError_t launch_prefill_gate_up(const uint16_t* x_bf16, int T, int H, int F, 
                                   reinterpret_cast<const int32_t*>(ws + L.pair_pos), qc, qs, qe, s);
   if (st != cudaSuccess) return st;
   CUtensorMap ma, mb, msa, msb;
-  constexpr int BN = 128;                           // 64 gate rows over 64 up rows
-  const uint64_t wrows = (uint64_t)b.E * 2 * F;
+  constexpr int BN = 128;                           // 64 gate rows interleaved with 64 up rows
+  // weights: [K bytes][gate, up][row], so the box {128 B, 2, 64} lands gate row i and up row i
+  // as shared-memory rows 2i and 2i+1 (and the scale box {16 B, 2, 64} their staging rows);
+  // the row extent stops F rows short of the bank so the up coordinate (row + F) stays inside
+  const uint64_t wrows = (uint64_t)b.E * 2 * F - F;
+  const uint64_t cdims[3] = {(uint64_t)H / 2, 2, wrows};
+  const uint64_t cstr[2] = {(uint64_t)F * (H / 2), (uint64_t)H / 2};
+  const uint32_t cbox[3] = {128, 2, BN / 2};
+  const uint64_t sdims[3] = {(uint64_t)H / 16, 2, wrows};
+  const uint64_t sstr[2] = {(uint64_t)F * (H / 16), (uint64_t)H / 16};
+  const uint32_t sbox[3] = {16, 2, BN / 2};
   if (!make_map(&ma, qc, H / 2, H / 2, P, 128, 128, true) ||
-      !make_map(&mb, b.codes, H / 2, H / 2, wrows, 128, BN / 2, true) ||
+      !make_map3(&mb, b.codes, cdims, cstr, cbox, true) ||
       !make_map(&msa, qs, H / 16, H / 16, P, 16, 128, false) ||
-      !make_map(&msb, b.scales, H / 16, H / 16, wrows, 16, BN / 2, false))
+      !make_map3(&msb, b.scales, sdims, sstr, sbox, false))
     return cudaErrorInvalidValue;
   GemmArgs a{qe, tiles, ws + L.h, reinterpret_cast<uint32_t*>(ws + L.error_word),
              P, H, 2 * F, F / (BN / 2), F, F, 0, 1, 0};
   a.alpha = b.alpha;
+  if (b.sf_atoms) {
+    a.b_atoms = b.sf_atoms;
+    a.b_tiles = F / 64;
+    a.kst = H / 64;
+  }
   a.n_group = a.n_tiles_n;                          // one group: M-tiles in order, N fastest
   const int max_tiles = P / 128 + (P < b.E ? P : b.E) + 1;
   return run_gemm<BN, true>(ma, mb, msa, msb, ma /* unused */, a, max_tiles, s);
@@ -935,6 +992,11 @@ cudaError_t launch_prefill_down(const moe_nvfp4_bank& b, moe_csr csr, const floa
   GemmArgs a{qe, reinterpret_cast<const int32_t*>(ws + L.tiles), ws + L.partial,
              reinterpret_cast<uint32_t*>(ws + L.error_word), P, F, H, H / BN, H, F, shift, g, 0};
   a.alpha = b.alpha;
+  if (b.sf_atoms) {
+    a.b_atoms = b.sf_atoms;
+    a.b_tiles = H / 128;
+    a.kst = F / 64;
+  }
   a.n_group = a.n_tiles_n;                          // one group: M-tiles in order, N fastest
   // the f16 partials [P][H]: box {64 columns, 32 rows}, 128-byte swizzle
   CUtensorMap mo;

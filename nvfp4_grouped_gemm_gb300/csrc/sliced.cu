@@ -23,7 +23,10 @@
 // Warp roles as in the prefill GEMM: warp 0 issues TMA (codes and scale staging images),
 // warp 1's one thread issues tcgen05.mma (kind::mxf4nvf4, scale_vec::4X), warps 2-5 move
 // the scale factors into TMEM with tcgen05.st, warps 6-9 (one per TMEM lane quarter) drain
-// the double-buffered accumulator.  Every mbarrier wait is bounded by a 2 s %globaltimer
+// the double-buffered accumulator.  With a prepacked bank (PACKED) the weights' scale
+// factors arrive as atoms, one contiguous copy per stage beside the slice staging; one
+// thread of warp 2 moves them into TMEM with tcgen05.cp and commits the copies to the
+// stage's full barrier; warps 2-5 then transpose only the slices'.  Every mbarrier wait is bounded by a 2 s %globaltimer
 // budget; on expiry the CTA sets MOE_DEVERR_TIMEOUT, drains its copies and frees its TMEM.
 #include <cmath>
 
@@ -85,6 +88,10 @@ struct SlicedArgs {
   int a_sf_group;              // down: g weight-scale rows per tensor-map row
   int sb_w;                    // bytes per slice-scale staging row: min(16*KSUB, scale pitch)
   const float* alpha = nullptr;   // [E] per-expert second-level weight scale, or none
+  // PACKED: the weights' 512-byte scale-factor atoms, one per (expert, 128-row tile, k-step
+  // of 64); n_tiles_n tiles per expert, kst k-steps per row
+  const uint8_t* a_atoms = nullptr;
+  int kst = 0;
 };
 
 
@@ -100,7 +107,7 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&a)[32]) {
   for (int i = 0; i < 32; ++i) a[i] = __uint_as_float(r[i]);
 }
 
-template <bool GATE_UP>
+template <bool GATE_UP, bool PACKED>
 __global__ void __launch_bounds__(SCfg<GATE_UP>::THREADS, 1)
 sliced_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                    const __grid_constant__ CUtensorMap tmap_sfa,
@@ -137,7 +144,8 @@ sliced_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&full[s], 1 + 4);
+      // TMA expect_tx + 4 transposer warps (+ PACKED: the commit of the atom copies)
+      mbar_init(&full[s], PACKED ? 1 + 4 + 1 : 1 + 4);
       mbar_init(&stg_full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -168,7 +176,8 @@ sliced_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
     if (lane == 0) {
       constexpr uint32_t tx_codes = C::A_BYTES + C::B_BYTES;
       const int g = GATE_UP ? 1 : args.a_sf_group;
-      const uint32_t tx_stg = (uint32_t)(GATE_UP ? C::SA_STG : 128 * sfrow) + (uint32_t)(C::NB * args.sb_w);
+      const uint32_t tx_stg = (PACKED ? 0u : (uint32_t)(GATE_UP ? C::SA_STG : 128 * sfrow)) +
+                              (uint32_t)(C::NB * args.sb_w);
       const uint64_t wpol = l2_evict_first_policy();
       // The slice half of a stage (B codes and B scale staging) reads what the previous
       // kernel writes; the weight half depends only on the tile list.  The weight halves of
@@ -207,13 +216,20 @@ sliced_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
           unsigned char* sb = smem + st * C::STAGE_BYTES;
           // sub-tiles that start past the row are not fetched (their k-steps are skipped)
           const int nsub = min(C::KSUB, (args.K / 2 - ks * C::KSUB * C::KB + C::KB - 1) / C::KB);
-          mbar_expect_tx(&stg_full[st], tx_stg);
+          const int nk = PACKED ? min(C::KSTEPS, args.kst - C::KSTEPS * ks) : 0;   // atoms
+          mbar_expect_tx(&stg_full[st], tx_stg + 512u * nk);
           mbar_expect_tx(&full[st], tx_codes / C::KSUB * nsub);
           // scale staging first: the transposers can start while the code tiles stream in
-          if (GATE_UP)
+          if (PACKED) {
+            const int t = w % args.n_tiles_n;
+            bulk_load(sb + OFF_SA,
+                      args.a_atoms + ((size_t)(tile.z * args.n_tiles_n + t) * args.kst + C::KSTEPS * ks) * 512,
+                      512u * nk, &stg_full[st]);
+          } else if (GATE_UP) {
             tma_load_3d_hint(sb + OFF_SA, &tmap_sfa, ks * 16 * C::KSUB, 0, wrow, &stg_full[st], wpol);
-          else
+          } else {
             tma_load_2d_hint(sb + OFF_SA, &tmap_sfa, 0, wrow / g, &stg_full[st], wpol);
+          }
 #pragma unroll
           for (int q = 0; q < C::KSUB; ++q) {
             if (q >= nsub) break;
@@ -291,7 +307,7 @@ sliced_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
     // Lane r of warp w writes TMEM lane 32*(w%4) + r.  A (weights, 128 rows): for k-step j,
     // columns 4j + x hold the scale word of row r + 32x.  B (32 slice rows), from column
     // 4*KSTEPS on: column 4j holds row r's word, 4j+1..4j+3 are zero.  Words past the row's
-    // K/16 bytes are zero.
+    // K/16 bytes are zero.  PACKED: B's only.
     const int n_it = ((n_work - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x) * k_stages;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const int g = GATE_UP ? 1 : args.a_sf_group;
@@ -303,9 +319,17 @@ sliced_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
       tc_fence_after();
       const uint32_t sb = smem_u32(smem + st * C::STAGE_BYTES);
       const int nvalid = min(KW, (sfrow - 4 * KW * ks) >> 2);
+      if (PACKED && warp == 2 && lane == 0) {
+        // the weight atoms into the stage's A columns, completing on full[st]
+#pragma unroll
+        for (int j = 0; j < KW; ++j)
+          if (j < nvalid) tc_cp_sf(sf_col0 + st * C::SF_COLS + 4 * j, sb + OFF_SA + 512 * j);
+        tc_commit(&full[st]);
+      }
       uint32_t va[4 * KW], vb[4 * KW];
 #pragma unroll
       for (int x = 0; x < 4; ++x) {
+        if (PACKED) break;
         const int row = lane + 32 * x;
         uint32_t a[KW];
         if (GATE_UP) {
@@ -341,7 +365,7 @@ sliced_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
       const uint32_t sfc = sf_col0 + st * C::SF_COLS + lane_base;
 #pragma unroll
       for (int q = 0; q < KW / 4; ++q) {
-        tc_st16(sfc + 16 * q, *reinterpret_cast<const uint32_t(*)[16]>(va + 16 * q));
+        if (!PACKED) tc_st16(sfc + 16 * q, *reinterpret_cast<const uint32_t(*)[16]>(va + 16 * q));
         tc_st16(sfc + 4 * KW + 16 * q, *reinterpret_cast<const uint32_t(*)[16]>(vb + 16 * q));
       }
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
@@ -419,7 +443,7 @@ template <bool GATE_UP>
 cudaError_t run_sliced(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msa,
                        const CUtensorMap& msb, const SlicedArgs& a, int max_tiles, cudaStream_t s) {
   using C = SCfg<GATE_UP>;
-  auto kern = sliced_gemm_kernel<GATE_UP>;
+  auto kern = a.a_atoms ? sliced_gemm_kernel<GATE_UP, true> : sliced_gemm_kernel<GATE_UP, false>;
   cudaError_t st = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (st != cudaSuccess) return st;
   int grid = max_tiles * a.n_tiles_n;
@@ -467,6 +491,10 @@ cudaError_t launch_sliced_gate_up(const uint16_t* x_bf16, int T, int H, int F, i
   SlicedArgs a{qe, tiles, reinterpret_cast<float*>(ws + L.h),
                reinterpret_cast<uint32_t*>(ws + L.error_word), H, 2 * F, F / 64, F, F, 1, sbw};
   a.alpha = b.alpha;
+  if (b.sf_atoms) {
+    a.a_atoms = b.sf_atoms;
+    a.kst = H / 64;
+  }
   const int max_tiles = (int)(rows / kSliceTile) + (P < b.E ? P : b.E) + 1;
   return run_sliced<true>(ma, mb, msa, msb, a, max_tiles, s);
 }
@@ -503,6 +531,10 @@ cudaError_t launch_sliced_down(const moe_nvfp4_bank& b, moe_csr csr, int T, int 
                reinterpret_cast<float*>(ws + L.partial),
                reinterpret_cast<uint32_t*>(ws + L.error_word), F, H, H / 128, H, F, g, sbw};
   a.alpha = b.alpha;
+  if (b.sf_atoms) {
+    a.a_atoms = b.sf_atoms;
+    a.kst = F / 64;
+  }
   const int max_tiles = (int)(rows / kSliceTile) + (P < b.E ? P : b.E) + 1;
   return run_sliced<false>(ma, mb, msa, msb, a, max_tiles, s);
 }

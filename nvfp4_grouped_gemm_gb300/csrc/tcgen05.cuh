@@ -37,9 +37,16 @@ __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint3
       ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
       : "memory");
 }
-// Two k-steps' scale-factor atoms (32 rows x 16 B each, the second one LBO bytes after the
-// first) into 8 TMEM columns: lanes 0..31 receive the atoms (lanes 32..127 receive bytes
-// the MMA does not read).
+// One k-step's scale factors of a 128-row operand into 4 TMEM columns from a 512-byte
+// atom in shared memory (byte 16r + 4x + b: scale byte b of row 32x + r; 32 rows of 16 B,
+// eight-row core matrices 128 B apart, no swizzle): lane r of every lane quarter receives
+// row r's 16 bytes (the 32x128b shape, multicast to the four quarters).  Issued by the MMA
+// thread before the MMAs that read the columns; the tensor pipe runs the two in issue
+// order, and a later commit also tracks the copy's reads of shared memory.
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint32_t atom_addr) {
+  const uint64_t d = smem_desc(atom_addr, 0, 128, 0);
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(d) : "memory");
+}
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"

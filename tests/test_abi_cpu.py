@@ -119,6 +119,37 @@ def test_host_validation_rejects_before_launch(lib):
                                               None, 256, 1 << 20, None) == 1
 
 
+def test_prepack_sizes_and_validation(lib):
+    """The prepacked scale plane is as large as the planar one; sizes it cannot tile, null
+    or misaligned pointers, a short buffer, an unknown order, and a bank whose plane was
+    written in the other call's row order are rejected on the host (no CUDA call)."""
+    assert lib.moe_nvfp4_sf_atoms_bytes(512, 1280, 2560) == 512 * 1280 * 2560 // 16
+    assert lib.moe_nvfp4_sf_atoms_bytes(288, 4096, 640) == 288 * 4096 * 640 // 16
+    assert lib.moe_nvfp4_sf_atoms_bytes(4, 192, 256) == 0          # rows % 128
+    assert lib.moe_nvfp4_sf_atoms_bytes(4, 256, 96) == 0           # in_f % 64
+    assert lib.moe_nvfp4_sf_atoms_bytes(0, 256, 256) == 0
+    n = 4 * 256 * 256 // 16
+    GU, ROWS = moe.SF_ATOMS_GATE_UP, moe.SF_ATOMS_ROWS
+    assert lib.moe_nvfp4_prepack_sf(None, 4, 256, 256, GU, 256, n, None) == 1
+    assert lib.moe_nvfp4_prepack_sf(256, 4, 256, 256, GU, None, n, None) == 1
+    assert lib.moe_nvfp4_prepack_sf(256, 4, 256, 256, GU, 256, n - 16, None) == 1
+    assert lib.moe_nvfp4_prepack_sf(256, 4, 256, 256, 3, 256, n, None) == 1
+    assert lib.moe_nvfp4_prepack_sf(256, 4, 256, 256, ROWS, 264, n, None) == 1
+    assert lib.moe_nvfp4_prepack_sf(256, 4, 192, 256, ROWS, 256, n, None) == 1
+    good = _native.CSR(16, 16, 16, 16)
+    # a gate/up bank (rows = 2F = 128, in_f = H = 256) carrying a down-order plane, and a
+    # misaligned plane
+    wrong = _native.Bank(16, 16, 16, 128, 256, None, 256, ROWS)
+    assert lib.moe_grouped_gate_up_silu_nvfp4(16, 4, 256, 64, 2, ctypes.byref(wrong), good, 0,
+                                              256, 1 << 30, None) == 1
+    odd = _native.Bank(16, 16, 16, 128, 256, None, 264, GU)
+    assert lib.moe_grouped_gate_up_silu_nvfp4(16, 4, 256, 64, 2, ctypes.byref(odd), good, 0,
+                                              256, 1 << 30, None) == 1
+    dwrong = _native.Bank(16, 16, 16, 256, 64, None, 256, GU)
+    assert lib.moe_grouped_down_combine_nvfp4(ctypes.byref(dwrong), good, 16, 4, 256, 64, 2, 0,
+                                              256, 256, 1 << 30, None) == 1
+
+
 def test_kernel_launch_count_host_logic(lib):
     """The per-layer kernel count the library reports follows its own launch plan: decode
     below 256 pairs runs x-gather, gate/up, h-prep, down and combine after the CSR; from 256
