@@ -47,8 +47,9 @@ def parse():
     ap.add_argument("--batches", type=int, default=8, help="distinct input batches rotated")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=1)
-    ap.add_argument("--sf-prepack", default="off", choices=["on", "off"],
-                    help="give the layer banks with prepacked scale factors (moe_nvfp4_prepack_sf)")
+    ap.add_argument("--sf-prepack", default="on", choices=["on", "off"],
+                    help="give the layer banks with prepacked scale factors "
+                         "(moe_nvfp4_prepack_sf, one-time, before timing); off: planar only")
     ap.add_argument("--no-subresults", dest="subresults", action="store_false",
                     help="time only --workload (by default N=1 also times " +
                     ", ".join(("prefill", "verify_T128", "decode_T1", "union_U60")) + ")")
@@ -567,7 +568,8 @@ def measure(name, steps, warmup, batches, dev, rank, world, sf_prepack=False):
                + wl.P * wl.F * 4)
         gu_s = float(np.mean(gu_ms)) * 1e-3
         fpk, fpk_src = peak_fp4(peaks, sustained=False)
-        ratio = recorded_traffic([name, "prefill_T1024"], "gemm_kernel<128,1>")
+        ratio = recorded_traffic([name, "prefill_T1024"],
+                                 "gemm_kernel<128,1,%d>" % (1 if sf_prepack else 0))
         gu_flops = wl.P * 2 * (2 * wl.F * wl.H)
         roof = {"bound": "hbm", "kernel": "prefill gate_up (graph of tiles + Q(x) + tcgen05 "
                 "block-scaled GEMM)", "achieved": alg / gu_s / 1e9, "peak": pk, "unit": "GB/s",
@@ -593,7 +595,8 @@ def measure(name, steps, warmup, batches, dev, rank, world, sf_prepack=False):
         alg = sum(gu_bytes) / len(gu_bytes)
         # from moe.decode_tensor_core_min_pairs() pairs the decode call runs the sliced form
         sliced = wl.P >= moe.decode_tensor_core_min_pairs()
-        ratio = (recorded_traffic([name, "verify_T128"], "sliced_gemm_kernel<1>") if sliced
+        ratio = (recorded_traffic([name, "verify_T128"],
+                                  "sliced_gemm_kernel<1,%d>" % (1 if sf_prepack else 0)) if sliced
                  else recorded_traffic([name, "decode_T8"], "gate_up_tma_kernel"))
         roof = {"bound": "hbm", "kernel": "decode gate_up+SiLU (moe_grouped_gate_up_silu_nvfp4; " +
                 ("x slices + tcgen05 sliced GEMM)" if sliced else "x staging + TMA-fed mma.sync kernel)"),
@@ -802,6 +805,15 @@ def measure(name, steps, warmup, batches, dev, rank, world, sf_prepack=False):
            "how": ("pipelined copies: " if best is e2e_pipelined else "zero copy: ") + best["how"],
            "y_equals_device_run": best["y_equals_device_run"], "pipelined": e2e_pipelined,
            "zero_copy": e2e_zero_copy, "with_copies": e2e_copies}
+    # every workspace the layers used: a set bit (a bounded wait that ran out, an invalid
+    # expert id) means some step's result is not the layer's, so no number is reported
+    torch.cuda.synchronize(dev)
+    for lay in lay2:
+        for (T_, path_), bb in lay._bufs.items():
+            code = moe.get_device_error(bb["ws"])
+            if code != 0:
+                raise RuntimeError(f"device error word {code} in the ({T_}, {path_}) workspace "
+                                   f"of {name}")
     del sets, lay2
 
     # the library's own count of the kernels the CSR, gate/up and down calls launch, plus routing

@@ -456,7 +456,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
 // chunk before the MMAs need it (an A tile takes about 2 us to land even from L2 while the
 // weights stream).  The epilogue stages its partials in 2 KiB per warp (two 32-column TMA
 // stores, 64-byte swizzle), which leaves room for five B stages.  Warp roles and outputs
-// are those of gemm_kernel<128, false>.
+// are those of gemm_kernel<128, false>; with prepacked weight atoms (PACKED) the B stages
+// need no transposer work: one thread copies each stage's atoms into TMEM with
+// tcgen05.cp and commits the copies to the stage's full barrier.
 constexpr int kChunkN = 4;
 constexpr int kResidentKS = 3;                      // k-stages of A held (F <= 768)
 
@@ -536,9 +538,9 @@ down_resident_kernel(const __grid_constant__ CUtensorMap tmap_a,
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      // PACKED: the stage's codes and scale-factor atoms, both TMA bytes; otherwise the
-      // codes and one arrive per transposer warp
-      mbar_init(&full[s], PACKED ? 1 : 1 + 4);
+      // the stage's codes (TMA bytes) and its weight scale factors in TMEM: PACKED, the
+      // commit of the atom copies; otherwise one arrive per transposer warp
+      mbar_init(&full[s], PACKED ? 1 + 1 : 1 + 4);
       mbar_init(&stg_full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -612,12 +614,13 @@ down_resident_kernel(const __grid_constant__ CUtensorMap tmap_a,
             }
             unsigned char* sb = bring + st * C::STAGE_BYTES;
             if (PACKED) {
-              // the stage's k-steps of atoms: one contiguous copy
+              // the stage's k-steps of atoms: one contiguous copy, on the staging barrier
               const int nk = min(4, args.kst - 4 * ks);
-              mbar_expect_tx(&full[st], (uint32_t)(C::B_CODES + 512 * nk));
+              mbar_expect_tx(&stg_full[st], (uint32_t)(512 * nk));
+              mbar_expect_tx(&full[st], (uint32_t)C::B_CODES);
               bulk_load(sb + C::B_CODES,
                         args.b_atoms + ((size_t)(tile.z * args.b_tiles + n) * args.kst + 4 * ks) * 512,
-                        512u * nk, &full[st]);
+                        512u * nk, &stg_full[st]);
             } else {
               mbar_expect_tx(&stg_full[st], tx_sb);
               mbar_expect_tx(&full[st], C::B_CODES);
@@ -639,7 +642,7 @@ down_resident_kernel(const __grid_constant__ CUtensorMap tmap_a,
         for (int s = 0; s < C::STAGES; ++s) {
           if (it <= s) continue;
           const int last = s + ((it - 1 - s) / C::STAGES) * C::STAGES;
-          while (((!PACKED && !mbar_try(&stg_full[s], (last / C::STAGES) & 1)) ||
+          while ((!mbar_try(&stg_full[s], (last / C::STAGES) & 1) ||
                   !mbar_try(&full[s], (last / C::STAGES) & 1)) &&
                  global_ns() - t0 < 100000000ull) {
           }
@@ -692,12 +695,6 @@ down_resident_kernel(const __grid_constant__ CUtensorMap tmap_a,
             const uint64_t bo = (uint64_t)((st * C::STAGE_BYTES) >> 4);
             const uint32_t sfb = sfb_col0 + st * C::SFB_COLS;
             const int nk = min(4, (sfrow - 16 * ks) >> 2);   // k-steps past K are skipped
-            if (PACKED) {
-              const uint32_t atoms = smem_u32(bring + st * C::STAGE_BYTES + C::B_CODES);
-#pragma unroll
-              for (int j = 0; j < 4; ++j)
-                if (j < nk) tc_cp_sf(sfb + 4 * j, atoms + 512 * j);
-            }
 #pragma unroll
             for (int j = 0; j < 4; ++j)
               if (j < nk)
@@ -750,10 +747,13 @@ down_resident_kernel(const __grid_constant__ CUtensorMap tmap_a,
     };
     bool ok = write_sfa(0);
     int it = 0, ca = 0;
-    // PACKED: the weight scale factors reach TMEM by tcgen05.cp; only the chunks' A remain
-    if (PACKED)
+    // PACKED: one thread of warp 2 copies each stage's weight atoms into TMEM (tcgen05.cp,
+    // committed to the stage's full barrier); warps 3-5 arrive on no stage barrier, so they
+    // wait on none (a parity wait more than one phase behind would not return) and only
+    // write each chunk's A scale factors, in chunk order
+    if (PACKED && warp != 2)
       for (int q = 1; ok && blockIdx.x + q * gridDim.x < n_chunk; ++q) ok = write_sfa(q);
-    for (int c = blockIdx.x; c < n_chunk && ok && !PACKED; c += gridDim.x, ++ca) {
+    for (int c = blockIdx.x; c < n_chunk && ok && (!PACKED || warp == 2); c += gridDim.x, ++ca) {
       int m, n_lo, n_hi;
       chunk_range(c, nr, args.n_tiles_n, m, n_lo, n_hi);
       for (int n = n_lo; n < n_hi && ok; ++n) {
@@ -766,6 +766,16 @@ down_resident_kernel(const __grid_constant__ CUtensorMap tmap_a,
           tc_fence_after();
           const uint32_t sb = smem_u32(bring + st * C::STAGE_BYTES + C::B_CODES);
           const int nvalid = min(4, (sfrow - 16 * ks) >> 2);
+          if (PACKED) {
+            if (lane == 0) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                if (j < nvalid) tc_cp_sf(sfb_col0 + st * C::SFB_COLS + 4 * j, sb + 512 * j);
+              tc_commit(&full[st]);
+            }
+            __syncwarp();
+            continue;
+          }
           uint32_t vb[16];
 #pragma unroll
           for (int x = 0; x < 4; ++x) {
