@@ -420,3 +420,34 @@ def test_sliced_h_slices_bit_exact_against_the_oracle(name):
         assert np.array_equal(scales[rows], sc), f"slice {i} scales"
         assert np.array_equal(exps[rows], e.astype(np.int32)), f"slice {i} exponents"
         acc = acc + nvfp4.dequant_q(c, sc, e)
+
+
+@pytest.mark.parametrize("name", ["verify_T128", "verify_T32", "sliced_H4096"])
+def test_sliced_x_slices_bit_exact_against_the_oracle(name):
+    """The four residual slices of each pair's x row (its token's bf16 row) that the sliced
+    form writes equal the oracle's quantiser applied to the running residual, bit for bit,
+    in every CSR row: per-token CTAs (verify_T128), per-pair CTAs (verify_T32), H = 4096."""
+    from oracle import nvfp4
+    if name == "sliced_H4096":
+        wl = synth.logits_workload("sliced_H4096", 32, 4096, 256, 64, 8, seed=22)
+    else:
+        wl = synth.by_name(name)
+    assert wl.P >= moe.decode_tensor_core_min_pairs()
+    run = run_layer(wl)
+    assert run.err == 0
+    L, H, NS = run.ws, wl.H, 4
+    R = wl.P * NS
+    n_valid = int(run.offsets[-1])
+    codes = run.ws_raw[L["qx_codes"]:L["qx_codes"] + R * H // 2].reshape(R, H // 2)
+    scales = run.ws_raw[L["qx_scales"]:L["qx_scales"] + R * H // 16].reshape(R, H // 16)
+    exps = run.ws_raw[L["qx_exp"]:L["qx_exp"] + 4 * R].view(np.int32)
+    tok = run.pair_ids[:n_valid] // wl.k
+    v = synth.bf16_bits_to_f32(wl.x_bits)[tok].astype(np.float64)
+    acc = np.zeros_like(v)
+    for i in range(NS):
+        c, sc, e = nvfp4.quantize(v - acc)
+        rows = np.arange(n_valid) * NS + i
+        assert np.array_equal(codes[rows], c), f"slice {i} codes"
+        assert np.array_equal(scales[rows], sc), f"slice {i} scales"
+        assert np.array_equal(exps[rows], e.astype(np.int32)), f"slice {i} exponents"
+        acc = acc + nvfp4.dequant_q(c, sc, e)
