@@ -197,3 +197,31 @@ def test_tile_list_always_fits_its_workspace_region(lib, path, rpp, tile_rows, r
         counts = np.bincount(ids, minlength=E)
         tiles = int(np.sum((counts * rpp + tile_rows - 1) // tile_rows))
         assert 16 + 16 * tiles <= region, (T, k, E, tiles, region)
+
+
+@pytest.mark.parametrize("gate_up", [True, False])
+def test_prepack_layout_restatement_against_the_definition(gate_up):
+    """The numpy restatement the GPU prepack tests compare with, against a plain loop over
+    the layout's definition in include/moe.h (every byte of a small bank, both orders)."""
+    from prepack_layout import expected_atoms
+    rng = np.random.default_rng(7)
+    E, R, K = 2, 256, 192
+    S = K // 16
+    scales = rng.integers(0, 127, size=(E, R, S), dtype=np.uint8)
+    got = expected_atoms(scales, gate_up)
+    tiles, kst = R // 128, K // 64
+    want = np.zeros(E * tiles * kst * 512, np.uint8)
+    for e in range(E):
+        for t in range(tiles):
+            for j in range(kst):
+                a = (e * tiles + t) * kst + j
+                for r in range(32):
+                    for x in range(4):
+                        m = 32 * x + r
+                        if gate_up:
+                            row = (R // 2 if m % 2 else 0) + 64 * t + m // 2
+                        else:
+                            row = 128 * t + m
+                        for b in range(4):
+                            want[a * 512 + 16 * r + 4 * x + b] = scales[e, row, 4 * j + b]
+    assert np.array_equal(got, want)

@@ -19,22 +19,9 @@ import synth
 import oracle
 import nvfp4_grouped_gemm_gb300 as moe
 from gpu_util import run_layer, device_banks, assert_within
+from prepack_layout import expected_atoms
 
 pytestmark = pytest.mark.gpu
-
-
-def expected_atoms(scales: np.ndarray, gate_up: bool) -> np.ndarray:
-    """The atoms of a planar scale plane [E, rows, in_f/16], restated with numpy."""
-    E, R, S = scales.shape
-    tiles, kst = R // 128, S // 4
-    m = np.arange(128)
-    if gate_up:
-        F = R // 2
-        rows = 64 * np.arange(tiles)[:, None] + (np.where(m % 2 == 1, F, 0) + m // 2)[None, :]
-    else:
-        rows = 128 * np.arange(tiles)[:, None] + m[None, :]
-    w = scales[:, rows, :].reshape(E, tiles, 4, 32, kst, 4)      # [e, t, x, r, j, b]
-    return np.ascontiguousarray(w.transpose(0, 1, 4, 3, 2, 5)).reshape(-1)
 
 
 @pytest.mark.parametrize("gate_up,E,rows,in_f", [(True, 3, 256, 512), (False, 3, 512, 192),
