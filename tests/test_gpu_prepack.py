@@ -57,18 +57,33 @@ def _same_with_prepacked(wl, path):
     return got
 
 
+SHAPES = {
+    "prefill_F1152": (256, 512, 1152, 4, 4),      # general down GEMM
+    "prefill_F832": (256, 512, 832, 4, 4),        # its last k-stage holds one K-step of atoms
+    "prefill_F4096": (32, 4096, 4096, 16, 4),     # largest F and H: 64 K-steps per row
+    "sliced_F384": (40, 512, 384, 24, 8),         # sliced down: 6 of a stage's 12 K-steps
+    "sliced_H4096": (32, 4096, 256, 64, 8),       # sliced gate/up over 64 K-steps per row
+}
+
+
 @pytest.mark.parametrize("name,path", [("prefill_T256", moe.PATH_PREFILL),
                                        ("prefill_F1152", moe.PATH_PREFILL),
+                                       ("prefill_F832", moe.PATH_PREFILL),
+                                       ("prefill_F4096", moe.PATH_PREFILL),
                                        ("verify_T32", moe.PATH_DECODE),
                                        ("verify_T128", moe.PATH_DECODE),
+                                       ("sliced_F384", moe.PATH_DECODE),
+                                       ("sliced_H4096", moe.PATH_DECODE),
                                        ("decode_T8", moe.PATH_DECODE)])
 def test_layers_bit_identical_with_prepacked_banks(name, path):
     if name == "prefill_T256":
         wl = synth.prefill(seed=0, T=256)
-    elif name == "prefill_F1152":
-        wl = synth.logits_workload("prefill_F1152", 256, 512, 1152, 4, 4, seed=5)
+    elif name in SHAPES:
+        wl = synth.logits_workload(name, *SHAPES[name], seed=5)
     else:
         wl = synth.by_name(name)
+    if path == moe.PATH_DECODE and name.startswith("sliced"):
+        assert wl.P >= moe.decode_tensor_core_min_pairs()
     got = _same_with_prepacked(wl, path)
     if path == moe.PATH_DECODE:
         ids, w = oracle.route_topk(wl.logits, wl.k)
