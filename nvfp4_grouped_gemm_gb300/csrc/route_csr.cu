@@ -97,58 +97,76 @@ route_merge_kernel(const float* __restrict__ logits, int T, int E, int k,
 constexpr int kCsrThreads = 1024;
 constexpr int kCsrWarps = kCsrThreads / 32;
 
-__device__ __forceinline__ int block_exclusive_scan(int v, int* scratch, int* total) {
-  // scratch: kCsrWarps ints
+// Exclusive scan of four ints per thread across the block at once (one set of barriers
+// for all four); scratch: kCsrWarps int4.
+__device__ __forceinline__ int4 block_exclusive_scan4(int4 v, int4* scratch, int4* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
+  int4 x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
+    const int a = __shfl_up_sync(0xffffffffu, x.x, o), b = __shfl_up_sync(0xffffffffu, x.y, o);
+    const int c = __shfl_up_sync(0xffffffffu, x.z, o), d = __shfl_up_sync(0xffffffffu, x.w, o);
+    if (lane >= o) { x.x += a; x.y += b; x.z += c; x.w += d; }
   }
   if (lane == 31) scratch[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    int s = scratch[lane];
+    int4 q = scratch[lane];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      int y = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += y;
+      const int a = __shfl_up_sync(0xffffffffu, q.x, o), b = __shfl_up_sync(0xffffffffu, q.y, o);
+      const int c = __shfl_up_sync(0xffffffffu, q.z, o), d = __shfl_up_sync(0xffffffffu, q.w, o);
+      if (lane >= o) { q.x += a; q.y += b; q.z += c; q.w += d; }
     }
-    scratch[lane] = s;   // inclusive
+    scratch[lane] = q;   // inclusive
   }
   __syncthreads();
-  int base = warp ? scratch[warp - 1] : 0;
+  const int4 base = warp ? scratch[warp - 1] : make_int4(0, 0, 0, 0);
   *total = scratch[kCsrWarps - 1];
   __syncthreads();
-  return base + x - v;
+  return make_int4(base.x + x.x - v.x, base.y + x.y - v.y, base.z + x.z - v.z, base.w + x.w - v.w);
 }
 
-// The tile list of one operand layout, one expert per thread (threads tid < E hold their
-// expert's count and offset): an expert's cnt * rpp operand rows starting at off * rpp are
-// cut into tiles of tile_rows rows, listed in expert order.  Every thread of the CTA must
-// call it (it scans across the block).
-__device__ __forceinline__ void write_tile_list(int E, int cnt, int off, int rpp, int tile_rows,
-                                                int32_t* __restrict__ tiles, int* scratch) {
-  const int e = threadIdx.x;
-  const int m = e < E ? cnt * rpp : 0;
-  const int nt = (m + tile_rows - 1) / tile_rows;
-  int total;
-  const int base = block_exclusive_scan(nt, scratch, &total);
+// The cut of an expert's m operand rows (starting at row first) into tiles of tile_rows,
+// entries base, base + 1, ... of the list.
+__device__ __forceinline__ void write_tiles(int32_t* tiles, int base, int m, int first,
+                                            int tile_rows, int e) {
   int4* list = reinterpret_cast<int4*>(tiles + 4);
-  for (int i = 0; i < nt; ++i) {
+  for (int i = 0; (i * tile_rows) < m; ++i) {
     const int r = m - i * tile_rows;
-    list[base + i] = make_int4(off * rpp + i * tile_rows, r < tile_rows ? r : tile_rows, e, 0);
+    list[base + i] = make_int4(first + i * tile_rows, r < tile_rows ? r : tile_rows, e, 0);
   }
-  if (threadIdx.x == 0) tiles[0] = total;
 }
 
-// Both tile lists (the prefill GEMMs' 128-row M-tiles, the sliced decode GEMMs' 32-row
-// tiles over kDecodeSlices rows per pair), when the caller passed their regions.
-__device__ __forceinline__ void write_tile_lists(int E, int cnt, int off, int32_t* tiles,
-                                                 int32_t* slice_tiles, int* scratch) {
-  if (tiles) write_tile_list(E, cnt, off, 1, kTileRows, tiles, scratch);
-  if (slice_tiles) write_tile_list(E, cnt, off, kDecodeSlices, kSliceTileRows, slice_tiles, scratch);
+// From each expert's pair count (thread e < E holds expert e's; every thread of the CTA
+// calls it): the offsets, the active list and count, and both tile lists (the prefill
+// GEMMs' 128-row M-tiles, the sliced decode GEMMs' 32-row tiles over kDecodeSlices rows per
+// pair, each when the caller passed its region), from one block-wide scan of the four
+// per-expert quantities.  Returns the expert's offset.
+__device__ __forceinline__ int write_csr_lists(int E, int cnt, int32_t* __restrict__ offsets,
+                                               int32_t* __restrict__ active,
+                                               int32_t* __restrict__ n_active, int32_t* tiles,
+                                               int32_t* slice_tiles, int4* scratch) {
+  const int e = threadIdx.x;
+  const int c = e < E ? cnt : 0;
+  const int m0 = tiles ? c : 0, m1 = slice_tiles ? c * kDecodeSlices : 0;
+  const int4 v = make_int4(c, c > 0 ? 1 : 0, (m0 + kTileRows - 1) / kTileRows,
+                           (m1 + kSliceTileRows - 1) / kSliceTileRows);
+  int4 tot;
+  const int4 base = block_exclusive_scan4(v, scratch, &tot);
+  if (e < E) {
+    offsets[e] = base.x;
+    if (c > 0) active[base.y] = e;
+    if (tiles) write_tiles(tiles, base.z, m0, base.x, kTileRows, e);
+    if (slice_tiles) write_tiles(slice_tiles, base.w, m1, base.x * kDecodeSlices, kSliceTileRows, e);
+  }
+  if (e == 0) {
+    offsets[E] = tot.x;
+    *n_active = tot.y;
+    if (tiles) tiles[0] = tot.z;
+    if (slice_tiles) slice_tiles[0] = tot.w;
+  }
+  return base.x;
 }
 
 __global__ void __launch_bounds__(kCsrThreads, 1)
@@ -159,8 +177,8 @@ build_csr_kernel(const int32_t* __restrict__ ids_g, int P, int E, int32_t* __res
                  int32_t* slice_tiles) {
   extern __shared__ int smem[];
   int* hist = smem;                           // [kCsrWarps][E]
-  int* scratch = smem + kCsrWarps * E;        // [kCsrWarps]
-  int* ids_s = scratch + kCsrWarps;           // [P] when ids_in_smem
+  int4* scratch = reinterpret_cast<int4*>(smem + kCsrWarps * E);   // [kCsrWarps]
+  int* ids_s = smem + kCsrWarps * E + 4 * kCsrWarps;                // [P] when ids_in_smem
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int i = tid; i < kCsrWarps * E; i += kCsrThreads) hist[i] = 0;
   pdl_wait();                                 // the expert ids are complete
@@ -193,20 +211,9 @@ build_csr_kernel(const int32_t* __restrict__ ids_g, int P, int E, int32_t* __res
       cnt += c;
     }
   }
-  int total;
-  int off = block_exclusive_scan(tid < E ? cnt : 0, scratch, &total);
-  int act_total;
-  int act_pos = block_exclusive_scan((tid < E && cnt > 0) ? 1 : 0, scratch, &act_total);
-  if (tid < E) {
-    offsets[tid] = off;
-    if (cnt > 0) active[act_pos] = tid;
+  const int off = write_csr_lists(E, cnt, offsets, active, n_active, tiles, slice_tiles, scratch);
+  if (tid < E)
     for (int w = 0; w < kCsrWarps; ++w) hist[w * E + tid] += off;
-  }
-  if (tid == 0) {
-    offsets[E] = total;
-    *n_active = act_total;
-  }
-  write_tile_lists(E, cnt, off, tiles, slice_tiles, scratch);
   __syncthreads();
 
   // pass C: stable placement within each slice
@@ -276,7 +283,7 @@ __global__ void __launch_bounds__(kCsrThreads, 1)
 csr_scan_kernel(int32_t* __restrict__ cnt, int n_chunks, int E, int32_t* __restrict__ offsets,
                 int32_t* __restrict__ active, int32_t* __restrict__ n_active, int32_t* tiles,
                 int32_t* slice_tiles) {
-  __shared__ int scratch[kCsrWarps];
+  __shared__ int4 scratch[kCsrWarps];
   pdl_wait();
   pdl_trigger();
   const int e = threadIdx.x;
@@ -306,12 +313,8 @@ csr_scan_kernel(int32_t* __restrict__ cnt, int n_chunks, int E, int32_t* __restr
       }
     }
   }
-  int total, act_total;
-  const int off = block_exclusive_scan(e < E ? tot : 0, scratch, &total);
-  const int act = block_exclusive_scan((e < E && tot > 0) ? 1 : 0, scratch, &act_total);
+  const int off = write_csr_lists(E, tot, offsets, active, n_active, tiles, slice_tiles, scratch);
   if (e < E) {
-    offsets[e] = off;
-    if (tot > 0) active[act] = e;
     if (in_regs) {
 #pragma unroll
       for (int b = 0; b < kScanRegChunks; ++b)
@@ -320,11 +323,6 @@ csr_scan_kernel(int32_t* __restrict__ cnt, int n_chunks, int E, int32_t* __restr
       for (int b = 0; b < n_chunks; ++b) cnt[(size_t)b * E + e] += off;
     }
   }
-  if (e == 0) {
-    offsets[E] = total;
-    *n_active = act_total;
-  }
-  write_tile_lists(E, tot, off, tiles, slice_tiles, scratch);
 }
 
 __global__ void __launch_bounds__(kChunkThreads)
@@ -399,7 +397,7 @@ csr_small_kernel(const int32_t* __restrict__ ids_g, int P, int E, int32_t* __res
                  uint32_t* __restrict__ err, int32_t* tiles, int32_t* slice_tiles) {
   __shared__ int hist[kMaxE];
   __shared__ int ids_s[kCsrSmallPairs];
-  __shared__ int scratch[kCsrWarps];
+  __shared__ int4 scratch[kCsrWarps];
   const int tid = threadIdx.x;
   if (tid < E) hist[tid] = 0;
   pdl_wait();                                 // the expert ids are complete
@@ -419,19 +417,8 @@ csr_small_kernel(const int32_t* __restrict__ ids_g, int P, int E, int32_t* __res
   if (valid) atomicAdd(&hist[e], 1);
   __syncthreads();
   const int cnt = tid < E ? hist[tid] : 0;
-  int total, act_total;
-  const int off = block_exclusive_scan(cnt, scratch, &total);
-  const int act = block_exclusive_scan((tid < E && cnt > 0) ? 1 : 0, scratch, &act_total);
-  if (tid < E) {
-    offsets[tid] = off;
-    hist[tid] = off;
-    if (cnt > 0) active[act] = tid;
-  }
-  if (tid == 0) {
-    offsets[E] = total;
-    *n_active = act_total;
-  }
-  write_tile_lists(E, cnt, off, tiles, slice_tiles, scratch);
+  const int off = write_csr_lists(E, cnt, offsets, active, n_active, tiles, slice_tiles, scratch);
+  if (tid < E) hist[tid] = off;
   __syncthreads();
   // one warp places the pairs 32 at a time in ascending p: equal experts in a group are
   // matched and ranked by lane, hist[e] (the expert's next row) advances by the group
@@ -490,7 +477,7 @@ cudaError_t launch_build_csr(const int32_t* ids, int P, int k, int E, moe_csr cs
     return launch_pdl(csr_place_kernel, dim3(nb), dim3(kChunkThreads), smem, s, ids, P, E,
                       (const int32_t*)scratch, csr.pair_ids, pair_pos);
   }
-  size_t smem = (size_t)(kCsrWarps * E + kCsrWarps) * sizeof(int);
+  size_t smem = (size_t)(kCsrWarps * E + 4 * kCsrWarps) * sizeof(int);
   const int ids_in_smem = smem + (size_t)P * sizeof(int) <= 200 * 1024 ? 1 : 0;
   if (ids_in_smem) smem += (size_t)P * sizeof(int);
   cudaError_t st = cudaFuncSetAttribute(build_csr_kernel,
