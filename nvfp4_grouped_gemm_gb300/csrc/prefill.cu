@@ -5,9 +5,12 @@
 //   gemm_kernel     persistent, warp-specialised grouped GEMM over (M-tile, N-tile) work:
 //                   TMA (SWIZZLE_128B) feeds FP4 code tiles and row-major images of the
 //                   UE4M3 scale factors, four warps write the scale factors into TMEM
-//                   with tcgen05.st, one thread issues tcgen05.mma, eight warps drain
-//                   TMEM with tcgen05.ld and apply the epilogue (SiLU(g)*u -> h, or
-//                   z -> f16 partials)
+//                   with tcgen05.st (with a prepacked bank, the weights' arrive as atoms
+//                   that one thread copies in with tcgen05.cp), one thread issues
+//                   tcgen05.mma, eight warps drain TMEM with tcgen05.ld and apply the
+//                   epilogue (SiLU(g)*u -> h, or z -> f16 partials)
+//   down_resident_kernel  the down GEMM with each M-tile's Q(h) held in shared memory
+//                   while only the weights stream (F <= 768)
 // Q(x), Q(h) and the combine live in prefill_quant.cu.
 //
 // Every wait on an mbarrier is bounded by a 2 s %globaltimer budget; on expiry the CTA
