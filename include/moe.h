@@ -130,8 +130,9 @@ typedef struct moe_ws_layout {
   size_t error_word;   /* u32 device error word */
   size_t pair_pos;     /* i32 [P]   CSR position of pair p, -1 if its expert id is invalid */
   size_t h;            /* f32 [P][F] h = silu(g) * u, rows in CSR order */
-  size_t xg;           /* decode: f16 [P][H] activation rows gathered in CSR order, times 2^-xe */
-  size_t xe;           /* decode: i32 [P] power-of-two prescale of each gathered row */
+  size_t xg;           /* decode: f16 [T][H] each token's activation row times 2^-xe (the
+                          region holds P rows; rows T..P-1 are unused) */
+  size_t xe;           /* decode: i32 [T] power-of-two prescale of each token's row */
   size_t hg;           /* decode: f16 [P][F] h times 2^-he */
   size_t he;           /* decode: i32 [P] */
   size_t qx_codes;     /* prefill: u8 [P][H/2]  Q(x) in CSR order */
@@ -150,6 +151,8 @@ typedef struct moe_ws_layout {
                           rows of every pair (row0 and rows count slice rows) */
   size_t sync;         /* decode below moe_decode_tensor_core_min_pairs() pairs: u64 [6] sync
                           words of moe_decode_layer_nvfp4 (call counter, barrier counters) */
+  size_t row_tok;      /* decode below moe_decode_tensor_core_min_pairs() pairs: i32 [P] token
+                          of each CSR row (its xg / xe row) */
 } moe_ws_layout;
 
 /* Limits (MOE_ERR_UNSUPPORTED beyond them): 1 <= k <= min(E, 32); E <= 1024;

@@ -33,7 +33,7 @@ class CSR(ctypes.Structure):
 class WsLayout(ctypes.Structure):
     _fields_ = [(n, c_size) for n in (
         "total", "error_word", "pair_pos", "h", "xg", "xe", "hg", "he", "qx_codes", "qx_scales", "qx_exp",
-        "qh_codes", "qh_scales", "qh_exp", "partial", "tiles", "slice_tiles", "sync")]
+        "qh_codes", "qh_scales", "qh_exp", "partial", "tiles", "slice_tiles", "sync", "row_tok")]
 
 
 # (name, restype, argtypes) of every exported entry point declared in include/moe.h

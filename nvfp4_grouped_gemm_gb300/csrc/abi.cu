@@ -122,6 +122,7 @@ bool compute_layout(int T, int H, int F, int E, int k, int path, moe_ws_layout* 
     L->xe = take(P * sizeof(int32_t));
     L->hg = take(P * F * 2);
     L->he = take(P * sizeof(int32_t));
+    L->row_tok = take(P * sizeof(int32_t));
     L->sync = take(decode_layer_sync_bytes());
   } else {
     // operand rows per pair: the sliced decode form keeps kDecodeSlices slices of each row

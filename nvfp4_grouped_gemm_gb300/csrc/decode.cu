@@ -5,10 +5,11 @@
 // The grid is indexed by active expert, not by pair, so every active expert's rows are
 // streamed from HBM exactly once per call (the union-of-experts gather).  Kernels:
 //
-//   x_gather_kernel   CSR row r <- token x row as f16 times 2^-e (e from the row's amax,
-//                     so the largest magnitude lands in [2^14, 2^15): exact for bf16
-//                     values in f16's normal range); one warp per pair, the row read and
-//                     converted before the wait and stored at the pair's CSR row after it
+//   x_gather_kernel   token t's x row as f16 times 2^-e (e from the row's amax, so the
+//                     largest magnitude lands in [2^14, 2^15): exact for bf16 values in
+//                     f16's normal range), one warp per token, converted and stored before
+//                     the wait for the CSR; after it, each of the token's CSR rows gets
+//                     the token's index (row_tok), through which the gate/up units read x
 //   gate_up_kernel    CTA = (active expert, 16 gate rows + the matching 16 up rows); the
 //                     CTA's weight bytes land in shared memory with 16-byte cp.async
 //                     issued by every thread up front, the activation fragments come
@@ -75,22 +76,26 @@ __device__ __forceinline__ int swz_chunk(int lc) { return (lc ^ (((lc >> 3) & 1)
 // converted before the wait; after it, the row goes to the pair's CSR row pair_pos[p].
 template <int NP>
 __global__ void __launch_bounds__(256) x_gather_kernel(const uint16_t* __restrict__ x, int H, int k,
-                                                       int P, const int32_t* __restrict__ pair_pos,
+                                                       int T, const int32_t* __restrict__ pair_pos,
                                                        __half* __restrict__ xg,
-                                                       int32_t* __restrict__ xe) {
-  const int p = blockIdx.x * 8 + (threadIdx.x >> 5);
+                                                       int32_t* __restrict__ xe,
+                                                       int32_t* __restrict__ row_tok) {
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  const bool has = p < P;
-  // the whole row in registers (H <= 256 * NP: NP pieces of 8 values per lane)
+  const bool has = t < T;
+  // the whole row in registers (H <= 256 * NP: NP pieces of 8 values per lane); the row and
+  // its exponent depend on x alone, so they are stored before the wait
   uint4 v[NP];
-  const int e = x_row_f16<NP>(x + (size_t)(has ? p / k : 0) * H, has, H, lane, v);
+  const int e = x_row_f16<NP>(x + (size_t)(has ? t : 0) * H, has, H, lane, v);
+  if (has) {
+    if (lane == 0) xe[t] = e;
+    x_row_store<NP>(v, H, lane, xg + (size_t)t * H);
+  }
   pdl_wait();                                  // pair_pos is complete
   pdl_trigger();
-  if (!has) return;
-  const int pos = pair_pos[p];
-  if (pos < 0) return;                         // invalid expert id: the pair has no row
-  if (lane == 0) xe[pos] = e;
-  x_row_store<NP>(v, H, lane, xg + (size_t)pos * H);
+  if (!has || lane >= k) return;
+  const int pos = pair_pos[(size_t)t * k + lane];
+  if (pos >= 0) row_tok[pos] = t;              // invalid expert id: the pair has no row
 }
 
 // Same for h (f32 rows already in CSR order), F <= 128*NR: the row stays in registers, so
@@ -111,8 +116,8 @@ __global__ void __launch_bounds__(256) h_prep_kernel(const float* __restrict__ h
 // gate/up + SiLU
 // ---------------------------------------------------------------------------
 struct GateUpArgs {
-  const __half* xg;        // [P][H] gathered f16 activations
-  const int32_t* xe;       // [P]
+  const __half* xg;        // [T][H] f16 activation rows, one per token
+  const int32_t* xe;       // [T]
   const uint8_t* codes;
   const uint8_t* scales;
   int H, F;
@@ -121,6 +126,7 @@ struct GateUpArgs {
   const int32_t* n_active;
   float* h;
   const float* alpha = nullptr;   // [E] per-expert second-level weight scale, or none
+  const int32_t* row_tok = nullptr;   // [P] token of each CSR row
 };
 
 // Persistent: CTA c owns a contiguous range of work units u = (active expert, 16-row
@@ -183,7 +189,8 @@ __global__ void __launch_bounds__(256, 2) gate_up_kernel(const GateUpArgs args) 
     for (int tok0 = 0; tok0 < m; tok0 += 8) {
       const int live = min(8, m - tok0);
       if (e != cur_e || tok0 != cur_t0) {
-        const __half* xrow = args.xg + (size_t)(off + tok0 + g) * H + 32 * c;
+        const int xr = g < live ? args.row_tok[off + tok0 + g] : 0;
+        const __half* xrow = args.xg + (size_t)xr * H + 32 * c;
 #pragma unroll
         for (int j = 0; j < KMAX; ++j)
 #pragma unroll
@@ -253,7 +260,7 @@ __global__ void __launch_bounds__(256, 2) gate_up_kernel(const GateUpArgs args) 
           const int n = 2 * c + (q & 1);
           const int ii = i0 + g + 8 * (q >> 1);
           if (n < live) {
-            const int ex = args.xe[off + tok0 + n];
+            const int ex = args.xe[args.row_tok[off + tok0 + n]];
             const float al = args.alpha ? __ldg(args.alpha + e) : 1.0f;
             args.h[(size_t)(off + tok0 + n) * F + ii] =
                 silu_f(al * ldexpf(sg[q], ex)) * (al * ldexpf(su[q], ex));
@@ -511,7 +518,7 @@ gate_up_tma_kernel(const __grid_constant__ CUtensorMap tmap_c, const __grid_cons
     const Ring ring{cw * kTmaSlots, 1};
     int q = 0;                                             // stages consumed
     for (int u = u_beg + cw; u < u_end && !*abort_flag; u += kTmaWarps)
-      if (!gu_consume_unit<NB, ALPHA>(args, u, smem, stage_bytes, full, empty, ring, q, abort_flag))
+      if (!gu_consume_unit<NB, ALPHA, true, true>(args, u, smem, stage_bytes, full, empty, ring, q, abort_flag))
         break;
   }
   __syncthreads();
@@ -593,11 +600,12 @@ cudaError_t launch_decode_gate_up(const uint16_t* x_bf16, int T, int H, int F, i
   const int P = T * k;
   __half* xg = reinterpret_cast<__half*>(ws + L.xg);
   int32_t* xe = reinterpret_cast<int32_t*>(ws + L.xe);
+  int32_t* row_tok = reinterpret_cast<int32_t*>(ws + L.row_tok);
   const int np = H / 256;                         // 16-byte pieces per lane
   auto xk = np <= 4 ? x_gather_kernel<4> : np <= 8 ? x_gather_kernel<8>
           : np <= 12 ? x_gather_kernel<12> : x_gather_kernel<16>;
-  cudaError_t st = launch_pdl(xk, dim3((P + 7) / 8), dim3(256), 0, s, x_bf16, H, k,
-                              P, (const int32_t*)(ws + L.pair_pos), xg, xe);
+  cudaError_t st = launch_pdl(xk, dim3((T + 7) / 8), dim3(256), 0, s, x_bf16, H, k,
+                              T, (const int32_t*)(ws + L.pair_pos), xg, xe, row_tok);
   if (st != cudaSuccess) return st;
   {
     // TMA-fed warp units: K-chunks of at most 2 boxes of 128 bytes per row
@@ -625,6 +633,7 @@ cudaError_t launch_decode_gate_up(const uint16_t* x_bf16, int T, int H, int F, i
       GuTmaArgs ta{xg, xe, H, F, nh, nb, csr.expert_offsets, csr.active_experts, csr.n_active,
                    reinterpret_cast<float*>(ws + L.h), reinterpret_cast<uint32_t*>(ws + L.error_word)};
       ta.alpha = b.alpha;
+      ta.row_tok = row_tok;
       auto gk = b.alpha ? (nb == 1 ? gate_up_tma_kernel<1, true> : gate_up_tma_kernel<2, true>)
                         : (nb == 1 ? gate_up_tma_kernel<1, false> : gate_up_tma_kernel<2, false>);
       st = cudaFuncSetAttribute(gk, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -642,6 +651,7 @@ cudaError_t launch_decode_gate_up(const uint16_t* x_bf16, int T, int H, int F, i
   GateUpArgs a{xg, xe, b.codes, b.scales, H, F, csr.expert_offsets, csr.active_experts,
                csr.n_active, reinterpret_cast<float*>(ws + L.h)};
   a.alpha = b.alpha;
+  a.row_tok = row_tok;
   const long long max_units = (long long)(P < b.E ? P : b.E) * (F / 16);
   const size_t wbytes = (32 * (size_t)(H / 2) + 32 * (size_t)(H / 16) + 127) & ~size_t(127);
   const size_t smem = 2 * wbytes + 8 * 32 * 8 * sizeof(float);
