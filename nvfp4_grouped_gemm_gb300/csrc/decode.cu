@@ -625,7 +625,8 @@ cudaError_t launch_decode_gate_up(const uint16_t* x_bf16, int T, int H, int F, i
     const uint64_t sstr[3] = {(uint64_t)H / 16, (uint64_t)F * (H / 16), 16};
     const uint32_t sbox[4] = {16, 8, 2, (uint32_t)nb};
     // with fewer than ~8 units per SM the warps cannot keep enough bytes in flight and the
-    // CTA kernel below is faster (measured at one token: 40 us against 42 us per layer)
+    // CTA kernel below was faster (one token: 40 against 42 us per layer when first
+    // measured; level since, 32.9 against 33.0 us)
     const long long units_bound = (long long)(P < b.E ? P : b.E) * (F / 8);
     if (units_bound >= 8LL * num_sms() && smem <= 232448 &&
         make_map4(&mc, b.codes, cdims, cstr, cbox, true) &&
